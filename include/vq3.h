@@ -1,0 +1,188 @@
+/*
+ * vq3.h - C ABI of the VQ3 Hadamard-rotated vector-LUT MLP library (sm_103a).
+ *
+ * What the library computes (page titles and sections of the sources):
+ *   model card "anemll/anemll-forge-qwen3.8-27B", section "Release 0.2:
+ *   three-bit MLP, token-mixer rotations, distilled weights":
+ *     - every MLP matrix (gate, up, down) is a three-bit vector lookup table
+ *       "2x64": a codebook of 64 two-component FP16 centroids per matrix, one
+ *       six-bit index per pair of output channels (per input column), and an
+ *       FP16 scale per output channel;
+ *     - the input of each matrix is multiplied online by 1,024-wide Hadamard
+ *       blocks with seeded signs, the weights being stored in the rotated basis.
+ *   "ANEMLL ANE LLM conversion pipeline", section "Facts": the SiLU of the
+ *   gated MLP is 0.5*x*(1+tanh(x/2)) = x*sigmoid(x); vector LUTs run along
+ *   output channels.
+ *
+ * So for one matrix with d_out outputs and d_in inputs:
+ *   x'      = blockdiag(H_b diag(s)) x / sqrt(b)           (per row, b = block)
+ *   W[2p+c][i] = scale[2p+c] * C[idx[p][i]][c]             (c in {0,1})
+ *   y       = W x'
+ * and an MLP block is y = W_d R_d( silu(W_g R x) * (W_u R x) ).
+ *
+ * Conventions (every entry point):
+ *   - Return value: VQ3_OK (0) or a negative VQ3_E* code; vq3_last_error()
+ *     then returns a thread-local message. No C++ exception crosses the ABI.
+ *   - The caller owns every buffer. Device pointers must be 16-byte aligned
+ *     (VQ3_EALIGN otherwise). The library never allocates device memory; the
+ *     entry points that need scratch take a caller-supplied workspace.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Device work is enqueued asynchronously on it; arguments are
+ *     validated on the host before anything is enqueued, so an error return
+ *     means nothing was launched.
+ *   - FP16 data is passed as uint16_t bit patterns (IEEE binary16).
+ *   - Activations are row-major [rows][n]; rows == 0 is a valid no-op.
+ */
+#ifndef VQ3_H_
+#define VQ3_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define VQ3_OK 0
+#define VQ3_EINVAL (-1)       /* bad size, null pointer or inconsistent descriptor */
+#define VQ3_EALIGN (-2)       /* a device pointer is not 16-byte aligned */
+#define VQ3_EUNSUPPORTED (-3) /* shape outside what the kernels implement */
+#define VQ3_ECUDA (-4)        /* a CUDA runtime call failed (message has the CUDA error) */
+#define VQ3_ENOSPACE (-5)     /* workspace smaller than the size query returned */
+
+#define VQ3_CODEBOOK_SIZE 64
+#define VQ3_MAX_BLOCK 1024
+
+/*
+ * One VQ3 matrix, d_out x d_in. Cited: model card "anemll/anemll-forge-qwen3.8-27B",
+ * "Release 0.2" bullet "Three bits per MLP weight".
+ *   d_in  : input width; a multiple of 64 and of `block`.
+ *   d_out : output width; a multiple of 64 (so output channels pair up).
+ *   block : Hadamard block of the input rotation, a power of two in [2, 1024].
+ *   packed: device, 16-byte aligned, vq3_packed_bytes(d_in, d_out) bytes in the
+ *           GPU layout written by vq3_pack_layout.
+ *   codebook: device, [64][2] FP16 centroids (component 0 = even channel).
+ *   scales: device, [d_out] FP16 per-output-channel scales.
+ *   signs : device, bit-packed seeded signs over d_in (bit j of word j/32 set
+ *           => input j is negated before the Hadamard block), or NULL for all +1.
+ */
+typedef struct vq3_linear {
+  int d_in;
+  int d_out;
+  int block;
+  const void* packed;
+  const uint16_t* codebook;
+  const uint16_t* scales;
+  const uint32_t* signs;
+} vq3_linear;
+
+/* One SwiGLU block. gate and up read the same rotated input (same d_in, block
+ * and signs); down maps the intermediate width back: down.d_in == gate.d_out,
+ * down.d_out == gate.d_in. */
+typedef struct vq3_mlp_layer {
+  vq3_linear gate;
+  vq3_linear up;
+  vq3_linear down;
+} vq3_mlp_layer;
+
+/* Size in bytes of one matrix's GPU-layout indices (equal to the canonical
+ * stream's size: 6 bits per output pair and input column). 0 if unsupported. */
+size_t vq3_packed_bytes(int d_in, int d_out);
+
+/*
+ * Host-side, offline. Reorders a canonical index stream into the GPU layout.
+ * canonical: host, ceil(6*(d_out/2)*d_in/8) bytes. Index k = p*d_in + i
+ *   (output pair p, input column i) occupies stream bits [6k, 6k+6), stream bit
+ *   j being bit (j mod 8) of byte j/8 (least significant bit first).
+ * dst_host: host, vq3_packed_bytes(d_in, d_out) bytes, written in full.
+ * Errors: VQ3_EINVAL (null pointer), VQ3_EUNSUPPORTED (d_in or d_out not a
+ * positive multiple of 64).
+ */
+int vq3_pack_layout(const uint8_t* canonical, int d_in, int d_out, void* dst_host);
+
+/* Host-side inverse of vq3_pack_layout (pad bits of the canonical stream are
+ * written as zero). Same errors. */
+int vq3_unpack_layout(const void* packed_host, int d_in, int d_out, uint8_t* canonical);
+
+/*
+ * Blocked, normalised fast Walsh-Hadamard transform of each row:
+ *   out[r, j*b:(j+1)*b] = H_b diag(s_j) x[r, j*b:(j+1)*b] / sqrt(b).
+ * Cited: model card "anemll/anemll-forge-qwen3.8-27B", "Release 0.2" bullet
+ * "Token-mixer rotations" (1,024-wide Hadamard blocks with seeded signs).
+ * x, out: device FP16 [rows][n]; they may alias (in place). n % block == 0,
+ * block a power of two in [2, 1024]. signs: device bit-packed over n, or NULL.
+ * Arithmetic in FP32, one FP16 rounding at the end.
+ */
+int fwht_rotate(const uint16_t* x, int rows, int n, int block, const uint32_t* signs,
+                uint16_t* out, void* stream);
+
+/*
+ * Workspace for vq3_linear_forward / vq3_mlp_forward at `rows` rows. The
+ * workspace holds split-K partial sums, the rotated activations and arrival
+ * counters. It must be zero-filled once before its first use (vq3_workspace_init);
+ * every completed call leaves the counters at zero again. Calls that share a
+ * workspace must not overlap on the GPU (same stream, or ordered by events).
+ */
+size_t vq3_linear_workspace_bytes(int rows, const vq3_linear* L);
+size_t vq3_mlp_workspace_bytes(int rows, const vq3_mlp_layer* layer);
+int vq3_workspace_init(void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * One rotated VQ3 linear layer: out = fp16( W (R x) ), FP32 accumulation.
+ * x: device FP16 [rows][d_in]; out: device FP16 [rows][d_out] (must not alias x).
+ * Errors: VQ3_EINVAL, VQ3_EALIGN, VQ3_EUNSUPPORTED, VQ3_ENOSPACE, VQ3_ECUDA.
+ */
+int vq3_linear_forward(const uint16_t* x, int rows, const vq3_linear* L, uint16_t* out,
+                       void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * One SwiGLU MLP block with online rotations on both inputs:
+ *   h   = silu(W_g R_g x) * (W_u R_g x)      (FP32, stored as FP16)
+ *   out = fp16( W_d R_d h )
+ * Cited: model card "anemll/anemll-forge-qwen3.8-27B", "Release 0.2" table row
+ * "MLP gate / up / down" and bullets; "ANEMLL ANE LLM conversion pipeline",
+ * "Facts" (SiLU form).
+ * x: device FP16 [rows][d]; out: device FP16 [rows][d] (d = gate.d_in); out may
+ * not alias x. Same errors as vq3_linear_forward.
+ */
+int vq3_mlp_forward(const uint16_t* x, int rows, const vq3_mlp_layer* layer, uint16_t* out,
+                    void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Same as vq3_mlp_forward with HOST buffers: copies x (pinned or pageable host
+ * memory) to the workspace, runs the block, copies the result back into
+ * out_host and waits for the stream. Workspace: vq3_mlp_host_workspace_bytes.
+ */
+size_t vq3_mlp_host_workspace_bytes(int rows, const vq3_mlp_layer* layer);
+int vq3_mlp_forward_host(const uint16_t* x_host, int rows, const vq3_mlp_layer* layer,
+                         uint16_t* out_host, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Pre-norm residual step between stacked layers:
+ *   resid  <- fp16(resid + delta)                       (skipped if delta == NULL)
+ *   normed <- fp16(resid / sqrt(mean(resid^2) + eps))    (unit weight, FP32 math)
+ * resid, delta, normed: device FP16 [rows][n]; normed may not alias resid.
+ */
+int vq3_residual_rmsnorm(uint16_t* resid, const uint16_t* delta, int rows, int n, float eps,
+                         uint16_t* normed, void* stream);
+
+/*
+ * Debug/test: writes the dense weight of L from its GPU layout.
+ * apply_scale = 0: w_out[o][i] = C[idx[o/2][i]][o%2] (exact copy of the FP16 centroid);
+ * apply_scale = 1: w_out[o][i] = fp16(fp32(scale[o]) * fp32(C[...])) (the FP32
+ * product is exact, so this is the correctly rounded weight).
+ * w_out: device FP16 [d_out][d_in].
+ */
+int vq3_dequant_dense(const vq3_linear* L, int apply_scale, uint16_t* w_out, void* stream);
+
+/* Message for the last error on the calling thread ("" if none). */
+const char* vq3_last_error(void);
+
+/* Library build/version string. */
+const char* vq3_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VQ3_H_ */

@@ -1,0 +1,173 @@
+"""Seeded synthetic inputs for the VQ3 Hadamard-rotated vector-LUT MLP.
+
+This module is shared by the CPU oracle tests and by the CUDA path's tests and
+benchmark. It draws random numbers and nothing else: it holds none of the
+method's arithmetic (no unpacking, no rotation, no lookup, no matmul).
+
+The index stream is drawn directly in its canonical form. Uniform random 6-bit
+indices packed back to back are uniformly random bits, so the stream is random
+bytes whose pad bits (past the last index) are cleared. Both sides unpack it
+with their own code.
+
+Each workload seed feeds three independent PCG64 streams (seed sequences
+[seed, 0], [seed, 1] and [seed, 2]): activations, weights and sign bits. The
+weights therefore do not depend on the row count, so a row sweep runs the same
+block at every T, and the first rows of a taller X equal a shorter X. Inside the
+weight stream the order is fixed: for each matrix in order (gate, up, down for a
+block; layer by layer for a stack) the codebook, then the index stream, then the
+scales.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+HIDDEN = 5120
+INTERMEDIATE = 17408
+CODEBOOK_SIZE = 64
+CENTROID_DIM = 2
+INDEX_BITS = 6
+
+
+def rng(seed: int, stream: int = 1) -> np.random.Generator:
+    """Stream 0: activations; 1: weights; 2: sign bits."""
+    return np.random.Generator(np.random.PCG64([seed, stream]))
+
+
+def stream_bytes(d_in: int, d_out: int) -> int:
+    """Length in bytes of the canonical stream of a d_out x d_in matrix."""
+    bits = INDEX_BITS * (d_out // 2) * d_in
+    return (bits + 7) // 8
+
+
+def activations(g: np.random.Generator, rows: int, n: int, outlier_channels: int = 0,
+                outlier_scale: float = 50.0) -> np.ndarray:
+    """FP16 activations ~N(0,1); optionally `outlier_channels` seeded columns scaled up."""
+    x = g.standard_normal((rows, n), dtype=np.float64)
+    if outlier_channels:
+        cols = np.sort(g.choice(n, size=outlier_channels, replace=False))
+        x[:, cols] *= outlier_scale
+    return x.astype(np.float16)
+
+
+def codebook(g: np.random.Generator, std: float = 0.02) -> np.ndarray:
+    """FP16 codebook [64, 2] ~N(0, std)."""
+    return (g.standard_normal((CODEBOOK_SIZE, CENTROID_DIM)) * std).astype(np.float16)
+
+
+def index_stream(g: np.random.Generator, d_in: int, d_out: int) -> np.ndarray:
+    """Canonical index stream of uniformly random 6-bit indices (uint8 bytes)."""
+    nbytes = stream_bytes(d_in, d_out)
+    s = g.integers(0, 256, size=nbytes, dtype=np.uint8)
+    tail_bits = (INDEX_BITS * (d_out // 2) * d_in) % 8
+    if tail_bits:
+        s[-1] &= np.uint8((1 << tail_bits) - 1)
+    return s
+
+
+def scales(g: np.random.Generator, d_out: int, lo: float = 0.5, hi: float = 1.5) -> np.ndarray:
+    """FP16 per-output-channel scales ~U[lo, hi]."""
+    return g.uniform(lo, hi, size=d_out).astype(np.float16)
+
+
+def sign_bits(g: np.random.Generator, n: int) -> np.ndarray:
+    """Bit-packed seeded signs: bit j of word j//32 set means channel j is negated."""
+    words = (n + 31) // 32
+    w = g.integers(0, 2**32, size=words, dtype=np.uint64).astype(np.uint32)
+    tail = n % 32
+    if tail:
+        w[-1] &= np.uint32((1 << tail) - 1)
+    return w
+
+
+@dataclass
+class Matrix:
+    """One VQ3 matrix, d_out x d_in, in its canonical (interchange) form."""
+    d_in: int
+    d_out: int
+    block: int
+    codebook: np.ndarray  # [64, 2] float16
+    stream: np.ndarray    # canonical 6-bit LE index stream, uint8
+    scales: np.ndarray    # [d_out] float16
+    signs: np.ndarray | None = None  # bit-packed uint32 over d_in, or None (all +1)
+
+
+@dataclass
+class Block:
+    gate: Matrix
+    up: Matrix
+    down: Matrix
+
+
+@dataclass
+class Workload:
+    name: str
+    seed: int
+    x: np.ndarray  # [rows, d] float16
+    layers: list = field(default_factory=list)  # list[Block] or [Matrix]
+
+
+def matrix(g: np.random.Generator, d_in: int, d_out: int, block: int) -> Matrix:
+    c = codebook(g)
+    s = index_stream(g, d_in, d_out)
+    sc = scales(g, d_out)
+    return Matrix(d_in, d_out, block, c, s, sc)
+
+
+def mlp_block(g: np.random.Generator, hidden: int, inter: int, block: int) -> Block:
+    gate = matrix(g, hidden, inter, block)
+    up = matrix(g, hidden, inter, block)
+    down = matrix(g, inter, hidden, block)
+    return Block(gate, up, down)
+
+
+def add_signs(g: np.random.Generator, blk: Block) -> Block:
+    """Seeded sign vectors: one shared by gate and up (same input), one for down."""
+    s_in = sign_bits(g, blk.gate.d_in)
+    s_dn = sign_bits(g, blk.down.d_in)
+    blk.gate.signs = s_in
+    blk.up.signs = s_in
+    blk.down.signs = s_dn
+    return blk
+
+
+# ---- the five workloads (sizes and distributions as the benchmark specifies) ----
+
+def linear_256(seed: int = 0, rows: int = 8) -> Workload:
+    """A single VQ3 linear, 256 -> 256, one 256-point rotation block, 8 rows."""
+    x = activations(rng(seed, 0), rows, 256)
+    m = matrix(rng(seed, 1), 256, 256, 256)
+    return Workload("linear_256x256_T8", seed, x, [m])
+
+
+def mlp_27b(seed: int = 1, rows: int = 8, outlier_channels: int = 0, hidden: int = HIDDEN,
+            inter: int = INTERMEDIATE, block: int = 1024, name: str | None = None) -> Workload:
+    """One SwiGLU block at the 27B-dense shape (hidden 5120, intermediate 17408)."""
+    x = activations(rng(seed, 0), rows, hidden, outlier_channels=outlier_channels)
+    blk = mlp_block(rng(seed, 1), hidden, inter, block)
+    return Workload(name or f"mlp_{hidden}x{inter}_T{rows}", seed, x, [blk])
+
+
+def mlp_prefill_outliers(seed: int = 2, rows: int = 64) -> Workload:
+    """Config of 64 prefill rows with 1% of the 5120 channels (51) scaled x50."""
+    return mlp_27b(seed=seed, rows=rows, outlier_channels=round(0.01 * HIDDEN),
+                   name=f"mlp_5120x17408_T{rows}_outliers")
+
+
+def mlp_stack(seed: int = 3, rows: int = 8, layers: int = 64, hidden: int = HIDDEN,
+              inter: int = INTERMEDIATE, block: int = 1024) -> Workload:
+    """`layers` independent MLP blocks with a residual stream of `rows` rows."""
+    x = activations(rng(seed, 0), rows, hidden)
+    g = rng(seed, 1)
+    blocks = [mlp_block(g, hidden, inter, block) for _ in range(layers)]
+    return Workload(f"mlp_stack{layers}_{hidden}x{inter}_T{rows}", seed, x, blocks)
+
+
+def mlp_sweep(seed: int = 4, rows: int = 8) -> Workload:
+    """Row-sweep workload: the same block shape at T in {1, 8, 64, 512, 2048, 4096}."""
+    return mlp_27b(seed=seed, rows=rows, name=f"mlp_5120x17408_T{rows}_sweep")
+
+
+SWEEP_ROWS = (1, 8, 64, 512, 2048, 4096)
