@@ -1,0 +1,386 @@
+"""Benchmark of the VQ3 Hadamard-rotated vector-LUT MLP block on GB300.
+
+Default workload: one SwiGLU block at the 27B-dense shape (hidden 5120,
+intermediate 17408), T = 8 speculative-verify rows, seed 1. One step is one
+full block forward (rotate x, gate/up with SiLU*mul, rotate h, down) through
+the library's C ABI. Weights stream from HBM: the timed loop cycles through
+enough independent weight sets (>= 4x L2) that no step finds its weights in L2.
+
+Prints one JSON line (rank 0). `--impl reference` times the CPU oracle instead
+(the reference arm of this repository, on the host cores).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synth import inputs as S  # noqa: E402
+
+HIDDEN, INTER = S.HIDDEN, S.INTERMEDIATE
+BLOCK_BYTES = 3 * S.stream_bytes(HIDDEN, INTER) + 2 * (2 * INTER + HIDDEN) + 3 * 64 * 2 * 2  # 100,350,720
+GATE_UP_BYTES = 2 * S.stream_bytes(HIDDEN, INTER) + 2 * (2 * INTER) + 2 * 64 * 2 * 2
+FLOP_PER_ROW = 2 * (2 * HIDDEN * INTER + INTER * HIDDEN)  # 534,773,760
+METRIC = "VQ3 Hadamard-MLP rows/s; weight GB/s vs HBM peak @T=8; TFLOP/s @prefill"
+
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def cpu_cores() -> dict:
+    try:
+        aff = len(os.sched_getaffinity(0))
+    except AttributeError:
+        aff = os.cpu_count()
+    blas = None
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        blas = max((i.get("num_threads", 0) for i in info if i.get("user_api") == "blas"), default=None)
+    except Exception:
+        pass
+    return {"cpu_count": os.cpu_count(), "affinity": aff, "blas_threads": blas}
+
+
+# ------------------------------------------------------------------ oracle (CPU baseline / reference arm)
+
+class OracleSample:
+    """A bounded sample of one block for the CPU oracle: each step computes
+    1/frac of every matrix's output channels (gate and up rows [0, I/frac),
+    down rows [0, H/frac)), i.e. 1/frac of one block's arithmetic, with both
+    rotations in full. The down rows read h' of the whole block, computed once
+    by the oracle at set-up (untimed). A step counts as rows/frac rows."""
+
+    def __init__(self, rows: int, frac: int):
+        from oracle import vq3_oracle as O
+        self.O = O
+        self.wl = S.mlp_27b(seed=1, rows=rows)
+        self.frac = frac
+        blk = self.wl.layers[0]
+        g = O.linear_f64(self.wl.x, blk.gate)
+        u = O.linear_f64(self.wl.x, blk.up)
+        self.h = O.silu(g) * u
+
+    def step(self) -> float:
+        O, blk = self.O, self.wl.layers[0]
+        n_gu, n_dn = INTER // self.frac, HIDDEN // self.frac
+        xr = O.rotate(self.wl.x.astype(np.float64), blk.gate.block, blk.gate.signs)
+        Wg = O.dense_weight(blk.gate.stream, blk.gate.codebook, blk.gate.scales, HIDDEN, INTER, rows=(0, n_gu))
+        Wu = O.dense_weight(blk.up.stream, blk.up.codebook, blk.up.scales, HIDDEN, INTER, rows=(0, n_gu))
+        _ = O.silu(xr @ Wg.T) * (xr @ Wu.T)
+        hr = O.rotate(self.h, blk.down.block, blk.down.signs)
+        Wd = O.dense_weight(blk.down.stream, blk.down.codebook, blk.down.scales, INTER, HIDDEN, rows=(0, n_dn))
+        _ = hr @ Wd.T
+        return self.wl.x.shape[0] / self.frac
+
+
+def time_oracle(rows: int, frac: int, steps: int, warmup: int):
+    smp = OracleSample(rows, frac)
+    for _ in range(warmup):
+        smp.step()
+    t0 = time.perf_counter()
+    units = 0.0
+    for _ in range(steps):
+        units += smp.step()
+    dt = time.perf_counter() - t0
+    return units / dt, dt
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self) -> dict:
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args) -> dict | None:
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    from bit_vector_lut_gb300 import vq3
+
+    rows = args.rows
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_sets = max(2, math.ceil(4 * l2 / BLOCK_BYTES))
+    sets = []
+    for k in range(n_sets):
+        wl = S.mlp_27b(seed=1 + 1000 * k, rows=rows)
+        sets.append(vq3.MLP.from_block(wl.layers[0], dev))
+        if k == 0:
+            x_host = wl.x
+    x = torch.from_numpy(x_host).to(dev)
+    out = torch.empty_like(x)
+    ws = vq3.workspace(vq3.mlp_workspace_bytes(rows, sets[0]), dev)
+    torch.cuda.synchronize(dev)
+    # a side stream: CUDA graphs cannot be captured on the legacy default stream
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        return _run_ours_on(args, torch, vq3, dev, stream, rows, sets, x_host, x, out, ws, l2, n_sets, rank, world,
+                            local)
+
+
+def _run_ours_on(args, torch, vq3, dev, stream, rows, sets, x_host, x, out, ws, l2, n_sets, rank, world, local):
+
+    def step(i):
+        vq3.mlp_forward(x, sets[i % n_sets], out=out, ws=ws, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+
+    # one CUDA graph per weight set (one block forward each); step i replays graph i % n_sets
+    graphs = []
+    for i in range(n_sets):
+        gph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gph, stream=stream):
+            step(i)
+        graphs.append(gph)
+    torch.cuda.synchronize(dev)
+    for gph in graphs:
+        gph.replay()
+    torch.cuda.synchronize(dev)
+    steps = args.steps
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)  # nvidia-smi start-up
+        barrier()
+        e0.record(stream)
+        for i in range(steps):
+            graphs[i % n_sets].replay()
+        e1.record(stream)
+        barrier()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / steps
+    value = world * rows * steps / (ms / 1e3)
+
+    # dominant kernel: the gate/up half (rotate x + gate/up gemv), timed alone with events
+    # on the launching stream, cycling weight sets like the main loop
+    ga = torch.cuda.Event(enable_timing=True)
+    gb = torch.cuda.Event(enable_timing=True)
+    gu_ms = 0.0
+    n_gu = 0
+    for i in range(3 * n_sets):
+        ga.record(stream)
+        vq3.mlp_gate_up(x, sets[i % n_sets], ws, stream)
+        gb.record(stream)
+        vq3.mlp_down(rows, sets[i % n_sets], out, ws, stream)
+        gb.synchronize()
+        if i >= n_sets:
+            gu_ms += ga.elapsed_time(gb)
+            n_gu += 1
+    gu_ms /= n_gu
+    pk = peaks()
+    achieved = GATE_UP_BYTES / (gu_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "vq3 gate/up half (rotate x + gate/up GEMM, SiLU*mul)",
+                "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": args.traffic,
+                "peak_source": pk["source"], "ms_per_launch": round(gu_ms, 5),
+                "algorithmic_bytes_per_launch": GATE_UP_BYTES,
+                "block_weight_gbs": round(BLOCK_BYTES / (ms_per_step / 1e3) / 1e9, 1),
+                "block_frac_of_hbm": round(BLOCK_BYTES / (ms_per_step / 1e3) / 1e9 / pk["hbm_gbs"], 4)}
+
+    # end to end through the host-buffer entry point (copies in the timed region)
+    hws = vq3.workspace(vq3.mlp_host_workspace_bytes(rows, sets[0]), dev, stream)
+    xh = torch.from_numpy(x_host).pin_memory().numpy()
+    yh = torch.empty((rows, HIDDEN), dtype=torch.float16).pin_memory().numpy()
+    e2e_steps = max(n_sets, min(steps, 2000))
+    for i in range(n_sets):
+        vq3.mlp_forward_host(xh, sets[i % n_sets], hws, out=yh, stream=stream)
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        vq3.mlp_forward_host(xh, sets[i % n_sets], hws, out=yh, stream=stream)
+    dt = time.perf_counter() - t0
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([dt], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dt = float(t.item())
+    e2e = {"value": round(world * rows * e2e_steps / dt, 1), "unit": "rows/s",
+           "h2d_bytes_per_step": int(x_host.nbytes), "d2h_bytes_per_step": int(rows * HIDDEN * 2),
+           "api": "vq3_mlp_forward_host (pageable->pinned host buffers)"}
+
+    extra = {}
+    if not args.quick and rank == 0:
+        extra = prefill_sweep(vq3, dev, stream, pk)
+
+    launches = vq3.mlp_kernel_launches(rows, sets[0]) * steps
+    line = None
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world, "steps": steps,
+                "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f16 (fp32 accumulate)", "data": "synthetic",
+                "config": {"workload": f"mlp_5120x17408_T{rows}", "hidden": HIDDEN, "intermediate": INTER,
+                           "rows": rows, "rotation_block": 1024, "seed": 1, "weight_sets": n_sets,
+                           "l2": f"weights rotate over {n_sets} independent sets "
+                                 f"({n_sets * BLOCK_BYTES / 1e6:.0f} MB > 4x L2 {l2 / 1e6:.0f} MB)",
+                           "timing": "CUDA graph of weight-set cycles; CUDA events on the launching stream",
+                           "parallelism": f"replicas x{world}"},
+                "clocks": clk.summary(), "e2e": e2e, "gpu_launches": launches, "roofline": roofline}
+        if extra:
+            line["prefill_sweep"] = extra
+        if world == 1 and not args.no_cpu_baseline:
+            rate, dt = time_oracle(rows, args.oracle_frac, args.oracle_steps, 1)
+            line["cpu_baseline"] = {"value": round(rate, 3), "unit": "rows/s", "cores": cpu_cores(),
+                                    "kind": "oracle",
+                                    "sample": f"{args.oracle_steps} oracle samples of 1/{args.oracle_frac} of the "
+                                              f"block's intermediate channels at T={rows} ({dt:.1f} s), "
+                                              f"scaled to whole rows"}
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return line
+
+
+def prefill_sweep(vq3, dev, stream, pk) -> dict:
+    """TFLOP/s of one block at prefill row counts (weights L2-resident across repeats at these sizes is
+    irrelevant: they are tensor-bound)."""
+    import torch
+    res = {}
+    wl = S.mlp_27b(seed=4, rows=1)
+    layer = vq3.MLP.from_block(wl.layers[0], dev)
+    for rows in (64, 512, 2048, 4096):
+        x = torch.from_numpy(S.activations(S.rng(4, 0), rows, HIDDEN)).to(dev)
+        out = torch.empty_like(x)
+        ws = vq3.workspace(vq3.mlp_workspace_bytes(rows, layer), dev, stream)
+        for _ in range(2):
+            vq3.mlp_forward(x, layer, out=out, ws=ws, stream=stream)
+        reps = 3 if rows >= 2048 else 10
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            vq3.mlp_forward(x, layer, out=out, ws=ws, stream=stream)
+        b.record(stream)
+        b.synchronize()
+        ms = a.elapsed_time(b) / reps
+        tf = FLOP_PER_ROW * rows / (ms / 1e3) / 1e12
+        res[f"T{rows}"] = {"ms": round(ms, 4), "tflops": round(tf, 2), "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4),
+                           "rows_per_s": round(rows / (ms / 1e3), 1)}
+    return res
+
+
+def run_reference(args) -> dict | None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    rows = args.rows
+    rate, dt = time_oracle(rows, args.oracle_frac, args.steps, args.warmup)
+    sample = (f"each step: oracle on 1/{args.oracle_frac} of one block's intermediate channels at T={rows}, "
+              f"scaled to whole rows")
+    return {"impl": "reference", "metric": METRIC, "value": round(rate, 3), "unit": "rows/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"mlp_5120x17408_T{rows}", "hidden": HIDDEN, "intermediate": INTER, "rows": rows,
+                       "rotation_block": 1024, "seed": 1},
+            "cpu_baseline": {"value": round(rate, 3), "unit": "rows/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(rate, 3), "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--rows", type=int, default=8)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--quick", action="store_true", help="skip the prefill sweep")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-frac", type=int, default=16)
+    ap.add_argument("--oracle-steps", type=int, default=8)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the dominant kernel from an ncu capture, if current")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,444 @@
+// C ABI of the VQ3 library: argument validation, host-side layout packing,
+// workspace carving and kernel dispatch. No device memory is allocated here.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "vq3_internal.h"
+
+namespace vq3 {
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+int ok() {
+  g_err.clear();
+  return VQ3_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(VQ3_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool pow2_block(int b) { return b >= 2 && b <= VQ3_MAX_BLOCK && (b & (b - 1)) == 0; }
+
+int check_linear(const vq3_linear* L, const char* name) {
+  if (!L) return fail(VQ3_EINVAL, "%s: null descriptor", name);
+  if (L->d_in <= 0 || L->d_out <= 0) return fail(VQ3_EINVAL, "%s: d_in=%d d_out=%d must be positive", name, L->d_in, L->d_out);
+  if (!layout_supported(L->d_in, L->d_out))
+    return fail(VQ3_EUNSUPPORTED, "%s: d_in=%d and d_out=%d must be multiples of 64", name, L->d_in, L->d_out);
+  if (!pow2_block(L->block)) return fail(VQ3_EINVAL, "%s: block=%d must be a power of two in [2, 1024]", name, L->block);
+  if (L->d_in % L->block) return fail(VQ3_EINVAL, "%s: d_in=%d is not a multiple of block=%d", name, L->d_in, L->block);
+  if (!L->packed || !L->codebook || !L->scales) return fail(VQ3_EINVAL, "%s: null packed/codebook/scales", name);
+  if (!aligned(L->packed, 16)) return fail(VQ3_EALIGN, "%s: packed indices not 16-byte aligned", name);
+  if (!aligned(L->codebook, 4) || !aligned(L->scales, 4) || (L->signs && !aligned(L->signs, 4)))
+    return fail(VQ3_EALIGN, "%s: codebook, scales and signs must be 4-byte aligned", name);
+  return VQ3_OK;
+}
+
+// ---- workspace carving ----------------------------------------------------
+
+struct LinearWs {
+  size_t xr, partial, counters, total;
+};
+
+LinearWs linear_ws(int rows, int d_in, int d_out) {
+  LinearWs w{};
+  const int kc = pick_kc_len(d_in);
+  const int n_kc = kc ? d_in / kc : 0;
+  size_t off = 0;
+  w.xr = off;
+  off = round_up(off + (size_t)rows * d_in * 2, 256);
+  w.partial = off;
+  off = round_up(off + (size_t)n_kc * kMaxPassRows * d_out * sizeof(float), 256);
+  w.counters = off;
+  off = round_up(off + (size_t)(d_out / kSuChannels) * sizeof(unsigned), 256);
+  w.total = off;
+  return w;
+}
+
+struct MlpWs {
+  size_t xr, h, partial, counters, total;
+};
+
+MlpWs mlp_ws(int rows, const vq3_mlp_layer* l) {
+  MlpWs w{};
+  const int H = l->gate.d_in, I = l->gate.d_out;
+  const int n_kc_gu = H / pick_kc_len(H), n_kc_dn = I / pick_kc_len(I);
+  const size_t part_gu = (size_t)n_kc_gu * 2 * kMaxPassRows * I;
+  const size_t part_dn = (size_t)n_kc_dn * kMaxPassRows * H;
+  size_t off = 0;
+  w.xr = off;
+  off = round_up(off + (size_t)rows * H * 2, 256);
+  w.h = off;
+  off = round_up(off + (size_t)rows * I * 2, 256);
+  w.partial = off;
+  off = round_up(off + (part_gu > part_dn ? part_gu : part_dn) * sizeof(float), 256);
+  w.counters = off;
+  const int groups = (I > H ? I : H) / kSuChannels;
+  off = round_up(off + (size_t)groups * sizeof(unsigned), 256);
+  w.total = off;
+  return w;
+}
+
+int check_mlp(const vq3_mlp_layer* l) {
+  if (!l) return fail(VQ3_EINVAL, "mlp: null layer");
+  int rc;
+  if ((rc = check_linear(&l->gate, "gate"))) return rc;
+  if ((rc = check_linear(&l->up, "up"))) return rc;
+  if ((rc = check_linear(&l->down, "down"))) return rc;
+  if (l->up.d_in != l->gate.d_in || l->up.d_out != l->gate.d_out || l->up.block != l->gate.block ||
+      l->up.signs != l->gate.signs)
+    return fail(VQ3_EINVAL, "mlp: gate and up must share d_in, d_out, block and signs");
+  if (l->down.d_in != l->gate.d_out || l->down.d_out != l->gate.d_in)
+    return fail(VQ3_EINVAL, "mlp: down must be %d -> %d (got %d -> %d)", l->gate.d_out, l->gate.d_in, l->down.d_in,
+                l->down.d_out);
+  return VQ3_OK;
+}
+
+GemvMat gemv_mat(const vq3_linear& L) {
+  GemvMat m;
+  m.packed = static_cast<const uint4*>(L.packed);
+  m.codebook = reinterpret_cast<const uint32_t*>(L.codebook);
+  m.scales = L.scales;
+  return m;
+}
+
+// One matrix (or gate+up) over all rows, in passes of at most kMaxPassRows rows.
+cudaError_t run_gemv(const uint16_t* xr, int rows, int d_in, int d_out, int n_mats, const vq3_linear* mats,
+                     float* partial, unsigned* counters, int mode, uint16_t* out, cudaStream_t st) {
+  GemvArgs a{};
+  a.d_in = d_in;
+  a.d_out = d_out;
+  a.kc_len = pick_kc_len(d_in);
+  a.n_mats = n_mats;
+  for (int i = 0; i < n_mats; ++i) a.mats[i] = gemv_mat(mats[i]);
+  a.partial = partial;
+  a.counters = counters;
+  a.mode = mode;
+  for (int r0 = 0; r0 < rows; r0 += kMaxPassRows) {
+    a.rows = rows - r0 < kMaxPassRows ? rows - r0 : kMaxPassRows;
+    a.xr = xr + (size_t)r0 * d_in;
+    a.out = out + (size_t)r0 * d_out;
+    cudaError_t e = launch_gemv(a, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+uint32_t read_bits6(const uint8_t* s, size_t k) {
+  const size_t bit = 6 * k;
+  const size_t byte = bit / 8;
+  const unsigned sh = (unsigned)(bit % 8);
+  uint32_t v = s[byte];
+  if (sh > 2) v |= (uint32_t)s[byte + 1] << 8;
+  return (v >> sh) & 63u;
+}
+
+}  // namespace
+}  // namespace vq3
+
+using namespace vq3;
+
+extern "C" {
+
+const char* vq3_last_error(void) { return g_err.c_str(); }
+
+const char* vq3_version(void) { return "vq3-gb300 0.1 (sm_103a; layout su64x64-m16n8k16)"; }
+
+size_t vq3_packed_bytes(int d_in, int d_out) {
+  if (!layout_supported(d_in, d_out)) return 0;
+  return (size_t)(d_out / kSuChannels) * (size_t)(d_in / kSuInputs) * kSuBytes;
+}
+
+int vq3_pack_layout(const uint8_t* canonical, int d_in, int d_out, void* dst_host) {
+  if (!canonical || !dst_host) return fail(VQ3_EINVAL, "pack_layout: null pointer");
+  if (!layout_supported(d_in, d_out))
+    return fail(VQ3_EUNSUPPORTED, "pack_layout: d_in=%d, d_out=%d must be positive multiples of 64", d_in, d_out);
+  uint8_t* dst = static_cast<uint8_t*>(dst_host);
+  const int n_mg = d_out / kSuChannels, n_kg = d_in / kSuInputs;
+  for (int mg = 0; mg < n_mg; ++mg) {
+    for (int kg = 0; kg < n_kg; ++kg) {
+      const size_t su = (size_t)mg * n_kg + kg;
+      for (int lane = 0; lane < 32; ++lane) {
+        const int g = lane / 4, t = lane % 4;
+        uint32_t w[13] = {0};
+        for (int n = 0; n < 64; ++n) {
+          const int s = n / 16, m = (n / 4) % 4, e = n % 4;
+          const int p = mg * 32 + m * 8 + g;
+          static const int koff[4] = {0, 1, 8, 9};
+          const int i = kg * 64 + s * 16 + 2 * t + koff[e];
+          const uint32_t idx = read_bits6(canonical, (size_t)p * d_in + i);
+          const int bit = 6 * n;
+          w[bit / 32] |= idx << (bit % 32);
+          if (bit % 32 > 26) w[bit / 32 + 1] |= idx >> (32 - bit % 32);
+        }
+        for (int wi = 0; wi < 12; ++wi) memcpy(dst + lane_word_offset(su, lane, wi), &w[wi], 4);
+      }
+    }
+  }
+  return ok();
+}
+
+int vq3_unpack_layout(const void* packed_host, int d_in, int d_out, uint8_t* canonical) {
+  if (!canonical || !packed_host) return fail(VQ3_EINVAL, "unpack_layout: null pointer");
+  if (!layout_supported(d_in, d_out))
+    return fail(VQ3_EUNSUPPORTED, "unpack_layout: d_in=%d, d_out=%d must be positive multiples of 64", d_in, d_out);
+  const uint8_t* src = static_cast<const uint8_t*>(packed_host);
+  const size_t count = (size_t)(d_out / 2) * d_in;
+  const size_t nbytes = (6 * count + 7) / 8;
+  memset(canonical, 0, nbytes);
+  const int n_mg = d_out / kSuChannels, n_kg = d_in / kSuInputs;
+  for (int mg = 0; mg < n_mg; ++mg) {
+    for (int kg = 0; kg < n_kg; ++kg) {
+      const size_t su = (size_t)mg * n_kg + kg;
+      for (int lane = 0; lane < 32; ++lane) {
+        const int g = lane / 4, t = lane % 4;
+        uint32_t w[13] = {0};
+        for (int wi = 0; wi < 12; ++wi) memcpy(&w[wi], src + lane_word_offset(su, lane, wi), 4);
+        for (int n = 0; n < 64; ++n) {
+          const int s = n / 16, m = (n / 4) % 4, e = n % 4;
+          const int p = mg * 32 + m * 8 + g;
+          static const int koff[4] = {0, 1, 8, 9};
+          const int i = kg * 64 + s * 16 + 2 * t + koff[e];
+          const int bit = 6 * n;
+          const uint64_t v = ((uint64_t)w[bit / 32 + 1] << 32) | w[bit / 32];
+          const uint32_t idx = (uint32_t)(v >> (bit % 32)) & 63u;
+          const size_t k = (size_t)p * d_in + i;
+          const size_t sb = 6 * k;
+          canonical[sb / 8] |= (uint8_t)(idx << (sb % 8));
+          if (sb % 8 > 2) canonical[sb / 8 + 1] |= (uint8_t)(idx >> (8 - sb % 8));
+        }
+      }
+    }
+  }
+  return ok();
+}
+
+int fwht_rotate(const uint16_t* x, int rows, int n, int block, const uint32_t* signs, uint16_t* out, void* stream) {
+  if (rows < 0 || n <= 0) return fail(VQ3_EINVAL, "fwht_rotate: rows=%d n=%d", rows, n);
+  if (!pow2_block(block)) return fail(VQ3_EINVAL, "fwht_rotate: block=%d must be a power of two in [2, 1024]", block);
+  if (n % block) return fail(VQ3_EINVAL, "fwht_rotate: n=%d is not a multiple of block=%d", n, block);
+  if (rows == 0) return ok();
+  if (!x || !out) return fail(VQ3_EINVAL, "fwht_rotate: null x/out");
+  if (!aligned(x, 16) || !aligned(out, 16) || (signs && !aligned(signs, 4)))
+    return fail(VQ3_EALIGN, "fwht_rotate: x/out must be 16-byte aligned, signs 4-byte aligned");
+  cudaError_t e = launch_fwht(x, rows, n, block, signs, out, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fwht_rotate launch");
+  return ok();
+}
+
+size_t vq3_linear_workspace_bytes(int rows, const vq3_linear* L) {
+  if (!L || rows < 0 || !layout_supported(L->d_in, L->d_out)) return 0;
+  return linear_ws(rows, L->d_in, L->d_out).total;
+}
+
+size_t vq3_mlp_workspace_bytes(int rows, const vq3_mlp_layer* layer) {
+  if (!layer || rows < 0 || !layout_supported(layer->gate.d_in, layer->gate.d_out)) return 0;
+  return mlp_ws(rows, layer).total;
+}
+
+int vq3_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
+  if (!workspace) return fail(VQ3_EINVAL, "workspace_init: null workspace");
+  cudaError_t e = cudaMemsetAsync(workspace, 0, ws_bytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "workspace_init memset");
+  return ok();
+}
+
+int vq3_linear_forward(const uint16_t* x, int rows, const vq3_linear* L, uint16_t* out, void* workspace,
+                       size_t ws_bytes, void* stream) {
+  int rc = check_linear(L, "linear");
+  if (rc) return rc;
+  if (rows < 0) return fail(VQ3_EINVAL, "linear: rows=%d", rows);
+  if (rows == 0) return ok();
+  if (!x || !out || !workspace) return fail(VQ3_EINVAL, "linear: null x/out/workspace");
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(workspace, 256))
+    return fail(VQ3_EALIGN, "linear: x/out must be 16-byte aligned and the workspace 256-byte aligned");
+  const LinearWs w = linear_ws(rows, L->d_in, L->d_out);
+  if (ws_bytes < w.total) return fail(VQ3_ENOSPACE, "linear: workspace %zu < %zu bytes", ws_bytes, w.total);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  uint16_t* xr = reinterpret_cast<uint16_t*>(ws + w.xr);
+  cudaError_t e = launch_fwht(x, rows, L->d_in, L->block, L->signs, xr, st);
+  if (e != cudaSuccess) return cuda_fail(e, "linear: rotate launch");
+  e = run_gemv(xr, rows, L->d_in, L->d_out, 1, L, reinterpret_cast<float*>(ws + w.partial),
+               reinterpret_cast<unsigned*>(ws + w.counters), kModeLinear, out, st);
+  if (e != cudaSuccess) return cuda_fail(e, "linear: gemv launch");
+  return ok();
+}
+
+namespace {
+
+struct MlpCall {
+  int rc;
+  MlpWs w;
+  char* ws;
+  cudaStream_t st;
+};
+
+MlpCall mlp_prepare(int rows, const vq3_mlp_layer* layer, void* workspace, size_t ws_bytes, void* stream,
+                    const char* name) {
+  MlpCall c{};
+  c.rc = check_mlp(layer);
+  if (c.rc) return c;
+  if (rows < 0) {
+    c.rc = fail(VQ3_EINVAL, "%s: rows=%d", name, rows);
+    return c;
+  }
+  if (rows == 0) return c;
+  if (!workspace) {
+    c.rc = fail(VQ3_EINVAL, "%s: null workspace", name);
+    return c;
+  }
+  if (!aligned(workspace, 256)) {
+    c.rc = fail(VQ3_EALIGN, "%s: workspace must be 256-byte aligned", name);
+    return c;
+  }
+  c.w = mlp_ws(rows, layer);
+  if (ws_bytes < c.w.total) {
+    c.rc = fail(VQ3_ENOSPACE, "%s: workspace %zu < %zu bytes", name, ws_bytes, c.w.total);
+    return c;
+  }
+  c.ws = static_cast<char*>(workspace);
+  c.st = static_cast<cudaStream_t>(stream);
+  return c;
+}
+
+int gate_up_half(const uint16_t* x, int rows, const vq3_mlp_layer* layer, const MlpCall& c) {
+  const int H = layer->gate.d_in, I = layer->gate.d_out;
+  uint16_t* xr = reinterpret_cast<uint16_t*>(c.ws + c.w.xr);
+  uint16_t* h = reinterpret_cast<uint16_t*>(c.ws + c.w.h);
+  cudaError_t e = launch_fwht(x, rows, H, layer->gate.block, layer->gate.signs, xr, c.st);
+  if (e != cudaSuccess) return cuda_fail(e, "mlp: rotate x launch");
+  const vq3_linear gu[2] = {layer->gate, layer->up};
+  e = run_gemv(xr, rows, H, I, 2, gu, reinterpret_cast<float*>(c.ws + c.w.partial),
+               reinterpret_cast<unsigned*>(c.ws + c.w.counters), kModeSwiglu, h, c.st);
+  if (e != cudaSuccess) return cuda_fail(e, "mlp: gate/up launch");
+  return VQ3_OK;
+}
+
+int down_half(int rows, const vq3_mlp_layer* layer, uint16_t* out, const MlpCall& c) {
+  const int H = layer->gate.d_in, I = layer->gate.d_out;
+  uint16_t* h = reinterpret_cast<uint16_t*>(c.ws + c.w.h);
+  cudaError_t e = launch_fwht(h, rows, I, layer->down.block, layer->down.signs, h, c.st);
+  if (e != cudaSuccess) return cuda_fail(e, "mlp: rotate h launch");
+  e = run_gemv(h, rows, I, H, 1, &layer->down, reinterpret_cast<float*>(c.ws + c.w.partial),
+               reinterpret_cast<unsigned*>(c.ws + c.w.counters), kModeLinear, out, c.st);
+  if (e != cudaSuccess) return cuda_fail(e, "mlp: down launch");
+  return VQ3_OK;
+}
+
+}  // namespace
+
+int vq3_mlp_forward(const uint16_t* x, int rows, const vq3_mlp_layer* layer, uint16_t* out, void* workspace,
+                    size_t ws_bytes, void* stream) {
+  MlpCall c = mlp_prepare(rows, layer, workspace, ws_bytes, stream, "mlp");
+  if (c.rc || rows == 0) return c.rc ? c.rc : ok();
+  if (!x || !out) return fail(VQ3_EINVAL, "mlp: null x/out");
+  if (!aligned(x, 16) || !aligned(out, 16)) return fail(VQ3_EALIGN, "mlp: x/out must be 16-byte aligned");
+  int rc = gate_up_half(x, rows, layer, c);
+  if (rc) return rc;
+  rc = down_half(rows, layer, out, c);
+  if (rc) return rc;
+  return ok();
+}
+
+int vq3_mlp_gate_up(const uint16_t* x, int rows, const vq3_mlp_layer* layer, void* workspace, size_t ws_bytes,
+                    void* stream) {
+  MlpCall c = mlp_prepare(rows, layer, workspace, ws_bytes, stream, "mlp_gate_up");
+  if (c.rc || rows == 0) return c.rc ? c.rc : ok();
+  if (!x) return fail(VQ3_EINVAL, "mlp_gate_up: null x");
+  if (!aligned(x, 16)) return fail(VQ3_EALIGN, "mlp_gate_up: x must be 16-byte aligned");
+  int rc = gate_up_half(x, rows, layer, c);
+  return rc ? rc : ok();
+}
+
+int vq3_mlp_down(int rows, const vq3_mlp_layer* layer, uint16_t* out, void* workspace, size_t ws_bytes,
+                 void* stream) {
+  MlpCall c = mlp_prepare(rows, layer, workspace, ws_bytes, stream, "mlp_down");
+  if (c.rc || rows == 0) return c.rc ? c.rc : ok();
+  if (!out) return fail(VQ3_EINVAL, "mlp_down: null out");
+  if (!aligned(out, 16)) return fail(VQ3_EALIGN, "mlp_down: out must be 16-byte aligned");
+  int rc = down_half(rows, layer, out, c);
+  return rc ? rc : ok();
+}
+
+int vq3_mlp_kernel_launches(int rows, const vq3_mlp_layer* layer) {
+  if (check_mlp(layer) || rows < 0) return -1;
+  if (rows == 0) return 0;
+  const int passes = (rows + kMaxPassRows - 1) / kMaxPassRows;
+  return 2 + 2 * passes;  // two rotations, one gate/up and one down launch per row pass
+}
+
+size_t vq3_mlp_host_workspace_bytes(int rows, const vq3_mlp_layer* layer) {
+  const size_t base = vq3_mlp_workspace_bytes(rows, layer);
+  if (!base) return 0;
+  const size_t io = round_up((size_t)rows * layer->gate.d_in * 2, 256);
+  return base + 2 * io;
+}
+
+int vq3_mlp_forward_host(const uint16_t* x_host, int rows, const vq3_mlp_layer* layer, uint16_t* out_host,
+                         void* workspace, size_t ws_bytes, void* stream) {
+  int rc = check_mlp(layer);
+  if (rc) return rc;
+  if (rows < 0) return fail(VQ3_EINVAL, "mlp_host: rows=%d", rows);
+  if (rows == 0) return ok();
+  if (!x_host || !out_host || !workspace) return fail(VQ3_EINVAL, "mlp_host: null x/out/workspace");
+  if (!aligned(workspace, 256)) return fail(VQ3_EALIGN, "mlp_host: workspace must be 256-byte aligned");
+  const size_t need = vq3_mlp_host_workspace_bytes(rows, layer);
+  if (ws_bytes < need) return fail(VQ3_ENOSPACE, "mlp_host: workspace %zu < %zu bytes", ws_bytes, need);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = (size_t)rows * layer->gate.d_in * 2;
+  const size_t io = round_up(bytes, 256);
+  char* ws = static_cast<char*>(workspace);
+  uint16_t* xd = reinterpret_cast<uint16_t*>(ws);
+  uint16_t* yd = reinterpret_cast<uint16_t*>(ws + io);
+  cudaError_t e = cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e, "mlp_host: copy in");
+  rc = vq3_mlp_forward(xd, rows, layer, yd, ws + 2 * io, ws_bytes - 2 * io, stream);
+  if (rc) return rc;
+  e = cudaMemcpyAsync(out_host, yd, bytes, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return cuda_fail(e, "mlp_host: copy out");
+  e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "mlp_host: synchronize");
+  return ok();
+}
+
+int vq3_residual_rmsnorm(uint16_t* resid, const uint16_t* delta, int rows, int n, float eps, uint16_t* normed,
+                         void* stream) {
+  if (rows < 0 || n <= 0 || !(eps >= 0.f)) return fail(VQ3_EINVAL, "residual_rmsnorm: rows=%d n=%d eps=%g", rows, n, eps);
+  if (rows == 0) return ok();
+  if (!resid || !normed) return fail(VQ3_EINVAL, "residual_rmsnorm: null resid/normed");
+  if (!aligned(resid, 16) || !aligned(normed, 16) || (delta && !aligned(delta, 16)))
+    return fail(VQ3_EALIGN, "residual_rmsnorm: pointers must be 16-byte aligned");
+  cudaError_t e = launch_residual_rmsnorm(resid, delta, rows, n, eps, normed, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "residual_rmsnorm launch");
+  return ok();
+}
+
+int vq3_dequant_dense(const vq3_linear* L, int apply_scale, uint16_t* w_out, void* stream) {
+  int rc = check_linear(L, "dequant");
+  if (rc) return rc;
+  if (!w_out) return fail(VQ3_EINVAL, "dequant: null w_out");
+  if (!aligned(w_out, 16)) return fail(VQ3_EALIGN, "dequant: w_out must be 16-byte aligned");
+  cudaError_t e = launch_dequant(*L, apply_scale ? 1 : 0, w_out, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "dequant launch");
+  return ok();
+}
+
+}  // extern "C"

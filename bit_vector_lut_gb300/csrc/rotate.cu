@@ -1,0 +1,159 @@
+// Online Hadamard rotation and the residual/RMSNorm step.
+//
+// fwht_rotate: out[r, blk] = H_b diag(s_blk) x[r, blk] / sqrt(b) for every
+// b-wide block of every row, H_b in Sylvester (natural) order. Source: model
+// card "anemll/anemll-forge-qwen3.8-27B", section "Release 0.2: three-bit MLP,
+// token-mixer rotations, distilled weights", bullet "Token-mixer rotations"
+// (1,024-wide Hadamard blocks with seeded signs, the MLP inputs rotated the
+// same way).
+//
+// One CTA owns one (row, block): each thread keeps b/128 values in registers,
+// the butterflies whose partner is in the same thread run in registers, those
+// across lanes use warp shuffles and those across warps go through shared
+// memory. FP32 arithmetic, one FP16 rounding at the end.
+#include <cuda_fp16.h>
+
+#include "vq3_internal.h"
+
+namespace vq3 {
+namespace {
+
+constexpr int kRotThreads = 128;
+
+// Element j of the block lives in thread (j % 128) slot (j / 128) while the
+// block is in "lane-major" form. Butterflies of stride h < 32 pair lanes within
+// a warp (shuffle), strides 32 and 64 pair warps (shared memory), strides >= 128
+// pair slots of the same thread (registers).
+template <int B>
+__global__ void __launch_bounds__(kRotThreads) fwht_kernel(const uint16_t* __restrict__ x, int n,
+                                                            const uint32_t* __restrict__ signs,
+                                                            uint16_t* out, float scale) {
+  constexpr int V = (B + kRotThreads - 1) / kRotThreads;  // values per thread
+  constexpr int ACTIVE = B < kRotThreads ? B : kRotThreads;
+  __shared__ float sm[V * kRotThreads];
+  const int tid = threadIdx.x;
+  const int blocks_per_row = n / B;
+  const int row = blockIdx.x / blocks_per_row;
+  const int blk = blockIdx.x % blocks_per_row;
+  const size_t base = (size_t)row * n + (size_t)blk * B;
+
+  float v[V];
+#pragma unroll
+  for (int s = 0; s < V; ++s) {
+    const int j = s * kRotThreads + tid;
+    float f = 0.f;
+    if (tid < ACTIVE) {
+      f = __half2float(__ushort_as_half(x[base + j]));
+      if (signs) {
+        const int col = blk * B + j;
+        if ((__ldg(signs + (col >> 5)) >> (col & 31)) & 1u) f = -f;
+      }
+    }
+    v[s] = f;
+  }
+
+  // strides 1..16 (and up to B/2 when B <= 32): lanes of one warp
+#pragma unroll
+  for (int h = 1; h < 32 && h < B; h <<= 1) {
+#pragma unroll
+    for (int s = 0; s < V; ++s) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[s], h);
+      v[s] = (tid & h) ? (o - v[s]) : (v[s] + o);
+    }
+  }
+  // strides 32 and 64: across warps through shared memory
+#pragma unroll
+  for (int h = 32; h < kRotThreads && h < B; h <<= 1) {
+#pragma unroll
+    for (int s = 0; s < V; ++s) sm[s * kRotThreads + tid] = v[s];
+    __syncthreads();
+#pragma unroll
+    for (int s = 0; s < V; ++s) {
+      const float o = sm[s * kRotThreads + (tid ^ h)];
+      v[s] = (tid & h) ? (o - v[s]) : (v[s] + o);
+    }
+    __syncthreads();
+  }
+  // strides >= 128: slots of the same thread
+#pragma unroll
+  for (int hs = 1; hs < V; hs <<= 1) {
+#pragma unroll
+    for (int s = 0; s < V; ++s) {
+      if ((s & hs) == 0) {
+        const float a = v[s], c = v[s + hs];
+        v[s] = a + c;
+        v[s + hs] = a - c;
+      }
+    }
+  }
+
+#pragma unroll
+  for (int s = 0; s < V; ++s) {
+    const int j = s * kRotThreads + tid;
+    if (tid < ACTIVE) out[base + j] = __half_as_ushort(__float2half_rn(v[s] * scale));
+  }
+}
+
+template <int B>
+cudaError_t launch_b(const uint16_t* x, int rows, int n, const uint32_t* signs, uint16_t* out,
+                     cudaStream_t st) {
+  const float scale = 1.0f / sqrtf((float)B);
+  const long long grid = (long long)rows * (n / B);
+  fwht_kernel<B><<<(unsigned)grid, kRotThreads, 0, st>>>(x, n, signs, out, scale);
+  return cudaGetLastError();
+}
+
+// resid <- fp16(resid + delta); normed <- fp16(resid * rsqrt(mean(resid^2) + eps))
+__global__ void __launch_bounds__(256) residual_rmsnorm_kernel(uint16_t* resid, const uint16_t* delta, int n,
+                                                               float eps, uint16_t* normed) {
+  __shared__ float red[8];
+  const size_t base = (size_t)blockIdx.x * n;
+  float ss = 0.f;
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    float r = __half2float(__ushort_as_half(resid[base + j]));
+    if (delta) {
+      const __half s = __float2half_rn(r + __half2float(__ushort_as_half(delta[base + j])));
+      resid[base + j] = __half_as_ushort(s);
+      r = __half2float(s);
+    }
+    ss += r * r;
+  }
+#pragma unroll
+  for (int h = 16; h > 0; h >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, h);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
+  const float inv = 1.0f / sqrtf(tot / (float)n + eps);
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    const float r = __half2float(__ushort_as_half(resid[base + j]));
+    normed[base + j] = __half_as_ushort(__float2half_rn(r * inv));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fwht(const uint16_t* x, int rows, int n, int block, const uint32_t* signs,
+                        uint16_t* out, cudaStream_t st) {
+  switch (block) {
+    case 2: return launch_b<2>(x, rows, n, signs, out, st);
+    case 4: return launch_b<4>(x, rows, n, signs, out, st);
+    case 8: return launch_b<8>(x, rows, n, signs, out, st);
+    case 16: return launch_b<16>(x, rows, n, signs, out, st);
+    case 32: return launch_b<32>(x, rows, n, signs, out, st);
+    case 64: return launch_b<64>(x, rows, n, signs, out, st);
+    case 128: return launch_b<128>(x, rows, n, signs, out, st);
+    case 256: return launch_b<256>(x, rows, n, signs, out, st);
+    case 512: return launch_b<512>(x, rows, n, signs, out, st);
+    case 1024: return launch_b<1024>(x, rows, n, signs, out, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_residual_rmsnorm(uint16_t* resid, const uint16_t* delta, int rows, int n, float eps,
+                                    uint16_t* normed, cudaStream_t st) {
+  residual_rmsnorm_kernel<<<rows, 256, 0, st>>>(resid, delta, n, eps, normed);
+  return cudaGetLastError();
+}
+
+}  // namespace vq3

@@ -1,0 +1,264 @@
+"""Python binding of libvq3.so (argument marshalling only).
+
+Every step of the VQ3 MLP path runs in the library's CUDA kernels; this module
+only turns torch tensors into raw pointers and streams, and raises on a
+non-zero status. PyTorch supplies device memory and streams. Importing this
+module fails loudly when the library has not been built: there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_float, c_int, c_size_t, c_uint8, c_void_p
+
+import numpy as np
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libvq3.so")
+
+VQ3_OK = 0
+ERRORS = {-1: "VQ3_EINVAL", -2: "VQ3_EALIGN", -3: "VQ3_EUNSUPPORTED", -4: "VQ3_ECUDA", -5: "VQ3_ENOSPACE"}
+
+
+class Vq3Error(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{ERRORS.get(code, code)}: {msg}")
+        self.code = code
+
+
+class vq3_linear(ctypes.Structure):
+    _fields_ = [("d_in", c_int), ("d_out", c_int), ("block", c_int), ("packed", c_void_p),
+                ("codebook", c_void_p), ("scales", c_void_p), ("signs", c_void_p)]
+
+
+class vq3_mlp_layer(ctypes.Structure):
+    _fields_ = [("gate", vq3_linear), ("up", vq3_linear), ("down", vq3_linear)]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    sig = {
+        "vq3_packed_bytes": (c_size_t, [c_int, c_int]),
+        "vq3_pack_layout": (c_int, [POINTER(c_uint8), c_int, c_int, c_void_p]),
+        "vq3_unpack_layout": (c_int, [c_void_p, c_int, c_int, POINTER(c_uint8)]),
+        "fwht_rotate": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]),
+        "vq3_linear_workspace_bytes": (c_size_t, [c_int, POINTER(vq3_linear)]),
+        "vq3_mlp_workspace_bytes": (c_size_t, [c_int, POINTER(vq3_mlp_layer)]),
+        "vq3_workspace_init": (c_int, [c_void_p, c_size_t, c_void_p]),
+        "vq3_linear_forward": (c_int, [c_void_p, c_int, POINTER(vq3_linear), c_void_p, c_void_p, c_size_t, c_void_p]),
+        "vq3_mlp_forward": (c_int, [c_void_p, c_int, POINTER(vq3_mlp_layer), c_void_p, c_void_p, c_size_t, c_void_p]),
+        "vq3_mlp_gate_up": (c_int, [c_void_p, c_int, POINTER(vq3_mlp_layer), c_void_p, c_size_t, c_void_p]),
+        "vq3_mlp_down": (c_int, [c_int, POINTER(vq3_mlp_layer), c_void_p, c_void_p, c_size_t, c_void_p]),
+        "vq3_mlp_kernel_launches": (c_int, [c_int, POINTER(vq3_mlp_layer)]),
+        "vq3_mlp_host_workspace_bytes": (c_size_t, [c_int, POINTER(vq3_mlp_layer)]),
+        "vq3_mlp_forward_host": (c_int, [c_void_p, c_int, POINTER(vq3_mlp_layer), c_void_p, c_void_p, c_size_t,
+                                         c_void_p]),
+        "vq3_residual_rmsnorm": (c_int, [c_void_p, c_void_p, c_int, c_int, c_float, c_void_p, c_void_p]),
+        "vq3_dequant_dense": (c_int, [POINTER(vq3_linear), c_int, c_void_p, c_void_p]),
+        "vq3_last_error": (ctypes.c_char_p, []),
+        "vq3_version": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def _check(rc: int) -> None:
+    if rc != VQ3_OK:
+        raise Vq3Error(rc, lib.vq3_last_error().decode())
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def version() -> str:
+    return lib.vq3_version().decode()
+
+
+# ---------------------------------------------------------------- layout (host)
+
+def packed_bytes(d_in: int, d_out: int) -> int:
+    return int(lib.vq3_packed_bytes(d_in, d_out))
+
+
+def pack_layout(canonical: np.ndarray, d_in: int, d_out: int) -> np.ndarray:
+    """Canonical 6-bit little-endian stream -> GPU layout (host bytes)."""
+    src = np.ascontiguousarray(canonical, dtype=np.uint8)
+    dst = np.empty(max(packed_bytes(d_in, d_out), 1), dtype=np.uint8)
+    _check(lib.vq3_pack_layout(src.ctypes.data_as(POINTER(c_uint8)), d_in, d_out, dst.ctypes.data_as(c_void_p)))
+    return dst
+
+
+def unpack_layout(packed: np.ndarray, d_in: int, d_out: int) -> np.ndarray:
+    src = np.ascontiguousarray(packed, dtype=np.uint8)
+    n = (6 * (d_out // 2) * d_in + 7) // 8
+    dst = np.empty(n, dtype=np.uint8)
+    _check(lib.vq3_unpack_layout(src.ctypes.data_as(c_void_p), d_in, d_out, dst.ctypes.data_as(POINTER(c_uint8))))
+    return dst
+
+
+# ---------------------------------------------------------------- weights on the device
+
+class Linear:
+    """One VQ3 matrix resident on the GPU (packed indices, codebook, scales, signs)."""
+
+    def __init__(self, d_in, d_out, block, packed: torch.Tensor, codebook: torch.Tensor, scales: torch.Tensor,
+                 signs: torch.Tensor | None = None):
+        self.d_in, self.d_out, self.block = int(d_in), int(d_out), int(block)
+        self.packed, self.codebook, self.scales, self.signs = packed, codebook, scales, signs
+        self.struct = vq3_linear(self.d_in, self.d_out, self.block, _ptr(packed), _ptr(codebook), _ptr(scales),
+                                 _ptr(signs))
+
+    @classmethod
+    def from_canonical(cls, d_in, d_out, block, stream, codebook, scales, signs=None, device="cuda"):
+        packed = torch.from_numpy(pack_layout(stream, d_in, d_out)).to(device)
+        cb = torch.from_numpy(np.ascontiguousarray(codebook, dtype=np.float16)).to(device)
+        sc = torch.from_numpy(np.ascontiguousarray(scales, dtype=np.float16)).to(device)
+        sg = None
+        if signs is not None:
+            sg = torch.from_numpy(np.ascontiguousarray(signs, dtype=np.uint32).view(np.int32)).to(device)
+        return cls(d_in, d_out, block, packed, cb, sc, sg)
+
+    @classmethod
+    def from_matrix(cls, m, device="cuda"):
+        """From any object with d_in, d_out, block, stream, codebook, scales, signs fields."""
+        return cls.from_canonical(m.d_in, m.d_out, m.block, m.stream, m.codebook, m.scales, m.signs, device)
+
+
+class MLP:
+    """One SwiGLU block: gate and up share the input rotation; down has its own."""
+
+    def __init__(self, gate: Linear, up: Linear, down: Linear):
+        self.gate, self.up, self.down = gate, up, down
+        self.struct = vq3_mlp_layer(gate.struct, up.struct, down.struct)
+
+    @classmethod
+    def from_block(cls, blk, device="cuda"):
+        gate = Linear.from_matrix(blk.gate, device)
+        if blk.up.signs is not None and blk.gate.signs is not None and np.array_equal(blk.up.signs, blk.gate.signs):
+            up = Linear.from_canonical(blk.up.d_in, blk.up.d_out, blk.up.block, blk.up.stream, blk.up.codebook,
+                                       blk.up.scales, None, device)
+            up.signs = gate.signs
+            up.struct.signs = gate.struct.signs
+        else:
+            up = Linear.from_matrix(blk.up, device)
+        down = Linear.from_matrix(blk.down, device)
+        return cls(gate, up, down)
+
+    @property
+    def hidden(self) -> int:
+        return self.gate.d_in
+
+
+# ---------------------------------------------------------------- workspaces
+
+def linear_workspace_bytes(rows: int, lin: Linear) -> int:
+    return int(lib.vq3_linear_workspace_bytes(rows, ctypes.byref(lin.struct)))
+
+
+def mlp_workspace_bytes(rows: int, layer: MLP) -> int:
+    return int(lib.vq3_mlp_workspace_bytes(rows, ctypes.byref(layer.struct)))
+
+
+def mlp_host_workspace_bytes(rows: int, layer: MLP) -> int:
+    return int(lib.vq3_mlp_host_workspace_bytes(rows, ctypes.byref(layer.struct)))
+
+
+def workspace(nbytes: int, device="cuda", stream=None) -> torch.Tensor:
+    """A device buffer of nbytes, zero-filled by the library (counters start at zero)."""
+    ws = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    _check(lib.vq3_workspace_init(ws.data_ptr(), ws.numel(), _stream(stream)))
+    return ws
+
+
+# ---------------------------------------------------------------- operations
+
+def fwht_rotate(x: torch.Tensor, block: int, signs: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+    rows, n = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    _check(lib.fwht_rotate(x.data_ptr(), rows, n, block, _ptr(signs), out.data_ptr(), _stream(stream)))
+    return out
+
+
+def linear_forward(x: torch.Tensor, lin: Linear, out=None, ws=None, stream=None) -> torch.Tensor:
+    rows = x.shape[0]
+    if out is None:
+        out = torch.empty((rows, lin.d_out), dtype=torch.float16, device=x.device)
+    if ws is None:
+        ws = workspace(linear_workspace_bytes(rows, lin), x.device, stream)
+    _check(lib.vq3_linear_forward(x.data_ptr(), rows, ctypes.byref(lin.struct), out.data_ptr(), ws.data_ptr(),
+                                  ws.numel(), _stream(stream)))
+    return out
+
+
+def mlp_forward(x: torch.Tensor, layer: MLP, out=None, ws=None, stream=None) -> torch.Tensor:
+    rows = x.shape[0]
+    if out is None:
+        out = torch.empty((rows, layer.down.d_out), dtype=torch.float16, device=x.device)
+    if ws is None:
+        ws = workspace(mlp_workspace_bytes(rows, layer), x.device, stream)
+    _check(lib.vq3_mlp_forward(x.data_ptr(), rows, ctypes.byref(layer.struct), out.data_ptr(), ws.data_ptr(),
+                               ws.numel(), _stream(stream)))
+    return out
+
+
+def mlp_gate_up(x: torch.Tensor, layer: MLP, ws: torch.Tensor, stream=None) -> None:
+    _check(lib.vq3_mlp_gate_up(x.data_ptr(), x.shape[0], ctypes.byref(layer.struct), ws.data_ptr(), ws.numel(),
+                               _stream(stream)))
+
+
+def mlp_down(rows: int, layer: MLP, out: torch.Tensor, ws: torch.Tensor, stream=None) -> torch.Tensor:
+    _check(lib.vq3_mlp_down(rows, ctypes.byref(layer.struct), out.data_ptr(), ws.data_ptr(), ws.numel(),
+                            _stream(stream)))
+    return out
+
+
+def mlp_kernel_launches(rows: int, layer: MLP) -> int:
+    return int(lib.vq3_mlp_kernel_launches(rows, ctypes.byref(layer.struct)))
+
+
+def mlp_forward_host(x: np.ndarray, layer: MLP, ws: torch.Tensor, out: np.ndarray | None = None,
+                     stream=None) -> np.ndarray:
+    """Host buffers in and out (the library copies through the workspace and waits)."""
+    x = np.ascontiguousarray(x, dtype=np.float16)
+    rows = x.shape[0]
+    if out is None:
+        out = np.empty((rows, layer.down.d_out), dtype=np.float16)
+    _check(lib.vq3_mlp_forward_host(x.ctypes.data_as(c_void_p), rows, ctypes.byref(layer.struct),
+                                    out.ctypes.data_as(c_void_p), ws.data_ptr(), ws.numel(), _stream(stream)))
+    return out
+
+
+def residual_rmsnorm(resid: torch.Tensor, delta: torch.Tensor | None, eps: float = 1e-6, normed=None,
+                     stream=None) -> torch.Tensor:
+    rows, n = resid.shape
+    if normed is None:
+        normed = torch.empty_like(resid)
+    _check(lib.vq3_residual_rmsnorm(resid.data_ptr(), _ptr(delta), rows, n, eps, normed.data_ptr(), _stream(stream)))
+    return normed
+
+
+def dequant_dense(lin: Linear, apply_scale: bool, stream=None) -> torch.Tensor:
+    w = torch.empty((lin.d_out, lin.d_in), dtype=torch.float16, device=lin.packed.device)
+    _check(lib.vq3_dequant_dense(ctypes.byref(lin.struct), 1 if apply_scale else 0, w.data_ptr(), _stream(stream)))
+    return w

@@ -23,9 +23,11 @@
  * Conventions (every entry point):
  *   - Return value: VQ3_OK (0) or a negative VQ3_E* code; vq3_last_error()
  *     then returns a thread-local message. No C++ exception crosses the ABI.
- *   - The caller owns every buffer. Device pointers must be 16-byte aligned
- *     (VQ3_EALIGN otherwise). The library never allocates device memory; the
- *     entry points that need scratch take a caller-supplied workspace.
+ *   - The caller owns every buffer. Activation, output and packed-index
+ *     pointers must be 16-byte aligned, codebook, scale and sign pointers
+ *     4-byte aligned and workspaces 256-byte aligned (VQ3_EALIGN otherwise).
+ *     The library never allocates device memory; the entry points that need
+ *     scratch take a caller-supplied workspace.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream). Device work is enqueued asynchronously on it; arguments are
  *     validated on the host before anything is enqueued, so an error return
@@ -39,13 +41,19 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define VQ3_API __attribute__((visibility("default")))
+#else
+#define VQ3_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
 
 #define VQ3_OK 0
 #define VQ3_EINVAL (-1)       /* bad size, null pointer or inconsistent descriptor */
-#define VQ3_EALIGN (-2)       /* a device pointer is not 16-byte aligned */
+#define VQ3_EALIGN (-2)       /* a pointer breaks the alignment rule above */
 #define VQ3_EUNSUPPORTED (-3) /* shape outside what the kernels implement */
 #define VQ3_ECUDA (-4)        /* a CUDA runtime call failed (message has the CUDA error) */
 #define VQ3_ENOSPACE (-5)     /* workspace smaller than the size query returned */
@@ -87,7 +95,7 @@ typedef struct vq3_mlp_layer {
 
 /* Size in bytes of one matrix's GPU-layout indices (equal to the canonical
  * stream's size: 6 bits per output pair and input column). 0 if unsupported. */
-size_t vq3_packed_bytes(int d_in, int d_out);
+VQ3_API size_t vq3_packed_bytes(int d_in, int d_out);
 
 /*
  * Host-side, offline. Reorders a canonical index stream into the GPU layout.
@@ -98,11 +106,11 @@ size_t vq3_packed_bytes(int d_in, int d_out);
  * Errors: VQ3_EINVAL (null pointer), VQ3_EUNSUPPORTED (d_in or d_out not a
  * positive multiple of 64).
  */
-int vq3_pack_layout(const uint8_t* canonical, int d_in, int d_out, void* dst_host);
+VQ3_API int vq3_pack_layout(const uint8_t* canonical, int d_in, int d_out, void* dst_host);
 
 /* Host-side inverse of vq3_pack_layout (pad bits of the canonical stream are
  * written as zero). Same errors. */
-int vq3_unpack_layout(const void* packed_host, int d_in, int d_out, uint8_t* canonical);
+VQ3_API int vq3_unpack_layout(const void* packed_host, int d_in, int d_out, uint8_t* canonical);
 
 /*
  * Blocked, normalised fast Walsh-Hadamard transform of each row:
@@ -113,7 +121,7 @@ int vq3_unpack_layout(const void* packed_host, int d_in, int d_out, uint8_t* can
  * block a power of two in [2, 1024]. signs: device bit-packed over n, or NULL.
  * Arithmetic in FP32, one FP16 rounding at the end.
  */
-int fwht_rotate(const uint16_t* x, int rows, int n, int block, const uint32_t* signs,
+VQ3_API int fwht_rotate(const uint16_t* x, int rows, int n, int block, const uint32_t* signs,
                 uint16_t* out, void* stream);
 
 /*
@@ -123,16 +131,16 @@ int fwht_rotate(const uint16_t* x, int rows, int n, int block, const uint32_t* s
  * every completed call leaves the counters at zero again. Calls that share a
  * workspace must not overlap on the GPU (same stream, or ordered by events).
  */
-size_t vq3_linear_workspace_bytes(int rows, const vq3_linear* L);
-size_t vq3_mlp_workspace_bytes(int rows, const vq3_mlp_layer* layer);
-int vq3_workspace_init(void* workspace, size_t ws_bytes, void* stream);
+VQ3_API size_t vq3_linear_workspace_bytes(int rows, const vq3_linear* L);
+VQ3_API size_t vq3_mlp_workspace_bytes(int rows, const vq3_mlp_layer* layer);
+VQ3_API int vq3_workspace_init(void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * One rotated VQ3 linear layer: out = fp16( W (R x) ), FP32 accumulation.
  * x: device FP16 [rows][d_in]; out: device FP16 [rows][d_out] (must not alias x).
  * Errors: VQ3_EINVAL, VQ3_EALIGN, VQ3_EUNSUPPORTED, VQ3_ENOSPACE, VQ3_ECUDA.
  */
-int vq3_linear_forward(const uint16_t* x, int rows, const vq3_linear* L, uint16_t* out,
+VQ3_API int vq3_linear_forward(const uint16_t* x, int rows, const vq3_linear* L, uint16_t* out,
                        void* workspace, size_t ws_bytes, void* stream);
 
 /*
@@ -145,16 +153,32 @@ int vq3_linear_forward(const uint16_t* x, int rows, const vq3_linear* L, uint16_
  * x: device FP16 [rows][d]; out: device FP16 [rows][d] (d = gate.d_in); out may
  * not alias x. Same errors as vq3_linear_forward.
  */
-int vq3_mlp_forward(const uint16_t* x, int rows, const vq3_mlp_layer* layer, uint16_t* out,
+VQ3_API int vq3_mlp_forward(const uint16_t* x, int rows, const vq3_mlp_layer* layer, uint16_t* out,
                     void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * The two halves of vq3_mlp_forward, for callers that schedule or time them
+ * separately (same workspace, same stream order):
+ *   vq3_mlp_gate_up: h = silu(W_g R_g x) * (W_u R_g x), kept in the workspace;
+ *   vq3_mlp_down:    out = fp16( W_d R_d h ), h read from the workspace.
+ * Calling gate_up then down equals one vq3_mlp_forward, bit for bit.
+ */
+VQ3_API int vq3_mlp_gate_up(const uint16_t* x, int rows, const vq3_mlp_layer* layer, void* workspace,
+                            size_t ws_bytes, void* stream);
+VQ3_API int vq3_mlp_down(int rows, const vq3_mlp_layer* layer, uint16_t* out, void* workspace, size_t ws_bytes,
+                         void* stream);
+
+/* Number of kernels one vq3_mlp_forward call launches at `rows` rows (-1 on a
+ * bad descriptor). */
+VQ3_API int vq3_mlp_kernel_launches(int rows, const vq3_mlp_layer* layer);
 
 /*
  * Same as vq3_mlp_forward with HOST buffers: copies x (pinned or pageable host
  * memory) to the workspace, runs the block, copies the result back into
  * out_host and waits for the stream. Workspace: vq3_mlp_host_workspace_bytes.
  */
-size_t vq3_mlp_host_workspace_bytes(int rows, const vq3_mlp_layer* layer);
-int vq3_mlp_forward_host(const uint16_t* x_host, int rows, const vq3_mlp_layer* layer,
+VQ3_API size_t vq3_mlp_host_workspace_bytes(int rows, const vq3_mlp_layer* layer);
+VQ3_API int vq3_mlp_forward_host(const uint16_t* x_host, int rows, const vq3_mlp_layer* layer,
                          uint16_t* out_host, void* workspace, size_t ws_bytes, void* stream);
 
 /*
@@ -163,7 +187,7 @@ int vq3_mlp_forward_host(const uint16_t* x_host, int rows, const vq3_mlp_layer* 
  *   normed <- fp16(resid / sqrt(mean(resid^2) + eps))    (unit weight, FP32 math)
  * resid, delta, normed: device FP16 [rows][n]; normed may not alias resid.
  */
-int vq3_residual_rmsnorm(uint16_t* resid, const uint16_t* delta, int rows, int n, float eps,
+VQ3_API int vq3_residual_rmsnorm(uint16_t* resid, const uint16_t* delta, int rows, int n, float eps,
                          uint16_t* normed, void* stream);
 
 /*
@@ -173,13 +197,13 @@ int vq3_residual_rmsnorm(uint16_t* resid, const uint16_t* delta, int rows, int n
  * product is exact, so this is the correctly rounded weight).
  * w_out: device FP16 [d_out][d_in].
  */
-int vq3_dequant_dense(const vq3_linear* L, int apply_scale, uint16_t* w_out, void* stream);
+VQ3_API int vq3_dequant_dense(const vq3_linear* L, int apply_scale, uint16_t* w_out, void* stream);
 
 /* Message for the last error on the calling thread ("" if none). */
-const char* vq3_last_error(void);
+VQ3_API const char* vq3_last_error(void);
 
 /* Library build/version string. */
-const char* vq3_version(void);
+VQ3_API const char* vq3_version(void);
 
 #ifdef __cplusplus
 }

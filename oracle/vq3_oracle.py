@@ -39,6 +39,7 @@ computed here.
 
 from __future__ import annotations
 
+import functools
 import math
 
 import numpy as np
@@ -63,9 +64,11 @@ def unpack_indices(stream: np.ndarray, start: int, count: int) -> np.ndarray:
     b1 = (last_bit + 7) // 8
     bits = np.unpackbits(stream[b0:b1], bitorder="little")
     skip = first_bit - 8 * b0
-    bits = bits[skip: skip + INDEX_BITS * count].reshape(count, INDEX_BITS).astype(np.int64)
-    weights = np.int64(1) << np.arange(INDEX_BITS, dtype=np.int64)
-    return bits @ weights
+    bits = bits[skip: skip + INDEX_BITS * count].reshape(count, INDEX_BITS)
+    idx = np.zeros(count, dtype=np.int64)
+    for b in range(INDEX_BITS):
+        idx |= bits[:, b].astype(np.int64) << b
+    return idx
 
 
 def pack_indices(idx: np.ndarray) -> np.ndarray:
@@ -123,12 +126,17 @@ def popcount_parity(m: np.ndarray) -> np.ndarray:
     return parity
 
 
+@functools.lru_cache(maxsize=16)
 def hadamard(b: int) -> np.ndarray:
-    """Sylvester Hadamard matrix of order b (a power of two): H[r][c] = (-1)^popcount(r & c)."""
+    """Sylvester Hadamard matrix of order b (a power of two): H[r][c] = (-1)^popcount(r & c).
+
+    The returned array is cached and read-only."""
     if b < 1 or b & (b - 1):
         raise ValueError("Hadamard order must be a power of two")
     r = np.arange(b)
-    return 1.0 - 2.0 * popcount_parity(r[:, None] & r[None, :]).astype(np.float64)
+    H = 1.0 - 2.0 * popcount_parity(r[:, None] & r[None, :]).astype(np.float64)
+    H.setflags(write=False)
+    return H
 
 
 def sign_vector(sign_words, n: int) -> np.ndarray:

@@ -1,0 +1,140 @@
+"""Host-side checks of the C-ABI library (no GPU): it loads, exports every
+symbol include/vq3.h declares, packs the canonical stream losslessly, and
+rejects bad arguments with the documented status before touching the GPU."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import vq3_oracle as O
+from synth import inputs as S
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+vq3 = pytest.importorskip("bit_vector_lut_gb300.vq3", reason="libvq3.so not built")
+
+
+def declared_symbols():
+    txt = open(os.path.join(ROOT, "include", "vq3.h")).read()
+    return re.findall(r"VQ3_API\s+[\w\s\*]+?\b(\w+)\s*\(", txt)
+
+
+def test_exports_every_declared_symbol():
+    names = declared_symbols()
+    assert len(names) >= 15
+    lib = ctypes.CDLL(vq3.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_string():
+    assert "sm_103a" in vq3.version()
+
+
+@pytest.mark.parametrize("d_in,d_out", [(64, 64), (256, 256), (128, 192), (5120, 128)])
+def test_pack_roundtrip(d_in, d_out):
+    s = S.index_stream(S.rng(d_in + d_out), d_in, d_out)
+    p = vq3.pack_layout(s, d_in, d_out)
+    assert p.size == vq3.packed_bytes(d_in, d_out) == s.size
+    assert np.array_equal(vq3.unpack_layout(p, d_in, d_out), s)
+
+
+@pytest.mark.parametrize("pattern", ["zeros", "all63", "ramp", "alternate"])
+def test_pack_edge_patterns(pattern):
+    d_in, d_out = 128, 64
+    n = (d_out // 2) * d_in
+    idx = {"zeros": np.zeros(n, int), "all63": np.full(n, 63), "ramp": np.arange(n) % 64,
+           "alternate": (np.arange(n) % 2) * 63}[pattern]
+    s = O.pack_indices(idx)
+    p = vq3.pack_layout(s, d_in, d_out)
+    assert np.array_equal(vq3.unpack_layout(p, d_in, d_out), s)
+    if pattern in ("zeros", "all63"):
+        assert np.array_equal(np.unique(p), np.unique(s))
+
+
+def test_pack_full_size_roundtrip():
+    m = S.matrix(S.rng(1), 5120, 17408, 1024)
+    p = vq3.pack_layout(m.stream, 5120, 17408)
+    assert p.size == 33_423_360
+    assert np.array_equal(vq3.unpack_layout(p, 5120, 17408), m.stream)
+
+
+def test_layout_places_lane_fragments():
+    # the GPU layout is a permutation of index positions: a single nonzero index
+    # moves to exactly one 6-bit field of the packed buffer
+    d_in, d_out = 64, 64
+    for (p_, i_) in [(0, 0), (5, 9), (31, 63), (17, 40)]:
+        idx = np.zeros((d_out // 2, d_in), int)
+        idx[p_, i_] = 0b101101
+        pk = vq3.pack_layout(O.pack_indices(idx), d_in, d_out)
+        bits = np.unpackbits(pk, bitorder="little")
+        assert bits.sum() == 4
+
+
+def test_sizes_and_unsupported_shapes():
+    assert vq3.packed_bytes(5120, 17408) == 33_423_360
+    assert vq3.packed_bytes(100, 64) == 0
+    with pytest.raises(vq3.Vq3Error) as e:
+        vq3.pack_layout(np.zeros(10, np.uint8), 100, 64)
+    assert e.value.code == -3
+
+
+def fake_linear(d_in=256, d_out=256, block=256, packed=0x10000, cb=0x20000, sc=0x30000, signs=None):
+    return vq3.vq3_linear(d_in, d_out, block, packed, cb, sc, signs)
+
+
+def test_error_paths_never_launch():
+    L = fake_linear()
+    lib = vq3.lib
+    # rows == 0 is a valid no-op even with fake device pointers
+    assert lib.vq3_linear_forward(0x40000, 0, ctypes.byref(L), 0x50000, 0x60000, 1 << 20, None) == 0
+    # negative rows
+    assert lib.vq3_linear_forward(0x40000, -1, ctypes.byref(L), 0x50000, 0x60000, 1 << 20, None) == -1
+    # bad block size
+    assert lib.vq3_linear_forward(0x40000, 8, ctypes.byref(fake_linear(block=3)), 0x50000, 0x60000, 1 << 20, None) == -1
+    # d_in not a multiple of the block
+    assert lib.vq3_linear_forward(0x40000, 8, ctypes.byref(fake_linear(d_in=320, block=256)), 0x50000, 0x60000,
+                                  1 << 20, None) == -1
+    # unsupported width
+    assert lib.vq3_linear_forward(0x40000, 8, ctypes.byref(fake_linear(d_out=96)), 0x50000, 0x60000, 1 << 20,
+                                  None) == -3
+    # null pointers
+    assert lib.vq3_linear_forward(0x40000, 8, ctypes.byref(fake_linear(packed=None)), 0x50000, 0x60000, 1 << 20,
+                                  None) == -1
+    assert lib.vq3_linear_forward(None, 8, ctypes.byref(L), 0x50000, 0x60000, 1 << 20, None) == -1
+    # misaligned packed indices / activations
+    assert lib.vq3_linear_forward(0x40000, 8, ctypes.byref(fake_linear(packed=0x10008)), 0x50000, 0x60000,
+                                  1 << 20, None) == -2
+    assert lib.vq3_linear_forward(0x40004, 8, ctypes.byref(L), 0x50000, 0x60000, 1 << 20, None) == -2
+    # workspace too small
+    need = lib.vq3_linear_workspace_bytes(8, ctypes.byref(L))
+    assert need > 0
+    assert lib.vq3_linear_forward(0x40000, 8, ctypes.byref(L), 0x50000, 0x60000, need - 1, None) == -5
+    assert "workspace" in lib.vq3_last_error().decode()
+
+
+def test_mlp_descriptor_checks():
+    lib = vq3.lib
+    g = fake_linear(256, 512, 256)
+    u = fake_linear(256, 512, 256)
+    d = fake_linear(512, 256, 256)
+    ok = vq3.vq3_mlp_layer(g, u, d)
+    assert lib.vq3_mlp_forward(0x40000, 0, ctypes.byref(ok), 0x50000, 0x60000, 1 << 24, None) == 0
+    bad_down = vq3.vq3_mlp_layer(g, u, fake_linear(512, 128, 256))
+    assert lib.vq3_mlp_forward(0x40000, 8, ctypes.byref(bad_down), 0x50000, 0x60000, 1 << 24, None) == -1
+    bad_signs = vq3.vq3_mlp_layer(g, fake_linear(256, 512, 256, signs=0x70000), d)
+    assert lib.vq3_mlp_forward(0x40000, 8, ctypes.byref(bad_signs), 0x50000, 0x60000, 1 << 24, None) == -1
+    assert lib.vq3_mlp_workspace_bytes(8, ctypes.byref(ok)) > 0
+    assert lib.vq3_mlp_host_workspace_bytes(8, ctypes.byref(ok)) > lib.vq3_mlp_workspace_bytes(8, ctypes.byref(ok))
+
+
+def test_fwht_argument_checks():
+    lib = vq3.lib
+    assert lib.fwht_rotate(0x40000, 0, 1024, 1024, None, 0x50000, None) == 0
+    assert lib.fwht_rotate(0x40000, 2, 1000, 1024, None, 0x50000, None) == -1
+    assert lib.fwht_rotate(0x40000, 2, 2048, 2048, None, 0x50000, None) == -1
+    assert lib.fwht_rotate(0x40002, 2, 1024, 1024, None, 0x50000, None) == -2
+    assert lib.vq3_residual_rmsnorm(0x40000, None, 0, 64, 1e-6, 0x50000, None) == 0
+    assert lib.vq3_residual_rmsnorm(0x40000, None, 2, 64, -1.0, 0x50000, None) == -1
