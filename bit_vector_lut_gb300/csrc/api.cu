@@ -151,6 +151,33 @@ uint32_t read_bits6(const uint8_t* s, size_t k) {
 }
 
 }  // namespace
+
+int mlp_validate(const uint16_t* x, int rows, const vq3_mlp_layer* layer, const uint16_t* out) {
+  int rc = check_mlp(layer);
+  if (rc) return rc;
+  if (rows < 0) return fail(VQ3_EINVAL, "mlp: rows=%d", rows);
+  if (rows == 0) return VQ3_OK;
+  if (!x || !out) return fail(VQ3_EINVAL, "mlp: null x/out");
+  if (!aligned(x, 16) || !aligned(out, 16)) return fail(VQ3_EALIGN, "mlp: x/out must be 16-byte aligned");
+  return VQ3_OK;
+}
+
+int set_error(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+void mlp_counter_range(int rows, const vq3_mlp_layer* layer, size_t* offset, size_t* bytes) {
+  const MlpWs w = mlp_ws(rows, layer);
+  *offset = w.counters;
+  *bytes = w.total - w.counters;
+}
+
 }  // namespace vq3
 
 using namespace vq3;

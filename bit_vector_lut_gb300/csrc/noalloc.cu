@@ -1,0 +1,73 @@
+// vq3_mlp_forward_noalloc: the MLP block with its scratch in a fixed device array.
+//
+// Some callers cannot call cudaMalloc: a plugin running inside a host framework
+// that owns every device allocation, a serving process that reserved its whole
+// memory budget up front, or code that must not allocate while another thread
+// captures a CUDA graph. For them this entry point takes the scratch that
+// vq3_mlp_forward reads from a caller workspace out of the file-scope array
+// below instead. The array is part of the library's device image: every GPU
+// that loads this module holds it until the process exits.
+#include <mutex>
+
+#include "vq3_internal.h"
+
+namespace vq3 {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)VQ3_NOALLOC_SCRATCH_BYTES;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device. In host code the
+// array's name is only a host-side stand-in, so the address comes from
+// cudaGetSymbolAddress, once per device, with that device current.
+cudaError_t scratch_address(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace vq3
+
+using namespace vq3;
+
+extern "C" int vq3_mlp_forward_noalloc(const uint16_t* x, int rows, const vq3_mlp_layer* layer, uint16_t* out,
+                                       void* stream) {
+  int rc = mlp_validate(x, rows, layer, out);
+  if (rc) return rc;
+  if (rows == 0) return set_error(VQ3_OK, "");
+  const size_t need = vq3_mlp_workspace_bytes(rows, layer);
+  if (need > kNoAllocScratchBytes)
+    return set_error(VQ3_ENOSPACE,
+                     "mlp_noalloc: %d rows of a %d/%d block need %zu bytes of scratch, more than the fixed "
+                     "%zu-byte array (VQ3_NOALLOC_SCRATCH_BYTES); use vq3_mlp_forward with a workspace",
+                     rows, layer->gate.d_in, layer->gate.d_out, need, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  cudaError_t e = scratch_address(&scratch);
+  if (e != cudaSuccess)
+    return set_error(VQ3_ECUDA, "mlp_noalloc: cudaGetSymbolAddress: %s (%s)", cudaGetErrorName(e),
+                     cudaGetErrorString(e));
+  // The array keeps the previous call's contents; the arrival counters must start at zero.
+  size_t off = 0, bytes = 0;
+  mlp_counter_range(rows, layer, &off, &bytes);
+  e = cudaMemsetAsync(static_cast<char*>(scratch) + off, 0, bytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess)
+    return set_error(VQ3_ECUDA, "mlp_noalloc: clearing counters: %s (%s)", cudaGetErrorName(e),
+                     cudaGetErrorString(e));
+  return vq3_mlp_forward(x, rows, layer, out, scratch, kNoAllocScratchBytes, stream);
+}

@@ -101,4 +101,13 @@ cudaError_t launch_residual_rmsnorm(uint16_t* resid, const uint16_t* delta, int 
                                     float eps, uint16_t* normed, cudaStream_t st);
 cudaError_t launch_dequant(const vq3_linear& L, int apply_scale, uint16_t* w_out, cudaStream_t st);
 
+// Byte range of the arrival counters inside an MLP workspace laid out for `rows`.
+void mlp_counter_range(int rows, const vq3_mlp_layer* layer, size_t* offset, size_t* bytes);
+
+// Checks the arguments of an MLP call except the workspace (status as the entry points).
+int mlp_validate(const uint16_t* x, int rows, const vq3_mlp_layer* layer, const uint16_t* out);
+
+// Records the thread-local error message and returns `code`.
+int set_error(int code, const char* fmt, ...);
+
 }  // namespace vq3

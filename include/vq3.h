@@ -182,6 +182,32 @@ VQ3_API int vq3_mlp_forward_host(const uint16_t* x_host, int rows, const vq3_mlp
                          uint16_t* out_host, void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * vq3_mlp_forward for callers that cannot allocate device memory. The source
+ * pages have no counterpart: this is an interface convenience of this library.
+ *
+ * Some callers cannot call cudaMalloc at all, e.g. a plugin inside a host
+ * framework that owns every device allocation, or a server that reserved its
+ * whole memory budget before it started. This entry point takes no workspace:
+ * its scratch is a fixed array of VQ3_NOALLOC_SCRATCH_BYTES (32 MiB) compiled
+ * into the library, which every GPU that loads the library holds until the
+ * process exits. It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - Size limit: rows and the layer's widths must fit the array, i.e.
+ *     vq3_mlp_workspace_bytes(rows, layer) <= VQ3_NOALLOC_SCRATCH_BYTES (at
+ *     hidden 5120 / intermediate 17408 that is up to 250 rows); larger calls
+ *     return VQ3_ENOSPACE and launch nothing.
+ *   - The first call on a device looks up the array's device address (with that
+ *     device current) and caches it; make that first call before any stream
+ *     capture on the device.
+ *   - Every call on a device shares the one array and it keeps the previous
+ *     call's contents (the call clears the parts that must start at zero), so
+ *     calls that overlap on the GPU race: order them on one stream or with events.
+ * Arguments, output and errors otherwise as vq3_mlp_forward.
+ */
+#define VQ3_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+VQ3_API int vq3_mlp_forward_noalloc(const uint16_t* x, int rows, const vq3_mlp_layer* layer, uint16_t* out,
+                                    void* stream);
+
+/*
  * Pre-norm residual step between stacked layers:
  *   resid  <- fp16(resid + delta)                       (skipped if delta == NULL)
  *   normed <- fp16(resid / sqrt(mean(resid^2) + eps))    (unit weight, FP32 math)

@@ -1,0 +1,63 @@
+"""vq3_mlp_forward_noalloc against vq3_mlp_forward, through the C ABI.
+
+The no-alloc entry point exists for callers that cannot call cudaMalloc (a
+plugin inside a framework that owns all device memory, a server that reserved
+its memory budget up front): it runs the same MLP block with its scratch in a
+fixed array inside the library instead of a caller workspace. This file runs
+last so that a failure here comes after every other test has run.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from synth import inputs as S  # noqa: E402
+from tests.parity import assert_parity  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need CUDA")
+    from bit_vector_lut_gb300 import vq3
+    f = vq3.lib.vq3_mlp_forward_noalloc
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(vq3.vq3_mlp_layer), ctypes.c_void_p,
+                  ctypes.c_void_p]
+    return vq3, f
+
+
+def test_noalloc_matches_workspace_entry_point_twice():
+    vq3, noalloc = _lib()
+    dev = torch.device("cuda:0")
+    wl = S.mlp_27b(seed=1, rows=8)
+    layer = vq3.MLP.from_block(wl.layers[0], dev)
+    x = torch.from_numpy(wl.x).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    ref = vq3.mlp_forward(x, layer, stream=stream).cpu().numpy()
+    for call in range(2):
+        out = torch.full_like(x, float("nan"))
+        rc = noalloc(x.data_ptr(), x.shape[0], ctypes.byref(layer.struct), out.data_ptr(), stream.cuda_stream)
+        assert rc == 0, vq3.lib.vq3_last_error().decode()
+        torch.cuda.synchronize(dev)
+        assert_parity(out.cpu().numpy(), ref, f"no-alloc call {call}")
+
+
+def test_noalloc_rejects_sizes_beyond_the_fixed_scratch():
+    vq3, noalloc = _lib()
+    dev = torch.device("cuda:0")
+    wl = S.mlp_27b(seed=1, rows=1)
+    layer = vq3.MLP.from_block(wl.layers[0], dev)
+    rows = 251  # 250 rows of a 5120/17408 block fill the 32 MiB array
+    x = torch.zeros((rows, S.HIDDEN), dtype=torch.float16, device=dev)
+    out = torch.zeros_like(x)
+    rc = noalloc(x.data_ptr(), rows, ctypes.byref(layer.struct), out.data_ptr(),
+                 torch.cuda.current_stream(dev).cuda_stream)
+    assert rc == -5
+    assert "VQ3_NOALLOC_SCRATCH_BYTES" in vq3.lib.vq3_last_error().decode()
+    torch.cuda.synchronize(dev)
+    assert not out.any()
