@@ -41,7 +41,8 @@ int check_linear(const vq3_linear* L, const char* name) {
   if (!L) return fail(VQ3_EINVAL, "%s: null descriptor", name);
   if (L->d_in <= 0 || L->d_out <= 0) return fail(VQ3_EINVAL, "%s: d_in=%d d_out=%d must be positive", name, L->d_in, L->d_out);
   if (!layout_supported(L->d_in, L->d_out))
-    return fail(VQ3_EUNSUPPORTED, "%s: d_in=%d and d_out=%d must be multiples of 64", name, L->d_in, L->d_out);
+    return fail(VQ3_EUNSUPPORTED, "%s: d_in=%d must be a multiple of 64 and d_out=%d a multiple of 256", name, L->d_in,
+                L->d_out);
   if (!pow2_block(L->block)) return fail(VQ3_EINVAL, "%s: block=%d must be a power of two in [2, 1024]", name, L->block);
   if (L->d_in % L->block) return fail(VQ3_EINVAL, "%s: d_in=%d is not a multiple of block=%d", name, L->d_in, L->block);
   if (!L->packed || !L->codebook || !L->scales) return fail(VQ3_EINVAL, "%s: null packed/codebook/scales", name);
@@ -52,20 +53,38 @@ int check_linear(const vq3_linear* L, const char* name) {
 }
 
 // ---- workspace carving ----------------------------------------------------
+//
+// [status word (256 B)][rotated input, fragment order][h' fragment order (MLP
+// only)][split-K pieces][counter words, kept zero]
+
+// Row tiles of a fragment-order buffer for `rows` rows: whole passes.
+int frag_tiles(int rows) {
+  const int per = dec_tiles_per_pass(rows);
+  const int tiles = row_tiles(rows);
+  return (tiles + per - 1) / per * per;
+}
+
+size_t frag_bytes(int rows, int n) { return (size_t)frag_tiles(rows) * (n / 64) * 1024; }
+
+size_t pieces_bytes(int rows, int d_in, int d_out, int n_mats) {
+  const int grid = dec_grid(d_in, d_out, n_mats);
+  const size_t piece = (size_t)512 * dec_tiles_per_pass(rows) * sizeof(float);
+  return (size_t)(d_out / kSuChannels) * n_mats * dec_max_pieces(d_in, d_out, n_mats, grid) * piece;
+}
 
 struct LinearWs {
-  size_t xr, partial, counters, total;
+  size_t status, xf, pieces, counters, total;
 };
 
 LinearWs linear_ws(int rows, int d_in, int d_out) {
   LinearWs w{};
-  const int kc = pick_kc_len(d_in);
-  const int n_kc = kc ? d_in / kc : 0;
   size_t off = 0;
-  w.xr = off;
-  off = round_up(off + (size_t)rows * d_in * 2, 256);
-  w.partial = off;
-  off = round_up(off + (size_t)n_kc * kMaxPassRows * d_out * sizeof(float), 256);
+  w.status = off;
+  off += 256;
+  w.xf = off;
+  off = round_up(off + frag_bytes(rows, d_in), 256);
+  w.pieces = off;
+  off = round_up(off + pieces_bytes(rows, d_in, d_out, 1), 256);
   w.counters = off;
   off = round_up(off + (size_t)(d_out / kSuChannels) * sizeof(unsigned), 256);
   w.total = off;
@@ -73,22 +92,23 @@ LinearWs linear_ws(int rows, int d_in, int d_out) {
 }
 
 struct MlpWs {
-  size_t xr, h, partial, counters, total;
+  size_t status, xf, hf, pieces, counters, total;
 };
 
 MlpWs mlp_ws(int rows, const vq3_mlp_layer* l) {
   MlpWs w{};
   const int H = l->gate.d_in, I = l->gate.d_out;
-  const int n_kc_gu = H / pick_kc_len(H), n_kc_dn = I / pick_kc_len(I);
-  const size_t part_gu = (size_t)n_kc_gu * 2 * kMaxPassRows * I;
-  const size_t part_dn = (size_t)n_kc_dn * kMaxPassRows * H;
+  const size_t p_gu = pieces_bytes(rows, H, I, 2);
+  const size_t p_dn = pieces_bytes(rows, I, H, 1);
   size_t off = 0;
-  w.xr = off;
-  off = round_up(off + (size_t)rows * H * 2, 256);
-  w.h = off;
-  off = round_up(off + (size_t)rows * I * 2, 256);
-  w.partial = off;
-  off = round_up(off + (part_gu > part_dn ? part_gu : part_dn) * sizeof(float), 256);
+  w.status = off;
+  off += 256;
+  w.xf = off;
+  off = round_up(off + frag_bytes(rows, H), 256);
+  w.hf = off;
+  off = round_up(off + frag_bytes(rows, I), 256);
+  w.pieces = off;
+  off = round_up(off + (p_gu > p_dn ? p_gu : p_dn), 256);
   w.counters = off;
   const int groups = (I > H ? I : H) / kSuChannels;
   off = round_up(off + (size_t)groups * sizeof(unsigned), 256);
@@ -111,32 +131,112 @@ int check_mlp(const vq3_mlp_layer* l) {
   return VQ3_OK;
 }
 
-GemvMat gemv_mat(const vq3_linear& L) {
-  GemvMat m;
+DecMat dec_mat(const vq3_linear& L) {
+  DecMat m;
   m.packed = static_cast<const uint4*>(L.packed);
   m.codebook = reinterpret_cast<const uint32_t*>(L.codebook);
   m.scales = L.scales;
   return m;
 }
 
-// One matrix (or gate+up) over all rows, in passes of at most kMaxPassRows rows.
-cudaError_t run_gemv(const uint16_t* xr, int rows, int d_in, int d_out, int n_mats, const vq3_linear* mats,
-                     float* partial, unsigned* counters, int mode, uint16_t* out, cudaStream_t st) {
-  GemvArgs a{};
+DecArgs decode_args(const uint32_t* xf, int tiles, int d_in, int d_out, int n_mats, const vq3_linear* mats,
+                    float* pieces, int* status) {
+  DecArgs a{};
+  a.xfrag = xf;
+  a.n_tiles = tiles;
   a.d_in = d_in;
   a.d_out = d_out;
-  a.kc_len = pick_kc_len(d_in);
   a.n_mats = n_mats;
-  for (int i = 0; i < n_mats; ++i) a.mats[i] = gemv_mat(mats[i]);
-  a.partial = partial;
-  a.counters = counters;
-  a.mode = mode;
-  for (int r0 = 0; r0 < rows; r0 += kMaxPassRows) {
-    a.rows = rows - r0 < kMaxPassRows ? rows - r0 : kMaxPassRows;
-    a.xr = xr + (size_t)r0 * d_in;
-    a.out = out + (size_t)r0 * d_out;
-    cudaError_t e = launch_gemv(a, st);
+  for (int i = 0; i < n_mats; ++i) a.mats[i] = dec_mat(mats[i]);
+  a.pieces = pieces;
+  a.grid = dec_grid(d_in, d_out, n_mats);
+  a.max_pieces = dec_max_pieces(d_in, d_out, n_mats, a.grid);
+  a.status = status;
+  return a;
+}
+
+PieceMap piece_map(const DecArgs& d, int nt) {
+  PieceMap pm{};
+  pm.pieces = d.pieces;
+  pm.n_kg = d.d_in / kSuInputs;
+  pm.n_mats = d.n_mats;
+  pm.n_segments = (d.d_out / kSuChannels) * d.n_mats;
+  pm.grid = d.grid;
+  pm.max_pieces = d.max_pieces;
+  pm.nt = nt;
+  return pm;
+}
+
+// out = fp16(scale * W (R in)) for one matrix, all rows: rotate into fragment
+// order, then per pass of 8/16/32 rows a decode and a combine.
+cudaError_t run_linear(const uint16_t* in, int rows, const vq3_linear& L, uint32_t* xf, float* pieces, int* status,
+                       uint16_t* out, cudaStream_t st) {
+  const int tiles = frag_tiles(rows);
+  cudaError_t e = launch_fwht_frag(in, rows, L.d_in, L.block, L.signs, xf, tiles, st);
+  if (e != cudaSuccess) return e;
+  DecArgs d = decode_args(xf, tiles, L.d_in, L.d_out, 1, &L, pieces, status);
+  const int per = dec_tiles_per_pass(rows);
+  for (int nt0 = 0; nt0 < tiles; nt0 += per) {
+    d.nt0 = nt0;
+    if ((e = launch_decode(d, per, st)) != cudaSuccess) return e;
+    LinearOutArgs o{};
+    o.pm = piece_map(d, per);
+    o.scales = L.scales;
+    o.d_out = L.d_out;
+    o.row0 = nt0 * 8;
+    o.rows = rows - o.row0 < per * 8 ? rows - o.row0 : per * 8;
+    o.out = out;
+    if ((e = launch_linear_out(o, st)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// h' = R_d(silu(W_g R_g x) * (W_u R_g x)) in fragment order, all rows.
+cudaError_t run_gate_up(const uint16_t* x, int rows, const vq3_mlp_layer& l, uint32_t* xf, uint32_t* hf,
+                        float* pieces, int* status, cudaStream_t st) {
+  const int tiles = frag_tiles(rows);
+  cudaError_t e = launch_fwht_frag(x, rows, l.gate.d_in, l.gate.block, l.gate.signs, xf, tiles, st);
+  if (e != cudaSuccess) return e;
+  const vq3_linear gu[2] = {l.gate, l.up};
+  DecArgs d = decode_args(xf, tiles, l.gate.d_in, l.gate.d_out, 2, gu, pieces, status);
+  const int per = dec_tiles_per_pass(rows);
+  for (int nt0 = 0; nt0 < tiles; nt0 += per) {
+    d.nt0 = nt0;
+    if ((e = launch_decode(d, per, st)) != cudaSuccess) return e;
+    SwigluRotateArgs c{};
+    c.pm = piece_map(d, per);
+    c.scale_gate = l.gate.scales;
+    c.scale_up = l.up.scales;
+    c.d_inter = l.gate.d_out;
+    c.row0 = nt0 * 8;
+    c.rows = rows - c.row0 < per * 8 ? rows - c.row0 : per * 8;
+    c.block = l.down.block;
+    c.signs = l.down.signs;
+    c.hfrag = hf;
+    c.n_tiles = tiles;
+    if ((e = launch_swiglu_rotate(c, st)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// out = fp16(s_d * W_d h') for all rows, h' in fragment order.
+cudaError_t run_down(const uint32_t* hf, int rows, const vq3_mlp_layer& l, float* pieces, int* status, uint16_t* out,
+                     cudaStream_t st) {
+  const int tiles = frag_tiles(rows);
+  DecArgs d = decode_args(hf, tiles, l.down.d_in, l.down.d_out, 1, &l.down, pieces, status);
+  const int per = dec_tiles_per_pass(rows);
+  for (int nt0 = 0; nt0 < tiles; nt0 += per) {
+    d.nt0 = nt0;
+    cudaError_t e = launch_decode(d, per, st);
     if (e != cudaSuccess) return e;
+    LinearOutArgs o{};
+    o.pm = piece_map(d, per);
+    o.scales = l.down.scales;
+    o.d_out = l.down.d_out;
+    o.row0 = nt0 * 8;
+    o.rows = rows - o.row0 < per * 8 ? rows - o.row0 : per * 8;
+    o.out = out;
+    if ((e = launch_linear_out(o, st)) != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
@@ -172,6 +272,24 @@ int set_error(int code, const char* fmt, ...) {
   return code;
 }
 
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 152;  // no device visible: size for a GB300
+  }
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = 152;
+    }
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
 void mlp_counter_range(int rows, const vq3_mlp_layer* layer, size_t* offset, size_t* bytes) {
   const MlpWs w = mlp_ws(rows, layer);
   *offset = w.counters;
@@ -186,7 +304,7 @@ extern "C" {
 
 const char* vq3_last_error(void) { return g_err.c_str(); }
 
-const char* vq3_version(void) { return "vq3-gb300 0.1 (sm_103a; layout su64x64-m16n8k16)"; }
+const char* vq3_version(void) { return "vq3-gb300 0.2 (sm_103a; layout su64x64-m16n8k16)"; }
 
 size_t vq3_packed_bytes(int d_in, int d_out) {
   if (!layout_supported(d_in, d_out)) return 0;
@@ -196,7 +314,7 @@ size_t vq3_packed_bytes(int d_in, int d_out) {
 int vq3_pack_layout(const uint8_t* canonical, int d_in, int d_out, void* dst_host) {
   if (!canonical || !dst_host) return fail(VQ3_EINVAL, "pack_layout: null pointer");
   if (!layout_supported(d_in, d_out))
-    return fail(VQ3_EUNSUPPORTED, "pack_layout: d_in=%d, d_out=%d must be positive multiples of 64", d_in, d_out);
+    return fail(VQ3_EUNSUPPORTED, "pack_layout: d_in=%d and d_out=%d must be positive multiples of 64", d_in, d_out);
   uint8_t* dst = static_cast<uint8_t*>(dst_host);
   const int n_mg = d_out / kSuChannels, n_kg = d_in / kSuInputs;
   for (int mg = 0; mg < n_mg; ++mg) {
@@ -225,7 +343,7 @@ int vq3_pack_layout(const uint8_t* canonical, int d_in, int d_out, void* dst_hos
 int vq3_unpack_layout(const void* packed_host, int d_in, int d_out, uint8_t* canonical) {
   if (!canonical || !packed_host) return fail(VQ3_EINVAL, "unpack_layout: null pointer");
   if (!layout_supported(d_in, d_out))
-    return fail(VQ3_EUNSUPPORTED, "unpack_layout: d_in=%d, d_out=%d must be positive multiples of 64", d_in, d_out);
+    return fail(VQ3_EUNSUPPORTED, "unpack_layout: d_in=%d and d_out=%d must be positive multiples of 64", d_in, d_out);
   const uint8_t* src = static_cast<const uint8_t*>(packed_host);
   const size_t count = (size_t)(d_out / 2) * d_in;
   const size_t nbytes = (6 * count + 7) / 8;
@@ -287,6 +405,15 @@ int vq3_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
   return ok();
 }
 
+int vq3_workspace_status(const void* workspace, int* status_host, void* stream) {
+  if (!workspace || !status_host) return fail(VQ3_EINVAL, "workspace_status: null pointer");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(status_host, workspace, sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace_status copy");
+  return ok();
+}
+
 int vq3_linear_forward(const uint16_t* x, int rows, const vq3_linear* L, uint16_t* out, void* workspace,
                        size_t ws_bytes, void* stream) {
   int rc = check_linear(L, "linear");
@@ -300,12 +427,9 @@ int vq3_linear_forward(const uint16_t* x, int rows, const vq3_linear* L, uint16_
   if (ws_bytes < w.total) return fail(VQ3_ENOSPACE, "linear: workspace %zu < %zu bytes", ws_bytes, w.total);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
-  uint16_t* xr = reinterpret_cast<uint16_t*>(ws + w.xr);
-  cudaError_t e = launch_fwht(x, rows, L->d_in, L->block, L->signs, xr, st);
-  if (e != cudaSuccess) return cuda_fail(e, "linear: rotate launch");
-  e = run_gemv(xr, rows, L->d_in, L->d_out, 1, L, reinterpret_cast<float*>(ws + w.partial),
-               reinterpret_cast<unsigned*>(ws + w.counters), kModeLinear, out, st);
-  if (e != cudaSuccess) return cuda_fail(e, "linear: gemv launch");
+  cudaError_t e = run_linear(x, rows, *L, reinterpret_cast<uint32_t*>(ws + w.xf),
+                             reinterpret_cast<float*>(ws + w.pieces), reinterpret_cast<int*>(ws + w.status), out, st);
+  if (e != cudaSuccess) return cuda_fail(e, "linear: launch");
   return ok();
 }
 
@@ -347,25 +471,17 @@ MlpCall mlp_prepare(int rows, const vq3_mlp_layer* layer, void* workspace, size_
 }
 
 int gate_up_half(const uint16_t* x, int rows, const vq3_mlp_layer* layer, const MlpCall& c) {
-  const int H = layer->gate.d_in, I = layer->gate.d_out;
-  uint16_t* xr = reinterpret_cast<uint16_t*>(c.ws + c.w.xr);
-  uint16_t* h = reinterpret_cast<uint16_t*>(c.ws + c.w.h);
-  cudaError_t e = launch_fwht(x, rows, H, layer->gate.block, layer->gate.signs, xr, c.st);
-  if (e != cudaSuccess) return cuda_fail(e, "mlp: rotate x launch");
-  const vq3_linear gu[2] = {layer->gate, layer->up};
-  e = run_gemv(xr, rows, H, I, 2, gu, reinterpret_cast<float*>(c.ws + c.w.partial),
-               reinterpret_cast<unsigned*>(c.ws + c.w.counters), kModeSwiglu, h, c.st);
+  cudaError_t e = run_gate_up(x, rows, *layer, reinterpret_cast<uint32_t*>(c.ws + c.w.xf),
+                              reinterpret_cast<uint32_t*>(c.ws + c.w.hf), reinterpret_cast<float*>(c.ws + c.w.pieces),
+                              reinterpret_cast<int*>(c.ws + c.w.status), c.st);
   if (e != cudaSuccess) return cuda_fail(e, "mlp: gate/up launch");
   return VQ3_OK;
 }
 
 int down_half(int rows, const vq3_mlp_layer* layer, uint16_t* out, const MlpCall& c) {
-  const int H = layer->gate.d_in, I = layer->gate.d_out;
-  uint16_t* h = reinterpret_cast<uint16_t*>(c.ws + c.w.h);
-  cudaError_t e = launch_fwht(h, rows, I, layer->down.block, layer->down.signs, h, c.st);
-  if (e != cudaSuccess) return cuda_fail(e, "mlp: rotate h launch");
-  e = run_gemv(h, rows, I, H, 1, &layer->down, reinterpret_cast<float*>(c.ws + c.w.partial),
-               reinterpret_cast<unsigned*>(c.ws + c.w.counters), kModeLinear, out, c.st);
+  cudaError_t e = run_down(reinterpret_cast<const uint32_t*>(c.ws + c.w.hf), rows, *layer,
+                           reinterpret_cast<float*>(c.ws + c.w.pieces), reinterpret_cast<int*>(c.ws + c.w.status), out,
+                           c.st);
   if (e != cudaSuccess) return cuda_fail(e, "mlp: down launch");
   return VQ3_OK;
 }
@@ -408,8 +524,8 @@ int vq3_mlp_down(int rows, const vq3_mlp_layer* layer, uint16_t* out, void* work
 int vq3_mlp_kernel_launches(int rows, const vq3_mlp_layer* layer) {
   if (check_mlp(layer) || rows < 0) return -1;
   if (rows == 0) return 0;
-  const int passes = (rows + kMaxPassRows - 1) / kMaxPassRows;
-  return 2 + 2 * passes;  // two rotations, one gate/up and one down launch per row pass
+  const int passes = frag_tiles(rows) / dec_tiles_per_pass(rows);
+  return 1 + 4 * passes;  // rotation of x; per row pass: gate/up decode, SwiGLU+rotation, down decode, output
 }
 
 size_t vq3_mlp_host_workspace_bytes(int rows, const vq3_mlp_layer* layer) {

@@ -35,68 +35,105 @@ inline bool layout_supported(int d_in, int d_out) {
   return d_in > 0 && d_out > 0 && d_in % kSuInputs == 0 && d_out % kSuChannels == 0;
 }
 
-// Position of index (p, i) in the GPU layout: byte offset of its 16-byte word
-// group is not unique (an index may straddle two words), so this returns the
-// lane string coordinates instead.
-struct LanePos {
-  size_t su;  // super-unit number
-  int lane;   // 0..31
-  int n;      // index number inside the lane string, 0..63
-};
-
-inline LanePos lane_pos(int d_in, int p, int i) {
-  const int mg = p / 32, pl = p % 32, m = pl / 8, g = pl % 8;
-  const int kg = i / 64, il = i % 64, s = il / 16, r = il % 16;
-  int t, e;
-  if (r < 8) { t = r / 2; e = r % 2; } else { t = (r - 8) / 2; e = 2 + r % 2; }
-  LanePos lp;
-  lp.su = (size_t)mg * (size_t)(d_in / 64) + (size_t)kg;
-  lp.lane = g * 4 + t;
-  lp.n = (s * 4 + m) * 4 + e;
-  return lp;
-}
-
-// Byte offset inside the matrix of 32-bit word w (0..11) of lane L of SU su.
-inline size_t lane_word_offset(size_t su, int lane, int w) {
+// Byte offset of 32-bit word w (0..11) of lane L's string in SU su.
+__host__ __device__ inline size_t lane_word_offset(size_t su, int lane, int w) {
   return su * kSuBytes + (size_t)((w / 4) * 32 + lane) * 16 + (size_t)(w % 4) * 4;
 }
+
+// ---------------------------------------------------------------------------
+// Rotated activations in "fragment order" (what the decode kernel reads):
+// for each 64-input column group kg and each 8-row tile nt, 256 32-bit words;
+// word v of lane L = 4g + t holds the FP16 pair (x'[8nt+g][kg*64 + 16s + 2t + 8h],
+// x'[8nt+g][... + 1]) with v = 2s + h (s = 0..3, h = 0..1): the B fragments of
+// four m16n8k16 MMAs, 32 contiguous bytes per lane. Rows past the last valid
+// row are zero. Word index: ((kg * n_tiles + nt) * 32 + L) * 8 + v.
+// ---------------------------------------------------------------------------
+__host__ __device__ inline size_t frag_half_index(int row, int col, int n_tiles) {
+  const int kg = col / 64, cl = col % 64, s = cl / 16, r = cl % 16;
+  const int h = r / 8, t = (r % 8) / 2, half = r % 2;
+  const int nt = row / 8, g = row % 8;
+  const int lane = 4 * g + t, v = 2 * s + h;
+  return ((((size_t)kg * n_tiles + nt) * 32 + lane) * 8 + v) * 2 + half;
+}
+
+inline int row_tiles(int rows) { return (rows + 7) / 8; }
 
 // ---------------------------------------------------------------------------
 // kernels (launch wrappers; all return cudaGetLastError() after launch)
 // ---------------------------------------------------------------------------
 
-struct GemvMat {
+enum MatMode { kModeLinear = 0, kModeSwiglu = 1 };
+
+struct DecMat {
   const uint4* packed;
   const uint32_t* codebook;  // [64] FP16x2 words (component 0 in the low half)
   const uint16_t* scales;    // [d_out]
 };
 
-enum GemvMode { kModeLinear = 0, kModeSwiglu = 1 };
-
-struct GemvArgs {
-  const uint16_t* xr;  // rotated input, FP16 [rows][d_in] (row stride d_in)
-  int rows;            // valid rows of this pass (<= 8 * n_tiles)
-  int d_in, d_out;
-  int kc_len;          // inputs per K chunk (multiple of 64, divides d_in)
-  int n_mats;          // 1 (linear) or 2 (gate and up)
-  GemvMat mats[2];
-  float* partial;      // [n_kc][n_mats][kMaxPassRows][d_out]
-  unsigned* counters;  // [d_out / 64], zero on entry, zero on exit
-  int mode;
-  uint16_t* out;       // FP16 [rows][d_out] (row stride d_out)
+// One launch of the decode kernel over row tiles [nt0, nt0 + NT) of the input:
+// writes the per-segment partial sums ("pieces"); a combine kernel finishes.
+struct DecArgs {
+  const uint32_t* xfrag;  // rotated input in fragment order, n_tiles row tiles
+  int n_tiles;            // row tiles of xfrag (all rows)
+  int nt0;                // first row tile of this pass
+  int d_in, d_out;        // per matrix
+  int n_mats;             // 1 (linear) or 2 (gate and up, interleaved segments)
+  DecMat mats[2];
+  float* pieces;          // [n_segments][max_pieces][512 * NT] partial sums
+  int grid, max_pieces;
+  int* status;            // device status word (set to 2 if the lookup tables are misplaced)
 };
 
-constexpr int kMaxPassRows = 32;
+// Where the pieces of a decode launch are and how many CTAs contributed.
+struct PieceMap {
+  const float* pieces;
+  int n_kg;               // 64-input column groups of d_in
+  int n_mats;
+  int n_segments;         // (d_out / 64) * n_mats
+  int grid, max_pieces;
+  int nt;                 // row tiles per piece (NT)
+};
 
-inline int pick_kc_len(int d_in) {
-  for (int c = 1024; c >= 64; c >>= 1)
-    if (d_in % c == 0) return c;
-  return 0;
-}
+// Sums gate and up pieces, h = silu(s_g*g) * (s_u*u), rotates h by the down
+// projection's Hadamard blocks (signs) and writes h' in fragment order.
+struct SwigluRotateArgs {
+  PieceMap pm;
+  const uint16_t* scale_gate;
+  const uint16_t* scale_up;
+  int d_inter;            // intermediate width (gate/up d_out)
+  int rows;               // valid rows of the pass
+  int row0;               // first row of the pass
+  int block;              // down rotation block
+  const uint32_t* signs;  // down signs or null
+  uint32_t* hfrag;        // output, fragment order, n_tiles row tiles
+  int n_tiles;
+};
 
-cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t st);
+// Sums pieces, y = scale * sum, writes FP16 rows [row0, row0 + rows) of out.
+struct LinearOutArgs {
+  PieceMap pm;
+  const uint16_t* scales;
+  int d_out;
+  int rows, row0;
+  uint16_t* out;          // row-major [*][d_out]
+};
+
+cudaError_t launch_swiglu_rotate(const SwigluRotateArgs& a, cudaStream_t st);
+cudaError_t launch_linear_out(const LinearOutArgs& a, cudaStream_t st);
+
+constexpr int kDecWarps = 8;
+constexpr int kDecMaxGrid = 2048;
+
+int device_sm_count();
+int dec_tiles_per_pass(int rows);  // 1, 2 or 4 row tiles (8, 16 or 32 rows)
+int dec_grid(int d_in, int d_out, int n_mats);  // never more CTAs than cells
+int dec_max_pieces(int d_in, int d_out, int n_mats, int grid);
+cudaError_t launch_decode(const DecArgs& a, int nt, cudaStream_t st);
 cudaError_t launch_fwht(const uint16_t* x, int rows, int n, int block, const uint32_t* signs,
                         uint16_t* out, cudaStream_t st);
+// Same rotation, written in fragment order (rows padded with zeros to 8 * n_tiles).
+cudaError_t launch_fwht_frag(const uint16_t* x, int rows, int n, int block, const uint32_t* signs,
+                             uint32_t* xfrag, int n_tiles, cudaStream_t st);
 cudaError_t launch_residual_rmsnorm(uint16_t* resid, const uint16_t* delta, int rows, int n,
                                     float eps, uint16_t* normed, cudaStream_t st);
 cudaError_t launch_dequant(const vq3_linear& L, int apply_scale, uint16_t* w_out, cudaStream_t st);

@@ -49,6 +49,7 @@ def _load() -> ctypes.CDLL:
         "vq3_linear_workspace_bytes": (c_size_t, [c_int, POINTER(vq3_linear)]),
         "vq3_mlp_workspace_bytes": (c_size_t, [c_int, POINTER(vq3_mlp_layer)]),
         "vq3_workspace_init": (c_int, [c_void_p, c_size_t, c_void_p]),
+        "vq3_workspace_status": (c_int, [c_void_p, POINTER(c_int), c_void_p]),
         "vq3_linear_forward": (c_int, [c_void_p, c_int, POINTER(vq3_linear), c_void_p, c_void_p, c_size_t, c_void_p]),
         "vq3_mlp_forward": (c_int, [c_void_p, c_int, POINTER(vq3_mlp_layer), c_void_p, c_void_p, c_size_t, c_void_p]),
         "vq3_mlp_gate_up": (c_int, [c_void_p, c_int, POINTER(vq3_mlp_layer), c_void_p, c_size_t, c_void_p]),
@@ -187,6 +188,13 @@ def workspace(nbytes: int, device="cuda", stream=None) -> torch.Tensor:
     ws = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
     _check(lib.vq3_workspace_init(ws.data_ptr(), ws.numel(), _stream(stream)))
     return ws
+
+
+def workspace_status(ws: torch.Tensor, stream=None) -> int:
+    """0 unless a kernel's bounded wait ran out while using this workspace."""
+    v = c_int(0)
+    _check(lib.vq3_workspace_status(ws.data_ptr(), ctypes.byref(v), _stream(stream)))
+    return int(v.value)
 
 
 # ---------------------------------------------------------------- operations

@@ -126,14 +126,20 @@ VQ3_API int fwht_rotate(const uint16_t* x, int rows, int n, int block, const uin
 
 /*
  * Workspace for vq3_linear_forward / vq3_mlp_forward at `rows` rows. The
- * workspace holds split-K partial sums, the rotated activations and arrival
- * counters. It must be zero-filled once before its first use (vq3_workspace_init);
- * every completed call leaves the counters at zero again. Calls that share a
- * workspace must not overlap on the GPU (same stream, or ordered by events).
+ * workspace holds a device status word, the rotated activations, split-K
+ * partial sums and arrival counters. It must be zero-filled once before its
+ * first use (vq3_workspace_init); every completed call leaves the counters at
+ * zero again. Calls that share a workspace must not overlap on the GPU (same
+ * stream, or ordered by events).
+ * Device status: the first 32-bit word of the workspace stays 0 unless a
+ * kernel found an internal invariant broken (then nonzero; the outputs of that
+ * call are invalid).
+ * vq3_workspace_status copies it to the host after the stream's prior work.
  */
 VQ3_API size_t vq3_linear_workspace_bytes(int rows, const vq3_linear* L);
 VQ3_API size_t vq3_mlp_workspace_bytes(int rows, const vq3_mlp_layer* layer);
 VQ3_API int vq3_workspace_init(void* workspace, size_t ws_bytes, void* stream);
+VQ3_API int vq3_workspace_status(const void* workspace, int* status_host, void* stream);
 
 /*
  * One rotated VQ3 linear layer: out = fp16( W (R x) ), FP32 accumulation.
@@ -193,8 +199,8 @@ VQ3_API int vq3_mlp_forward_host(const uint16_t* x_host, int rows, const vq3_mlp
  * process exits. It calls no cudaMalloc, cudaFree or other allocating routine.
  *   - Size limit: rows and the layer's widths must fit the array, i.e.
  *     vq3_mlp_workspace_bytes(rows, layer) <= VQ3_NOALLOC_SCRATCH_BYTES (at
- *     hidden 5120 / intermediate 17408 that is up to 250 rows); larger calls
- *     return VQ3_ENOSPACE and launch nothing.
+ *     hidden 5120 / intermediate 17408 on a 152-SM GB300 that is up to 293
+ *     rows); larger calls return VQ3_ENOSPACE and launch nothing.
  *   - The first call on a device looks up the array's device address (with that
  *     device current) and caches it; make that first call before any stream
  *     capture on the device.

@@ -33,7 +33,7 @@ def test_version_string():
     assert "sm_103a" in vq3.version()
 
 
-@pytest.mark.parametrize("d_in,d_out", [(64, 64), (256, 256), (128, 192), (5120, 128)])
+@pytest.mark.parametrize("d_in,d_out", [(64, 256), (256, 256), (128, 512), (5120, 256)])
 def test_pack_roundtrip(d_in, d_out):
     s = S.index_stream(S.rng(d_in + d_out), d_in, d_out)
     p = vq3.pack_layout(s, d_in, d_out)
@@ -43,7 +43,7 @@ def test_pack_roundtrip(d_in, d_out):
 
 @pytest.mark.parametrize("pattern", ["zeros", "all63", "ramp", "alternate"])
 def test_pack_edge_patterns(pattern):
-    d_in, d_out = 128, 64
+    d_in, d_out = 128, 256
     n = (d_out // 2) * d_in
     idx = {"zeros": np.zeros(n, int), "all63": np.full(n, 63), "ramp": np.arange(n) % 64,
            "alternate": (np.arange(n) % 2) * 63}[pattern]
@@ -61,11 +61,11 @@ def test_pack_full_size_roundtrip():
     assert np.array_equal(vq3.unpack_layout(p, 5120, 17408), m.stream)
 
 
-def test_layout_places_lane_fragments():
+def test_layout_is_a_permutation_of_index_fields():
     # the GPU layout is a permutation of index positions: a single nonzero index
     # moves to exactly one 6-bit field of the packed buffer
-    d_in, d_out = 64, 64
-    for (p_, i_) in [(0, 0), (5, 9), (31, 63), (17, 40)]:
+    d_in, d_out = 64, 256
+    for (p_, i_) in [(0, 0), (5, 9), (127, 63), (17, 40)]:
         idx = np.zeros((d_out // 2, d_in), int)
         idx[p_, i_] = 0b101101
         pk = vq3.pack_layout(O.pack_indices(idx), d_in, d_out)
@@ -75,7 +75,8 @@ def test_layout_places_lane_fragments():
 
 def test_sizes_and_unsupported_shapes():
     assert vq3.packed_bytes(5120, 17408) == 33_423_360
-    assert vq3.packed_bytes(100, 64) == 0
+    assert vq3.packed_bytes(100, 256) == 0
+    assert vq3.packed_bytes(64, 96) == 0
     with pytest.raises(vq3.Vq3Error) as e:
         vq3.pack_layout(np.zeros(10, np.uint8), 100, 64)
     assert e.value.code == -3
@@ -122,7 +123,7 @@ def test_mlp_descriptor_checks():
     d = fake_linear(512, 256, 256)
     ok = vq3.vq3_mlp_layer(g, u, d)
     assert lib.vq3_mlp_forward(0x40000, 0, ctypes.byref(ok), 0x50000, 0x60000, 1 << 24, None) == 0
-    bad_down = vq3.vq3_mlp_layer(g, u, fake_linear(512, 128, 256))
+    bad_down = vq3.vq3_mlp_layer(g, u, fake_linear(512, 512, 256))
     assert lib.vq3_mlp_forward(0x40000, 8, ctypes.byref(bad_down), 0x50000, 0x60000, 1 << 24, None) == -1
     bad_signs = vq3.vq3_mlp_layer(g, fake_linear(256, 512, 256, signs=0x70000), d)
     assert lib.vq3_mlp_forward(0x40000, 8, ctypes.byref(bad_signs), 0x50000, 0x60000, 1 << 24, None) == -1

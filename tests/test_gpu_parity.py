@@ -76,7 +76,7 @@ def test_fwht_closed_forms(vq3):
 
 # ------------------------------------------------------------------ layout (bit-exact)
 
-@pytest.mark.parametrize("d_in,d_out", [(256, 256), (128, 192), (5120, 17408)])
+@pytest.mark.parametrize("d_in,d_out", [(256, 256), (128, 512), (5120, 17408), (17408, 5120)])
 def test_dequant_bit_exact(vq3, d_in, d_out):
     m = S.matrix(S.rng(d_in + 7), d_in, d_out, 64)
     lin = vq3.Linear.from_matrix(m, DEV)
@@ -111,7 +111,7 @@ def test_linear_ragged_rows(vq3, rows):
 
 
 def test_linear_closed_form_all_equal(vq3):
-    d_in, d_out, b, k = 256, 128, 64, 37
+    d_in, d_out, b, k = 256, 256, 64, 37
     m = S.matrix(S.rng(4), d_in, d_out, b)
     m.stream = O.pack_indices(np.full((d_out // 2) * d_in, k))
     x = S.activations(S.rng(4, 0), 8, d_in)
@@ -157,6 +157,7 @@ def test_mlp_repeat_deterministic_and_counters_reset(vq3, cfg1):
     b = vq3.mlp_forward(x, layer, ws=ws).cpu().numpy()
     assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
     assert_parity(b, ref, "second call")
+    assert vq3.workspace_status(ws) == 0
 
 
 def test_mlp_host_api_equals_device_api(vq3, cfg1):

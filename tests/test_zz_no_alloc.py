@@ -52,7 +52,9 @@ def test_noalloc_rejects_sizes_beyond_the_fixed_scratch():
     dev = torch.device("cuda:0")
     wl = S.mlp_27b(seed=1, rows=1)
     layer = vq3.MLP.from_block(wl.layers[0], dev)
-    rows = 251  # 250 rows of a 5120/17408 block fill the 32 MiB array
+    cap = 32 * 1024 * 1024
+    rows = next(r for r in range(1, 4096)
+                if vq3.lib.vq3_mlp_workspace_bytes(r, ctypes.byref(layer.struct)) > cap)
     x = torch.zeros((rows, S.HIDDEN), dtype=torch.float16, device=dev)
     out = torch.zeros_like(x)
     rc = noalloc(x.data_ptr(), rows, ctypes.byref(layer.struct), out.data_ptr(),
