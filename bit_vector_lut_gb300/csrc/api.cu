@@ -151,6 +151,7 @@ DecArgs decode_args(const uint32_t* xf, int tiles, int d_in, int d_out, int n_ma
   a.pieces = pieces;
   a.grid = dec_grid(d_in, d_out, n_mats);
   a.max_pieces = dec_max_pieces(d_in, d_out, n_mats, a.grid);
+  a.ksplit = dec_ksplit(d_in, d_out, n_mats);
   a.status = status;
   return a;
 }
@@ -160,7 +161,8 @@ PieceMap piece_map(const DecArgs& d, int nt) {
   pm.pieces = d.pieces;
   pm.n_kg = d.d_in / kSuInputs;
   pm.n_mats = d.n_mats;
-  pm.n_segments = (d.d_out / kSuChannels) * d.n_mats;
+  pm.n_groups = dec_groups(d.d_in, d.d_out, d.n_mats);
+  pm.seg_per_group = kDecWarps / d.ksplit;
   pm.grid = d.grid;
   pm.max_pieces = d.max_pieces;
   pm.nt = nt;

@@ -34,8 +34,8 @@ struct SegPieces {
 };
 
 __device__ __forceinline__ SegPieces seg_pieces(const PieceMap& pm, int sg) {
-  const long long cells = (long long)pm.n_segments * pm.n_kg;
-  const long long x0 = (long long)sg * pm.n_kg;
+  const long long cells = (long long)pm.n_groups * pm.n_kg;
+  const long long x0 = (long long)(sg / pm.seg_per_group) * pm.n_kg;
   const int b0 = cta_of(x0, cells, pm.grid), b1 = cta_of(x0 + pm.n_kg - 1, cells, pm.grid);
   SegPieces sp;
   sp.base = pm.pieces + (size_t)sg * pm.max_pieces * 512 * pm.nt;
@@ -43,19 +43,19 @@ __device__ __forceinline__ SegPieces seg_pieces(const PieceMap& pm, int sg) {
   return sp;
 }
 
-constexpr int kMaxFast = 8;  // pieces per segment loaded in one batch
-
-// Loads of item `it` over a segment's pieces: all issued before any is used
-// (up to kMaxFast at a time), then summed in K order.
+// Sum of item `it` over a segment's pieces, in K order. The loads of a batch
+// of up to P pieces are all issued before the first add, so a batch costs one
+// round trip to L2.
+template <int P>
 __device__ __forceinline__ float sum_seg(const SegPieces& sp, int it, int piece_floats) {
   float s = 0.f;
   const float* p = sp.base + it;
-  for (int q0 = 0; q0 < sp.count; q0 += kMaxFast) {
-    float v[kMaxFast];
+  for (int q0 = 0; q0 < sp.count; q0 += P) {
+    float v[P];
 #pragma unroll
-    for (int q = 0; q < kMaxFast; ++q) v[q] = (q0 + q < sp.count) ? __ldcg(p + (size_t)(q0 + q) * piece_floats) : 0.f;
+    for (int q = 0; q < P; ++q) v[q] = (q0 + q < sp.count) ? __ldcg(p + (size_t)(q0 + q) * piece_floats) : 0.f;
 #pragma unroll
-    for (int q = 0; q < kMaxFast; ++q) s += v[q];
+    for (int q = 0; q < P; ++q) s += v[q];
   }
   return s;
 }
@@ -86,16 +86,40 @@ __global__ void __launch_bounds__(kCThreads) swiglu_rotate_kernel(SwigluRotateAr
 
   const bool live = r < a.rows;
   constexpr int PER = SPAN / kCThreads > 0 ? SPAN / kCThreads : 1;
+  constexpr int P = 8;  // pieces per batch
   float gs[PER], us[PER];
 #pragma unroll
-  for (int k = 0; k < PER; ++k) {
-    const int c = tid + k * kCThreads;
-    gs[k] = us[k] = 0.f;
-    if (live && c < SPAN) {
-      const int q = c >> 6;
-      const int it = item_of(r, c & 63, a.pm.nt);
-      gs[k] = sum_seg(segs[2 * q], it, piece_floats);
-      us[k] = sum_seg(segs[2 * q + 1], it, piece_floats);
+  for (int k = 0; k < PER; ++k) gs[k] = us[k] = 0.f;
+  if (live) {
+    // one batch: PER channels x 2 matrices x P pieces, all loads in flight together
+    int pmax = 0;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int c = tid + k * kCThreads;
+      if (c < SPAN) pmax = max(pmax, max(segs[2 * (c >> 6)].count, segs[2 * (c >> 6) + 1].count));
+    }
+    for (int q0 = 0; q0 < pmax; q0 += P) {
+      float vg[PER][P], vu[PER][P];
+#pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        const int c = tid + k * kCThreads;
+        const int q = (c < SPAN) ? (c >> 6) : 0;
+        const int it = item_of(r, c & 63, a.pm.nt);
+        const SegPieces& sgp = segs[2 * q];
+        const SegPieces& sup = segs[2 * q + 1];
+#pragma unroll
+        for (int j = 0; j < P; ++j) {
+          vg[k][j] = (c < SPAN && q0 + j < sgp.count) ? __ldcg(sgp.base + it + (size_t)(q0 + j) * piece_floats) : 0.f;
+          vu[k][j] = (c < SPAN && q0 + j < sup.count) ? __ldcg(sup.base + it + (size_t)(q0 + j) * piece_floats) : 0.f;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < PER; ++k)
+#pragma unroll
+        for (int j = 0; j < P; ++j) {
+          gs[k] += vg[k][j];
+          us[k] += vu[k][j];
+        }
     }
   }
 #pragma unroll
@@ -130,21 +154,23 @@ __global__ void __launch_bounds__(kCThreads) swiglu_rotate_kernel(SwigluRotateAr
     out[frag_half_index(row, span0 + c, a.n_tiles)] = __half_as_ushort(__float2half_rn(hb[c] * scale));
 }
 
-// One CTA: one 64-channel group x one row tile.
-__global__ void __launch_bounds__(128) linear_out_kernel(LinearOutArgs a) {
+// One CTA: 256 items of one segment's pieces (one thread per item).
+__global__ void __launch_bounds__(256) linear_out_kernel(LinearOutArgs a) {
   __shared__ SegPieces seg;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
-  const int grp = blockIdx.x, tile = blockIdx.y;
-  if (threadIdx.x == 0) seg = seg_pieces(a.pm, grp);
+  const int sg = blockIdx.x;
+  const int it = blockIdx.y * 256 + threadIdx.x;  // item of the piece
+  if (threadIdx.x == 0) seg = seg_pieces(a.pm, sg);
   __syncthreads();
-  const int piece_floats = 512 * a.pm.nt;
-  for (int e = threadIdx.x; e < 8 * 64; e += 128) {
-    const int r = e >> 6, c = e & 63;
-    const int rp = tile * 8 + r;
-    if (rp >= a.rows) continue;
-    const int ch = grp * 64 + c;
-    const float y = sum_seg(seg, item_of(rp, c, a.pm.nt), piece_floats);
+  const float y = sum_seg<32>(seg, it, 512 * a.pm.nt);
+  // item -> (row of the pass, channel): it = ((m*NT + nt)*4 + j)*32 + L
+  const int L = it & 31, idx = it >> 5;
+  const int j = idx & 3, mnt = idx >> 2, nt = mnt % a.pm.nt, m = mnt / a.pm.nt;
+  const int g = L >> 2, t = L & 3;
+  const int ch = (sg * 32 + 8 * m + g) * 2 + (j >> 1);
+  const int rp = nt * 8 + 2 * t + (j & 1);
+  if (rp < a.rows) {
     const float s = __half2float(__ushort_as_half(a.scales[ch]));
     a.out[(size_t)(a.row0 + rp) * a.d_out + ch] = __half_as_ushort(__float2half_rn(s * y));
   }
@@ -182,7 +208,7 @@ cudaError_t launch_swiglu_rotate(const SwigluRotateArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_linear_out(const LinearOutArgs& a, cudaStream_t st) {
-  return launch_pdl(linear_out_kernel, dim3(a.d_out / 64, a.pm.nt), dim3(128), st, a);
+  return launch_pdl(linear_out_kernel, dim3(a.d_out / 64, 2 * a.pm.nt), dim3(256), st, a);
 }
 
 }  // namespace vq3

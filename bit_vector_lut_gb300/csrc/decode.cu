@@ -85,11 +85,19 @@ __device__ __forceinline__ uint32_t lut(uint32_t saddr) {
 // string and the 32*NT bytes of B fragments) into its warp's slot of a shared-
 // memory ring with cp.async, kSlots cells ahead, and later reads back exactly
 // the bytes it copied, so no other lane is involved.
-template <int NT>
 struct Ring {
-  static constexpr int kSlots = NT == 4 ? 2 : 3;
-  static constexpr int kSlotBytes = 1536 + 1024 * NT;  // per warp
+  static constexpr int kSlots = 3;
+  static constexpr int kSlotBytes = 1536;  // one lane-fragment index string set (a super-unit)
   static constexpr int kWarpBytes = kSlots * kSlotBytes;
+};
+
+// Column groups of activation fragments staged per chunk (NT KB each).
+template <int NT>
+struct Xs {
+  static constexpr int kKg = NT == 1 ? 32 : (NT == 2 ? 16 : 8);
+  static constexpr int kBytes = kKg * NT * 1024;
+  // per-segment reduction buffer when warps split K (at most kDecWarps / 2 segments)
+  static constexpr int kRedBytes = (kDecWarps / 2) * 512 * NT * 4;
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g) {
@@ -107,17 +115,10 @@ __device__ __forceinline__ uint4 lds128(uint32_t saddr) {
   return v;
 }
 
-// slot layout (per warp): [q=0..2][32 lanes][16 B] index words, then
-// [nt][h=0..1][32 lanes][16 B] B fragments
-template <int NT>
-__device__ __forceinline__ void copy_cell(uint32_t slot, int lane, const uint4* su_lane, const uint4* xf_lane) {
+// slot layout (per warp): [q=0..2][32 lanes][16 B] index words
+__device__ __forceinline__ void copy_su(uint32_t slot, int lane, const uint4* su_lane) {
 #pragma unroll
   for (int q = 0; q < 3; ++q) cp_async16(slot + (uint32_t)(q * 512 + lane * 16), su_lane + q * 32);
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-      cp_async16(slot + (uint32_t)(1536 + (nt * 2 + h) * 512 + lane * 16), xf_lane + nt * 64 + h);
 }
 
 template <int S, int M, int NT>
@@ -146,8 +147,11 @@ __device__ __forceinline__ void kstep(const uint32_t (&w)[12], uint32_t lanebase
   mma_step<S, 3, NT>(w, lanebase, acc, b);
 }
 
+// One super-unit: index string from the warp's ring slot, B fragments from the
+// CTA's activation stage (xb = this column group's NT KB, fragment order).
 template <int NT>
-__device__ __forceinline__ void compute_cell(uint32_t slot, int lane, uint32_t lanebase, float (&acc)[4][NT][4]) {
+__device__ __forceinline__ void compute_cell(uint32_t slot, uint32_t xb, int lane, uint32_t lanebase,
+                                             float (&acc)[4][NT][4]) {
   uint32_t w[12];
 #pragma unroll
   for (int q = 0; q < 3; ++q) {
@@ -162,7 +166,7 @@ __device__ __forceinline__ void compute_cell(uint32_t slot, int lane, uint32_t l
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const uint4 v = lds128(slot + (uint32_t)(1536 + (nt * 2 + h) * 512 + lane * 16));
+      const uint4 v = lds128(xb + (uint32_t)((nt * 2 + h) * 512 + lane * 16));
       b[nt][4 * h + 0] = v.x;
       b[nt][4 * h + 1] = v.y;
       b[nt][4 * h + 2] = v.z;
@@ -184,31 +188,37 @@ __device__ __forceinline__ int cta_of(long long x, long long cells, int grid) {
 }
 
 template <int NT>
-__global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) decode_kernel(DecArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecArgs a) {
   constexpr int ITEMS = 16 * NT;      // accumulator values per lane
   constexpr int PIECE = 32 * ITEMS;   // floats per piece
-  // dynamic shared memory: [prefetch rings][pad to 16 KB][2 tables][kDecWarps * PIECE floats]
+  // dynamic shared memory: [index rings][activation stage][reduction][pad to 16 KB][2 tables]
   extern __shared__ __align__(16) unsigned char dsm[];
   const uint32_t dbase = static_cast<uint32_t>(__cvta_generic_to_shared(dsm));
-  constexpr uint32_t kRingBytes = kDecWarps * Ring<NT>::kWarpBytes;
-  const uint32_t tab_off = ((dbase + kRingBytes + kTabAlign - 1) & ~(kTabAlign - 1)) - dbase;
+  constexpr uint32_t kRingBytes = kDecWarps * Ring::kWarpBytes;
+  const uint32_t xs = dbase + kRingBytes;
+  float* red = reinterpret_cast<float*>(dsm + kRingBytes + Xs<NT>::kBytes);
+  const uint32_t tab_off =
+      ((dbase + kRingBytes + Xs<NT>::kBytes + Xs<NT>::kRedBytes + kTabAlign - 1) & ~(kTabAlign - 1)) - dbase;
   uint32_t* tabs = reinterpret_cast<uint32_t*>(dsm + tab_off);
-  float* red = reinterpret_cast<float*>(dsm + tab_off + 2 * kTabWords * 4);
   const uint32_t tbase = dbase + tab_off;
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const uint32_t ring = dbase + (uint32_t)(warp * Ring<NT>::kWarpBytes);
+  const uint32_t ring = dbase + (uint32_t)(warp * Ring::kWarpBytes);
 
+  // Segments (64-channel output group x matrix) form groups of S = kDecWarps/R.
+  // Warp w works on segment w % S of the group and on the column groups kg with
+  // kg % R == w / S; a cell is one group x one 64-input column group.
+  const int R = a.ksplit, S = kDecWarps / R;
+  const int seg_local = warp % S, kphase = warp / S;
   const int n_kg = a.d_in / kSuInputs;
-  const int n_groups = a.d_out / kSuChannels;
-  const int n_seg = n_groups * a.n_mats;
-  const long long cells = (long long)n_seg * n_kg;
+  const int n_seg = (a.d_out / kSuChannels) * a.n_mats;
+  const int n_grp = (n_seg + S - 1) / S;
+  const long long cells = (long long)n_grp * n_kg;
   const long long c0 = range_begin(cells, a.grid, blockIdx.x);
   const long long c1 = range_begin(cells, a.grid, blockIdx.x + 1);
   if (c1 <= c0) return;  // uniform: no work
-  const int ncells = (int)(c1 - c0);
   if (tbase & (kTabAlign - 1)) {  // the address trick needs the 16 KB alignment; set by construction
     if (tid == 0 && a.status) atomicExch(a.status, 2);
     return;
@@ -218,51 +228,61 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) decode_kernel(DecAr
     tabs[i] = __ldg(a.mats[0].codebook + (i >> 5));
     if (a.n_mats > 1) tabs[kTabWords + i] = __ldg(a.mats[1].codebook + (i >> 5));
   }
-  __syncthreads();
-  // Programmatic dependent launch: everything above overlaps the kernel that
-  // writes the rotated input; wait for it here, and let the next kernel launch.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;");
 
-  // The warp's k-th cell is local cell lc = warp + 8k. The issue cursor walks
-  // (segment, column group) incrementally: no division in the loop.
   const bool two = a.n_mats > 1;
-  int i_lc = warp, i_sg, i_kg;
-  {
-    const long long cw = c0 + warp;
-    i_sg = (int)(cw / n_kg);
-    i_kg = (int)(cw % n_kg);
-  }
-  const uint4* xf_base = reinterpret_cast<const uint4*>(a.xfrag) + ((size_t)a.nt0 * 32 + lane) * 2;
-  const size_t xf_kg_stride = (size_t)a.n_tiles * 64;  // uint4 per column group
+  // index prefetch cursor: the warp walks the cells of the range whose column
+  // group is in its K phase, loading its own segment's super-unit of each
+  long long ci = c0;
+  int i_g = (int)(c0 / n_kg), i_kg = (int)(c0 % n_kg);
+  auto to_phase = [&]() {
+    while (ci < c1 && (i_kg & (R - 1)) != kphase) {
+      ++ci;
+      if (++i_kg == n_kg) {
+        i_kg = 0;
+        ++i_g;
+      }
+    }
+  };
+  to_phase();
   int k_issue = 0;
   auto issue = [&]() {
-    const uint32_t slot = ring + (uint32_t)((k_issue % Ring<NT>::kSlots) * Ring<NT>::kSlotBytes);
-    if (i_lc < ncells) {
-      const int mat = two ? (i_sg & 1) : 0;
-      const int mg = two ? (i_sg >> 1) : i_sg;
-      const uint4* su = (mat ? a.mats[1].packed : a.mats[0].packed) + ((size_t)mg * n_kg + i_kg) * kSuUint4 + lane;
-      copy_cell<NT>(slot, lane, su, xf_base + (size_t)i_kg * xf_kg_stride);
+    const uint32_t slot = ring + (uint32_t)((k_issue % Ring::kSlots) * Ring::kSlotBytes);
+    const int sg = i_g * S + seg_local;
+    if (ci < c1 && sg < n_seg) {
+      const int mat = two ? (sg & 1) : 0;
+      const int mg = two ? (sg >> 1) : sg;
+      copy_su(slot, lane, (mat ? a.mats[1].packed : a.mats[0].packed) + ((size_t)mg * n_kg + i_kg) * kSuUint4 + lane);
     }
-    cp_async_commit();  // one group per cell, empty past the end
+    cp_async_commit();  // one group per cell of this warp, empty past the end
     ++k_issue;
-    i_lc += kDecWarps;
-    i_kg += kDecWarps;
-    while (i_kg >= n_kg) {
-      i_kg -= n_kg;
-      ++i_sg;
+    if (ci < c1) {
+      ++ci;
+      if (++i_kg == n_kg) {
+        i_kg = 0;
+        ++i_g;
+      }
+      to_phase();
     }
   };
 #pragma unroll
-  for (int k = 0; k < Ring<NT>::kSlots; ++k) issue();
-  int k_use = 0;
+  for (int k = 0; k < Ring::kSlots; ++k) issue();  // weights do not depend on the previous kernel
+  __syncthreads();
+  // Programmatic dependent launch: the above overlaps the kernel that writes the
+  // rotated input; wait for it before staging activations.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
 
+  const uint4* xf_g = reinterpret_cast<const uint4*>(a.xfrag);
+  int k_use = 0;
   float acc[4][NT][4];
   long long c = c0;
   while (c < c1) {
-    const int sg = (int)(c / n_kg);
-    const long long seg_end = ((long long)(sg + 1) * n_kg < c1) ? (long long)(sg + 1) * n_kg : c1;
-    const int lc_end = (int)(seg_end - c0);
+    const int g = (int)(c / n_kg);
+    const long long g_end = ((long long)(g + 1) * n_kg < c1) ? (long long)(g + 1) * n_kg : c1;
+    const int sg = g * S + seg_local;
+    const bool live = sg < n_seg;
+    const uint32_t lane_base =
+        tbase | (uint32_t)(lane * 4) | ((two && (sg & 1)) ? (uint32_t)(kTabWords * 4) : 0u);
 #pragma unroll
     for (int m = 0; m < 4; ++m)
 #pragma unroll
@@ -270,40 +290,74 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) decode_kernel(DecAr
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[m][nt][j] = 0.f;
 
-    // this warp's cells of the segment, in sequence order
-    const uint32_t lane_base = tbase | (uint32_t)(lane * 4) | ((two && (sg & 1)) ? (uint32_t)(kTabWords * 4) : 0u);
-    while (warp + kDecWarps * k_use < lc_end) {
-      cp_async_wait<Ring<NT>::kSlots - 1>();  // this cell's copies have landed
-      compute_cell<NT>(ring + (uint32_t)((k_use % Ring<NT>::kSlots) * Ring<NT>::kSlotBytes), lane, lane_base, acc);
-      issue();  // refill the slot just read, kSlots cells ahead
-      ++k_use;
+    while (c < g_end) {
+      // stage the activation fragments of up to Xs<NT>::kKg column groups
+      const int kA = (int)(c % n_kg);
+      const int len = (int)((g_end - c) < Xs<NT>::kKg ? (g_end - c) : Xs<NT>::kKg);
+      __syncthreads();  // every warp is done with the previous stage
+      {
+        const int per_kg = NT * 64;  // uint4 per column group
+        for (int e = tid; e < len * per_kg; e += kThreads) {
+          const int k = e / per_kg, r = e % per_kg;
+          cp_async16(xs + (uint32_t)(e * 16), xf_g + ((size_t)(kA + k) * a.n_tiles + a.nt0) * 64 + r);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+      }
+      __syncthreads();
+      for (int k = 0; k < len; ++k) {
+        if (((kA + k) & (R - 1)) != kphase) continue;  // another warp's K phase
+        cp_async_wait<Ring::kSlots - 1>();  // this cell's index copies have landed
+        if (live)
+          compute_cell<NT>(ring + (uint32_t)((k_use % Ring::kSlots) * Ring::kSlotBytes),
+                           xs + (uint32_t)(k * NT * 1024), lane, lane_base, acc);
+        issue();  // refill the slot just read, kSlots cells ahead
+        ++k_use;
+      }
+      c += len;
     }
-
-    // sum the eight warps' accumulators of this segment: one piece
+    // this CTA's part of group g: one piece per segment
+    const int piece = blockIdx.x - cta_of((long long)g * n_kg, cells, a.grid);
+    if (R == 1) {
+      if (live) {
+        float* pc = a.pieces + ((size_t)sg * a.max_pieces + piece) * PIECE;
 #pragma unroll
-    for (int m = 0; m < 4; ++m)
+        for (int m = 0; m < 4; ++m)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) red[(warp * ITEMS + (m * NT + nt) * 4 + j) * 32 + lane] = acc[m][nt][j];
-    __syncthreads();
-    const int piece = blockIdx.x - cta_of((long long)sg * n_kg, cells, a.grid);
-    float* pc = a.pieces + ((size_t)sg * a.max_pieces + piece) * PIECE;
-    for (int it = tid; it < PIECE; it += kThreads) {
-      float s = 0.f;
+            for (int j = 0; j < 4; ++j) pc[((m * NT + nt) * 4 + j) * 32 + lane] = acc[m][nt][j];
+      }
+    } else {
+      // the R warps of a segment add their sums in K-phase order (deterministic)
+      for (int r = 0; r < R; ++r) {
+        if (kphase == r) {
+          float* rd = red + seg_local * PIECE;
 #pragma unroll
-      for (int wq = 0; wq < kDecWarps; ++wq) s += red[wq * PIECE + it];
-      pc[it] = s;
+          for (int m = 0; m < 4; ++m)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int it = ((m * NT + nt) * 4 + j) * 32 + lane;
+                rd[it] = (r == 0) ? acc[m][nt][j] : rd[it] + acc[m][nt][j];
+              }
+        }
+        __syncthreads();
+      }
+      for (int e = tid; e < S * PIECE; e += kThreads) {
+        const int sl = e / PIECE, it = e % PIECE;
+        const int sg2 = g * S + sl;
+        if (sg2 < n_seg) a.pieces[((size_t)sg2 * a.max_pieces + piece) * PIECE + it] = red[e];
+      }
+      __syncthreads();
     }
-    __syncthreads();
-    c = seg_end;
   }
 }
 
 template <int NT>
 cudaError_t launch_nt(const DecArgs& a, cudaStream_t st) {
-  const int dyn = kDecWarps * Ring<NT>::kWarpBytes + (int)kTabAlign + 2 * kTabWords * 4 +
-                  kDecWarps * 32 * 16 * NT * (int)sizeof(float);
+  const int dyn = kDecWarps * Ring::kWarpBytes + Xs<NT>::kBytes + Xs<NT>::kRedBytes + (int)kTabAlign + 2 * kTabWords * 4;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -311,6 +365,8 @@ cudaError_t launch_nt(const DecArgs& a, cudaStream_t st) {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
     e = cudaFuncSetAttribute(decode_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(decode_kernel<NT>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
@@ -333,19 +389,40 @@ cudaError_t launch_nt(const DecArgs& a, cudaStream_t st) {
 
 int dec_tiles_per_pass(int rows) { return rows <= 8 ? 1 : (rows <= 16 ? 2 : 4); }
 
+// K split inside a CTA: enough warps per output segment in total (over the
+// whole grid) are shared out as R warps per segment per CTA, so that each
+// segment ends up with a handful of CTA pieces rather than one per warp.
+int dec_ksplit(int d_in, int d_out, int n_mats) {
+  const int n_seg = (d_out / kSuChannels) * n_mats;
+  int sms = device_sm_count();
+  if (sms > kDecMaxGrid) sms = kDecMaxGrid;
+  const long long warps_per_seg = (long long)kDecWarps * sms / n_seg;
+  int r = 1;
+  while (r < kDecWarps && 2LL * r * 3 <= warps_per_seg) r *= 2;
+  const int n_kg = d_in / kSuInputs;
+  while (r > 1 && r > n_kg) r /= 2;
+  return r;
+}
+
+int dec_groups(int d_in, int d_out, int n_mats) {
+  const int n_seg = (d_out / kSuChannels) * n_mats;
+  const int s = kDecWarps / dec_ksplit(d_in, d_out, n_mats);
+  return (n_seg + s - 1) / s;
+}
+
 int dec_grid(int d_in, int d_out, int n_mats) {
-  int g = 2 * device_sm_count();
+  int g = device_sm_count();
   if (g > kDecMaxGrid) g = kDecMaxGrid;
-  const long long cells = (long long)(d_out / kSuChannels) * n_mats * (d_in / kSuInputs);
+  const long long cells = (long long)dec_groups(d_in, d_out, n_mats) * (d_in / kSuInputs);
   return cells < g ? (int)cells : g;  // every CTA owns at least one cell
 }
 
 int dec_max_pieces(int d_in, int d_out, int n_mats, int grid) {
   const long long n_kg = d_in / kSuInputs;
-  const long long n_seg = (long long)(d_out / kSuChannels) * n_mats;
-  const long long cells = n_seg * n_kg;
+  const long long n_grp = dec_groups(d_in, d_out, n_mats);
+  const long long cells = n_grp * n_kg;
   int best = 1;
-  for (long long s = 0; s < n_seg; ++s) {
+  for (long long s = 0; s < n_grp; ++s) {
     const long long x0 = s * n_kg, x1 = x0 + n_kg - 1;
     const long long b0 = ((x0 + 1) * grid - 1) / cells, b1 = ((x1 + 1) * grid - 1) / cells;
     if (b1 - b0 + 1 > best) best = (int)(b1 - b0 + 1);

@@ -42,18 +42,21 @@ __host__ __device__ inline size_t lane_word_offset(size_t su, int lane, int w) {
 
 // ---------------------------------------------------------------------------
 // Rotated activations in "fragment order" (what the decode kernel reads):
-// for each 64-input column group kg and each 8-row tile nt, 256 32-bit words;
-// word v of lane L = 4g + t holds the FP16 pair (x'[8nt+g][kg*64 + 16s + 2t + 8h],
-// x'[8nt+g][... + 1]) with v = 2s + h (s = 0..3, h = 0..1): the B fragments of
-// four m16n8k16 MMAs, 32 contiguous bytes per lane. Rows past the last valid
-// row are zero. Word index: ((kg * n_tiles + nt) * 32 + L) * 8 + v.
+// for each 64-input column group kg and each 8-row tile nt, 256 32-bit words
+// (1 KB). Lane L = 4g + t needs the FP16 pairs w_v = (x'[8nt+g][kg*64 + 16s +
+// 2t + 8hh], x'[8nt+g][... + 1]), v = 2s + hh (s = 0..3, hh = 0..1): the B
+// fragments of four m16n8k16 MMAs. They are stored as two 16-byte chunks per
+// lane, chunk h = v/4 of lane L at tile offset (h*32 + L)*16, so a warp's two
+// 128-bit loads each read 512 contiguous bytes without bank conflicts. Rows
+// past the last valid row are zero.
 // ---------------------------------------------------------------------------
 __host__ __device__ inline size_t frag_half_index(int row, int col, int n_tiles) {
   const int kg = col / 64, cl = col % 64, s = cl / 16, r = cl % 16;
-  const int h = r / 8, t = (r % 8) / 2, half = r % 2;
+  const int hh = r / 8, t = (r % 8) / 2, half = r % 2;
   const int nt = row / 8, g = row % 8;
-  const int lane = 4 * g + t, v = 2 * s + h;
-  return ((((size_t)kg * n_tiles + nt) * 32 + lane) * 8 + v) * 2 + half;
+  const int lane = 4 * g + t, v = 2 * s + hh;
+  const size_t word = ((size_t)kg * n_tiles + nt) * 256 + (size_t)((v / 4) * 32 + lane) * 4 + (v % 4);
+  return word * 2 + half;
 }
 
 inline int row_tiles(int rows) { return (rows + 7) / 8; }
@@ -81,6 +84,7 @@ struct DecArgs {
   DecMat mats[2];
   float* pieces;          // [n_segments][max_pieces][512 * NT] partial sums
   int grid, max_pieces;
+  int ksplit;             // warps per segment inside a CTA
   int* status;            // device status word (set to 2 if the lookup tables are misplaced)
 };
 
@@ -89,7 +93,8 @@ struct PieceMap {
   const float* pieces;
   int n_kg;               // 64-input column groups of d_in
   int n_mats;
-  int n_segments;         // (d_out / 64) * n_mats
+  int n_groups;           // segment groups
+  int seg_per_group;      // kDecWarps / ksplit
   int grid, max_pieces;
   int nt;                 // row tiles per piece (NT)
 };
@@ -121,11 +126,13 @@ struct LinearOutArgs {
 cudaError_t launch_swiglu_rotate(const SwigluRotateArgs& a, cudaStream_t st);
 cudaError_t launch_linear_out(const LinearOutArgs& a, cudaStream_t st);
 
-constexpr int kDecWarps = 8;
+constexpr int kDecWarps = 16;  // warps per decode CTA = segments per group
 constexpr int kDecMaxGrid = 2048;
 
 int device_sm_count();
 int dec_tiles_per_pass(int rows);  // 1, 2 or 4 row tiles (8, 16 or 32 rows)
+int dec_ksplit(int d_in, int d_out, int n_mats);  // warps per segment inside a CTA (power of two)
+int dec_groups(int d_in, int d_out, int n_mats);  // segment groups (kDecWarps / ksplit segments each)
 int dec_grid(int d_in, int d_out, int n_mats);  // never more CTAs than cells
 int dec_max_pieces(int d_in, int d_out, int n_mats, int grid);
 cudaError_t launch_decode(const DecArgs& a, int nt, cudaStream_t st);
