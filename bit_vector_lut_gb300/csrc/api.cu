@@ -66,14 +66,48 @@ int frag_tiles(int rows) {
 
 size_t frag_bytes(int rows, int n) { return (size_t)frag_tiles(rows) * (n / 64) * 1024; }
 
-size_t pieces_bytes(int rows, int d_in, int d_out, int n_mats) {
-  const int grid = dec_grid(d_in, d_out, n_mats);
+// Pieces of one decode pass of the multi-kernel path (the MLP halves).
+size_t multi_pieces_bytes(int rows, int d_in, int d_out, int n_mats) {
   const size_t piece = (size_t)512 * dec_tiles_per_pass(rows) * sizeof(float);
-  return (size_t)(d_out / kSuChannels) * n_mats * dec_max_pieces(d_in, d_out, n_mats, grid) * piece;
+  const size_t n_seg = (size_t)(d_out / kSuChannels) * n_mats;
+  return n_seg * dec_max_pieces(d_in, d_out, n_mats, dec_grid(d_in, d_out, n_mats)) * piece;
 }
 
+// Pieces of one decode step of the persistent kernel.
+size_t persist_pieces_bytes(int rows, int d_in, int d_out, int n_mats) {
+  const int nt = dec_tiles_per_pass(rows);
+  const size_t piece = (size_t)512 * nt * sizeof(float);
+  const size_t n_seg = (size_t)(d_out / kSuChannels) * n_mats;
+  const int grid = persist_decode_grid(d_in, d_out, n_mats, persist_grid(nt));
+  return n_seg * persist_max_pieces(d_in, d_out, n_mats, grid) * piece;
+}
+
+int seg_groups(int d_out, int n_mats) { return ((d_out / kSuChannels) * n_mats + kDecWarps - 1) / kDecWarps; }
+
+// Counter words of the persistent kernel (word 0: finished CTAs).
+struct CtlLayout {
+  int off_g, off_hd, off_o, n;
+};
+
+CtlLayout ctl_mlp(int H, int I) {
+  CtlLayout c{};
+  c.off_g = 1;                          // gate/up segment groups
+  c.off_hd = c.off_g + seg_groups(I, 2);  // h chunks (at most I/64): SwiGLU tasks done
+  c.off_o = c.off_hd + I / 64;          // down segment groups
+  c.n = c.off_o + seg_groups(H, 1);
+  return c;
+}
+
+CtlLayout ctl_linear(int d_in, int d_out) {
+  CtlLayout c{};
+  c.off_o = c.off_g = c.off_hd = 1;
+  c.n = c.off_o + seg_groups(d_out, 1);
+  return c;
+}
+
+// [status word (256 B)][pieces][counter words, zero between calls]
 struct LinearWs {
-  size_t status, xf, pieces, counters, total;
+  size_t status, pieces, counters, total;
 };
 
 LinearWs linear_ws(int rows, int d_in, int d_out) {
@@ -81,25 +115,25 @@ LinearWs linear_ws(int rows, int d_in, int d_out) {
   size_t off = 0;
   w.status = off;
   off += 256;
-  w.xf = off;
-  off = round_up(off + frag_bytes(rows, d_in), 256);
   w.pieces = off;
-  off = round_up(off + pieces_bytes(rows, d_in, d_out, 1), 256);
+  off = round_up(off + persist_pieces_bytes(rows, d_in, d_out, 1), 256);
   w.counters = off;
-  off = round_up(off + (size_t)(d_out / kSuChannels) * sizeof(unsigned), 256);
+  off = round_up(off + (size_t)ctl_linear(d_in, d_out).n * sizeof(unsigned), 256);
   w.total = off;
   return w;
 }
 
+// [status word][x' fragments][h' fragments][h fp32][pieces of the halves]
+// [gate/up pieces][down pieces][counter words, zero between calls]
 struct MlpWs {
-  size_t status, xf, hf, pieces, counters, total;
+  size_t status, xf, hf, hbuf, pieces, pieces1, pieces3, counters, total;
 };
 
 MlpWs mlp_ws(int rows, const vq3_mlp_layer* l) {
   MlpWs w{};
   const int H = l->gate.d_in, I = l->gate.d_out;
-  const size_t p_gu = pieces_bytes(rows, H, I, 2);
-  const size_t p_dn = pieces_bytes(rows, I, H, 1);
+  const size_t p_gu = multi_pieces_bytes(rows, H, I, 2);
+  const size_t p_dn = multi_pieces_bytes(rows, I, H, 1);
   size_t off = 0;
   w.status = off;
   off += 256;
@@ -107,11 +141,16 @@ MlpWs mlp_ws(int rows, const vq3_mlp_layer* l) {
   off = round_up(off + frag_bytes(rows, H), 256);
   w.hf = off;
   off = round_up(off + frag_bytes(rows, I), 256);
+  w.hbuf = off;
+  off = round_up(off + (size_t)8 * dec_tiles_per_pass(rows) * I * sizeof(float), 256);
   w.pieces = off;
   off = round_up(off + (p_gu > p_dn ? p_gu : p_dn), 256);
+  w.pieces1 = off;
+  off = round_up(off + persist_pieces_bytes(rows, H, I, 2), 256);
+  w.pieces3 = off;
+  off = round_up(off + persist_pieces_bytes(rows, I, H, 1), 256);
   w.counters = off;
-  const int groups = (I > H ? I : H) / kSuChannels;
-  off = round_up(off + (size_t)groups * sizeof(unsigned), 256);
+  off = round_up(off + (size_t)ctl_mlp(H, I).n * sizeof(unsigned), 256);
   w.total = off;
   return w;
 }
@@ -169,30 +208,6 @@ PieceMap piece_map(const DecArgs& d, int nt) {
   return pm;
 }
 
-// out = fp16(scale * W (R in)) for one matrix, all rows: rotate into fragment
-// order, then per pass of 8/16/32 rows a decode and a combine.
-cudaError_t run_linear(const uint16_t* in, int rows, const vq3_linear& L, uint32_t* xf, float* pieces, int* status,
-                       uint16_t* out, cudaStream_t st) {
-  const int tiles = frag_tiles(rows);
-  cudaError_t e = launch_fwht_frag(in, rows, L.d_in, L.block, L.signs, xf, tiles, st);
-  if (e != cudaSuccess) return e;
-  DecArgs d = decode_args(xf, tiles, L.d_in, L.d_out, 1, &L, pieces, status);
-  const int per = dec_tiles_per_pass(rows);
-  for (int nt0 = 0; nt0 < tiles; nt0 += per) {
-    d.nt0 = nt0;
-    if ((e = launch_decode(d, per, st)) != cudaSuccess) return e;
-    LinearOutArgs o{};
-    o.pm = piece_map(d, per);
-    o.scales = L.scales;
-    o.d_out = L.d_out;
-    o.row0 = nt0 * 8;
-    o.rows = rows - o.row0 < per * 8 ? rows - o.row0 : per * 8;
-    o.out = out;
-    if ((e = launch_linear_out(o, st)) != cudaSuccess) return e;
-  }
-  return cudaSuccess;
-}
-
 // h' = R_d(silu(W_g R_g x) * (W_u R_g x)) in fragment order, all rows.
 cudaError_t run_gate_up(const uint16_t* x, int rows, const vq3_mlp_layer& l, uint32_t* xf, uint32_t* hf,
                         float* pieces, int* status, cudaStream_t st) {
@@ -239,6 +254,72 @@ cudaError_t run_down(const uint32_t* hf, int rows, const vq3_mlp_layer& l, float
     o.rows = rows - o.row0 < per * 8 ? rows - o.row0 : per * 8;
     o.out = out;
     if ((e = launch_linear_out(o, st)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// The persistent kernel over all rows, one launch per pass of 8/16/32 rows.
+// `layer` null: a single linear layer L.
+struct PersistBufs {
+  float *hbuf, *pieces1, *pieces3;
+  unsigned* ctl;
+  int* status;
+};
+
+cudaError_t run_persistent(const uint16_t* x, int rows, const vq3_mlp_layer* layer, const vq3_linear* L,
+                           const PersistBufs& b, uint16_t* out, cudaStream_t st) {
+  const int nt = dec_tiles_per_pass(rows);
+  PersistArgs a{};
+  a.x = x;
+  a.hbuf = b.hbuf;
+  a.pieces1 = b.pieces1;
+  a.pieces3 = b.pieces3;
+  a.ctl = b.ctl;
+  a.status = b.status;
+  a.out = out;
+  a.grid = persist_grid(nt);
+  CtlLayout c{};
+  if (layer) {
+    const int H = layer->gate.d_in, I = layer->gate.d_out;
+    a.mlp = 1;
+    a.d_model = H;
+    a.d_inter = I;
+    a.d_model_out = H;
+    a.block_in = layer->gate.block;
+    a.signs_in = layer->gate.signs;
+    a.block_dn = layer->down.block;
+    a.signs_dn = layer->down.signs;
+    a.x_chunk = persist_chunk(H, a.block_in);
+    a.h_chunk = persist_chunk(I, a.block_dn);
+    a.gate = dec_mat(layer->gate);
+    a.up = dec_mat(layer->up);
+    a.down = dec_mat(layer->down);
+    a.grid1 = persist_decode_grid(H, I, 2, a.grid);
+    a.max_pieces1 = persist_max_pieces(H, I, 2, a.grid1);
+    a.grid3 = persist_decode_grid(I, H, 1, a.grid);
+    a.max_pieces3 = persist_max_pieces(I, H, 1, a.grid3);
+    c = ctl_mlp(H, I);
+  } else {
+    a.mlp = 0;
+    a.d_model = L->d_in;
+    a.d_model_out = L->d_out;
+    a.block_in = L->block;
+    a.signs_in = L->signs;
+    a.x_chunk = persist_chunk(L->d_in, a.block_in);
+    a.gate = a.up = a.down = dec_mat(*L);
+    a.grid1 = persist_decode_grid(L->d_in, L->d_out, 1, a.grid);
+    a.max_pieces1 = persist_max_pieces(L->d_in, L->d_out, 1, a.grid1);
+    c = ctl_linear(L->d_in, L->d_out);
+  }
+  a.n_ctl = c.n;
+  a.off_g = c.off_g;
+  a.off_hd = c.off_hd;
+  a.off_o = c.off_o;
+  for (int row0 = 0; row0 < rows; row0 += 8 * nt) {
+    a.row0 = row0;
+    a.rows = rows - row0 < 8 * nt ? rows - row0 : 8 * nt;
+    cudaError_t e = launch_persistent(a, nt, st);
+    if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
@@ -429,8 +510,11 @@ int vq3_linear_forward(const uint16_t* x, int rows, const vq3_linear* L, uint16_
   if (ws_bytes < w.total) return fail(VQ3_ENOSPACE, "linear: workspace %zu < %zu bytes", ws_bytes, w.total);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
-  cudaError_t e = run_linear(x, rows, *L, reinterpret_cast<uint32_t*>(ws + w.xf),
-                             reinterpret_cast<float*>(ws + w.pieces), reinterpret_cast<int*>(ws + w.status), out, st);
+  PersistBufs b{};
+  b.pieces1 = reinterpret_cast<float*>(ws + w.pieces);
+  b.ctl = reinterpret_cast<unsigned*>(ws + w.counters);
+  b.status = reinterpret_cast<int*>(ws + w.status);
+  cudaError_t e = run_persistent(x, rows, nullptr, L, b, out, st);
   if (e != cudaSuccess) return cuda_fail(e, "linear: launch");
   return ok();
 }
@@ -496,10 +580,14 @@ int vq3_mlp_forward(const uint16_t* x, int rows, const vq3_mlp_layer* layer, uin
   if (c.rc || rows == 0) return c.rc ? c.rc : ok();
   if (!x || !out) return fail(VQ3_EINVAL, "mlp: null x/out");
   if (!aligned(x, 16) || !aligned(out, 16)) return fail(VQ3_EALIGN, "mlp: x/out must be 16-byte aligned");
-  int rc = gate_up_half(x, rows, layer, c);
-  if (rc) return rc;
-  rc = down_half(rows, layer, out, c);
-  if (rc) return rc;
+  PersistBufs b{};
+  b.hbuf = reinterpret_cast<float*>(c.ws + c.w.hbuf);
+  b.pieces1 = reinterpret_cast<float*>(c.ws + c.w.pieces1);
+  b.pieces3 = reinterpret_cast<float*>(c.ws + c.w.pieces3);
+  b.ctl = reinterpret_cast<unsigned*>(c.ws + c.w.counters);
+  b.status = reinterpret_cast<int*>(c.ws + c.w.status);
+  cudaError_t e = run_persistent(x, rows, layer, nullptr, b, out, c.st);
+  if (e != cudaSuccess) return cuda_fail(e, "mlp: launch");
   return ok();
 }
 
@@ -526,8 +614,7 @@ int vq3_mlp_down(int rows, const vq3_mlp_layer* layer, uint16_t* out, void* work
 int vq3_mlp_kernel_launches(int rows, const vq3_mlp_layer* layer) {
   if (check_mlp(layer) || rows < 0) return -1;
   if (rows == 0) return 0;
-  const int passes = frag_tiles(rows) / dec_tiles_per_pass(rows);
-  return 1 + 4 * passes;  // rotation of x; per row pass: gate/up decode, SwiGLU+rotation, down decode, output
+  return frag_tiles(rows) / dec_tiles_per_pass(rows);  // one persistent kernel per row pass
 }
 
 size_t vq3_mlp_host_workspace_bytes(int rows, const vq3_mlp_layer* layer) {

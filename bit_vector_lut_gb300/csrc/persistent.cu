@@ -1,0 +1,851 @@
+// The small-row-count path (T <= 32 rows per pass) of the VQ3 MLP block and of
+// a single VQ3 linear layer: one persistent cooperative kernel per pass.
+//
+// What it computes (model card "anemll/anemll-forge-qwen3.8-27B", section
+// "Release 0.2: three-bit MLP, token-mixer rotations, distilled weights": every
+// MLP matrix a 2x64 vector LUT with per-channel scales, each matrix input
+// multiplied online by blocked Hadamard matrices with seeded signs; SiLU as
+// x*sigmoid(x) per "ANEMLL ANE LLM conversion pipeline", section "Facts"):
+//   g, u = W_g R_in x, W_u R_in x      decode, split-K partial sums ("pieces")
+//   h    = silu(s_g g) * (s_u u)       one task per 64 intermediate channels
+//   y    = W_d R_dn h                  decode, pieces
+//   out  = fp16(s_d y)                 one task per 64 output channels x 8-row tile
+// A single matrix runs the first decode and the output tasks.
+//
+// The rotations R = blockdiag(H_b diag(s)) / sqrt(b) are not separate steps: a
+// decoding CTA rotates the chunks of x (or h) its column groups lie in, straight
+// into its shared-memory activation stage. x is an input; h is complete per chunk
+// when that chunk's SwiGLU tasks have counted themselves done.
+//
+// There are no grid-wide barriers. Every consumer waits only for what it reads,
+// through counters in the workspace: segment groups count the CTAs that wrote
+// their pieces, h chunks count finished SwiGLU tasks. Waits poll a bounded number
+// of times (on timeout the status word gets 3 and the kernel still ends). The
+// cooperative launch makes all CTAs co-resident and no wait depends on work
+// ordered after it in any CTA, so every wait ends. The last CTA to finish
+// resets the counters to zero for the next launch.
+//
+// Decode: the m16n8k16 tensor-core path. A tcgen05.mma takes the same time for
+// any N up to 256, so at N = 8..32 it would absorb ~5 indices per clock per SM,
+// a sixth of what streaming the indices at HBM speed needs; m16n8k16 absorbs
+// ~60, which leaves the decode itself (shift, mask, shared-memory lookup, byte
+// permute per index) as the limit.
+//   - Each CTA holds lane-private copies of the three codebooks (entry k of lane
+//     L at word k*32 + L) at a 16 KB-aligned shared address, so a lookup is one
+//     shift, one LOP3 and one bank-conflict-free load.
+//   - Segments (64 output channels x matrix) are grouped 16 at a time, one per
+//     warp; a cell is one group x one 64-input column group, and every CTA owns a
+//     contiguous run of cells. Its activation stage holds the fragments of up to
+//     32/NT cells' column groups (all 16 warps read them), and every warp streams
+//     its own segment's index strings through a 3-deep cp.async ring.
+//   - A warp's sum over its run of a segment is one piece; consumers sum a
+//     segment's pieces in CTA (= K) order, so results do not depend on timing.
+#include <cuda_fp16.h>
+
+#include "vq3_internal.h"
+
+namespace vq3 {
+namespace {
+
+constexpr int kWarps = kDecWarps;  // 16
+constexpr int kThreads = kWarps * 32;
+constexpr int kTabWords = 64 * 32;
+constexpr uint32_t kTabAlign = 16384;
+constexpr long long kSpinLimit = 1ll << 21;  // polls of one wait: well over a second
+
+// ------------------------------------------------------------------ primitives
+
+// Not volatile: a pure function of its registers, free to schedule.
+__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Shared address of the lookup for lane index N: bits [6N, 6N+6) of the lane's
+// 384-bit string moved to bits [7, 13) (entry stride 32 lanes x 4 bytes), OR-ed
+// with the table base, the lane's column and the matrix's table offset.
+template <int N>
+__device__ __forceinline__ uint32_t lut_addr(const uint32_t (&w)[12], uint32_t lanebase) {
+  constexpr int pos = 6 * N;
+  constexpr int wd = pos / 32;
+  constexpr int off = pos % 32;
+  uint32_t v;
+  if constexpr (off >= 7) {
+    const uint32_t hi = (wd + 1 < 12) ? w[wd + 1] : 0u;
+    v = __funnelshift_r(w[wd], hi, off - 7);
+  } else {
+    v = w[wd] << (7 - off);
+  }
+  return (v & 0x1F80u) | lanebase;
+}
+
+// The tables are read-only while cells are decoded: a pure load, free to reorder.
+__device__ __forceinline__ uint32_t lut(uint32_t saddr) {
+  uint32_t v;
+  asm("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(saddr));
+  return v;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t saddr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(saddr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+__device__ __forceinline__ long long range_begin(long long cells, int grid, int b) {
+  return (long long)b * cells / grid;
+}
+
+// CTA owning cell x (largest b with range_begin(b) <= x).
+__device__ __forceinline__ int cta_of(long long x, long long cells, int grid) {
+  return (int)(((x + 1) * grid - 1) / cells);
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+
+// ------------------------------------------------------------------ counters
+
+// Thread 0 polls until *p >= target (bounded; after any timeout in the launch,
+// status 3, it returns at once).
+__device__ __forceinline__ void poll_geq(const unsigned* p, unsigned target, int* status) {
+  if (*(volatile int*)status == 3) return;
+  long long it = 0;
+  while (ld_acquire(p) < target) {
+    if (++it > kSpinLimit) {
+      atomicExch(status, 3);
+      return;
+    }
+    __nanosleep(32);
+  }
+}
+
+// The CTA's writes so far become visible, then *p += 1 (and *p2 += 1).
+__device__ __forceinline__ void signal(unsigned* p, unsigned* p2) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(p, 1u);
+    if (p2) atomicAdd(p2, 1u);
+  }
+}
+
+// ------------------------------------------------------------------ geometry
+
+struct DecodeJob {
+  int d_in, d_out, n_mats;
+  const uint4* packed0;
+  const uint4* packed1;
+  const uint16_t* scales0;
+  float* pieces;            // [n_seg][max_pieces][512 * NT]
+  int grid, max_pieces;     // decoding CTAs (<= cells) and piece slots per segment
+  uint32_t tab;             // shared address of matrix 0's table (16 KB aligned); matrix 1 at +8192
+  // activation source, rotated into the stage: rows [0, rows) at src + r * src_ld
+  size_t src_ld;
+  int rows, block, chunk;   // valid rows; rotation block; chunk (whole blocks, columns)
+  const uint32_t* signs;
+  const unsigned* ready;    // per chunk: complete when >= ready_target (null: ready at launch)
+  unsigned ready_target;
+  unsigned* group_done;     // per segment group: +1 per CTA whose pieces of the group are written
+
+  __device__ int n_kg() const { return d_in / kSuInputs; }
+  __device__ int n_seg() const { return (d_out / kSuChannels) * n_mats; }
+  __device__ int n_grp() const { return (n_seg() + kWarps - 1) / kWarps; }
+  __device__ long long cells() const { return (long long)n_grp() * n_kg(); }
+  // CTAs that write pieces of segment group g (slots 0 .. count-1)
+  __device__ int contributors(int g) const {
+    const long long x0 = (long long)g * n_kg();
+    return cta_of(x0 + n_kg() - 1, cells(), grid) - cta_of(x0, cells(), grid) + 1;
+  }
+  __device__ const float* seg_pieces(int sg, int piece_floats) const {
+    return pieces + (size_t)sg * max_pieces * piece_floats;
+  }
+};
+
+struct SmemView {
+  uint32_t ring, stage, tab;  // shared addresses
+  float* scratch;             // rotation scratch: 4 KB per warp
+  int* flag;                  // one word for the last-CTA test
+};
+
+// Item `it` of a piece -> (row of the pass, channel within the 64-channel group).
+// Piece layout: it = ((m * NT + nt) * 4 + j) * 32 + lane, the m16n8k16 accumulator order.
+template <int NT>
+__device__ __forceinline__ void item_pos(int it, int& row, int& ch) {
+  const int L = it & 31, idx = it >> 5;
+  const int j = idx & 3, mnt = idx >> 2, nt = mnt % NT, m = mnt / NT;
+  ch = (8 * m + (L >> 2)) * 2 + (j >> 1);
+  row = nt * 8 + 2 * (L & 3) + (j & 1);
+}
+
+// ------------------------------------------------------------------ rotation into the stage
+//
+// Stage layout: slot p (cell rs + p of the round, column group kg(p)) holds NT
+// 1 KB row tiles; tile nt holds the B fragments of rows 8nt .. 8nt+7: the 16-byte
+// chunk q = h*32 + 4g + t (row g, half h) carries columns 32h + 8i + 2t + {0, 1}
+// (i = 0..3) of the column group as FP16 pairs. Chunk q is stored at position
+// q ^ (p & 7), which keeps both the rotation's writes (one row, 16 column groups
+// per warp instruction) and the decode's reads (512 contiguous bytes) free of
+// bank conflicts.
+
+template <int NT>
+struct StageCfg {
+  static constexpr int kSlots = NT == 1 ? 32 : (NT == 2 ? 16 : 8);  // column groups per round
+  static constexpr int kBytes = kSlots * NT * 1024;
+};
+
+__device__ __forceinline__ uint32_t stage_chunk_addr(uint32_t stage, int p, int nt_count, int nt, int q) {
+  return stage + (uint32_t)((p * nt_count + nt) * 1024 + ((q ^ (p & 7)) << 4));
+}
+
+__device__ __forceinline__ void sts128(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Butterflies of stride S (in register index) over v[0 .. 32).
+template <int S>
+__device__ __forceinline__ void bfly32(float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if ((i & S) == 0) {
+      const float x0 = v[i], x1 = v[i + S];
+      v[i] = x0 + x1;
+      v[i + S] = x0 - x1;
+    }
+}
+
+// Butterflies of register strides 1 .. min(32, limit)/2.
+__device__ __forceinline__ void fwht32(float (&v)[32], int limit) {
+  if (limit > 1) bfly32<1>(v);
+  if (limit > 2) bfly32<2>(v);
+  if (limit > 4) bfly32<4>(v);
+  if (limit > 8) bfly32<8>(v);
+  if (limit > 16) bfly32<16>(v);
+}
+
+// Hadamard butterflies of strides 1 .. block/2 over buf[0 .. n) (n a multiple of block).
+__device__ __forceinline__ void fwht_smem(float* buf, int n, int block) {
+  for (int lh = 0; (1 << lh) < block; ++lh) {
+    const int h = 1 << lh;
+    for (int q = threadIdx.x; q < n / 2; q += kThreads) {
+      const int i0 = ((q >> lh) << (lh + 1)) + (q & (h - 1)), i1 = i0 + h;
+      const float x0 = buf[i0], x1 = buf[i1];
+      buf[i0] = x0 + x1;
+      buf[i1] = x0 - x1;
+    }
+    __syncthreads();
+  }
+}
+
+__device__ __forceinline__ float load1(const uint16_t* p) { return __half2float(__ushort_as_half(__ldg(p))); }
+__device__ __forceinline__ float load1(const float* p) { return __ldcg(p); }
+
+__device__ __forceinline__ bool sign_bit(const uint32_t* signs, int col) {
+  return (__ldg(signs + (col >> 5)) >> (col & 31)) & 1u;
+}
+
+// Offset in the round's window of chunk c's first column group, and whether the
+// chunk holds any of the window's column groups (kg_s .. kg_s + len - 1, cyclic).
+__device__ __forceinline__ bool chunk_in_window(int c, int ckg, int kg_s, int len, int n_kg) {
+  const int d0 = (c * ckg - kg_s + n_kg) % n_kg;
+  return d0 < len || d0 + ckg > n_kg;
+}
+
+// Writes the stage slots of round [rs, rs + len): the rotated activations of each
+// slot's column group, rows < a.rows (other rows are left as they are: an MMA
+// column depends on its own B column only, and their outputs are never stored).
+template <int NT, typename T>
+__device__ __forceinline__ void stage_round(const DecodeJob& a, const T* src, long long rs, int len, const SmemView& sv) {
+  const int n_kg = a.n_kg();
+  const int ckg = a.chunk / kSuInputs;
+  const int n_chunks = n_kg / ckg;
+  const int kg_s = (int)(rs % n_kg);
+  const float scale = 1.0f / sqrtf((float)a.block);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (a.chunk == 1024) {
+    // one (chunk, row) per warp: lane L holds columns L + 32 j, then 32 L + c
+    float* m = sv.scratch + warp * 1024;
+    int item = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+      if (!chunk_in_window(c, ckg, kg_s, len, n_kg)) continue;
+      for (int row = 0; row < a.rows; ++row, ++item) {
+        if ((item & (kWarps - 1)) != warp) continue;
+        const T* s = src + (size_t)row * a.src_ld + c * 1024;
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = load1(s + 32 * j + lane);
+        if (a.signs) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (sign_bit(a.signs, c * 1024 + 32 * j + lane)) v[j] = -v[j];
+        }
+        fwht32(v, a.block >> 5);  // column strides 32 .. block/2
+#pragma unroll
+        for (int j = 0; j < 32; ++j) m[j * 32 + (lane ^ j)] = v[j];
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = m[lane * 32 + (k ^ lane)];
+        __syncwarp();
+        fwht32(v, a.block);  // column strides 1 .. min(block, 32)/2
+        const int kg = c * ckg + (lane >> 1), h = lane & 1, nt = row >> 3, g = row & 7;
+        for (int p = (kg - kg_s + n_kg) % n_kg; p < len; p += n_kg)
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            sts128(stage_chunk_addr(sv.stage, p, NT, nt, h * 32 + 4 * g + t),
+                   pack_half2(v[2 * t] * scale, v[2 * t + 1] * scale),
+                   pack_half2(v[8 + 2 * t] * scale, v[9 + 2 * t] * scale),
+                   pack_half2(v[16 + 2 * t] * scale, v[17 + 2 * t] * scale),
+                   pack_half2(v[24 + 2 * t] * scale, v[25 + 2 * t] * scale));
+      }
+    }
+    return;
+  }
+  // smaller chunks: CTA-wide butterflies over [8 rows][chunk] fp32 in the scratch
+  float* buf = sv.scratch;
+  for (int c = 0; c < n_chunks; ++c) {
+    if (!chunk_in_window(c, ckg, kg_s, len, n_kg)) continue;
+    for (int nt = 0; nt < NT; ++nt) {
+      const int nr = a.rows - nt * 8 < 8 ? a.rows - nt * 8 : 8;
+      if (nr <= 0) break;
+      for (int e = threadIdx.x; e < nr * a.chunk; e += kThreads) {
+        const int rr = e / a.chunk, col = c * a.chunk + e % a.chunk;
+        float v = load1(src + (size_t)(nt * 8 + rr) * a.src_ld + col);
+        if (a.signs && sign_bit(a.signs, col)) v = -v;
+        buf[e] = v;
+      }
+      __syncthreads();
+      fwht_smem(buf, nr * a.chunk, a.block);
+      // one 16-byte fragment chunk per item: (row, column group of the chunk, h, t)
+      for (int e = threadIdx.x; e < nr * ckg * 8; e += kThreads) {
+        const int rr = e / (ckg * 8), kl = (e / 8) % ckg, h = (e / 4) & 1, t = e & 3;
+        const float* r = buf + rr * a.chunk + kl * 64 + 32 * h + 2 * t;
+        const int kg = c * ckg + kl;
+        for (int p = (kg - kg_s + n_kg) % n_kg; p < len; p += n_kg)
+          sts128(stage_chunk_addr(sv.stage, p, NT, nt, h * 32 + 4 * rr + t), pack_half2(r[0] * scale, r[1] * scale),
+                 pack_half2(r[8] * scale, r[9] * scale), pack_half2(r[16] * scale, r[17] * scale),
+                 pack_half2(r[24] * scale, r[25] * scale));
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// ------------------------------------------------------------------ decode
+
+template <int S, int M, int NT>
+__device__ __forceinline__ void mma_step(const uint32_t (&w)[12], uint32_t lanebase, float (&acc)[4][NT][4],
+                                         const uint32_t (&b)[NT][8]) {
+  constexpr int n0 = (S * 4 + M) * 4;
+  const uint32_t l0 = lut(lut_addr<n0 + 0>(w, lanebase));
+  const uint32_t l1 = lut(lut_addr<n0 + 1>(w, lanebase));
+  const uint32_t l2 = lut(lut_addr<n0 + 2>(w, lanebase));
+  const uint32_t l3 = lut(lut_addr<n0 + 3>(w, lanebase));
+  uint32_t a[4];
+  a[0] = __byte_perm(l0, l1, 0x5410);  // row g   (channel 2p):   inputs k, k+1
+  a[1] = __byte_perm(l0, l1, 0x7632);  // row g+8 (channel 2p+1): inputs k, k+1
+  a[2] = __byte_perm(l2, l3, 0x5410);  // row g:   inputs k+8, k+9
+  a[3] = __byte_perm(l2, l3, 0x7632);  // row g+8: inputs k+8, k+9
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) mma16816(acc[M][nt], a, b[nt][2 * S], b[nt][2 * S + 1]);
+}
+
+template <int S, int NT>
+__device__ __forceinline__ void kstep(const uint32_t (&w)[12], uint32_t lanebase, float (&acc)[4][NT][4],
+                                      const uint32_t (&b)[NT][8]) {
+  mma_step<S, 0, NT>(w, lanebase, acc, b);
+  mma_step<S, 1, NT>(w, lanebase, acc, b);
+  mma_step<S, 2, NT>(w, lanebase, acc, b);
+  mma_step<S, 3, NT>(w, lanebase, acc, b);
+}
+
+// One super-unit: the lane's index string from its ring slot, the B fragments
+// of stage slot p (NT KB at xb, chunks swizzled by p & 7).
+template <int NT>
+__device__ __forceinline__ void compute_cell(uint32_t slot, uint32_t xb, int lane, int swz, uint32_t lanebase,
+                                             float (&acc)[4][NT][4]) {
+  uint32_t w[12];
+#pragma unroll
+  for (int q = 0; q < 3; ++q) {
+    const uint4 v = lds128(slot + (uint32_t)(q * 512 + lane * 16));
+    w[4 * q + 0] = v.x;
+    w[4 * q + 1] = v.y;
+    w[4 * q + 2] = v.z;
+    w[4 * q + 3] = v.w;
+  }
+  uint32_t b[NT][8];
+  const uint32_t lo = (uint32_t)((lane ^ swz) * 16);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 v = lds128(xb + (uint32_t)((nt * 2 + h) * 512) + lo);
+      b[nt][4 * h + 0] = v.x;
+      b[nt][4 * h + 1] = v.y;
+      b[nt][4 * h + 2] = v.z;
+      b[nt][4 * h + 3] = v.w;
+    }
+  kstep<0, NT>(w, lanebase, acc, b);
+  kstep<1, NT>(w, lanebase, acc, b);
+  kstep<2, NT>(w, lanebase, acc, b);
+  kstep<3, NT>(w, lanebase, acc, b);
+}
+
+struct Cursor {
+  long long c;    // next cell whose index copies are to be issued
+  int g, kg;      // its group and column group
+  int k;          // copies issued so far
+  uint32_t slot;  // ring slot of the next copy: byte offset (k % kSlots) * kSlotBytes
+};
+
+constexpr int kSlots = 3;
+constexpr int kSlotBytes = kSuBytes;  // one super-unit
+constexpr int kWarpRing = kSlots * kSlotBytes;
+
+__device__ __forceinline__ void cell_range(const DecodeJob& a, long long& c0, long long& c1) {
+  const long long cells = a.cells();
+  c0 = range_begin(cells, a.grid, blockIdx.x);
+  c1 = range_begin(cells, a.grid, blockIdx.x + 1);
+}
+
+// Issues the index copies of the warp's segment in the cursor's next cell (an
+// empty commit group past the range end or for a segment past the last).
+__device__ __forceinline__ void issue_cell(const DecodeJob& a, Cursor& cur, long long c1, uint32_t ring) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t slot = ring + cur.slot;
+  const int sg = cur.g * kWarps + warp;
+  if (cur.c < c1 && sg < a.n_seg()) {
+    const bool two = a.n_mats > 1;
+    const int mat = two ? (sg & 1) : 0;
+    const int mg = two ? (sg >> 1) : sg;
+    const uint4* su = (mat ? a.packed1 : a.packed0) + ((size_t)mg * a.n_kg() + cur.kg) * kSuUint4 + lane;
+#pragma unroll
+    for (int q = 0; q < 3; ++q) cp_async16(slot + (uint32_t)(q * 512 + lane * 16), su + q * 32);
+  }
+  cp_async_commit();
+  ++cur.k;
+  cur.slot = cur.slot == (kSlots - 1) * kSlotBytes ? 0u : cur.slot + kSlotBytes;
+  ++cur.c;
+  if (++cur.kg == a.n_kg()) {
+    cur.kg = 0;
+    ++cur.g;
+  }
+}
+
+// Index copies of the first n cells of the CTA's range.
+__device__ __forceinline__ Cursor decode_begin(const DecodeJob& a, const SmemView& sv, int n) {
+  Cursor cur{0, 0, 0, 0, 0u};
+  if ((int)blockIdx.x >= a.grid) return cur;
+  long long c0, c1;
+  cell_range(a, c0, c1);
+  cur.c = c0;
+  cur.g = (int)(c0 / a.n_kg());
+  cur.kg = (int)(c0 % a.n_kg());
+  const uint32_t ring = sv.ring + (uint32_t)((threadIdx.x >> 5) * kWarpRing);
+  for (int k = 0; k < n; ++k) issue_cell(a, cur, c1, ring);
+  return cur;
+}
+
+// Decodes the CTA's range of cells; `cur` has issued the copies of the first
+// cur.k cells (1 .. kSlots), the rest of the prologue follows the first stage.
+template <int NT, typename T>
+__device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cursor& cur, const SmemView& sv,
+                                           int* status) {
+  constexpr int PIECE = 512 * NT;
+  constexpr int KS = StageCfg<NT>::kSlots;
+  if ((int)blockIdx.x >= a.grid) return;  // uniform over the CTA
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n_kg = a.n_kg(), n_seg = a.n_seg();
+  long long c0, c1;
+  cell_range(a, c0, c1);
+  const uint32_t ring = sv.ring + (uint32_t)(warp * kWarpRing);
+  const bool two = a.n_mats > 1;
+  uint32_t use_slot = 0;  // ring slot of the next cell to compute
+  int g = (int)(c0 / n_kg), kg = (int)(c0 % n_kg);  // group and column group of the next cell
+  float acc[4][NT][4];
+  uint32_t lane_base = 0;
+  bool live = false;
+  int sg = 0;
+  for (long long rs = c0; rs < c1; rs += KS) {
+    const int len = (int)((c1 - rs) < KS ? (c1 - rs) : KS);
+    if (a.ready) {
+      // the chunks of the round's column groups must be complete
+      if (tid == 0) {
+        const int ckg = a.chunk / kSuInputs, kg_s = (int)(rs % n_kg);
+        for (int c = 0; c < n_kg / ckg; ++c)
+          if (chunk_in_window(c, ckg, kg_s, len, n_kg)) poll_geq(a.ready + c, a.ready_target, status);
+        __threadfence();
+      }
+      __syncthreads();
+    }
+    stage_round<NT, T>(a, src, rs, len, sv);
+    while (cur.k < kSlots) issue_cell(a, cur, c1, ring);  // rest of the prologue
+    __syncthreads();
+    for (int p = 0; p < len; ++p) {
+      const long long c = rs + p;
+      if (c == c0 || kg == 0) {  // the range's part of group g starts
+        sg = g * kWarps + warp;
+        live = sg < n_seg;
+        lane_base = a.tab | (uint32_t)(lane * 4) | ((two && (sg & 1)) ? 8192u : 0u);
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[m][nt][j] = 0.f;
+      }
+      cp_async_wait<kSlots - 1>();  // this cell's index copies have landed
+      if (live)
+        compute_cell<NT>(ring + use_slot, sv.stage + (uint32_t)(p * NT * 1024), lane, p & 7, lane_base, acc);
+      issue_cell(a, cur, c1, ring);  // refill the slot just read, kSlots cells ahead
+      use_slot = use_slot == (kSlots - 1) * kSlotBytes ? 0u : use_slot + kSlotBytes;
+      if (c + 1 == c1 || kg + 1 == n_kg) {
+        // this warp's segment over the range's part of group g: one piece
+        if (live) {
+          const int piece = blockIdx.x - cta_of((long long)g * n_kg, a.cells(), a.grid);
+          float* pc = a.pieces + ((size_t)sg * a.max_pieces + piece) * PIECE;
+#pragma unroll
+          for (int m = 0; m < 4; ++m)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int j = 0; j < 4; ++j) __stcg(pc + ((m * NT + nt) * 4 + j) * 32 + lane, acc[m][nt][j]);
+        }
+        signal(a.group_done + g, nullptr);
+      }
+      if (++kg == n_kg) {
+        kg = 0;
+        ++g;
+      }
+    }
+    __syncthreads();  // every warp is done with the stage
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+}
+
+// ------------------------------------------------------------------ SwiGLU and output tasks
+
+// SwiGLU tasks: one per 64 intermediate channels mg, h = silu(s_g g) * (s_u u)
+// for the pass's rows as fp32 into hbuf [rows][d_inter]; a CTA takes mg and
+// mg + grid together so that their loads overlap. Each task counts itself done
+// in its h chunk's word.
+template <int NT>
+__device__ __forceinline__ void swiglu_tasks(const PersistArgs& a, const DecodeJob& gu, unsigned* h_done,
+                                             int* status) {
+  constexpr int PIECE = 512 * NT;
+  constexpr int P = 8;
+  const int n_mg = a.d_inter / kSuChannels;
+  const int per_chunk = a.h_chunk / kSuChannels;
+  const int G = gridDim.x;
+  for (int m0 = blockIdx.x; m0 < n_mg; m0 += 2 * G) {
+    const int m1 = m0 + G;
+    const bool two = m1 < n_mg;
+    const int g0 = (2 * m0) / kWarps, g1 = two ? (2 * m1) / kWarps : g0;  // groups of segments 2m, 2m+1
+    const int n0 = gu.contributors(g0), n1 = two ? gu.contributors(g1) : 0;
+    if (threadIdx.x == 0) {
+      poll_geq(gu.group_done + g0, (unsigned)n0, status);
+      if (two) poll_geq(gu.group_done + g1, (unsigned)n1, status);
+      __threadfence();
+    }
+    __syncthreads();
+    const float* pg0 = gu.seg_pieces(2 * m0, PIECE);
+    const float* pu0 = gu.seg_pieces(2 * m0 + 1, PIECE);
+    const float* pg1 = gu.seg_pieces(2 * m1 - (two ? 0 : 2 * G), PIECE);  // unused unless two
+    const float* pu1 = pg1 + (size_t)gu.max_pieces * PIECE;
+#pragma unroll
+    for (int q = 0; q < NT; ++q) {
+      const int it = q * 512 + threadIdx.x;
+      float s[4] = {0.f, 0.f, 0.f, 0.f};
+      const int nmax = n0 > n1 ? n0 : n1;
+      for (int q0 = 0; q0 < nmax; q0 += P) {
+        float v[4][P];
+#pragma unroll
+        for (int j = 0; j < P; ++j) {
+          const size_t o = it + (size_t)(q0 + j) * PIECE;
+          v[0][j] = (q0 + j < n0) ? __ldcg(pg0 + o) : 0.f;
+          v[1][j] = (q0 + j < n0) ? __ldcg(pu0 + o) : 0.f;
+          v[2][j] = (q0 + j < n1) ? __ldcg(pg1 + o) : 0.f;
+          v[3][j] = (q0 + j < n1) ? __ldcg(pu1 + o) : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < P; ++j) {
+          s[0] += v[0][j];
+          s[1] += v[1][j];
+          s[2] += v[2][j];
+          s[3] += v[3][j];
+        }
+      }
+      int r, c;
+      item_pos<NT>(it, r, c);
+      if (r < a.rows) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          if (k == 1 && !two) break;
+          const int ch = (k ? m1 : m0) * kSuChannels + c;
+          const float sgv = __half2float(__ushort_as_half(a.gate.scales[ch]));
+          const float suv = __half2float(__ushort_as_half(a.up.scales[ch]));
+          __stcg(a.hbuf + (size_t)r * a.d_inter + ch, silu_f(sgv * s[2 * k]) * (suv * s[2 * k + 1]));
+        }
+      }
+    }
+    signal(h_done + m0 / per_chunk, two ? h_done + m1 / per_chunk : nullptr);
+  }
+}
+
+// One task per (64 output channels, 8-row tile): out = fp16(scale * sum of pieces).
+template <int NT>
+__device__ __forceinline__ void output_tasks(const PersistArgs& a, const DecodeJob& j, int* status) {
+  constexpr int PIECE = 512 * NT;
+  constexpr int P = 32;
+  const int n_seg = j.d_out / kSuChannels;
+  for (int t = blockIdx.x; t < n_seg * NT; t += gridDim.x) {
+    const int sg = t / NT, part = t % NT;
+    const int g = sg / kWarps;
+    const int count = j.contributors(g);
+    if (threadIdx.x == 0) {
+      poll_geq(j.group_done + g, (unsigned)count, status);
+      __threadfence();
+    }
+    __syncthreads();
+    const int it = part * 512 + threadIdx.x;
+    const float* base = j.seg_pieces(sg, PIECE) + it;
+    float y = 0.f;
+    for (int q0 = 0; q0 < count; q0 += P) {
+      float v[P];
+#pragma unroll
+      for (int q = 0; q < P; ++q) v[q] = (q0 + q < count) ? __ldcg(base + (size_t)(q0 + q) * PIECE) : 0.f;
+#pragma unroll
+      for (int q = 0; q < P; ++q) y += v[q];
+    }
+    int r, c;
+    item_pos<NT>(it, r, c);
+    if (r < a.rows) {
+      const int ch = sg * kSuChannels + c;
+      const float s = __half2float(__ushort_as_half(j.scales0[ch]));
+      a.out[(size_t)(a.row0 + r) * j.d_out + ch] = __half_as_ushort(__float2half_rn(s * y));
+    }
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+
+template <int NT>
+struct Smem {
+  static constexpr uint32_t kRing = kWarps * kWarpRing;
+  static constexpr uint32_t kStage = StageCfg<NT>::kBytes;
+  static constexpr uint32_t kScratch = kWarps * 4096;  // rotation scratch, 4 KB per warp
+  static constexpr uint32_t kTabs = 3 * kTabWords * 4;  // gate, up, down (or one matrix)
+  static constexpr uint32_t kTotal = kRing + kStage + kScratch + kTabAlign + kTabs;
+};
+
+// Lane-private tables: entry k of matrix t replicated into words k*32 .. k*32+31
+// at tab + t*8192, written 4 lanes (16 bytes) at a time.
+__device__ void load_tables(uint32_t tab, const uint32_t* cb0, const uint32_t* cb1, const uint32_t* cb2) {
+  for (int i = threadIdx.x; i < 3 * 64 * 8; i += kThreads) {
+    const int t = i / 512, k = (i >> 3) & 63, q = i & 7;
+    const uint32_t* cb = t == 0 ? cb0 : (t == 1 ? cb1 : cb2);
+    if (cb) {
+      const uint32_t v = __ldg(cb + k);
+      sts128(tab + (uint32_t)(t * 8192 + k * 128 + q * 16), v, v, v, v);
+    }
+  }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) {
+  extern __shared__ __align__(16) unsigned char dsm[];
+  __shared__ int s_flag;
+  SmemView sv;
+  const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(dsm));
+  sv.ring = base;
+  sv.stage = base + Smem<NT>::kRing;
+  sv.scratch = reinterpret_cast<float*>(dsm + Smem<NT>::kRing + Smem<NT>::kStage);
+  sv.tab = (base + Smem<NT>::kRing + Smem<NT>::kStage + Smem<NT>::kScratch + kTabAlign - 1) & ~(kTabAlign - 1);
+  sv.flag = &s_flag;
+  int* status = a.status;
+  unsigned* ctl = a.ctl;
+
+  DecodeJob j1;
+  j1.d_in = a.d_model;
+  j1.d_out = a.mlp ? a.d_inter : a.d_model_out;
+  j1.n_mats = a.mlp ? 2 : 1;
+  j1.packed0 = a.gate.packed;
+  j1.packed1 = a.up.packed;
+  j1.scales0 = a.gate.scales;
+  j1.pieces = a.pieces1;
+  j1.grid = a.grid1;
+  j1.max_pieces = a.max_pieces1;
+  j1.tab = sv.tab;
+  j1.src_ld = (size_t)a.d_model;
+  j1.rows = a.rows;
+  j1.block = a.block_in;
+  j1.chunk = a.x_chunk;
+  j1.signs = a.signs_in;
+  j1.ready = nullptr;
+  j1.ready_target = 0;
+  j1.group_done = ctl + (a.mlp ? a.off_g : a.off_o);
+
+  load_tables(sv.tab, a.gate.codebook, a.mlp ? a.up.codebook : nullptr, a.mlp ? a.down.codebook : nullptr);
+  // one cell's index copies, then the rotation of x (its loads not queued behind
+  // the bulk of the prologue), then the rest of the prologue
+  Cursor cur = decode_begin(j1, sv, 1);
+  decode_run<NT, uint16_t>(j1, a.x + (size_t)a.row0 * a.d_model, cur, sv, status);
+
+  if (a.mlp) {
+    DecodeJob j3;
+    j3.d_in = a.d_inter;
+    j3.d_out = a.d_model;
+    j3.n_mats = 1;
+    j3.packed0 = j3.packed1 = a.down.packed;
+    j3.scales0 = a.down.scales;
+    j3.pieces = a.pieces3;
+    j3.grid = a.grid3;
+    j3.max_pieces = a.max_pieces3;
+    j3.tab = sv.tab + 16384u;
+    j3.src_ld = (size_t)a.d_inter;
+    j3.rows = a.rows;
+    j3.block = a.block_dn;
+    j3.chunk = a.h_chunk;
+    j3.signs = a.signs_dn;
+    j3.ready = ctl + a.off_hd;
+    j3.ready_target = (unsigned)(a.h_chunk / kSuChannels);
+    j3.group_done = ctl + a.off_o;
+    swiglu_tasks<NT>(a, j1, ctl + a.off_hd, status);
+    Cursor cur3 = decode_begin(j3, sv, kSlots);  // in flight while waiting for h chunks
+    decode_run<NT, float>(j3, a.hbuf, cur3, sv, status);
+    output_tasks<NT>(a, j3, status);
+  } else {
+    output_tasks<NT>(a, j1, status);
+  }
+
+  cp_async_wait<0>();
+  // the last CTA to finish clears the counters for the next launch
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_flag = atomicAdd(ctl, 1u) + 1 == gridDim.x;
+    __threadfence();
+  }
+  __syncthreads();
+  if (s_flag)
+    for (int i = threadIdx.x; i < a.n_ctl; i += kThreads) ctl[i] = 0u;
+}
+
+template <int NT>
+cudaError_t launch_nt(const PersistArgs& a, cudaStream_t st) {
+  const int smem = (int)Smem<NT>::kTotal;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(persistent_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, persistent_kernel<NT>, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+template <int NT>
+int occupancy() {
+  int n = 0;
+  if (cudaFuncSetAttribute(persistent_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)Smem<NT>::kTotal) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, persistent_kernel<NT>, kThreads, Smem<NT>::kTotal) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
+  return n > 0 ? n : 1;
+}
+
+}  // namespace
+
+int persist_grid(int nt) {
+  static int cache[64][3] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return device_sm_count();
+  }
+  const int slot = nt == 1 ? 0 : (nt == 2 ? 1 : 2);
+  if (!cache[dev][slot]) {
+    const int occ = nt == 1 ? occupancy<1>() : (nt == 2 ? occupancy<2>() : occupancy<4>());
+    const int g = occ * device_sm_count();
+    cache[dev][slot] = g > kDecMaxGrid ? kDecMaxGrid : g;
+  }
+  return cache[dev][slot];
+}
+
+int persist_decode_grid(int d_in, int d_out, int n_mats, int grid) {
+  const int n_seg = (d_out / kSuChannels) * n_mats;
+  const long long cells = (long long)((n_seg + kDecWarps - 1) / kDecWarps) * (d_in / kSuInputs);
+  return cells < grid ? (int)cells : grid;  // every decoding CTA owns at least one cell
+}
+
+int persist_max_pieces(int d_in, int d_out, int n_mats, int grid) {
+  const long long n_kg = d_in / kSuInputs;
+  const long long n_seg = (long long)(d_out / kSuChannels) * n_mats;
+  const long long n_grp = (n_seg + kDecWarps - 1) / kDecWarps;
+  const long long cells = n_grp * n_kg;
+  int best = 1;
+  for (long long s = 0; s < n_grp; ++s) {
+    const long long x0 = s * n_kg, x1 = x0 + n_kg - 1;
+    const long long b0 = ((x0 + 1) * grid - 1) / cells, b1 = ((x1 + 1) * grid - 1) / cells;
+    if (b1 - b0 + 1 > best) best = (int)(b1 - b0 + 1);
+  }
+  return best;
+}
+
+int persist_chunk(int d, int block) {
+  const int span = block < kSuChannels ? kSuChannels : block;
+  int chunk = span;
+  while (chunk * 2 <= 1024 && d % (chunk * 2) == 0) chunk *= 2;
+  return chunk;
+}
+
+cudaError_t launch_persistent(const PersistArgs& a, int nt, cudaStream_t st) {
+  switch (nt) {
+    case 1: return launch_nt<1>(a, st);
+    case 2: return launch_nt<2>(a, st);
+    case 4: return launch_nt<4>(a, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace vq3

@@ -136,6 +136,41 @@ int dec_groups(int d_in, int d_out, int n_mats);  // segment groups (kDecWarps /
 int dec_grid(int d_in, int d_out, int n_mats);  // never more CTAs than cells
 int dec_max_pieces(int d_in, int d_out, int n_mats, int grid);
 cudaError_t launch_decode(const DecArgs& a, int nt, cudaStream_t st);
+// One pass (up to 32 rows) of the MLP block, or of a single linear layer, as
+// one persistent cooperative kernel. Its steps (decode gate/up, SwiGLU, decode
+// down, output) hand over through counters in `ctl` rather than grid barriers;
+// the rotations happen inside the decode steps.
+struct PersistArgs {
+  const uint16_t* x;        // row-major [*][d_model]
+  int row0, rows;           // rows of this pass: [row0, row0 + rows), rows <= 8 * NT
+  int mlp;                  // 1: MLP block (gate, up, down); 0: one linear layer (gate)
+  int d_model, d_inter;     // MLP: hidden and intermediate widths; linear: d_model = d_in
+  int d_model_out;          // linear: d_out
+  int block_in, block_dn;   // rotation blocks of the gate/up (or linear) input and of the down input
+  const uint32_t* signs_in; // sign bits or null
+  const uint32_t* signs_dn;
+  int x_chunk, h_chunk;     // columns per rotation chunk of x and of h (whole blocks, <= 1024)
+  DecMat gate, up, down;
+  float* hbuf;              // h of this pass before rotation, fp32 [8 * NT][d_inter] (MLP only)
+  float* pieces1;           // split-K partial sums of the gate/up (or linear) decode
+  float* pieces3;           // same for down
+  int grid;                 // CTAs (all co-resident)
+  int grid1, max_pieces1;   // decode grid and piece slots per segment: gate/up (or linear)
+  int grid3, max_pieces3;   // same for down
+  unsigned* ctl;            // n_ctl counter words, zero before and after every launch
+  int n_ctl;
+  int off_g, off_hd, off_o; // word offsets: gate/up segment groups, h chunks (SwiGLU tasks
+                            // done), output segment groups; word 0 counts finished CTAs
+  int* status;              // workspace status word (3: a wait timed out)
+  uint16_t* out;            // row-major [*][d_model] (linear: [*][d_out])
+};
+
+int persist_grid(int nt);  // CTAs of the persistent kernel: resident CTAs per SM x SMs
+int persist_decode_grid(int d_in, int d_out, int n_mats, int grid);  // decoding CTAs (<= cells)
+int persist_max_pieces(int d_in, int d_out, int n_mats, int grid);
+int persist_chunk(int d, int block);  // rotation chunk: whole blocks, up to 1024 columns
+cudaError_t launch_persistent(const PersistArgs& a, int nt, cudaStream_t st);
+
 cudaError_t launch_fwht(const uint16_t* x, int rows, int n, int block, const uint32_t* signs,
                         uint16_t* out, cudaStream_t st);
 // Same rotation, written in fragment order (rows padded with zeros to 8 * n_tiles).
