@@ -29,9 +29,13 @@ from synth import inputs as S  # noqa: E402
 
 HIDDEN, INTER = S.HIDDEN, S.INTERMEDIATE
 BLOCK_BYTES = 3 * S.stream_bytes(HIDDEN, INTER) + 2 * (2 * INTER + HIDDEN) + 3 * 64 * 2 * 2  # 100,350,720
-GATE_UP_BYTES = 2 * S.stream_bytes(HIDDEN, INTER) + 2 * (2 * INTER) + 2 * 64 * 2 * 2
 FLOP_PER_ROW = 2 * (2 * HIDDEN * INTER + INTER * HIDDEN)  # 534,773,760
 METRIC = "VQ3 Hadamard-MLP rows/s; weight GB/s vs HBM peak @T=8; TFLOP/s @prefill"
+REF_BUDGET_S = 100.0
+# DRAM bytes (read + write) of one persistent_kernel launch at T=8, from the ncu capture
+# summarised in profiles/persistent_kernel_mlp_5120x17408_T8.md; None when the kernel has
+# changed since that capture.
+TRAFFIC_PER_LAUNCH = 103_720_704
 
 
 def peaks() -> dict:
@@ -45,6 +49,22 @@ def peaks() -> dict:
 
 def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def max_over_ranks(v: float, world: int, device=None) -> float:
+    """The largest of every rank's v (each rank passes its own); v itself when world == 1."""
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Units all ranks processed per second of the slowest rank (replicas: same work on each rank)."""
+    return world * units_per_rank / seconds
 
 
 def cpu_cores() -> dict:
@@ -65,37 +85,42 @@ def cpu_cores() -> dict:
 # ------------------------------------------------------------------ oracle (CPU baseline / reference arm)
 
 class OracleSample:
-    """A bounded sample of one block for the CPU oracle: each step computes
-    1/frac of every matrix's output channels (gate and up rows [0, I/frac),
-    down rows [0, H/frac)), i.e. 1/frac of one block's arithmetic, with both
-    rotations in full. The down rows read h' of the whole block, computed once
-    by the oracle at set-up (untimed). A step counts as rows/frac rows."""
+    """A bounded sample of one block for the CPU oracle. A step dequantises and
+    applies a fraction `f` of every matrix's output channels (gate and up rows
+    [0, n_gu), down rows [0, n_dn)) in FP64, as the oracle does for a whole
+    block. Both rotations (the oracle's explicit block-matrix products) and h for
+    the down rows are computed once at set-up, untimed. A step counts as
+    T * (its share of the block's three weight products' multiply-adds) rows."""
 
-    def __init__(self, rows: int, frac: int):
+    def __init__(self, rows: int, f: float):
         from oracle import vq3_oracle as O
         self.O = O
         self.wl = S.mlp_27b(seed=1, rows=rows)
-        self.frac = frac
         blk = self.wl.layers[0]
+        self.xr = O.rotate(self.wl.x.astype(np.float64), blk.gate.block, blk.gate.signs)
         g = O.linear_f64(self.wl.x, blk.gate)
         u = O.linear_f64(self.wl.x, blk.up)
-        self.h = O.silu(g) * u
+        self.hr = O.rotate(O.silu(g) * u, blk.down.block, blk.down.signs)
+        self.set_fraction(f)
+
+    def set_fraction(self, f: float):
+        self.n_gu = max(2, 2 * int(round(INTER * f / 2)))
+        self.n_dn = max(2, 2 * int(round(HIDDEN * f / 2)))
+        macs = 2 * self.n_gu * HIDDEN + self.n_dn * INTER
+        self.share = macs / (3 * HIDDEN * INTER)
 
     def step(self) -> float:
         O, blk = self.O, self.wl.layers[0]
-        n_gu, n_dn = INTER // self.frac, HIDDEN // self.frac
-        xr = O.rotate(self.wl.x.astype(np.float64), blk.gate.block, blk.gate.signs)
-        Wg = O.dense_weight(blk.gate.stream, blk.gate.codebook, blk.gate.scales, HIDDEN, INTER, rows=(0, n_gu))
-        Wu = O.dense_weight(blk.up.stream, blk.up.codebook, blk.up.scales, HIDDEN, INTER, rows=(0, n_gu))
-        _ = O.silu(xr @ Wg.T) * (xr @ Wu.T)
-        hr = O.rotate(self.h, blk.down.block, blk.down.signs)
-        Wd = O.dense_weight(blk.down.stream, blk.down.codebook, blk.down.scales, INTER, HIDDEN, rows=(0, n_dn))
-        _ = hr @ Wd.T
-        return self.wl.x.shape[0] / self.frac
+        Wg = O.dense_weight(blk.gate.stream, blk.gate.codebook, blk.gate.scales, HIDDEN, INTER, rows=(0, self.n_gu))
+        Wu = O.dense_weight(blk.up.stream, blk.up.codebook, blk.up.scales, HIDDEN, INTER, rows=(0, self.n_gu))
+        _ = O.silu(self.xr @ Wg.T) * (self.xr @ Wu.T)
+        Wd = O.dense_weight(blk.down.stream, blk.down.codebook, blk.down.scales, INTER, HIDDEN, rows=(0, self.n_dn))
+        _ = self.hr @ Wd.T
+        return self.wl.x.shape[0] * self.share
 
 
-def time_oracle(rows: int, frac: int, steps: int, warmup: int):
-    smp = OracleSample(rows, frac)
+def time_oracle(rows: int, f: float, steps: int, warmup: int):
+    smp = OracleSample(rows, f)
     for _ in range(warmup):
         smp.step()
     t0 = time.perf_counter()
@@ -103,7 +128,7 @@ def time_oracle(rows: int, frac: int, steps: int, warmup: int):
     for _ in range(steps):
         units += smp.step()
     dt = time.perf_counter() - t0
-    return units / dt, dt
+    return units / dt, dt, smp
 
 
 # ------------------------------------------------------------------ clocks
@@ -227,40 +252,32 @@ def _run_ours_on(args, torch, vq3, dev, stream, rows, sets, x_host, x, out, ws, 
             graphs[i % n_sets].replay()
         e1.record(stream)
         barrier()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     ms_per_step = ms / steps
-    value = world * rows * steps / (ms / 1e3)
+    value = whole_job_rate(rows * steps, world, ms / 1e3)
 
-    # dominant kernel: the gate/up half (rotate x + gate/up gemv), timed alone with events
-    # on the launching stream, cycling weight sets like the main loop
-    ga = torch.cuda.Event(enable_timing=True)
-    gb = torch.cuda.Event(enable_timing=True)
-    gu_ms = 0.0
-    n_gu = 0
-    for i in range(3 * n_sets):
+    # dominant kernel: the block's one launch (persistent_kernel), each launch bracketed by
+    # events on the launching stream, cycling weight sets like the main loop; median of 60
+    durs = []
+    for i in range(n_sets + 60):
+        ga = torch.cuda.Event(enable_timing=True)
+        gb = torch.cuda.Event(enable_timing=True)
         ga.record(stream)
-        vq3.mlp_gate_up(x, sets[i % n_sets], ws, stream)
+        vq3.mlp_forward(x, sets[i % n_sets], out=out, ws=ws, stream=stream)
         gb.record(stream)
-        vq3.mlp_down(rows, sets[i % n_sets], out, ws, stream)
         gb.synchronize()
         if i >= n_sets:
-            gu_ms += ga.elapsed_time(gb)
-            n_gu += 1
-    gu_ms /= n_gu
+            durs.append(ga.elapsed_time(gb))
+    k_ms = float(np.median(durs))
     pk = peaks()
-    achieved = GATE_UP_BYTES / (gu_ms / 1e3) / 1e9
-    roofline = {"bound": "hbm", "kernel": "vq3 gate/up half (rotate x + gate/up GEMM, SiLU*mul)",
+    achieved = BLOCK_BYTES / (k_ms / 1e3) / 1e9
+    traffic = args.traffic if args.traffic is not None else TRAFFIC_PER_LAUNCH
+    roofline = {"bound": "hbm", "kernel": "persistent_kernel (whole MLP block, one launch)",
                 "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": args.traffic,
-                "peak_source": pk["source"], "ms_per_launch": round(gu_ms, 5),
-                "algorithmic_bytes_per_launch": GATE_UP_BYTES,
-                "block_weight_gbs": round(BLOCK_BYTES / (ms_per_step / 1e3) / 1e9, 1),
-                "block_frac_of_hbm": round(BLOCK_BYTES / (ms_per_step / 1e3) / 1e9 / pk["hbm_gbs"], 4)}
+                "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic,
+                "peak_source": f"{pk['source']} (HBM copy, burst)", "ms_per_launch": round(k_ms, 5),
+                "algorithmic_bytes_per_launch": BLOCK_BYTES,
+                "block_weight_gbs_timed_loop": round(BLOCK_BYTES / (ms_per_step / 1e3) / 1e9, 1)}
 
     # end to end through the host-buffer entry point (copies in the timed region)
     hws = vq3.workspace(vq3.mlp_host_workspace_bytes(rows, sets[0]), dev, stream)
@@ -273,13 +290,8 @@ def _run_ours_on(args, torch, vq3, dev, stream, rows, sets, x_host, x, out, ws, 
     t0 = time.perf_counter()
     for i in range(e2e_steps):
         vq3.mlp_forward_host(xh, sets[i % n_sets], hws, out=yh, stream=stream)
-    dt = time.perf_counter() - t0
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([dt], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dt = float(t.item())
-    e2e = {"value": round(world * rows * e2e_steps / dt, 1), "unit": "rows/s",
+    dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+    e2e = {"value": round(whole_job_rate(rows * e2e_steps, world, dt), 1), "unit": "rows/s",
            "h2d_bytes_per_step": int(x_host.nbytes), "d2h_bytes_per_step": int(rows * HIDDEN * 2),
            "api": "vq3_mlp_forward_host (pageable->pinned host buffers)"}
 
@@ -303,12 +315,13 @@ def _run_ours_on(args, torch, vq3, dev, stream, rows, sets, x_host, x, out, ws, 
         if extra:
             line["prefill_sweep"] = extra
         if world == 1 and not args.no_cpu_baseline:
-            rate, dt = time_oracle(rows, args.oracle_frac, args.oracle_steps, 1)
+            rate, dt, smp = time_oracle(rows, 1.0 / args.oracle_frac, args.oracle_steps, 1)
             line["cpu_baseline"] = {"value": round(rate, 3), "unit": "rows/s", "cores": cpu_cores(),
                                     "kind": "oracle",
-                                    "sample": f"{args.oracle_steps} oracle samples of 1/{args.oracle_frac} of the "
-                                              f"block's intermediate channels at T={rows} ({dt:.1f} s), "
-                                              f"scaled to whole rows"}
+                                    "sample": f"{args.oracle_steps} oracle steps at T={rows}, each {smp.n_gu} gate "
+                                              f"and up channels and {smp.n_dn} down channels "
+                                              f"({smp.share:.4f} of the block's multiply-adds; rotations untimed), "
+                                              f"{dt:.1f} s, scaled to whole rows"}
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -348,9 +361,16 @@ def run_reference(args) -> dict | None:
     if rank != 0:
         return None
     rows = args.rows
-    rate, dt = time_oracle(rows, args.oracle_frac, args.steps, args.warmup)
-    sample = (f"each step: oracle on 1/{args.oracle_frac} of one block's intermediate channels at T={rows}, "
-              f"scaled to whole rows")
+    # size each step so that warm-up + timed steps take about REF_BUDGET_S of host time
+    smp = OracleSample(rows, 1.0 / 64)
+    t0 = time.perf_counter()
+    smp.step()
+    t64 = time.perf_counter() - t0
+    per_step = REF_BUDGET_S / (args.steps + args.warmup)
+    f = min(0.25, max(1e-6, per_step / t64 / 64))
+    rate, dt, smp = time_oracle(rows, f, args.steps, args.warmup)
+    sample = (f"each step: {smp.n_gu} gate and up channels and {smp.n_dn} down channels of one block at T={rows} "
+              f"({smp.share:.6f} of its multiply-adds, FP64; rotations untimed), scaled to whole rows")
     return {"impl": "reference", "metric": METRIC, "value": round(rate, 3), "unit": "rows/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -370,8 +390,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="skip the prefill sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--oracle-frac", type=int, default=16)
-    ap.add_argument("--oracle-steps", type=int, default=8)
+    ap.add_argument("--oracle-frac", type=int, default=8)
+    ap.add_argument("--oracle-steps", type=int, default=32)
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture, if current")
     args = ap.parse_args()

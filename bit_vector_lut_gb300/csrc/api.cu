@@ -53,24 +53,15 @@ int check_linear(const vq3_linear* L, const char* name) {
 }
 
 // ---- workspace carving ----------------------------------------------------
-//
-// [status word (256 B)][rotated input, fragment order][h' fragment order (MLP
-// only)][split-K pieces][counter words, kept zero]
 
-// Row tiles of a fragment-order buffer for `rows` rows: whole passes.
-int frag_tiles(int rows) {
-  const int per = dec_tiles_per_pass(rows);
-  const int tiles = row_tiles(rows);
-  return (tiles + per - 1) / per * per;
-}
+// Row tiles per pass of the persistent kernel for `rows` rows, passes of at
+// most `pass_cap` rows (8, 16 or 32).
+int pass_tiles(int rows, int pass_cap) { return dec_tiles_per_pass(rows < pass_cap ? rows : pass_cap); }
 
-size_t frag_bytes(int rows, int n) { return (size_t)frag_tiles(rows) * (n / 64) * 1024; }
-
-// Pieces of one decode pass of the multi-kernel path (the MLP halves).
-size_t multi_pieces_bytes(int rows, int d_in, int d_out, int n_mats) {
-  const size_t piece = (size_t)512 * dec_tiles_per_pass(rows) * sizeof(float);
-  const size_t n_seg = (size_t)(d_out / kSuChannels) * n_mats;
-  return n_seg * dec_max_pieces(d_in, d_out, n_mats, dec_grid(d_in, d_out, n_mats)) * piece;
+// Passes of the persistent kernel for `rows` rows.
+int passes(int rows, int pass_cap) {
+  const int per = 8 * pass_tiles(rows, pass_cap);
+  return (rows + per - 1) / per;
 }
 
 // Pieces of one decode step of the persistent kernel.
@@ -123,28 +114,20 @@ LinearWs linear_ws(int rows, int d_in, int d_out) {
   return w;
 }
 
-// [status word][x' fragments][h' fragments][h fp32][pieces of the halves]
-// [gate/up pieces][down pieces][counter words, zero between calls]
+// [status word (256 B)][h of one pass, fp32][gate/up pieces][down pieces]
+// [counter words, zero between calls]
 struct MlpWs {
-  size_t status, xf, hf, hbuf, pieces, pieces1, pieces3, counters, total;
+  size_t status, hbuf, pieces1, pieces3, counters, total;
 };
 
 MlpWs mlp_ws(int rows, const vq3_mlp_layer* l) {
   MlpWs w{};
   const int H = l->gate.d_in, I = l->gate.d_out;
-  const size_t p_gu = multi_pieces_bytes(rows, H, I, 2);
-  const size_t p_dn = multi_pieces_bytes(rows, I, H, 1);
   size_t off = 0;
   w.status = off;
   off += 256;
-  w.xf = off;
-  off = round_up(off + frag_bytes(rows, H), 256);
-  w.hf = off;
-  off = round_up(off + frag_bytes(rows, I), 256);
   w.hbuf = off;
   off = round_up(off + (size_t)8 * dec_tiles_per_pass(rows) * I * sizeof(float), 256);
-  w.pieces = off;
-  off = round_up(off + (p_gu > p_dn ? p_gu : p_dn), 256);
   w.pieces1 = off;
   off = round_up(off + persist_pieces_bytes(rows, H, I, 2), 256);
   w.pieces3 = off;
@@ -178,86 +161,6 @@ DecMat dec_mat(const vq3_linear& L) {
   return m;
 }
 
-DecArgs decode_args(const uint32_t* xf, int tiles, int d_in, int d_out, int n_mats, const vq3_linear* mats,
-                    float* pieces, int* status) {
-  DecArgs a{};
-  a.xfrag = xf;
-  a.n_tiles = tiles;
-  a.d_in = d_in;
-  a.d_out = d_out;
-  a.n_mats = n_mats;
-  for (int i = 0; i < n_mats; ++i) a.mats[i] = dec_mat(mats[i]);
-  a.pieces = pieces;
-  a.grid = dec_grid(d_in, d_out, n_mats);
-  a.max_pieces = dec_max_pieces(d_in, d_out, n_mats, a.grid);
-  a.ksplit = dec_ksplit(d_in, d_out, n_mats);
-  a.status = status;
-  return a;
-}
-
-PieceMap piece_map(const DecArgs& d, int nt) {
-  PieceMap pm{};
-  pm.pieces = d.pieces;
-  pm.n_kg = d.d_in / kSuInputs;
-  pm.n_mats = d.n_mats;
-  pm.n_groups = dec_groups(d.d_in, d.d_out, d.n_mats);
-  pm.seg_per_group = kDecWarps / d.ksplit;
-  pm.grid = d.grid;
-  pm.max_pieces = d.max_pieces;
-  pm.nt = nt;
-  return pm;
-}
-
-// h' = R_d(silu(W_g R_g x) * (W_u R_g x)) in fragment order, all rows.
-cudaError_t run_gate_up(const uint16_t* x, int rows, const vq3_mlp_layer& l, uint32_t* xf, uint32_t* hf,
-                        float* pieces, int* status, cudaStream_t st) {
-  const int tiles = frag_tiles(rows);
-  cudaError_t e = launch_fwht_frag(x, rows, l.gate.d_in, l.gate.block, l.gate.signs, xf, tiles, st);
-  if (e != cudaSuccess) return e;
-  const vq3_linear gu[2] = {l.gate, l.up};
-  DecArgs d = decode_args(xf, tiles, l.gate.d_in, l.gate.d_out, 2, gu, pieces, status);
-  const int per = dec_tiles_per_pass(rows);
-  for (int nt0 = 0; nt0 < tiles; nt0 += per) {
-    d.nt0 = nt0;
-    if ((e = launch_decode(d, per, st)) != cudaSuccess) return e;
-    SwigluRotateArgs c{};
-    c.pm = piece_map(d, per);
-    c.scale_gate = l.gate.scales;
-    c.scale_up = l.up.scales;
-    c.d_inter = l.gate.d_out;
-    c.row0 = nt0 * 8;
-    c.rows = rows - c.row0 < per * 8 ? rows - c.row0 : per * 8;
-    c.block = l.down.block;
-    c.signs = l.down.signs;
-    c.hfrag = hf;
-    c.n_tiles = tiles;
-    if ((e = launch_swiglu_rotate(c, st)) != cudaSuccess) return e;
-  }
-  return cudaSuccess;
-}
-
-// out = fp16(s_d * W_d h') for all rows, h' in fragment order.
-cudaError_t run_down(const uint32_t* hf, int rows, const vq3_mlp_layer& l, float* pieces, int* status, uint16_t* out,
-                     cudaStream_t st) {
-  const int tiles = frag_tiles(rows);
-  DecArgs d = decode_args(hf, tiles, l.down.d_in, l.down.d_out, 1, &l.down, pieces, status);
-  const int per = dec_tiles_per_pass(rows);
-  for (int nt0 = 0; nt0 < tiles; nt0 += per) {
-    d.nt0 = nt0;
-    cudaError_t e = launch_decode(d, per, st);
-    if (e != cudaSuccess) return e;
-    LinearOutArgs o{};
-    o.pm = piece_map(d, per);
-    o.scales = l.down.scales;
-    o.d_out = l.down.d_out;
-    o.row0 = nt0 * 8;
-    o.rows = rows - o.row0 < per * 8 ? rows - o.row0 : per * 8;
-    o.out = out;
-    if ((e = launch_linear_out(o, st)) != cudaSuccess) return e;
-  }
-  return cudaSuccess;
-}
-
 // The persistent kernel over all rows, one launch per pass of 8/16/32 rows.
 // `layer` null: a single linear layer L.
 struct PersistBufs {
@@ -266,9 +169,8 @@ struct PersistBufs {
   int* status;
 };
 
-cudaError_t run_persistent(const uint16_t* x, int rows, const vq3_mlp_layer* layer, const vq3_linear* L,
+cudaError_t run_persistent(const uint16_t* x, int rows, int nt, const vq3_mlp_layer* layer, const vq3_linear* L,
                            const PersistBufs& b, uint16_t* out, cudaStream_t st) {
-  const int nt = dec_tiles_per_pass(rows);
   PersistArgs a{};
   a.x = x;
   a.hbuf = b.hbuf;
@@ -373,8 +275,8 @@ int device_sm_count() {
   return cache[dev];
 }
 
-void mlp_counter_range(int rows, const vq3_mlp_layer* layer, size_t* offset, size_t* bytes) {
-  const MlpWs w = mlp_ws(rows, layer);
+void mlp_counter_range(int rows, int pass_cap, const vq3_mlp_layer* layer, size_t* offset, size_t* bytes) {
+  const MlpWs w = mlp_ws(rows < pass_cap ? rows : pass_cap, layer);
   *offset = w.counters;
   *bytes = w.total - w.counters;
 }
@@ -514,7 +416,7 @@ int vq3_linear_forward(const uint16_t* x, int rows, const vq3_linear* L, uint16_
   b.pieces1 = reinterpret_cast<float*>(ws + w.pieces);
   b.ctl = reinterpret_cast<unsigned*>(ws + w.counters);
   b.status = reinterpret_cast<int*>(ws + w.status);
-  cudaError_t e = run_persistent(x, rows, nullptr, L, b, out, st);
+  cudaError_t e = run_persistent(x, rows, dec_tiles_per_pass(rows), nullptr, L, b, out, st);
   if (e != cudaSuccess) return cuda_fail(e, "linear: launch");
   return ok();
 }
@@ -528,8 +430,8 @@ struct MlpCall {
   cudaStream_t st;
 };
 
-MlpCall mlp_prepare(int rows, const vq3_mlp_layer* layer, void* workspace, size_t ws_bytes, void* stream,
-                    const char* name) {
+MlpCall mlp_prepare(int rows, int pass_cap, const vq3_mlp_layer* layer, void* workspace, size_t ws_bytes,
+                    void* stream, const char* name) {
   MlpCall c{};
   c.rc = check_mlp(layer);
   if (c.rc) return c;
@@ -546,7 +448,7 @@ MlpCall mlp_prepare(int rows, const vq3_mlp_layer* layer, void* workspace, size_
     c.rc = fail(VQ3_EALIGN, "%s: workspace must be 256-byte aligned", name);
     return c;
   }
-  c.w = mlp_ws(rows, layer);
+  c.w = mlp_ws(rows < pass_cap ? rows : pass_cap, layer);
   if (ws_bytes < c.w.total) {
     c.rc = fail(VQ3_ENOSPACE, "%s: workspace %zu < %zu bytes", name, ws_bytes, c.w.total);
     return c;
@@ -556,27 +458,20 @@ MlpCall mlp_prepare(int rows, const vq3_mlp_layer* layer, void* workspace, size_
   return c;
 }
 
-int gate_up_half(const uint16_t* x, int rows, const vq3_mlp_layer* layer, const MlpCall& c) {
-  cudaError_t e = run_gate_up(x, rows, *layer, reinterpret_cast<uint32_t*>(c.ws + c.w.xf),
-                              reinterpret_cast<uint32_t*>(c.ws + c.w.hf), reinterpret_cast<float*>(c.ws + c.w.pieces),
-                              reinterpret_cast<int*>(c.ws + c.w.status), c.st);
-  if (e != cudaSuccess) return cuda_fail(e, "mlp: gate/up launch");
-  return VQ3_OK;
-}
-
-int down_half(int rows, const vq3_mlp_layer* layer, uint16_t* out, const MlpCall& c) {
-  cudaError_t e = run_down(reinterpret_cast<const uint32_t*>(c.ws + c.w.hf), rows, *layer,
-                           reinterpret_cast<float*>(c.ws + c.w.pieces), reinterpret_cast<int*>(c.ws + c.w.status), out,
-                           c.st);
-  if (e != cudaSuccess) return cuda_fail(e, "mlp: down launch");
-  return VQ3_OK;
-}
-
 }  // namespace
 
-int vq3_mlp_forward(const uint16_t* x, int rows, const vq3_mlp_layer* layer, uint16_t* out, void* workspace,
-                    size_t ws_bytes, void* stream) {
-  MlpCall c = mlp_prepare(rows, layer, workspace, ws_bytes, stream, "mlp");
+}  // extern "C"
+
+namespace vq3 {
+
+size_t mlp_workspace_bytes_capped(int rows, const vq3_mlp_layer* layer, int pass_cap) {
+  if (!layer || rows < 0 || !layout_supported(layer->gate.d_in, layer->gate.d_out)) return 0;
+  return mlp_ws(rows < pass_cap ? rows : pass_cap, layer).total;
+}
+
+int mlp_forward_capped(const uint16_t* x, int rows, const vq3_mlp_layer* layer, uint16_t* out, void* workspace,
+                       size_t ws_bytes, void* stream, int pass_cap) {
+  MlpCall c = mlp_prepare(rows, pass_cap, layer, workspace, ws_bytes, stream, "mlp");
   if (c.rc || rows == 0) return c.rc ? c.rc : ok();
   if (!x || !out) return fail(VQ3_EINVAL, "mlp: null x/out");
   if (!aligned(x, 16) || !aligned(out, 16)) return fail(VQ3_EALIGN, "mlp: x/out must be 16-byte aligned");
@@ -586,35 +481,24 @@ int vq3_mlp_forward(const uint16_t* x, int rows, const vq3_mlp_layer* layer, uin
   b.pieces3 = reinterpret_cast<float*>(c.ws + c.w.pieces3);
   b.ctl = reinterpret_cast<unsigned*>(c.ws + c.w.counters);
   b.status = reinterpret_cast<int*>(c.ws + c.w.status);
-  cudaError_t e = run_persistent(x, rows, layer, nullptr, b, out, c.st);
+  cudaError_t e = run_persistent(x, rows, pass_tiles(rows, pass_cap), layer, nullptr, b, out, c.st);
   if (e != cudaSuccess) return cuda_fail(e, "mlp: launch");
   return ok();
 }
 
-int vq3_mlp_gate_up(const uint16_t* x, int rows, const vq3_mlp_layer* layer, void* workspace, size_t ws_bytes,
-                    void* stream) {
-  MlpCall c = mlp_prepare(rows, layer, workspace, ws_bytes, stream, "mlp_gate_up");
-  if (c.rc || rows == 0) return c.rc ? c.rc : ok();
-  if (!x) return fail(VQ3_EINVAL, "mlp_gate_up: null x");
-  if (!aligned(x, 16)) return fail(VQ3_EALIGN, "mlp_gate_up: x must be 16-byte aligned");
-  int rc = gate_up_half(x, rows, layer, c);
-  return rc ? rc : ok();
-}
+}  // namespace vq3
 
-int vq3_mlp_down(int rows, const vq3_mlp_layer* layer, uint16_t* out, void* workspace, size_t ws_bytes,
-                 void* stream) {
-  MlpCall c = mlp_prepare(rows, layer, workspace, ws_bytes, stream, "mlp_down");
-  if (c.rc || rows == 0) return c.rc ? c.rc : ok();
-  if (!out) return fail(VQ3_EINVAL, "mlp_down: null out");
-  if (!aligned(out, 16)) return fail(VQ3_EALIGN, "mlp_down: out must be 16-byte aligned");
-  int rc = down_half(rows, layer, out, c);
-  return rc ? rc : ok();
+extern "C" {
+
+int vq3_mlp_forward(const uint16_t* x, int rows, const vq3_mlp_layer* layer, uint16_t* out, void* workspace,
+                    size_t ws_bytes, void* stream) {
+  return mlp_forward_capped(x, rows, layer, out, workspace, ws_bytes, stream, 32);
 }
 
 int vq3_mlp_kernel_launches(int rows, const vq3_mlp_layer* layer) {
   if (check_mlp(layer) || rows < 0) return -1;
   if (rows == 0) return 0;
-  return frag_tiles(rows) / dec_tiles_per_pass(rows);  // one persistent kernel per row pass
+  return passes(rows, 32);  // one persistent kernel per pass of 8, 16 or 32 rows
 }
 
 size_t vq3_mlp_host_workspace_bytes(int rows, const vq3_mlp_layer* layer) {

@@ -51,23 +51,32 @@ extern "C" int vq3_mlp_forward_noalloc(const uint16_t* x, int rows, const vq3_ml
   int rc = mlp_validate(x, rows, layer, out);
   if (rc) return rc;
   if (rows == 0) return set_error(VQ3_OK, "");
-  const size_t need = vq3_mlp_workspace_bytes(rows, layer);
-  if (need > kNoAllocScratchBytes)
+  // the largest pass (32, 16 or 8 rows) whose scratch fits the array; more rows run as more passes
+  int cap = 0;
+  size_t need = 0;
+  for (int c = 32; c >= 8; c /= 2) {
+    need = mlp_workspace_bytes_capped(rows, layer, c);
+    if (need <= kNoAllocScratchBytes) {
+      cap = c;
+      break;
+    }
+  }
+  if (!cap)
     return set_error(VQ3_ENOSPACE,
-                     "mlp_noalloc: %d rows of a %d/%d block need %zu bytes of scratch, more than the fixed "
-                     "%zu-byte array (VQ3_NOALLOC_SCRATCH_BYTES); use vq3_mlp_forward with a workspace",
-                     rows, layer->gate.d_in, layer->gate.d_out, need, kNoAllocScratchBytes);
+                     "mlp_noalloc: a %d/%d block needs %zu bytes of scratch even in 8-row passes, more than "
+                     "the fixed %zu-byte array (VQ3_NOALLOC_SCRATCH_BYTES); use vq3_mlp_forward with a workspace",
+                     layer->gate.d_in, layer->gate.d_out, need, kNoAllocScratchBytes);
   void* scratch = nullptr;
   cudaError_t e = scratch_address(&scratch);
   if (e != cudaSuccess)
     return set_error(VQ3_ECUDA, "mlp_noalloc: cudaGetSymbolAddress: %s (%s)", cudaGetErrorName(e),
                      cudaGetErrorString(e));
-  // The array keeps the previous call's contents; the arrival counters must start at zero.
+  // The array keeps the previous call's contents; the counter words must start at zero.
   size_t off = 0, bytes = 0;
-  mlp_counter_range(rows, layer, &off, &bytes);
+  mlp_counter_range(rows, cap, layer, &off, &bytes);
   e = cudaMemsetAsync(static_cast<char*>(scratch) + off, 0, bytes, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess)
     return set_error(VQ3_ECUDA, "mlp_noalloc: clearing counters: %s (%s)", cudaGetErrorName(e),
                      cudaGetErrorString(e));
-  return vq3_mlp_forward(x, rows, layer, out, scratch, kNoAllocScratchBytes, stream);
+  return mlp_forward_capped(x, rows, layer, out, scratch, kNoAllocScratchBytes, stream, cap);
 }

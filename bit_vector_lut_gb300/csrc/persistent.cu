@@ -796,6 +796,8 @@ int occupancy() {
 
 }  // namespace
 
+int dec_tiles_per_pass(int rows) { return rows <= 8 ? 1 : (rows <= 16 ? 2 : 4); }
+
 int persist_grid(int nt) {
   static int cache[64][3] = {};
   int dev = 0;

@@ -24,13 +24,10 @@ constexpr int kRotThreads = 128;
 // block is in "lane-major" form. Butterflies of stride h < 32 pair lanes within
 // a warp (shuffle), strides 32 and 64 pair warps (shared memory), strides >= 128
 // pair slots of the same thread (registers).
-// FRAG = false: out[row][col] row-major (may alias x). FRAG = true: out is the
-// fragment-order buffer of the decode kernel (n_tiles row tiles); rows at or past
-// `rows` are written as zeros without reading x.
-template <int B, bool FRAG>
-__global__ void __launch_bounds__(kRotThreads) fwht_kernel(const uint16_t* __restrict__ x, int n, int rows,
-                                                            const uint32_t* __restrict__ signs,
-                                                            uint16_t* out, float scale, int n_tiles) {
+// out[row][col] row-major (may alias x: every element is read before any is written).
+template <int B>
+__global__ void __launch_bounds__(kRotThreads) fwht_kernel(const uint16_t* x, int n, const uint32_t* __restrict__ signs,
+                                                            uint16_t* out, float scale) {
   constexpr int V = (B + kRotThreads - 1) / kRotThreads;  // values per thread
   constexpr int ACTIVE = B < kRotThreads ? B : kRotThreads;
   __shared__ float sm[V * kRotThreads];
@@ -40,16 +37,12 @@ __global__ void __launch_bounds__(kRotThreads) fwht_kernel(const uint16_t* __res
   const int blk = blockIdx.x % blocks_per_row;
   const size_t base = (size_t)row * n + (size_t)blk * B;
 
-  // Programmatic dependent launch: the input may come from the previous kernel.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;");
-  const bool live = row < rows;  // uniform per CTA
   float v[V];
 #pragma unroll
   for (int s = 0; s < V; ++s) {
     const int j = s * kRotThreads + tid;
     float f = 0.f;
-    if (tid < ACTIVE && live) {
+    if (tid < ACTIVE) {
       f = __half2float(__ushort_as_half(x[base + j]));
       if (signs) {
         const int col = blk * B + j;
@@ -97,38 +90,14 @@ __global__ void __launch_bounds__(kRotThreads) fwht_kernel(const uint16_t* __res
 #pragma unroll
   for (int s = 0; s < V; ++s) {
     const int j = s * kRotThreads + tid;
-    if (tid < ACTIVE) {
-      const uint16_t hv = __half_as_ushort(__float2half_rn(v[s] * scale));
-      if constexpr (FRAG) {
-        out[frag_half_index(row, blk * B + j, n_tiles)] = hv;
-      } else {
-        out[base + j] = hv;
-      }
-    }
+    if (tid < ACTIVE) out[base + j] = __half_as_ushort(__float2half_rn(v[s] * scale));
   }
 }
 
 template <int B>
-cudaError_t launch_b(const uint16_t* x, int rows, int n, const uint32_t* signs, uint16_t* out, int n_tiles,
-                     cudaStream_t st) {
-  const float scale = 1.0f / sqrtf((float)B);
-  if (n_tiles > 0) {
-    const long long grid = (long long)n_tiles * 8 * (n / B);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kRotThreads);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, fwht_kernel<B, true>, x, n, rows, signs, out, scale, n_tiles);
-    if (e != cudaSuccess) return e;
-  } else {
-    const long long grid = (long long)rows * (n / B);
-    fwht_kernel<B, false><<<(unsigned)grid, kRotThreads, 0, st>>>(x, n, rows, signs, out, scale, 0);
-  }
+cudaError_t launch_b(const uint16_t* x, int rows, int n, const uint32_t* signs, uint16_t* out, cudaStream_t st) {
+  const long long grid = (long long)rows * (n / B);
+  fwht_kernel<B><<<(unsigned)grid, kRotThreads, 0, st>>>(x, n, signs, out, 1.0f / sqrtf((float)B));
   return cudaGetLastError();
 }
 
@@ -164,18 +133,18 @@ __global__ void __launch_bounds__(256) residual_rmsnorm_kernel(uint16_t* resid, 
 
 namespace {
 cudaError_t launch_any(const uint16_t* x, int rows, int n, int block, const uint32_t* signs, uint16_t* out,
-                       int n_tiles, cudaStream_t st) {
+                       cudaStream_t st) {
   switch (block) {
-    case 2: return launch_b<2>(x, rows, n, signs, out, n_tiles, st);
-    case 4: return launch_b<4>(x, rows, n, signs, out, n_tiles, st);
-    case 8: return launch_b<8>(x, rows, n, signs, out, n_tiles, st);
-    case 16: return launch_b<16>(x, rows, n, signs, out, n_tiles, st);
-    case 32: return launch_b<32>(x, rows, n, signs, out, n_tiles, st);
-    case 64: return launch_b<64>(x, rows, n, signs, out, n_tiles, st);
-    case 128: return launch_b<128>(x, rows, n, signs, out, n_tiles, st);
-    case 256: return launch_b<256>(x, rows, n, signs, out, n_tiles, st);
-    case 512: return launch_b<512>(x, rows, n, signs, out, n_tiles, st);
-    case 1024: return launch_b<1024>(x, rows, n, signs, out, n_tiles, st);
+    case 2: return launch_b<2>(x, rows, n, signs, out, st);
+    case 4: return launch_b<4>(x, rows, n, signs, out, st);
+    case 8: return launch_b<8>(x, rows, n, signs, out, st);
+    case 16: return launch_b<16>(x, rows, n, signs, out, st);
+    case 32: return launch_b<32>(x, rows, n, signs, out, st);
+    case 64: return launch_b<64>(x, rows, n, signs, out, st);
+    case 128: return launch_b<128>(x, rows, n, signs, out, st);
+    case 256: return launch_b<256>(x, rows, n, signs, out, st);
+    case 512: return launch_b<512>(x, rows, n, signs, out, st);
+    case 1024: return launch_b<1024>(x, rows, n, signs, out, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -183,12 +152,7 @@ cudaError_t launch_any(const uint16_t* x, int rows, int n, int block, const uint
 
 cudaError_t launch_fwht(const uint16_t* x, int rows, int n, int block, const uint32_t* signs,
                         uint16_t* out, cudaStream_t st) {
-  return launch_any(x, rows, n, block, signs, out, 0, st);
-}
-
-cudaError_t launch_fwht_frag(const uint16_t* x, int rows, int n, int block, const uint32_t* signs,
-                             uint32_t* xfrag, int n_tiles, cudaStream_t st) {
-  return launch_any(x, rows, n, block, signs, reinterpret_cast<uint16_t*>(xfrag), n_tiles, st);
+  return launch_any(x, rows, n, block, signs, out, st);
 }
 
 cudaError_t launch_residual_rmsnorm(uint16_t* resid, const uint16_t* delta, int rows, int n, float eps,

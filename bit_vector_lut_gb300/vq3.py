@@ -52,8 +52,6 @@ def _load() -> ctypes.CDLL:
         "vq3_workspace_status": (c_int, [c_void_p, POINTER(c_int), c_void_p]),
         "vq3_linear_forward": (c_int, [c_void_p, c_int, POINTER(vq3_linear), c_void_p, c_void_p, c_size_t, c_void_p]),
         "vq3_mlp_forward": (c_int, [c_void_p, c_int, POINTER(vq3_mlp_layer), c_void_p, c_void_p, c_size_t, c_void_p]),
-        "vq3_mlp_gate_up": (c_int, [c_void_p, c_int, POINTER(vq3_mlp_layer), c_void_p, c_size_t, c_void_p]),
-        "vq3_mlp_down": (c_int, [c_int, POINTER(vq3_mlp_layer), c_void_p, c_void_p, c_size_t, c_void_p]),
         "vq3_mlp_kernel_launches": (c_int, [c_int, POINTER(vq3_mlp_layer)]),
         "vq3_mlp_host_workspace_bytes": (c_size_t, [c_int, POINTER(vq3_mlp_layer)]),
         "vq3_mlp_forward_host": (c_int, [c_void_p, c_int, POINTER(vq3_mlp_layer), c_void_p, c_void_p, c_size_t,
@@ -227,17 +225,6 @@ def mlp_forward(x: torch.Tensor, layer: MLP, out=None, ws=None, stream=None) -> 
         ws = workspace(mlp_workspace_bytes(rows, layer), x.device, stream)
     _check(lib.vq3_mlp_forward(x.data_ptr(), rows, ctypes.byref(layer.struct), out.data_ptr(), ws.data_ptr(),
                                ws.numel(), _stream(stream)))
-    return out
-
-
-def mlp_gate_up(x: torch.Tensor, layer: MLP, ws: torch.Tensor, stream=None) -> None:
-    _check(lib.vq3_mlp_gate_up(x.data_ptr(), x.shape[0], ctypes.byref(layer.struct), ws.data_ptr(), ws.numel(),
-                               _stream(stream)))
-
-
-def mlp_down(rows: int, layer: MLP, out: torch.Tensor, ws: torch.Tensor, stream=None) -> torch.Tensor:
-    _check(lib.vq3_mlp_down(rows, ctypes.byref(layer.struct), out.data_ptr(), ws.data_ptr(), ws.numel(),
-                            _stream(stream)))
     return out
 
 

@@ -125,15 +125,18 @@ VQ3_API int fwht_rotate(const uint16_t* x, int rows, int n, int block, const uin
                 uint16_t* out, void* stream);
 
 /*
- * Workspace for vq3_linear_forward / vq3_mlp_forward at `rows` rows. The
- * workspace holds a device status word, the rotated activations, split-K
- * partial sums and arrival counters. It must be zero-filled once before its
- * first use (vq3_workspace_init); every completed call leaves the counters at
- * zero again. Calls that share a workspace must not overlap on the GPU (same
+ * Workspace for vq3_linear_forward / vq3_mlp_forward at `rows` rows. It holds
+ * a device status word, h of one pass of up to 32 rows (MLP), the split-K
+ * partial sums of both decode steps and the counters through which the steps
+ * of one launch hand over. It must be zero-filled once before its first use
+ * (vq3_workspace_init); every completed call leaves the counters at zero
+ * again. Calls that share a workspace must not overlap on the GPU (same
  * stream, or ordered by events).
- * Device status: the first 32-bit word of the workspace stays 0 unless a
- * kernel found an internal invariant broken (then nonzero; the outputs of that
- * call are invalid).
+ * Device status: the first 32-bit word of the workspace stays 0. It becomes 3
+ * if a wait inside a kernel gave up after its bounded number of polls (about
+ * a second); the kernel still ends, the outputs of that call are invalid, and
+ * later calls on the workspace skip their waits until vq3_workspace_init
+ * clears the word.
  * vq3_workspace_status copies it to the host after the stream's prior work.
  */
 VQ3_API size_t vq3_linear_workspace_bytes(int rows, const vq3_linear* L);
@@ -151,8 +154,10 @@ VQ3_API int vq3_linear_forward(const uint16_t* x, int rows, const vq3_linear* L,
 
 /*
  * One SwiGLU MLP block with online rotations on both inputs:
- *   h   = silu(W_g R_g x) * (W_u R_g x)      (FP32, stored as FP16)
- *   out = fp16( W_d R_d h )
+ *   h   = silu(W_g R_g x) * (W_u R_g x)      (FP32)
+ *   out = fp16( W_d R_d h )                  (R_d h rounded to FP16 once, as the MMA operand)
+ * One cooperative kernel per pass of up to 8, 16 or 32 rows; all of its CTAs
+ * are resident at once and hand over between steps through workspace counters.
  * Cited: model card "anemll/anemll-forge-qwen3.8-27B", "Release 0.2" table row
  * "MLP gate / up / down" and bullets; "ANEMLL ANE LLM conversion pipeline",
  * "Facts" (SiLU form).
@@ -162,20 +167,8 @@ VQ3_API int vq3_linear_forward(const uint16_t* x, int rows, const vq3_linear* L,
 VQ3_API int vq3_mlp_forward(const uint16_t* x, int rows, const vq3_mlp_layer* layer, uint16_t* out,
                     void* workspace, size_t ws_bytes, void* stream);
 
-/*
- * The two halves of vq3_mlp_forward, for callers that schedule or time them
- * separately (same workspace, same stream order):
- *   vq3_mlp_gate_up: h = silu(W_g R_g x) * (W_u R_g x), kept in the workspace;
- *   vq3_mlp_down:    out = fp16( W_d R_d h ), h read from the workspace.
- * Calling gate_up then down equals one vq3_mlp_forward, bit for bit.
- */
-VQ3_API int vq3_mlp_gate_up(const uint16_t* x, int rows, const vq3_mlp_layer* layer, void* workspace,
-                            size_t ws_bytes, void* stream);
-VQ3_API int vq3_mlp_down(int rows, const vq3_mlp_layer* layer, uint16_t* out, void* workspace, size_t ws_bytes,
-                         void* stream);
-
-/* Number of kernels one vq3_mlp_forward call launches at `rows` rows (-1 on a
- * bad descriptor). */
+/* Number of kernels one vq3_mlp_forward call launches at `rows` rows: one per
+ * pass of 8, 16 or 32 rows (-1 on a bad descriptor). */
 VQ3_API int vq3_mlp_kernel_launches(int rows, const vq3_mlp_layer* layer);
 
 /*
@@ -197,10 +190,10 @@ VQ3_API int vq3_mlp_forward_host(const uint16_t* x_host, int rows, const vq3_mlp
  * its scratch is a fixed array of VQ3_NOALLOC_SCRATCH_BYTES (32 MiB) compiled
  * into the library, which every GPU that loads the library holds until the
  * process exits. It calls no cudaMalloc, cudaFree or other allocating routine.
- *   - Size limit: rows and the layer's widths must fit the array, i.e.
- *     vq3_mlp_workspace_bytes(rows, layer) <= VQ3_NOALLOC_SCRATCH_BYTES (at
- *     hidden 5120 / intermediate 17408 on a 152-SM GB300 that is up to 293
- *     rows); larger calls return VQ3_ENOSPACE and launch nothing.
+ *   - Size limit: any row count runs, in passes of 32, 16 or 8 rows: the
+ *     largest pass whose scratch fits the array (16 rows at hidden 5120 /
+ *     intermediate 17408 on a 152-SM GB300). Widths whose scratch exceeds the
+ *     array even in 8-row passes return VQ3_ENOSPACE and launch nothing.
  *   - The first call on a device looks up the array's device address (with that
  *     device current) and caches it; make that first call before any stream
  *     capture on the device.

@@ -47,19 +47,37 @@ def test_noalloc_matches_workspace_entry_point_twice():
         assert_parity(out.cpu().numpy(), ref, f"no-alloc call {call}")
 
 
-def test_noalloc_rejects_sizes_beyond_the_fixed_scratch():
+def test_noalloc_runs_rows_beyond_one_pass():
+    # 64 rows: more rows than the largest pass that fits the fixed array, so several passes
     vq3, noalloc = _lib()
     dev = torch.device("cuda:0")
-    wl = S.mlp_27b(seed=1, rows=1)
+    wl = S.mlp_prefill_outliers(seed=2, rows=64)
     layer = vq3.MLP.from_block(wl.layers[0], dev)
+    x = torch.from_numpy(wl.x).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    ref = vq3.mlp_forward(x, layer, stream=stream).cpu().numpy()
+    out = torch.full_like(x, float("nan"))
+    rc = noalloc(x.data_ptr(), x.shape[0], ctypes.byref(layer.struct), out.data_ptr(), stream.cuda_stream)
+    assert rc == 0, vq3.lib.vq3_last_error().decode()
+    torch.cuda.synchronize(dev)
+    assert_parity(out.cpu().numpy(), ref, "no-alloc, 64 rows")
+
+
+def test_noalloc_rejects_widths_beyond_the_fixed_scratch():
+    # hidden 16384 / intermediate 262144 needs more than 32 MiB of scratch even in 8-row
+    # passes; the call is refused on the host before anything is launched, so the
+    # descriptor's device pointers are never read (aligned placeholders)
+    vq3, noalloc = _lib()
+    H, I = 16384, 262144
+    fake = 1 << 20
+
+    def lin(d_in, d_out):
+        return vq3.vq3_linear(d_in, d_out, 1024, fake, fake, fake, None)
+
+    layer = vq3.vq3_mlp_layer(lin(H, I), lin(H, I), lin(I, H))
+    rows = 8
     cap = 32 * 1024 * 1024
-    rows = next(r for r in range(1, 4096)
-                if vq3.lib.vq3_mlp_workspace_bytes(r, ctypes.byref(layer.struct)) > cap)
-    x = torch.zeros((rows, S.HIDDEN), dtype=torch.float16, device=dev)
-    out = torch.zeros_like(x)
-    rc = noalloc(x.data_ptr(), rows, ctypes.byref(layer.struct), out.data_ptr(),
-                 torch.cuda.current_stream(dev).cuda_stream)
+    assert vq3.lib.vq3_mlp_workspace_bytes(rows, ctypes.byref(layer)) > cap
+    rc = noalloc(fake, rows, ctypes.byref(layer), fake, None)
     assert rc == -5
     assert "VQ3_NOALLOC_SCRATCH_BYTES" in vq3.lib.vq3_last_error().decode()
-    torch.cuda.synchronize(dev)
-    assert not out.any()
