@@ -412,11 +412,16 @@ __device__ __forceinline__ void compute_cell(uint32_t slot, uint32_t xb, int lan
   kstep<3, NT>(w, lanebase, acc, b);
 }
 
+// Index-copy cursor of one warp: the next cell of its CTA's range whose copies
+// are to be issued. All of it advances by increments; the group-dependent parts
+// are recomputed only when a group ends.
 struct Cursor {
-  long long c;    // next cell whose index copies are to be issued
-  int g, kg;      // its group and column group
-  int k;          // copies issued so far
-  uint32_t slot;  // ring slot of the next copy: byte offset (k % kSlots) * kSlotBytes
+  const uint4* src;  // this lane's first 16 bytes of the warp's segment SU in the next cell
+  int left;          // cells of the range not yet issued
+  int kg_left;       // column groups left in the current group (including the next cell)
+  int g;             // group of the next cell
+  uint32_t slot;     // ring slot of the next copy: byte offset
+  bool live;         // the warp's segment exists in group g
 };
 
 constexpr int kSlots = 3;
@@ -429,46 +434,51 @@ __device__ __forceinline__ void cell_range(const DecodeJob& a, long long& c0, lo
   c1 = range_begin(cells, a.grid, blockIdx.x + 1);
 }
 
+// Points the cursor at column group kg of group g.
+__device__ __forceinline__ void cursor_group(const DecodeJob& a, Cursor& cur, int g, int kg) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sg = g * kWarps + warp;
+  const int n_kg = a.n_kg();
+  cur.g = g;
+  cur.kg_left = n_kg - kg;
+  cur.live = sg < a.n_seg();
+  const bool two = a.n_mats > 1;
+  const int mat = two ? (sg & 1) : 0;
+  const int mg = two ? (sg >> 1) : sg;
+  cur.src = (mat ? a.packed1 : a.packed0) + ((size_t)mg * n_kg + kg) * kSuUint4 + lane;
+}
+
 // Issues the index copies of the warp's segment in the cursor's next cell (an
 // empty commit group past the range end or for a segment past the last).
-__device__ __forceinline__ void issue_cell(const DecodeJob& a, Cursor& cur, long long c1, uint32_t ring) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t slot = ring + cur.slot;
-  const int sg = cur.g * kWarps + warp;
-  if (cur.c < c1 && sg < a.n_seg()) {
-    const bool two = a.n_mats > 1;
-    const int mat = two ? (sg & 1) : 0;
-    const int mg = two ? (sg >> 1) : sg;
-    const uint4* su = (mat ? a.packed1 : a.packed0) + ((size_t)mg * a.n_kg() + cur.kg) * kSuUint4 + lane;
-#pragma unroll
-    for (int q = 0; q < 3; ++q) cp_async16(slot + (uint32_t)(q * 512 + lane * 16), su + q * 32);
+__device__ __forceinline__ void issue_cell(const DecodeJob& a, Cursor& cur, uint32_t ring_lane) {
+  if (cur.left > 0 && cur.live) {
+    const uint32_t s = ring_lane + cur.slot;
+    cp_async16(s, cur.src);
+    cp_async16(s + 512, cur.src + 32);
+    cp_async16(s + 1024, cur.src + 64);
   }
   cp_async_commit();
-  ++cur.k;
   cur.slot = cur.slot == (kSlots - 1) * kSlotBytes ? 0u : cur.slot + kSlotBytes;
-  ++cur.c;
-  if (++cur.kg == a.n_kg()) {
-    cur.kg = 0;
-    ++cur.g;
-  }
+  cur.src += kSuUint4;
+  --cur.left;
+  if (--cur.kg_left == 0 && cur.left > 0) cursor_group(a, cur, cur.g + 1, 0);
 }
 
 // Index copies of the first n cells of the CTA's range.
 __device__ __forceinline__ Cursor decode_begin(const DecodeJob& a, const SmemView& sv, int n) {
-  Cursor cur{0, 0, 0, 0, 0u};
+  Cursor cur{nullptr, 0, 0, 0, 0u, false};
   if ((int)blockIdx.x >= a.grid) return cur;
   long long c0, c1;
   cell_range(a, c0, c1);
-  cur.c = c0;
-  cur.g = (int)(c0 / a.n_kg());
-  cur.kg = (int)(c0 % a.n_kg());
-  const uint32_t ring = sv.ring + (uint32_t)((threadIdx.x >> 5) * kWarpRing);
-  for (int k = 0; k < n; ++k) issue_cell(a, cur, c1, ring);
+  cur.left = (int)(c1 - c0);
+  cursor_group(a, cur, (int)(c0 / a.n_kg()), (int)(c0 % a.n_kg()));
+  const uint32_t ring_lane = sv.ring + (uint32_t)((threadIdx.x >> 5) * kWarpRing + (threadIdx.x & 31) * 16);
+  for (int k = 0; k < n; ++k) issue_cell(a, cur, ring_lane);
   return cur;
 }
 
-// Decodes the CTA's range of cells; `cur` has issued the copies of the first
-// cur.k cells (1 .. kSlots), the rest of the prologue follows the first stage.
+// Decodes the CTA's range of cells; `cur` has issued the copies of its first
+// 1 .. kSlots cells, the rest of the prologue follows the first stage.
 template <int NT, typename T>
 __device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cursor& cur, const SmemView& sv,
                                            int* status) {
@@ -480,15 +490,20 @@ __device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cur
   long long c0, c1;
   cell_range(a, c0, c1);
   const uint32_t ring = sv.ring + (uint32_t)(warp * kWarpRing);
+  const uint32_t ring_lane = ring + (uint32_t)(lane * 16);
   const bool two = a.n_mats > 1;
   uint32_t use_slot = 0;  // ring slot of the next cell to compute
+  int issued = (int)(c1 - c0) - cur.left;  // copies issued so far (the prologue)
   int g = (int)(c0 / n_kg), kg = (int)(c0 % n_kg);  // group and column group of the next cell
   float acc[4][NT][4];
   uint32_t lane_base = 0;
   bool live = false;
   int sg = 0;
-  for (long long rs = c0; rs < c1; rs += KS) {
-    const int len = (int)((c1 - rs) < KS ? (c1 - rs) : KS);
+  const int total = (int)(c1 - c0);
+  int first = 1;  // the next cell starts the range's part of a group
+  for (int r0 = 0; r0 < total; r0 += KS) {
+    const long long rs = c0 + r0;
+    const int len = total - r0 < KS ? total - r0 : KS;
     if (a.ready) {
       // the chunks of the round's column groups must be complete
       if (tid == 0) {
@@ -500,11 +515,10 @@ __device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cur
       __syncthreads();
     }
     stage_round<NT, T>(a, src, rs, len, sv);
-    while (cur.k < kSlots) issue_cell(a, cur, c1, ring);  // rest of the prologue
+    for (; issued < kSlots; ++issued) issue_cell(a, cur, ring_lane);  // rest of the prologue
     __syncthreads();
     for (int p = 0; p < len; ++p) {
-      const long long c = rs + p;
-      if (c == c0 || kg == 0) {  // the range's part of group g starts
+      if (first) {  // the range's part of group g starts
         sg = g * kWarps + warp;
         live = sg < n_seg;
         lane_base = a.tab | (uint32_t)(lane * 4) | ((two && (sg & 1)) ? 8192u : 0u);
@@ -518,9 +532,10 @@ __device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cur
       cp_async_wait<kSlots - 1>();  // this cell's index copies have landed
       if (live)
         compute_cell<NT>(ring + use_slot, sv.stage + (uint32_t)(p * NT * 1024), lane, p & 7, lane_base, acc);
-      issue_cell(a, cur, c1, ring);  // refill the slot just read, kSlots cells ahead
+      issue_cell(a, cur, ring_lane);  // refill the slot just read, kSlots cells ahead
       use_slot = use_slot == (kSlots - 1) * kSlotBytes ? 0u : use_slot + kSlotBytes;
-      if (c + 1 == c1 || kg + 1 == n_kg) {
+      first = (++kg == n_kg);
+      if (first || r0 + p + 1 == total) {
         // this warp's segment over the range's part of group g: one piece
         if (live) {
           const int piece = blockIdx.x - cta_of((long long)g * n_kg, a.cells(), a.grid);
@@ -534,7 +549,7 @@ __device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cur
         }
         signal(a.group_done + g, nullptr);
       }
-      if (++kg == n_kg) {
+      if (first) {
         kg = 0;
         ++g;
       }
