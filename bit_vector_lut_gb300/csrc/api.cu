@@ -226,6 +226,80 @@ cudaError_t run_persistent(const uint16_t* x, int rows, int nt, const vq3_mlp_la
   return cudaSuccess;
 }
 
+// ---- many-row (prefill) path: rotate, tensor-core GEMM with the LUT decoded
+// into shared memory, (SwiGLU, rotate, GEMM)
+
+constexpr int kPrefillRows = 64;  // from this many rows on, the tcgen05 path
+
+// [status word (256 B)][x' FP16 [rows][d_in]][h FP32 [rows][d_inter]][h' FP16 [rows][d_inter]]
+struct PrefillWs {
+  size_t status, xr, h, hr, total;
+};
+
+PrefillWs prefill_ws(int rows, int d_in, int d_inter) {
+  PrefillWs w{};
+  size_t off = 0;
+  w.status = off;
+  off += 256;
+  w.xr = off;
+  off = round_up(off + (size_t)rows * d_in * 2, 256);
+  w.h = off;
+  off = round_up(off + (size_t)rows * d_inter * 4, 256);
+  w.hr = off;
+  off = round_up(off + (size_t)rows * d_inter * 2, 256);
+  w.total = off;
+  return w;
+}
+
+PrefillArgs prefill_args(const uint16_t* xr, int rows, const vq3_linear& m0, const vq3_linear* m1, int* status) {
+  PrefillArgs a{};
+  a.x = xr;
+  a.rows = rows;
+  a.d_in = m0.d_in;
+  a.d_out = m0.d_out;
+  a.swiglu = m1 ? 1 : 0;
+  a.packed0 = static_cast<const uint4*>(m0.packed);
+  a.cb0 = reinterpret_cast<const uint32_t*>(m0.codebook);
+  a.scale0 = m0.scales;
+  if (m1) {
+    a.packed1 = static_cast<const uint4*>(m1->packed);
+    a.cb1 = reinterpret_cast<const uint32_t*>(m1->codebook);
+    a.scale1 = m1->scales;
+  }
+  a.status = status;
+  return a;
+}
+
+cudaError_t run_prefill_mlp(const uint16_t* x, int rows, const vq3_mlp_layer& l, char* ws, uint16_t* out,
+                            cudaStream_t st) {
+  const int H = l.gate.d_in, I = l.gate.d_out;
+  const PrefillWs w = prefill_ws(rows, H, I);
+  uint16_t* xr = reinterpret_cast<uint16_t*>(ws + w.xr);
+  float* h = reinterpret_cast<float*>(ws + w.h);
+  uint16_t* hr = reinterpret_cast<uint16_t*>(ws + w.hr);
+  int* status = reinterpret_cast<int*>(ws + w.status);
+  cudaError_t e = launch_fwht(x, rows, H, l.gate.block, l.gate.signs, xr, st);
+  if (e != cudaSuccess) return e;
+  PrefillArgs gu = prefill_args(xr, rows, l.gate, &l.up, status);
+  gu.out32 = h;
+  if ((e = launch_prefill_gemm(gu, st)) != cudaSuccess) return e;
+  if ((e = launch_fwht_f32(h, rows, I, l.down.block, l.down.signs, hr, st)) != cudaSuccess) return e;
+  PrefillArgs dn = prefill_args(hr, rows, l.down, nullptr, status);
+  dn.out16 = out;
+  return launch_prefill_gemm(dn, st);
+}
+
+cudaError_t run_prefill_linear(const uint16_t* x, int rows, const vq3_linear& L, char* ws, uint16_t* out,
+                               cudaStream_t st) {
+  const PrefillWs w = prefill_ws(rows, L.d_in, 0);
+  uint16_t* xr = reinterpret_cast<uint16_t*>(ws + w.xr);
+  cudaError_t e = launch_fwht(x, rows, L.d_in, L.block, L.signs, xr, st);
+  if (e != cudaSuccess) return e;
+  PrefillArgs a = prefill_args(xr, rows, L, nullptr, reinterpret_cast<int*>(ws + w.status));
+  a.out16 = out;
+  return launch_prefill_gemm(a, st);
+}
+
 uint32_t read_bits6(const uint8_t* s, size_t k) {
   const size_t bit = 6 * k;
   const size_t byte = bit / 8;
@@ -375,11 +449,13 @@ int fwht_rotate(const uint16_t* x, int rows, int n, int block, const uint32_t* s
 
 size_t vq3_linear_workspace_bytes(int rows, const vq3_linear* L) {
   if (!L || rows < 0 || !layout_supported(L->d_in, L->d_out)) return 0;
+  if (rows >= kPrefillRows) return prefill_ws(rows, L->d_in, 0).total;
   return linear_ws(rows, L->d_in, L->d_out).total;
 }
 
 size_t vq3_mlp_workspace_bytes(int rows, const vq3_mlp_layer* layer) {
   if (!layer || rows < 0 || !layout_supported(layer->gate.d_in, layer->gate.d_out)) return 0;
+  if (rows >= kPrefillRows) return prefill_ws(rows, layer->gate.d_in, layer->gate.d_out).total;
   return mlp_ws(rows, layer).total;
 }
 
@@ -408,10 +484,17 @@ int vq3_linear_forward(const uint16_t* x, int rows, const vq3_linear* L, uint16_
   if (!x || !out || !workspace) return fail(VQ3_EINVAL, "linear: null x/out/workspace");
   if (!aligned(x, 16) || !aligned(out, 16) || !aligned(workspace, 256))
     return fail(VQ3_EALIGN, "linear: x/out must be 16-byte aligned and the workspace 256-byte aligned");
-  const LinearWs w = linear_ws(rows, L->d_in, L->d_out);
-  if (ws_bytes < w.total) return fail(VQ3_ENOSPACE, "linear: workspace %zu < %zu bytes", ws_bytes, w.total);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
+  if (rows >= kPrefillRows) {
+    const size_t need = prefill_ws(rows, L->d_in, 0).total;
+    if (ws_bytes < need) return fail(VQ3_ENOSPACE, "linear: workspace %zu < %zu bytes", ws_bytes, need);
+    cudaError_t e = run_prefill_linear(x, rows, *L, ws, out, st);
+    if (e != cudaSuccess) return cuda_fail(e, "linear: launch");
+    return ok();
+  }
+  const LinearWs w = linear_ws(rows, L->d_in, L->d_out);
+  if (ws_bytes < w.total) return fail(VQ3_ENOSPACE, "linear: workspace %zu < %zu bytes", ws_bytes, w.total);
   PersistBufs b{};
   b.pieces1 = reinterpret_cast<float*>(ws + w.pieces);
   b.ctl = reinterpret_cast<unsigned*>(ws + w.counters);
@@ -492,13 +575,24 @@ extern "C" {
 
 int vq3_mlp_forward(const uint16_t* x, int rows, const vq3_mlp_layer* layer, uint16_t* out, void* workspace,
                     size_t ws_bytes, void* stream) {
-  return mlp_forward_capped(x, rows, layer, out, workspace, ws_bytes, stream, 32);
+  if (rows < kPrefillRows) return mlp_forward_capped(x, rows, layer, out, workspace, ws_bytes, stream, 32);
+  int rc = check_mlp(layer);
+  if (rc) return rc;
+  if (!x || !out || !workspace) return fail(VQ3_EINVAL, "mlp: null x/out/workspace");
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(workspace, 256))
+    return fail(VQ3_EALIGN, "mlp: x/out must be 16-byte aligned and the workspace 256-byte aligned");
+  const size_t need = prefill_ws(rows, layer->gate.d_in, layer->gate.d_out).total;
+  if (ws_bytes < need) return fail(VQ3_ENOSPACE, "mlp: workspace %zu < %zu bytes", ws_bytes, need);
+  cudaError_t e = run_prefill_mlp(x, rows, *layer, static_cast<char*>(workspace), out, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mlp: launch");
+  return ok();
 }
 
 int vq3_mlp_kernel_launches(int rows, const vq3_mlp_layer* layer) {
   if (check_mlp(layer) || rows < 0) return -1;
   if (rows == 0) return 0;
-  return passes(rows, 32);  // one persistent kernel per pass of 8, 16 or 32 rows
+  if (rows >= kPrefillRows) return 4;  // rotate x, gate/up GEMM, rotate h, down GEMM
+  return passes(rows, 32);             // one persistent kernel per pass of 8, 16 or 32 rows
 }
 
 size_t vq3_mlp_host_workspace_bytes(int rows, const vq3_mlp_layer* layer) {

@@ -1,0 +1,457 @@
+// The many-row path (prefill, T >= 64) of the VQ3 matrices: a tensor-core GEMM
+// on 5th-generation tensor cores (tcgen05) whose weight operand is decoded from
+// the three-bit vector LUT on the fly.
+//
+// What it computes (model card "anemll/anemll-forge-qwen3.8-27B", section
+// "Release 0.2: three-bit MLP, token-mixer rotations, distilled weights": a 2x64
+// vector LUT per matrix, one six-bit index per output pair and input, per-channel
+// scales; SiLU per "ANEMLL ANE LLM conversion pipeline", "Facts"), for activations
+// already rotated (x' = R x, in FP16):
+//   linear / down:  y[r][o] = fp16( s[o] * sum_i W0[o][i] x'[r][i] ),  W0[2p+c][i] = C[idx[p][i]][c]
+//   gate + up:      h[r][j] = silu(s_g[j] g[r][j]) * (s_u[j] u[r][j])  (FP32)
+//
+// One CTA computes one output tile of 128 channels x N rows (N <= 256), with the
+// FP32 accumulator D[channel][row] in tensor memory, over K in steps of 64 inputs
+// (one column group of the packed super-units):
+//   warps 0-3  loaders: for stage s of a K step, copy the activation tile
+//              B[N][64] and the two super-units of index strings (cp.async); each
+//              thread's copies arrive on the stage's load barrier when they land,
+//              so the loaders run up to kStages steps ahead.
+//   warps 4-7  decoders: once the stage's index strings are in, each thread takes
+//              half of one lane string of one super-unit, looks its 32 indices up
+//              in a lane-private shared-memory copy of the codebook and pairs
+//              neighbouring inputs of a channel with a byte permute into the FP16
+//              words of A[128][64]. A and B are in the K-major "core matrix" layout
+//              (8 rows x 16 bytes per 128-byte block) that the MMA's shared-memory
+//              descriptors read.
+//   warp 8     one lane issues tcgen05.mma (M = 128, N, K = 16) four times per K
+//              step, and tcgen05.commit frees the stage (and, at the end, marks
+//              the accumulator complete).
+//   warps 8-11 epilogue: tcgen05.ld of the accumulator (each warp its 32 lanes),
+//              scale (and SwiGLU: the tile's rows 0-63 are gate channels, rows
+//              64-127 the up channels with the same indices) and store.
+// A 3-deep stage ring with mbarriers connects loaders, decoders and the MMA issuer. All
+// waits are bounded: one that runs out sets the status word to 3 and the kernel
+// carries on to its end (results invalid).
+#include <cuda_fp16.h>
+
+#include "vq3_internal.h"
+
+namespace vq3 {
+namespace {
+
+constexpr int kPThreads = 12 * 32;
+constexpr int kLoadWarps = 4;  // warps 0-3
+constexpr int kDecWarps = 4;   // warps 4-7
+constexpr int kMmaWarp = 8;
+constexpr int kEpiWarp0 = 8;
+constexpr int kStages = 3;
+constexpr int kTileM = 128;                    // output channels per tile
+constexpr int kATile = kTileM * 64 * 2;        // 16 KB of FP16
+constexpr int kTabWords = 64 * 32;
+constexpr uint32_t kTabAlign = 16384;
+constexpr long long kWaitSpin = 1ll << 22;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of parity `parity` to complete.
+__device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, int* status) {
+  long long it = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if (++it > kWaitSpin) {
+      atomicExch(status, 3);
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ void cp_async16_zfill(uint32_t saddr, const void* g, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16, %2;" ::"r"(saddr), "l"(g), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(g) : "memory");
+}
+// Arrives on the mbarrier once all of this thread's earlier cp.async copies have
+// landed (counted among the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor for a K-major operand without swizzle: core
+// matrices of 8 rows x 16 bytes stored as 128 contiguous bytes; lbo = byte step
+// between core matrices along K, sbo = byte step along M/N.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// The same for a K-major operand in the 128-byte swizzle layout: rows of 64 FP16
+// (128 bytes), 8-row atoms of 1 KB (sbo), the 16-byte chunk c of row r stored at
+// chunk position c ^ (r % 8); the atoms are 1 KB aligned. K advances inside an
+// atom by moving the start address (32 bytes per 16 elements).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1 << 16;                    // leading byte offset: unused with this swizzle
+  d |= (uint64_t)(1024u >> 4) << 32;         // stride byte offset: one 8-row atom
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;                    // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: kind::f16 with FP16 A and B, FP32 D, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_f16(int m, int n) {
+  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void sts32(uint32_t a, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
+// Lookup address of index N of a lane string: bits [6N, 6N+6) moved to [7, 13)
+// (entry stride 32 lanes x 4 bytes), OR-ed with the table base and lane column.
+template <int N>
+__device__ __forceinline__ uint32_t lut_addr(const uint32_t (&w)[12], uint32_t lanebase) {
+  constexpr int pos = 6 * N, wd = pos >> 5, off = pos & 31;
+  uint32_t v;
+  if constexpr (off >= 7) {
+    const uint32_t hi = (wd + 1 < 12) ? w[wd + 1] : 0u;
+    v = __funnelshift_r(w[wd], hi, off - 7);
+  } else {
+    v = w[wd] << (7 - off);
+  }
+  return (v & 0x1F80u) | lanebase;
+}
+
+// Byte offset of (row, k) in a K-major core-matrix tile with `rows` rows and 64
+// columns of K: core matrix (row/8, k/8) at (k/8) * rows * 16 + (row/8) * 128.
+__device__ __forceinline__ uint32_t tile_off(int row, int k, int rows) {
+  return (uint32_t)((k >> 3) * rows * 16 + (row >> 3) * 128 + (row & 7) * 16 + (k & 7) * 2);
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+// Decodes the producer thread's share of the weight tile of one K step: a
+// quarter (k-step s of 16 inputs) of lane string L of super-unit su of the tile.
+// A-fragment order of the lane string (see vq3_internal.h): index n = (s*4 + m)*4
+// + e is pair m*8 + g at input s*16 + {2t, 2t+1, 2t+8, 2t+9}[e].
+template <int S, int M>
+__device__ __forceinline__ void decode_pairs(const uint32_t (&w)[12], int g, int t, int row0, uint32_t a_tile,
+                                             uint32_t lanebase) {
+  constexpr int n0 = (S * 4 + M) * 4;
+  const uint32_t l0 = lds32(lut_addr<n0 + 0>(w, lanebase));
+  const uint32_t l1 = lds32(lut_addr<n0 + 1>(w, lanebase));
+  const uint32_t l2 = lds32(lut_addr<n0 + 2>(w, lanebase));
+  const uint32_t l3 = lds32(lut_addr<n0 + 3>(w, lanebase));
+  const int r = row0 + 2 * (M * 8 + g);  // channel 2p of the tile; 2p+1 is the next row
+  const int k = S * 16 + 2 * t;
+  sts32(a_tile + tile_off(r, k, kTileM), __byte_perm(l0, l1, 0x5410));
+  sts32(a_tile + tile_off(r + 1, k, kTileM), __byte_perm(l0, l1, 0x7632));
+  sts32(a_tile + tile_off(r, k + 8, kTileM), __byte_perm(l2, l3, 0x5410));
+  sts32(a_tile + tile_off(r + 1, k + 8, kTileM), __byte_perm(l2, l3, 0x7632));
+}
+
+template <int S>
+__device__ __forceinline__ void decode_quarter_s(const uint32_t (&w)[12], int lane, int row0, uint32_t a_tile,
+                                                 uint32_t lanebase) {
+  const int g = lane >> 2, t = lane & 3;
+  decode_pairs<S, 0>(w, g, t, row0, a_tile, lanebase);
+  decode_pairs<S, 1>(w, g, t, row0, a_tile, lanebase);
+  decode_pairs<S, 2>(w, g, t, row0, a_tile, lanebase);
+  decode_pairs<S, 3>(w, g, t, row0, a_tile, lanebase);
+}
+
+__device__ __forceinline__ void decode_quarter(const uint32_t (&w)[12], int s, int lane, int row0, uint32_t a_tile,
+                                               uint32_t lanebase) {
+  switch (s) {
+    case 0: decode_quarter_s<0>(w, lane, row0, a_tile, lanebase); break;
+    case 1: decode_quarter_s<1>(w, lane, row0, a_tile, lanebase); break;
+    case 2: decode_quarter_s<2>(w, lane, row0, a_tile, lanebase); break;
+    default: decode_quarter_s<3>(w, lane, row0, a_tile, lanebase); break;
+  }
+}
+
+constexpr int kIdxBytes = 2 * kSuBytes;  // index strings of the tile's two super-units per K step
+
+template <int N>
+struct PfSmem {
+  static constexpr int kBTile = N * 64 * 2;
+  static constexpr int kStageBytes = kATile + kBTile + kIdxBytes;
+  static_assert(kStageBytes % 1024 == 0 && kATile % 1024 == 0, "B tiles start on 1 KB swizzle atoms");
+  static constexpr int kTotal = 1024 + kStages * kStageBytes + (int)kTabAlign + 2 * kTabWords * 4 + 64 * 16 * 4;
+};
+
+template <int N>
+__global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs a) {
+  extern __shared__ __align__(16) unsigned char dsm[];
+  __shared__ __align__(8) unsigned long long s_bars[3 * kStages + 1];
+  __shared__ uint32_t s_tmem;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t raw = smem_u32(dsm);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // 1 KB aligned stages (swizzle atoms)
+  const uint32_t tabs = (base + kStages * PfSmem<N>::kStageBytes + kTabAlign - 1) & ~(kTabAlign - 1);
+  float* xch = reinterpret_cast<float*>(dsm + (tabs - raw) + 2 * kTabWords * 4);  // up values for SwiGLU
+  const uint32_t bar0 = smem_u32(s_bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };                 // A decoded
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };    // stage consumed
+  auto load_bar = [&](int s) { return bar0 + 8u * (2 * kStages + s); }; // B and indices landed
+  const uint32_t dfull_bar = bar0 + 8u * (3 * kStages);
+  auto a_tile = [&](int s) { return base + (uint32_t)(s * PfSmem<N>::kStageBytes); };
+  auto b_tile = [&](int s) { return base + (uint32_t)(s * PfSmem<N>::kStageBytes + kATile); };
+  auto i_tile = [&](int s) { return base + (uint32_t)(s * PfSmem<N>::kStageBytes + kATile + PfSmem<N>::kBTile); };
+
+  const int mt = blockIdx.x;        // output tile
+  const int row0 = blockIdx.y * N;  // first row of the tile
+  const int n_kg = a.d_in / 64;
+
+  // codebook tables (lane-private copies): matrix 0 at tabs, matrix 1 at tabs + 8192
+  for (int i = tid; i < 2 * 64 * 8; i += kPThreads) {
+    const int t2 = i / 512, k = (i >> 3) & 63, q = i & 7;
+    const uint32_t* cb = t2 ? a.cb1 : a.cb0;
+    if (cb) {
+      const uint32_t v = __ldg(cb + k);
+      asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(tabs + (uint32_t)(t2 * 8192 + k * 128 + q * 16)),
+                   "r"(v)
+                   : "memory");
+    }
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), kDecWarps * 32);
+      mbar_init(empty_bar(s), 1);
+      mbar_init(load_bar(s), kLoadWarps * 32);
+    }
+    mbar_init(dfull_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                 "r"((uint32_t)(N < 32 ? 32 : N))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp < kLoadWarps) {
+    // ------------------------------------------------------------ loaders
+    const int rows = a.rows;
+    // the tile's two super-units: (matrix, channel group); the second is past the
+    // last channel when d_out is an odd multiple of 64 (its A rows are never stored)
+    const int mg0 = a.swiglu ? mt : 2 * mt, mg1 = a.swiglu ? mt : 2 * mt + 1;
+    const bool live1 = a.swiglu || mg1 < a.d_out / 64;
+    const uint4* su0 = a.packed0 + (size_t)mg0 * n_kg * kSuUint4;
+    const uint4* su1 = (a.swiglu ? a.packed1 : a.packed0) + (size_t)(live1 ? mg1 : mg0) * n_kg * kSuUint4;
+    for (int kk = 0; kk < n_kg; ++kk) {
+      const int st = kk % kStages;
+      if (kk >= kStages) mbar_wait(empty_bar(st), (uint32_t)((kk / kStages - 1) & 1), a.status);
+      // activation tile: N rows x 64 inputs (128 bytes per row), 16 bytes per
+      // copy, in the 128-byte swizzle layout; eight consecutive threads copy one row
+      const uint32_t bt = b_tile(st);
+      for (int e = tid; e < N * 8; e += kLoadWarps * 32) {
+        const int n = e >> 3, c = e & 7;
+        const int r = row0 + n;
+        const uint16_t* src = a.x + (size_t)(r < rows ? r : 0) * a.d_in + kk * 64 + c * 8;
+        cp_async16_zfill(bt + (uint32_t)((n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4)), src, r < rows);
+      }
+      // index strings of the two super-units (96 16-byte chunks each)
+      for (int e = tid; e < 2 * kSuUint4; e += kLoadWarps * 32) {
+        const uint4* s = (e < kSuUint4 ? su0 : su1) + (size_t)kk * kSuUint4 + (e % kSuUint4);
+        cp_async16(i_tile(st) + (uint32_t)(e * 16), s);
+      }
+      cp_async_arrive(load_bar(st));
+    }
+    cp_async_wait_all();
+  } else if (warp < kLoadWarps + kDecWarps) {
+    // ------------------------------------------------------------ decoders
+    // thread -> (super-unit su of the tile, lane string L, half hh of the string)
+    const int dt = tid - kLoadWarps * 32;
+    const int su = dt >> 6, L = (dt >> 1) & 31, hh = dt & 1;
+    const int mg1 = a.swiglu ? mt : 2 * mt + 1;
+    const bool live = su == 0 || a.swiglu || mg1 < a.d_out / 64;
+    const uint32_t lanebase = tabs | (uint32_t)(lane * 4) | ((a.swiglu && su == 1) ? 8192u : 0u);
+    for (int kk = 0; kk < n_kg; ++kk) {
+      const int st = kk % kStages;
+      if (kk >= kStages) mbar_wait(empty_bar(st), (uint32_t)((kk / kStages - 1) & 1), a.status);
+      mbar_wait(load_bar(st), (uint32_t)((kk / kStages) & 1), a.status);
+      if (live) {
+        uint32_t w[12];
+        const uint32_t is = i_tile(st) + (uint32_t)(su * kSuBytes);
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+          const uint32_t o = is + (uint32_t)((q * 32 + L) * 16);
+          uint32_t v0, v1, v2, v3;
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3) : "r"(o));
+          w[4 * q + 0] = v0;
+          w[4 * q + 1] = v1;
+          w[4 * q + 2] = v2;
+          w[4 * q + 3] = v3;
+        }
+        decode_quarter(w, 2 * hh, L, su * 64, a_tile(st), lanebase);
+        decode_quarter(w, 2 * hh + 1, L, su * 64, a_tile(st), lanebase);
+      }
+      fence_proxy_async();  // the generic-proxy writes of A, before the MMA reads them
+      mbar_arrive(full_bar(st));
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(kTileM, N);
+      for (int kk = 0; kk < n_kg; ++kk) {
+        const int st = kk % kStages;
+        mbar_wait(load_bar(st), (uint32_t)((kk / kStages) & 1), a.status);
+        mbar_wait(full_bar(st), (uint32_t)((kk / kStages) & 1), a.status);
+        fence_proxy_async();  // the activation tile (cp.async, generic proxy) before the MMA reads it
+        tc_fence_after();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          // K = 16: two core matrices along K
+          const uint64_t ad = smem_desc(a_tile(st) + (uint32_t)(j * 2 * kTileM * 16), kTileM * 16, 128);
+          const uint64_t bd = smem_desc_sw128(b_tile(st) + (uint32_t)(j * 32));
+          mma_ss(tmem, ad, bd, idesc, (kk > 0 || j > 0) ? 1u : 0u);
+        }
+        mma_commit(empty_bar(st));
+      }
+      mma_commit(dfull_bar);
+    }
+  }
+  if (warp >= kEpiWarp0) {
+    // ------------------------------------------------------------ epilogue
+    __syncwarp();  // the MMA warp's lanes reconverge once lane 0 has issued every MMA
+    const int quarter = warp - kEpiWarp0;  // TMEM lanes 32*quarter .. +31 = tile rows
+    const int row = quarter * 32 + lane;   // tile row = output channel of the tile
+    mbar_wait(dfull_bar, 0u, a.status);
+    tc_fence_after();
+    const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+    if (!a.swiglu) {
+      const int ch = mt * kTileM + row;
+      const bool live = ch < a.d_out;
+      const float sc = live ? __half2float(__ushort_as_half(a.scale0[ch])) : 0.f;
+#pragma unroll 1
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld16(taddr + (uint32_t)c0, r);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int rr = row0 + c0 + j;
+          if (live && rr < a.rows)
+            a.out16[(size_t)rr * a.d_out + ch] = __half_as_ushort(__float2half_rn(sc * __uint_as_float(r[j])));
+        }
+      }
+    } else {
+      // rows 0-63: gate channel mt*64 + row; rows 64-127: up channel mt*64 + row - 64
+      const int jch = mt * 64 + (row & 63);
+      const bool up = row >= 64;
+      const float sc = __half2float(__ushort_as_half(up ? a.scale1[jch] : a.scale0[jch]));
+#pragma unroll 1
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld16(taddr + (uint32_t)c0, r);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (up) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) xch[(row - 64) * 16 + j] = sc * __uint_as_float(r[j]);
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (!up) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int rr = row0 + c0 + j;
+            const float hv = silu_f(sc * __uint_as_float(r[j])) * xch[row * 16 + j];
+            if (rr < a.rows) __stcg(a.out32 + (size_t)rr * a.d_out + jch, hv);
+          }
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"((uint32_t)(N < 32 ? 32 : N))
+                 : "memory");
+  }
+}
+
+template <int N>
+cudaError_t launch_n(const PrefillArgs& a, cudaStream_t st) {
+  const int smem = PfSmem<N>::kTotal;
+  cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int m_tiles = a.swiglu ? a.d_out / 64 : (a.d_out + kTileM - 1) / kTileM;
+  const dim3 grid(m_tiles, (a.rows + N - 1) / N);
+  prefill_gemm_kernel<N><<<grid, kPThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int prefill_tile_rows(int rows) {
+  if (rows >= 256) return 256;
+  if (rows > 128) return 256;
+  if (rows > 64) return 128;
+  return 64;
+}
+
+cudaError_t launch_prefill_gemm(const PrefillArgs& a, cudaStream_t st) {
+  switch (prefill_tile_rows(a.rows)) {
+    case 64: return launch_n<64>(a, st);
+    case 128: return launch_n<128>(a, st);
+    default: return launch_n<256>(a, st);
+  }
+}
+
+}  // namespace vq3

@@ -24,9 +24,13 @@ constexpr int kRotThreads = 128;
 // block is in "lane-major" form. Butterflies of stride h < 32 pair lanes within
 // a warp (shuffle), strides 32 and 64 pair warps (shared memory), strides >= 128
 // pair slots of the same thread (registers).
-// out[row][col] row-major (may alias x: every element is read before any is written).
-template <int B>
-__global__ void __launch_bounds__(kRotThreads) fwht_kernel(const uint16_t* x, int n, const uint32_t* __restrict__ signs,
+__device__ __forceinline__ float load_elem(const uint16_t* p) { return __half2float(__ushort_as_half(*p)); }
+__device__ __forceinline__ float load_elem(const float* p) { return *p; }
+
+// out[row][col] row-major FP16 (may alias an FP16 x: every element is read before
+// any is written). T: FP16 (uint16_t) or FP32 input.
+template <int B, typename T>
+__global__ void __launch_bounds__(kRotThreads) fwht_kernel(const T* x, int n, const uint32_t* __restrict__ signs,
                                                             uint16_t* out, float scale) {
   constexpr int V = (B + kRotThreads - 1) / kRotThreads;  // values per thread
   constexpr int ACTIVE = B < kRotThreads ? B : kRotThreads;
@@ -43,7 +47,7 @@ __global__ void __launch_bounds__(kRotThreads) fwht_kernel(const uint16_t* x, in
     const int j = s * kRotThreads + tid;
     float f = 0.f;
     if (tid < ACTIVE) {
-      f = __half2float(__ushort_as_half(x[base + j]));
+      f = load_elem(x + base + j);
       if (signs) {
         const int col = blk * B + j;
         if ((__ldg(signs + (col >> 5)) >> (col & 31)) & 1u) f = -f;
@@ -94,10 +98,10 @@ __global__ void __launch_bounds__(kRotThreads) fwht_kernel(const uint16_t* x, in
   }
 }
 
-template <int B>
-cudaError_t launch_b(const uint16_t* x, int rows, int n, const uint32_t* signs, uint16_t* out, cudaStream_t st) {
+template <int B, typename T>
+cudaError_t launch_b(const T* x, int rows, int n, const uint32_t* signs, uint16_t* out, cudaStream_t st) {
   const long long grid = (long long)rows * (n / B);
-  fwht_kernel<B><<<(unsigned)grid, kRotThreads, 0, st>>>(x, n, signs, out, 1.0f / sqrtf((float)B));
+  fwht_kernel<B, T><<<(unsigned)grid, kRotThreads, 0, st>>>(x, n, signs, out, 1.0f / sqrtf((float)B));
   return cudaGetLastError();
 }
 
@@ -132,19 +136,20 @@ __global__ void __launch_bounds__(256) residual_rmsnorm_kernel(uint16_t* resid, 
 }  // namespace
 
 namespace {
-cudaError_t launch_any(const uint16_t* x, int rows, int n, int block, const uint32_t* signs, uint16_t* out,
+template <typename T>
+cudaError_t launch_any(const T* x, int rows, int n, int block, const uint32_t* signs, uint16_t* out,
                        cudaStream_t st) {
   switch (block) {
-    case 2: return launch_b<2>(x, rows, n, signs, out, st);
-    case 4: return launch_b<4>(x, rows, n, signs, out, st);
-    case 8: return launch_b<8>(x, rows, n, signs, out, st);
-    case 16: return launch_b<16>(x, rows, n, signs, out, st);
-    case 32: return launch_b<32>(x, rows, n, signs, out, st);
-    case 64: return launch_b<64>(x, rows, n, signs, out, st);
-    case 128: return launch_b<128>(x, rows, n, signs, out, st);
-    case 256: return launch_b<256>(x, rows, n, signs, out, st);
-    case 512: return launch_b<512>(x, rows, n, signs, out, st);
-    case 1024: return launch_b<1024>(x, rows, n, signs, out, st);
+    case 2: return launch_b<2, T>(x, rows, n, signs, out, st);
+    case 4: return launch_b<4, T>(x, rows, n, signs, out, st);
+    case 8: return launch_b<8, T>(x, rows, n, signs, out, st);
+    case 16: return launch_b<16, T>(x, rows, n, signs, out, st);
+    case 32: return launch_b<32, T>(x, rows, n, signs, out, st);
+    case 64: return launch_b<64, T>(x, rows, n, signs, out, st);
+    case 128: return launch_b<128, T>(x, rows, n, signs, out, st);
+    case 256: return launch_b<256, T>(x, rows, n, signs, out, st);
+    case 512: return launch_b<512, T>(x, rows, n, signs, out, st);
+    case 1024: return launch_b<1024, T>(x, rows, n, signs, out, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -152,7 +157,12 @@ cudaError_t launch_any(const uint16_t* x, int rows, int n, int block, const uint
 
 cudaError_t launch_fwht(const uint16_t* x, int rows, int n, int block, const uint32_t* signs,
                         uint16_t* out, cudaStream_t st) {
-  return launch_any(x, rows, n, block, signs, out, st);
+  return launch_any<uint16_t>(x, rows, n, block, signs, out, st);
+}
+
+cudaError_t launch_fwht_f32(const float* x, int rows, int n, int block, const uint32_t* signs, uint16_t* out,
+                            cudaStream_t st) {
+  return launch_any<float>(x, rows, n, block, signs, out, st);
 }
 
 cudaError_t launch_residual_rmsnorm(uint16_t* resid, const uint16_t* delta, int rows, int n, float eps,

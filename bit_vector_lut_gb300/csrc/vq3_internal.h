@@ -92,6 +92,29 @@ cudaError_t launch_persistent(const PersistArgs& a, int nt, cudaStream_t st);
 
 cudaError_t launch_fwht(const uint16_t* x, int rows, int n, int block, const uint32_t* signs,
                         uint16_t* out, cudaStream_t st);
+// Same rotation of FP32 rows, written as FP16.
+cudaError_t launch_fwht_f32(const float* x, int rows, int n, int block, const uint32_t* signs, uint16_t* out,
+                            cudaStream_t st);
+
+// One VQ3 matrix (or the gate/up pair) against rotated FP16 activations on
+// tcgen05 tensor cores: out16 = fp16(s0 * W0 x') for one matrix, or, with
+// swiglu, out32 = silu(s0 * W0 x') * (s1 * W1 x') in FP32 (W0 gate, W1 up).
+struct PrefillArgs {
+  const uint16_t* x;       // rotated activations, FP16 [rows][d_in], 16-byte aligned
+  int rows, d_in, d_out;   // d_out: output channels (swiglu: the intermediate width)
+  int swiglu;
+  const uint4* packed0;    // GPU-layout indices of W0 (and W1)
+  const uint4* packed1;
+  const uint32_t* cb0;     // codebooks
+  const uint32_t* cb1;
+  const uint16_t* scale0;  // per-output-channel scales
+  const uint16_t* scale1;
+  uint16_t* out16;         // [rows][d_out] FP16 (no swiglu)
+  float* out32;            // [rows][d_out] FP32 (swiglu)
+  int* status;             // status word (3: a wait timed out)
+};
+int prefill_tile_rows(int rows);  // rows per output tile: 64, 128 or 256
+cudaError_t launch_prefill_gemm(const PrefillArgs& a, cudaStream_t st);
 cudaError_t launch_residual_rmsnorm(uint16_t* resid, const uint16_t* delta, int rows, int n,
                                     float eps, uint16_t* normed, cudaStream_t st);
 cudaError_t launch_dequant(const vq3_linear& L, int apply_scale, uint16_t* w_out, cudaStream_t st);
