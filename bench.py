@@ -295,9 +295,10 @@ def _run_ours_on(args, torch, vq3, dev, stream, rows, sets, x_host, x, out, ws, 
            "h2d_bytes_per_step": int(x_host.nbytes), "d2h_bytes_per_step": int(rows * HIDDEN * 2),
            "api": "vq3_mlp_forward_host (pageable->pinned host buffers)"}
 
-    extra = {}
+    extra, stack = {}, {}
     if not args.quick and rank == 0:
         extra = prefill_sweep(vq3, dev, stream, pk)
+        stack = stack64(vq3, dev, stream, pk)
 
     launches = vq3.mlp_kernel_launches(rows, sets[0]) * steps
     line = None
@@ -314,6 +315,8 @@ def _run_ours_on(args, torch, vq3, dev, stream, rows, sets, x_host, x, out, ws, 
                 "clocks": clk.summary(), "e2e": e2e, "gpu_launches": launches, "roofline": roofline}
         if extra:
             line["prefill_sweep"] = extra
+        if stack:
+            line["stack64"] = stack
         if world == 1 and not args.no_cpu_baseline:
             rate, dt, smp = time_oracle(rows, 1.0 / args.oracle_frac, args.oracle_steps, 1)
             line["cpu_baseline"] = {"value": round(rate, 3), "unit": "rows/s", "cores": cpu_cores(),
@@ -354,6 +357,49 @@ def prefill_sweep(vq3, dev, stream, pk) -> dict:
         res[f"T{rows}"] = {"ms": round(ms, 4), "tflops": round(tf, 2), "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4),
                            "rows_per_s": round(rows / (ms / 1e3), 1)}
     return res
+
+
+def stack64(vq3, dev, stream, pk) -> dict:
+    """The 64-layer stack at T = 8: per layer a residual add + RMSNorm and one MLP block
+    (6.42 GB of packed weights, so every layer streams from HBM), one CUDA graph of all
+    64 layers, timed with events on its stream over 5 replays after 2 warm-up replays."""
+    import torch
+    seed, rows, layers_n = 3, 8, 64
+    x = torch.from_numpy(S.activations(S.rng(seed, 0), rows, HIDDEN)).to(dev)
+    g = S.rng(seed, 1)
+    layers = [vq3.MLP.from_block(S.mlp_block(g, HIDDEN, INTER, 1024), dev) for _ in range(layers_n)]
+    resid = torch.empty_like(x)
+    normed = torch.empty_like(x)
+    y = torch.empty_like(x)
+    ws = vq3.workspace(vq3.mlp_workspace_bytes(rows, layers[0]), dev, stream)
+
+    def run():
+        resid.copy_(x)
+        for li, layer in enumerate(layers):
+            vq3.residual_rmsnorm(resid, y if li > 0 else None, 1e-6, normed, stream=stream)
+            vq3.mlp_forward(normed, layer, out=y, ws=ws, stream=stream)
+        vq3.residual_rmsnorm(resid, y, 1e-6, normed, stream=stream)
+
+    run()
+    torch.cuda.synchronize(dev)
+    gph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gph, stream=stream):
+        run()
+    for _ in range(2):
+        gph.replay()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    reps = 5
+    a.record(stream)
+    for _ in range(reps):
+        gph.replay()
+    b.record(stream)
+    b.synchronize()
+    ms = a.elapsed_time(b) / reps
+    gbs = layers_n * BLOCK_BYTES / (ms / 1e3) / 1e9
+    return {"ms_per_stack": round(ms, 4), "rows_per_s": round(rows / (ms / 1e3), 1),
+            "weight_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4),
+            "status": vq3.workspace_status(ws, stream)}
 
 
 def run_reference(args) -> dict | None:

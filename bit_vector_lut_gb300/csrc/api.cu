@@ -4,6 +4,8 @@
 #include <cstdio>
 #include <cstring>
 #include <string>
+#include <thread>
+#include <vector>
 
 #include "vq3_internal.h"
 
@@ -300,6 +302,26 @@ cudaError_t run_prefill_linear(const uint16_t* x, int rows, const vq3_linear& L,
   return launch_prefill_gemm(a, st);
 }
 
+// Runs fn(i) for i in [0, n) on up to hardware_concurrency host threads (the
+// channel groups of a matrix touch disjoint bytes of both layouts).
+template <typename F>
+void parallel_for(int n, F fn) {
+  unsigned hw = std::thread::hardware_concurrency();
+  const int nt = (int)(hw == 0 ? 1 : (hw > 64 ? 64 : hw));
+  const int k = n < nt ? n : nt;
+  if (k <= 1) {
+    for (int i = 0; i < n; ++i) fn(i);
+    return;
+  }
+  std::vector<std::thread> th;
+  th.reserve(k);
+  for (int j = 0; j < k; ++j)
+    th.emplace_back([=] {
+      for (int i = j; i < n; i += k) fn(i);
+    });
+  for (auto& x : th) x.join();
+}
+
 uint32_t read_bits6(const uint8_t* s, size_t k) {
   const size_t bit = 6 * k;
   const size_t byte = bit / 8;
@@ -376,7 +398,7 @@ int vq3_pack_layout(const uint8_t* canonical, int d_in, int d_out, void* dst_hos
     return fail(VQ3_EUNSUPPORTED, "pack_layout: d_in=%d and d_out=%d must be positive multiples of 64", d_in, d_out);
   uint8_t* dst = static_cast<uint8_t*>(dst_host);
   const int n_mg = d_out / kSuChannels, n_kg = d_in / kSuInputs;
-  for (int mg = 0; mg < n_mg; ++mg) {
+  parallel_for(n_mg, [=](int mg) {
     for (int kg = 0; kg < n_kg; ++kg) {
       const size_t su = (size_t)mg * n_kg + kg;
       for (int lane = 0; lane < 32; ++lane) {
@@ -395,7 +417,7 @@ int vq3_pack_layout(const uint8_t* canonical, int d_in, int d_out, void* dst_hos
         for (int wi = 0; wi < 12; ++wi) memcpy(dst + lane_word_offset(su, lane, wi), &w[wi], 4);
       }
     }
-  }
+  });
   return ok();
 }
 
@@ -408,7 +430,7 @@ int vq3_unpack_layout(const void* packed_host, int d_in, int d_out, uint8_t* can
   const size_t nbytes = (6 * count + 7) / 8;
   memset(canonical, 0, nbytes);
   const int n_mg = d_out / kSuChannels, n_kg = d_in / kSuInputs;
-  for (int mg = 0; mg < n_mg; ++mg) {
+  parallel_for(n_mg, [=](int mg) {
     for (int kg = 0; kg < n_kg; ++kg) {
       const size_t su = (size_t)mg * n_kg + kg;
       for (int lane = 0; lane < 32; ++lane) {
@@ -430,7 +452,7 @@ int vq3_unpack_layout(const void* packed_host, int d_in, int d_out, uint8_t* can
         }
       }
     }
-  }
+  });
   return ok();
 }
 
