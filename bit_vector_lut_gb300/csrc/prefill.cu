@@ -35,6 +35,8 @@
 // carries on to its end (results invalid).
 #include <cuda_fp16.h>
 
+#include <utility>
+
 #include "vq3_internal.h"
 
 namespace vq3 {
@@ -179,43 +181,39 @@ __device__ __forceinline__ uint32_t tile_off(int row, int k, int rows) {
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
-// Decodes the producer thread's share of the weight tile of one K step: a
-// quarter (k-step s of 16 inputs) of lane string L of super-unit su of the tile.
-// A-fragment order of the lane string (see vq3_internal.h): index n = (s*4 + m)*4
-// + e is pair m*8 + g at input s*16 + {2t, 2t+1, 2t+8, 2t+9}[e].
-template <int S, int M>
-__device__ __forceinline__ void decode_pairs(const uint32_t (&w)[12], int g, int t, int row0, uint32_t a_tile,
-                                             uint32_t lanebase) {
-  constexpr int n0 = (S * 4 + M) * 4;
-  const uint32_t l0 = lds32(lut_addr<n0 + 0>(w, lanebase));
-  const uint32_t l1 = lds32(lut_addr<n0 + 1>(w, lanebase));
-  const uint32_t l2 = lds32(lut_addr<n0 + 2>(w, lanebase));
-  const uint32_t l3 = lds32(lut_addr<n0 + 3>(w, lanebase));
-  const int r = row0 + 2 * (M * 8 + g);  // channel 2p of the tile; 2p+1 is the next row
-  const int k = S * 16 + 2 * t;
-  sts32(a_tile + tile_off(r, k, kTileM), __byte_perm(l0, l1, 0x5410));
-  sts32(a_tile + tile_off(r + 1, k, kTileM), __byte_perm(l0, l1, 0x7632));
-  sts32(a_tile + tile_off(r, k + 8, kTileM), __byte_perm(l2, l3, 0x5410));
-  sts32(a_tile + tile_off(r + 1, k + 8, kTileM), __byte_perm(l2, l3, 0x7632));
+template <int N0, int... J>
+__device__ __forceinline__ void lookups(const uint32_t (&w)[12], uint32_t lanebase, uint32_t (&lk)[32],
+                                        std::integer_sequence<int, J...>) {
+  ((lk[J] = lds32(lut_addr<N0 + J>(w, lanebase))), ...);
 }
 
-template <int S>
-__device__ __forceinline__ void decode_quarter_s(const uint32_t (&w)[12], int lane, int row0, uint32_t a_tile,
-                                                 uint32_t lanebase) {
+// Decodes the producer thread's share of the weight tile of one K step: half
+// (input steps S0 = 2*HH and S0 + 1, 16 inputs each) of lane string L = lane of
+// one super-unit. A-fragment order of the lane string (see vq3_internal.h):
+// index n = (s*4 + m)*4 + e is pair m*8 + g at input s*16 + {2t, 2t+1, 2t+8, 2t+9}[e]
+// with g = L/4, t = L%4. All 32 lookups are issued before the first store, so
+// one shared-memory latency covers them. Channels 2p and 2p+1 of a pair are 16
+// bytes apart in the tile; lanes with g >= 4 store the odd channel first, which
+// puts the 32 lanes of each store on 32 different banks.
+template <int HH>
+__device__ __forceinline__ void decode_half(const uint32_t (&w)[12], int lane, int row0, uint32_t a_tile,
+                                            uint32_t lanebase) {
+  uint32_t lk[32];
+  lookups<HH * 32>(w, lanebase, lk, std::make_integer_sequence<int, 32>{});
   const int g = lane >> 2, t = lane & 3;
-  decode_pairs<S, 0>(w, g, t, row0, a_tile, lanebase);
-  decode_pairs<S, 1>(w, g, t, row0, a_tile, lanebase);
-  decode_pairs<S, 2>(w, g, t, row0, a_tile, lanebase);
-  decode_pairs<S, 3>(w, g, t, row0, a_tile, lanebase);
-}
-
-__device__ __forceinline__ void decode_quarter(const uint32_t (&w)[12], int s, int lane, int row0, uint32_t a_tile,
-                                               uint32_t lanebase) {
-  switch (s) {
-    case 0: decode_quarter_s<0>(w, lane, row0, a_tile, lanebase); break;
-    case 1: decode_quarter_s<1>(w, lane, row0, a_tile, lanebase); break;
-    case 2: decode_quarter_s<2>(w, lane, row0, a_tile, lanebase); break;
-    default: decode_quarter_s<3>(w, lane, row0, a_tile, lanebase); break;
+  const uint32_t swap = g >= 4 ? 16u : 0u;
+  const uint32_t sel_a = g >= 4 ? 0x7632u : 0x5410u, sel_b = sel_a ^ 0x2222u;
+#pragma unroll
+  for (int sm = 0; sm < 8; ++sm) {  // (s - S0, m)
+    const int S = 2 * HH + (sm >> 2), M = sm & 3;
+    const uint32_t* l = lk + 4 * sm;
+    const int r = row0 + 2 * (M * 8 + g);  // channel 2p of the tile; 2p+1 is the next row
+    const int k = S * 16 + 2 * t;
+    const uint32_t o0 = a_tile + tile_off(r, k, kTileM), o8 = a_tile + tile_off(r, k + 8, kTileM);
+    sts32(o0 + swap, __byte_perm(l[0], l[1], sel_a));
+    sts32(o0 + (16u - swap), __byte_perm(l[0], l[1], sel_b));
+    sts32(o8 + swap, __byte_perm(l[2], l[3], sel_a));
+    sts32(o8 + (16u - swap), __byte_perm(l[2], l[3], sel_b));
   }
 }
 
@@ -314,9 +312,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs 
     cp_async_wait_all();
   } else if (warp < kLoadWarps + kDecWarps) {
     // ------------------------------------------------------------ decoders
-    // thread -> (super-unit su of the tile, lane string L, half hh of the string)
+    // warp -> (super-unit su of the tile, half hh of the lane strings); lane -> lane string
     const int dt = tid - kLoadWarps * 32;
-    const int su = dt >> 6, L = (dt >> 1) & 31, hh = dt & 1;
+    const int su = dt >> 6, hh = (dt >> 5) & 1, L = lane;
     const int mg1 = a.swiglu ? mt : 2 * mt + 1;
     const bool live = su == 0 || a.swiglu || mg1 < a.d_out / 64;
     const uint32_t lanebase = tabs | (uint32_t)(lane * 4) | ((a.swiglu && su == 1) ? 8192u : 0u);
@@ -337,8 +335,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs 
           w[4 * q + 2] = v2;
           w[4 * q + 3] = v3;
         }
-        decode_quarter(w, 2 * hh, L, su * 64, a_tile(st), lanebase);
-        decode_quarter(w, 2 * hh + 1, L, su * 64, a_tile(st), lanebase);
+        if (hh == 0)
+          decode_half<0>(w, L, su * 64, a_tile(st), lanebase);
+        else
+          decode_half<1>(w, L, su * 64, a_tile(st), lanebase);
       }
       fence_proxy_async();  // the generic-proxy writes of A, before the MMA reads them
       mbar_arrive(full_bar(st));
