@@ -98,44 +98,51 @@ CtlLayout ctl_linear(int d_in, int d_out) {
   return c;
 }
 
-// [status word (256 B)][pieces][counter words, zero between calls]
+// Every workspace starts [status word (256 B)][counter words, zero between
+// calls]. The decode kernel's hand-over counters and the prefill GEMM's part
+// flags share the counter words, so one workspace serves any row count.
+constexpr size_t kCtlOffset = 256;
+
+size_t ctl_bytes(int n_words) {
+  const int n = n_words > prefill_max_grid() ? n_words : prefill_max_grid();
+  return round_up((size_t)n * sizeof(unsigned), 256);
+}
+size_t mlp_ctl_bytes(int H, int I) { return ctl_bytes(ctl_mlp(H, I).n); }
+size_t linear_ctl_bytes(int d_in, int d_out) { return ctl_bytes(ctl_linear(d_in, d_out).n); }
+
+// [status word][counter words][pieces]
 struct LinearWs {
-  size_t status, pieces, counters, total;
+  size_t status, counters, pieces, total;
 };
 
 LinearWs linear_ws(int rows, int d_in, int d_out) {
   LinearWs w{};
-  size_t off = 0;
-  w.status = off;
-  off += 256;
+  w.status = 0;
+  w.counters = kCtlOffset;
+  size_t off = kCtlOffset + linear_ctl_bytes(d_in, d_out);
   w.pieces = off;
   off = round_up(off + persist_pieces_bytes(rows, d_in, d_out, 1), 256);
-  w.counters = off;
-  off = round_up(off + (size_t)ctl_linear(d_in, d_out).n * sizeof(unsigned), 256);
   w.total = off;
   return w;
 }
 
-// [status word (256 B)][h of one pass, fp32][gate/up pieces][down pieces]
-// [counter words, zero between calls]
+// [status word][counter words][h of one pass, fp32][gate/up pieces][down pieces]
 struct MlpWs {
-  size_t status, hbuf, pieces1, pieces3, counters, total;
+  size_t status, counters, hbuf, pieces1, pieces3, total;
 };
 
 MlpWs mlp_ws(int rows, const vq3_mlp_layer* l) {
   MlpWs w{};
   const int H = l->gate.d_in, I = l->gate.d_out;
-  size_t off = 0;
-  w.status = off;
-  off += 256;
+  w.status = 0;
+  w.counters = kCtlOffset;
+  size_t off = kCtlOffset + mlp_ctl_bytes(H, I);
   w.hbuf = off;
   off = round_up(off + (size_t)8 * dec_tiles_per_pass(rows) * I * sizeof(float), 256);
   w.pieces1 = off;
   off = round_up(off + persist_pieces_bytes(rows, H, I, 2), 256);
   w.pieces3 = off;
   off = round_up(off + persist_pieces_bytes(rows, I, H, 1), 256);
-  w.counters = off;
-  off = round_up(off + (size_t)ctl_mlp(H, I).n * sizeof(unsigned), 256);
   w.total = off;
   return w;
 }
@@ -233,27 +240,31 @@ cudaError_t run_persistent(const uint16_t* x, int rows, int nt, const vq3_mlp_la
 
 constexpr int kPrefillRows = 64;  // from this many rows on, the tcgen05 path
 
-// [status word (256 B)][x' FP16 [rows][d_in]][h FP32 [rows][d_inter]][h' FP16 [rows][d_inter]]
+// [status word][counter words: part flags][x' FP16 [rows][d_in]]
+// [h FP32 [rows][d_inter]][h' FP16 [rows][d_inter]][parts of split tiles]
 struct PrefillWs {
-  size_t status, xr, h, hr, total;
+  size_t status, flags, xr, h, hr, part, total;
 };
 
-PrefillWs prefill_ws(int rows, int d_in, int d_inter) {
+PrefillWs prefill_ws(int rows, int d_in, int d_inter, size_t ctl) {
   PrefillWs w{};
-  size_t off = 0;
-  w.status = off;
-  off += 256;
+  w.status = 0;
+  w.flags = kCtlOffset;
+  size_t off = kCtlOffset + ctl;
   w.xr = off;
   off = round_up(off + (size_t)rows * d_in * 2, 256);
   w.h = off;
   off = round_up(off + (size_t)rows * d_inter * 4, 256);
   w.hr = off;
   off = round_up(off + (size_t)rows * d_inter * 2, 256);
+  w.part = off;
+  off = round_up(off + prefill_part_bytes(rows), 256);
   w.total = off;
   return w;
 }
 
-PrefillArgs prefill_args(const uint16_t* xr, int rows, const vq3_linear& m0, const vq3_linear* m1, int* status) {
+PrefillArgs prefill_args(const uint16_t* xr, int rows, const vq3_linear& m0, const vq3_linear* m1, char* ws,
+                         const PrefillWs& w) {
   PrefillArgs a{};
   a.x = xr;
   a.rows = rows;
@@ -268,36 +279,37 @@ PrefillArgs prefill_args(const uint16_t* xr, int rows, const vq3_linear& m0, con
     a.cb1 = reinterpret_cast<const uint32_t*>(m1->codebook);
     a.scale1 = m1->scales;
   }
-  a.status = status;
+  a.status = reinterpret_cast<int*>(ws + w.status);
+  a.flags = reinterpret_cast<unsigned*>(ws + w.flags);
+  a.part = reinterpret_cast<float*>(ws + w.part);
   return a;
 }
 
 cudaError_t run_prefill_mlp(const uint16_t* x, int rows, const vq3_mlp_layer& l, char* ws, uint16_t* out,
                             cudaStream_t st) {
   const int H = l.gate.d_in, I = l.gate.d_out;
-  const PrefillWs w = prefill_ws(rows, H, I);
+  const PrefillWs w = prefill_ws(rows, H, I, mlp_ctl_bytes(H, I));
   uint16_t* xr = reinterpret_cast<uint16_t*>(ws + w.xr);
   float* h = reinterpret_cast<float*>(ws + w.h);
   uint16_t* hr = reinterpret_cast<uint16_t*>(ws + w.hr);
-  int* status = reinterpret_cast<int*>(ws + w.status);
   cudaError_t e = launch_fwht(x, rows, H, l.gate.block, l.gate.signs, xr, st);
   if (e != cudaSuccess) return e;
-  PrefillArgs gu = prefill_args(xr, rows, l.gate, &l.up, status);
+  PrefillArgs gu = prefill_args(xr, rows, l.gate, &l.up, ws, w);
   gu.out32 = h;
   if ((e = launch_prefill_gemm(gu, st)) != cudaSuccess) return e;
   if ((e = launch_fwht_f32(h, rows, I, l.down.block, l.down.signs, hr, st)) != cudaSuccess) return e;
-  PrefillArgs dn = prefill_args(hr, rows, l.down, nullptr, status);
+  PrefillArgs dn = prefill_args(hr, rows, l.down, nullptr, ws, w);
   dn.out16 = out;
   return launch_prefill_gemm(dn, st);
 }
 
 cudaError_t run_prefill_linear(const uint16_t* x, int rows, const vq3_linear& L, char* ws, uint16_t* out,
                                cudaStream_t st) {
-  const PrefillWs w = prefill_ws(rows, L.d_in, 0);
+  const PrefillWs w = prefill_ws(rows, L.d_in, 0, linear_ctl_bytes(L.d_in, L.d_out));
   uint16_t* xr = reinterpret_cast<uint16_t*>(ws + w.xr);
   cudaError_t e = launch_fwht(x, rows, L.d_in, L.block, L.signs, xr, st);
   if (e != cudaSuccess) return e;
-  PrefillArgs a = prefill_args(xr, rows, L, nullptr, reinterpret_cast<int*>(ws + w.status));
+  PrefillArgs a = prefill_args(xr, rows, L, nullptr, ws, w);
   a.out16 = out;
   return launch_prefill_gemm(a, st);
 }
@@ -371,10 +383,9 @@ int device_sm_count() {
   return cache[dev];
 }
 
-void mlp_counter_range(int rows, int pass_cap, const vq3_mlp_layer* layer, size_t* offset, size_t* bytes) {
-  const MlpWs w = mlp_ws(rows < pass_cap ? rows : pass_cap, layer);
-  *offset = w.counters;
-  *bytes = w.total - w.counters;
+void mlp_counter_range(const vq3_mlp_layer* layer, size_t* offset, size_t* bytes) {
+  *offset = kCtlOffset;
+  *bytes = mlp_ctl_bytes(layer->gate.d_in, layer->gate.d_out);
 }
 
 }  // namespace vq3
@@ -471,13 +482,14 @@ int fwht_rotate(const uint16_t* x, int rows, int n, int block, const uint32_t* s
 
 size_t vq3_linear_workspace_bytes(int rows, const vq3_linear* L) {
   if (!L || rows < 0 || !layout_supported(L->d_in, L->d_out)) return 0;
-  if (rows >= kPrefillRows) return prefill_ws(rows, L->d_in, 0).total;
+  if (rows >= kPrefillRows) return prefill_ws(rows, L->d_in, 0, linear_ctl_bytes(L->d_in, L->d_out)).total;
   return linear_ws(rows, L->d_in, L->d_out).total;
 }
 
 size_t vq3_mlp_workspace_bytes(int rows, const vq3_mlp_layer* layer) {
   if (!layer || rows < 0 || !layout_supported(layer->gate.d_in, layer->gate.d_out)) return 0;
-  if (rows >= kPrefillRows) return prefill_ws(rows, layer->gate.d_in, layer->gate.d_out).total;
+  const int H = layer->gate.d_in, I = layer->gate.d_out;
+  if (rows >= kPrefillRows) return prefill_ws(rows, H, I, mlp_ctl_bytes(H, I)).total;
   return mlp_ws(rows, layer).total;
 }
 
@@ -509,7 +521,7 @@ int vq3_linear_forward(const uint16_t* x, int rows, const vq3_linear* L, uint16_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   if (rows >= kPrefillRows) {
-    const size_t need = prefill_ws(rows, L->d_in, 0).total;
+    const size_t need = prefill_ws(rows, L->d_in, 0, linear_ctl_bytes(L->d_in, L->d_out)).total;
     if (ws_bytes < need) return fail(VQ3_ENOSPACE, "linear: workspace %zu < %zu bytes", ws_bytes, need);
     cudaError_t e = run_prefill_linear(x, rows, *L, ws, out, st);
     if (e != cudaSuccess) return cuda_fail(e, "linear: launch");
@@ -603,7 +615,8 @@ int vq3_mlp_forward(const uint16_t* x, int rows, const vq3_mlp_layer* layer, uin
   if (!x || !out || !workspace) return fail(VQ3_EINVAL, "mlp: null x/out/workspace");
   if (!aligned(x, 16) || !aligned(out, 16) || !aligned(workspace, 256))
     return fail(VQ3_EALIGN, "mlp: x/out must be 16-byte aligned and the workspace 256-byte aligned");
-  const size_t need = prefill_ws(rows, layer->gate.d_in, layer->gate.d_out).total;
+  const int H = layer->gate.d_in, I = layer->gate.d_out;
+  const size_t need = prefill_ws(rows, H, I, mlp_ctl_bytes(H, I)).total;
   if (ws_bytes < need) return fail(VQ3_ENOSPACE, "mlp: workspace %zu < %zu bytes", ws_bytes, need);
   cudaError_t e = run_prefill_mlp(x, rows, *layer, static_cast<char*>(workspace), out, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "mlp: launch");

@@ -73,7 +73,7 @@ extern "C" int vq3_mlp_forward_noalloc(const uint16_t* x, int rows, const vq3_ml
                      cudaGetErrorString(e));
   // The array keeps the previous call's contents; the counter words must start at zero.
   size_t off = 0, bytes = 0;
-  mlp_counter_range(rows, cap, layer, &off, &bytes);
+  mlp_counter_range(layer, &off, &bytes);
   e = cudaMemsetAsync(static_cast<char*>(scratch) + off, 0, bytes, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess)
     return set_error(VQ3_ECUDA, "mlp_noalloc: clearing counters: %s (%s)", cudaGetErrorName(e),

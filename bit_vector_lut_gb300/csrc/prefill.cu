@@ -42,11 +42,13 @@
 namespace vq3 {
 namespace {
 
-constexpr int kPThreads = 12 * 32;
+constexpr int kPThreads = 13 * 32;
 constexpr int kLoadWarps = 4;  // warps 0-3
 constexpr int kDecWarps = 4;   // warps 4-7
 constexpr int kMmaWarp = 8;
-constexpr int kEpiWarp0 = 8;
+constexpr int kEpiWarp0 = 9;   // warps 9-12
+constexpr int kEpiThreads = 4 * 32;
+constexpr int kMinSteps = 8;  // fewest K steps per CTA
 constexpr int kStages = 3;
 constexpr int kTileM = 128;                    // output channels per tile
 constexpr int kATile = kTileM * 64 * 2;        // 16 KB of FP16
@@ -227,10 +229,38 @@ struct PfSmem {
   static constexpr int kTotal = 1024 + kStages * kStageBytes + (int)kTabAlign + 2 * kTabWords * 4 + 64 * 16 * 4;
 };
 
+// This CTA's share of the (tile, K step) space: steps [begin(c), begin(c + 1)).
+__host__ __device__ __forceinline__ long long range_begin(int c, long long work, int grid) {
+  return work * c / grid;
+}
+
+// One segment of a CTA's range: K steps [k0, k1) of tile t.
+struct Seg {
+  int t, k0, k1;
+};
+__device__ __forceinline__ Seg seg_at(long long s, long long s1, int n_kg) {
+  Seg g;
+  g.t = (int)(s / n_kg);
+  g.k0 = (int)(s - (long long)g.t * n_kg);
+  const long long left = s1 - s;
+  g.k1 = left < (long long)(n_kg - g.k0) ? g.k0 + (int)left : n_kg;
+  return g;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// One CTA per SM: the smallest configuration still needs more than half of an
+// SM's shared memory, so no two CTAs ever share an SM (and its tensor memory).
+static_assert(2 * PfSmem<64>::kTotal > 228 * 1024, "one prefill CTA per SM");
+
 template <int N>
 __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs a) {
   extern __shared__ __align__(16) unsigned char dsm[];
-  __shared__ __align__(8) unsigned long long s_bars[3 * kStages + 1];
+  __shared__ __align__(8) unsigned long long s_bars[3 * kStages + 4];
   __shared__ uint32_t s_tmem;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t raw = smem_u32(dsm);
@@ -241,14 +271,16 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs 
   auto full_bar = [&](int s) { return bar0 + 8u * s; };                 // A decoded
   auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };    // stage consumed
   auto load_bar = [&](int s) { return bar0 + 8u * (2 * kStages + s); }; // B and indices landed
-  const uint32_t dfull_bar = bar0 + 8u * (3 * kStages);
+  auto acc_full = [&](int b) { return bar0 + 8u * (3 * kStages + b); }; // accumulator b complete
+  auto acc_empty = [&](int b) { return bar0 + 8u * (3 * kStages + 2 + b); };  // accumulator b drained
   auto a_tile = [&](int s) { return base + (uint32_t)(s * PfSmem<N>::kStageBytes); };
   auto b_tile = [&](int s) { return base + (uint32_t)(s * PfSmem<N>::kStageBytes + kATile); };
   auto i_tile = [&](int s) { return base + (uint32_t)(s * PfSmem<N>::kStageBytes + kATile + PfSmem<N>::kBTile); };
 
-  const int mt = blockIdx.x;        // output tile
-  const int row0 = blockIdx.y * N;  // first row of the tile
   const int n_kg = a.d_in / 64;
+  const int n_tiles = (a.rows + N - 1) / N;  // row tiles
+  const long long s0 = range_begin(blockIdx.x, a.work, gridDim.x);
+  const long long s1 = range_begin(blockIdx.x + 1, a.work, gridDim.x);
 
   // codebook tables (lane-private copies): matrix 0 at tabs, matrix 1 at tabs + 8192
   for (int i = tid; i < 2 * 64 * 8; i += kPThreads) {
@@ -267,12 +299,15 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs 
       mbar_init(empty_bar(s), 1);
       mbar_init(load_bar(s), kLoadWarps * 32);
     }
-    mbar_init(dfull_bar, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), kEpiThreads);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
-                 "r"((uint32_t)(N < 32 ? 32 : N))
+                 "r"((uint32_t)(2 * N))
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -284,30 +319,36 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs 
   if (warp < kLoadWarps) {
     // ------------------------------------------------------------ loaders
     const int rows = a.rows;
-    // the tile's two super-units: (matrix, channel group); the second is past the
-    // last channel when d_out is an odd multiple of 64 (its A rows are never stored)
-    const int mg0 = a.swiglu ? mt : 2 * mt, mg1 = a.swiglu ? mt : 2 * mt + 1;
-    const bool live1 = a.swiglu || mg1 < a.d_out / 64;
-    const uint4* su0 = a.packed0 + (size_t)mg0 * n_kg * kSuUint4;
-    const uint4* su1 = (a.swiglu ? a.packed1 : a.packed0) + (size_t)(live1 ? mg1 : mg0) * n_kg * kSuUint4;
-    for (int kk = 0; kk < n_kg; ++kk) {
-      const int st = kk % kStages;
-      if (kk >= kStages) mbar_wait(empty_bar(st), (uint32_t)((kk / kStages - 1) & 1), a.status);
-      // activation tile: N rows x 64 inputs (128 bytes per row), 16 bytes per
-      // copy, in the 128-byte swizzle layout; eight consecutive threads copy one row
-      const uint32_t bt = b_tile(st);
-      for (int e = tid; e < N * 8; e += kLoadWarps * 32) {
-        const int n = e >> 3, c = e & 7;
-        const int r = row0 + n;
-        const uint16_t* src = a.x + (size_t)(r < rows ? r : 0) * a.d_in + kk * 64 + c * 8;
-        cp_async16_zfill(bt + (uint32_t)((n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4)), src, r < rows);
+    int it = 0;
+    for (long long s = s0; s < s1;) {
+      const Seg g = seg_at(s, s1, n_kg);
+      const int mt = g.t / n_tiles, row0 = (g.t - mt * n_tiles) * N;
+      // the tile's two super-units: (matrix, channel group); the second is past the
+      // last channel when d_out is an odd multiple of 64 (its A rows are never stored)
+      const int mg0 = a.swiglu ? mt : 2 * mt, mg1 = a.swiglu ? mt : 2 * mt + 1;
+      const bool live1 = a.swiglu || mg1 < a.d_out / 64;
+      const uint4* su0 = a.packed0 + (size_t)mg0 * n_kg * kSuUint4;
+      const uint4* su1 = (a.swiglu ? a.packed1 : a.packed0) + (size_t)(live1 ? mg1 : mg0) * n_kg * kSuUint4;
+      for (int kk = g.k0; kk < g.k1; ++kk, ++it) {
+        const int st = it % kStages;
+        if (it >= kStages) mbar_wait(empty_bar(st), (uint32_t)((it / kStages - 1) & 1), a.status);
+        // activation tile: N rows x 64 inputs (128 bytes per row), 16 bytes per
+        // copy, in the 128-byte swizzle layout; eight consecutive threads copy one row
+        const uint32_t bt = b_tile(st);
+        for (int e = tid; e < N * 8; e += kLoadWarps * 32) {
+          const int n = e >> 3, c = e & 7;
+          const int r = row0 + n;
+          const uint16_t* src = a.x + (size_t)(r < rows ? r : 0) * a.d_in + kk * 64 + c * 8;
+          cp_async16_zfill(bt + (uint32_t)((n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4)), src, r < rows);
+        }
+        // index strings of the two super-units (96 16-byte chunks each)
+        for (int e = tid; e < 2 * kSuUint4; e += kLoadWarps * 32) {
+          const uint4* src = (e < kSuUint4 ? su0 : su1) + (size_t)kk * kSuUint4 + (e % kSuUint4);
+          cp_async16(i_tile(st) + (uint32_t)(e * 16), src);
+        }
+        cp_async_arrive(load_bar(st));
       }
-      // index strings of the two super-units (96 16-byte chunks each)
-      for (int e = tid; e < 2 * kSuUint4; e += kLoadWarps * 32) {
-        const uint4* s = (e < kSuUint4 ? su0 : su1) + (size_t)kk * kSuUint4 + (e % kSuUint4);
-        cp_async16(i_tile(st) + (uint32_t)(e * 16), s);
-      }
-      cp_async_arrive(load_bar(st));
+      s += g.k1 - g.k0;
     }
     cp_async_wait_all();
   } else if (warp < kLoadWarps + kDecWarps) {
@@ -315,105 +356,190 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs 
     // warp -> (super-unit su of the tile, half hh of the lane strings); lane -> lane string
     const int dt = tid - kLoadWarps * 32;
     const int su = dt >> 6, hh = (dt >> 5) & 1, L = lane;
-    const int mg1 = a.swiglu ? mt : 2 * mt + 1;
-    const bool live = su == 0 || a.swiglu || mg1 < a.d_out / 64;
     const uint32_t lanebase = tabs | (uint32_t)(lane * 4) | ((a.swiglu && su == 1) ? 8192u : 0u);
-    for (int kk = 0; kk < n_kg; ++kk) {
-      const int st = kk % kStages;
-      if (kk >= kStages) mbar_wait(empty_bar(st), (uint32_t)((kk / kStages - 1) & 1), a.status);
-      mbar_wait(load_bar(st), (uint32_t)((kk / kStages) & 1), a.status);
-      if (live) {
-        uint32_t w[12];
-        const uint32_t is = i_tile(st) + (uint32_t)(su * kSuBytes);
+    int it = 0;
+    for (long long s = s0; s < s1;) {
+      const Seg g = seg_at(s, s1, n_kg);
+      const int mt = g.t / n_tiles;
+      const bool live = su == 0 || a.swiglu || 2 * mt + 1 < a.d_out / 64;
+      for (int kk = g.k0; kk < g.k1; ++kk, ++it) {
+        const int st = it % kStages;
+        if (it >= kStages) mbar_wait(empty_bar(st), (uint32_t)((it / kStages - 1) & 1), a.status);
+        mbar_wait(load_bar(st), (uint32_t)((it / kStages) & 1), a.status);
+        if (live) {
+          uint32_t w[12];
+          const uint32_t is = i_tile(st) + (uint32_t)(su * kSuBytes);
 #pragma unroll
-        for (int q = 0; q < 3; ++q) {
-          const uint32_t o = is + (uint32_t)((q * 32 + L) * 16);
-          uint32_t v0, v1, v2, v3;
-          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3) : "r"(o));
-          w[4 * q + 0] = v0;
-          w[4 * q + 1] = v1;
-          w[4 * q + 2] = v2;
-          w[4 * q + 3] = v3;
+          for (int q = 0; q < 3; ++q) {
+            const uint32_t o = is + (uint32_t)((q * 32 + L) * 16);
+            uint32_t v0, v1, v2, v3;
+            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3) : "r"(o));
+            w[4 * q + 0] = v0;
+            w[4 * q + 1] = v1;
+            w[4 * q + 2] = v2;
+            w[4 * q + 3] = v3;
+          }
+          if (hh == 0)
+            decode_half<0>(w, L, su * 64, a_tile(st), lanebase);
+          else
+            decode_half<1>(w, L, su * 64, a_tile(st), lanebase);
         }
-        if (hh == 0)
-          decode_half<0>(w, L, su * 64, a_tile(st), lanebase);
-        else
-          decode_half<1>(w, L, su * 64, a_tile(st), lanebase);
+        fence_proxy_async();  // the generic-proxy writes of A, before the MMA reads them
+        mbar_arrive(full_bar(st));
       }
-      fence_proxy_async();  // the generic-proxy writes of A, before the MMA reads them
-      mbar_arrive(full_bar(st));
+      s += g.k1 - g.k0;
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(kTileM, N);
-      for (int kk = 0; kk < n_kg; ++kk) {
-        const int st = kk % kStages;
-        mbar_wait(load_bar(st), (uint32_t)((kk / kStages) & 1), a.status);
-        mbar_wait(full_bar(st), (uint32_t)((kk / kStages) & 1), a.status);
-        fence_proxy_async();  // the activation tile (cp.async, generic proxy) before the MMA reads it
+      int it = 0, q = 0;
+      for (long long s = s0; s < s1; ++q) {
+        const Seg g = seg_at(s, s1, n_kg);
+        const int b = q & 1;
+        if (q >= 2) mbar_wait(acc_empty(b), (uint32_t)(((q >> 1) - 1) & 1), a.status);
         tc_fence_after();
+        const uint32_t acc = tmem + (uint32_t)(b * N);
+        for (int kk = g.k0; kk < g.k1; ++kk, ++it) {
+          const int st = it % kStages;
+          mbar_wait(load_bar(st), (uint32_t)((it / kStages) & 1), a.status);
+          mbar_wait(full_bar(st), (uint32_t)((it / kStages) & 1), a.status);
+          fence_proxy_async();  // the activation tile (cp.async, generic proxy) before the MMA reads it
+          tc_fence_after();
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          // K = 16: two core matrices along K
-          const uint64_t ad = smem_desc(a_tile(st) + (uint32_t)(j * 2 * kTileM * 16), kTileM * 16, 128);
-          const uint64_t bd = smem_desc_sw128(b_tile(st) + (uint32_t)(j * 32));
-          mma_ss(tmem, ad, bd, idesc, (kk > 0 || j > 0) ? 1u : 0u);
+          for (int j = 0; j < 4; ++j) {
+            // K = 16: two core matrices along K
+            const uint64_t ad = smem_desc(a_tile(st) + (uint32_t)(j * 2 * kTileM * 16), kTileM * 16, 128);
+            const uint64_t bd = smem_desc_sw128(b_tile(st) + (uint32_t)(j * 32));
+            mma_ss(acc, ad, bd, idesc, (kk > g.k0 || j > 0) ? 1u : 0u);
+          }
+          mma_commit(empty_bar(st));
         }
-        mma_commit(empty_bar(st));
+        mma_commit(acc_full(b));
+        s += g.k1 - g.k0;
       }
-      mma_commit(dfull_bar);
     }
-  }
-  if (warp >= kEpiWarp0) {
+    __syncwarp();
+  } else {
     // ------------------------------------------------------------ epilogue
-    __syncwarp();  // the MMA warp's lanes reconverge once lane 0 has issued every MMA
-    const int quarter = warp - kEpiWarp0;  // TMEM lanes 32*quarter .. +31 = tile rows
-    const int row = quarter * 32 + lane;   // tile row = output channel of the tile
-    mbar_wait(dfull_bar, 0u, a.status);
-    tc_fence_after();
-    const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
-    if (!a.swiglu) {
-      const int ch = mt * kTileM + row;
-      const bool live = ch < a.d_out;
-      const float sc = live ? __half2float(__ushort_as_half(a.scale0[ch])) : 0.f;
+    // TMEM lanes 32*(warp % 4) .. +31 = tile rows = output channels of the tile
+    const int row = (warp & 3) * 32 + lane;
+    const int e = tid - kEpiWarp0 * 32;
+    const bool waits = *(volatile int*)a.status == 0;
+    int q = 0;
+    for (long long s = s0; s < s1; ++q) {
+      const Seg g = seg_at(s, s1, n_kg);
+      const int mt = g.t / n_tiles, row0 = (g.t - mt * n_tiles) * N;
+      const int cols = a.rows - row0 < N ? a.rows - row0 : N;  // valid rows of this tile
+      const int b = q & 1;
+      mbar_wait(acc_full(b), (uint32_t)((q >> 1) & 1), a.status);
+      tc_fence_after();
+      const uint32_t taddr = tmem + (uint32_t)(b * N) + ((uint32_t)((warp & 3) * 32) << 16);
+      if (g.k0 > 0) {
+        // a later part of a tile started by an earlier CTA: hand the raw sums over
+        float* part = a.part + (size_t)blockIdx.x * kTileM * N;
 #pragma unroll 1
-      for (int c0 = 0; c0 < N; c0 += 16) {
-        uint32_t r[16];
-        tmem_ld16(taddr + (uint32_t)c0, r);
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        for (int c0 = 0; c0 < cols; c0 += 16) {
+          uint32_t r[16];
+          tmem_ld16(taddr + (uint32_t)c0, r);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int rr = row0 + c0 + j;
-          if (live && rr < a.rows)
-            a.out16[(size_t)rr * a.d_out + ch] = __half_as_ushort(__float2half_rn(sc * __uint_as_float(r[j])));
+          for (int j = 0; j < 16; ++j) __stcg(part + (size_t)(c0 + j) * kTileM + row, __uint_as_float(r[j]));
         }
-      }
-    } else {
-      // rows 0-63: gate channel mt*64 + row; rows 64-127: up channel mt*64 + row - 64
-      const int jch = mt * 64 + (row & 63);
-      const bool up = row >= 64;
-      const float sc = __half2float(__ushort_as_half(up ? a.scale1[jch] : a.scale0[jch]));
-#pragma unroll 1
-      for (int c0 = 0; c0 < N; c0 += 16) {
-        uint32_t r[16];
-        tmem_ld16(taddr + (uint32_t)c0, r);
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        if (up) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) xch[(row - 64) * 16 + j] = sc * __uint_as_float(r[j]);
-        }
+        tc_fence_before();
+        mbar_arrive(acc_empty(b));
+        __threadfence();
         asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (!up) {
+        if (e == 0) asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a.flags + blockIdx.x), "r"(1u) : "memory");
+      } else {
+        // the tile's first part: add the later parts (CTAs blockIdx.x + 1 ...) in K order
+        int n_parts = 0;
+        if (g.k1 < n_kg) {
+          const long long tile_end = (long long)(g.t + 1) * n_kg;
+          while ((int)blockIdx.x + 1 + n_parts < (int)gridDim.x &&
+                 range_begin(blockIdx.x + 1 + n_parts, a.work, gridDim.x) < tile_end)
+            ++n_parts;
+          if (e == 0 && waits) {
+            for (int p = 1; p <= n_parts; ++p) {
+              long long spin = 0;
+              while (ld_acquire_u32(a.flags + blockIdx.x + p) == 0u) {
+                if (++spin > kWaitSpin) {
+                  atomicExch(a.status, 3);
+                  break;
+                }
+                __nanosleep(64);
+              }
+            }
+          }
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+        }
+        const float* parts = a.part + (size_t)(blockIdx.x + 1) * kTileM * N;
+        if (!a.swiglu) {
+          const int ch = mt * kTileM + row;
+          const bool live = ch < a.d_out;
+          const float sc = live ? __half2float(__ushort_as_half(a.scale0[ch])) : 0.f;
+#pragma unroll 1
+          for (int c0 = 0; c0 < cols; c0 += 16) {
+            uint32_t r[16];
+            tmem_ld16(taddr + (uint32_t)c0, r);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            float v[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int rr = row0 + c0 + j;
-            const float hv = silu_f(sc * __uint_as_float(r[j])) * xch[row * 16 + j];
-            if (rr < a.rows) __stcg(a.out32 + (size_t)rr * a.d_out + jch, hv);
+            for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+            for (int p = 0; p < n_parts; ++p) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] += __ldcg(parts + (size_t)p * kTileM * N + (size_t)(c0 + j) * kTileM + row);
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int rr = row0 + c0 + j;
+              if (live && c0 + j < cols)
+                a.out16[(size_t)rr * a.d_out + ch] = __half_as_ushort(__float2half_rn(sc * v[j]));
+            }
+          }
+        } else {
+          // rows 0-63: gate channel mt*64 + row; rows 64-127: up channel mt*64 + row - 64
+          const int jch = mt * 64 + (row & 63);
+          const bool up = row >= 64;
+          const float sc = __half2float(__ushort_as_half(up ? a.scale1[jch] : a.scale0[jch]));
+#pragma unroll 1
+          for (int c0 = 0; c0 < cols; c0 += 16) {
+            uint32_t r[16];
+            tmem_ld16(taddr + (uint32_t)c0, r);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+            for (int p = 0; p < n_parts; ++p) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] += __ldcg(parts + (size_t)p * kTileM * N + (size_t)(c0 + j) * kTileM + row);
+            }
+            if (up) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) xch[(row - 64) * 16 + j] = sc * v[j];
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (!up) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int rr = row0 + c0 + j;
+                const float hv = silu_f(sc * v[j]) * xch[row * 16 + j];
+                if (c0 + j < cols) __stcg(a.out32 + (size_t)rr * a.d_out + jch, hv);
+              }
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
           }
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        tc_fence_before();
+        mbar_arrive(acc_empty(b));
+        if (n_parts) {
+          // every epilogue thread has read the parts: their flags go back to zero
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          if (e == 0)
+            for (int p = 1; p <= n_parts; ++p) a.flags[blockIdx.x + p] = 0u;
+        }
       }
+      s += g.k1 - g.k0;
     }
   }
 
@@ -421,29 +547,58 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs 
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"((uint32_t)(N < 32 ? 32 : N))
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"((uint32_t)(2 * N))
                  : "memory");
   }
 }
 
 template <int N>
-cudaError_t launch_n(const PrefillArgs& a, cudaStream_t st) {
+cudaError_t launch_n(PrefillArgs a, cudaStream_t st) {
   const int smem = PfSmem<N>::kTotal;
   cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int m_tiles = a.swiglu ? a.d_out / 64 : (a.d_out + kTileM - 1) / kTileM;
-  const dim3 grid(m_tiles, (a.rows + N - 1) / N);
-  prefill_gemm_kernel<N><<<grid, kPThreads, smem, st>>>(a);
+  a.work = prefill_work(a.rows, a.d_in, a.d_out, a.swiglu);
+  const int grid = prefill_grid(a.rows, a.d_in, a.d_out, a.swiglu);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kPThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // the first part of a split tile waits for the others
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, prefill_gemm_kernel<N>, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 }  // namespace
 
 int prefill_tile_rows(int rows) {
-  if (rows >= 256) return 256;
   if (rows > 128) return 256;
   if (rows > 64) return 128;
   return 64;
+}
+
+long long prefill_work(int rows, int d_in, int d_out, int swiglu) {
+  const long long m_tiles = swiglu ? d_out / 64 : (d_out + kTileM - 1) / kTileM;
+  const int n = prefill_tile_rows(rows);
+  return m_tiles * ((rows + n - 1) / n) * (d_in / 64);
+}
+
+int prefill_max_grid() { return device_sm_count(); }
+
+int prefill_grid(int rows, int d_in, int d_out, int swiglu) {
+  const long long work = prefill_work(rows, d_in, d_out, swiglu);
+  const long long g = work / kMinSteps;
+  const int cap = prefill_max_grid();
+  return g < 1 ? 1 : (g < cap ? (int)g : cap);
+}
+
+size_t prefill_part_bytes(int rows) {
+  return (size_t)prefill_max_grid() * kTileM * prefill_tile_rows(rows) * sizeof(float);
 }
 
 cudaError_t launch_prefill_gemm(const PrefillArgs& a, cudaStream_t st) {

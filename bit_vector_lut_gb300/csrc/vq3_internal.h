@@ -112,8 +112,15 @@ struct PrefillArgs {
   uint16_t* out16;         // [rows][d_out] FP16 (no swiglu)
   float* out32;            // [rows][d_out] FP32 (swiglu)
   int* status;             // status word (3: a wait timed out)
+  float* part;             // split-tile sums, one 128 x tile-rows FP32 slot per CTA
+  unsigned* flags;         // one word per CTA, zero between calls: its slot is filled
+  long long work;          // (tile, K step) pairs; set by launch_prefill_gemm
 };
 int prefill_tile_rows(int rows);  // rows per output tile: 64, 128 or 256
+long long prefill_work(int rows, int d_in, int d_out, int swiglu);
+int prefill_max_grid();           // most CTAs of one launch (one per SM)
+int prefill_grid(int rows, int d_in, int d_out, int swiglu);
+size_t prefill_part_bytes(int rows);  // size of PrefillArgs::part
 cudaError_t launch_prefill_gemm(const PrefillArgs& a, cudaStream_t st);
 cudaError_t launch_residual_rmsnorm(uint16_t* resid, const uint16_t* delta, int rows, int n,
                                     float eps, uint16_t* normed, cudaStream_t st);
@@ -125,8 +132,8 @@ size_t mlp_workspace_bytes_capped(int rows, const vq3_mlp_layer* layer, int pass
 int mlp_forward_capped(const uint16_t* x, int rows, const vq3_mlp_layer* layer, uint16_t* out, void* workspace,
                        size_t ws_bytes, void* stream, int pass_cap);
 
-// Byte range of the counter words inside an MLP workspace (same rows and pass cap).
-void mlp_counter_range(int rows, int pass_cap, const vq3_mlp_layer* layer, size_t* offset, size_t* bytes);
+// Byte range of the counter words inside an MLP workspace (the same for every row count).
+void mlp_counter_range(const vq3_mlp_layer* layer, size_t* offset, size_t* bytes);
 
 // Checks the arguments of an MLP call except the workspace (status as the entry points).
 int mlp_validate(const uint16_t* x, int rows, const vq3_mlp_layer* layer, const uint16_t* out);

@@ -100,7 +100,7 @@ def test_linear_256_config(vq3):
     assert_parity(got, O.linear_f64(wl.x, m), "linear 256x256 T=8")
 
 
-@pytest.mark.parametrize("rows", [1, 3, 8, 9, 16, 17, 33, 64, 100])
+@pytest.mark.parametrize("rows", [1, 3, 8, 9, 16, 17, 33, 64, 100, 300])
 def test_linear_ragged_rows(vq3, rows):
     m = S.matrix(S.rng(3), 1024, 512, 1024)
     m.signs = S.sign_bits(S.rng(3, 2), 1024)
@@ -195,6 +195,36 @@ def test_mlp_row_sweep(vq3, sweep, rows):
     # the first `rows` rows of the tallest X are the sweep input at that T
     got = vq3.mlp_forward(f16(wl.x[:rows]), layer).cpu().numpy()
     assert_parity(got, ref[:rows], f"sweep T={rows}")
+
+
+@pytest.mark.parametrize("rows", [65, 129, 300, 1000])
+def test_mlp_ragged_prefill_rows(vq3, sweep, rows):
+    """Row counts that leave a partly filled row tile (64-, 128- and 256-row tiles)."""
+    wl, blk, layer, ref = sweep
+    got = vq3.mlp_forward(f16(wl.x[:rows]), layer).cpu().numpy()
+    assert_parity(got, ref[:rows], f"ragged prefill T={rows}")
+
+
+def test_mlp_prefill_repeat_bit_identical(vq3, sweep):
+    """Split tiles are summed in a fixed order: two calls give the same bits."""
+    wl, blk, layer, ref = sweep
+    x = f16(wl.x[:512])
+    ws = vq3.workspace(vq3.mlp_workspace_bytes(512, layer))
+    a = vq3.mlp_forward(x, layer, ws=ws).clone()
+    b = vq3.mlp_forward(x, layer, ws=ws)
+    assert torch.equal(a, b)
+    assert vq3.workspace_status(ws) == 0
+
+
+def test_workspace_shared_across_row_counts(vq3, sweep):
+    """One workspace, sized for the largest call, serves the many-row and the
+    few-row path in any order (their counter words sit at the same place)."""
+    wl, blk, layer, ref = sweep
+    ws = vq3.workspace(max(vq3.mlp_workspace_bytes(r, layer) for r in (8, 32, 2048)))
+    for rows in (2048, 8, 64, 32, 2048, 1):
+        got = vq3.mlp_forward(f16(wl.x[:rows]), layer, ws=ws).cpu().numpy()
+        assert_parity(got, ref[:rows], f"shared workspace T={rows}")
+    assert vq3.workspace_status(ws) == 0
 
 
 def test_mlp_with_seeded_signs(vq3):
