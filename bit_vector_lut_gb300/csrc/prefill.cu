@@ -367,10 +367,13 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs 
         if (it >= kStages) mbar_wait(empty_bar(st), (uint32_t)((it / kStages - 1) & 1), a.status);
         mbar_wait(load_bar(st), (uint32_t)((it / kStages) & 1), a.status);
         if (live) {
-          uint32_t w[12];
+          // half hh of the string is bits [192 hh, 192 hh + 192): words 0-6 or 6-11,
+          // i.e. 16-byte chunks 0-1 or 1-2
+          uint32_t w[12] = {};
           const uint32_t is = i_tile(st) + (uint32_t)(su * kSuBytes);
 #pragma unroll
           for (int q = 0; q < 3; ++q) {
+            if (q == 2 - 2 * hh) continue;
             const uint32_t o = is + (uint32_t)((q * 32 + L) * 16);
             uint32_t v0, v1, v2, v3;
             asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3) : "r"(o));
@@ -516,14 +519,14 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs 
             }
             if (up) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j) xch[(row - 64) * 16 + j] = sc * v[j];
+              for (int j = 0; j < 16; ++j) xch[j * 64 + (row - 64)] = sc * v[j];
             }
             asm volatile("bar.sync 1, 128;" ::: "memory");
             if (!up) {
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 const int rr = row0 + c0 + j;
-                const float hv = silu_f(sc * v[j]) * xch[row * 16 + j];
+                const float hv = silu_f(sc * v[j]) * xch[j * 64 + row];
                 if (c0 + j < cols) __stcg(a.out32 + (size_t)rr * a.d_out + jch, hv);
               }
             }
