@@ -510,9 +510,8 @@ __device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cur
         const int ckg = a.chunk / kSuInputs, kg_s = (int)(rs % n_kg);
         for (int c = 0; c < n_kg / ckg; ++c)
           if (chunk_in_window(c, ckg, kg_s, len, n_kg)) poll_geq(a.ready + c, a.ready_target, status);
-        __threadfence();
       }
-      __syncthreads();
+      __syncthreads();  // thread 0's acquire loads, then the barrier: the chunks are visible to the CTA
     }
     stage_round<NT, T>(a, src, rs, len, sv);
     for (; issued < kSlots; ++issued) issue_cell(a, cur, ring_lane);  // rest of the prologue
@@ -748,7 +747,8 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
     j3.ready_target = (unsigned)(a.h_chunk / kSuChannels);
     j3.group_done = ctl + a.off_o;
     swiglu_tasks<NT>(a, j1, ctl + a.off_hd, status);
-    Cursor cur3 = decode_begin(j3, sv, kSlots);  // in flight while waiting for h chunks
+    // one cell's index copies ahead of the h rotation, the rest after it (as for x)
+    Cursor cur3 = decode_begin(j3, sv, 1);
     decode_run<NT, float>(j3, a.hbuf, cur3, sv, status);
     output_tasks<NT>(a, j3, status);
   } else {

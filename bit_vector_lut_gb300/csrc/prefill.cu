@@ -33,6 +33,7 @@
 // A 3-deep stage ring with mbarriers connects loaders, decoders and the MMA issuer. All
 // waits are bounded: one that runs out sets the status word to 3 and the kernel
 // carries on to its end (results invalid).
+#include <cuda.h>  // CUtensorMap; the encoder is fetched from the driver at run time
 #include <cuda_fp16.h>
 
 #include <utility>
@@ -42,11 +43,12 @@
 namespace vq3 {
 namespace {
 
-constexpr int kPThreads = 13 * 32;
-constexpr int kLoadWarps = 4;  // warps 0-3
-constexpr int kDecWarps = 4;   // warps 4-7
-constexpr int kMmaWarp = 8;
-constexpr int kEpiWarp0 = 9;   // warps 9-12
+constexpr int kTmaWarp = 0;                     // lane 0 issues the tile copies
+constexpr int kDecWarp0 = 1;
+constexpr int kDecWarps = 8;                    // warps 1-8
+constexpr int kMmaWarp = kDecWarp0 + kDecWarps;  // 9
+constexpr int kEpiWarp0 = kMmaWarp + 1;          // warps 10-13
+constexpr int kPThreads = (kEpiWarp0 + 4) * 32;
 constexpr int kEpiThreads = 4 * 32;
 constexpr int kMinSteps = 8;  // fewest K steps per CTA
 constexpr int kStages = 3;
@@ -84,18 +86,22 @@ __device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, int* st
   }
 }
 
-__device__ __forceinline__ void cp_async16_zfill(uint32_t saddr, const void* g, bool valid) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 16, %2;" ::"r"(saddr), "l"(g), "r"(valid ? 16 : 0) : "memory");
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
-__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(g) : "memory");
+// Tile (x, y) of a 2D tensor map into shared memory; completes `bytes` of the barrier's transaction count.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
 }
-// Arrives on the mbarrier once all of this thread's earlier cp.async copies have
-// landed (counted among the barrier's expected arrivals).
-__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+// Contiguous global -> shared copy (16-byte aligned, a multiple of 16 bytes).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -183,31 +189,31 @@ __device__ __forceinline__ uint32_t tile_off(int row, int k, int rows) {
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
-template <int N0, int... J>
-__device__ __forceinline__ void lookups(const uint32_t (&w)[12], uint32_t lanebase, uint32_t (&lk)[32],
+template <int N0, int NL, int... J>
+__device__ __forceinline__ void lookups(const uint32_t (&w)[12], uint32_t lanebase, uint32_t (&lk)[NL],
                                         std::integer_sequence<int, J...>) {
   ((lk[J] = lds32(lut_addr<N0 + J>(w, lanebase))), ...);
 }
 
-// Decodes the producer thread's share of the weight tile of one K step: half
-// (input steps S0 = 2*HH and S0 + 1, 16 inputs each) of lane string L = lane of
-// one super-unit. A-fragment order of the lane string (see vq3_internal.h):
-// index n = (s*4 + m)*4 + e is pair m*8 + g at input s*16 + {2t, 2t+1, 2t+8, 2t+9}[e]
-// with g = L/4, t = L%4. All 32 lookups are issued before the first store, so
-// one shared-memory latency covers them. Channels 2p and 2p+1 of a pair are 16
+// Decodes the producer thread's share of the weight tile of one K step: input
+// steps S0 .. S0 + NS - 1 (16 inputs each) of lane string L = lane of one
+// super-unit. A-fragment order of the lane string (see vq3_internal.h): index
+// n = (s*4 + m)*4 + e is pair m*8 + g at input s*16 + {2t, 2t+1, 2t+8, 2t+9}[e]
+// with g = L/4, t = L%4. All lookups are issued before the first store, so one
+// shared-memory latency covers them. Channels 2p and 2p+1 of a pair are 16
 // bytes apart in the tile; lanes with g >= 4 store the odd channel first, which
 // puts the 32 lanes of each store on 32 different banks.
-template <int HH>
-__device__ __forceinline__ void decode_half(const uint32_t (&w)[12], int lane, int row0, uint32_t a_tile,
-                                            uint32_t lanebase) {
-  uint32_t lk[32];
-  lookups<HH * 32>(w, lanebase, lk, std::make_integer_sequence<int, 32>{});
+template <int S0, int NS>
+__device__ __forceinline__ void decode_steps(const uint32_t (&w)[12], int lane, int row0, uint32_t a_tile,
+                                             uint32_t lanebase) {
+  uint32_t lk[16 * NS];
+  lookups<S0 * 16, 16 * NS>(w, lanebase, lk, std::make_integer_sequence<int, 16 * NS>{});
   const int g = lane >> 2, t = lane & 3;
   const uint32_t swap = g >= 4 ? 16u : 0u;
   const uint32_t sel_a = g >= 4 ? 0x7632u : 0x5410u, sel_b = sel_a ^ 0x2222u;
 #pragma unroll
-  for (int sm = 0; sm < 8; ++sm) {  // (s - S0, m)
-    const int S = 2 * HH + (sm >> 2), M = sm & 3;
+  for (int sm = 0; sm < 4 * NS; ++sm) {  // (s - S0, m)
+    const int S = S0 + (sm >> 2), M = sm & 3;
     const uint32_t* l = lk + 4 * sm;
     const int r = row0 + 2 * (M * 8 + g);  // channel 2p of the tile; 2p+1 is the next row
     const int k = S * 16 + 2 * t;
@@ -216,6 +222,30 @@ __device__ __forceinline__ void decode_half(const uint32_t (&w)[12], int lane, i
     sts32(o0 + (16u - swap), __byte_perm(l[0], l[1], sel_b));
     sts32(o8 + swap, __byte_perm(l[2], l[3], sel_a));
     sts32(o8 + (16u - swap), __byte_perm(l[2], l[3], sel_b));
+  }
+}
+
+// Decoder warps per super-unit and input steps per warp.
+constexpr int kDecPerSu = kDecWarps / 2;
+constexpr int kStepsPerDec = 4 / kDecPerSu;
+static_assert(kDecWarps == 2 || kDecWarps == 4 || kDecWarps == 8, "decoder warps split the 4 input steps evenly");
+
+__device__ __forceinline__ void decode_part(const uint32_t (&w)[12], int part, int lane, int row0, uint32_t a_tile,
+                                            uint32_t lanebase) {
+  if constexpr (kStepsPerDec == 1) {
+    switch (part) {
+      case 0: decode_steps<0, 1>(w, lane, row0, a_tile, lanebase); break;
+      case 1: decode_steps<1, 1>(w, lane, row0, a_tile, lanebase); break;
+      case 2: decode_steps<2, 1>(w, lane, row0, a_tile, lanebase); break;
+      default: decode_steps<3, 1>(w, lane, row0, a_tile, lanebase); break;
+    }
+  } else if constexpr (kStepsPerDec == 2) {
+    if (part == 0)
+      decode_steps<0, 2>(w, lane, row0, a_tile, lanebase);
+    else
+      decode_steps<2, 2>(w, lane, row0, a_tile, lanebase);
+  } else {
+    decode_steps<0, 4>(w, lane, row0, a_tile, lanebase);
   }
 }
 
@@ -258,7 +288,8 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
 static_assert(2 * PfSmem<64>::kTotal > 228 * 1024, "one prefill CTA per SM");
 
 template <int N>
-__global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs a) {
+__global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid_constant__ PrefillArgs a,
+                                                                     const __grid_constant__ CUtensorMap xmap) {
   extern __shared__ __align__(16) unsigned char dsm[];
   __shared__ __align__(8) unsigned long long s_bars[3 * kStages + 4];
   __shared__ uint32_t s_tmem;
@@ -297,7 +328,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs 
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full_bar(s), kDecWarps * 32);
       mbar_init(empty_bar(s), 1);
-      mbar_init(load_bar(s), kLoadWarps * 32);
+      mbar_init(load_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(acc_full(b), 1);
@@ -316,46 +347,40 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs 
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
-  if (warp < kLoadWarps) {
-    // ------------------------------------------------------------ loaders
-    const int rows = a.rows;
-    int it = 0;
-    for (long long s = s0; s < s1;) {
-      const Seg g = seg_at(s, s1, n_kg);
-      const int mt = g.t / n_tiles, row0 = (g.t - mt * n_tiles) * N;
-      // the tile's two super-units: (matrix, channel group); the second is past the
-      // last channel when d_out is an odd multiple of 64 (its A rows are never stored)
-      const int mg0 = a.swiglu ? mt : 2 * mt, mg1 = a.swiglu ? mt : 2 * mt + 1;
-      const bool live1 = a.swiglu || mg1 < a.d_out / 64;
-      const uint4* su0 = a.packed0 + (size_t)mg0 * n_kg * kSuUint4;
-      const uint4* su1 = (a.swiglu ? a.packed1 : a.packed0) + (size_t)(live1 ? mg1 : mg0) * n_kg * kSuUint4;
-      for (int kk = g.k0; kk < g.k1; ++kk, ++it) {
-        const int st = it % kStages;
-        if (it >= kStages) mbar_wait(empty_bar(st), (uint32_t)((it / kStages - 1) & 1), a.status);
-        // activation tile: N rows x 64 inputs (128 bytes per row), 16 bytes per
-        // copy, in the 128-byte swizzle layout; eight consecutive threads copy one row
-        const uint32_t bt = b_tile(st);
-        for (int e = tid; e < N * 8; e += kLoadWarps * 32) {
-          const int n = e >> 3, c = e & 7;
-          const int r = row0 + n;
-          const uint16_t* src = a.x + (size_t)(r < rows ? r : 0) * a.d_in + kk * 64 + c * 8;
-          cp_async16_zfill(bt + (uint32_t)((n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4)), src, r < rows);
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------ tile copies
+    if (lane == 0) {
+      constexpr uint32_t kTx = (uint32_t)(PfSmem<N>::kBTile + kIdxBytes);
+      int it = 0;
+      for (long long s = s0; s < s1;) {
+        const Seg g = seg_at(s, s1, n_kg);
+        const int mt = g.t / n_tiles, row0 = (g.t - mt * n_tiles) * N;
+        // the tile's two super-units: (matrix, channel group); the second is past the
+        // last channel when d_out is an odd multiple of 64 (its A rows are never stored)
+        const int mg0 = a.swiglu ? mt : 2 * mt, mg1 = a.swiglu ? mt : 2 * mt + 1;
+        const bool live1 = a.swiglu || mg1 < a.d_out / 64;
+        const uint4* su0 = a.packed0 + (size_t)mg0 * n_kg * kSuUint4;
+        const uint4* su1 = (a.swiglu ? a.packed1 : a.packed0) + (size_t)(live1 ? mg1 : mg0) * n_kg * kSuUint4;
+        for (int kk = g.k0; kk < g.k1; ++kk, ++it) {
+          const int st = it % kStages;
+          if (it >= kStages) mbar_wait(empty_bar(st), (uint32_t)((it / kStages - 1) & 1), a.status);
+          mbar_expect_tx(load_bar(st), kTx);
+          // activation tile: N rows x 64 inputs in the 128-byte swizzle layout (rows
+          // past the last are filled with zeros)
+          tma_load_2d(b_tile(st), &xmap, kk * 64, row0, load_bar(st));
+          bulk_load(i_tile(st), su0 + (size_t)kk * kSuUint4, kSuBytes, load_bar(st));
+          bulk_load(i_tile(st) + kSuBytes, su1 + (size_t)kk * kSuUint4, kSuBytes, load_bar(st));
         }
-        // index strings of the two super-units (96 16-byte chunks each)
-        for (int e = tid; e < 2 * kSuUint4; e += kLoadWarps * 32) {
-          const uint4* src = (e < kSuUint4 ? su0 : su1) + (size_t)kk * kSuUint4 + (e % kSuUint4);
-          cp_async16(i_tile(st) + (uint32_t)(e * 16), src);
-        }
-        cp_async_arrive(load_bar(st));
+        s += g.k1 - g.k0;
       }
-      s += g.k1 - g.k0;
     }
-    cp_async_wait_all();
-  } else if (warp < kLoadWarps + kDecWarps) {
+    __syncwarp();
+  } else if (warp < kDecWarp0 + kDecWarps) {
     // ------------------------------------------------------------ decoders
-    // warp -> (super-unit su of the tile, half hh of the lane strings); lane -> lane string
-    const int dt = tid - kLoadWarps * 32;
-    const int su = dt >> 6, hh = (dt >> 5) & 1, L = lane;
+    // warp -> (super-unit su of the tile, part of the lane strings); lane -> lane string
+    const int dw = warp - kDecWarp0;
+    const int su = dw / kDecPerSu, part = dw % kDecPerSu, L = lane;
+    const int s_lo = part * kStepsPerDec, s_hi = s_lo + kStepsPerDec;  // input steps of this warp
     const uint32_t lanebase = tabs | (uint32_t)(lane * 4) | ((a.swiglu && su == 1) ? 8192u : 0u);
     int it = 0;
     for (long long s = s0; s < s1;) {
@@ -367,13 +392,13 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs 
         if (it >= kStages) mbar_wait(empty_bar(st), (uint32_t)((it / kStages - 1) & 1), a.status);
         mbar_wait(load_bar(st), (uint32_t)((it / kStages) & 1), a.status);
         if (live) {
-          // half hh of the string is bits [192 hh, 192 hh + 192): words 0-6 or 6-11,
-          // i.e. 16-byte chunks 0-1 or 1-2
+          // input steps [s_lo, s_hi) are bits [96 s_lo, 96 s_hi) of the string: words
+          // 3 s_lo .. 3 s_hi (the last for indices that straddle two words)
           uint32_t w[12] = {};
           const uint32_t is = i_tile(st) + (uint32_t)(su * kSuBytes);
 #pragma unroll
           for (int q = 0; q < 3; ++q) {
-            if (q == 2 - 2 * hh) continue;
+            if (4 * q > 3 * s_hi || 4 * q + 3 < 3 * s_lo) continue;
             const uint32_t o = is + (uint32_t)((q * 32 + L) * 16);
             uint32_t v0, v1, v2, v3;
             asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3) : "r"(o));
@@ -382,10 +407,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs 
             w[4 * q + 2] = v2;
             w[4 * q + 3] = v3;
           }
-          if (hh == 0)
-            decode_half<0>(w, L, su * 64, a_tile(st), lanebase);
-          else
-            decode_half<1>(w, L, su * 64, a_tile(st), lanebase);
+          decode_part(w, part, L, su * 64, a_tile(st), lanebase);
         }
         fence_proxy_async();  // the generic-proxy writes of A, before the MMA reads them
         mbar_arrive(full_bar(st));
@@ -407,7 +429,6 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs 
           const int st = it % kStages;
           mbar_wait(load_bar(st), (uint32_t)((it / kStages) & 1), a.status);
           mbar_wait(full_bar(st), (uint32_t)((it / kStages) & 1), a.status);
-          fence_proxy_async();  // the activation tile (cp.async, generic proxy) before the MMA reads it
           tc_fence_after();
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -555,11 +576,46 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs 
   }
 }
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      p = nullptr;
+    }
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// The activations [rows][d_in] FP16 as tiles of 64 inputs x N rows in the
+// 128-byte swizzle layout; rows past the last read as zeros.
+cudaError_t activation_map(const PrefillArgs& a, int n, CUtensorMap* map) {
+  const EncodeTiledFn enc = encode_tiled();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)a.d_in, (cuuint64_t)a.rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)a.d_in * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)n};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(a.x), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int N>
 cudaError_t launch_n(PrefillArgs a, cudaStream_t st) {
   const int smem = PfSmem<N>::kTotal;
   cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  alignas(64) CUtensorMap xmap;
+  if ((e = activation_map(a, N, &xmap)) != cudaSuccess) return e;
   a.work = prefill_work(a.rows, a.d_in, a.d_out, a.swiglu);
   const int grid = prefill_grid(a.rows, a.d_in, a.d_out, a.swiglu);
   cudaLaunchConfig_t cfg = {};
@@ -572,7 +628,7 @@ cudaError_t launch_n(PrefillArgs a, cudaStream_t st) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, prefill_gemm_kernel<N>, a);
+  e = cudaLaunchKernelEx(&cfg, prefill_gemm_kernel<N>, a, xmap);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
