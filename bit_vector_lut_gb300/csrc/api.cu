@@ -238,7 +238,7 @@ cudaError_t run_persistent(const uint16_t* x, int rows, int nt, const vq3_mlp_la
 // ---- many-row (prefill) path: rotate, tensor-core GEMM with the LUT decoded
 // into shared memory, (SwiGLU, rotate, GEMM)
 
-constexpr int kPrefillRows = 64;  // from this many rows on, the tcgen05 path
+constexpr int kPrefillRows = 17;  // from this many rows on, the tcgen05 path (the decode kernel is faster up to 16)
 
 // [status word][counter words: part flags][x' FP16 [rows][d_in]]
 // [h FP32 [rows][d_inter]][h' FP16 [rows][d_inter]][parts of split tiles]

@@ -51,7 +51,8 @@ constexpr int kEpiWarp0 = kMmaWarp + 1;          // warps 10-13
 constexpr int kPThreads = (kEpiWarp0 + 4) * 32;
 constexpr int kEpiThreads = 4 * 32;
 constexpr int kMinSteps = 8;  // fewest K steps per CTA
-constexpr int kStages = 3;
+constexpr int kMaxStages = 6;
+constexpr int kPrefetchSteps = 8;  // index strings are prefetched into L2 this many K steps ahead
 constexpr int kTileM = 128;                    // output channels per tile
 constexpr int kATile = kTileM * 64 * 2;        // 16 KB of FP16
 constexpr int kTabWords = 64 * 32;
@@ -95,6 +96,10 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
+}
+// Brings a contiguous global range (16-byte aligned, a multiple of 16 bytes) into L2.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 // Contiguous global -> shared copy (16-byte aligned, a multiple of 16 bytes).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -256,6 +261,9 @@ struct PfSmem {
   static constexpr int kBTile = N * 64 * 2;
   static constexpr int kStageBytes = kATile + kBTile + kIdxBytes;
   static_assert(kStageBytes % 1024 == 0 && kATile % 1024 == 0, "B tiles start on 1 KB swizzle atoms");
+  // stages in flight: as many as fit, up to kMaxStages (the K loop is latency-bound at small N)
+  static constexpr int kStages = N >= 256 ? 3 : (N >= 128 ? 5 : 6);
+  static_assert(kStages <= kMaxStages, "barrier array size");
   static constexpr int kTotal = 1024 + kStages * kStageBytes + (int)kTabAlign + 2 * kTabWords * 4 + 64 * 16 * 4;
 };
 
@@ -291,7 +299,8 @@ template <int N>
 __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid_constant__ PrefillArgs a,
                                                                      const __grid_constant__ CUtensorMap xmap) {
   extern __shared__ __align__(16) unsigned char dsm[];
-  __shared__ __align__(8) unsigned long long s_bars[3 * kStages + 4];
+  constexpr int kStages = PfSmem<N>::kStages;
+  __shared__ __align__(8) unsigned long long s_bars[3 * kMaxStages + 4];
   __shared__ uint32_t s_tmem;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t raw = smem_u32(dsm);
@@ -367,6 +376,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
           mbar_expect_tx(load_bar(st), kTx);
           // activation tile: N rows x 64 inputs in the 128-byte swizzle layout (rows
           // past the last are filled with zeros)
+          if (kk + kPrefetchSteps < g.k1) {
+            prefetch_l2(su0 + (size_t)(kk + kPrefetchSteps) * kSuUint4, kSuBytes);
+            prefetch_l2(su1 + (size_t)(kk + kPrefetchSteps) * kSuUint4, kSuBytes);
+          }
           tma_load_2d(b_tile(st), &xmap, kk * 64, row0, load_bar(st));
           bulk_load(i_tile(st), su0 + (size_t)kk * kSuUint4, kSuBytes, load_bar(st));
           bulk_load(i_tile(st) + kSuBytes, su1 + (size_t)kk * kSuUint4, kSuBytes, load_bar(st));

@@ -127,8 +127,8 @@ VQ3_API int fwht_rotate(const uint16_t* x, int rows, int n, int block, const uin
 /*
  * Workspace for vq3_linear_forward / vq3_mlp_forward at `rows` rows. It holds
  * a device status word and counter words (both at fixed offsets), then
- * scratch: below 64 rows h of one pass of up to 32 rows (MLP) and the split-K
- * partial sums of both decode steps; from 64 rows on x', h, h' and the sums of
+ * scratch: below 17 rows h of one pass of up to 16 rows (MLP) and the split-K
+ * partial sums of both decode steps; from 17 rows on x', h, h' and the sums of
  * tiles split between CTAs. It must be zero-filled once before its first use
  * (vq3_workspace_init); every completed call leaves the counters at zero
  * again, so a workspace of the largest size needed serves calls of any row
@@ -158,9 +158,9 @@ VQ3_API int vq3_linear_forward(const uint16_t* x, int rows, const vq3_linear* L,
  * One SwiGLU MLP block with online rotations on both inputs:
  *   h   = silu(W_g R_g x) * (W_u R_g x)      (FP32)
  *   out = fp16( W_d R_d h )                  (R_d h rounded to FP16 once, as the MMA operand)
- * Below 64 rows: one cooperative kernel per pass of up to 8, 16 or 32 rows;
+ * Below 17 rows: one cooperative kernel per pass of up to 8 or 16 rows;
  * all of its CTAs are resident at once and hand over between steps through
- * workspace counters. From 64 rows on: four kernels (rotate x; gate/up GEMM
+ * workspace counters. From 17 rows on: four kernels (rotate x; gate/up GEMM
  * on the tensor cores with SwiGLU fused; rotate h; down GEMM), each GEMM one
  * cooperative launch of one CTA per SM that shares out the (tile, K step)
  * pairs evenly; a tile split between CTAs is summed in K order by the CTA
@@ -175,7 +175,7 @@ VQ3_API int vq3_mlp_forward(const uint16_t* x, int rows, const vq3_mlp_layer* la
                     void* workspace, size_t ws_bytes, void* stream);
 
 /* Number of kernels one vq3_mlp_forward call launches at `rows` rows: one per
- * pass of 8, 16 or 32 rows below 64 rows, 4 from 64 rows on (-1 on a bad
+ * pass of 8 or 16 rows below 17 rows, 4 from 17 rows on (-1 on a bad
  * descriptor). */
 VQ3_API int vq3_mlp_kernel_launches(int rows, const vq3_mlp_layer* layer);
 

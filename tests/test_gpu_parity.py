@@ -197,9 +197,9 @@ def test_mlp_row_sweep(vq3, sweep, rows):
     assert_parity(got, ref[:rows], f"sweep T={rows}")
 
 
-@pytest.mark.parametrize("rows", [65, 129, 300, 1000])
+@pytest.mark.parametrize("rows", [17, 40, 65, 129, 300, 1000])
 def test_mlp_ragged_prefill_rows(vq3, sweep, rows):
-    """Row counts that leave a partly filled row tile (64-, 128- and 256-row tiles)."""
+    """Row counts on the tensor-core path that leave a partly filled row tile (64-, 128- and 256-row tiles)."""
     wl, blk, layer, ref = sweep
     got = vq3.mlp_forward(f16(wl.x[:rows]), layer).cpu().numpy()
     assert_parity(got, ref[:rows], f"ragged prefill T={rows}")
@@ -221,7 +221,7 @@ def test_workspace_shared_across_row_counts(vq3, sweep):
     few-row path in any order (their counter words sit at the same place)."""
     wl, blk, layer, ref = sweep
     ws = vq3.workspace(max(vq3.mlp_workspace_bytes(r, layer) for r in (8, 32, 2048)))
-    for rows in (2048, 8, 64, 32, 2048, 1):
+    for rows in (2048, 8, 64, 16, 32, 2048, 1):
         got = vq3.mlp_forward(f16(wl.x[:rows]), layer, ws=ws).cpu().numpy()
         assert_parity(got, ref[:rows], f"shared workspace T={rows}")
     assert vq3.workspace_status(ws) == 0

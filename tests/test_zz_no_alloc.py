@@ -63,6 +63,23 @@ def test_noalloc_runs_rows_beyond_one_pass():
     assert_parity(out.cpu().numpy(), ref, "no-alloc, 64 rows")
 
 
+def test_noalloc_narrow_block_uses_32_row_passes():
+    # a narrow block fits 32-row passes of the decode kernel: 40 rows = one pass of 32 and one of 8
+    from oracle import vq3_oracle as O
+    vq3, noalloc = _lib()
+    dev = torch.device("cuda:0")
+    wl = S.mlp_27b(seed=13, rows=40, hidden=1024, inter=2048, block=1024)
+    blk = wl.layers[0]
+    layer = vq3.MLP.from_block(blk, dev)
+    x = torch.from_numpy(wl.x).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    out = torch.full_like(x, float("nan"))
+    rc = noalloc(x.data_ptr(), x.shape[0], ctypes.byref(layer.struct), out.data_ptr(), stream.cuda_stream)
+    assert rc == 0, vq3.lib.vq3_last_error().decode()
+    torch.cuda.synchronize(dev)
+    assert_parity(out.cpu().numpy(), O.mlp_f64(wl.x, blk), "no-alloc narrow, 40 rows")
+
+
 def test_noalloc_rejects_widths_beyond_the_fixed_scratch():
     # hidden 16384 / intermediate 262144 needs more than 32 MiB of scratch even in 8-row
     # passes; the call is refused on the host before anything is launched, so the
