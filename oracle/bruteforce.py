@@ -5,7 +5,7 @@ scalar definition (bit reads of the stream, Hadamard entries from the parity of
 popcount(r & c), SiLU through math.exp, sums in Python floats). It serves as a
 pin for the NumPy oracle on shapes small enough for scalar loops.
 
-Sources as in the oracle module: model card "anemll/anemll-forge-qwen3.8-27B",
+Index formats as in the oracle module ("2x64", "2x16", "lut4"). Sources as in the oracle module: model card "anemll/anemll-forge-qwen3.8-27B",
 section "Release 0.2: three-bit MLP, token-mixer rotations, distilled weights";
 "ANEMLL ANE LLM conversion pipeline", section "Facts".
 """
@@ -19,10 +19,14 @@ def stream_bit(stream, j: int) -> int:
     return (int(stream[j // 8]) >> (j % 8)) & 1
 
 
-def index_at(stream, k: int) -> int:
+# format -> (index bits, output channels per index)
+_FMT = {"2x64": (6, 2), "2x16": (4, 2), "lut4": (4, 1)}
+
+
+def index_at(stream, k: int, bits: int = 6) -> int:
     v = 0
-    for b in range(6):
-        v |= stream_bit(stream, 6 * k + b) << b
+    for b in range(bits):
+        v |= stream_bit(stream, bits * k + b) << b
     return v
 
 
@@ -50,9 +54,11 @@ def rotate_row(x, block: int, sign_words=None):
 
 
 def weight(m, o: int, i: int) -> float:
-    p, c = divmod(o, 2)
-    k = index_at(m.stream, p * m.d_in + i)
-    return float(m.scales[o]) * float(m.codebook[k][c])
+    bits, vec = _FMT[getattr(m, "fmt", "2x64") or "2x64"]
+    p, c = divmod(o, vec)
+    k = index_at(m.stream, p * m.d_in + i, bits)
+    entry = m.codebook[k]
+    return float(m.scales[o]) * float(entry[c] if vec > 1 else (entry[0] if hasattr(entry, "__len__") else entry))
 
 
 def linear_row(x, m):

@@ -19,20 +19,35 @@ Sources (page title, then section):
   [FACTS] "ANEMLL ANE LLM conversion pipeline", section "Facts" (SiLU written
           as 0.5*x*(1+tanh(x/2)); vector LUTs along input channels lost
           placement, so the vectors run along output channels).
+  [R01]   same model card, the release-comparison table (row "MLP gate / up /
+          down": two-bit vector LUT (2x16) in 38 layers, four-bit LUT in 26, in
+          the previous release; row "Token mixers": two-bit vector LUT and
+          four-bit LUT) and "ANEMLL ANE LLM conversion pipeline", "Facts" (the
+          previous target mixes 2-bit vector LUTs and 4-bit scalar LUTs).
+
+Index formats (FORMATS): "2x64" is the release's three-bit format (64
+two-component centroids, a six-bit index per output pair); "2x16" the two-bit
+vector format (16 two-component centroids, a four-bit index per output pair);
+"lut4" the four-bit scalar format (16 scalar entries, a four-bit index per
+weight). Every format has per-output-channel scales.
 
 Readings where the pages are silent (each also listed in the design notes):
-  * index k = p*d_in + i (pair-major, input fastest) occupies stream bits
-    [6k, 6k+6); stream bit j is bit (j mod 8) of byte j//8 (LSB first);
+  * index k = p*d_in + i (group-major, input fastest; a group is an output pair
+    for the vector formats, one output channel for "lut4") occupies stream bits
+    [b k, b k + b) for index width b; stream bit j is bit (j mod 8) of byte j//8
+    (LSB first);
   * centroid component c of index idx[p, i] is the weight of output channel
-    2p+c at input column i; the scale multiplies after the lookup;
+    2p+c at input column i (the single entry, of channel p, for "lut4"); the
+    scale multiplies after the lookup;
   * the rotation of a row is x' = blockdiag(H_b diag(s)) x / sqrt(b), with H_b
     the Sylvester Hadamard matrix H[r][c] = (-1)^popcount(r & c) and s = +1
     unless seed signs are given; gate and up share x', down has its own;
   * SiLU(z) = z / (1 + exp(-z)), identical to the pages' tanh form.
 
 Parity pins: every function here is pinned by tests in tests/test_oracle_pins.py
-(closed forms, invariants, a hand-derived packing example and a pure-Python
-brute force in oracle/bruteforce.py). No function is "parity unpinned" except
+and, for the "2x16" and "lut4" formats, tests/test_oracle_formats.py (closed
+forms, invariants, hand-derived packing examples, weights written out by hand
+and a pure-Python brute force in oracle/bruteforce.py). No function is "parity unpinned" except
 the whole-model quality figures, which need trained weights and are not
 computed here.
 """
@@ -47,47 +62,58 @@ import numpy as np
 INDEX_BITS = 6
 CODEBOOK_SIZE = 64
 
+# format -> (index bits, centroid dimension = output channels per index, codebook entries)
+FORMATS = {"2x64": (6, 2, 64), "2x16": (4, 2, 16), "lut4": (4, 1, 16)}
+
+
+def fmt_of(m) -> str:
+    """Format of a matrix object (the release's 2x64 when it names none)."""
+    return getattr(m, "fmt", "2x64") or "2x64"
+
 
 # ---------------------------------------------------------------------------
 # canonical index stream  ([R02] "Three bits per MLP weight")
 # ---------------------------------------------------------------------------
 
-def unpack_indices(stream: np.ndarray, start: int, count: int) -> np.ndarray:
+def unpack_indices(stream: np.ndarray, start: int, count: int, bits_per: int = INDEX_BITS) -> np.ndarray:
     """Indices start .. start+count-1 of a canonical stream, as int64.
 
-    Index k occupies bits [6k, 6k+6) of the stream, least significant bit first.
+    Index k occupies bits [b k, b k + b) of the stream (b = bits_per), least
+    significant bit first.
     """
     stream = np.asarray(stream, dtype=np.uint8)
-    first_bit = INDEX_BITS * start
-    last_bit = INDEX_BITS * (start + count)
+    first_bit = bits_per * start
+    last_bit = bits_per * (start + count)
     b0 = first_bit // 8
     b1 = (last_bit + 7) // 8
     bits = np.unpackbits(stream[b0:b1], bitorder="little")
     skip = first_bit - 8 * b0
-    bits = bits[skip: skip + INDEX_BITS * count].reshape(count, INDEX_BITS)
+    bits = bits[skip: skip + bits_per * count].reshape(count, bits_per)
     idx = np.zeros(count, dtype=np.int64)
-    for b in range(INDEX_BITS):
+    for b in range(bits_per):
         idx |= bits[:, b].astype(np.int64) << b
     return idx
 
 
-def pack_indices(idx: np.ndarray) -> np.ndarray:
+def pack_indices(idx: np.ndarray, bits_per: int = INDEX_BITS) -> np.ndarray:
     """Inverse of unpack_indices for a whole stream (pad bits zero)."""
     idx = np.asarray(idx, dtype=np.int64).reshape(-1)
-    if idx.size and (idx.min() < 0 or idx.max() >= CODEBOOK_SIZE):
-        raise ValueError("indices must lie in [0, 64)")
-    bits = ((idx[:, None] >> np.arange(INDEX_BITS)) & 1).astype(np.uint8).reshape(-1)
+    if idx.size and (idx.min() < 0 or idx.max() >= (1 << bits_per)):
+        raise ValueError(f"indices must lie in [0, {1 << bits_per})")
+    bits = ((idx[:, None] >> np.arange(bits_per)) & 1).astype(np.uint8).reshape(-1)
     pad = (-bits.size) % 8
     if pad:
         bits = np.concatenate([bits, np.zeros(pad, np.uint8)])
     return np.packbits(bits, bitorder="little")
 
 
-def index_matrix(stream: np.ndarray, d_in: int, d_out: int, p0: int = 0, p1: int | None = None) -> np.ndarray:
-    """idx[p, i] for pairs p0 <= p < p1 (default: all d_out/2 pairs)."""
+def index_matrix(stream: np.ndarray, d_in: int, d_out: int, p0: int = 0, p1: int | None = None,
+                 fmt: str = "2x64") -> np.ndarray:
+    """idx[p, i] for output groups p0 <= p < p1 (default: all d_out / vec groups)."""
+    bits_per, vec, _ = FORMATS[fmt]
     if p1 is None:
-        p1 = d_out // 2
-    return unpack_indices(stream, p0 * d_in, (p1 - p0) * d_in).reshape(p1 - p0, d_in)
+        p1 = d_out // vec
+    return unpack_indices(stream, p0 * d_in, (p1 - p0) * d_in, bits_per).reshape(p1 - p0, d_in)
 
 
 # ---------------------------------------------------------------------------
@@ -95,19 +121,21 @@ def index_matrix(stream: np.ndarray, d_in: int, d_out: int, p0: int = 0, p1: int
 # ---------------------------------------------------------------------------
 
 def dense_weight(stream, codebook, scales, d_in: int, d_out: int, apply_scale: bool = True,
-                 rows: tuple[int, int] | None = None) -> np.ndarray:
-    """W[2p+c, i] = scale[2p+c] * C[idx[p, i]][c] in float64, for output rows [r0, r1).
+                 rows: tuple[int, int] | None = None, fmt: str = "2x64") -> np.ndarray:
+    """W[v p + c, i] = scale[v p + c] * C[idx[p, i]][c] in float64 (v = centroid
+    dimension: 2 for the vector formats, 1 for "lut4"), for output rows [r0, r1).
 
     Both factors are FP16; their product is exact in float64 (and in float32).
     """
+    _, vec, entries = FORMATS[fmt]
     r0, r1 = (0, d_out) if rows is None else rows
-    if r0 % 2 or r1 % 2:
-        raise ValueError("row range must cover whole output-channel pairs")
-    idx = index_matrix(stream, d_in, d_out, r0 // 2, r1 // 2)
-    C = np.asarray(codebook, dtype=np.float16).astype(np.float64)
+    if r0 % vec or r1 % vec:
+        raise ValueError("row range must cover whole output-channel groups")
+    idx = index_matrix(stream, d_in, d_out, r0 // vec, r1 // vec, fmt)
+    C = np.asarray(codebook, dtype=np.float16).astype(np.float64).reshape(entries, vec)
     W = np.empty((r1 - r0, d_in), dtype=np.float64)
-    W[0::2, :] = C[idx, 0]
-    W[1::2, :] = C[idx, 1]
+    for c in range(vec):
+        W[c::vec, :] = C[idx, c]
     if apply_scale:
         W *= np.asarray(scales, dtype=np.float16).astype(np.float64)[r0:r1, None]
     return W
@@ -197,7 +225,7 @@ def linear_f64(x, m, round_rotated: bool = False, row_chunk: int = 2048) -> np.n
     y = np.empty((xr.shape[0], m.d_out), dtype=np.float64)
     for r0 in range(0, m.d_out, row_chunk):
         r1 = min(m.d_out, r0 + row_chunk)
-        W = dense_weight(m.stream, m.codebook, m.scales, m.d_in, m.d_out, rows=(r0, r1))
+        W = dense_weight(m.stream, m.codebook, m.scales, m.d_in, m.d_out, rows=(r0, r1), fmt=fmt_of(m))
         y[:, r0:r1] = xr @ W.T
     return y
 

@@ -30,15 +30,21 @@ CODEBOOK_SIZE = 64
 CENTROID_DIM = 2
 INDEX_BITS = 6
 
+# index format -> (index bits, centroid dimension, codebook entries); "2x64" is the
+# three-bit vector format, "2x16" the two-bit vector format, "lut4" the four-bit
+# scalar format
+FORMATS = {"2x64": (6, 2, 64), "2x16": (4, 2, 16), "lut4": (4, 1, 16)}
+
 
 def rng(seed: int, stream: int = 1) -> np.random.Generator:
     """Stream 0: activations; 1: weights; 2: sign bits."""
     return np.random.Generator(np.random.PCG64([seed, stream]))
 
 
-def stream_bytes(d_in: int, d_out: int) -> int:
+def stream_bytes(d_in: int, d_out: int, fmt: str = "2x64") -> int:
     """Length in bytes of the canonical stream of a d_out x d_in matrix."""
-    bits = INDEX_BITS * (d_out // 2) * d_in
+    nb, vec, _ = FORMATS[fmt]
+    bits = nb * (d_out // vec) * d_in
     return (bits + 7) // 8
 
 
@@ -52,16 +58,18 @@ def activations(g: np.random.Generator, rows: int, n: int, outlier_channels: int
     return x.astype(np.float16)
 
 
-def codebook(g: np.random.Generator, std: float = 0.02) -> np.ndarray:
-    """FP16 codebook [64, 2] ~N(0, std)."""
-    return (g.standard_normal((CODEBOOK_SIZE, CENTROID_DIM)) * std).astype(np.float16)
+def codebook(g: np.random.Generator, std: float = 0.02, fmt: str = "2x64") -> np.ndarray:
+    """FP16 codebook [entries, centroid dim] ~N(0, std) ([64, 2] for "2x64")."""
+    _, vec, entries = FORMATS[fmt]
+    return (g.standard_normal((entries, vec)) * std).astype(np.float16)
 
 
-def index_stream(g: np.random.Generator, d_in: int, d_out: int) -> np.ndarray:
-    """Canonical index stream of uniformly random 6-bit indices (uint8 bytes)."""
-    nbytes = stream_bytes(d_in, d_out)
+def index_stream(g: np.random.Generator, d_in: int, d_out: int, fmt: str = "2x64") -> np.ndarray:
+    """Canonical index stream of uniformly random indices (uint8 bytes)."""
+    nb, vec, _ = FORMATS[fmt]
+    nbytes = stream_bytes(d_in, d_out, fmt)
     s = g.integers(0, 256, size=nbytes, dtype=np.uint8)
-    tail_bits = (INDEX_BITS * (d_out // 2) * d_in) % 8
+    tail_bits = (nb * (d_out // vec) * d_in) % 8
     if tail_bits:
         s[-1] &= np.uint8((1 << tail_bits) - 1)
     return s
@@ -88,10 +96,11 @@ class Matrix:
     d_in: int
     d_out: int
     block: int
-    codebook: np.ndarray  # [64, 2] float16
-    stream: np.ndarray    # canonical 6-bit LE index stream, uint8
+    codebook: np.ndarray  # [entries, centroid dim] float16 ([64, 2] for "2x64")
+    stream: np.ndarray    # canonical LE index stream, uint8
     scales: np.ndarray    # [d_out] float16
     signs: np.ndarray | None = None  # bit-packed uint32 over d_in, or None (all +1)
+    fmt: str = "2x64"     # index format (FORMATS)
 
 
 @dataclass
@@ -109,17 +118,17 @@ class Workload:
     layers: list = field(default_factory=list)  # list[Block] or [Matrix]
 
 
-def matrix(g: np.random.Generator, d_in: int, d_out: int, block: int) -> Matrix:
-    c = codebook(g)
-    s = index_stream(g, d_in, d_out)
+def matrix(g: np.random.Generator, d_in: int, d_out: int, block: int, fmt: str = "2x64") -> Matrix:
+    c = codebook(g, fmt=fmt)
+    s = index_stream(g, d_in, d_out, fmt)
     sc = scales(g, d_out)
-    return Matrix(d_in, d_out, block, c, s, sc)
+    return Matrix(d_in, d_out, block, c, s, sc, None, fmt)
 
 
-def mlp_block(g: np.random.Generator, hidden: int, inter: int, block: int) -> Block:
-    gate = matrix(g, hidden, inter, block)
-    up = matrix(g, hidden, inter, block)
-    down = matrix(g, inter, hidden, block)
+def mlp_block(g: np.random.Generator, hidden: int, inter: int, block: int, fmt: str = "2x64") -> Block:
+    gate = matrix(g, hidden, inter, block, fmt)
+    up = matrix(g, hidden, inter, block, fmt)
+    down = matrix(g, inter, hidden, block, fmt)
     return Block(gate, up, down)
 
 
@@ -143,11 +152,12 @@ def linear_256(seed: int = 0, rows: int = 8) -> Workload:
 
 
 def mlp_27b(seed: int = 1, rows: int = 8, outlier_channels: int = 0, hidden: int = HIDDEN,
-            inter: int = INTERMEDIATE, block: int = 1024, name: str | None = None) -> Workload:
+            inter: int = INTERMEDIATE, block: int = 1024, name: str | None = None, fmt: str = "2x64") -> Workload:
     """One SwiGLU block at the 27B-dense shape (hidden 5120, intermediate 17408)."""
     x = activations(rng(seed, 0), rows, hidden, outlier_channels=outlier_channels)
-    blk = mlp_block(rng(seed, 1), hidden, inter, block)
-    return Workload(name or f"mlp_{hidden}x{inter}_T{rows}", seed, x, [blk])
+    blk = mlp_block(rng(seed, 1), hidden, inter, block, fmt)
+    suffix = "" if fmt == "2x64" else f"_{fmt}"
+    return Workload(name or f"mlp_{hidden}x{inter}_T{rows}{suffix}", seed, x, [blk])
 
 
 def mlp_prefill_outliers(seed: int = 2, rows: int = 64) -> Workload:
@@ -171,3 +181,12 @@ def mlp_sweep(seed: int = 4, rows: int = 8) -> Workload:
 
 
 SWEEP_ROWS = (1, 8, 64, 512, 2048, 4096)
+
+
+# the previous release's MLP formats at the same shape: seed 5 for "2x16", 6 for "lut4"
+FORMAT_SEEDS = {"2x16": 5, "lut4": 6}
+
+
+def mlp_format(fmt: str, rows: int = 8) -> Workload:
+    """One block at 5120/17408 in another index format (two-bit vector or four-bit scalar LUT)."""
+    return mlp_27b(seed=FORMAT_SEEDS[fmt], rows=rows, fmt=fmt)
