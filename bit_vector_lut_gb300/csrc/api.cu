@@ -47,6 +47,7 @@ int check_linear(const vq3_linear* L, const char* name) {
                 L->d_out);
   if (!pow2_block(L->block)) return fail(VQ3_EINVAL, "%s: block=%d must be a power of two in [2, 1024]", name, L->block);
   if (L->d_in % L->block) return fail(VQ3_EINVAL, "%s: d_in=%d is not a multiple of block=%d", name, L->d_in, L->block);
+  if (!format_supported(L->format)) return fail(VQ3_EUNSUPPORTED, "%s: unknown index format %d", name, L->format);
   if (!L->packed || !L->codebook || !L->scales) return fail(VQ3_EINVAL, "%s: null packed/codebook/scales", name);
   if (!aligned(L->packed, 16)) return fail(VQ3_EALIGN, "%s: packed indices not 16-byte aligned", name);
   if (!aligned(L->codebook, 4) || !aligned(L->scales, 4) || (L->signs && !aligned(L->signs, 4)))
@@ -156,6 +157,8 @@ int check_mlp(const vq3_mlp_layer* l) {
   if (l->up.d_in != l->gate.d_in || l->up.d_out != l->gate.d_out || l->up.block != l->gate.block ||
       l->up.signs != l->gate.signs)
     return fail(VQ3_EINVAL, "mlp: gate and up must share d_in, d_out, block and signs");
+  if (l->up.format != l->gate.format || l->down.format != l->gate.format)
+    return fail(VQ3_EINVAL, "mlp: gate, up and down must share one index format");
   if (l->down.d_in != l->gate.d_out || l->down.d_out != l->gate.d_in)
     return fail(VQ3_EINVAL, "mlp: down must be %d -> %d (got %d -> %d)", l->gate.d_out, l->gate.d_in, l->down.d_in,
                 l->down.d_out);
@@ -193,6 +196,7 @@ cudaError_t run_persistent(const uint16_t* x, int rows, int nt, const vq3_mlp_la
   if (layer) {
     const int H = layer->gate.d_in, I = layer->gate.d_out;
     a.mlp = 1;
+    a.format = layer->gate.format;
     a.d_model = H;
     a.d_inter = I;
     a.d_model_out = H;
@@ -212,6 +216,7 @@ cudaError_t run_persistent(const uint16_t* x, int rows, int nt, const vq3_mlp_la
     c = ctl_mlp(H, I);
   } else {
     a.mlp = 0;
+    a.format = L->format;
     a.d_model = L->d_in;
     a.d_model_out = L->d_out;
     a.block_in = L->block;
@@ -271,6 +276,7 @@ PrefillArgs prefill_args(const uint16_t* xr, int rows, const vq3_linear& m0, con
   a.d_in = m0.d_in;
   a.d_out = m0.d_out;
   a.swiglu = m1 ? 1 : 0;
+  a.format = m0.format;
   a.packed0 = static_cast<const uint4*>(m0.packed);
   a.cb0 = reinterpret_cast<const uint32_t*>(m0.codebook);
   a.scale0 = m0.scales;
@@ -334,13 +340,32 @@ void parallel_for(int n, F fn) {
   for (auto& x : th) x.join();
 }
 
-uint32_t read_bits6(const uint8_t* s, size_t k) {
-  const size_t bit = 6 * k;
+// Index k of a canonical stream of nb-bit indices (nb = 4 or 6).
+uint32_t read_index(const uint8_t* s, size_t k, int nb) {
+  const size_t bit = (size_t)nb * k;
   const size_t byte = bit / 8;
   const unsigned sh = (unsigned)(bit % 8);
   uint32_t v = s[byte];
-  if (sh > 2) v |= (uint32_t)s[byte + 1] << 8;
-  return (v >> sh) & 63u;
+  if (sh + nb > 8) v |= (uint32_t)s[byte + 1] << 8;
+  return (v >> sh) & ((1u << nb) - 1u);
+}
+
+// Where index n of lane `lane`'s string in SU (mg, kg) belongs: its canonical
+// output group (pair for the vector formats, channel for the scalar one) and input.
+struct LanePos {
+  int group, input;
+};
+LanePos lane_pos(int format, int mg, int kg, int lane, int n) {
+  static const int koff[4] = {0, 1, 8, 9};
+  const int g = lane / 4, t = lane % 4;
+  const int c = format_vec(format) == 1 ? n % 2 : 0;
+  const int nn = format_vec(format) == 1 ? n / 2 : n;
+  const int s = nn / 16, m = (nn / 4) % 4, e = nn % 4;
+  const int p = mg * 32 + m * 8 + g;
+  LanePos q;
+  q.group = format_vec(format) == 1 ? 2 * p + c : p;
+  q.input = kg * 64 + s * 16 + 2 * t + koff[e];
+  return q;
 }
 
 }  // namespace
@@ -398,34 +423,74 @@ const char* vq3_last_error(void) { return g_err.c_str(); }
 
 const char* vq3_version(void) { return "vq3-gb300 0.2 (sm_103a; layout su64x64-m16n8k16)"; }
 
-size_t vq3_packed_bytes(int d_in, int d_out) {
-  if (!layout_supported(d_in, d_out)) return 0;
-  return (size_t)(d_out / kSuChannels) * (size_t)(d_in / kSuInputs) * kSuBytes;
+size_t vq3_packed_bytes_fmt(int format, int d_in, int d_out) {
+  if (!format_supported(format) || !layout_supported(d_in, d_out)) return 0;
+  return (size_t)(d_out / kSuChannels) * (size_t)(d_in / kSuInputs) * (size_t)format_su_bytes(format);
 }
 
-int vq3_pack_layout(const uint8_t* canonical, int d_in, int d_out, void* dst_host) {
+size_t vq3_packed_bytes(int d_in, int d_out) { return vq3_packed_bytes_fmt(VQ3_FORMAT_2X64, d_in, d_out); }
+
+int vq3_pack_layout_fmt(int format, const uint8_t* canonical, int d_in, int d_out, void* dst_host) {
   if (!canonical || !dst_host) return fail(VQ3_EINVAL, "pack_layout: null pointer");
+  if (!format_supported(format)) return fail(VQ3_EUNSUPPORTED, "pack_layout: unknown format %d", format);
   if (!layout_supported(d_in, d_out))
     return fail(VQ3_EUNSUPPORTED, "pack_layout: d_in=%d and d_out=%d must be positive multiples of 64", d_in, d_out);
   uint8_t* dst = static_cast<uint8_t*>(dst_host);
+  const int n_mg = d_out / kSuChannels, n_kg = d_in / kSuInputs;
+  const int nb = format_bits(format), vec = format_vec(format), words = format_words(format);
+  const int su_bytes = format_su_bytes(format), n_idx = 128 / vec;
+  parallel_for(n_mg, [=](int mg) {
+    for (int kg = 0; kg < n_kg; ++kg) {
+      const size_t su = (size_t)mg * n_kg + kg;
+      for (int lane = 0; lane < 32; ++lane) {
+        uint32_t w[17] = {0};
+        for (int n = 0; n < n_idx; ++n) {
+          const LanePos q = lane_pos(format, mg, kg, lane, n);
+          const uint32_t idx = read_index(canonical, (size_t)q.group * d_in + q.input, nb);
+          const int bit = nb * n;
+          w[bit / 32] |= idx << (bit % 32);
+          if (bit % 32 + nb > 32) w[bit / 32 + 1] |= idx >> (32 - bit % 32);
+        }
+        for (int wi = 0; wi < words; ++wi) memcpy(dst + lane_word_offset(su, lane, wi, su_bytes), &w[wi], 4);
+      }
+    }
+  });
+  return ok();
+}
+
+int vq3_pack_layout(const uint8_t* canonical, int d_in, int d_out, void* dst_host) {
+  return vq3_pack_layout_fmt(VQ3_FORMAT_2X64, canonical, d_in, d_out, dst_host);
+}
+
+int vq3_unpack_layout_fmt(int format, const void* packed_host, int d_in, int d_out, uint8_t* canonical) {
+  if (!canonical || !packed_host) return fail(VQ3_EINVAL, "unpack_layout: null pointer");
+  if (!format_supported(format)) return fail(VQ3_EUNSUPPORTED, "unpack_layout: unknown format %d", format);
+  if (!layout_supported(d_in, d_out))
+    return fail(VQ3_EUNSUPPORTED, "unpack_layout: d_in=%d and d_out=%d must be positive multiples of 64", d_in, d_out);
+  const uint8_t* src = static_cast<const uint8_t*>(packed_host);
+  const int nb = format_bits(format), vec = format_vec(format), words = format_words(format);
+  const int su_bytes = format_su_bytes(format), n_idx = 128 / vec;
+  const size_t count = (size_t)(d_out / vec) * d_in;
+  memset(canonical, 0, (nb * count + 7) / 8);
   const int n_mg = d_out / kSuChannels, n_kg = d_in / kSuInputs;
   parallel_for(n_mg, [=](int mg) {
     for (int kg = 0; kg < n_kg; ++kg) {
       const size_t su = (size_t)mg * n_kg + kg;
       for (int lane = 0; lane < 32; ++lane) {
-        const int g = lane / 4, t = lane % 4;
-        uint32_t w[13] = {0};
-        for (int n = 0; n < 64; ++n) {
-          const int s = n / 16, m = (n / 4) % 4, e = n % 4;
-          const int p = mg * 32 + m * 8 + g;
-          static const int koff[4] = {0, 1, 8, 9};
-          const int i = kg * 64 + s * 16 + 2 * t + koff[e];
-          const uint32_t idx = read_bits6(canonical, (size_t)p * d_in + i);
-          const int bit = 6 * n;
-          w[bit / 32] |= idx << (bit % 32);
-          if (bit % 32 > 26) w[bit / 32 + 1] |= idx >> (32 - bit % 32);
+        uint32_t w[17] = {0};
+        for (int wi = 0; wi < words; ++wi) memcpy(&w[wi], src + lane_word_offset(su, lane, wi, su_bytes), 4);
+        for (int n = 0; n < n_idx; ++n) {
+          const LanePos q = lane_pos(format, mg, kg, lane, n);
+          const int bit = nb * n;
+          const uint64_t v = ((uint64_t)w[bit / 32 + 1] << 32) | w[bit / 32];
+          const uint32_t idx = (uint32_t)(v >> (bit % 32)) & ((1u << nb) - 1u);
+          // one channel group mg spans a whole number of stream bytes (64 channels x
+          // d_in inputs, d_in a multiple of 64), so threads on different mg never
+          // write the same byte
+          const size_t sb = (size_t)nb * ((size_t)q.group * d_in + q.input);
+          canonical[sb / 8] |= (uint8_t)(idx << (sb % 8));
+          if (sb % 8 + nb > 8) canonical[sb / 8 + 1] |= (uint8_t)(idx >> (8 - sb % 8));
         }
-        for (int wi = 0; wi < 12; ++wi) memcpy(dst + lane_word_offset(su, lane, wi), &w[wi], 4);
       }
     }
   });
@@ -433,38 +498,7 @@ int vq3_pack_layout(const uint8_t* canonical, int d_in, int d_out, void* dst_hos
 }
 
 int vq3_unpack_layout(const void* packed_host, int d_in, int d_out, uint8_t* canonical) {
-  if (!canonical || !packed_host) return fail(VQ3_EINVAL, "unpack_layout: null pointer");
-  if (!layout_supported(d_in, d_out))
-    return fail(VQ3_EUNSUPPORTED, "unpack_layout: d_in=%d and d_out=%d must be positive multiples of 64", d_in, d_out);
-  const uint8_t* src = static_cast<const uint8_t*>(packed_host);
-  const size_t count = (size_t)(d_out / 2) * d_in;
-  const size_t nbytes = (6 * count + 7) / 8;
-  memset(canonical, 0, nbytes);
-  const int n_mg = d_out / kSuChannels, n_kg = d_in / kSuInputs;
-  parallel_for(n_mg, [=](int mg) {
-    for (int kg = 0; kg < n_kg; ++kg) {
-      const size_t su = (size_t)mg * n_kg + kg;
-      for (int lane = 0; lane < 32; ++lane) {
-        const int g = lane / 4, t = lane % 4;
-        uint32_t w[13] = {0};
-        for (int wi = 0; wi < 12; ++wi) memcpy(&w[wi], src + lane_word_offset(su, lane, wi), 4);
-        for (int n = 0; n < 64; ++n) {
-          const int s = n / 16, m = (n / 4) % 4, e = n % 4;
-          const int p = mg * 32 + m * 8 + g;
-          static const int koff[4] = {0, 1, 8, 9};
-          const int i = kg * 64 + s * 16 + 2 * t + koff[e];
-          const int bit = 6 * n;
-          const uint64_t v = ((uint64_t)w[bit / 32 + 1] << 32) | w[bit / 32];
-          const uint32_t idx = (uint32_t)(v >> (bit % 32)) & 63u;
-          const size_t k = (size_t)p * d_in + i;
-          const size_t sb = 6 * k;
-          canonical[sb / 8] |= (uint8_t)(idx << (sb % 8));
-          if (sb % 8 > 2) canonical[sb / 8 + 1] |= (uint8_t)(idx >> (8 - sb % 8));
-        }
-      }
-    }
-  });
-  return ok();
+  return vq3_unpack_layout_fmt(VQ3_FORMAT_2X64, packed_host, d_in, d_out, canonical);
 }
 
 int fwht_rotate(const uint16_t* x, int rows, int n, int block, const uint32_t* signs, uint16_t* out, void* stream) {

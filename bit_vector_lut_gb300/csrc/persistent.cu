@@ -49,8 +49,14 @@ namespace {
 
 constexpr int kWarps = kDecWarps;  // 16
 constexpr int kThreads = kWarps * 32;
-constexpr int kTabWords = 64 * 32;
-constexpr uint32_t kTabAlign = 16384;
+// Lane-private codebook tables: entry k of lane L at word k*32 + L; one table
+// per matrix, kTabStride bytes apart, the pair of gate and up tables aligned to
+// twice that so the matrix choice is an OR of the table offset.
+template <int F>
+struct Tab {
+  static constexpr uint32_t kStride = (uint32_t)Fmt<F>::kEntries * 128u;  // 8 KB or 2 KB
+  static constexpr uint32_t kAlign = 2u * kStride;
+};
 constexpr long long kSpinLimit = 1ll << 21;  // polls of one wait: well over a second
 
 // ------------------------------------------------------------------ primitives
@@ -63,22 +69,26 @@ __device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Shared address of the lookup for lane index N: bits [6N, 6N+6) of the lane's
-// 384-bit string moved to bits [7, 13) (entry stride 32 lanes x 4 bytes), OR-ed
-// with the table base, the lane's column and the matrix's table offset.
-template <int N>
-__device__ __forceinline__ uint32_t lut_addr(const uint32_t (&w)[12], uint32_t lanebase) {
-  constexpr int pos = 6 * N;
+// Shared address of the lookup for lane index N: bits [b N, b N + b) of the
+// lane's string (b = index width) moved to bits [7, 7 + b) (entry stride 32 lanes
+// x 4 bytes), OR-ed with the table base, the lane's column and the matrix's
+// table offset.
+template <int F, int N>
+__device__ __forceinline__ uint32_t lut_addr(const uint32_t (&w)[Fmt<F>::kWords], uint32_t lanebase) {
+  constexpr int kB = Fmt<F>::kBits;
+  constexpr int pos = kB * N;
   constexpr int wd = pos / 32;
   constexpr int off = pos % 32;
+  constexpr uint32_t mask = ((1u << kB) - 1u) << 7;
   uint32_t v;
-  if constexpr (off >= 7) {
-    const uint32_t hi = (wd + 1 < 12) ? w[wd + 1] : 0u;
-    v = __funnelshift_r(w[wd], hi, off - 7);
+  if constexpr (off + kB > 32) {
+    v = __funnelshift_r(w[wd], w[wd + 1], off - 7);  // the field straddles two words
+  } else if constexpr (off >= 7) {
+    v = w[wd] >> (off - 7);
   } else {
     v = w[wd] << (7 - off);
   }
-  return (v & 0x1F80u) | lanebase;
+  return (v & mask) | lanebase;
 }
 
 // The tables are read-only while cells are decoded: a pure load, free to reorder.
@@ -354,40 +364,65 @@ __device__ __forceinline__ void stage_round(const DecodeJob& a, const T* src, lo
 
 // ------------------------------------------------------------------ decode
 
-template <int S, int M, int NT>
-__device__ __forceinline__ void mma_step(const uint32_t (&w)[12], uint32_t lanebase, float (&acc)[4][NT][4],
-                                         const uint32_t (&b)[NT][8]) {
-  constexpr int n0 = (S * 4 + M) * 4;
-  const uint32_t l0 = lut(lut_addr<n0 + 0>(w, lanebase));
-  const uint32_t l1 = lut(lut_addr<n0 + 1>(w, lanebase));
-  const uint32_t l2 = lut(lut_addr<n0 + 2>(w, lanebase));
-  const uint32_t l3 = lut(lut_addr<n0 + 3>(w, lanebase));
+// A fragment of k-step S, 16-channel tile M, from the lane's string.
+template <int F, int S, int M>
+__device__ __forceinline__ void a_frag(const uint32_t (&w)[Fmt<F>::kWords], uint32_t lanebase, uint32_t (&a)[4]) {
+  if constexpr (Fmt<F>::kVec == 2) {
+    // one index per output pair: entry = (channel 2p, channel 2p+1)
+    constexpr int n0 = (S * 4 + M) * 4;
+    const uint32_t l0 = lut(lut_addr<F, n0 + 0>(w, lanebase));
+    const uint32_t l1 = lut(lut_addr<F, n0 + 1>(w, lanebase));
+    const uint32_t l2 = lut(lut_addr<F, n0 + 2>(w, lanebase));
+    const uint32_t l3 = lut(lut_addr<F, n0 + 3>(w, lanebase));
+    a[0] = __byte_perm(l0, l1, 0x5410);  // row g   (channel 2p):   inputs k, k+1
+    a[1] = __byte_perm(l0, l1, 0x7632);  // row g+8 (channel 2p+1): inputs k, k+1
+    a[2] = __byte_perm(l2, l3, 0x5410);  // row g:   inputs k+8, k+9
+    a[3] = __byte_perm(l2, l3, 0x7632);  // row g+8: inputs k+8, k+9
+  } else {
+    // one index per weight, index (e, c) at n0 + 2e + c: entry = the weight in the low half
+    constexpr int n0 = (S * 4 + M) * 8;
+    uint32_t l[8];
+    l[0] = lut(lut_addr<F, n0 + 0>(w, lanebase));
+    l[1] = lut(lut_addr<F, n0 + 1>(w, lanebase));
+    l[2] = lut(lut_addr<F, n0 + 2>(w, lanebase));
+    l[3] = lut(lut_addr<F, n0 + 3>(w, lanebase));
+    l[4] = lut(lut_addr<F, n0 + 4>(w, lanebase));
+    l[5] = lut(lut_addr<F, n0 + 5>(w, lanebase));
+    l[6] = lut(lut_addr<F, n0 + 6>(w, lanebase));
+    l[7] = lut(lut_addr<F, n0 + 7>(w, lanebase));
+    a[0] = __byte_perm(l[0], l[2], 0x5410);  // row g   (channel 2p):   inputs k, k+1
+    a[1] = __byte_perm(l[1], l[3], 0x5410);  // row g+8 (channel 2p+1): inputs k, k+1
+    a[2] = __byte_perm(l[4], l[6], 0x5410);  // row g:   inputs k+8, k+9
+    a[3] = __byte_perm(l[5], l[7], 0x5410);  // row g+8: inputs k+8, k+9
+  }
+}
+
+template <int F, int S, int M, int NT>
+__device__ __forceinline__ void mma_step(const uint32_t (&w)[Fmt<F>::kWords], uint32_t lanebase,
+                                         float (&acc)[4][NT][4], const uint32_t (&b)[NT][8]) {
   uint32_t a[4];
-  a[0] = __byte_perm(l0, l1, 0x5410);  // row g   (channel 2p):   inputs k, k+1
-  a[1] = __byte_perm(l0, l1, 0x7632);  // row g+8 (channel 2p+1): inputs k, k+1
-  a[2] = __byte_perm(l2, l3, 0x5410);  // row g:   inputs k+8, k+9
-  a[3] = __byte_perm(l2, l3, 0x7632);  // row g+8: inputs k+8, k+9
+  a_frag<F, S, M>(w, lanebase, a);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) mma16816(acc[M][nt], a, b[nt][2 * S], b[nt][2 * S + 1]);
 }
 
-template <int S, int NT>
-__device__ __forceinline__ void kstep(const uint32_t (&w)[12], uint32_t lanebase, float (&acc)[4][NT][4],
-                                      const uint32_t (&b)[NT][8]) {
-  mma_step<S, 0, NT>(w, lanebase, acc, b);
-  mma_step<S, 1, NT>(w, lanebase, acc, b);
-  mma_step<S, 2, NT>(w, lanebase, acc, b);
-  mma_step<S, 3, NT>(w, lanebase, acc, b);
+template <int F, int S, int NT>
+__device__ __forceinline__ void kstep(const uint32_t (&w)[Fmt<F>::kWords], uint32_t lanebase,
+                                      float (&acc)[4][NT][4], const uint32_t (&b)[NT][8]) {
+  mma_step<F, S, 0, NT>(w, lanebase, acc, b);
+  mma_step<F, S, 1, NT>(w, lanebase, acc, b);
+  mma_step<F, S, 2, NT>(w, lanebase, acc, b);
+  mma_step<F, S, 3, NT>(w, lanebase, acc, b);
 }
 
 // One super-unit: the lane's index string from its ring slot, the B fragments
 // of stage slot p (NT KB at xb, chunks swizzled by p & 7).
-template <int NT>
+template <int F, int NT>
 __device__ __forceinline__ void compute_cell(uint32_t slot, uint32_t xb, int lane, int swz, uint32_t lanebase,
                                              float (&acc)[4][NT][4]) {
-  uint32_t w[12];
+  uint32_t w[Fmt<F>::kWords];
 #pragma unroll
-  for (int q = 0; q < 3; ++q) {
+  for (int q = 0; q < FmtSizes<F>::kChunks; ++q) {
     const uint4 v = lds128(slot + (uint32_t)(q * 512 + lane * 16));
     w[4 * q + 0] = v.x;
     w[4 * q + 1] = v.y;
@@ -406,10 +441,10 @@ __device__ __forceinline__ void compute_cell(uint32_t slot, uint32_t xb, int lan
       b[nt][4 * h + 2] = v.z;
       b[nt][4 * h + 3] = v.w;
     }
-  kstep<0, NT>(w, lanebase, acc, b);
-  kstep<1, NT>(w, lanebase, acc, b);
-  kstep<2, NT>(w, lanebase, acc, b);
-  kstep<3, NT>(w, lanebase, acc, b);
+  kstep<F, 0, NT>(w, lanebase, acc, b);
+  kstep<F, 1, NT>(w, lanebase, acc, b);
+  kstep<F, 2, NT>(w, lanebase, acc, b);
+  kstep<F, 3, NT>(w, lanebase, acc, b);
 }
 
 // Index-copy cursor of one warp: the next cell of its CTA's range whose copies
@@ -425,8 +460,12 @@ struct Cursor {
 };
 
 constexpr int kSlots = 3;
-constexpr int kSlotBytes = kSuBytes;  // one super-unit
-constexpr int kWarpRing = kSlots * kSlotBytes;
+// A warp's ring: kSlots slots of one super-unit each.
+template <int F>
+struct Ring {
+  static constexpr int kSlotBytes = FmtSizes<F>::kSuBytes;
+  static constexpr int kWarpBytes = kSlots * kSlotBytes;
+};
 
 __device__ __forceinline__ void cell_range(const DecodeJob& a, long long& c0, long long& c1) {
   const long long cells = a.cells();
@@ -435,6 +474,7 @@ __device__ __forceinline__ void cell_range(const DecodeJob& a, long long& c0, lo
 }
 
 // Points the cursor at column group kg of group g.
+template <int F>
 __device__ __forceinline__ void cursor_group(const DecodeJob& a, Cursor& cur, int g, int kg) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sg = g * kWarps + warp;
@@ -445,41 +485,43 @@ __device__ __forceinline__ void cursor_group(const DecodeJob& a, Cursor& cur, in
   const bool two = a.n_mats > 1;
   const int mat = two ? (sg & 1) : 0;
   const int mg = two ? (sg >> 1) : sg;
-  cur.src = (mat ? a.packed1 : a.packed0) + ((size_t)mg * n_kg + kg) * kSuUint4 + lane;
+  cur.src = (mat ? a.packed1 : a.packed0) + ((size_t)mg * n_kg + kg) * FmtSizes<F>::kSuUint4 + lane;
 }
 
 // Issues the index copies of the warp's segment in the cursor's next cell (an
 // empty commit group past the range end or for a segment past the last).
+template <int F>
 __device__ __forceinline__ void issue_cell(const DecodeJob& a, Cursor& cur, uint32_t ring_lane) {
   if (cur.left > 0 && cur.live) {
     const uint32_t s = ring_lane + cur.slot;
-    cp_async16(s, cur.src);
-    cp_async16(s + 512, cur.src + 32);
-    cp_async16(s + 1024, cur.src + 64);
+#pragma unroll
+    for (int q = 0; q < FmtSizes<F>::kChunks; ++q) cp_async16(s + (uint32_t)(q * 512), cur.src + 32 * q);
   }
   cp_async_commit();
-  cur.slot = cur.slot == (kSlots - 1) * kSlotBytes ? 0u : cur.slot + kSlotBytes;
-  cur.src += kSuUint4;
+  constexpr uint32_t kSlot = (uint32_t)Ring<F>::kSlotBytes;
+  cur.slot = cur.slot == (kSlots - 1) * kSlot ? 0u : cur.slot + kSlot;
+  cur.src += FmtSizes<F>::kSuUint4;
   --cur.left;
-  if (--cur.kg_left == 0 && cur.left > 0) cursor_group(a, cur, cur.g + 1, 0);
+  if (--cur.kg_left == 0 && cur.left > 0) cursor_group<F>(a, cur, cur.g + 1, 0);
 }
 
 // Index copies of the first n cells of the CTA's range.
+template <int F>
 __device__ __forceinline__ Cursor decode_begin(const DecodeJob& a, const SmemView& sv, int n) {
   Cursor cur{nullptr, 0, 0, 0, 0u, false};
   if ((int)blockIdx.x >= a.grid) return cur;
   long long c0, c1;
   cell_range(a, c0, c1);
   cur.left = (int)(c1 - c0);
-  cursor_group(a, cur, (int)(c0 / a.n_kg()), (int)(c0 % a.n_kg()));
-  const uint32_t ring_lane = sv.ring + (uint32_t)((threadIdx.x >> 5) * kWarpRing + (threadIdx.x & 31) * 16);
-  for (int k = 0; k < n; ++k) issue_cell(a, cur, ring_lane);
+  cursor_group<F>(a, cur, (int)(c0 / a.n_kg()), (int)(c0 % a.n_kg()));
+  const uint32_t ring_lane = sv.ring + (uint32_t)((threadIdx.x >> 5) * Ring<F>::kWarpBytes + (threadIdx.x & 31) * 16);
+  for (int k = 0; k < n; ++k) issue_cell<F>(a, cur, ring_lane);
   return cur;
 }
 
 // Decodes the CTA's range of cells; `cur` has issued the copies of its first
 // 1 .. kSlots cells, the rest of the prologue follows the first stage.
-template <int NT, typename T>
+template <int F, int NT, typename T>
 __device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cursor& cur, const SmemView& sv,
                                            int* status) {
   constexpr int PIECE = 512 * NT;
@@ -489,7 +531,8 @@ __device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cur
   const int n_kg = a.n_kg(), n_seg = a.n_seg();
   long long c0, c1;
   cell_range(a, c0, c1);
-  const uint32_t ring = sv.ring + (uint32_t)(warp * kWarpRing);
+  const uint32_t ring = sv.ring + (uint32_t)(warp * Ring<F>::kWarpBytes);
+  constexpr uint32_t kSlot = (uint32_t)Ring<F>::kSlotBytes;
   const uint32_t ring_lane = ring + (uint32_t)(lane * 16);
   const bool two = a.n_mats > 1;
   uint32_t use_slot = 0;  // ring slot of the next cell to compute
@@ -514,13 +557,13 @@ __device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cur
       __syncthreads();  // thread 0's acquire loads, then the barrier: the chunks are visible to the CTA
     }
     stage_round<NT, T>(a, src, rs, len, sv);
-    for (; issued < kSlots; ++issued) issue_cell(a, cur, ring_lane);  // rest of the prologue
+    for (; issued < kSlots; ++issued) issue_cell<F>(a, cur, ring_lane);  // rest of the prologue
     __syncthreads();
     for (int p = 0; p < len; ++p) {
       if (first) {  // the range's part of group g starts
         sg = g * kWarps + warp;
         live = sg < n_seg;
-        lane_base = a.tab | (uint32_t)(lane * 4) | ((two && (sg & 1)) ? 8192u : 0u);
+        lane_base = a.tab | (uint32_t)(lane * 4) | ((two && (sg & 1)) ? Tab<F>::kStride : 0u);
 #pragma unroll
         for (int m = 0; m < 4; ++m)
 #pragma unroll
@@ -530,9 +573,9 @@ __device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cur
       }
       cp_async_wait<kSlots - 1>();  // this cell's index copies have landed
       if (live)
-        compute_cell<NT>(ring + use_slot, sv.stage + (uint32_t)(p * NT * 1024), lane, p & 7, lane_base, acc);
-      issue_cell(a, cur, ring_lane);  // refill the slot just read, kSlots cells ahead
-      use_slot = use_slot == (kSlots - 1) * kSlotBytes ? 0u : use_slot + kSlotBytes;
+        compute_cell<F, NT>(ring + use_slot, sv.stage + (uint32_t)(p * NT * 1024), lane, p & 7, lane_base, acc);
+      issue_cell<F>(a, cur, ring_lane);  // refill the slot just read, kSlots cells ahead
+      use_slot = use_slot == (kSlots - 1) * kSlot ? 0u : use_slot + kSlot;
       first = (++kg == n_kg);
       if (first || r0 + p + 1 == total) {
         // this warp's segment over the range's part of group g: one piece
@@ -665,38 +708,49 @@ __device__ __forceinline__ void output_tasks(const PersistArgs& a, const DecodeJ
 
 // ------------------------------------------------------------------ the kernel
 
-template <int NT>
+template <int NT, int F>
 struct Smem {
-  static constexpr uint32_t kRing = kWarps * kWarpRing;
+  static constexpr uint32_t kRing = kWarps * Ring<F>::kWarpBytes;
   static constexpr uint32_t kStage = StageCfg<NT>::kBytes;
   static constexpr uint32_t kScratch = kWarps * 4096;  // rotation scratch, 4 KB per warp
-  static constexpr uint32_t kTabs = 3 * kTabWords * 4;  // gate, up, down (or one matrix)
-  static constexpr uint32_t kTotal = kRing + kStage + kScratch + kTabAlign + kTabs;
+  static constexpr uint32_t kTabs = 3 * Tab<F>::kStride;  // gate, up, down (or one matrix)
+  static constexpr uint32_t kTotal = kRing + kStage + kScratch + Tab<F>::kAlign + kTabs;
 };
 
 // Lane-private tables: entry k of matrix t replicated into words k*32 .. k*32+31
-// at tab + t*8192, written 4 lanes (16 bytes) at a time.
+// at tab + t * stride, written 4 lanes (16 bytes) at a time. A vector format's
+// codebook word k is (component 0 | component 1 << 16); a scalar entry is
+// stored as (entry | entry << 16).
+template <int F>
 __device__ void load_tables(uint32_t tab, const uint32_t* cb0, const uint32_t* cb1, const uint32_t* cb2) {
-  for (int i = threadIdx.x; i < 3 * 64 * 8; i += kThreads) {
-    const int t = i / 512, k = (i >> 3) & 63, q = i & 7;
+  constexpr int E = Fmt<F>::kEntries;
+  for (int i = threadIdx.x; i < 3 * E * 8; i += kThreads) {
+    const int t = i / (E * 8), k = (i >> 3) % E, q = i & 7;
     const uint32_t* cb = t == 0 ? cb0 : (t == 1 ? cb1 : cb2);
     if (cb) {
-      const uint32_t v = __ldg(cb + k);
-      sts128(tab + (uint32_t)(t * 8192 + k * 128 + q * 16), v, v, v, v);
+      uint32_t v;
+      if constexpr (Fmt<F>::kVec == 2) {
+        v = __ldg(cb + k);
+      } else {
+        const uint32_t h = __ldg(reinterpret_cast<const uint16_t*>(cb) + k);
+        v = h | (h << 16);
+      }
+      sts128(tab + (uint32_t)(t * Tab<F>::kStride + k * 128 + q * 16), v, v, v, v);
     }
   }
 }
 
-template <int NT>
+template <int NT, int F>
 __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) {
   extern __shared__ __align__(16) unsigned char dsm[];
   __shared__ int s_flag;
   SmemView sv;
   const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(dsm));
   sv.ring = base;
-  sv.stage = base + Smem<NT>::kRing;
-  sv.scratch = reinterpret_cast<float*>(dsm + Smem<NT>::kRing + Smem<NT>::kStage);
-  sv.tab = (base + Smem<NT>::kRing + Smem<NT>::kStage + Smem<NT>::kScratch + kTabAlign - 1) & ~(kTabAlign - 1);
+  using SM = Smem<NT, F>;
+  sv.stage = base + SM::kRing;
+  sv.scratch = reinterpret_cast<float*>(dsm + SM::kRing + SM::kStage);
+  sv.tab = (base + SM::kRing + SM::kStage + SM::kScratch + Tab<F>::kAlign - 1) & ~(Tab<F>::kAlign - 1);
   sv.flag = &s_flag;
   int* status = a.status;
   unsigned* ctl = a.ctl;
@@ -721,11 +775,11 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
   j1.ready_target = 0;
   j1.group_done = ctl + (a.mlp ? a.off_g : a.off_o);
 
-  load_tables(sv.tab, a.gate.codebook, a.mlp ? a.up.codebook : nullptr, a.mlp ? a.down.codebook : nullptr);
+  load_tables<F>(sv.tab, a.gate.codebook, a.mlp ? a.up.codebook : nullptr, a.mlp ? a.down.codebook : nullptr);
   // one cell's index copies, then the rotation of x (its loads not queued behind
   // the bulk of the prologue), then the rest of the prologue
-  Cursor cur = decode_begin(j1, sv, 1);
-  decode_run<NT, uint16_t>(j1, a.x + (size_t)a.row0 * a.d_model, cur, sv, status);
+  Cursor cur = decode_begin<F>(j1, sv, 1);
+  decode_run<F, NT, uint16_t>(j1, a.x + (size_t)a.row0 * a.d_model, cur, sv, status);
 
   if (a.mlp) {
     DecodeJob j3;
@@ -737,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
     j3.pieces = a.pieces3;
     j3.grid = a.grid3;
     j3.max_pieces = a.max_pieces3;
-    j3.tab = sv.tab + 16384u;
+    j3.tab = sv.tab + 2u * Tab<F>::kStride;
     j3.src_ld = (size_t)a.d_inter;
     j3.rows = a.rows;
     j3.block = a.block_dn;
@@ -748,8 +802,8 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
     j3.group_done = ctl + a.off_o;
     swiglu_tasks<NT>(a, j1, ctl + a.off_hd, status);
     // one cell's index copies ahead of the h rotation, the rest after it (as for x)
-    Cursor cur3 = decode_begin(j3, sv, 1);
-    decode_run<NT, float>(j3, a.hbuf, cur3, sv, status);
+    Cursor cur3 = decode_begin<F>(j3, sv, 1);
+    decode_run<F, NT, float>(j3, a.hbuf, cur3, sv, status);
     output_tasks<NT>(a, j3, status);
   } else {
     output_tasks<NT>(a, j1, status);
@@ -768,16 +822,22 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
     for (int i = threadIdx.x; i < a.n_ctl; i += kThreads) ctl[i] = 0u;
 }
 
-template <int NT>
+// Every format's kernel needs more than half an SM's shared memory: one CTA per SM,
+// so the grid (and the workspace sized from it) is the same for all formats.
+static_assert(2 * Smem<1, VQ3_FORMAT_2X16>::kTotal > 228 * 1024, "one CTA per SM");
+static_assert(Smem<4, VQ3_FORMAT_LUT4>::kTotal <= 227 * 1024 && Smem<4, VQ3_FORMAT_2X64>::kTotal <= 227 * 1024,
+              "shared memory per CTA");
+
+template <int NT, int F>
 cudaError_t launch_nt(const PersistArgs& a, cudaStream_t st) {
-  const int smem = (int)Smem<NT>::kTotal;
+  const int smem = (int)Smem<NT, F>::kTotal;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(persistent_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(persistent_kernel<NT, F>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
@@ -791,17 +851,18 @@ cudaError_t launch_nt(const PersistArgs& a, cudaStream_t st) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, persistent_kernel<NT>, a);
+  e = cudaLaunchKernelEx(&cfg, persistent_kernel<NT, F>, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 template <int NT>
 int occupancy() {
+  using K = Smem<NT, VQ3_FORMAT_2X64>;
   int n = 0;
-  if (cudaFuncSetAttribute(persistent_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)Smem<NT>::kTotal) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, persistent_kernel<NT>, kThreads, Smem<NT>::kTotal) !=
+  if (cudaFuncSetAttribute(persistent_kernel<NT, VQ3_FORMAT_2X64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)K::kTotal) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, persistent_kernel<NT, VQ3_FORMAT_2X64>, kThreads, K::kTotal) !=
           cudaSuccess) {
     cudaGetLastError();
     return 1;
@@ -856,11 +917,23 @@ int persist_chunk(int d, int block) {
   return chunk;
 }
 
-cudaError_t launch_persistent(const PersistArgs& a, int nt, cudaStream_t st) {
+namespace {
+template <int F>
+cudaError_t launch_fmt(const PersistArgs& a, int nt, cudaStream_t st) {
   switch (nt) {
-    case 1: return launch_nt<1>(a, st);
-    case 2: return launch_nt<2>(a, st);
-    case 4: return launch_nt<4>(a, st);
+    case 1: return launch_nt<1, F>(a, st);
+    case 2: return launch_nt<2, F>(a, st);
+    case 4: return launch_nt<4, F>(a, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+}  // namespace
+
+cudaError_t launch_persistent(const PersistArgs& a, int nt, cudaStream_t st) {
+  switch (a.format) {
+    case VQ3_FORMAT_2X64: return launch_fmt<VQ3_FORMAT_2X64>(a, nt, st);
+    case VQ3_FORMAT_2X16: return launch_fmt<VQ3_FORMAT_2X16>(a, nt, st);
+    case VQ3_FORMAT_LUT4: return launch_fmt<VQ3_FORMAT_LUT4>(a, nt, st);
     default: return cudaErrorInvalidValue;
   }
 }

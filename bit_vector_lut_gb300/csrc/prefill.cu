@@ -55,8 +55,13 @@ constexpr int kMaxStages = 6;
 constexpr int kPrefetchSteps = 8;  // index strings are prefetched into L2 this many K steps ahead
 constexpr int kTileM = 128;                    // output channels per tile
 constexpr int kATile = kTileM * 64 * 2;        // 16 KB of FP16
-constexpr int kTabWords = 64 * 32;
-constexpr uint32_t kTabAlign = 16384;
+// Lane-private codebook tables (entry k of lane L at word k*32 + L), the gate and
+// up tables kStride bytes apart and aligned to twice that (matrix choice by OR).
+template <int F>
+struct PfTab {
+  static constexpr uint32_t kStride = (uint32_t)Fmt<F>::kEntries * 128u;
+  static constexpr uint32_t kAlign = 2u * kStride;
+};
 constexpr long long kWaitSpin = 1ll << 22;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -171,19 +176,23 @@ __device__ __forceinline__ void sts32(uint32_t a, uint32_t v) {
   asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 
-// Lookup address of index N of a lane string: bits [6N, 6N+6) moved to [7, 13)
-// (entry stride 32 lanes x 4 bytes), OR-ed with the table base and lane column.
-template <int N>
-__device__ __forceinline__ uint32_t lut_addr(const uint32_t (&w)[12], uint32_t lanebase) {
-  constexpr int pos = 6 * N, wd = pos >> 5, off = pos & 31;
+// Lookup address of index N of a lane string: bits [b N, b N + b) (b = index
+// width) moved to [7, 7 + b) (entry stride 32 lanes x 4 bytes), OR-ed with the
+// table base and lane column.
+template <int F, int N>
+__device__ __forceinline__ uint32_t lut_addr(const uint32_t (&w)[Fmt<F>::kWords], uint32_t lanebase) {
+  constexpr int kB = Fmt<F>::kBits;
+  constexpr int pos = kB * N, wd = pos >> 5, off = pos & 31;
+  constexpr uint32_t mask = ((1u << kB) - 1u) << 7;
   uint32_t v;
-  if constexpr (off >= 7) {
-    const uint32_t hi = (wd + 1 < 12) ? w[wd + 1] : 0u;
-    v = __funnelshift_r(w[wd], hi, off - 7);
+  if constexpr (off + kB > 32) {
+    v = __funnelshift_r(w[wd], w[wd + 1], off - 7);  // the field straddles two words
+  } else if constexpr (off >= 7) {
+    v = w[wd] >> (off - 7);
   } else {
     v = w[wd] << (7 - off);
   }
-  return (v & 0x1F80u) | lanebase;
+  return (v & mask) | lanebase;
 }
 
 // Byte offset of (row, k) in a K-major core-matrix tile with `rows` rows and 64
@@ -194,39 +203,52 @@ __device__ __forceinline__ uint32_t tile_off(int row, int k, int rows) {
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
-template <int N0, int NL, int... J>
-__device__ __forceinline__ void lookups(const uint32_t (&w)[12], uint32_t lanebase, uint32_t (&lk)[NL],
+template <int F, int N0, int NL, int... J>
+__device__ __forceinline__ void lookups(const uint32_t (&w)[Fmt<F>::kWords], uint32_t lanebase, uint32_t (&lk)[NL],
                                         std::integer_sequence<int, J...>) {
-  ((lk[J] = lds32(lut_addr<N0 + J>(w, lanebase))), ...);
+  ((lk[J] = lds32(lut_addr<F, N0 + J>(w, lanebase))), ...);
 }
 
 // Decodes the producer thread's share of the weight tile of one K step: input
 // steps S0 .. S0 + NS - 1 (16 inputs each) of lane string L = lane of one
-// super-unit. A-fragment order of the lane string (see vq3_internal.h): index
-// n = (s*4 + m)*4 + e is pair m*8 + g at input s*16 + {2t, 2t+1, 2t+8, 2t+9}[e]
-// with g = L/4, t = L%4. All lookups are issued before the first store, so one
-// shared-memory latency covers them. Channels 2p and 2p+1 of a pair are 16
-// bytes apart in the tile; lanes with g >= 4 store the odd channel first, which
-// puts the 32 lanes of each store on 32 different banks.
-template <int S0, int NS>
-__device__ __forceinline__ void decode_steps(const uint32_t (&w)[12], int lane, int row0, uint32_t a_tile,
-                                             uint32_t lanebase) {
-  uint32_t lk[16 * NS];
-  lookups<S0 * 16, 16 * NS>(w, lanebase, lk, std::make_integer_sequence<int, 16 * NS>{});
+// super-unit. Lane-string order (see vq3_internal.h): for the vector formats
+// index n = (s*4 + m)*4 + e is pair m*8 + g at input s*16 + {2t, 2t+1, 2t+8,
+// 2t+9}[e]; for the scalar format index 2n + c is channel 2(m*8 + g) + c at the
+// same input; g = L/4, t = L%4. All lookups are issued before the first store,
+// so one shared-memory latency covers them. Channels 2p and 2p+1 of a pair are
+// 16 bytes apart in the tile; lanes with g >= 4 store the odd channel first,
+// which puts the 32 lanes of each store on 32 different banks.
+template <int F, int S0, int NS>
+__device__ __forceinline__ void decode_steps(const uint32_t (&w)[Fmt<F>::kWords], int lane, int row0,
+                                             uint32_t a_tile, uint32_t lanebase) {
+  constexpr int kPerStep = 32 / Fmt<F>::kVec;  // lookups per k-step of 16 inputs: 16 (vector) or 32 (scalar)
+  uint32_t lk[kPerStep * NS];
+  lookups<F, S0 * kPerStep, kPerStep * NS>(w, lanebase, lk, std::make_integer_sequence<int, kPerStep * NS>{});
   const int g = lane >> 2, t = lane & 3;
-  const uint32_t swap = g >= 4 ? 16u : 0u;
-  const uint32_t sel_a = g >= 4 ? 0x7632u : 0x5410u, sel_b = sel_a ^ 0x2222u;
+  const bool odd_first = g >= 4;
+  const uint32_t swap = odd_first ? 16u : 0u;
+  const uint32_t sel_a = odd_first ? 0x7632u : 0x5410u, sel_b = sel_a ^ 0x2222u;
 #pragma unroll
   for (int sm = 0; sm < 4 * NS; ++sm) {  // (s - S0, m)
     const int S = S0 + (sm >> 2), M = sm & 3;
-    const uint32_t* l = lk + 4 * sm;
     const int r = row0 + 2 * (M * 8 + g);  // channel 2p of the tile; 2p+1 is the next row
     const int k = S * 16 + 2 * t;
     const uint32_t o0 = a_tile + tile_off(r, k, kTileM), o8 = a_tile + tile_off(r, k + 8, kTileM);
-    sts32(o0 + swap, __byte_perm(l[0], l[1], sel_a));
-    sts32(o0 + (16u - swap), __byte_perm(l[0], l[1], sel_b));
-    sts32(o8 + swap, __byte_perm(l[2], l[3], sel_a));
-    sts32(o8 + (16u - swap), __byte_perm(l[2], l[3], sel_b));
+    if constexpr (Fmt<F>::kVec == 2) {
+      const uint32_t* l = lk + 4 * sm;
+      sts32(o0 + swap, __byte_perm(l[0], l[1], sel_a));
+      sts32(o0 + (16u - swap), __byte_perm(l[0], l[1], sel_b));
+      sts32(o8 + swap, __byte_perm(l[2], l[3], sel_a));
+      sts32(o8 + (16u - swap), __byte_perm(l[2], l[3], sel_b));
+    } else {
+      const uint32_t* l = lk + 8 * sm;  // index (e, c) at 2e + c
+      const uint32_t a0 = __byte_perm(l[0], l[2], 0x5410), a1 = __byte_perm(l[1], l[3], 0x5410);
+      const uint32_t a2 = __byte_perm(l[4], l[6], 0x5410), a3 = __byte_perm(l[5], l[7], 0x5410);
+      sts32(o0 + swap, odd_first ? a1 : a0);
+      sts32(o0 + (16u - swap), odd_first ? a0 : a1);
+      sts32(o8 + swap, odd_first ? a3 : a2);
+      sts32(o8 + (16u - swap), odd_first ? a2 : a3);
+    }
   }
 }
 
@@ -235,36 +257,39 @@ constexpr int kDecPerSu = kDecWarps / 2;
 constexpr int kStepsPerDec = 4 / kDecPerSu;
 static_assert(kDecWarps == 2 || kDecWarps == 4 || kDecWarps == 8, "decoder warps split the 4 input steps evenly");
 
-__device__ __forceinline__ void decode_part(const uint32_t (&w)[12], int part, int lane, int row0, uint32_t a_tile,
-                                            uint32_t lanebase) {
+template <int F>
+__device__ __forceinline__ void decode_part(const uint32_t (&w)[Fmt<F>::kWords], int part, int lane, int row0,
+                                            uint32_t a_tile, uint32_t lanebase) {
   if constexpr (kStepsPerDec == 1) {
     switch (part) {
-      case 0: decode_steps<0, 1>(w, lane, row0, a_tile, lanebase); break;
-      case 1: decode_steps<1, 1>(w, lane, row0, a_tile, lanebase); break;
-      case 2: decode_steps<2, 1>(w, lane, row0, a_tile, lanebase); break;
-      default: decode_steps<3, 1>(w, lane, row0, a_tile, lanebase); break;
+      case 0: decode_steps<F, 0, 1>(w, lane, row0, a_tile, lanebase); break;
+      case 1: decode_steps<F, 1, 1>(w, lane, row0, a_tile, lanebase); break;
+      case 2: decode_steps<F, 2, 1>(w, lane, row0, a_tile, lanebase); break;
+      default: decode_steps<F, 3, 1>(w, lane, row0, a_tile, lanebase); break;
     }
   } else if constexpr (kStepsPerDec == 2) {
     if (part == 0)
-      decode_steps<0, 2>(w, lane, row0, a_tile, lanebase);
+      decode_steps<F, 0, 2>(w, lane, row0, a_tile, lanebase);
     else
-      decode_steps<2, 2>(w, lane, row0, a_tile, lanebase);
+      decode_steps<F, 2, 2>(w, lane, row0, a_tile, lanebase);
   } else {
-    decode_steps<0, 4>(w, lane, row0, a_tile, lanebase);
+    decode_steps<F, 0, 4>(w, lane, row0, a_tile, lanebase);
   }
 }
 
-constexpr int kIdxBytes = 2 * kSuBytes;  // index strings of the tile's two super-units per K step
-
-template <int N>
+template <int N, int F>
 struct PfSmem {
   static constexpr int kBTile = N * 64 * 2;
+  static constexpr int kSu = FmtSizes<F>::kSuBytes;
+  static constexpr int kIdxBytes = 2 * kSu;  // index strings of the tile's two super-units per K step
   static constexpr int kStageBytes = kATile + kBTile + kIdxBytes;
   static_assert(kStageBytes % 1024 == 0 && kATile % 1024 == 0, "B tiles start on 1 KB swizzle atoms");
   // stages in flight: as many as fit, up to kMaxStages (the K loop is latency-bound at small N)
   static constexpr int kStages = N >= 256 ? 3 : (N >= 128 ? 5 : 6);
   static_assert(kStages <= kMaxStages, "barrier array size");
-  static constexpr int kTotal = 1024 + kStages * kStageBytes + (int)kTabAlign + 2 * kTabWords * 4 + 64 * 16 * 4;
+  static constexpr int kTotal = 1024 + kStages * kStageBytes + (int)PfTab<F>::kAlign + 2 * (int)PfTab<F>::kStride +
+                                64 * 16 * 4;
+  static_assert(kTotal <= 227 * 1024, "shared memory per CTA");
 };
 
 // This CTA's share of the (tile, K step) space: steps [begin(c), begin(c + 1)).
@@ -293,42 +318,52 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
 
 // One CTA per SM: the smallest configuration still needs more than half of an
 // SM's shared memory, so no two CTAs ever share an SM (and its tensor memory).
-static_assert(2 * PfSmem<64>::kTotal > 228 * 1024, "one prefill CTA per SM");
+static_assert(2 * PfSmem<64, VQ3_FORMAT_2X16>::kTotal > 228 * 1024, "one prefill CTA per SM");
 
-template <int N>
+template <int N, int F>
 __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid_constant__ PrefillArgs a,
                                                                      const __grid_constant__ CUtensorMap xmap) {
   extern __shared__ __align__(16) unsigned char dsm[];
-  constexpr int kStages = PfSmem<N>::kStages;
+  using PS = PfSmem<N, F>;
+  constexpr int kStages = PS::kStages;
   __shared__ __align__(8) unsigned long long s_bars[3 * kMaxStages + 4];
   __shared__ uint32_t s_tmem;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t raw = smem_u32(dsm);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 1 KB aligned stages (swizzle atoms)
-  const uint32_t tabs = (base + kStages * PfSmem<N>::kStageBytes + kTabAlign - 1) & ~(kTabAlign - 1);
-  float* xch = reinterpret_cast<float*>(dsm + (tabs - raw) + 2 * kTabWords * 4);  // up values for SwiGLU
+  const uint32_t tabs = (base + kStages * PS::kStageBytes + PfTab<F>::kAlign - 1) & ~(PfTab<F>::kAlign - 1);
+  float* xch = reinterpret_cast<float*>(dsm + (tabs - raw) + 2 * PfTab<F>::kStride);  // up values for SwiGLU
   const uint32_t bar0 = smem_u32(s_bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };                 // A decoded
   auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };    // stage consumed
   auto load_bar = [&](int s) { return bar0 + 8u * (2 * kStages + s); }; // B and indices landed
   auto acc_full = [&](int b) { return bar0 + 8u * (3 * kStages + b); }; // accumulator b complete
   auto acc_empty = [&](int b) { return bar0 + 8u * (3 * kStages + 2 + b); };  // accumulator b drained
-  auto a_tile = [&](int s) { return base + (uint32_t)(s * PfSmem<N>::kStageBytes); };
-  auto b_tile = [&](int s) { return base + (uint32_t)(s * PfSmem<N>::kStageBytes + kATile); };
-  auto i_tile = [&](int s) { return base + (uint32_t)(s * PfSmem<N>::kStageBytes + kATile + PfSmem<N>::kBTile); };
+  auto a_tile = [&](int s) { return base + (uint32_t)(s * PS::kStageBytes); };
+  auto b_tile = [&](int s) { return base + (uint32_t)(s * PS::kStageBytes + kATile); };
+  auto i_tile = [&](int s) { return base + (uint32_t)(s * PS::kStageBytes + kATile + PS::kBTile); };
 
   const int n_kg = a.d_in / 64;
   const int n_tiles = (a.rows + N - 1) / N;  // row tiles
   const long long s0 = range_begin(blockIdx.x, a.work, gridDim.x);
   const long long s1 = range_begin(blockIdx.x + 1, a.work, gridDim.x);
 
-  // codebook tables (lane-private copies): matrix 0 at tabs, matrix 1 at tabs + 8192
-  for (int i = tid; i < 2 * 64 * 8; i += kPThreads) {
-    const int t2 = i / 512, k = (i >> 3) & 63, q = i & 7;
+  // codebook tables (lane-private copies): matrix 0 at tabs, matrix 1 one stride on; a
+  // vector entry is (component 0 | component 1 << 16), a scalar one (entry | entry << 16)
+  constexpr int E = Fmt<F>::kEntries;
+  for (int i = tid; i < 2 * E * 8; i += kPThreads) {
+    const int t2 = i / (E * 8), k = (i >> 3) % E, q = i & 7;
     const uint32_t* cb = t2 ? a.cb1 : a.cb0;
     if (cb) {
-      const uint32_t v = __ldg(cb + k);
-      asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(tabs + (uint32_t)(t2 * 8192 + k * 128 + q * 16)),
+      uint32_t v;
+      if constexpr (Fmt<F>::kVec == 2) {
+        v = __ldg(cb + k);
+      } else {
+        const uint32_t h = __ldg(reinterpret_cast<const uint16_t*>(cb) + k);
+        v = h | (h << 16);
+      }
+      asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
+                       tabs + (uint32_t)(t2 * PfTab<F>::kStride + k * 128 + q * 16)),
                    "r"(v)
                    : "memory");
     }
@@ -359,7 +394,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ tile copies
     if (lane == 0) {
-      constexpr uint32_t kTx = (uint32_t)(PfSmem<N>::kBTile + kIdxBytes);
+      constexpr uint32_t kTx = (uint32_t)(PS::kBTile + PS::kIdxBytes);
+      constexpr int kSuU4 = FmtSizes<F>::kSuUint4;
+      constexpr uint32_t kSuB = (uint32_t)PS::kSu;
       int it = 0;
       for (long long s = s0; s < s1;) {
         const Seg g = seg_at(s, s1, n_kg);
@@ -368,8 +405,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
         // last channel when d_out is an odd multiple of 64 (its A rows are never stored)
         const int mg0 = a.swiglu ? mt : 2 * mt, mg1 = a.swiglu ? mt : 2 * mt + 1;
         const bool live1 = a.swiglu || mg1 < a.d_out / 64;
-        const uint4* su0 = a.packed0 + (size_t)mg0 * n_kg * kSuUint4;
-        const uint4* su1 = (a.swiglu ? a.packed1 : a.packed0) + (size_t)(live1 ? mg1 : mg0) * n_kg * kSuUint4;
+        const uint4* su0 = a.packed0 + (size_t)mg0 * n_kg * kSuU4;
+        const uint4* su1 = (a.swiglu ? a.packed1 : a.packed0) + (size_t)(live1 ? mg1 : mg0) * n_kg * kSuU4;
         for (int kk = g.k0; kk < g.k1; ++kk, ++it) {
           const int st = it % kStages;
           if (it >= kStages) mbar_wait(empty_bar(st), (uint32_t)((it / kStages - 1) & 1), a.status);
@@ -377,12 +414,12 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
           // activation tile: N rows x 64 inputs in the 128-byte swizzle layout (rows
           // past the last are filled with zeros)
           if (kk + kPrefetchSteps < g.k1) {
-            prefetch_l2(su0 + (size_t)(kk + kPrefetchSteps) * kSuUint4, kSuBytes);
-            prefetch_l2(su1 + (size_t)(kk + kPrefetchSteps) * kSuUint4, kSuBytes);
+            prefetch_l2(su0 + (size_t)(kk + kPrefetchSteps) * kSuU4, kSuB);
+            prefetch_l2(su1 + (size_t)(kk + kPrefetchSteps) * kSuU4, kSuB);
           }
           tma_load_2d(b_tile(st), &xmap, kk * 64, row0, load_bar(st));
-          bulk_load(i_tile(st), su0 + (size_t)kk * kSuUint4, kSuBytes, load_bar(st));
-          bulk_load(i_tile(st) + kSuBytes, su1 + (size_t)kk * kSuUint4, kSuBytes, load_bar(st));
+          bulk_load(i_tile(st), su0 + (size_t)kk * kSuU4, kSuB, load_bar(st));
+          bulk_load(i_tile(st) + kSuB, su1 + (size_t)kk * kSuU4, kSuB, load_bar(st));
         }
         s += g.k1 - g.k0;
       }
@@ -394,7 +431,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
     const int dw = warp - kDecWarp0;
     const int su = dw / kDecPerSu, part = dw % kDecPerSu, L = lane;
     const int s_lo = part * kStepsPerDec, s_hi = s_lo + kStepsPerDec;  // input steps of this warp
-    const uint32_t lanebase = tabs | (uint32_t)(lane * 4) | ((a.swiglu && su == 1) ? 8192u : 0u);
+    const uint32_t lanebase = tabs | (uint32_t)(lane * 4) | ((a.swiglu && su == 1) ? PfTab<F>::kStride : 0u);
     int it = 0;
     for (long long s = s0; s < s1;) {
       const Seg g = seg_at(s, s1, n_kg);
@@ -405,13 +442,14 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
         if (it >= kStages) mbar_wait(empty_bar(st), (uint32_t)((it / kStages - 1) & 1), a.status);
         mbar_wait(load_bar(st), (uint32_t)((it / kStages) & 1), a.status);
         if (live) {
-          // input steps [s_lo, s_hi) are bits [96 s_lo, 96 s_hi) of the string: words
-          // 3 s_lo .. 3 s_hi (the last for indices that straddle two words)
-          uint32_t w[12] = {};
-          const uint32_t is = i_tile(st) + (uint32_t)(su * kSuBytes);
+          // input steps [s_lo, s_hi) are words kW s_lo .. kW s_hi of the string (kW
+          // words per step; the last word for six-bit indices that straddle two)
+          constexpr int kW = Fmt<F>::kWords / 4;
+          uint32_t w[Fmt<F>::kWords] = {};
+          const uint32_t is = i_tile(st) + (uint32_t)(su * PS::kSu);
 #pragma unroll
-          for (int q = 0; q < 3; ++q) {
-            if (4 * q > 3 * s_hi || 4 * q + 3 < 3 * s_lo) continue;
+          for (int q = 0; q < FmtSizes<F>::kChunks; ++q) {
+            if (4 * q > kW * s_hi || 4 * q + 3 < kW * s_lo) continue;
             const uint32_t o = is + (uint32_t)((q * 32 + L) * 16);
             uint32_t v0, v1, v2, v3;
             asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3) : "r"(o));
@@ -420,7 +458,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
             w[4 * q + 2] = v2;
             w[4 * q + 3] = v3;
           }
-          decode_part(w, part, L, su * 64, a_tile(st), lanebase);
+          decode_part<F>(w, part, L, su * 64, a_tile(st), lanebase);
         }
         fence_proxy_async();  // the generic-proxy writes of A, before the MMA reads them
         mbar_arrive(full_bar(st));
@@ -622,10 +660,10 @@ cudaError_t activation_map(const PrefillArgs& a, int n, CUtensorMap* map) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int N>
+template <int N, int F>
 cudaError_t launch_n(PrefillArgs a, cudaStream_t st) {
-  const int smem = PfSmem<N>::kTotal;
-  cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const int smem = PfSmem<N, F>::kTotal;
+  cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel<N, F>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   alignas(64) CUtensorMap xmap;
   if ((e = activation_map(a, N, &xmap)) != cudaSuccess) return e;
@@ -641,7 +679,7 @@ cudaError_t launch_n(PrefillArgs a, cudaStream_t st) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, prefill_gemm_kernel<N>, a, xmap);
+  e = cudaLaunchKernelEx(&cfg, prefill_gemm_kernel<N, F>, a, xmap);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -673,11 +711,23 @@ size_t prefill_part_bytes(int rows) {
   return (size_t)prefill_max_grid() * kTileM * prefill_tile_rows(rows) * sizeof(float);
 }
 
-cudaError_t launch_prefill_gemm(const PrefillArgs& a, cudaStream_t st) {
+namespace {
+template <int F>
+cudaError_t launch_fmt(const PrefillArgs& a, cudaStream_t st) {
   switch (prefill_tile_rows(a.rows)) {
-    case 64: return launch_n<64>(a, st);
-    case 128: return launch_n<128>(a, st);
-    default: return launch_n<256>(a, st);
+    case 64: return launch_n<64, F>(a, st);
+    case 128: return launch_n<128, F>(a, st);
+    default: return launch_n<256, F>(a, st);
+  }
+}
+}  // namespace
+
+cudaError_t launch_prefill_gemm(const PrefillArgs& a, cudaStream_t st) {
+  switch (a.format) {
+    case VQ3_FORMAT_2X64: return launch_fmt<VQ3_FORMAT_2X64>(a, st);
+    case VQ3_FORMAT_2X16: return launch_fmt<VQ3_FORMAT_2X16>(a, st);
+    case VQ3_FORMAT_LUT4: return launch_fmt<VQ3_FORMAT_LUT4>(a, st);
+    default: return cudaErrorInvalidValue;
   }
 }
 

@@ -12,32 +12,72 @@ namespace vq3 {
 // ---------------------------------------------------------------------------
 // GPU index layout ("super-units").
 //
-// A super-unit (SU) covers 64 output channels (32 output pairs) x 64 input
-// columns: 2048 six-bit indices, 1536 bytes. SU (mg, kg) of a matrix starts at
-// byte (mg * (d_in/64) + kg) * 1536, so one output group's K range is
-// contiguous. Inside an SU, warp lane L (g = L/4, t = L%4) owns 64 indices
-// (384 bits = 12 words); its words 4q..4q+3 are the 16 bytes at SU offset
-// (q*32 + L)*16, q = 0..2, so each of the three 128-bit loads of a warp reads
-// 512 contiguous bytes. Lane index n (bits [6n, 6n+6) of the lane's 384-bit
-// string, least significant bit first) is
+// A super-unit (SU) covers 64 output channels x 64 input columns. SU (mg, kg)
+// of a matrix starts at byte (mg * (d_in/64) + kg) * SU bytes, so one output
+// group's K range is contiguous. Inside an SU, warp lane L (g = L/4, t = L%4)
+// owns a string of W 32-bit words (its indices, least significant bit first);
+// words 4q..4q+3 are the 16 bytes at SU offset (q*32 + L)*16, so each 128-bit
+// load of a warp reads 512 contiguous bytes. With index width b, index n of
+// the string sits at bits [b n, b n + b). For the vector formats (one index per
+// output pair) the lane holds 64 indices,
 //     n = (s*4 + m)*4 + e          s: k-step of 16 inputs, m: 16-channel tile
 //     pair  p = mg*32 + m*8 + g
 //     input i = kg*64 + s*16 + {2t, 2t+1, 2t+8, 2t+9}[e]
-// which is exactly what lane L needs for the A fragment of an m16n8k16 MMA
-// whose row g is channel 2p and row g+8 is channel 2p+1.
+// and for the scalar format (one index per weight) 128 indices,
+//     n = ((s*4 + m)*4 + e)*2 + c, channel 2p + c, p and i as above,
+// which is what lane L needs for the A fragment of an m16n8k16 MMA whose row g
+// is channel 2p and row g+8 is channel 2p+1.
+//   format  b  indices/lane  W   SU bytes
+//   2x64    6  64            12  1536
+//   2x16    4  64             8  1024
+//   lut4    4  128           16  2048
 // ---------------------------------------------------------------------------
 constexpr int kSuChannels = 64;
 constexpr int kSuInputs = 64;
-constexpr int kSuBytes = 1536;
+constexpr int kSuBytes = 1536;           // the three-bit format's SU
 constexpr int kSuUint4 = kSuBytes / 16;  // 96
+constexpr int kMaxSuBytes = 2048;
+
+template <int F>
+struct Fmt;
+template <>
+struct Fmt<VQ3_FORMAT_2X64> {
+  static constexpr int kBits = 6, kVec = 2, kEntries = 64, kWords = 12;
+};
+template <>
+struct Fmt<VQ3_FORMAT_2X16> {
+  static constexpr int kBits = 4, kVec = 2, kEntries = 16, kWords = 8;
+};
+template <>
+struct Fmt<VQ3_FORMAT_LUT4> {
+  static constexpr int kBits = 4, kVec = 1, kEntries = 16, kWords = 16;
+};
+// Derived sizes: 16-byte chunks per lane string, SU bytes and uint4s, indices per lane string.
+template <int F>
+struct FmtSizes {
+  static constexpr int kChunks = Fmt<F>::kWords / 4;
+  static constexpr int kSuBytes = kChunks * 512;
+  static constexpr int kSuUint4 = kSuBytes / 16;
+  static constexpr int kIndices = 128 / Fmt<F>::kVec;
+};
+
+inline bool format_supported(int f) { return f == VQ3_FORMAT_2X64 || f == VQ3_FORMAT_2X16 || f == VQ3_FORMAT_LUT4; }
+inline int format_bits(int f) { return f == VQ3_FORMAT_2X64 ? 6 : 4; }
+inline int format_vec(int f) { return f == VQ3_FORMAT_LUT4 ? 1 : 2; }
+inline int format_words(int f) { return f == VQ3_FORMAT_2X64 ? 12 : (f == VQ3_FORMAT_2X16 ? 8 : 16); }
+inline int format_su_bytes(int f) { return format_words(f) / 4 * 512; }
 
 inline bool layout_supported(int d_in, int d_out) {
   return d_in > 0 && d_out > 0 && d_in % kSuInputs == 0 && d_out % kSuChannels == 0;
 }
 
-// Byte offset of 32-bit word w (0..11) of lane L's string in SU su.
+// Byte offset of 32-bit word w of lane L's string in SU su (three-bit format).
 __host__ __device__ inline size_t lane_word_offset(size_t su, int lane, int w) {
   return su * kSuBytes + (size_t)((w / 4) * 32 + lane) * 16 + (size_t)(w % 4) * 4;
+}
+// The same for an SU of su_bytes bytes.
+__host__ __device__ inline size_t lane_word_offset(size_t su, int lane, int w, int su_bytes) {
+  return su * su_bytes + (size_t)((w / 4) * 32 + lane) * 16 + (size_t)(w % 4) * 4;
 }
 
 // ---------------------------------------------------------------------------
@@ -46,7 +86,7 @@ __host__ __device__ inline size_t lane_word_offset(size_t su, int lane, int w) {
 
 struct DecMat {
   const uint4* packed;
-  const uint32_t* codebook;  // [64] FP16x2 words (component 0 in the low half)
+  const uint32_t* codebook;  // [entries] FP16x2 words (component 0 in the low half); [16] FP16 for lut4
   const uint16_t* scales;    // [d_out]
 };
 
@@ -63,6 +103,7 @@ struct PersistArgs {
   const uint16_t* x;        // row-major [*][d_model]
   int row0, rows;           // rows of this pass: [row0, row0 + rows), rows <= 8 * NT
   int mlp;                  // 1: MLP block (gate, up, down); 0: one linear layer (gate)
+  int format;               // VQ3_FORMAT_* of every matrix
   int d_model, d_inter;     // MLP: hidden and intermediate widths; linear: d_model = d_in
   int d_model_out;          // linear: d_out
   int block_in, block_dn;   // rotation blocks of the gate/up (or linear) input and of the down input
@@ -103,6 +144,7 @@ struct PrefillArgs {
   const uint16_t* x;       // rotated activations, FP16 [rows][d_in], 16-byte aligned
   int rows, d_in, d_out;   // d_out: output channels (swiglu: the intermediate width)
   int swiglu;
+  int format;              // VQ3_FORMAT_* of W0 (and W1)
   const uint4* packed0;    // GPU-layout indices of W0 (and W1)
   const uint4* packed1;
   const uint32_t* cb0;     // codebooks

@@ -30,7 +30,11 @@ class Vq3Error(RuntimeError):
 
 class vq3_linear(ctypes.Structure):
     _fields_ = [("d_in", c_int), ("d_out", c_int), ("block", c_int), ("packed", c_void_p),
-                ("codebook", c_void_p), ("scales", c_void_p), ("signs", c_void_p)]
+                ("codebook", c_void_p), ("scales", c_void_p), ("signs", c_void_p), ("format", c_int)]
+
+
+# index formats (VQ3_FORMAT_* in vq3.h): name -> (code, index bits, output channels per index)
+FORMATS = {"2x64": (0, 6, 2), "2x16": (1, 4, 2), "lut4": (2, 4, 1)}
 
 
 class vq3_mlp_layer(ctypes.Structure):
@@ -45,6 +49,9 @@ def _load() -> ctypes.CDLL:
         "vq3_packed_bytes": (c_size_t, [c_int, c_int]),
         "vq3_pack_layout": (c_int, [POINTER(c_uint8), c_int, c_int, c_void_p]),
         "vq3_unpack_layout": (c_int, [c_void_p, c_int, c_int, POINTER(c_uint8)]),
+        "vq3_packed_bytes_fmt": (c_size_t, [c_int, c_int, c_int]),
+        "vq3_pack_layout_fmt": (c_int, [c_int, POINTER(c_uint8), c_int, c_int, c_void_p]),
+        "vq3_unpack_layout_fmt": (c_int, [c_int, c_void_p, c_int, c_int, POINTER(c_uint8)]),
         "fwht_rotate": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]),
         "vq3_linear_workspace_bytes": (c_size_t, [c_int, POINTER(vq3_linear)]),
         "vq3_mlp_workspace_bytes": (c_size_t, [c_int, POINTER(vq3_mlp_layer)]),
@@ -94,23 +101,26 @@ def version() -> str:
 
 # ---------------------------------------------------------------- layout (host)
 
-def packed_bytes(d_in: int, d_out: int) -> int:
-    return int(lib.vq3_packed_bytes(d_in, d_out))
+def packed_bytes(d_in: int, d_out: int, fmt: str = "2x64") -> int:
+    return int(lib.vq3_packed_bytes_fmt(FORMATS[fmt][0], d_in, d_out))
 
 
-def pack_layout(canonical: np.ndarray, d_in: int, d_out: int) -> np.ndarray:
-    """Canonical 6-bit little-endian stream -> GPU layout (host bytes)."""
+def pack_layout(canonical: np.ndarray, d_in: int, d_out: int, fmt: str = "2x64") -> np.ndarray:
+    """Canonical little-endian index stream -> GPU layout (host bytes)."""
     src = np.ascontiguousarray(canonical, dtype=np.uint8)
-    dst = np.empty(max(packed_bytes(d_in, d_out), 1), dtype=np.uint8)
-    _check(lib.vq3_pack_layout(src.ctypes.data_as(POINTER(c_uint8)), d_in, d_out, dst.ctypes.data_as(c_void_p)))
+    dst = np.empty(max(packed_bytes(d_in, d_out, fmt), 1), dtype=np.uint8)
+    _check(lib.vq3_pack_layout_fmt(FORMATS[fmt][0], src.ctypes.data_as(POINTER(c_uint8)), d_in, d_out,
+                                   dst.ctypes.data_as(c_void_p)))
     return dst
 
 
-def unpack_layout(packed: np.ndarray, d_in: int, d_out: int) -> np.ndarray:
+def unpack_layout(packed: np.ndarray, d_in: int, d_out: int, fmt: str = "2x64") -> np.ndarray:
+    code, nb, vec = FORMATS[fmt]
     src = np.ascontiguousarray(packed, dtype=np.uint8)
-    n = (6 * (d_out // 2) * d_in + 7) // 8
+    n = (nb * (d_out // vec) * d_in + 7) // 8
     dst = np.empty(n, dtype=np.uint8)
-    _check(lib.vq3_unpack_layout(src.ctypes.data_as(c_void_p), d_in, d_out, dst.ctypes.data_as(POINTER(c_uint8))))
+    _check(lib.vq3_unpack_layout_fmt(code, src.ctypes.data_as(c_void_p), d_in, d_out,
+                                     dst.ctypes.data_as(POINTER(c_uint8))))
     return dst
 
 
@@ -120,26 +130,28 @@ class Linear:
     """One VQ3 matrix resident on the GPU (packed indices, codebook, scales, signs)."""
 
     def __init__(self, d_in, d_out, block, packed: torch.Tensor, codebook: torch.Tensor, scales: torch.Tensor,
-                 signs: torch.Tensor | None = None):
-        self.d_in, self.d_out, self.block = int(d_in), int(d_out), int(block)
+                 signs: torch.Tensor | None = None, fmt: str = "2x64"):
+        self.d_in, self.d_out, self.block, self.fmt = int(d_in), int(d_out), int(block), fmt
         self.packed, self.codebook, self.scales, self.signs = packed, codebook, scales, signs
         self.struct = vq3_linear(self.d_in, self.d_out, self.block, _ptr(packed), _ptr(codebook), _ptr(scales),
-                                 _ptr(signs))
+                                 _ptr(signs), FORMATS[fmt][0])
 
     @classmethod
-    def from_canonical(cls, d_in, d_out, block, stream, codebook, scales, signs=None, device="cuda"):
-        packed = torch.from_numpy(pack_layout(stream, d_in, d_out)).to(device)
-        cb = torch.from_numpy(np.ascontiguousarray(codebook, dtype=np.float16)).to(device)
+    def from_canonical(cls, d_in, d_out, block, stream, codebook, scales, signs=None, device="cuda",
+                       fmt: str = "2x64"):
+        packed = torch.from_numpy(pack_layout(stream, d_in, d_out, fmt)).to(device)
+        cb = torch.from_numpy(np.ascontiguousarray(codebook, dtype=np.float16).reshape(-1)).to(device)
         sc = torch.from_numpy(np.ascontiguousarray(scales, dtype=np.float16)).to(device)
         sg = None
         if signs is not None:
             sg = torch.from_numpy(np.ascontiguousarray(signs, dtype=np.uint32).view(np.int32)).to(device)
-        return cls(d_in, d_out, block, packed, cb, sc, sg)
+        return cls(d_in, d_out, block, packed, cb, sc, sg, fmt)
 
     @classmethod
     def from_matrix(cls, m, device="cuda"):
-        """From any object with d_in, d_out, block, stream, codebook, scales, signs fields."""
-        return cls.from_canonical(m.d_in, m.d_out, m.block, m.stream, m.codebook, m.scales, m.signs, device)
+        """From any object with d_in, d_out, block, stream, codebook, scales, signs (and fmt) fields."""
+        return cls.from_canonical(m.d_in, m.d_out, m.block, m.stream, m.codebook, m.scales, m.signs, device,
+                                  getattr(m, "fmt", "2x64") or "2x64")
 
 
 class MLP:
@@ -154,7 +166,7 @@ class MLP:
         gate = Linear.from_matrix(blk.gate, device)
         if blk.up.signs is not None and blk.gate.signs is not None and np.array_equal(blk.up.signs, blk.gate.signs):
             up = Linear.from_canonical(blk.up.d_in, blk.up.d_out, blk.up.block, blk.up.stream, blk.up.codebook,
-                                       blk.up.scales, None, device)
+                                       blk.up.scales, None, device, getattr(blk.up, "fmt", "2x64") or "2x64")
             up.signs = gate.signs
             up.struct.signs = gate.struct.signs
         else:

@@ -62,14 +62,36 @@ extern "C" {
 #define VQ3_MAX_BLOCK 1024
 
 /*
+ * Index formats (vq3_linear.format). Cited: model card
+ * "anemll/anemll-forge-qwen3.8-27B", "Release 0.2" bullet "Three bits per MLP
+ * weight" (2x64) and the release-comparison table rows "MLP gate / up / down"
+ * and "Token mixers" (the previous release's two-bit vector LUT, 2x16, and
+ * four-bit LUT). Every format has per-output-channel FP16 scales.
+ *   VQ3_FORMAT_2X64: 64 two-component FP16 centroids, one 6-bit index per
+ *                    output pair and input (3 bits per weight).
+ *   VQ3_FORMAT_2X16: 16 two-component FP16 centroids, one 4-bit index per
+ *                    output pair and input (2 bits per weight).
+ *   VQ3_FORMAT_LUT4: 16 scalar FP16 entries, one 4-bit index per weight
+ *                    (4 bits per weight).
+ * Canonical stream of a format with index width b and v output channels per
+ * index: index k = p*d_in + i (output group p = channels v*p .. v*p+v-1, input
+ * column i) occupies stream bits [b*k, b*k + b), stream bit j being bit (j mod 8)
+ * of byte j/8 (least significant bit first); ceil(b*(d_out/v)*d_in/8) bytes.
+ */
+#define VQ3_FORMAT_2X64 0
+#define VQ3_FORMAT_2X16 1
+#define VQ3_FORMAT_LUT4 2
+
+/*
  * One VQ3 matrix, d_out x d_in. Cited: model card "anemll/anemll-forge-qwen3.8-27B",
- * "Release 0.2" bullet "Three bits per MLP weight".
+ * "Release 0.2" bullet "Three bits per MLP weight" (and the formats above).
  *   d_in  : input width; a multiple of 64 and of `block`.
  *   d_out : output width; a multiple of 64 (so output channels pair up).
  *   block : Hadamard block of the input rotation, a power of two in [2, 1024].
- *   packed: device, 16-byte aligned, vq3_packed_bytes(d_in, d_out) bytes in the
- *           GPU layout written by vq3_pack_layout.
- *   codebook: device, [64][2] FP16 centroids (component 0 = even channel).
+ *   packed: device, 16-byte aligned, vq3_packed_bytes_fmt(format, d_in, d_out)
+ *           bytes in the GPU layout written by vq3_pack_layout_fmt.
+ *   codebook: device, FP16 centroids: [64][2] (2X64), [16][2] (2X16; component
+ *           0 = even channel of the pair) or [16] (LUT4); 4-byte aligned.
  *   scales: device, [d_out] FP16 per-output-channel scales.
  *   signs : device, bit-packed seeded signs over d_in (bit j of word j/32 set
  *           => input j is negated before the Hadamard block), or NULL for all +1.
@@ -82,11 +104,12 @@ typedef struct vq3_linear {
   const uint16_t* codebook;
   const uint16_t* scales;
   const uint32_t* signs;
+  int format;  // VQ3_FORMAT_*; 0 (the three-bit format) in a zero-initialised descriptor
 } vq3_linear;
 
 /* One SwiGLU block. gate and up read the same rotated input (same d_in, block
  * and signs); down maps the intermediate width back: down.d_in == gate.d_out,
- * down.d_out == gate.d_in. */
+ * down.d_out == gate.d_in. The three matrices share one index format. */
 typedef struct vq3_mlp_layer {
   vq3_linear gate;
   vq3_linear up;
@@ -111,6 +134,14 @@ VQ3_API int vq3_pack_layout(const uint8_t* canonical, int d_in, int d_out, void*
 /* Host-side inverse of vq3_pack_layout (pad bits of the canonical stream are
  * written as zero). Same errors. */
 VQ3_API int vq3_unpack_layout(const void* packed_host, int d_in, int d_out, uint8_t* canonical);
+
+/* The same three calls for any index format (VQ3_FORMAT_*): the GPU layout is
+ * built from super-units of 64 output channels x 64 inputs (1536, 1024 or 2048
+ * bytes), the same size as the canonical stream. An unknown format gives 0 /
+ * VQ3_EUNSUPPORTED. */
+VQ3_API size_t vq3_packed_bytes_fmt(int format, int d_in, int d_out);
+VQ3_API int vq3_pack_layout_fmt(int format, const uint8_t* canonical, int d_in, int d_out, void* dst_host);
+VQ3_API int vq3_unpack_layout_fmt(int format, const void* packed_host, int d_in, int d_out, uint8_t* canonical);
 
 /*
  * Blocked, normalised fast Walsh-Hadamard transform of each row:

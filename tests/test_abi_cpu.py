@@ -139,3 +139,48 @@ def test_fwht_argument_checks():
     assert lib.fwht_rotate(0x40002, 2, 1024, 1024, None, 0x50000, None) == -2
     assert lib.vq3_residual_rmsnorm(0x40000, None, 0, 64, 1e-6, 0x50000, None) == 0
     assert lib.vq3_residual_rmsnorm(0x40000, None, 2, 64, -1.0, 0x50000, None) == -1
+
+
+# ---------------------------------------------------------------- other index formats
+
+@pytest.mark.parametrize("fmt", ["2x16", "lut4"])
+@pytest.mark.parametrize("d_in,d_out", [(64, 64), (256, 256), (128, 512), (5120, 256)])
+def test_pack_roundtrip_formats(fmt, d_in, d_out):
+    s = S.index_stream(S.rng(d_in + d_out + 7), d_in, d_out, fmt)
+    p = vq3.pack_layout(s, d_in, d_out, fmt)
+    assert p.size == vq3.packed_bytes(d_in, d_out, fmt) == s.size
+    assert np.array_equal(vq3.unpack_layout(p, d_in, d_out, fmt), s)
+
+
+@pytest.mark.parametrize("fmt", ["2x16", "lut4"])
+def test_layout_formats_are_permutations_of_index_fields(fmt):
+    # a single nonzero four-bit index (0b1011: three set bits) moves to exactly one field
+    _, nb, vec = vq3.FORMATS[fmt]
+    d_in, d_out = 128, 128
+    for (g_, i_) in [(0, 0), (5, 9), (d_out // vec - 1, 127), (17, 40)]:
+        idx = np.zeros((d_out // vec, d_in), int)
+        idx[g_, i_] = 0b1011
+        pk = vq3.pack_layout(O.pack_indices(idx, nb), d_in, d_out, fmt)
+        assert np.unpackbits(pk, bitorder="little").sum() == 3
+        assert np.array_equal(O.index_matrix(vq3.unpack_layout(pk, d_in, d_out, fmt), d_in, d_out, fmt=fmt), idx)
+
+
+def test_format_checks():
+    lib = vq3.lib
+    assert vq3.packed_bytes(5120, 17408, "2x16") == 5120 * 17408 * 2 // 8
+    assert vq3.packed_bytes(5120, 17408, "lut4") == 5120 * 17408 * 4 // 8
+    assert lib.vq3_packed_bytes_fmt(7, 256, 256) == 0
+    dst = np.zeros(1024, np.uint8)
+    src = np.zeros(1024, np.uint8)
+    rc = lib.vq3_pack_layout_fmt(7, src.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)), 64, 64,
+                                 dst.ctypes.data_as(ctypes.c_void_p))
+    assert rc == -3
+    bad = fake_linear()
+    bad.format = 7
+    assert lib.vq3_linear_forward(0x40000, 8, ctypes.byref(bad), 0x50000, 0x60000, 1 << 24, None) == -3
+    g = fake_linear(256, 512, 256)
+    u = fake_linear(256, 512, 256)
+    d = fake_linear(512, 256, 256)
+    d.format = 1
+    mixed = vq3.vq3_mlp_layer(g, u, d)
+    assert lib.vq3_mlp_forward(0x40000, 8, ctypes.byref(mixed), 0x50000, 0x60000, 1 << 24, None) == -1
