@@ -298,10 +298,11 @@ def _run_ours_on(args, torch, vq3, dev, stream, rows, sets, x_host, x, out, ws, 
            "h2d_bytes_per_step": int(x_host.nbytes), "d2h_bytes_per_step": int(rows * HIDDEN * 2),
            "api": "vq3_mlp_forward_host (pageable->pinned host buffers)"}
 
-    extra, stack = {}, {}
+    extra, stack, fmts = {}, {}, {}
     if not args.quick and rank == 0:
         extra = prefill_sweep(vq3, dev, stream, pk)
         stack = stack64(vq3, dev, stream, pk)
+        fmts = format_lines(vq3, dev, stream, pk, l2)
 
     launches = vq3.mlp_kernel_launches(rows, sets[0]) * steps
     line = None
@@ -320,6 +321,8 @@ def _run_ours_on(args, torch, vq3, dev, stream, rows, sets, x_host, x, out, ws, 
             line["prefill_sweep"] = extra
         if stack:
             line["stack64"] = stack
+        if fmts:
+            line["formats"] = fmts
         if world == 1 and not args.no_cpu_baseline:
             rate, dt, smp = time_oracle(rows, 1.0 / args.oracle_frac, args.oracle_steps, 1)
             line["cpu_baseline"] = {"value": round(rate, 3), "unit": "rows/s", "cores": cpu_cores(),
@@ -332,6 +335,66 @@ def _run_ours_on(args, torch, vq3, dev, stream, rows, sets, x_host, x, out, ws, 
         import torch.distributed as dist
         dist.destroy_process_group()
     return line
+
+
+def format_bytes(fmt: str) -> int:
+    """Algorithmic bytes of one block in another index format: packed indices, scales, codebooks."""
+    _, vec, entries = S.FORMATS[fmt]
+    return (3 * S.stream_bytes(HIDDEN, INTER, fmt) + 2 * (2 * INTER + HIDDEN) + 3 * entries * vec * 2)
+
+
+def format_lines(vq3, dev, stream, pk, l2) -> dict:
+    """The block in the previous release's formats (two-bit vector LUT, four-bit scalar LUT): T = 8
+    through a CUDA graph cycling weight sets that together exceed 4x L2 (weight GB/s against the HBM
+    copy peak), and the 2048-row prefill (TFLOP/s)."""
+    import torch
+    res = {}
+    for fmt in ("2x16", "lut4"):
+        nbytes = format_bytes(fmt)
+        n_sets = max(2, math.ceil(4 * l2 / nbytes))
+        sets = [vq3.MLP.from_block(S.mlp_block(S.rng(S.FORMAT_SEEDS[fmt] + 1000 * k, 1), HIDDEN, INTER, 1024, fmt),
+                                   dev) for k in range(n_sets)]
+        x = torch.from_numpy(S.activations(S.rng(S.FORMAT_SEEDS[fmt], 0), 8, HIDDEN)).to(dev)
+        out = torch.empty_like(x)
+        ws = vq3.workspace(vq3.mlp_workspace_bytes(8, sets[0]), dev, stream)
+        for i in range(n_sets):
+            vq3.mlp_forward(x, sets[i], out=out, ws=ws, stream=stream)
+        gph = torch.cuda.CUDAGraph()
+        reps = 20 * n_sets
+        with torch.cuda.graph(gph, stream=stream):
+            for i in range(reps):
+                vq3.mlp_forward(x, sets[i % n_sets], out=out, ws=ws, stream=stream)
+        gph.replay()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(3):
+            gph.replay()
+        b.record(stream)
+        b.synchronize()
+        ms8 = a.elapsed_time(b) / (3 * reps)
+        gbs = nbytes / (ms8 / 1e3) / 1e9
+        rows = 2048
+        xp = torch.from_numpy(S.activations(S.rng(S.FORMAT_SEEDS[fmt], 0), rows, HIDDEN)).to(dev)
+        outp = torch.empty_like(xp)
+        wsp = vq3.workspace(vq3.mlp_workspace_bytes(rows, sets[0]), dev, stream)
+        for _ in range(2):
+            vq3.mlp_forward(xp, sets[0], out=outp, ws=wsp, stream=stream)
+        a.record(stream)
+        for _ in range(3):
+            vq3.mlp_forward(xp, sets[0], out=outp, ws=wsp, stream=stream)
+        b.record(stream)
+        b.synchronize()
+        msp = a.elapsed_time(b) / 3
+        tf = FLOP_PER_ROW * rows / (msp / 1e3) / 1e12
+        res[fmt] = {"bits_per_weight": S.FORMATS[fmt][0] // S.FORMATS[fmt][1],
+                    "algorithmic_bytes": nbytes, "T8_us": round(ms8 * 1e3, 2), "T8_rows_per_s": round(8 / (ms8 / 1e3), 1),
+                    "T8_weight_gbs": round(gbs, 1), "T8_frac_of_hbm": round(gbs / pk["hbm_gbs"], 4),
+                    "T2048_ms": round(msp, 4), "T2048_tflops": round(tf, 2),
+                    "T2048_frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4),
+                    "status": vq3.workspace_status(ws) | vq3.workspace_status(wsp)}
+    return res
 
 
 def prefill_sweep(vq3, dev, stream, pk) -> dict:
