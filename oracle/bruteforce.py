@@ -58,7 +58,14 @@ def weight(m, o: int, i: int) -> float:
     p, c = divmod(o, vec)
     k = index_at(m.stream, p * m.d_in + i, bits)
     entry = m.codebook[k]
-    return float(m.scales[o]) * float(entry[c] if vec > 1 else (entry[0] if hasattr(entry, "__len__") else entry))
+    w = float(m.scales[o]) * float(entry[c] if vec > 1 else (entry[0] if hasattr(entry, "__len__") else entry))
+    U = getattr(m, "lr_u", None)
+    V = getattr(m, "lr_v", None)
+    if U is not None and V is not None:
+        # low-rank correction: + sum_j U[o][j] V[j][i]
+        for j in range(len(V)):
+            w += float(U[o][j]) * float(V[j][i])
+    return w
 
 
 def linear_row(x, m):

@@ -25,6 +25,12 @@ Sources (page title, then section):
           four-bit LUT) and "ANEMLL ANE LLM conversion pipeline", "Facts" (the
           previous target mixes 2-bit vector LUTs and 4-bit scalar LUTs).
 
+Low-rank correction ([R01] row "Token mixers": rank-64 factors; "ANEMLL ANE
+LLM conversion pipeline", "Facts": rank-64 residual correction): a matrix may
+carry FP16 factors U [d_out, r] and V [r, d_in]; its weight is then
+diag(s) C[idx] + U V, the factors acting on the same rotated input as the
+lookup-table part and the scales on the lookup-table part only.
+
 Index formats (FORMATS): "2x64" is the release's three-bit format (64
 two-component centroids, a six-bit index per output pair); "2x16" the two-bit
 vector format (16 two-component centroids, a four-bit index per output pair);
@@ -214,8 +220,19 @@ def _as_f16_f64(a) -> np.ndarray:
     return np.asarray(a, dtype=np.float16).astype(np.float64)
 
 
+def lowrank_f64(xr, m) -> np.ndarray | None:
+    """U (V x') for the rotated rows xr of a matrix with low-rank factors, else None."""
+    U = getattr(m, "lr_u", None)
+    V = getattr(m, "lr_v", None)
+    if U is None or V is None:
+        return None
+    z = np.asarray(xr, np.float64) @ _as_f16_f64(V).T
+    return z @ _as_f16_f64(U).T
+
+
 def linear_f64(x, m, round_rotated: bool = False, row_chunk: int = 2048) -> np.ndarray:
-    """y = W (R x) in float64 for one VQ3 matrix `m` (fields as in synth.inputs.Matrix).
+    """y = W (R x) in float64 for one VQ3 matrix `m` (fields as in synth.inputs.Matrix),
+    plus U (V R x) when the matrix carries low-rank factors.
 
     x is taken at its own precision (FP16 inputs convert exactly); nothing is rounded.
     """
@@ -227,6 +244,9 @@ def linear_f64(x, m, round_rotated: bool = False, row_chunk: int = 2048) -> np.n
         r1 = min(m.d_out, r0 + row_chunk)
         W = dense_weight(m.stream, m.codebook, m.scales, m.d_in, m.d_out, rows=(r0, r1), fmt=fmt_of(m))
         y[:, r0:r1] = xr @ W.T
+    lr = lowrank_f64(xr, m)
+    if lr is not None:
+        y += lr
     return y
 
 

@@ -101,6 +101,8 @@ class Matrix:
     scales: np.ndarray    # [d_out] float16
     signs: np.ndarray | None = None  # bit-packed uint32 over d_in, or None (all +1)
     fmt: str = "2x64"     # index format (FORMATS)
+    lr_u: np.ndarray | None = None  # low-rank factor U [d_out, r] float16, or None
+    lr_v: np.ndarray | None = None  # low-rank factor V [r, d_in] float16
 
 
 @dataclass
@@ -130,6 +132,14 @@ def mlp_block(g: np.random.Generator, hidden: int, inter: int, block: int, fmt: 
     up = matrix(g, hidden, inter, block, fmt)
     down = matrix(g, inter, hidden, block, fmt)
     return Block(gate, up, down)
+
+
+def add_lowrank(g: np.random.Generator, m: Matrix, rank: int = 64, std: float = 0.01) -> Matrix:
+    """Seeded FP16 low-rank factors U [d_out, rank], V [rank, d_in] ~N(0, std) (drawn U then V;
+    callers pass a stream of its own, [seed, 3], so the other inputs do not move)."""
+    m.lr_u = (g.standard_normal((m.d_out, rank)) * std).astype(np.float16)
+    m.lr_v = (g.standard_normal((rank, m.d_in)) * std).astype(np.float16)
+    return m
 
 
 def add_signs(g: np.random.Generator, blk: Block) -> Block:
