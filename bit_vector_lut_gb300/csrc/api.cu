@@ -48,6 +48,11 @@ int check_linear(const vq3_linear* L, const char* name) {
   if (!pow2_block(L->block)) return fail(VQ3_EINVAL, "%s: block=%d must be a power of two in [2, 1024]", name, L->block);
   if (L->d_in % L->block) return fail(VQ3_EINVAL, "%s: d_in=%d is not a multiple of block=%d", name, L->d_in, L->block);
   if (!format_supported(L->format)) return fail(VQ3_EUNSUPPORTED, "%s: unknown index format %d", name, L->format);
+  if (L->lr_rank < 0 || L->lr_rank > 64 || L->lr_rank % 8)
+    return fail(VQ3_EUNSUPPORTED, "%s: lr_rank=%d must be 0 or a multiple of 8 up to 64", name, L->lr_rank);
+  if (L->lr_rank && (!L->lr_u || !L->lr_v)) return fail(VQ3_EINVAL, "%s: null low-rank factors", name);
+  if (L->lr_rank && (!aligned(L->lr_u, 16) || !aligned(L->lr_v, 16)))
+    return fail(VQ3_EALIGN, "%s: low-rank factors must be 16-byte aligned", name);
   if (!L->packed || !L->codebook || !L->scales) return fail(VQ3_EINVAL, "%s: null packed/codebook/scales", name);
   if (!aligned(L->packed, 16)) return fail(VQ3_EALIGN, "%s: packed indices not 16-byte aligned", name);
   if (!aligned(L->codebook, 4) || !aligned(L->scales, 4) || (L->signs && !aligned(L->signs, 4)))
@@ -111,18 +116,25 @@ size_t ctl_bytes(int n_words) {
 size_t mlp_ctl_bytes(int H, int I) { return ctl_bytes(ctl_mlp(H, I).n); }
 size_t linear_ctl_bytes(int d_in, int d_out) { return ctl_bytes(ctl_linear(d_in, d_out).n); }
 
-// [status word][counter words][pieces]
+// [status word][counter words][pieces]([x' FP16 [rows][d_in]][z FP32 [rows][rank]] with
+// low-rank factors)
 struct LinearWs {
-  size_t status, counters, pieces, total;
+  size_t status, counters, pieces, xr, z, total;
 };
 
-LinearWs linear_ws(int rows, int d_in, int d_out) {
+LinearWs linear_ws(int rows, int d_in, int d_out, int rank) {
   LinearWs w{};
   w.status = 0;
   w.counters = kCtlOffset;
   size_t off = kCtlOffset + linear_ctl_bytes(d_in, d_out);
   w.pieces = off;
   off = round_up(off + persist_pieces_bytes(rows, d_in, d_out, 1), 256);
+  w.xr = w.z = off;
+  if (rank) {
+    off = round_up(off + (size_t)rows * d_in * 2, 256);
+    w.z = off;
+    off = round_up(off + (size_t)rows * rank * sizeof(float), 256);
+  }
   w.total = off;
   return w;
 }
@@ -157,6 +169,8 @@ int check_mlp(const vq3_mlp_layer* l) {
   if (l->up.d_in != l->gate.d_in || l->up.d_out != l->gate.d_out || l->up.block != l->gate.block ||
       l->up.signs != l->gate.signs)
     return fail(VQ3_EINVAL, "mlp: gate and up must share d_in, d_out, block and signs");
+  if (l->gate.lr_rank || l->up.lr_rank || l->down.lr_rank)
+    return fail(VQ3_EUNSUPPORTED, "mlp: low-rank factors are supported on single linear layers only");
   if (l->up.format != l->gate.format || l->down.format != l->gate.format)
     return fail(VQ3_EINVAL, "mlp: gate, up and down must share one index format");
   if (l->down.d_in != l->gate.d_out || l->down.d_out != l->gate.d_in)
@@ -179,6 +193,7 @@ struct PersistBufs {
   float *hbuf, *pieces1, *pieces3;
   unsigned* ctl;
   int* status;
+  float* lr_z;  // z = V x' of the low-rank correction (linear layer with factors)
 };
 
 cudaError_t run_persistent(const uint16_t* x, int rows, int nt, const vq3_mlp_layer* layer, const vq3_linear* L,
@@ -217,6 +232,9 @@ cudaError_t run_persistent(const uint16_t* x, int rows, int nt, const vq3_mlp_la
   } else {
     a.mlp = 0;
     a.format = L->format;
+    a.lr_u = L->lr_u;
+    a.lr_z = b.lr_z;
+    a.lr_rank = L->lr_rank;
     a.d_model = L->d_in;
     a.d_model_out = L->d_out;
     a.block_in = L->block;
@@ -247,11 +265,12 @@ constexpr int kPrefillRows = 17;  // from this many rows on, the tcgen05 path (t
 
 // [status word][counter words: part flags][x' FP16 [rows][d_in]]
 // [h FP32 [rows][d_inter]][h' FP16 [rows][d_inter]][parts of split tiles]
+// ([z FP32 [rows][rank]] with low-rank factors)
 struct PrefillWs {
-  size_t status, flags, xr, h, hr, part, total;
+  size_t status, flags, xr, h, hr, part, z, total;
 };
 
-PrefillWs prefill_ws(int rows, int d_in, int d_inter, size_t ctl) {
+PrefillWs prefill_ws(int rows, int d_in, int d_inter, size_t ctl, int rank = 0) {
   PrefillWs w{};
   w.status = 0;
   w.flags = kCtlOffset;
@@ -264,6 +283,8 @@ PrefillWs prefill_ws(int rows, int d_in, int d_inter, size_t ctl) {
   off = round_up(off + (size_t)rows * d_inter * 2, 256);
   w.part = off;
   off = round_up(off + prefill_part_bytes(rows), 256);
+  w.z = off;
+  off = round_up(off + (size_t)rows * rank * sizeof(float), 256);
   w.total = off;
   return w;
 }
@@ -311,11 +332,18 @@ cudaError_t run_prefill_mlp(const uint16_t* x, int rows, const vq3_mlp_layer& l,
 
 cudaError_t run_prefill_linear(const uint16_t* x, int rows, const vq3_linear& L, char* ws, uint16_t* out,
                                cudaStream_t st) {
-  const PrefillWs w = prefill_ws(rows, L.d_in, 0, linear_ctl_bytes(L.d_in, L.d_out));
+  const PrefillWs w = prefill_ws(rows, L.d_in, 0, linear_ctl_bytes(L.d_in, L.d_out), L.lr_rank);
   uint16_t* xr = reinterpret_cast<uint16_t*>(ws + w.xr);
   cudaError_t e = launch_fwht(x, rows, L.d_in, L.block, L.signs, xr, st);
   if (e != cudaSuccess) return e;
   PrefillArgs a = prefill_args(xr, rows, L, nullptr, ws, w);
+  if (L.lr_rank) {
+    float* z = reinterpret_cast<float*>(ws + w.z);
+    if ((e = launch_lowrank_project(xr, rows, L.d_in, L.lr_v, L.lr_rank, z, st)) != cudaSuccess) return e;
+    a.lr_u = L.lr_u;
+    a.lr_z = z;
+    a.lr_rank = L.lr_rank;
+  }
   a.out16 = out;
   return launch_prefill_gemm(a, st);
 }
@@ -516,8 +544,9 @@ int fwht_rotate(const uint16_t* x, int rows, int n, int block, const uint32_t* s
 
 size_t vq3_linear_workspace_bytes(int rows, const vq3_linear* L) {
   if (!L || rows < 0 || !layout_supported(L->d_in, L->d_out)) return 0;
-  if (rows >= kPrefillRows) return prefill_ws(rows, L->d_in, 0, linear_ctl_bytes(L->d_in, L->d_out)).total;
-  return linear_ws(rows, L->d_in, L->d_out).total;
+  if (rows >= kPrefillRows)
+    return prefill_ws(rows, L->d_in, 0, linear_ctl_bytes(L->d_in, L->d_out), L->lr_rank).total;
+  return linear_ws(rows, L->d_in, L->d_out, L->lr_rank).total;
 }
 
 size_t vq3_mlp_workspace_bytes(int rows, const vq3_mlp_layer* layer) {
@@ -555,18 +584,26 @@ int vq3_linear_forward(const uint16_t* x, int rows, const vq3_linear* L, uint16_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   if (rows >= kPrefillRows) {
-    const size_t need = prefill_ws(rows, L->d_in, 0, linear_ctl_bytes(L->d_in, L->d_out)).total;
+    const size_t need = prefill_ws(rows, L->d_in, 0, linear_ctl_bytes(L->d_in, L->d_out), L->lr_rank).total;
     if (ws_bytes < need) return fail(VQ3_ENOSPACE, "linear: workspace %zu < %zu bytes", ws_bytes, need);
     cudaError_t e = run_prefill_linear(x, rows, *L, ws, out, st);
     if (e != cudaSuccess) return cuda_fail(e, "linear: launch");
     return ok();
   }
-  const LinearWs w = linear_ws(rows, L->d_in, L->d_out);
+  const LinearWs w = linear_ws(rows, L->d_in, L->d_out, L->lr_rank);
   if (ws_bytes < w.total) return fail(VQ3_ENOSPACE, "linear: workspace %zu < %zu bytes", ws_bytes, w.total);
   PersistBufs b{};
   b.pieces1 = reinterpret_cast<float*>(ws + w.pieces);
   b.ctl = reinterpret_cast<unsigned*>(ws + w.counters);
   b.status = reinterpret_cast<int*>(ws + w.status);
+  if (L->lr_rank) {
+    // z = V x' for all rows ahead of the decode kernel, whose output step adds U z
+    uint16_t* xr = reinterpret_cast<uint16_t*>(ws + w.xr);
+    b.lr_z = reinterpret_cast<float*>(ws + w.z);
+    cudaError_t e = launch_fwht(x, rows, L->d_in, L->block, L->signs, xr, st);
+    if (e == cudaSuccess) e = launch_lowrank_project(xr, rows, L->d_in, L->lr_v, L->lr_rank, b.lr_z, st);
+    if (e != cudaSuccess) return cuda_fail(e, "linear: launch");
+  }
   cudaError_t e = run_persistent(x, rows, dec_tiles_per_pass(rows), nullptr, L, b, out, st);
   if (e != cudaSuccess) return cuda_fail(e, "linear: launch");
   return ok();

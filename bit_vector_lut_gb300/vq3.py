@@ -30,7 +30,8 @@ class Vq3Error(RuntimeError):
 
 class vq3_linear(ctypes.Structure):
     _fields_ = [("d_in", c_int), ("d_out", c_int), ("block", c_int), ("packed", c_void_p),
-                ("codebook", c_void_p), ("scales", c_void_p), ("signs", c_void_p), ("format", c_int)]
+                ("codebook", c_void_p), ("scales", c_void_p), ("signs", c_void_p), ("format", c_int),
+                ("lr_rank", c_int), ("lr_u", c_void_p), ("lr_v", c_void_p)]
 
 
 # index formats (VQ3_FORMAT_* in vq3.h): name -> (code, index bits, output channels per index)
@@ -130,28 +131,36 @@ class Linear:
     """One VQ3 matrix resident on the GPU (packed indices, codebook, scales, signs)."""
 
     def __init__(self, d_in, d_out, block, packed: torch.Tensor, codebook: torch.Tensor, scales: torch.Tensor,
-                 signs: torch.Tensor | None = None, fmt: str = "2x64"):
+                 signs: torch.Tensor | None = None, fmt: str = "2x64", lr_u: torch.Tensor | None = None,
+                 lr_v: torch.Tensor | None = None):
         self.d_in, self.d_out, self.block, self.fmt = int(d_in), int(d_out), int(block), fmt
         self.packed, self.codebook, self.scales, self.signs = packed, codebook, scales, signs
+        self.lr_u, self.lr_v = lr_u, lr_v
+        rank = 0 if lr_u is None else int(lr_u.shape[1])
         self.struct = vq3_linear(self.d_in, self.d_out, self.block, _ptr(packed), _ptr(codebook), _ptr(scales),
-                                 _ptr(signs), FORMATS[fmt][0])
+                                 _ptr(signs), FORMATS[fmt][0], rank, _ptr(lr_u), _ptr(lr_v))
 
     @classmethod
     def from_canonical(cls, d_in, d_out, block, stream, codebook, scales, signs=None, device="cuda",
-                       fmt: str = "2x64"):
+                       fmt: str = "2x64", lr_u=None, lr_v=None):
         packed = torch.from_numpy(pack_layout(stream, d_in, d_out, fmt)).to(device)
         cb = torch.from_numpy(np.ascontiguousarray(codebook, dtype=np.float16).reshape(-1)).to(device)
         sc = torch.from_numpy(np.ascontiguousarray(scales, dtype=np.float16)).to(device)
         sg = None
         if signs is not None:
             sg = torch.from_numpy(np.ascontiguousarray(signs, dtype=np.uint32).view(np.int32)).to(device)
-        return cls(d_in, d_out, block, packed, cb, sc, sg, fmt)
+        lu = lv = None
+        if lr_u is not None:
+            lu = torch.from_numpy(np.ascontiguousarray(lr_u, dtype=np.float16)).to(device)
+            lv = torch.from_numpy(np.ascontiguousarray(lr_v, dtype=np.float16)).to(device)
+        return cls(d_in, d_out, block, packed, cb, sc, sg, fmt, lu, lv)
 
     @classmethod
     def from_matrix(cls, m, device="cuda"):
         """From any object with d_in, d_out, block, stream, codebook, scales, signs (and fmt) fields."""
         return cls.from_canonical(m.d_in, m.d_out, m.block, m.stream, m.codebook, m.scales, m.signs, device,
-                                  getattr(m, "fmt", "2x64") or "2x64")
+                                  getattr(m, "fmt", "2x64") or "2x64", getattr(m, "lr_u", None),
+                                  getattr(m, "lr_v", None))
 
 
 class MLP:

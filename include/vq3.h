@@ -95,6 +95,15 @@ extern "C" {
  *   scales: device, [d_out] FP16 per-output-channel scales.
  *   signs : device, bit-packed seeded signs over d_in (bit j of word j/32 set
  *           => input j is negated before the Hadamard block), or NULL for all +1.
+ *   format: VQ3_FORMAT_*.
+ *   lr_rank, lr_u, lr_v: optional low-rank correction (model card
+ *           "anemll/anemll-forge-qwen3.8-27B", table row "Token mixers": rank-64
+ *           factors): the weight becomes diag(scales) C[idx] + U V, with U =
+ *           lr_u [d_out][lr_rank] and V = lr_v [lr_rank][d_in], device FP16,
+ *           16-byte aligned, acting on the rotated input like the lookup-table
+ *           part (the scales apply to the lookup-table part only). lr_rank = 0
+ *           (no factors) or a multiple of 8 up to 64. Single linear layers only:
+ *           vq3_mlp_forward rejects matrices with factors.
  */
 typedef struct vq3_linear {
   int d_in;
@@ -105,6 +114,9 @@ typedef struct vq3_linear {
   const uint16_t* scales;
   const uint32_t* signs;
   int format;  // VQ3_FORMAT_*; 0 (the three-bit format) in a zero-initialised descriptor
+  int lr_rank;  // 0: no low-rank correction
+  const uint16_t* lr_u;
+  const uint16_t* lr_v;
 } vq3_linear;
 
 /* One SwiGLU block. gate and up read the same rotated input (same d_in, block

@@ -184,3 +184,20 @@ def test_format_checks():
     d.format = 1
     mixed = vq3.vq3_mlp_layer(g, u, d)
     assert lib.vq3_mlp_forward(0x40000, 8, ctypes.byref(mixed), 0x50000, 0x60000, 1 << 24, None) == -1
+
+
+def test_lowrank_descriptor_checks():
+    lib = vq3.lib
+    L = fake_linear()
+    L.lr_rank, L.lr_u, L.lr_v = 12, 0x80000, 0x90000
+    assert lib.vq3_linear_forward(0x40000, 8, ctypes.byref(L), 0x50000, 0x60000, 1 << 24, None) == -3
+    L.lr_rank, L.lr_u, L.lr_v = 64, None, None
+    assert lib.vq3_linear_forward(0x40000, 8, ctypes.byref(L), 0x50000, 0x60000, 1 << 24, None) == -1
+    L.lr_rank, L.lr_u, L.lr_v = 64, 0x80008, 0x90000
+    assert lib.vq3_linear_forward(0x40000, 8, ctypes.byref(L), 0x50000, 0x60000, 1 << 24, None) == -2
+    L.lr_u = 0x80000
+    assert lib.vq3_linear_workspace_bytes(8, ctypes.byref(L)) > lib.vq3_linear_workspace_bytes(8, ctypes.byref(fake_linear()))
+    g = fake_linear(256, 512, 256)
+    g.lr_rank, g.lr_u, g.lr_v = 64, 0x80000, 0x90000
+    mlp = vq3.vq3_mlp_layer(g, fake_linear(256, 512, 256), fake_linear(512, 256, 256))
+    assert lib.vq3_mlp_forward(0x40000, 8, ctypes.byref(mlp), 0x50000, 0x60000, 1 << 24, None) == -3

@@ -1,0 +1,64 @@
+"""GPU parity for the low-rank correction of a linear layer, W = diag(s) C[idx]
++ U V on the rotated input (model card "anemll/anemll-forge-qwen3.8-27B",
+table row "Token mixers": rank-64 factors): the decode kernel (up to 16 rows)
+and the tensor-core GEMM (from 17 rows) against the oracle."""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from oracle import vq3_oracle as O  # noqa: E402
+from synth import inputs as S  # noqa: E402
+from tests.parity import assert_parity  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def vq3():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need CUDA")
+    from bit_vector_lut_gb300 import vq3 as m
+    return m
+
+
+def f16(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float16)).to(DEV)
+
+
+@pytest.mark.parametrize("fmt", ["2x64", "2x16", "lut4"])
+@pytest.mark.parametrize("rank", [8, 64])
+@pytest.mark.parametrize("rows", [1, 8, 16, 17, 64, 300])
+def test_linear_with_factors(vq3, fmt, rank, rows):
+    m = S.matrix(S.rng(70), 1024, 512, 1024, fmt)
+    m.signs = S.sign_bits(S.rng(70, 2), 1024)
+    S.add_lowrank(S.rng(70, 3), m, rank, 0.02)
+    x = S.activations(S.rng(70, 0), rows, 1024)
+    got = vq3.linear_forward(f16(x), vq3.Linear.from_matrix(m, DEV)).cpu().numpy()
+    ref = O.linear_f64(x, m)
+    assert_parity(got, ref, f"{fmt} rank {rank} rows={rows}")
+    # the correction is not negligible: without it the output would fail the same bar
+    m0 = S.Matrix(m.d_in, m.d_out, m.block, m.codebook, m.stream, m.scales, m.signs, fmt)
+    assert O.rel_max_err(O.linear_f64(x, m0), ref) > 1e-2
+
+
+@pytest.mark.parametrize("rows", [8, 64])
+def test_token_mixer_shape_with_factors(vq3, rows):
+    # a 5120 -> 6144 projection with rank-64 factors (token-mixer shapes are not on the pages: synthetic)
+    m = S.matrix(S.rng(71), 5120, 6144, 1024, "2x16")
+    S.add_lowrank(S.rng(71, 3), m, 64, 0.02)
+    x = S.activations(S.rng(71, 0), rows, 5120)
+    got = vq3.linear_forward(f16(x), vq3.Linear.from_matrix(m, DEV)).cpu().numpy()
+    assert_parity(got, O.linear_f64(x, m), f"5120->6144 rank 64 rows={rows}")
+
+
+def test_zero_factors_bit_identical(vq3):
+    m = S.matrix(S.rng(72), 512, 256, 512)
+    x = f16(S.activations(S.rng(72, 0), 8, 512))
+    a = vq3.linear_forward(x, vq3.Linear.from_matrix(m, DEV)).cpu().numpy()
+    m.lr_u = np.zeros((256, 16), np.float16)
+    m.lr_v = np.zeros((16, 512), np.float16)
+    b = vq3.linear_forward(x, vq3.Linear.from_matrix(m, DEV)).cpu().numpy()
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
