@@ -298,11 +298,12 @@ def _run_ours_on(args, torch, vq3, dev, stream, rows, sets, x_host, x, out, ws, 
            "h2d_bytes_per_step": int(x_host.nbytes), "d2h_bytes_per_step": int(rows * HIDDEN * 2),
            "api": "vq3_mlp_forward_host (pageable->pinned host buffers)"}
 
-    extra, stack, fmts = {}, {}, {}
+    extra, stack, fmts, mixers = {}, {}, {}, {}
     if not args.quick and rank == 0:
         extra = prefill_sweep(vq3, dev, stream, pk)
         stack = stack64(vq3, dev, stream, pk)
         fmts = format_lines(vq3, dev, stream, pk, l2)
+        mixers = token_mixer_lines(vq3, dev, stream, pk, l2)
 
     launches = vq3.mlp_kernel_launches(rows, sets[0]) * steps
     line = None
@@ -323,6 +324,8 @@ def _run_ours_on(args, torch, vq3, dev, stream, rows, sets, x_host, x, out, ws, 
             line["stack64"] = stack
         if fmts:
             line["formats"] = fmts
+        if mixers:
+            line["token_mixers"] = mixers
         if world == 1 and not args.no_cpu_baseline:
             rate, dt, smp = time_oracle(rows, 1.0 / args.oracle_frac, args.oracle_steps, 1)
             line["cpu_baseline"] = {"value": round(rate, 3), "unit": "rows/s", "cores": cpu_cores(),
@@ -394,6 +397,48 @@ def format_lines(vq3, dev, stream, pk, l2) -> dict:
                     "T2048_ms": round(msp, 4), "T2048_tflops": round(tf, 2),
                     "T2048_frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4),
                     "status": vq3.workspace_status(ws) | vq3.workspace_status(wsp)}
+    return res
+
+
+# token-mixer projections: the pages give their formats (two-bit vector LUT in layers 0-23, four-bit
+# LUT in 24-63, rank-64 FP16 factors, 1024-wide input rotations) but not their shapes: these are synthetic
+TOKEN_MIXERS = (("in_proj_5120x12288", 5120, 12288), ("out_proj_6144x5120", 6144, 5120))
+
+
+def token_mixer_lines(vq3, dev, stream, pk, l2) -> dict:
+    """One projection per (shape, format) with rank-64 factors at T = 8 and T = 64: the median of 20
+    launches, each bracketed by events on the stream after a write of 2 x L2 that evicts the weights."""
+    import torch
+    res = {}
+    flush = torch.empty(int(2 * l2), dtype=torch.uint8, device=dev)
+    for name, d_in, d_out in TOKEN_MIXERS:
+        for fmt in ("2x16", "lut4"):
+            m = S.matrix(S.rng(80, 1), d_in, d_out, 1024, fmt)
+            S.add_lowrank(S.rng(80, 3), m, 64, 0.02)
+            lin = vq3.Linear.from_matrix(m, dev)
+            nbytes = S.stream_bytes(d_in, d_out, fmt) + 2 * d_out + 2 * S.FORMATS[fmt][2] * S.FORMATS[fmt][1] \
+                + 2 * 64 * (d_in + d_out)
+            for rows in (8, 64):
+                x = torch.from_numpy(S.activations(S.rng(80, 0), rows, d_in)).to(dev)
+                out = torch.empty((rows, d_out), dtype=torch.float16, device=dev)
+                ws = vq3.workspace(vq3.linear_workspace_bytes(rows, lin), dev, stream)
+                durs = []
+                for it in range(23):
+                    flush.fill_(it & 0xFF)
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    vq3.linear_forward(x, lin, out=out, ws=ws, stream=stream)
+                    b.record(stream)
+                    b.synchronize()
+                    if it >= 3:
+                        durs.append(a.elapsed_time(b))
+                ms = float(np.median(durs))
+                gbs = nbytes / (ms / 1e3) / 1e9
+                res[f"{name}_{fmt}_T{rows}"] = {"us": round(ms * 1e3, 2), "weight_bytes": nbytes,
+                                               "weight_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4),
+                                               "tflops": round(2 * d_in * d_out * rows / (ms / 1e3) / 1e12, 2),
+                                               "status": vq3.workspace_status(ws)}
     return res
 
 

@@ -116,10 +116,10 @@ size_t ctl_bytes(int n_words) {
 size_t mlp_ctl_bytes(int H, int I) { return ctl_bytes(ctl_mlp(H, I).n); }
 size_t linear_ctl_bytes(int d_in, int d_out) { return ctl_bytes(ctl_linear(d_in, d_out).n); }
 
-// [status word][counter words][pieces]([x' FP16 [rows][d_in]][z FP32 [rows][rank]] with
-// low-rank factors)
+// [status word][counter words][pieces]([x' FP16 [rows][d_in]][U V x' FP32 [rows][d_out]]
+// [projection sums FP32 [chunks][rows][rank]] with low-rank factors)
 struct LinearWs {
-  size_t status, counters, pieces, xr, z, total;
+  size_t status, counters, pieces, xr, ylr, zpart, total;
 };
 
 LinearWs linear_ws(int rows, int d_in, int d_out, int rank) {
@@ -129,11 +129,13 @@ LinearWs linear_ws(int rows, int d_in, int d_out, int rank) {
   size_t off = kCtlOffset + linear_ctl_bytes(d_in, d_out);
   w.pieces = off;
   off = round_up(off + persist_pieces_bytes(rows, d_in, d_out, 1), 256);
-  w.xr = w.z = off;
+  w.xr = w.ylr = w.zpart = off;
   if (rank) {
     off = round_up(off + (size_t)rows * d_in * 2, 256);
-    w.z = off;
-    off = round_up(off + (size_t)rows * rank * sizeof(float), 256);
+    w.ylr = off;
+    off = round_up(off + (size_t)rows * d_out * sizeof(float), 256);
+    w.zpart = off;
+    off = round_up(off + (size_t)lowrank_chunks(d_in) * rows * rank * sizeof(float), 256);
   }
   w.total = off;
   return w;
@@ -193,7 +195,7 @@ struct PersistBufs {
   float *hbuf, *pieces1, *pieces3;
   unsigned* ctl;
   int* status;
-  float* lr_z;  // z = V x' of the low-rank correction (linear layer with factors)
+  float* lr_y;  // U V x' of the low-rank correction (linear layer with factors)
 };
 
 cudaError_t run_persistent(const uint16_t* x, int rows, int nt, const vq3_mlp_layer* layer, const vq3_linear* L,
@@ -232,9 +234,7 @@ cudaError_t run_persistent(const uint16_t* x, int rows, int nt, const vq3_mlp_la
   } else {
     a.mlp = 0;
     a.format = L->format;
-    a.lr_u = L->lr_u;
-    a.lr_z = b.lr_z;
-    a.lr_rank = L->lr_rank;
+    a.lr_y = b.lr_y;
     a.d_model = L->d_in;
     a.d_model_out = L->d_out;
     a.block_in = L->block;
@@ -265,12 +265,12 @@ constexpr int kPrefillRows = 17;  // from this many rows on, the tcgen05 path (t
 
 // [status word][counter words: part flags][x' FP16 [rows][d_in]]
 // [h FP32 [rows][d_inter]][h' FP16 [rows][d_inter]][parts of split tiles]
-// ([z FP32 [rows][rank]] with low-rank factors)
+// ([U V x' FP32 [rows][d_out]][projection sums FP32 [chunks][rows][rank]] with low-rank factors)
 struct PrefillWs {
-  size_t status, flags, xr, h, hr, part, z, total;
+  size_t status, flags, xr, h, hr, part, ylr, zpart, total;
 };
 
-PrefillWs prefill_ws(int rows, int d_in, int d_inter, size_t ctl, int rank = 0) {
+PrefillWs prefill_ws(int rows, int d_in, int d_inter, size_t ctl, int rank = 0, int d_out = 0) {
   PrefillWs w{};
   w.status = 0;
   w.flags = kCtlOffset;
@@ -283,8 +283,12 @@ PrefillWs prefill_ws(int rows, int d_in, int d_inter, size_t ctl, int rank = 0) 
   off = round_up(off + (size_t)rows * d_inter * 2, 256);
   w.part = off;
   off = round_up(off + prefill_part_bytes(rows), 256);
-  w.z = off;
-  off = round_up(off + (size_t)rows * rank * sizeof(float), 256);
+  w.ylr = w.zpart = off;
+  if (rank) {
+    off = round_up(off + (size_t)rows * d_out * sizeof(float), 256);
+    w.zpart = off;
+    off = round_up(off + (size_t)lowrank_chunks(d_in) * rows * rank * sizeof(float), 256);
+  }
   w.total = off;
   return w;
 }
@@ -332,17 +336,17 @@ cudaError_t run_prefill_mlp(const uint16_t* x, int rows, const vq3_mlp_layer& l,
 
 cudaError_t run_prefill_linear(const uint16_t* x, int rows, const vq3_linear& L, char* ws, uint16_t* out,
                                cudaStream_t st) {
-  const PrefillWs w = prefill_ws(rows, L.d_in, 0, linear_ctl_bytes(L.d_in, L.d_out), L.lr_rank);
+  const PrefillWs w = prefill_ws(rows, L.d_in, 0, linear_ctl_bytes(L.d_in, L.d_out), L.lr_rank, L.d_out);
   uint16_t* xr = reinterpret_cast<uint16_t*>(ws + w.xr);
   cudaError_t e = launch_fwht(x, rows, L.d_in, L.block, L.signs, xr, st);
   if (e != cudaSuccess) return e;
   PrefillArgs a = prefill_args(xr, rows, L, nullptr, ws, w);
   if (L.lr_rank) {
-    float* z = reinterpret_cast<float*>(ws + w.z);
-    if ((e = launch_lowrank_project(xr, rows, L.d_in, L.lr_v, L.lr_rank, z, st)) != cudaSuccess) return e;
-    a.lr_u = L.lr_u;
-    a.lr_z = z;
-    a.lr_rank = L.lr_rank;
+    float* ylr = reinterpret_cast<float*>(ws + w.ylr);
+    float* zpart = reinterpret_cast<float*>(ws + w.zpart);
+    if ((e = launch_lowrank(xr, rows, L.d_in, L.lr_v, L.lr_u, L.lr_rank, L.d_out, zpart, ylr, st)) != cudaSuccess)
+      return e;
+    a.lr_y = ylr;
   }
   a.out16 = out;
   return launch_prefill_gemm(a, st);
@@ -545,7 +549,7 @@ int fwht_rotate(const uint16_t* x, int rows, int n, int block, const uint32_t* s
 size_t vq3_linear_workspace_bytes(int rows, const vq3_linear* L) {
   if (!L || rows < 0 || !layout_supported(L->d_in, L->d_out)) return 0;
   if (rows >= kPrefillRows)
-    return prefill_ws(rows, L->d_in, 0, linear_ctl_bytes(L->d_in, L->d_out), L->lr_rank).total;
+    return prefill_ws(rows, L->d_in, 0, linear_ctl_bytes(L->d_in, L->d_out), L->lr_rank, L->d_out).total;
   return linear_ws(rows, L->d_in, L->d_out, L->lr_rank).total;
 }
 
@@ -584,7 +588,7 @@ int vq3_linear_forward(const uint16_t* x, int rows, const vq3_linear* L, uint16_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   if (rows >= kPrefillRows) {
-    const size_t need = prefill_ws(rows, L->d_in, 0, linear_ctl_bytes(L->d_in, L->d_out), L->lr_rank).total;
+    const size_t need = prefill_ws(rows, L->d_in, 0, linear_ctl_bytes(L->d_in, L->d_out), L->lr_rank, L->d_out).total;
     if (ws_bytes < need) return fail(VQ3_ENOSPACE, "linear: workspace %zu < %zu bytes", ws_bytes, need);
     cudaError_t e = run_prefill_linear(x, rows, *L, ws, out, st);
     if (e != cudaSuccess) return cuda_fail(e, "linear: launch");
@@ -597,11 +601,13 @@ int vq3_linear_forward(const uint16_t* x, int rows, const vq3_linear* L, uint16_
   b.ctl = reinterpret_cast<unsigned*>(ws + w.counters);
   b.status = reinterpret_cast<int*>(ws + w.status);
   if (L->lr_rank) {
-    // z = V x' for all rows ahead of the decode kernel, whose output step adds U z
+    // U V x' for all rows ahead of the decode kernel, whose output step adds it
     uint16_t* xr = reinterpret_cast<uint16_t*>(ws + w.xr);
-    b.lr_z = reinterpret_cast<float*>(ws + w.z);
+    b.lr_y = reinterpret_cast<float*>(ws + w.ylr);
     cudaError_t e = launch_fwht(x, rows, L->d_in, L->block, L->signs, xr, st);
-    if (e == cudaSuccess) e = launch_lowrank_project(xr, rows, L->d_in, L->lr_v, L->lr_rank, b.lr_z, st);
+    if (e == cudaSuccess)
+      e = launch_lowrank(xr, rows, L->d_in, L->lr_v, L->lr_u, L->lr_rank, L->d_out,
+                         reinterpret_cast<float*>(ws + w.zpart), b.lr_y, st);
     if (e != cudaSuccess) return cuda_fail(e, "linear: launch");
   }
   cudaError_t e = run_persistent(x, rows, dec_tiles_per_pass(rows), nullptr, L, b, out, st);

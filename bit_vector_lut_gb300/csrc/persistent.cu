@@ -702,21 +702,7 @@ __device__ __forceinline__ void output_tasks(const PersistArgs& a, const DecodeJ
       const int ch = sg * kSuChannels + c;
       const float s = __half2float(__ushort_as_half(j.scales0[ch]));
       float v = s * y;
-      if (a.lr_rank) {
-        // low-rank correction: + sum_q U[ch][q] z[row][q]
-        const uint16_t* u = a.lr_u + (size_t)ch * a.lr_rank;
-        const float* zr = a.lr_z + (size_t)(a.row0 + r) * a.lr_rank;
-        for (int q = 0; q < a.lr_rank; q += 8) {
-          const uint4 uu = __ldg(reinterpret_cast<const uint4*>(u + q));
-          const __half2* h = reinterpret_cast<const __half2*>(&uu);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 f = __half22float2(h[k]);
-            v = fmaf(f.x, __ldcg(zr + q + 2 * k), v);
-            v = fmaf(f.y, __ldcg(zr + q + 2 * k + 1), v);
-          }
-        }
-      }
+      if (a.lr_y) v += __ldg(a.lr_y + (size_t)(a.row0 + r) * j.d_out + ch);  // low-rank correction
       a.out[(size_t)(a.row0 + r) * j.d_out + ch] = __half_as_ushort(__float2half_rn(v));
     }
   }

@@ -567,36 +567,11 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] *= sc;
-            if (a.lr_rank && live) {
-              // low-rank correction: + sum_q U[ch][q] z[row][q] (z rows are read by every
-              // lane of the warp at once: one broadcast per load)
-              const uint16_t* u = a.lr_u + (size_t)ch * a.lr_rank;
-              for (int q = 0; q < a.lr_rank; q += 8) {
-                const uint4 uu = __ldg(reinterpret_cast<const uint4*>(u + q));
-                const __half2* h = reinterpret_cast<const __half2*>(&uu);
-                float uf[8];
+            if (a.lr_y && live) {
+              // low-rank correction, one value per output (lanes: consecutive channels)
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  const float2 f = __half22float2(h[k]);
-                  uf[2 * k] = f.x;
-                  uf[2 * k + 1] = f.y;
-                }
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  if (c0 + j < cols) {
-                    const float4* zr = reinterpret_cast<const float4*>(a.lr_z + (size_t)(row0 + c0 + j) * a.lr_rank + q);
-                    const float4 z0 = __ldg(zr), z1 = __ldg(zr + 1);
-                    v[j] = fmaf(uf[0], z0.x, v[j]);
-                    v[j] = fmaf(uf[1], z0.y, v[j]);
-                    v[j] = fmaf(uf[2], z0.z, v[j]);
-                    v[j] = fmaf(uf[3], z0.w, v[j]);
-                    v[j] = fmaf(uf[4], z1.x, v[j]);
-                    v[j] = fmaf(uf[5], z1.y, v[j]);
-                    v[j] = fmaf(uf[6], z1.z, v[j]);
-                    v[j] = fmaf(uf[7], z1.w, v[j]);
-                  }
-                }
-              }
+              for (int j = 0; j < 16; ++j)
+                if (c0 + j < cols) v[j] += __ldg(a.lr_y + (size_t)(row0 + c0 + j) * a.d_out + ch);
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {

@@ -104,9 +104,8 @@ struct PersistArgs {
   int row0, rows;           // rows of this pass: [row0, row0 + rows), rows <= 8 * NT
   int mlp;                  // 1: MLP block (gate, up, down); 0: one linear layer (gate)
   int format;               // VQ3_FORMAT_* of every matrix
-  const uint16_t* lr_u;     // low-rank correction (linear layer only): U [d_out][lr_rank] FP16
-  const float* lr_z;        // z = V x' [rows][lr_rank] FP32 for all rows of the call
-  int lr_rank;              // 0: none
+  const float* lr_y;        // low-rank correction U V x' [rows][d_out] FP32 for all rows of the
+                            // call (linear layer only), or null
   int d_model, d_inter;     // MLP: hidden and intermediate widths; linear: d_model = d_in
   int d_model_out;          // linear: d_out
   int block_in, block_dn;   // rotation blocks of the gate/up (or linear) input and of the down input
@@ -157,9 +156,7 @@ struct PrefillArgs {
   uint16_t* out16;         // [rows][d_out] FP16 (no swiglu)
   float* out32;            // [rows][d_out] FP32 (swiglu)
   int* status;             // status word (3: a wait timed out)
-  const uint16_t* lr_u;    // low-rank correction (no swiglu): U [d_out][lr_rank] FP16
-  const float* lr_z;       // z = V x' [rows][lr_rank] FP32
-  int lr_rank;             // 0: none
+  const float* lr_y;       // low-rank correction U V x' [rows][d_out] FP32 (no swiglu), or null
   float* part;             // split-tile sums, one 128 x tile-rows FP32 slot per CTA
   unsigned* flags;         // one word per CTA, zero between calls: its slot is filled
   long long work;          // (tile, K step) pairs; set by launch_prefill_gemm
@@ -173,9 +170,12 @@ cudaError_t launch_prefill_gemm(const PrefillArgs& a, cudaStream_t st);
 cudaError_t launch_residual_rmsnorm(uint16_t* resid, const uint16_t* delta, int rows, int n,
                                     float eps, uint16_t* normed, cudaStream_t st);
 cudaError_t launch_dequant(const vq3_linear& L, int apply_scale, uint16_t* w_out, cudaStream_t st);
-// z[r][j] = sum_i V[j][i] xr[r][i] in FP32 for the low-rank correction (V [rank][d_in] FP16).
-cudaError_t launch_lowrank_project(const uint16_t* xr, int rows, int d_in, const uint16_t* V, int rank, float* z,
-                                   cudaStream_t st);
+// ylr[r][o] = sum_j U[o][j] z[r][j], z[r][j] = sum_i V[j][i] xr[r][i] (FP32) for the low-rank
+// correction (V [rank][d_in], U [d_out][rank] FP16); the projection's sums over
+// lowrank_chunks(d_in) input chunks go through part [chunks][rows][rank].
+int lowrank_chunks(int d_in);
+cudaError_t launch_lowrank(const uint16_t* xr, int rows, int d_in, const uint16_t* V, const uint16_t* U, int rank,
+                           int d_out, float* part, float* ylr, cudaStream_t st);
 
 // vq3_mlp_forward with passes of at most `pass_cap` rows (8, 16 or 32), and its
 // workspace size; vq3_mlp_forward itself uses 32.
