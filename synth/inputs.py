@@ -200,3 +200,32 @@ FORMAT_SEEDS = {"2x16": 5, "lut4": 6}
 def mlp_format(fmt: str, rows: int = 8) -> Workload:
     """One block at 5120/17408 in another index format (two-bit vector or four-bit scalar LUT)."""
     return mlp_27b(seed=FORMAT_SEEDS[fmt], rows=rows, fmt=fmt)
+
+
+# ---- gated delta-rule token mixer (the 8-row block of the pages' DeltaNet layers) ----
+
+@dataclass
+class DeltaRuleInputs:
+    q: np.ndarray      # [T, H, d_k] float16
+    k: np.ndarray      # [T, H, d_k] float16, rows of unit length (up to FP16 rounding)
+    v: np.ndarray      # [T, H, d_v] float16
+    beta: np.ndarray   # [T, H] float32 in (0, 1): write strength
+    alpha: np.ndarray  # [T, H] float32 in (0, 1]: decay gate
+    state: np.ndarray  # [H, d_k, d_v] float32: state before the first token
+
+
+def delta_rule_inputs(seed: int = 9, tokens: int = 8, heads: int = 16, d_k: int = 128, d_v: int = 128) -> DeltaRuleInputs:
+    """Seeded inputs of the delta-rule block: queries, keys (unit rows, as the layer
+    normalises them) and values ~N(0,1) from stream [seed, 0]; strengths ~U[0.05, 0.95] and
+    gates ~U[0.9, 1] from [seed, 1]; the initial state ~N(0, 0.1) from [seed, 2]. Head counts
+    and widths are not on the pages: the defaults are synthetic."""
+    g = rng(seed, 0)
+    q = g.standard_normal((tokens, heads, d_k))
+    k = g.standard_normal((tokens, heads, d_k))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = g.standard_normal((tokens, heads, d_v))
+    gg = rng(seed, 1)
+    beta = gg.uniform(0.05, 0.95, (tokens, heads)).astype(np.float32)
+    alpha = gg.uniform(0.9, 1.0, (tokens, heads)).astype(np.float32)
+    state = (rng(seed, 2).standard_normal((heads, d_k, d_v)) * 0.1).astype(np.float32)
+    return DeltaRuleInputs(q.astype(np.float16), k.astype(np.float16), v.astype(np.float16), beta, alpha, state)
