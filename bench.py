@@ -304,6 +304,7 @@ def _run_ours_on(args, torch, vq3, dev, stream, rows, sets, x_host, x, out, ws, 
         stack = stack64(vq3, dev, stream, pk)
         fmts = format_lines(vq3, dev, stream, pk, l2)
         mixers = token_mixer_lines(vq3, dev, stream, pk, l2)
+        mixers.update(delta_rule_lines(vq3, dev, stream))
 
     launches = vq3.mlp_kernel_launches(rows, sets[0]) * steps
     line = None
@@ -439,6 +440,36 @@ def token_mixer_lines(vq3, dev, stream, pk, l2) -> dict:
                                                "weight_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4),
                                                "tflops": round(2 * d_in * d_out * rows / (ms / 1e3) / 1e12, 2),
                                                "status": vq3.workspace_status(ws)}
+    return res
+
+
+def delta_rule_lines(vq3, dev, stream) -> dict:
+    """The gated delta-rule block (16 heads, d_k = d_v = 128: synthetic sizes) at 8 tokens (one
+    verify block) and 64 tokens (a prefill chunk): mean of 50 calls in a CUDA graph."""
+    import torch
+    res = {}
+    for tokens in (8, 64):
+        w = S.delta_rule_inputs(seed=12, tokens=tokens, heads=16, d_k=128, d_v=128)
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+        q, k, v, be, al, st0 = t(w.q), t(w.k), t(w.v), t(w.beta), t(w.alpha), t(w.state)
+        state = st0.clone()
+        out = torch.empty((tokens, 16, 128), dtype=torch.float16, device=dev)
+        vq3.delta_rule_forward(q, k, v, be, al, state, out=out, stream=stream)
+        gph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gph, stream=stream):
+            for _ in range(50):
+                vq3.delta_rule_forward(q, k, v, be, al, state, out=out, stream=stream)
+        gph.replay()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(3):
+            gph.replay()
+        b.record(stream)
+        b.synchronize()
+        us = a.elapsed_time(b) / 150 * 1e3
+        res[f"delta_rule_16x128x128_T{tokens}"] = {"us": round(us, 2), "tokens_per_s": round(tokens / (us / 1e6), 1)}
     return res
 
 

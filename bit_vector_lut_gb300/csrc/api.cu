@@ -700,6 +700,22 @@ int vq3_mlp_forward(const uint16_t* x, int rows, const vq3_mlp_layer* layer, uin
   return ok();
 }
 
+int vq3_delta_rule_forward(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* beta,
+                           const float* alpha, int tokens, int heads, int d_k, int d_v, float* state, uint16_t* out,
+                           void* stream) {
+  if (tokens < 0 || heads <= 0) return fail(VQ3_EINVAL, "delta_rule: tokens=%d heads=%d", tokens, heads);
+  if (d_k < 8 || d_k > 256 || d_k % 8 || d_v <= 0 || d_v % 16)
+    return fail(VQ3_EUNSUPPORTED, "delta_rule: d_k=%d must be a multiple of 8 in [8, 256], d_v=%d a multiple of 16",
+                d_k, d_v);
+  if (!state) return fail(VQ3_EINVAL, "delta_rule: null state");
+  if (tokens == 0) return ok();
+  if (!q || !k || !v || !beta || !alpha || !out) return fail(VQ3_EINVAL, "delta_rule: null pointer");
+  cudaError_t e = launch_delta_rule(q, k, v, beta, alpha, tokens, heads, d_k, d_v, state, out,
+                                    static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "delta_rule: launch");
+  return ok();
+}
+
 int vq3_mlp_kernel_launches(int rows, const vq3_mlp_layer* layer) {
   if (check_mlp(layer) || rows < 0) return -1;
   if (rows == 0) return 0;

@@ -170,6 +170,10 @@ cudaError_t launch_prefill_gemm(const PrefillArgs& a, cudaStream_t st);
 cudaError_t launch_residual_rmsnorm(uint16_t* resid, const uint16_t* delta, int rows, int n,
                                     float eps, uint16_t* normed, cudaStream_t st);
 cudaError_t launch_dequant(const vq3_linear& L, int apply_scale, uint16_t* w_out, cudaStream_t st);
+// Gated delta-rule token mixer over blocks of 8 tokens (layouts as vq3_delta_rule_forward).
+cudaError_t launch_delta_rule(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* beta,
+                              const float* alpha, int tokens, int heads, int d_k, int d_v, float* state,
+                              uint16_t* out, cudaStream_t st);
 // ylr[r][o] = sum_j U[o][j] z[r][j], z[r][j] = sum_i V[j][i] xr[r][i] (FP32) for the low-rank
 // correction (V [rank][d_in], U [d_out][rank] FP16); the projection's sums over
 // lowrank_chunks(d_in) input chunks go through part [chunks][rows][rank].

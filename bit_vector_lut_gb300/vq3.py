@@ -66,6 +66,8 @@ def _load() -> ctypes.CDLL:
                                          c_void_p]),
         "vq3_residual_rmsnorm": (c_int, [c_void_p, c_void_p, c_int, c_int, c_float, c_void_p, c_void_p]),
         "vq3_dequant_dense": (c_int, [POINTER(vq3_linear), c_int, c_void_p, c_void_p]),
+        "vq3_delta_rule_forward": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
+                                           c_int, c_void_p, c_void_p, c_void_p]),
         "vq3_last_error": (ctypes.c_char_p, []),
         "vq3_version": (ctypes.c_char_p, []),
     }
@@ -278,3 +280,17 @@ def dequant_dense(lin: Linear, apply_scale: bool, stream=None) -> torch.Tensor:
     w = torch.empty((lin.d_out, lin.d_in), dtype=torch.float16, device=lin.packed.device)
     _check(lib.vq3_dequant_dense(ctypes.byref(lin.struct), 1 if apply_scale else 0, w.data_ptr(), _stream(stream)))
     return w
+
+
+# ---------------------------------------------------------------- gated delta rule
+
+def delta_rule_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, alpha: torch.Tensor,
+                       state: torch.Tensor, out=None, stream=None) -> torch.Tensor:
+    """Gated delta-rule token mixer over blocks of 8 tokens; `state` [H, d_k, d_v] FP32 is updated in place."""
+    tokens, heads, d_k = q.shape
+    d_v = v.shape[2]
+    if out is None:
+        out = torch.empty((tokens, heads, d_v), dtype=torch.float16, device=q.device)
+    _check(lib.vq3_delta_rule_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr(), alpha.data_ptr(),
+                                      tokens, heads, d_k, d_v, state.data_ptr(), out.data_ptr(), _stream(stream)))
+    return out

@@ -217,6 +217,25 @@ VQ3_API int vq3_linear_forward(const uint16_t* x, int rows, const vq3_linear* L,
 VQ3_API int vq3_mlp_forward(const uint16_t* x, int rows, const vq3_mlp_layer* layer, uint16_t* out,
                     void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * Gated delta-rule token mixer (the recurrent core of the pages' DeltaNet
+ * layers), processed in blocks of 8 tokens with the exact closed-form block
+ * inverse (I + N)^-1 = (I - N)(I + N^2)(I + N^4). Cited: model card
+ * "anemll/anemll-forge-qwen3.8-27B", "Faster exact graph (previous update)",
+ * bullet "Gated DeltaNet". Per head h, token t:
+ *   S <- alpha[t][h] S + beta[t][h] k_t (v_t - alpha[t][h] S^T k_t)^T,   out_t = S^T q_t
+ * q, k : device FP16 [tokens][heads][d_k];  v, out: device FP16 [tokens][heads][d_v]
+ * beta, alpha: device FP32 [tokens][heads];  state: device FP32 [heads][d_k][d_v],
+ *   read as the state before the first token and overwritten with the state after
+ *   the last (FP32 arithmetic throughout, out rounded to FP16 once).
+ * d_k a multiple of 8 in [8, 256]; d_v a multiple of 16. Deterministic.
+ * Errors: VQ3_EINVAL (null pointer, bad sizes), VQ3_EUNSUPPORTED (d_k, d_v),
+ * VQ3_ECUDA.
+ */
+VQ3_API int vq3_delta_rule_forward(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* beta,
+                                   const float* alpha, int tokens, int heads, int d_k, int d_v, float* state,
+                                   uint16_t* out, void* stream);
+
 /* Number of kernels one vq3_mlp_forward call launches at `rows` rows: one per
  * pass of 8 or 16 rows below 17 rows, 4 from 17 rows on (-1 on a bad
  * descriptor). */

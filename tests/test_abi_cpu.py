@@ -201,3 +201,13 @@ def test_lowrank_descriptor_checks():
     g.lr_rank, g.lr_u, g.lr_v = 64, 0x80000, 0x90000
     mlp = vq3.vq3_mlp_layer(g, fake_linear(256, 512, 256), fake_linear(512, 256, 256))
     assert lib.vq3_mlp_forward(0x40000, 8, ctypes.byref(mlp), 0x50000, 0x60000, 1 << 24, None) == -3
+
+
+def test_delta_rule_argument_checks():
+    f = vq3.lib.vq3_delta_rule_forward
+    p = 0x10000
+    assert f(p, p, p, p, p, 8, 4, 100, 64, p, p, None) == -3   # d_k not a multiple of 8
+    assert f(p, p, p, p, p, 8, 4, 128, 24, p, p, None) == -3   # d_v not a multiple of 16
+    assert f(p, p, p, p, p, 8, 0, 128, 64, p, p, None) == -1   # no heads
+    assert f(p, p, p, p, p, 8, 4, 128, 64, None, p, None) == -1
+    assert f(None, None, None, None, None, 0, 4, 128, 64, p, None, None) == 0  # zero tokens: nothing to do
