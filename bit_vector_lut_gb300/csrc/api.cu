@@ -196,6 +196,11 @@ struct PersistBufs {
   unsigned* ctl;
   int* status;
   float* lr_y;  // U V x' of the low-rank correction (linear layer with factors)
+  // pre-norm residual step fused ahead of the MLP block (see PersistArgs::norm)
+  int norm;
+  const uint16_t* res_delta;
+  uint16_t* res_out;
+  float eps;
 };
 
 cudaError_t run_persistent(const uint16_t* x, int rows, int nt, const vq3_mlp_layer* layer, const vq3_linear* L,
@@ -214,6 +219,10 @@ cudaError_t run_persistent(const uint16_t* x, int rows, int nt, const vq3_mlp_la
     const int H = layer->gate.d_in, I = layer->gate.d_out;
     a.mlp = 1;
     a.format = layer->gate.format;
+    a.norm = b.norm;
+    a.res_delta = b.res_delta;
+    a.res_out = b.res_out;
+    a.eps = b.eps;
     a.d_model = H;
     a.d_inter = I;
     a.d_model_out = H;
@@ -663,13 +672,21 @@ size_t mlp_workspace_bytes_capped(int rows, const vq3_mlp_layer* layer, int pass
   return mlp_ws(rows < pass_cap ? rows : pass_cap, layer).total;
 }
 
-int mlp_forward_capped(const uint16_t* x, int rows, const vq3_mlp_layer* layer, uint16_t* out, void* workspace,
-                       size_t ws_bytes, void* stream, int pass_cap) {
+namespace {
+// The decode-kernel MLP path; `norm` (optional) carries the fused pre-norm residual step.
+int mlp_forward_decode(const uint16_t* x, int rows, const vq3_mlp_layer* layer, uint16_t* out, void* workspace,
+                       size_t ws_bytes, void* stream, int pass_cap, const PersistBufs* norm) {
   MlpCall c = mlp_prepare(rows, pass_cap, layer, workspace, ws_bytes, stream, "mlp");
   if (c.rc || rows == 0) return c.rc ? c.rc : ok();
   if (!x || !out) return fail(VQ3_EINVAL, "mlp: null x/out");
   if (!aligned(x, 16) || !aligned(out, 16)) return fail(VQ3_EALIGN, "mlp: x/out must be 16-byte aligned");
   PersistBufs b{};
+  if (norm) {
+    b.norm = 1;
+    b.res_delta = norm->res_delta;
+    b.res_out = norm->res_out;
+    b.eps = norm->eps;
+  }
   b.hbuf = reinterpret_cast<float*>(c.ws + c.w.hbuf);
   b.pieces1 = reinterpret_cast<float*>(c.ws + c.w.pieces1);
   b.pieces3 = reinterpret_cast<float*>(c.ws + c.w.pieces3);
@@ -678,6 +695,12 @@ int mlp_forward_capped(const uint16_t* x, int rows, const vq3_mlp_layer* layer, 
   cudaError_t e = run_persistent(x, rows, pass_tiles(rows, pass_cap), layer, nullptr, b, out, c.st);
   if (e != cudaSuccess) return cuda_fail(e, "mlp: launch");
   return ok();
+}
+}  // namespace
+
+int mlp_forward_capped(const uint16_t* x, int rows, const vq3_mlp_layer* layer, uint16_t* out, void* workspace,
+                       size_t ws_bytes, void* stream, int pass_cap) {
+  return mlp_forward_decode(x, rows, layer, out, workspace, ws_bytes, stream, pass_cap, nullptr);
 }
 
 }  // namespace vq3
@@ -713,6 +736,37 @@ int vq3_delta_rule_forward(const uint16_t* q, const uint16_t* k, const uint16_t*
   cudaError_t e = launch_delta_rule(q, k, v, beta, alpha, tokens, heads, d_k, d_v, state, out,
                                     static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "delta_rule: launch");
+  return ok();
+}
+
+int vq3_mlp_forward_residual(const uint16_t* r_in, const uint16_t* delta, int rows, const vq3_mlp_layer* layer,
+                             float eps, uint16_t* r_out, uint16_t* out, void* workspace, size_t ws_bytes,
+                             void* stream) {
+  if (rows < 0 || !(eps >= 0.f)) return fail(VQ3_EINVAL, "mlp_residual: rows=%d eps=%g", rows, eps);
+  int rc = check_mlp(layer);
+  if (rc) return rc;
+  if (rows == 0) return ok();
+  if (!r_in || !r_out || !out || !workspace) return fail(VQ3_EINVAL, "mlp_residual: null pointer");
+  if (r_out == r_in || (delta && r_out == delta) || out == r_in || out == r_out || (delta && out == delta))
+    return fail(VQ3_EINVAL, "mlp_residual: r_out and out must not alias r_in, delta or each other");
+  if (!aligned(r_in, 16) || !aligned(r_out, 16) || !aligned(out, 16) || (delta && !aligned(delta, 16)))
+    return fail(VQ3_EALIGN, "mlp_residual: pointers must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (rows < kPrefillRows) {
+    PersistBufs nb{};
+    nb.res_delta = delta;
+    nb.res_out = r_out;
+    nb.eps = eps;
+    return mlp_forward_decode(r_in, rows, layer, out, workspace, ws_bytes, stream, 32, &nb);
+  }
+  // many rows: the RMSNorm kernel writes r' and the normed rows (into out, which the block
+  // reads before it writes its result there), then the tensor-core path
+  const int H = layer->gate.d_in, I = layer->gate.d_out;
+  const size_t need = prefill_ws(rows, H, I, mlp_ctl_bytes(H, I)).total;
+  if (ws_bytes < need) return fail(VQ3_ENOSPACE, "mlp_residual: workspace %zu < %zu bytes", ws_bytes, need);
+  cudaError_t e = launch_residual_rmsnorm2(r_in, delta, r_out, rows, H, eps, out, st);
+  if (e == cudaSuccess) e = run_prefill_mlp(out, rows, *layer, static_cast<char*>(workspace), out, st);
+  if (e != cudaSuccess) return cuda_fail(e, "mlp_residual: launch");
   return ok();
 }
 

@@ -171,6 +171,8 @@ struct DecodeJob {
   size_t src_ld;
   int rows, block, chunk;   // valid rows; rotation block; chunk (whole blocks, columns)
   const uint32_t* signs;
+  const float* inv;         // RMSNorm of the source rows: per-row 1/rms (shared memory), or null
+  const uint16_t* res_delta;  // with inv: the residual delta added to the source first, or null
   const unsigned* ready;    // per chunk: complete when >= ready_target (null: ready at launch)
   unsigned ready_target;
   unsigned* group_done;     // per segment group: +1 per CTA whose pieces of the group are written
@@ -271,6 +273,22 @@ __device__ __forceinline__ void fwht_smem(float* buf, int n, int block) {
 
 __device__ __forceinline__ float load1(const uint16_t* p) { return __half2float(__ushort_as_half(__ldg(p))); }
 __device__ __forceinline__ float load1(const float* p) { return __ldcg(p); }
+__device__ __forceinline__ float round16(float v) { return __half2float(__float2half_rn(v)); }
+
+// Source element (row, col) of the stage: for a normed source the pre-norm residual step
+// fp16(fp16(x + delta) * inv[row]), else the element itself.
+template <typename T>
+__device__ __forceinline__ float act(const DecodeJob& a, const T* src, int row, int col) {
+  const size_t o = (size_t)row * a.src_ld + col;
+  float v = load1(src + o);
+  if constexpr (sizeof(T) == 2) {
+    if (a.inv) {
+      if (a.res_delta) v = round16(v + load1(a.res_delta + o));
+      v = round16(v * a.inv[row]);
+    }
+  }
+  return v;
+}
 
 __device__ __forceinline__ bool sign_bit(const uint32_t* signs, int col) {
   return (__ldg(signs + (col >> 5)) >> (col & 31)) & 1u;
@@ -306,6 +324,22 @@ __device__ __forceinline__ void stage_round(const DecodeJob& a, const T* src, lo
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = load1(s + 32 * j + lane);
+        if constexpr (sizeof(T) == 2) {
+          if (a.inv) {
+            // pre-norm residual step: fp16(fp16(x + delta) * inv[row]), its loads after x's
+            const float iv = a.inv[row];
+            if (a.res_delta) {
+              const uint16_t* sd = a.res_delta + (size_t)row * a.src_ld + c * 1024;
+              float dl[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) dl[j] = load1(sd + 32 * j + lane);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = round16(v[j] + dl[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = round16(v[j] * iv);
+          }
+        }
         if (a.signs) {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
@@ -341,7 +375,7 @@ __device__ __forceinline__ void stage_round(const DecodeJob& a, const T* src, lo
       if (nr <= 0) break;
       for (int e = threadIdx.x; e < nr * a.chunk; e += kThreads) {
         const int rr = e / a.chunk, col = c * a.chunk + e % a.chunk;
-        float v = load1(src + (size_t)(nt * 8 + rr) * a.src_ld + col);
+        float v = act(a, src, nt * 8 + rr, col);
         if (a.signs && sign_bit(a.signs, col)) v = -v;
         buf[e] = v;
       }
@@ -746,6 +780,7 @@ template <int NT, int F>
 __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) {
   extern __shared__ __align__(16) unsigned char dsm[];
   __shared__ int s_flag;
+  __shared__ float s_inv[32];  // 1/rms of the pass's rows (pre-norm residual step)
   SmemView sv;
   const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(dsm));
   sv.ring = base;
@@ -773,6 +808,8 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
   j1.block = a.block_in;
   j1.chunk = a.x_chunk;
   j1.signs = a.signs_in;
+  j1.inv = a.norm ? s_inv : nullptr;
+  j1.res_delta = (a.norm && a.res_delta) ? a.res_delta + (size_t)a.row0 * a.d_model : nullptr;
   j1.ready = nullptr;
   j1.ready_target = 0;
   j1.group_done = ctl + (a.mlp ? a.off_g : a.off_o);
@@ -781,6 +818,43 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
   // one cell's index copies, then the rotation of x (its loads not queued behind
   // the bulk of the prologue), then the rest of the prologue
   Cursor cur = decode_begin<F>(j1, sv, 1);
+  if (a.norm) {
+    // pre-norm residual step for the pass's rows: r' = fp16(x + delta) over the whole row
+    // (every CTA, for its own 1/rms), the 64-column slices s with s % grid == CTA written to
+    // res_out; one warp per row, lanes over 8-column groups, a fixed reduction order
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, d = a.d_model;
+    for (int rr = warp; rr < a.rows; rr += kWarps) {
+      const size_t ro = (size_t)(a.row0 + rr) * d;
+      float ss = 0.f;
+      for (int c8 = lane * 8; c8 < d; c8 += 256) {
+        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(a.x + ro + c8));
+        uint4 rv = xv;
+        if (a.res_delta) {
+          const uint4 dv = __ldg(reinterpret_cast<const uint4*>(a.res_delta + ro + c8));
+          const __half2* xh = reinterpret_cast<const __half2*>(&xv);
+          const __half2* dh = reinterpret_cast<const __half2*>(&dv);
+          __half2* rh = reinterpret_cast<__half2*>(&rv);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 xf = __half22float2(xh[k]), df = __half22float2(dh[k]);
+            rh[k] = __floats2half2_rn(xf.x + df.x, xf.y + df.y);
+          }
+        }
+        const __half2* rh = reinterpret_cast<const __half2*>(&rv);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = __half22float2(rh[k]);
+          ss = fmaf(f.x, f.x, ss);
+          ss = fmaf(f.y, f.y, ss);
+        }
+        if ((c8 / 64) % (int)gridDim.x == (int)blockIdx.x) *reinterpret_cast<uint4*>(a.res_out + ro + c8) = rv;
+      }
+#pragma unroll
+      for (int h = 16; h > 0; h >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, h);
+      if (lane == 0) s_inv[rr] = 1.0f / sqrtf(ss / (float)d + a.eps);
+    }
+    __syncthreads();
+  }
   decode_run<F, NT, uint16_t>(j1, a.x + (size_t)a.row0 * a.d_model, cur, sv, status);
 
   if (a.mlp) {

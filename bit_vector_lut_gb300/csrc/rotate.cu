@@ -105,18 +105,21 @@ cudaError_t launch_b(const T* x, int rows, int n, const uint32_t* signs, uint16_
   return cudaGetLastError();
 }
 
-// resid <- fp16(resid + delta); normed <- fp16(resid * rsqrt(mean(resid^2) + eps))
-__global__ void __launch_bounds__(256) residual_rmsnorm_kernel(uint16_t* resid, const uint16_t* delta, int n,
-                                                               float eps, uint16_t* normed) {
+// resid_out <- fp16(resid_in + delta); normed <- fp16(resid_out * rsqrt(mean(resid_out^2) + eps))
+__global__ void __launch_bounds__(256) residual_rmsnorm_kernel(const uint16_t* resid_in, const uint16_t* delta,
+                                                               uint16_t* resid_out, int n, float eps,
+                                                               uint16_t* normed) {
   __shared__ float red[8];
   const size_t base = (size_t)blockIdx.x * n;
   float ss = 0.f;
   for (int j = threadIdx.x; j < n; j += blockDim.x) {
-    float r = __half2float(__ushort_as_half(resid[base + j]));
+    float r = __half2float(__ushort_as_half(resid_in[base + j]));
     if (delta) {
       const __half s = __float2half_rn(r + __half2float(__ushort_as_half(delta[base + j])));
-      resid[base + j] = __half_as_ushort(s);
+      resid_out[base + j] = __half_as_ushort(s);
       r = __half2float(s);
+    } else if (resid_out != resid_in) {
+      resid_out[base + j] = resid_in[base + j];
     }
     ss += r * r;
   }
@@ -128,7 +131,8 @@ __global__ void __launch_bounds__(256) residual_rmsnorm_kernel(uint16_t* resid, 
   for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
   const float inv = 1.0f / sqrtf(tot / (float)n + eps);
   for (int j = threadIdx.x; j < n; j += blockDim.x) {
-    const float r = __half2float(__ushort_as_half(resid[base + j]));
+    // the same thread wrote resid_out[base + j] above
+    const float r = __half2float(__ushort_as_half(resid_out[base + j]));
     normed[base + j] = __half_as_ushort(__float2half_rn(r * inv));
   }
 }
@@ -167,7 +171,13 @@ cudaError_t launch_fwht_f32(const float* x, int rows, int n, int block, const ui
 
 cudaError_t launch_residual_rmsnorm(uint16_t* resid, const uint16_t* delta, int rows, int n, float eps,
                                     uint16_t* normed, cudaStream_t st) {
-  residual_rmsnorm_kernel<<<rows, 256, 0, st>>>(resid, delta, n, eps, normed);
+  residual_rmsnorm_kernel<<<rows, 256, 0, st>>>(resid, delta, resid, n, eps, normed);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_residual_rmsnorm2(const uint16_t* resid_in, const uint16_t* delta, uint16_t* resid_out, int rows,
+                                     int n, float eps, uint16_t* normed, cudaStream_t st) {
+  residual_rmsnorm_kernel<<<rows, 256, 0, st>>>(resid_in, delta, resid_out, n, eps, normed);
   return cudaGetLastError();
 }
 

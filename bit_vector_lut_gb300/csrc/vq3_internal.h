@@ -106,6 +106,13 @@ struct PersistArgs {
   int format;               // VQ3_FORMAT_* of every matrix
   const float* lr_y;        // low-rank correction U V x' [rows][d_out] FP32 for all rows of the
                             // call (linear layer only), or null
+  // pre-norm residual step fused ahead of the block (MLP only): the block's input rows are
+  // fp16(r' / sqrt(mean(r'^2) + eps)) with r' = fp16(x + res_delta) (x alone when res_delta is
+  // null), and r' is written to res_out (which aliases neither x nor res_delta)
+  int norm;
+  const uint16_t* res_delta;
+  uint16_t* res_out;
+  float eps;
   int d_model, d_inter;     // MLP: hidden and intermediate widths; linear: d_model = d_in
   int d_model_out;          // linear: d_out
   int block_in, block_dn;   // rotation blocks of the gate/up (or linear) input and of the down input
@@ -169,6 +176,9 @@ size_t prefill_part_bytes(int rows);  // size of PrefillArgs::part
 cudaError_t launch_prefill_gemm(const PrefillArgs& a, cudaStream_t st);
 cudaError_t launch_residual_rmsnorm(uint16_t* resid, const uint16_t* delta, int rows, int n,
                                     float eps, uint16_t* normed, cudaStream_t st);
+// The same with the updated residual written to resid_out (may equal resid_in).
+cudaError_t launch_residual_rmsnorm2(const uint16_t* resid_in, const uint16_t* delta, uint16_t* resid_out, int rows,
+                                     int n, float eps, uint16_t* normed, cudaStream_t st);
 cudaError_t launch_dequant(const vq3_linear& L, int apply_scale, uint16_t* w_out, cudaStream_t st);
 // Gated delta-rule token mixer over blocks of 8 tokens (layouts as vq3_delta_rule_forward).
 cudaError_t launch_delta_rule(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* beta,

@@ -68,6 +68,8 @@ def _load() -> ctypes.CDLL:
         "vq3_dequant_dense": (c_int, [POINTER(vq3_linear), c_int, c_void_p, c_void_p]),
         "vq3_delta_rule_forward": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
                                            c_int, c_void_p, c_void_p, c_void_p]),
+        "vq3_mlp_forward_residual": (c_int, [c_void_p, c_void_p, c_int, POINTER(vq3_mlp_layer), c_float, c_void_p,
+                                             c_void_p, c_void_p, c_size_t, c_void_p]),
         "vq3_last_error": (ctypes.c_char_p, []),
         "vq3_version": (ctypes.c_char_p, []),
     }
@@ -293,4 +295,15 @@ def delta_rule_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: 
         out = torch.empty((tokens, heads, d_v), dtype=torch.float16, device=q.device)
     _check(lib.vq3_delta_rule_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr(), alpha.data_ptr(),
                                       tokens, heads, d_k, d_v, state.data_ptr(), out.data_ptr(), _stream(stream)))
+    return out
+
+
+def mlp_forward_residual(r_in: torch.Tensor, delta: torch.Tensor | None, layer: MLP, r_out: torch.Tensor,
+                         out: torch.Tensor, eps: float = 1e-6, ws=None, stream=None) -> torch.Tensor:
+    """One pre-norm residual layer: r_out = fp16(r_in + delta); out = MLP(RMSNorm(r_out))."""
+    rows = r_in.shape[0]
+    if ws is None:
+        ws = workspace(mlp_workspace_bytes(rows, layer), r_in.device, stream)
+    _check(lib.vq3_mlp_forward_residual(r_in.data_ptr(), _ptr(delta), rows, ctypes.byref(layer.struct), eps,
+                                        r_out.data_ptr(), out.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
     return out

@@ -236,6 +236,20 @@ VQ3_API int vq3_delta_rule_forward(const uint16_t* q, const uint16_t* k, const u
                                    const float* alpha, int tokens, int heads, int d_k, int d_v, float* state,
                                    uint16_t* out, void* stream);
 
+/*
+ * One layer of the pre-norm residual stack: r' = fp16(r_in + delta) (r_in alone when
+ * delta is NULL), n = fp16(r' / sqrt(mean(r'^2) + eps)) per row, out = the MLP block
+ * of n (as vq3_mlp_forward); r' is written to r_out. Up to 16 rows the residual
+ * step runs inside the block's kernel (each CTA computes the rows' RMS; the gate/up
+ * rotation normalises on the fly), from 17 rows on as a separate kernel. r_in,
+ * delta: device FP16 [rows][d]; r_out, out: device FP16 [rows][d], aliasing neither
+ * each other nor r_in or delta (callers alternate two residual buffers). Workspace
+ * as vq3_mlp_forward. Errors as vq3_mlp_forward.
+ */
+VQ3_API int vq3_mlp_forward_residual(const uint16_t* r_in, const uint16_t* delta, int rows,
+                                     const vq3_mlp_layer* layer, float eps, uint16_t* r_out, uint16_t* out,
+                                     void* workspace, size_t ws_bytes, void* stream);
+
 /* Number of kernels one vq3_mlp_forward call launches at `rows` rows: one per
  * pass of 8 or 16 rows below 17 rows, 4 from 17 rows on (-1 on a bad
  * descriptor). */
