@@ -254,6 +254,9 @@ cudaError_t run_persistent(const uint16_t* x, int rows, int nt, const vq3_mlp_la
     a.max_pieces1 = persist_max_pieces(L->d_in, L->d_out, 1, a.grid1);
     c = ctl_linear(L->d_in, L->d_out);
   }
+  if (layer ? !(persist_cells_fit(a.d_model, a.d_inter, 2, a.grid1) && persist_cells_fit(a.d_inter, a.d_model, 1, a.grid3))
+            : !persist_cells_fit(a.d_model, a.d_model_out, 1, a.grid1))
+    return cudaErrorInvalidValue;
   a.n_ctl = c.n;
   a.off_g = c.off_g;
   a.off_hd = c.off_hd;

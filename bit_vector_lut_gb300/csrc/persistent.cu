@@ -115,13 +115,15 @@ __device__ __forceinline__ uint4 lds128(uint32_t saddr) {
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
-__device__ __forceinline__ long long range_begin(long long cells, int grid, int b) {
-  return (long long)b * cells / grid;
+// 32-bit unsigned arithmetic throughout (the launcher checks cells * grid < 2^32):
+// these run on the path between steps, where a 64-bit division costs microseconds.
+__device__ __forceinline__ int range_begin(int cells, int grid, int b) {
+  return (int)((unsigned)b * (unsigned)cells / (unsigned)grid);
 }
 
 // CTA owning cell x (largest b with range_begin(b) <= x).
-__device__ __forceinline__ int cta_of(long long x, long long cells, int grid) {
-  return (int)(((x + 1) * grid - 1) / cells);
+__device__ __forceinline__ int cta_of(int x, int cells, int grid) {
+  return (int)((((unsigned)x + 1u) * (unsigned)grid - 1u) / (unsigned)cells);
 }
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -180,10 +182,10 @@ struct DecodeJob {
   __device__ int n_kg() const { return d_in / kSuInputs; }
   __device__ int n_seg() const { return (d_out / kSuChannels) * n_mats; }
   __device__ int n_grp() const { return (n_seg() + kWarps - 1) / kWarps; }
-  __device__ long long cells() const { return (long long)n_grp() * n_kg(); }
+  __device__ int cells() const { return n_grp() * n_kg(); }
   // CTAs that write pieces of segment group g (slots 0 .. count-1)
   __device__ int contributors(int g) const {
-    const long long x0 = (long long)g * n_kg();
+    const int x0 = g * n_kg();
     return cta_of(x0 + n_kg() - 1, cells(), grid) - cta_of(x0, cells(), grid) + 1;
   }
   __device__ const float* seg_pieces(int sg, int piece_floats) const {
@@ -297,7 +299,8 @@ __device__ __forceinline__ bool sign_bit(const uint32_t* signs, int col) {
 // Offset in the round's window of chunk c's first column group, and whether the
 // chunk holds any of the window's column groups (kg_s .. kg_s + len - 1, cyclic).
 __device__ __forceinline__ bool chunk_in_window(int c, int ckg, int kg_s, int len, int n_kg) {
-  const int d0 = (c * ckg - kg_s + n_kg) % n_kg;
+  int d0 = c * ckg - kg_s;  // in (-n_kg, n_kg)
+  if (d0 < 0) d0 += n_kg;
   return d0 < len || d0 + ckg > n_kg;
 }
 
@@ -305,11 +308,10 @@ __device__ __forceinline__ bool chunk_in_window(int c, int ckg, int kg_s, int le
 // slot's column group, rows < a.rows (other rows are left as they are: an MMA
 // column depends on its own B column only, and their outputs are never stored).
 template <int NT, typename T>
-__device__ __forceinline__ void stage_round(const DecodeJob& a, const T* src, long long rs, int len, const SmemView& sv) {
+__device__ __forceinline__ void stage_round(const DecodeJob& a, const T* src, int kg_s, int len, const SmemView& sv) {
   const int n_kg = a.n_kg();
   const int ckg = a.chunk / kSuInputs;
   const int n_chunks = n_kg / ckg;
-  const int kg_s = (int)(rs % n_kg);
   const float scale = 1.0f / sqrtf((float)a.block);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (a.chunk == 1024) {
@@ -354,7 +356,7 @@ __device__ __forceinline__ void stage_round(const DecodeJob& a, const T* src, lo
         __syncwarp();
         fwht32(v, a.block);  // column strides 1 .. min(block, 32)/2
         const int kg = c * ckg + (lane >> 1), h = lane & 1, nt = row >> 3, g = row & 7;
-        for (int p = (kg - kg_s + n_kg) % n_kg; p < len; p += n_kg)
+        for (int p = kg - kg_s < 0 ? kg - kg_s + n_kg : kg - kg_s; p < len; p += n_kg)
 #pragma unroll
           for (int t = 0; t < 4; ++t)
             sts128(stage_chunk_addr(sv.stage, p, NT, nt, h * 32 + 4 * g + t),
@@ -386,7 +388,7 @@ __device__ __forceinline__ void stage_round(const DecodeJob& a, const T* src, lo
         const int rr = e / (ckg * 8), kl = (e / 8) % ckg, h = (e / 4) & 1, t = e & 3;
         const float* r = buf + rr * a.chunk + kl * 64 + 32 * h + 2 * t;
         const int kg = c * ckg + kl;
-        for (int p = (kg - kg_s + n_kg) % n_kg; p < len; p += n_kg)
+        for (int p = kg - kg_s < 0 ? kg - kg_s + n_kg : kg - kg_s; p < len; p += n_kg)
           sts128(stage_chunk_addr(sv.stage, p, NT, nt, h * 32 + 4 * rr + t), pack_half2(r[0] * scale, r[1] * scale),
                  pack_half2(r[8] * scale, r[9] * scale), pack_half2(r[16] * scale, r[17] * scale),
                  pack_half2(r[24] * scale, r[25] * scale));
@@ -501,8 +503,8 @@ struct Ring {
   static constexpr int kWarpBytes = kSlots * kSlotBytes;
 };
 
-__device__ __forceinline__ void cell_range(const DecodeJob& a, long long& c0, long long& c1) {
-  const long long cells = a.cells();
+__device__ __forceinline__ void cell_range(const DecodeJob& a, int& c0, int& c1) {
+  const int cells = a.cells();
   c0 = range_begin(cells, a.grid, blockIdx.x);
   c1 = range_begin(cells, a.grid, blockIdx.x + 1);
 }
@@ -544,10 +546,10 @@ template <int F>
 __device__ __forceinline__ Cursor decode_begin(const DecodeJob& a, const SmemView& sv, int n) {
   Cursor cur{nullptr, 0, 0, 0, 0u, false};
   if ((int)blockIdx.x >= a.grid) return cur;
-  long long c0, c1;
+  int c0, c1;
   cell_range(a, c0, c1);
   cur.left = (int)(c1 - c0);
-  cursor_group<F>(a, cur, (int)(c0 / a.n_kg()), (int)(c0 % a.n_kg()));
+  cursor_group<F>(a, cur, c0 / a.n_kg(), c0 % a.n_kg());
   const uint32_t ring_lane = sv.ring + (uint32_t)((threadIdx.x >> 5) * Ring<F>::kWarpBytes + (threadIdx.x & 31) * 16);
   for (int k = 0; k < n; ++k) issue_cell<F>(a, cur, ring_lane);
   return cur;
@@ -563,7 +565,7 @@ __device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cur
   if ((int)blockIdx.x >= a.grid) return;  // uniform over the CTA
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n_kg = a.n_kg(), n_seg = a.n_seg();
-  long long c0, c1;
+  int c0, c1;
   cell_range(a, c0, c1);
   const uint32_t ring = sv.ring + (uint32_t)(warp * Ring<F>::kWarpBytes);
   constexpr uint32_t kSlot = (uint32_t)Ring<F>::kSlotBytes;
@@ -571,7 +573,7 @@ __device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cur
   const bool two = a.n_mats > 1;
   uint32_t use_slot = 0;  // ring slot of the next cell to compute
   int issued = (int)(c1 - c0) - cur.left;  // copies issued so far (the prologue)
-  int g = (int)(c0 / n_kg), kg = (int)(c0 % n_kg);  // group and column group of the next cell
+  int g = c0 / n_kg, kg = c0 % n_kg;  // group and column group of the next cell
   float acc[4][NT][4];
   uint32_t lane_base = 0;
   bool live = false;
@@ -579,18 +581,18 @@ __device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cur
   const int total = (int)(c1 - c0);
   int first = 1;  // the next cell starts the range's part of a group
   for (int r0 = 0; r0 < total; r0 += KS) {
-    const long long rs = c0 + r0;
+    const int kg_s = kg;  // column group of the round's first cell
     const int len = total - r0 < KS ? total - r0 : KS;
     if (a.ready) {
       // the chunks of the round's column groups must be complete
       if (tid == 0) {
-        const int ckg = a.chunk / kSuInputs, kg_s = (int)(rs % n_kg);
+        const int ckg = a.chunk / kSuInputs;
         for (int c = 0; c < n_kg / ckg; ++c)
           if (chunk_in_window(c, ckg, kg_s, len, n_kg)) poll_geq(a.ready + c, a.ready_target, status);
       }
       __syncthreads();  // thread 0's acquire loads, then the barrier: the chunks are visible to the CTA
     }
-    stage_round<NT, T>(a, src, rs, len, sv);
+    stage_round<NT, T>(a, src, kg_s, len, sv);
     for (; issued < kSlots; ++issued) issue_cell<F>(a, cur, ring_lane);  // rest of the prologue
     __syncthreads();
     for (int p = 0; p < len; ++p) {
@@ -614,7 +616,7 @@ __device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cur
       if (first || r0 + p + 1 == total) {
         // this warp's segment over the range's part of group g: one piece
         if (live) {
-          const int piece = blockIdx.x - cta_of((long long)g * n_kg, a.cells(), a.grid);
+          const int piece = blockIdx.x - cta_of(g * n_kg, a.cells(), a.grid);
           float* pc = a.pieces + ((size_t)sg * a.max_pieces + piece) * PIECE;
 #pragma unroll
           for (int m = 0; m < 4; ++m)
@@ -655,6 +657,19 @@ __device__ __forceinline__ void swiglu_tasks(const PersistArgs& a, const DecodeJ
     const bool two = m1 < n_mg;
     const int g0 = (2 * m0) / kWarps, g1 = two ? (2 * m1) / kWarps : g0;  // groups of segments 2m, 2m+1
     const int n0 = gu.contributors(g0), n1 = two ? gu.contributors(g1) : 0;
+    // the scales are inputs: their loads go out before the wait
+    float sc[NT][2][2];
+#pragma unroll
+    for (int q = 0; q < NT; ++q) {
+      int r, c;
+      item_pos<NT>(q * 512 + threadIdx.x, r, c);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int ch = (k && two ? m1 : m0) * kSuChannels + c;
+        sc[q][k][0] = __half2float(__ushort_as_half(__ldg(a.gate.scales + ch)));
+        sc[q][k][1] = __half2float(__ushort_as_half(__ldg(a.up.scales + ch)));
+      }
+    }
     if (threadIdx.x == 0) {
       poll_geq(gu.group_done + g0, (unsigned)n0, status);
       if (two) poll_geq(gu.group_done + g1, (unsigned)n1, status);
@@ -695,9 +710,7 @@ __device__ __forceinline__ void swiglu_tasks(const PersistArgs& a, const DecodeJ
         for (int k = 0; k < 2; ++k) {
           if (k == 1 && !two) break;
           const int ch = (k ? m1 : m0) * kSuChannels + c;
-          const float sgv = __half2float(__ushort_as_half(a.gate.scales[ch]));
-          const float suv = __half2float(__ushort_as_half(a.up.scales[ch]));
-          __stcg(a.hbuf + (size_t)r * a.d_inter + ch, silu_f(sgv * s[2 * k]) * (suv * s[2 * k + 1]));
+          __stcg(a.hbuf + (size_t)r * a.d_inter + ch, silu_f(sc[q][k][0] * s[2 * k]) * (sc[q][k][1] * s[2 * k + 1]));
         }
       }
     }
@@ -715,12 +728,18 @@ __device__ __forceinline__ void output_tasks(const PersistArgs& a, const DecodeJ
     const int sg = t / NT, part = t % NT;
     const int g = sg / kWarps;
     const int count = j.contributors(g);
+    // the scale and the low-rank term are inputs: their loads go out before the wait
+    const int it = part * 512 + threadIdx.x;
+    int r, c;
+    item_pos<NT>(it, r, c);
+    const int ch = sg * kSuChannels + c;
+    const float sc = __half2float(__ushort_as_half(__ldg(j.scales0 + ch)));
+    const float lr = (a.lr_y && r < a.rows) ? __ldg(a.lr_y + (size_t)(a.row0 + r) * j.d_out + ch) : 0.f;
     if (threadIdx.x == 0) {
       poll_geq(j.group_done + g, (unsigned)count, status);
       __threadfence();
     }
     __syncthreads();
-    const int it = part * 512 + threadIdx.x;
     const float* base = j.seg_pieces(sg, PIECE) + it;
     float y = 0.f;
     for (int q0 = 0; q0 < count; q0 += P) {
@@ -730,13 +749,9 @@ __device__ __forceinline__ void output_tasks(const PersistArgs& a, const DecodeJ
 #pragma unroll
       for (int q = 0; q < P; ++q) y += v[q];
     }
-    int r, c;
-    item_pos<NT>(it, r, c);
     if (r < a.rows) {
-      const int ch = sg * kSuChannels + c;
-      const float s = __half2float(__ushort_as_half(j.scales0[ch]));
-      float v = s * y;
-      if (a.lr_y) v += __ldg(a.lr_y + (size_t)(a.row0 + r) * j.d_out + ch);  // low-rank correction
+      float v = sc * y;
+      if (a.lr_y) v += lr;  // low-rank correction
       a.out[(size_t)(a.row0 + r) * j.d_out + ch] = __half_as_ushort(__float2half_rn(v));
     }
   }
@@ -970,6 +985,12 @@ int persist_decode_grid(int d_in, int d_out, int n_mats, int grid) {
   const int n_seg = (d_out / kSuChannels) * n_mats;
   const long long cells = (long long)((n_seg + kDecWarps - 1) / kDecWarps) * (d_in / kSuInputs);
   return cells < grid ? (int)cells : grid;  // every decoding CTA owns at least one cell
+}
+
+bool persist_cells_fit(int d_in, int d_out, int n_mats, int grid) {
+  const long long n_seg = (long long)(d_out / kSuChannels) * n_mats;
+  const long long cells = (n_seg + kDecWarps - 1) / kDecWarps * (d_in / kSuInputs);
+  return cells * grid < (1ll << 32);  // the kernel's cell arithmetic is 32-bit unsigned
 }
 
 int persist_max_pieces(int d_in, int d_out, int n_mats, int grid) {

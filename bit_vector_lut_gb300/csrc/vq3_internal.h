@@ -137,6 +137,8 @@ struct PersistArgs {
 int persist_grid(int nt);  // CTAs of the persistent kernel: resident CTAs per SM x SMs
 int persist_decode_grid(int d_in, int d_out, int n_mats, int grid);  // decoding CTAs (<= cells)
 int persist_max_pieces(int d_in, int d_out, int n_mats, int grid);
+// Whether the decode kernel's 32-bit cell arithmetic holds (cells x grid < 2^32).
+bool persist_cells_fit(int d_in, int d_out, int n_mats, int grid);
 int persist_chunk(int d, int block);  // rotation chunk: whole blocks, up to 1024 columns
 cudaError_t launch_persistent(const PersistArgs& a, int nt, cudaStream_t st);
 
