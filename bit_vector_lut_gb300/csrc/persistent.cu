@@ -296,13 +296,17 @@ __device__ __forceinline__ bool sign_bit(const uint32_t* signs, int col) {
   return (__ldg(signs + (col >> 5)) >> (col & 31)) & 1u;
 }
 
-// Offset in the round's window of chunk c's first column group, and whether the
-// chunk holds any of the window's column groups (kg_s .. kg_s + len - 1, cyclic).
-__device__ __forceinline__ bool chunk_in_window(int c, int ckg, int kg_s, int len, int n_kg) {
-  int d0 = c * ckg - kg_s;  // in (-n_kg, n_kg)
-  if (d0 < 0) d0 += n_kg;
-  return d0 < len || d0 + ckg > n_kg;
-}
+// The chunks that hold the round's column groups kg_s .. kg_s + len - 1 (cyclic over
+// n_chunks chunks of ckg column groups): n of them, from chunk first on, each once.
+struct Window {
+  int first, n, n_chunks;
+  __device__ Window(int kg_s, int len, int ckg, int n_chunks_) : n_chunks(n_chunks_) {
+    first = kg_s / ckg;
+    n = (kg_s - first * ckg + len + ckg - 1) / ckg;
+    if (n > n_chunks) n = n_chunks;
+  }
+  __device__ int chunk(int i) const { return first + i < n_chunks ? first + i : first + i - n_chunks; }
+};
 
 // Writes the stage slots of round [rs, rs + len): the rotated activations of each
 // slot's column group, rows < a.rows (other rows are left as they are: an MMA
@@ -318,8 +322,9 @@ __device__ __forceinline__ void stage_round(const DecodeJob& a, const T* src, in
     // one (chunk, row) per warp: lane L holds columns L + 32 j, then 32 L + c
     float* m = sv.scratch + warp * 1024;
     int item = 0;
-    for (int c = 0; c < n_chunks; ++c) {
-      if (!chunk_in_window(c, ckg, kg_s, len, n_kg)) continue;
+    const Window win(kg_s, len, ckg, n_chunks);
+    for (int i = 0; i < win.n; ++i) {
+      const int c = win.chunk(i);
       for (int row = 0; row < a.rows; ++row, ++item) {
         if ((item & (kWarps - 1)) != warp) continue;
         const T* s = src + (size_t)row * a.src_ld + c * 1024;
@@ -370,8 +375,9 @@ __device__ __forceinline__ void stage_round(const DecodeJob& a, const T* src, in
   }
   // smaller chunks: CTA-wide butterflies over [8 rows][chunk] fp32 in the scratch
   float* buf = sv.scratch;
-  for (int c = 0; c < n_chunks; ++c) {
-    if (!chunk_in_window(c, ckg, kg_s, len, n_kg)) continue;
+  const Window win(kg_s, len, ckg, n_chunks);
+  for (int i = 0; i < win.n; ++i) {
+    const int c = win.chunk(i);
     for (int nt = 0; nt < NT; ++nt) {
       const int nr = a.rows - nt * 8 < 8 ? a.rows - nt * 8 : 8;
       if (nr <= 0) break;
@@ -483,6 +489,49 @@ __device__ __forceinline__ void compute_cell(uint32_t slot, uint32_t xb, int lan
   kstep<F, 3, NT>(w, lanebase, acc, b);
 }
 
+// Lane-private tables: entry k of matrix t replicated into words k*32 .. k*32+31
+// at tab + t * stride, written 4 lanes (16 bytes) at a time. A vector format's
+// codebook word k is (component 0 | component 1 << 16); a scalar entry is
+// stored as (entry | entry << 16). The codebook loads go out at kernel start and
+// the stores follow the first rotation, so that their latencies overlap.
+template <int F>
+struct TableLoad {
+  static constexpr int E = Fmt<F>::kEntries;
+  static constexpr int kItems = 3 * E * 8;
+  static constexpr int kPer = (kItems + kThreads - 1) / kThreads;
+  const uint32_t* cb[3];
+  uint32_t v[kPer];
+  __device__ void load(const uint32_t* cb0, const uint32_t* cb1, const uint32_t* cb2) {
+    cb[0] = cb0;
+    cb[1] = cb1;
+    cb[2] = cb2;
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+      const int i = threadIdx.x + r * kThreads;
+      const int t = i / (E * 8), k = (i >> 3) % E;
+      const uint32_t* p = t == 0 ? cb[0] : (t == 1 ? cb[1] : cb[2]);
+      v[r] = 0u;
+      if (i < kItems && p) {
+        if constexpr (Fmt<F>::kVec == 2) {
+          v[r] = __ldg(p + k);
+        } else {
+          const uint32_t h = __ldg(reinterpret_cast<const uint16_t*>(p) + k);
+          v[r] = h | (h << 16);
+        }
+      }
+    }
+  }
+  __device__ void store(uint32_t tab) const {
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+      const int i = threadIdx.x + r * kThreads;
+      const int t = i / (E * 8), k = (i >> 3) % E, q = i & 7;
+      const uint32_t* p = t == 0 ? cb[0] : (t == 1 ? cb[1] : cb[2]);
+      if (i < kItems && p) sts128(tab + (uint32_t)(t * Tab<F>::kStride + k * 128 + q * 16), v[r], v[r], v[r], v[r]);
+    }
+  }
+};
+
 // Index-copy cursor of one warp: the next cell of its CTA's range whose copies
 // are to be issued. All of it advances by increments; the group-dependent parts
 // are recomputed only when a group ends.
@@ -559,10 +608,13 @@ __device__ __forceinline__ Cursor decode_begin(const DecodeJob& a, const SmemVie
 // 1 .. kSlots cells, the rest of the prologue follows the first stage.
 template <int F, int NT, typename T>
 __device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cursor& cur, const SmemView& sv,
-                                           int* status) {
+                                           const TableLoad<F>* tables, int* status) {
   constexpr int PIECE = 512 * NT;
   constexpr int KS = StageCfg<NT>::kSlots;
-  if ((int)blockIdx.x >= a.grid) return;  // uniform over the CTA
+  if ((int)blockIdx.x >= a.grid) {  // uniform over the CTA
+    if (tables) tables->store(sv.tab);  // for a later job; its first barrier orders them
+    return;
+  }
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n_kg = a.n_kg(), n_seg = a.n_seg();
   int c0, c1;
@@ -587,12 +639,13 @@ __device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cur
       // the chunks of the round's column groups must be complete
       if (tid == 0) {
         const int ckg = a.chunk / kSuInputs;
-        for (int c = 0; c < n_kg / ckg; ++c)
-          if (chunk_in_window(c, ckg, kg_s, len, n_kg)) poll_geq(a.ready + c, a.ready_target, status);
+        const Window win(kg_s, len, ckg, n_kg / ckg);
+        for (int i = 0; i < win.n; ++i) poll_geq(a.ready + win.chunk(i), a.ready_target, status);
       }
       __syncthreads();  // thread 0's acquire loads, then the barrier: the chunks are visible to the CTA
     }
     stage_round<NT, T>(a, src, kg_s, len, sv);
+    if (tables && r0 == 0) tables->store(sv.tab);  // ordered before the decode by the barrier below
     for (; issued < kSlots; ++issued) issue_cell<F>(a, cur, ring_lane);  // rest of the prologue
     __syncthreads();
     for (int p = 0; p < len; ++p) {
@@ -768,29 +821,6 @@ struct Smem {
   static constexpr uint32_t kTotal = kRing + kStage + kScratch + Tab<F>::kAlign + kTabs;
 };
 
-// Lane-private tables: entry k of matrix t replicated into words k*32 .. k*32+31
-// at tab + t * stride, written 4 lanes (16 bytes) at a time. A vector format's
-// codebook word k is (component 0 | component 1 << 16); a scalar entry is
-// stored as (entry | entry << 16).
-template <int F>
-__device__ void load_tables(uint32_t tab, const uint32_t* cb0, const uint32_t* cb1, const uint32_t* cb2) {
-  constexpr int E = Fmt<F>::kEntries;
-  for (int i = threadIdx.x; i < 3 * E * 8; i += kThreads) {
-    const int t = i / (E * 8), k = (i >> 3) % E, q = i & 7;
-    const uint32_t* cb = t == 0 ? cb0 : (t == 1 ? cb1 : cb2);
-    if (cb) {
-      uint32_t v;
-      if constexpr (Fmt<F>::kVec == 2) {
-        v = __ldg(cb + k);
-      } else {
-        const uint32_t h = __ldg(reinterpret_cast<const uint16_t*>(cb) + k);
-        v = h | (h << 16);
-      }
-      sts128(tab + (uint32_t)(t * Tab<F>::kStride + k * 128 + q * 16), v, v, v, v);
-    }
-  }
-}
-
 template <int NT, int F>
 __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) {
   extern __shared__ __align__(16) unsigned char dsm[];
@@ -829,7 +859,8 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
   j1.ready_target = 0;
   j1.group_done = ctl + (a.mlp ? a.off_g : a.off_o);
 
-  load_tables<F>(sv.tab, a.gate.codebook, a.mlp ? a.up.codebook : nullptr, a.mlp ? a.down.codebook : nullptr);
+  TableLoad<F> tables;
+  tables.load(a.gate.codebook, a.mlp ? a.up.codebook : nullptr, a.mlp ? a.down.codebook : nullptr);
   // one cell's index copies, then the rotation of x (its loads not queued behind
   // the bulk of the prologue), then the rest of the prologue
   Cursor cur = decode_begin<F>(j1, sv, 1);
@@ -870,7 +901,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
     }
     __syncthreads();
   }
-  decode_run<F, NT, uint16_t>(j1, a.x + (size_t)a.row0 * a.d_model, cur, sv, status);
+  decode_run<F, NT, uint16_t>(j1, a.x + (size_t)a.row0 * a.d_model, cur, sv, &tables, status);
 
   if (a.mlp) {
     DecodeJob j3;
@@ -894,7 +925,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
     swiglu_tasks<NT>(a, j1, ctl + a.off_hd, status);
     // one cell's index copies ahead of the h rotation, the rest after it (as for x)
     Cursor cur3 = decode_begin<F>(j3, sv, 1);
-    decode_run<F, NT, float>(j3, a.hbuf, cur3, sv, status);
+    decode_run<F, NT, float>(j3, a.hbuf, cur3, sv, nullptr, status);
     output_tasks<NT>(a, j3, status);
   } else {
     output_tasks<NT>(a, j1, status);
