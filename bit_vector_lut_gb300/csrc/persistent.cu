@@ -238,16 +238,49 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// (a * s, b * s) rounded to an FP16 pair; the products as scalar multiplies would round them.
+__device__ __forceinline__ uint32_t pack_half2_scaled(float a, float b, unsigned long long ss) {
+  unsigned long long x;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(x) : "l"(x), "l"(ss));
+  float p, q;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(p), "=f"(q) : "l"(x));
+  return pack_half2(p, q);
+}
+
 // Butterflies of stride S (in register index) over v[0 .. 32).
 template <int S>
 __device__ __forceinline__ void bfly32(float (&v)[32]) {
+  if constexpr (S == 1) {
 #pragma unroll
-  for (int i = 0; i < 32; ++i)
-    if ((i & S) == 0) {
-      const float x0 = v[i], x1 = v[i + S];
+    for (int i = 0; i < 32; i += 2) {
+      const float x0 = v[i], x1 = v[i + 1];
       v[i] = x0 + x1;
-      v[i + S] = x0 - x1;
+      v[i + 1] = x0 - x1;
     }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2)
+      if ((i & S) == 0) {
+        const float x0 = v[i], x1 = v[i + S], y0 = v[i + 1], y1 = v[i + S + 1];
+        v[i] = x0 + x1;
+        v[i + S] = x0 - x1;
+        v[i + 1] = y0 + y1;
+        v[i + S + 1] = y0 - y1;
+      }
+  }
+}
+
+// 32 x 32 bit transpose across the warp: bit b of lane r's result is bit r of lane b's word.
+__device__ __forceinline__ uint32_t warp_bit_transpose(uint32_t x, int lane) {
+  constexpr uint32_t m[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+  for (int r = 0; r < 5; ++r) {
+    const int sh = 16 >> r;
+    const uint32_t y = __shfl_xor_sync(0xffffffffu, x, sh);
+    x = (lane & sh) ? ((x & ~m[r]) | ((y >> sh) & m[r])) : ((x & m[r]) | ((y & m[r]) << sh));
+  }
+  return x;
 }
 
 // Butterflies of register strides 1 .. min(32, limit)/2.
@@ -321,6 +354,8 @@ __device__ __forceinline__ void stage_round(const DecodeJob& a, const T* src, in
   if (a.chunk == 1024) {
     // one (chunk, row) per warp: lane L holds columns L + 32 j, then 32 L + c
     float* m = sv.scratch + warp * 1024;
+    unsigned long long ss;  // (scale, scale)
+    asm("mov.b64 %0, {%1, %1};" : "=l"(ss) : "f"(scale));
     int item = 0;
     const Window win(kg_s, len, ckg, n_chunks);
     for (int i = 0; i < win.n; ++i) {
@@ -348,9 +383,10 @@ __device__ __forceinline__ void stage_round(const DecodeJob& a, const T* src, in
           }
         }
         if (a.signs) {
+          // bit j of t: the sign of column c * 1024 + 32 j + lane (one word per lane, transposed)
+          const uint32_t t = warp_bit_transpose(__ldg(a.signs + c * 32 + lane), lane);
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (sign_bit(a.signs, c * 1024 + 32 * j + lane)) v[j] = -v[j];
+          for (int j = 0; j < 32; ++j) v[j] = __int_as_float(__float_as_int(v[j]) ^ ((t << (31 - j)) & 0x80000000u));
         }
         fwht32(v, a.block >> 5);  // column strides 32 .. block/2
 #pragma unroll
@@ -365,10 +401,9 @@ __device__ __forceinline__ void stage_round(const DecodeJob& a, const T* src, in
 #pragma unroll
           for (int t = 0; t < 4; ++t)
             sts128(stage_chunk_addr(sv.stage, p, NT, nt, h * 32 + 4 * g + t),
-                   pack_half2(v[2 * t] * scale, v[2 * t + 1] * scale),
-                   pack_half2(v[8 + 2 * t] * scale, v[9 + 2 * t] * scale),
-                   pack_half2(v[16 + 2 * t] * scale, v[17 + 2 * t] * scale),
-                   pack_half2(v[24 + 2 * t] * scale, v[25 + 2 * t] * scale));
+                   pack_half2_scaled(v[2 * t], v[2 * t + 1], ss), pack_half2_scaled(v[8 + 2 * t], v[9 + 2 * t], ss),
+                   pack_half2_scaled(v[16 + 2 * t], v[17 + 2 * t], ss),
+                   pack_half2_scaled(v[24 + 2 * t], v[25 + 2 * t], ss));
       }
     }
     return;
