@@ -149,13 +149,17 @@ __device__ __forceinline__ void poll_geq(const unsigned* p, unsigned target, int
   }
 }
 
-// The CTA's writes so far become visible, then *p += 1 (and *p2 += 1).
+__device__ __forceinline__ void red_release(unsigned* p) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p) : "memory");
+}
+
+// The CTA's writes so far become visible, then *p += 1 (and *p2 += 1): the barrier orders
+// every thread's writes before thread 0's release increments.
 __device__ __forceinline__ void signal(unsigned* p, unsigned* p2) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(p, 1u);
-    if (p2) atomicAdd(p2, 1u);
+    red_release(p);
+    if (p2) red_release(p2);
   }
 }
 
@@ -761,9 +765,8 @@ __device__ __forceinline__ void swiglu_tasks(const PersistArgs& a, const DecodeJ
     if (threadIdx.x == 0) {
       poll_geq(gu.group_done + g0, (unsigned)n0, status);
       if (two) poll_geq(gu.group_done + g1, (unsigned)n1, status);
-      __threadfence();
     }
-    __syncthreads();
+    __syncthreads();  // thread 0's acquire loads, then the barrier: the pieces are visible to the CTA
     const float* pg0 = gu.seg_pieces(2 * m0, PIECE);
     const float* pu0 = gu.seg_pieces(2 * m0 + 1, PIECE);
     const float* pg1 = gu.seg_pieces(2 * m1 - (two ? 0 : 2 * G), PIECE);  // unused unless two
@@ -825,9 +828,8 @@ __device__ __forceinline__ void output_tasks(const PersistArgs& a, const DecodeJ
     const float lr = (a.lr_y && r < a.rows) ? __ldg(a.lr_y + (size_t)(a.row0 + r) * j.d_out + ch) : 0.f;
     if (threadIdx.x == 0) {
       poll_geq(j.group_done + g, (unsigned)count, status);
-      __threadfence();
     }
-    __syncthreads();
+    __syncthreads();  // as for the SwiGLU tasks
     const float* base = j.seg_pieces(sg, PIECE) + it;
     float y = 0.f;
     for (int q0 = 0; q0 < count; q0 += P) {
@@ -970,9 +972,9 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
   // the last CTA to finish clears the counters for the next launch
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    s_flag = atomicAdd(ctl, 1u) + 1 == gridDim.x;
-    __threadfence();
+    unsigned old;  // acquire and release: every CTA's waits precede the last CTA's clearing
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(ctl) : "memory");
+    s_flag = old + 1 == gridDim.x;
   }
   __syncthreads();
   if (s_flag)
