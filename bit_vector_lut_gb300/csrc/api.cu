@@ -1,5 +1,6 @@
 // C ABI of the VQ3 library: argument validation, host-side layout packing,
 // workspace carving and kernel dispatch. No device memory is allocated here.
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -257,6 +258,8 @@ cudaError_t run_persistent(const uint16_t* x, int rows, int nt, const vq3_mlp_la
   if (layer ? !(persist_cells_fit(a.d_model, a.d_inter, 2, a.grid1) && persist_cells_fit(a.d_inter, a.d_model, 1, a.grid3))
             : !persist_cells_fit(a.d_model, a.d_model_out, 1, a.grid1))
     return cudaErrorInvalidValue;
+  a.scale_in = 1.0f / std::sqrt((float)a.block_in);
+  a.scale_dn = a.mlp ? 1.0f / std::sqrt((float)a.block_dn) : 1.0f;
   a.n_ctl = c.n;
   a.off_g = c.off_g;
   a.off_hd = c.off_hd;

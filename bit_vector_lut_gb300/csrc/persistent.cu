@@ -176,6 +176,8 @@ struct DecodeJob {
   // activation source, rotated into the stage: rows [0, rows) at src + r * src_ld
   size_t src_ld;
   int rows, block, chunk;   // valid rows; rotation block; chunk (whole blocks, columns)
+  float scale;              // 1 / sqrt(block)
+  int c0, c1;               // this CTA's cells [c0, c1) (set when the job is made)
   const uint32_t* signs;
   const float* inv;         // RMSNorm of the source rows: per-row 1/rms (shared memory), or null
   const uint16_t* res_delta;  // with inv: the residual delta added to the source first, or null
@@ -334,12 +336,13 @@ __device__ __forceinline__ bool sign_bit(const uint32_t* signs, int col) {
 }
 
 // The chunks that hold the round's column groups kg_s .. kg_s + len - 1 (cyclic over
-// n_chunks chunks of ckg column groups): n of them, from chunk first on, each once.
+// n_chunks chunks of 2^lg column groups; a chunk is a power of two, like the rotation
+// block): n of them, from chunk first on, each once.
 struct Window {
   int first, n, n_chunks;
-  __device__ Window(int kg_s, int len, int ckg, int n_chunks_) : n_chunks(n_chunks_) {
-    first = kg_s / ckg;
-    n = (kg_s - first * ckg + len + ckg - 1) / ckg;
+  __device__ Window(int kg_s, int len, int lg, int n_chunks_) : n_chunks(n_chunks_) {
+    first = kg_s >> lg;
+    n = (kg_s - (first << lg) + len + (1 << lg) - 1) >> lg;
     if (n > n_chunks) n = n_chunks;
   }
   __device__ int chunk(int i) const { return first + i < n_chunks ? first + i : first + i - n_chunks; }
@@ -352,8 +355,9 @@ template <int NT, typename T>
 __device__ __forceinline__ void stage_round(const DecodeJob& a, const T* src, int kg_s, int len, const SmemView& sv) {
   const int n_kg = a.n_kg();
   const int ckg = a.chunk / kSuInputs;
-  const int n_chunks = n_kg / ckg;
-  const float scale = 1.0f / sqrtf((float)a.block);
+  const int lg = __ffs(ckg) - 1;  // ckg is a power of two
+  const int n_chunks = n_kg >> lg;
+  const float scale = a.scale;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (a.chunk == 1024) {
     // one (chunk, row) per warp: lane L holds columns L + 32 j, then 32 L + c
@@ -361,7 +365,7 @@ __device__ __forceinline__ void stage_round(const DecodeJob& a, const T* src, in
     unsigned long long ss;  // (scale, scale)
     asm("mov.b64 %0, {%1, %1};" : "=l"(ss) : "f"(scale));
     int item = 0;
-    const Window win(kg_s, len, ckg, n_chunks);
+    const Window win(kg_s, len, lg, n_chunks);
     for (int i = 0; i < win.n; ++i) {
       const int c = win.chunk(i);
       for (int row = 0; row < a.rows; ++row, ++item) {
@@ -414,7 +418,7 @@ __device__ __forceinline__ void stage_round(const DecodeJob& a, const T* src, in
   }
   // smaller chunks: CTA-wide butterflies over [8 rows][chunk] fp32 in the scratch
   float* buf = sv.scratch;
-  const Window win(kg_s, len, ckg, n_chunks);
+  const Window win(kg_s, len, lg, n_chunks);
   for (int i = 0; i < win.n; ++i) {
     const int c = win.chunk(i);
     for (int nt = 0; nt < NT; ++nt) {
@@ -592,9 +596,15 @@ struct Ring {
 };
 
 __device__ __forceinline__ void cell_range(const DecodeJob& a, int& c0, int& c1) {
+  c0 = a.c0;
+  c1 = a.c1;
+}
+
+// The job's cell range of this CTA.
+__device__ __forceinline__ void set_range(DecodeJob& a) {
   const int cells = a.cells();
-  c0 = range_begin(cells, a.grid, blockIdx.x);
-  c1 = range_begin(cells, a.grid, blockIdx.x + 1);
+  a.c0 = range_begin(cells, a.grid, blockIdx.x);
+  a.c1 = range_begin(cells, a.grid, blockIdx.x + 1);
 }
 
 // Points the cursor at column group kg of group g.
@@ -678,7 +688,8 @@ __device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cur
       // the chunks of the round's column groups must be complete
       if (tid == 0) {
         const int ckg = a.chunk / kSuInputs;
-        const Window win(kg_s, len, ckg, n_kg / ckg);
+        const int lg = __ffs(ckg) - 1;
+        const Window win(kg_s, len, lg, n_kg >> lg);
         for (int i = 0; i < win.n; ++i) poll_geq(a.ready + win.chunk(i), a.ready_target, status);
       }
       __syncthreads();  // thread 0's acquire loads, then the barrier: the chunks are visible to the CTA
@@ -863,6 +874,8 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
   extern __shared__ __align__(16) unsigned char dsm[];
   __shared__ int s_flag;
   __shared__ float s_inv[32];  // 1/rms of the pass's rows (pre-norm residual step)
+  __shared__ float s_part[32];  // sums of squares of the rows' column ranges
+  __shared__ int s_range3[2];   // the down step's cell range
   SmemView sv;
   const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(dsm));
   sv.ring = base;
@@ -888,6 +901,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
   j1.src_ld = (size_t)a.d_model;
   j1.rows = a.rows;
   j1.block = a.block_in;
+  j1.scale = a.scale_in;
   j1.chunk = a.x_chunk;
   j1.signs = a.signs_in;
   j1.inv = a.norm ? s_inv : nullptr;
@@ -895,6 +909,14 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
   j1.ready = nullptr;
   j1.ready_target = 0;
   j1.group_done = ctl + (a.mlp ? a.off_g : a.off_o);
+  set_range(j1);
+  if (a.mlp && threadIdx.x == 0) {
+    // the down step's cell range, worked out now, away from the hand-off before that step
+    const int n_seg3 = a.d_model / kSuChannels;
+    const int cells3 = (n_seg3 + kWarps - 1) / kWarps * (a.d_inter / kSuInputs);
+    s_range3[0] = range_begin(cells3, a.grid3, blockIdx.x);
+    s_range3[1] = range_begin(cells3, a.grid3, blockIdx.x + 1);
+  }
 
   TableLoad<F> tables;
   tables.load(a.gate.codebook, a.mlp ? a.up.codebook : nullptr, a.mlp ? a.down.codebook : nullptr);
@@ -904,37 +926,62 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
   if (a.norm) {
     // pre-norm residual step for the pass's rows: r' = fp16(x + delta) over the whole row
     // (every CTA, for its own 1/rms), the 64-column slices s with s % grid == CTA written to
-    // res_out; one warp per row, lanes over 8-column groups, a fixed reduction order
+    // res_out. Each row is split into `parts` column ranges, one warp each (parts = warps per
+    // row, a power of two); a lane's loads go out four 8-column groups at a time. The sum of
+    // squares is reduced in a fixed order: lanes in sequence, the warp's xor tree, parts in order.
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, d = a.d_model;
-    for (int rr = warp; rr < a.rows; rr += kWarps) {
+    int parts = 1;
+    while (parts * 2 * a.rows <= kWarps) parts *= 2;
+    const int n8 = d / 8;
+    for (int w = warp; w < a.rows * parts; w += kWarps) {
+      const int rr = w / parts, part = w % parts;
       const size_t ro = (size_t)(a.row0 + rr) * d;
+      const int g0 = part * n8 / parts, g1 = (part + 1) * n8 / parts;
       float ss = 0.f;
-      for (int c8 = lane * 8; c8 < d; c8 += 256) {
-        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(a.x + ro + c8));
-        uint4 rv = xv;
-        if (a.res_delta) {
-          const uint4 dv = __ldg(reinterpret_cast<const uint4*>(a.res_delta + ro + c8));
-          const __half2* xh = reinterpret_cast<const __half2*>(&xv);
-          const __half2* dh = reinterpret_cast<const __half2*>(&dv);
-          __half2* rh = reinterpret_cast<__half2*>(&rv);
+      for (int gb = g0; gb < g1; gb += 4 * 32) {
+        uint4 xv[4], dv[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 xf = __half22float2(xh[k]), df = __half22float2(dh[k]);
-            rh[k] = __floats2half2_rn(xf.x + df.x, xf.y + df.y);
+        for (int u = 0; u < 4; ++u) {
+          const int g = gb + u * 32 + lane;
+          if (g < g1) {
+            xv[u] = __ldg(reinterpret_cast<const uint4*>(a.x + ro) + g);
+            if (a.res_delta) dv[u] = __ldg(reinterpret_cast<const uint4*>(a.res_delta + ro) + g);
           }
         }
-        const __half2* rh = reinterpret_cast<const __half2*>(&rv);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 f = __half22float2(rh[k]);
-          ss = fmaf(f.x, f.x, ss);
-          ss = fmaf(f.y, f.y, ss);
+        for (int u = 0; u < 4; ++u) {
+          const int g = gb + u * 32 + lane;
+          if (g >= g1) break;
+          uint4 rv = xv[u];
+          if (a.res_delta) {
+            const __half2* xh = reinterpret_cast<const __half2*>(&xv[u]);
+            const __half2* dh = reinterpret_cast<const __half2*>(&dv[u]);
+            __half2* rh = reinterpret_cast<__half2*>(&rv);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 xf = __half22float2(xh[k]), df = __half22float2(dh[k]);
+              rh[k] = __floats2half2_rn(xf.x + df.x, xf.y + df.y);
+            }
+          }
+          const __half2* rh = reinterpret_cast<const __half2*>(&rv);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 f = __half22float2(rh[k]);
+            ss = fmaf(f.x, f.x, ss);
+            ss = fmaf(f.y, f.y, ss);
+          }
+          if ((g >> 3) % (int)gridDim.x == (int)blockIdx.x) *(reinterpret_cast<uint4*>(a.res_out + ro) + g) = rv;
         }
-        if ((c8 / 64) % (int)gridDim.x == (int)blockIdx.x) *reinterpret_cast<uint4*>(a.res_out + ro + c8) = rv;
       }
 #pragma unroll
       for (int h = 16; h > 0; h >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, h);
-      if (lane == 0) s_inv[rr] = 1.0f / sqrtf(ss / (float)d + a.eps);
+      if (lane == 0) s_part[w] = ss;
+    }
+    __syncthreads();
+    if ((int)threadIdx.x < a.rows) {
+      float ss = 0.f;
+      for (int q = 0; q < parts; ++q) ss += s_part[threadIdx.x * parts + q];
+      s_inv[threadIdx.x] = 1.0f / sqrtf(ss / (float)d + a.eps);
     }
     __syncthreads();
   }
@@ -954,11 +1001,14 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
     j3.src_ld = (size_t)a.d_inter;
     j3.rows = a.rows;
     j3.block = a.block_dn;
+    j3.scale = a.scale_dn;
     j3.chunk = a.h_chunk;
     j3.signs = a.signs_dn;
     j3.ready = ctl + a.off_hd;
     j3.ready_target = (unsigned)(a.h_chunk / kSuChannels);
     j3.group_done = ctl + a.off_o;
+    j3.c0 = s_range3[0];  // written by thread 0 before the first barrier of the gate/up step
+    j3.c1 = s_range3[1];
     swiglu_tasks<NT>(a, j1, ctl + a.off_hd, status);
     // one cell's index copies ahead of the h rotation, the rest after it (as for x)
     Cursor cur3 = decode_begin<F>(j3, sv, 1);

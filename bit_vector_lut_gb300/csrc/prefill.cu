@@ -51,7 +51,8 @@ constexpr int kEpiWarp0 = kMmaWarp + 1;          // warps 10-13
 constexpr int kPThreads = (kEpiWarp0 + 4) * 32;
 constexpr int kEpiThreads = 4 * 32;
 constexpr int kMinSteps = 8;  // fewest K steps per CTA
-constexpr int kMaxStages = 6;
+constexpr int kMaxStages = 12;  // load stages
+constexpr int kMaxAStages = 3;  // decoded A tiles
 constexpr int kPrefetchSteps = 8;  // index strings are prefetched into L2 this many K steps ahead
 constexpr int kTileM = 128;                    // output channels per tile
 constexpr int kATile = kTileM * 64 * 2;        // 16 KB of FP16
@@ -282,14 +283,25 @@ struct PfSmem {
   static constexpr int kBTile = N * 64 * 2;
   static constexpr int kSu = FmtSizes<F>::kSuBytes;
   static constexpr int kIdxBytes = 2 * kSu;  // index strings of the tile's two super-units per K step
-  static constexpr int kStageBytes = kATile + kBTile + kIdxBytes;
-  static_assert(kStageBytes % 1024 == 0 && kATile % 1024 == 0, "B tiles start on 1 KB swizzle atoms");
-  // stages in flight: as many as fit, up to kMaxStages (the K loop is latency-bound at small N)
-  static constexpr int kStages = N >= 256 ? 3 : (N >= 128 ? 5 : 6);
-  static_assert(kStages <= kMaxStages, "barrier array size");
-  static constexpr int kTotal = 1024 + kStages * kStageBytes + (int)PfTab<F>::kAlign + 2 * (int)PfTab<F>::kStride +
-                                64 * 16 * 4;
-  static_assert(kTotal <= 227 * 1024, "shared memory per CTA");
+  static constexpr int kLoadBytes = kBTile + kIdxBytes;
+  static_assert(kBTile % 1024 == 0 && kATile % 1024 == 0, "B tiles start on 1 KB swizzle atoms");
+  // alignment slack of the stage area, codebook tables (with their alignment slack), SwiGLU
+  // exchange; and room for the kernel's static shared memory
+  static constexpr int kFixed = 1024 + (int)PfTab<F>::kAlign + 2 * (int)PfTab<F>::kStride + 64 * 16 * 4;
+  static constexpr int kStaticRoom = 512;
+  // Decoded A tiles in flight: the decoders run ahead of the MMA by kAStages - 1 steps.
+  static constexpr int kAStages = N >= 256 ? 2 : 3;
+  // Load stages (B tile and index strings): as many as fit. The K loop is bound by the round
+  // trip from a stage's MMA completion through its refill to its next MMA, so the load ring,
+  // not the A tiles, sets how many steps are in flight.
+  static constexpr int kFit = (227 * 1024 - kStaticRoom - kFixed - kAStages * kATile) / kLoadBytes;
+  static constexpr int kLoadStages = kFit > kMaxStages ? kMaxStages : kFit;
+  static_assert(kLoadStages >= 2 && kAStages <= kMaxAStages, "stage counts");
+  static constexpr int kBOffset = kAStages * kATile;                 // B tiles
+  static constexpr int kIOffset = kBOffset + kLoadStages * kBTile;   // index strings
+  static constexpr int kStageArea = kIOffset + kLoadStages * kIdxBytes;
+  static constexpr int kTotal = kFixed + kStageArea;
+  static_assert(kTotal + kStaticRoom <= 227 * 1024, "shared memory per CTA");
 };
 
 // This CTA's share of the (tile, K step) space: steps [begin(c), begin(c + 1)).
@@ -325,23 +337,24 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
                                                                      const __grid_constant__ CUtensorMap xmap) {
   extern __shared__ __align__(16) unsigned char dsm[];
   using PS = PfSmem<N, F>;
-  constexpr int kStages = PS::kStages;
-  __shared__ __align__(8) unsigned long long s_bars[3 * kMaxStages + 4];
+  constexpr int kSL = PS::kLoadStages, kSA = PS::kAStages;
+  __shared__ __align__(8) unsigned long long s_bars[2 * kMaxStages + 2 * kMaxAStages + 4];
   __shared__ uint32_t s_tmem;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t raw = smem_u32(dsm);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 1 KB aligned stages (swizzle atoms)
-  const uint32_t tabs = (base + kStages * PS::kStageBytes + PfTab<F>::kAlign - 1) & ~(PfTab<F>::kAlign - 1);
+  const uint32_t tabs = (base + PS::kStageArea + PfTab<F>::kAlign - 1) & ~(PfTab<F>::kAlign - 1);
   float* xch = reinterpret_cast<float*>(dsm + (tabs - raw) + 2 * PfTab<F>::kStride);  // up values for SwiGLU
   const uint32_t bar0 = smem_u32(s_bars);
-  auto full_bar = [&](int s) { return bar0 + 8u * s; };                 // A decoded
-  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };    // stage consumed
-  auto load_bar = [&](int s) { return bar0 + 8u * (2 * kStages + s); }; // B and indices landed
-  auto acc_full = [&](int b) { return bar0 + 8u * (3 * kStages + b); }; // accumulator b complete
-  auto acc_empty = [&](int b) { return bar0 + 8u * (3 * kStages + 2 + b); };  // accumulator b drained
-  auto a_tile = [&](int s) { return base + (uint32_t)(s * PS::kStageBytes); };
-  auto b_tile = [&](int s) { return base + (uint32_t)(s * PS::kStageBytes + kATile); };
-  auto i_tile = [&](int s) { return base + (uint32_t)(s * PS::kStageBytes + kATile + PS::kBTile); };
+  auto load_full = [&](int s) { return bar0 + 8u * s; };                       // B and indices landed
+  auto load_empty = [&](int s) { return bar0 + 8u * (kSL + s); };              // B and indices consumed
+  auto a_full = [&](int s) { return bar0 + 8u * (2 * kSL + s); };              // A decoded
+  auto a_empty = [&](int s) { return bar0 + 8u * (2 * kSL + kSA + s); };       // A consumed
+  auto acc_full = [&](int b) { return bar0 + 8u * (2 * kSL + 2 * kSA + b); };  // accumulator b complete
+  auto acc_empty = [&](int b) { return bar0 + 8u * (2 * kSL + 2 * kSA + 2 + b); };  // accumulator b drained
+  auto a_tile = [&](int s) { return base + (uint32_t)(s * kATile); };
+  auto b_tile = [&](int s) { return base + (uint32_t)(PS::kBOffset + s * PS::kBTile); };
+  auto i_tile = [&](int s) { return base + (uint32_t)(PS::kIOffset + s * PS::kIdxBytes); };
 
   const int n_kg = a.d_in / 64;
   const int n_tiles = (a.rows + N - 1) / N;  // row tiles
@@ -369,10 +382,13 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
     }
   }
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(full_bar(s), kDecWarps * 32);
-      mbar_init(empty_bar(s), 1);
-      mbar_init(load_bar(s), 1);
+    for (int s = 0; s < kSL; ++s) {
+      mbar_init(load_full(s), 1);
+      mbar_init(load_empty(s), 1);
+    }
+    for (int s = 0; s < kSA; ++s) {
+      mbar_init(a_full(s), kDecWarps * 32);
+      mbar_init(a_empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(acc_full(b), 1);
@@ -408,18 +424,18 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
         const uint4* su0 = a.packed0 + (size_t)mg0 * n_kg * kSuU4;
         const uint4* su1 = (a.swiglu ? a.packed1 : a.packed0) + (size_t)(live1 ? mg1 : mg0) * n_kg * kSuU4;
         for (int kk = g.k0; kk < g.k1; ++kk, ++it) {
-          const int st = it % kStages;
-          if (it >= kStages) mbar_wait(empty_bar(st), (uint32_t)((it / kStages - 1) & 1), a.status);
-          mbar_expect_tx(load_bar(st), kTx);
+          const int ls = it % kSL;
+          if (it >= kSL) mbar_wait(load_empty(ls), (uint32_t)((it / kSL - 1) & 1), a.status);
+          mbar_expect_tx(load_full(ls), kTx);
           // activation tile: N rows x 64 inputs in the 128-byte swizzle layout (rows
           // past the last are filled with zeros)
           if (kk + kPrefetchSteps < g.k1) {
             prefetch_l2(su0 + (size_t)(kk + kPrefetchSteps) * kSuU4, kSuB);
             prefetch_l2(su1 + (size_t)(kk + kPrefetchSteps) * kSuU4, kSuB);
           }
-          tma_load_2d(b_tile(st), &xmap, kk * 64, row0, load_bar(st));
-          bulk_load(i_tile(st), su0 + (size_t)kk * kSuU4, kSuB, load_bar(st));
-          bulk_load(i_tile(st) + kSuB, su1 + (size_t)kk * kSuU4, kSuB, load_bar(st));
+          tma_load_2d(b_tile(ls), &xmap, kk * 64, row0, load_full(ls));
+          bulk_load(i_tile(ls), su0 + (size_t)kk * kSuU4, kSuB, load_full(ls));
+          bulk_load(i_tile(ls) + kSuB, su1 + (size_t)kk * kSuU4, kSuB, load_full(ls));
         }
         s += g.k1 - g.k0;
       }
@@ -438,15 +454,15 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
       const int mt = g.t / n_tiles;
       const bool live = su == 0 || a.swiglu || 2 * mt + 1 < a.d_out / 64;
       for (int kk = g.k0; kk < g.k1; ++kk, ++it) {
-        const int st = it % kStages;
-        if (it >= kStages) mbar_wait(empty_bar(st), (uint32_t)((it / kStages - 1) & 1), a.status);
-        mbar_wait(load_bar(st), (uint32_t)((it / kStages) & 1), a.status);
+        const int ls = it % kSL, as = it % kSA;
+        if (it >= kSA) mbar_wait(a_empty(as), (uint32_t)((it / kSA - 1) & 1), a.status);
+        mbar_wait(load_full(ls), (uint32_t)((it / kSL) & 1), a.status);
         if (live) {
           // input steps [s_lo, s_hi) are words kW s_lo .. kW s_hi of the string (kW
           // words per step; the last word for six-bit indices that straddle two)
           constexpr int kW = Fmt<F>::kWords / 4;
           uint32_t w[Fmt<F>::kWords] = {};
-          const uint32_t is = i_tile(st) + (uint32_t)(su * PS::kSu);
+          const uint32_t is = i_tile(ls) + (uint32_t)(su * PS::kSu);
 #pragma unroll
           for (int q = 0; q < FmtSizes<F>::kChunks; ++q) {
             if (4 * q > kW * s_hi || 4 * q + 3 < kW * s_lo) continue;
@@ -458,10 +474,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
             w[4 * q + 2] = v2;
             w[4 * q + 3] = v3;
           }
-          decode_part<F>(w, part, L, su * 64, a_tile(st), lanebase);
+          decode_part<F>(w, part, L, su * 64, a_tile(as), lanebase);
         }
         fence_proxy_async();  // the generic-proxy writes of A, before the MMA reads them
-        mbar_arrive(full_bar(st));
+        mbar_arrive(a_full(as));
       }
       s += g.k1 - g.k0;
     }
@@ -477,18 +493,19 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
         tc_fence_after();
         const uint32_t acc = tmem + (uint32_t)(b * N);
         for (int kk = g.k0; kk < g.k1; ++kk, ++it) {
-          const int st = it % kStages;
-          mbar_wait(load_bar(st), (uint32_t)((it / kStages) & 1), a.status);
-          mbar_wait(full_bar(st), (uint32_t)((it / kStages) & 1), a.status);
+          const int ls = it % kSL, as = it % kSA;
+          mbar_wait(load_full(ls), (uint32_t)((it / kSL) & 1), a.status);
+          mbar_wait(a_full(as), (uint32_t)((it / kSA) & 1), a.status);
           tc_fence_after();
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             // K = 16: two core matrices along K
-            const uint64_t ad = smem_desc(a_tile(st) + (uint32_t)(j * 2 * kTileM * 16), kTileM * 16, 128);
-            const uint64_t bd = smem_desc_sw128(b_tile(st) + (uint32_t)(j * 32));
+            const uint64_t ad = smem_desc(a_tile(as) + (uint32_t)(j * 2 * kTileM * 16), kTileM * 16, 128);
+            const uint64_t bd = smem_desc_sw128(b_tile(ls) + (uint32_t)(j * 32));
             mma_ss(acc, ad, bd, idesc, (kk > g.k0 || j > 0) ? 1u : 0u);
           }
-          mma_commit(empty_bar(st));
+          mma_commit(load_empty(ls));  // both complete when this step's MMAs have read their operands
+          mma_commit(a_empty(as));
         }
         mma_commit(acc_full(b));
         s += g.k1 - g.k0;

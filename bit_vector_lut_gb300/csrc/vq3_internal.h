@@ -116,6 +116,7 @@ struct PersistArgs {
   int d_model, d_inter;     // MLP: hidden and intermediate widths; linear: d_model = d_in
   int d_model_out;          // linear: d_out
   int block_in, block_dn;   // rotation blocks of the gate/up (or linear) input and of the down input
+  float scale_in, scale_dn; // 1 / sqrt(block), rounded as the float expression 1.0f / sqrtf(block)
   const uint32_t* signs_in; // sign bits or null
   const uint32_t* signs_dn;
   int x_chunk, h_chunk;     // columns per rotation chunk of x and of h (whole blocks, <= 1024)
