@@ -10,29 +10,31 @@
 //   linear / down:  y[r][o] = fp16( s[o] * sum_i W0[o][i] x'[r][i] ),  W0[2p+c][i] = C[idx[p][i]][c]
 //   gate + up:      h[r][j] = silu(s_g[j] g[r][j]) * (s_u[j] u[r][j])  (FP32)
 //
-// One CTA computes one output tile of 128 channels x N rows (N <= 256), with the
-// FP32 accumulator D[channel][row] in tensor memory, over K in steps of 64 inputs
-// (one column group of the packed super-units):
-//   warps 0-3  loaders: for stage s of a K step, copy the activation tile
-//              B[N][64] and the two super-units of index strings (cp.async); each
-//              thread's copies arrive on the stage's load barrier when they land,
-//              so the loaders run up to kStages steps ahead.
-//   warps 4-7  decoders: once the stage's index strings are in, each thread takes
-//              half of one lane string of one super-unit, looks its 32 indices up
-//              in a lane-private shared-memory copy of the codebook and pairs
-//              neighbouring inputs of a channel with a byte permute into the FP16
-//              words of A[128][64]. A and B are in the K-major "core matrix" layout
-//              (8 rows x 16 bytes per 128-byte block) that the MMA's shared-memory
-//              descriptors read.
-//   warp 8     one lane issues tcgen05.mma (M = 128, N, K = 16) four times per K
-//              step, and tcgen05.commit frees the stage (and, at the end, marks
-//              the accumulator complete).
-//   warps 8-11 epilogue: tcgen05.ld of the accumulator (each warp its 32 lanes),
-//              scale (and SwiGLU: the tile's rows 0-63 are gate channels, rows
-//              64-127 the up channels with the same indices) and store.
-// A 3-deep stage ring with mbarriers connects loaders, decoders and the MMA issuer. All
-// waits are bounded: one that runs out sets the status word to 3 and the kernel
-// carries on to its end (results invalid).
+// An output tile is 128 channels x N rows (N <= 256), its FP32 accumulator
+// D[channel][row] in tensor memory, summed over K in steps of 64 inputs (one column
+// group of the packed super-units). The work is a persistent stream-K split of the (tile, K step) space: each CTA takes a
+// contiguous run of steps; a tile split between CTAs is summed in K order by the CTA
+// holding its first steps, from the raw partial sums of the others (per-CTA flags).
+//   warp 0     lane 0 issues, per K step, the TMA copy of the activation tile B[N][64]
+//              (128-byte swizzle, rows past the last read as zeros), the bulk copies of
+//              the two super-units of index strings, and an L2 prefetch of the index
+//              strings a few steps further on, all completing on the step's load barrier.
+//   warps 1-8  decoders: once a step's index strings are in, each warp takes part of the
+//              lane strings of one super-unit, looks the indices up in a lane-private
+//              shared-memory copy of the codebook and pairs neighbouring inputs of a
+//              channel with a byte permute into the FP16 words of A[128][64], in the
+//              K-major "core matrix" layout (8 rows x 16 bytes per 128-byte block) that
+//              the MMA's shared-memory descriptors read.
+//   warp 9     one lane issues tcgen05.mma (M = 128, N, K = 16) four times per K step;
+//              tcgen05.commit releases the step's load stage and A tile, and at the end
+//              of a tile marks its accumulator (one of two in tensor memory) complete.
+//   warps 10-13 epilogue: tcgen05.ld of the accumulator (each warp its 32 lanes), the
+//              later parts of a split tile, scale (and SwiGLU: the tile's rows 0-63 are
+//              gate channels, rows 64-127 the up channels of the same 64) and store.
+// Two mbarrier rings connect them: load stages (B tile + index strings; as many as fit,
+// so that copies run far ahead) and decoded A tiles (two or three). All waits are
+// bounded: one that runs out sets the status word to 3 and the kernel carries on to its
+// end (results invalid).
 #include <cuda.h>  // CUtensorMap; the encoder is fetched from the driver at run time
 #include <cuda_fp16.h>
 
