@@ -35,7 +35,7 @@ REF_BUDGET_S = 100.0
 # DRAM bytes (read + write) of one persistent_kernel launch at T=8, from the ncu capture
 # summarised in profiles/persistent_kernel_mlp_5120x17408_T8.md; None when the kernel has
 # changed since that capture.
-TRAFFIC_PER_LAUNCH = None
+TRAFFIC_PER_LAUNCH = 103_634_688
 
 
 def peaks() -> dict:
@@ -417,39 +417,46 @@ TOKEN_MIXERS = (("in_proj_5120x12288", 5120, 12288), ("out_proj_6144x5120", 6144
 
 
 def token_mixer_lines(vq3, dev, stream, pk, l2) -> dict:
-    """One projection per (shape, format) with rank-64 factors at T = 8 and T = 64: the median of 20
-    launches, each bracketed by events on the stream after a write of 2 x L2 that evicts the weights."""
+    """One projection per (shape, format) with rank-64 factors at T = 8 and T = 64, through a CUDA
+    graph cycling copies of the layer that together exceed 4x L2 (as for the block's formats):
+    every launch of the rotation, the factor kernels and the decode kernel is in the graph."""
     import torch
     res = {}
-    flush = torch.empty(int(2 * l2), dtype=torch.uint8, device=dev)
     for name, d_in, d_out in TOKEN_MIXERS:
         for fmt in ("2x16", "lut4"):
             m = S.matrix(S.rng(80, 1), d_in, d_out, 1024, fmt)
             S.add_lowrank(S.rng(80, 3), m, 64, 0.02)
-            lin = vq3.Linear.from_matrix(m, dev)
             nbytes = S.stream_bytes(d_in, d_out, fmt) + 2 * d_out + 2 * S.FORMATS[fmt][2] * S.FORMATS[fmt][1] \
                 + 2 * 64 * (d_in + d_out)
+            n_sets = max(2, math.ceil(4 * l2 / nbytes))
+            lins = [vq3.Linear.from_matrix(m, dev) for _ in range(n_sets)]
             for rows in (8, 64):
                 x = torch.from_numpy(S.activations(S.rng(80, 0), rows, d_in)).to(dev)
                 out = torch.empty((rows, d_out), dtype=torch.float16, device=dev)
-                ws = vq3.workspace(vq3.linear_workspace_bytes(rows, lin), dev, stream)
-                durs = []
-                for it in range(23):
-                    flush.fill_(it & 0xFF)
-                    a = torch.cuda.Event(enable_timing=True)
-                    b = torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
+                ws = vq3.workspace(vq3.linear_workspace_bytes(rows, lins[0]), dev, stream)
+                for lin in lins:
                     vq3.linear_forward(x, lin, out=out, ws=ws, stream=stream)
-                    b.record(stream)
-                    b.synchronize()
-                    if it >= 3:
-                        durs.append(a.elapsed_time(b))
-                ms = float(np.median(durs))
+                gph = torch.cuda.CUDAGraph()
+                reps = 4 * n_sets
+                with torch.cuda.graph(gph, stream=stream):
+                    for i in range(reps):
+                        vq3.linear_forward(x, lins[i % n_sets], out=out, ws=ws, stream=stream)
+                gph.replay()
+                torch.cuda.synchronize(dev)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for _ in range(3):
+                    gph.replay()
+                b.record(stream)
+                b.synchronize()
+                ms = a.elapsed_time(b) / (3 * reps)
                 gbs = nbytes / (ms / 1e3) / 1e9
                 res[f"{name}_{fmt}_T{rows}"] = {"us": round(ms * 1e3, 2), "weight_bytes": nbytes,
                                                "weight_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4),
                                                "tflops": round(2 * d_in * d_out * rows / (ms / 1e3) / 1e12, 2),
-                                               "status": vq3.workspace_status(ws)}
+                                               "weight_copies": n_sets, "status": vq3.workspace_status(ws)}
+            del lins
     return res
 
 
