@@ -522,25 +522,24 @@ def stack64(vq3, dev, stream, pk) -> dict:
     """The 64-layer stack at T = 8: per layer a residual add + RMSNorm and one MLP block
     (6.42 GB of packed weights, so every layer streams from HBM), one CUDA graph of all
     64 layers, timed with events on its stream over 5 replays after 2 warm-up replays.
-    Each layer is one vq3_mlp_forward_residual call (the residual step fused into the
-    block's kernel) through two residual and two output buffers; the last residual add
-    is the standalone step."""
+    Each layer is one vq3_mlp_prenorm_step call: RMSNorm from the previous layer's
+    partial sums of squares, the block, and the residual add with the next partial sums
+    in the block's output step (two residual and two partial-sum buffers)."""
     import torch
     seed, rows, layers_n = 3, 8, 64
     x = torch.from_numpy(S.activations(S.rng(seed, 0), rows, HIDDEN)).to(dev)
     g = S.rng(seed, 1)
     layers = [vq3.MLP.from_block(S.mlp_block(g, HIDDEN, INTER, 1024), dev) for _ in range(layers_n)]
     res = [torch.empty_like(x), torch.empty_like(x)]
-    ys = [torch.empty_like(x), torch.empty_like(x)]
-    normed = torch.empty_like(x)
+    ss = [torch.empty((rows, HIDDEN // 16), dtype=torch.float32, device=dev) for _ in range(2)]
+    out = torch.empty_like(x)
     ws = vq3.workspace(vq3.mlp_workspace_bytes(rows, layers[0]), dev, stream)
 
     def run():
         res[0].copy_(x)
         for li, layer in enumerate(layers):
-            vq3.mlp_forward_residual(res[li % 2], ys[(li + 1) % 2] if li > 0 else None, layer, res[(li + 1) % 2],
-                                     ys[li % 2], ws=ws, stream=stream)
-        vq3.residual_rmsnorm(res[layers_n % 2], ys[(layers_n - 1) % 2], 1e-6, normed, stream=stream)
+            vq3.mlp_prenorm_step(res[li % 2], layer, out, res[(li + 1) % 2], ss=ss[li % 2] if li > 0 else None,
+                                 ss_next=ss[(li + 1) % 2], ws=ws, stream=stream)
 
     run()
     torch.cuda.synchronize(dev)

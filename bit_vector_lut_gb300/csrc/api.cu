@@ -202,6 +202,9 @@ struct PersistBufs {
   const uint16_t* res_delta;
   uint16_t* res_out;
   float eps;
+  const float* ss_in;  // residual stack chained by sums of squares (see PersistArgs)
+  uint16_t* res_next;
+  float* ss_next;
 };
 
 cudaError_t run_persistent(const uint16_t* x, int rows, int nt, const vq3_mlp_layer* layer, const vq3_linear* L,
@@ -223,6 +226,9 @@ cudaError_t run_persistent(const uint16_t* x, int rows, int nt, const vq3_mlp_la
     a.norm = b.norm;
     a.res_delta = b.res_delta;
     a.res_out = b.res_out;
+    a.ss_in = b.ss_in;
+    a.res_next = b.res_next;
+    a.ss_next = b.ss_next;
     a.eps = b.eps;
     a.d_model = H;
     a.d_inter = I;
@@ -692,6 +698,9 @@ int mlp_forward_decode(const uint16_t* x, int rows, const vq3_mlp_layer* layer, 
     b.res_delta = norm->res_delta;
     b.res_out = norm->res_out;
     b.eps = norm->eps;
+    b.ss_in = norm->ss_in;
+    b.res_next = norm->res_next;
+    b.ss_next = norm->ss_next;
   }
   b.hbuf = reinterpret_cast<float*>(c.ws + c.w.hbuf);
   b.pieces1 = reinterpret_cast<float*>(c.ws + c.w.pieces1);
@@ -773,6 +782,40 @@ int vq3_mlp_forward_residual(const uint16_t* r_in, const uint16_t* delta, int ro
   cudaError_t e = launch_residual_rmsnorm2(r_in, delta, r_out, rows, H, eps, out, st);
   if (e == cudaSuccess) e = run_prefill_mlp(out, rows, *layer, static_cast<char*>(workspace), out, st);
   if (e != cudaSuccess) return cuda_fail(e, "mlp_residual: launch");
+  return ok();
+}
+
+int vq3_mlp_prenorm_step(const uint16_t* r, const float* ss, int rows, const vq3_mlp_layer* layer, float eps,
+                         uint16_t* out, uint16_t* r_next, float* ss_next, void* workspace, size_t ws_bytes,
+                         void* stream) {
+  if (rows < 0 || !(eps >= 0.f)) return fail(VQ3_EINVAL, "mlp_prenorm: rows=%d eps=%g", rows, eps);
+  int rc = check_mlp(layer);
+  if (rc) return rc;
+  if (rows == 0) return ok();
+  if (!r || !out || !r_next || !workspace) return fail(VQ3_EINVAL, "mlp_prenorm: null pointer");
+  if (out == r || r_next == r || r_next == out || (ss && ss_next && (const void*)ss == (const void*)ss_next))
+    return fail(VQ3_EINVAL, "mlp_prenorm: out, r_next and ss_next must not alias r, ss or each other");
+  if (!aligned(r, 16) || !aligned(out, 16) || !aligned(r_next, 16) || (ss && !aligned(ss, 16)) ||
+      (ss_next && !aligned(ss_next, 16)))
+    return fail(VQ3_EALIGN, "mlp_prenorm: pointers must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (rows < kPrefillRows) {
+    PersistBufs nb{};
+    nb.eps = eps;
+    nb.ss_in = ss;
+    nb.res_next = r_next;
+    nb.ss_next = ss_next;
+    return mlp_forward_decode(r, rows, layer, out, workspace, ws_bytes, stream, 32, &nb);
+  }
+  // many rows: the RMSNorm kernel writes the normed rows into out (the block reads them
+  // before it writes its result there), the tensor-core path, then the residual step
+  const int H = layer->gate.d_in, I = layer->gate.d_out;
+  const size_t need = prefill_ws(rows, H, I, mlp_ctl_bytes(H, I)).total;
+  if (ws_bytes < need) return fail(VQ3_ENOSPACE, "mlp_prenorm: workspace %zu < %zu bytes", ws_bytes, need);
+  cudaError_t e = launch_residual_rmsnorm2(r, nullptr, const_cast<uint16_t*>(r), rows, H, eps, out, st);
+  if (e == cudaSuccess) e = run_prefill_mlp(out, rows, *layer, static_cast<char*>(workspace), out, st);
+  if (e == cudaSuccess) e = launch_residual_add_ss(r, out, r_next, ss_next, rows, H, st);
+  if (e != cudaSuccess) return cuda_fail(e, "mlp_prenorm: launch");
   return ok();
 }
 

@@ -822,7 +822,7 @@ __device__ __forceinline__ void swiglu_tasks(const PersistArgs& a, const DecodeJ
 
 // One task per (64 output channels, 8-row tile): out = fp16(scale * sum of pieces).
 template <int NT>
-__device__ __forceinline__ void output_tasks(const PersistArgs& a, const DecodeJob& j, int* status) {
+__device__ __forceinline__ void output_tasks(const PersistArgs& a, const DecodeJob& j, const SmemView& sv, int* status) {
   constexpr int PIECE = 512 * NT;
   constexpr int P = 32;
   const int n_seg = j.d_out / kSuChannels;
@@ -837,6 +837,7 @@ __device__ __forceinline__ void output_tasks(const PersistArgs& a, const DecodeJ
     const int ch = sg * kSuChannels + c;
     const float sc = __half2float(__ushort_as_half(__ldg(j.scales0 + ch)));
     const float lr = (a.lr_y && r < a.rows) ? __ldg(a.lr_y + (size_t)(a.row0 + r) * j.d_out + ch) : 0.f;
+    const float rin = (a.res_next && r < a.rows) ? load1(a.x + (size_t)(a.row0 + r) * j.d_out + ch) : 0.f;
     if (threadIdx.x == 0) {
       poll_geq(j.group_done + g, (unsigned)count, status);
     }
@@ -853,7 +854,28 @@ __device__ __forceinline__ void output_tasks(const PersistArgs& a, const DecodeJ
     if (r < a.rows) {
       float v = sc * y;
       if (a.lr_y) v += lr;  // low-rank correction
-      a.out[(size_t)(a.row0 + r) * j.d_out + ch] = __half_as_ushort(__float2half_rn(v));
+      const __half o16 = __float2half_rn(v);
+      a.out[(size_t)(a.row0 + r) * j.d_out + ch] = __half_as_ushort(o16);
+      if (a.res_next) {
+        // the next residual, r + out, and its squares for the partial sums below
+        const float rn = round16(rin + __half2float(o16));
+        a.res_next[(size_t)(a.row0 + r) * j.d_out + ch] = __half_as_ushort(__float2half_rn(rn));
+        sv.scratch[r * 64 + c] = __fmul_rn(rn, rn);
+      }
+    }
+    if (a.res_next && a.ss_next) {
+      // per row and 16-column group of this task: the squares summed in column order (the
+      // group of channel c is its 16-channel MMA tile, so a task holds whole groups)
+      __syncthreads();
+      const int rr = threadIdx.x >> 2, gq = threadIdx.x & 3;
+      const int m_lo = part * 4 / NT, m_hi = (part + 1) * 4 / NT;  // MMA tiles (= groups) of this task
+      if (rr < 8 * NT && rr < a.rows && gq >= m_lo && gq < m_hi) {
+        float ssum = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) ssum += sv.scratch[rr * 64 + 16 * gq + k];
+        a.ss_next[(size_t)(a.row0 + rr) * (j.d_out / 16) + sg * 4 + gq] = ssum;
+      }
+      __syncthreads();  // the scratch is reused by the next task
     }
   }
 }
@@ -923,7 +945,20 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
   // one cell's index copies, then the rotation of x (its loads not queued behind
   // the bulk of the prologue), then the rest of the prologue
   Cursor cur = decode_begin<F>(j1, sv, 1);
-  if (a.norm) {
+  if (a.norm && a.ss_in) {
+    // the rows' sums of squares from the previous layer's partials (16 columns each): one
+    // warp per row, lanes over the partials in a fixed order, then the warp's xor tree
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, n_part = a.d_model / 16;
+    for (int rr = warp; rr < a.rows; rr += kWarps) {
+      const float* p = a.ss_in + (size_t)(a.row0 + rr) * n_part;
+      float ss = 0.f;
+      for (int q = lane; q < n_part; q += 32) ss += __ldcg(p + q);
+#pragma unroll
+      for (int h = 16; h > 0; h >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, h);
+      if (lane == 0) s_inv[rr] = 1.0f / sqrtf(ss / (float)a.d_model + a.eps);
+    }
+    __syncthreads();
+  } else if (a.norm) {
     // pre-norm residual step for the pass's rows: r' = fp16(x + delta) over the whole row
     // (every CTA, for its own 1/rms), the 64-column slices s with s % grid == CTA written to
     // res_out. Each row is split into `parts` column ranges, one warp each (parts = warps per
@@ -970,7 +1005,8 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
             ss = fmaf(f.x, f.x, ss);
             ss = fmaf(f.y, f.y, ss);
           }
-          if ((g >> 3) % (int)gridDim.x == (int)blockIdx.x) *(reinterpret_cast<uint4*>(a.res_out + ro) + g) = rv;
+          if (a.res_out && (g >> 3) % (int)gridDim.x == (int)blockIdx.x)
+            *(reinterpret_cast<uint4*>(a.res_out + ro) + g) = rv;
         }
       }
 #pragma unroll
@@ -1013,9 +1049,9 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
     // one cell's index copies ahead of the h rotation, the rest after it (as for x)
     Cursor cur3 = decode_begin<F>(j3, sv, 1);
     decode_run<F, NT, float>(j3, a.hbuf, cur3, sv, nullptr, status);
-    output_tasks<NT>(a, j3, status);
+    output_tasks<NT>(a, j3, sv, status);
   } else {
-    output_tasks<NT>(a, j1, status);
+    output_tasks<NT>(a, j1, sv, status);
   }
 
   cp_async_wait<0>();

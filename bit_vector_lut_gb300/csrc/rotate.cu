@@ -137,6 +137,38 @@ __global__ void __launch_bounds__(256) residual_rmsnorm_kernel(const uint16_t* r
   }
 }
 
+// r_next = fp16(r + d) and, per 16 columns, the sum of r_next^2 in column order (each
+// square rounded to FP32, then added): the residual step that ends one layer of the
+// stack and starts the next one's RMSNorm. One CTA per row, one thread per 16 columns.
+__global__ void __launch_bounds__(256) residual_add_ss_kernel(const uint16_t* __restrict__ r,
+                                                              const uint16_t* __restrict__ d,
+                                                              uint16_t* __restrict__ r_next, float* __restrict__ ss,
+                                                              int n) {
+  const size_t base = (size_t)blockIdx.x * n;
+  for (int g = threadIdx.x; g < n / 16; g += blockDim.x) {
+    float s = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 rv = *reinterpret_cast<const uint4*>(r + base + 16 * g + 8 * h);
+      const uint4 dv = *reinterpret_cast<const uint4*>(d + base + 16 * g + 8 * h);
+      const __half2* rh = reinterpret_cast<const __half2*>(&rv);
+      const __half2* dh = reinterpret_cast<const __half2*>(&dv);
+      uint4 ov;
+      __half2* oh = reinterpret_cast<__half2*>(&ov);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 a = __half22float2(rh[k]), b = __half22float2(dh[k]);
+        oh[k] = __floats2half2_rn(a.x + b.x, a.y + b.y);
+        const float2 o = __half22float2(oh[k]);
+        s += __fmul_rn(o.x, o.x);
+        s += __fmul_rn(o.y, o.y);
+      }
+      *reinterpret_cast<uint4*>(r_next + base + 16 * g + 8 * h) = ov;
+    }
+    if (ss) ss[(size_t)blockIdx.x * (n / 16) + g] = s;
+  }
+}
+
 }  // namespace
 
 namespace {
@@ -172,6 +204,12 @@ cudaError_t launch_fwht_f32(const float* x, int rows, int n, int block, const ui
 cudaError_t launch_residual_rmsnorm(uint16_t* resid, const uint16_t* delta, int rows, int n, float eps,
                                     uint16_t* normed, cudaStream_t st) {
   residual_rmsnorm_kernel<<<rows, 256, 0, st>>>(resid, delta, resid, n, eps, normed);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_residual_add_ss(const uint16_t* r, const uint16_t* d, uint16_t* r_next, float* ss, int rows,
+                                   int n, cudaStream_t st) {
+  residual_add_ss_kernel<<<rows, 256, 0, st>>>(r, d, r_next, ss, n);
   return cudaGetLastError();
 }
 

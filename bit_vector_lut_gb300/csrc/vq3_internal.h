@@ -111,8 +111,15 @@ struct PersistArgs {
   // null), and r' is written to res_out (which aliases neither x nor res_delta)
   int norm;
   const uint16_t* res_delta;
-  uint16_t* res_out;
+  uint16_t* res_out;        // may be null: r' is then not written
   float eps;
+  // the residual stack chained by sums of squares (MLP only, norm set, res_delta null):
+  // ss_in (or null) holds the rows' sums of squares as FP32 partials per 16 columns,
+  // [rows][d / 16], in place of reading the rows; the output step also writes
+  // res_next = fp16(x + out) and its partials ss_next in the same layout
+  const float* ss_in;
+  uint16_t* res_next;
+  float* ss_next;
   int d_model, d_inter;     // MLP: hidden and intermediate widths; linear: d_model = d_in
   int d_model_out;          // linear: d_out
   int block_in, block_dn;   // rotation blocks of the gate/up (or linear) input and of the down input
@@ -177,6 +184,9 @@ int prefill_max_grid();           // most CTAs of one launch (one per SM)
 int prefill_grid(int rows, int d_in, int d_out, int swiglu);
 size_t prefill_part_bytes(int rows);  // size of PrefillArgs::part
 cudaError_t launch_prefill_gemm(const PrefillArgs& a, cudaStream_t st);
+// r_next = fp16(r + d), ss[row][g] = sum of r_next^2 over columns 16g .. 16g+15 (or none: ss null).
+cudaError_t launch_residual_add_ss(const uint16_t* r, const uint16_t* d, uint16_t* r_next, float* ss, int rows,
+                                   int n, cudaStream_t st);
 cudaError_t launch_residual_rmsnorm(uint16_t* resid, const uint16_t* delta, int rows, int n,
                                     float eps, uint16_t* normed, cudaStream_t st);
 // The same with the updated residual written to resid_out (may equal resid_in).

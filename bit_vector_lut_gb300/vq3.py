@@ -70,6 +70,8 @@ def _load() -> ctypes.CDLL:
                                            c_int, c_void_p, c_void_p, c_void_p]),
         "vq3_mlp_forward_residual": (c_int, [c_void_p, c_void_p, c_int, POINTER(vq3_mlp_layer), c_float, c_void_p,
                                              c_void_p, c_void_p, c_size_t, c_void_p]),
+        "vq3_mlp_prenorm_step": (c_int, [c_void_p, c_void_p, c_int, POINTER(vq3_mlp_layer), c_float, c_void_p,
+                                         c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
         "vq3_last_error": (ctypes.c_char_p, []),
         "vq3_version": (ctypes.c_char_p, []),
     }
@@ -307,3 +309,16 @@ def mlp_forward_residual(r_in: torch.Tensor, delta: torch.Tensor | None, layer: 
     _check(lib.vq3_mlp_forward_residual(r_in.data_ptr(), _ptr(delta), rows, ctypes.byref(layer.struct), eps,
                                         r_out.data_ptr(), out.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
     return out
+
+
+def mlp_prenorm_step(r: torch.Tensor, layer: MLP, out: torch.Tensor, r_next: torch.Tensor,
+                     ss: torch.Tensor | None = None, ss_next: torch.Tensor | None = None, eps: float = 1e-6,
+                     ws=None, stream=None) -> torch.Tensor:
+    """One pre-norm MLP sublayer: out = MLP(RMSNorm(r)), r_next = fp16(r + out); ss / ss_next are the
+    rows' FP32 sums of squares per 16 columns ([rows][d / 16]) of r and r_next."""
+    rows = r.shape[0]
+    if ws is None:
+        ws = workspace(mlp_workspace_bytes(rows, layer), r.device, stream)
+    _check(lib.vq3_mlp_prenorm_step(r.data_ptr(), _ptr(ss), rows, ctypes.byref(layer.struct), eps, out.data_ptr(),
+                                    r_next.data_ptr(), _ptr(ss_next), ws.data_ptr(), ws.numel(), _stream(stream)))
+    return r_next

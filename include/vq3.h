@@ -250,6 +250,27 @@ VQ3_API int vq3_mlp_forward_residual(const uint16_t* r_in, const uint16_t* delta
                                      const vq3_mlp_layer* layer, float eps, uint16_t* r_out, uint16_t* out,
                                      void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * One pre-norm MLP sublayer of the residual stack, chained through sums of squares so
+ * that no kernel reads whole rows for the RMS:
+ *   n      = fp16(r / sqrt(mean(r^2) + eps))   per row (unit-weight RMSNorm)
+ *   out    = the MLP block of n (as vq3_mlp_forward)
+ *   r_next = fp16(r + out)
+ *   ss_next[row][g] = sum over columns 16g .. 16g+15 of r_next^2, each square rounded
+ *                     to FP32 and added in column order
+ * ss, if not NULL, holds r's partial sums in the same layout (as the previous call wrote
+ * them) and the RMS is taken from them; NULL takes it from r's rows. ss_next may be NULL
+ * (the partials are then not written). Up to 16 rows everything runs inside the block's
+ * kernel (the residual step in its output step); from 17 rows on as an RMSNorm kernel,
+ * the tensor-core path and a residual kernel. r, out, r_next: device FP16 [rows][d];
+ * ss, ss_next: device FP32 [rows][d / 16]; all 16-byte aligned; out, r_next and ss_next
+ * alias neither r, ss nor each other. Workspace as vq3_mlp_forward. Errors as
+ * vq3_mlp_forward.
+ */
+VQ3_API int vq3_mlp_prenorm_step(const uint16_t* r, const float* ss, int rows, const vq3_mlp_layer* layer, float eps,
+                                 uint16_t* out, uint16_t* r_next, float* ss_next, void* workspace, size_t ws_bytes,
+                                 void* stream);
+
 /* Number of kernels one vq3_mlp_forward call launches at `rows` rows: one per
  * pass of 8 or 16 rows below 17 rows, 4 from 17 rows on (-1 on a bad
  * descriptor). */

@@ -131,6 +131,24 @@ def test_mlp_descriptor_checks():
     assert lib.vq3_mlp_host_workspace_bytes(8, ctypes.byref(ok)) > lib.vq3_mlp_workspace_bytes(8, ctypes.byref(ok))
 
 
+def test_prenorm_step_argument_checks():
+    lib = vq3.lib
+    L = vq3.vq3_mlp_layer(fake_linear(256, 512, 256), fake_linear(256, 512, 256), fake_linear(512, 256, 256))
+    f = lib.vq3_mlp_prenorm_step
+    ws = 1 << 24
+    # zero rows: nothing to do, no launch
+    assert f(0x40000, None, 0, ctypes.byref(L), 1e-6, 0x50000, 0x60000, None, 0x70000, ws, None) == 0
+    # bad eps, null r_next, r_next aliasing r, ss_next aliasing ss, out aliasing r
+    assert f(0x40000, None, 8, ctypes.byref(L), -1.0, 0x50000, 0x60000, None, 0x70000, ws, None) == -1
+    assert f(0x40000, None, 8, ctypes.byref(L), 1e-6, 0x50000, None, None, 0x70000, ws, None) == -1
+    assert f(0x40000, None, 8, ctypes.byref(L), 1e-6, 0x50000, 0x40000, None, 0x70000, ws, None) == -1
+    assert f(0x40000, 0x80000, 8, ctypes.byref(L), 1e-6, 0x50000, 0x60000, 0x80000, 0x70000, ws, None) == -1
+    assert f(0x40000, None, 8, ctypes.byref(L), 1e-6, 0x40000, 0x60000, None, 0x70000, ws, None) == -1
+    # misaligned partial sums
+    assert f(0x40000, 0x80004, 8, ctypes.byref(L), 1e-6, 0x50000, 0x60000, 0x90000, 0x70000, ws, None) == -2
+    assert "16-byte" in lib.vq3_last_error().decode()
+
+
 def test_fwht_argument_checks():
     lib = vq3.lib
     assert lib.fwht_rotate(0x40000, 0, 1024, 1024, None, 0x50000, None) == 0

@@ -1,7 +1,9 @@
 """GPU parity for one pre-norm residual layer, r' = fp16(r + delta), out =
 MLP(fp16(RMSNorm(r'))): fused into the block's kernel up to 16 rows, a separate
 RMSNorm kernel from 17 rows on (the stacked workload's residual add and RMSNorm,
-eps 1e-6, unit weight, FP16 storage), against the oracle."""
+eps 1e-6, unit weight, FP16 storage), against the oracle; and for the sublayer
+chained through sums of squares (out = MLP(RMSNorm(r)), r_next = fp16(r + out),
+FP32 partial sums of r_next^2 per 16 columns)."""
 
 import numpy as np
 import pytest
@@ -66,3 +68,47 @@ def test_residual_chain_matches_stack(vq3):
     vq3.residual_rmsnorm(ra, delta, 1e-6, normed)  # the last residual add: the standalone step
     ref = O.stack(x, blocks, 1e-6)
     assert_parity(ra.cpu().numpy(), ref, "4-layer residual chain")
+
+
+def partial_squares(r):
+    """FP32 sums of r^2 per 16 columns: each square rounded to FP32, added in column order."""
+    q = np.asarray(r, np.float16).astype(np.float32)
+    q = (q * q).astype(np.float32).reshape(q.shape[0], -1, 16)
+    s = np.zeros(q.shape[:2], np.float32)
+    for k in range(16):
+        s = (s + q[..., k]).astype(np.float32)
+    return s
+
+
+@pytest.mark.parametrize("rows", [1, 8, 16, 17, 40])
+@pytest.mark.parametrize("with_ss", [False, True])
+def test_prenorm_step(vq3, blk, rows, with_ss):
+    b, layer = blk
+    r = S.activations(S.rng(25, 0), rows, 5120)
+    ss = torch.from_numpy(partial_squares(r)).to(DEV) if with_ss else None
+    out = torch.empty((rows, 5120), dtype=torch.float16, device=DEV)
+    r_next = torch.empty_like(out)
+    ss_next = torch.empty((rows, 5120 // 16), dtype=torch.float32, device=DEV)
+    vq3.mlp_prenorm_step(f16(r), layer, out, r_next, ss=ss, ss_next=ss_next)
+    got = out.cpu().numpy()
+    assert_parity(got, O.mlp_f64(O.rmsnorm(r, 1e-6), b), f"prenorm step rows={rows} ss={with_ss}")
+    rn = r_next.cpu().numpy()
+    assert np.array_equal(rn.view(np.uint16), O.residual_add(r, got).view(np.uint16))
+    assert np.array_equal(ss_next.cpu().numpy(), partial_squares(rn))
+
+
+@pytest.mark.parametrize("rows", [8, 5, 20])
+def test_prenorm_chain_matches_stack(vq3, rows):
+    # four sublayers, each taking the previous one's residual and partial sums
+    blocks = [S.mlp_block(S.rng(30 + i, 1), 1024, 2048, 1024) for i in range(4)]
+    layers = [vq3.MLP.from_block(bb, DEV) for bb in blocks]
+    x = S.activations(S.rng(30, 0), rows, 1024)
+    r = [f16(x), torch.empty((rows, 1024), dtype=torch.float16, device=DEV)]
+    ss = [None, torch.empty((rows, 64), dtype=torch.float32, device=DEV),
+          torch.empty((rows, 64), dtype=torch.float32, device=DEV)]
+    out = torch.empty((rows, 1024), dtype=torch.float16, device=DEV)
+    for i, layer in enumerate(layers):
+        ss_in = ss[0] if i == 0 else ss[1 + (i - 1) % 2]
+        vq3.mlp_prenorm_step(r[i % 2], layer, out, r[(i + 1) % 2], ss=ss_in, ss_next=ss[1 + i % 2])
+    ref = O.stack(x, blocks, 1e-6)
+    assert_parity(r[len(layers) % 2].cpu().numpy(), ref, f"4-sublayer chain rows={rows}")
