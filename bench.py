@@ -35,7 +35,7 @@ REF_BUDGET_S = 100.0
 # DRAM bytes (read + write) of one persistent_kernel launch at T=8, from the ncu capture
 # summarised in profiles/persistent_kernel_mlp_5120x17408_T8.md; None when the kernel has
 # changed since that capture.
-TRAFFIC_PER_LAUNCH = 103_634_688
+TRAFFIC_PER_LAUNCH = 103_789_824
 
 
 def peaks() -> dict:
