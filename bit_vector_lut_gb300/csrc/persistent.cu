@@ -10,7 +10,13 @@
 //   h    = silu(s_g g) * (s_u u)       one task per 64 intermediate channels
 //   y    = W_d R_dn h                  decode, pieces
 //   out  = fp16(s_d y)                 one task per 64 output channels x 8-row tile
-// A single matrix runs the first decode and the output tasks.
+// A single matrix runs the first decode and the output tasks (adding its low-rank
+// correction U V x' when it has factors).
+//
+// In a stacked layer the pre-norm residual step is folded in: either the prologue
+// forms r' = fp16(x + delta) over whole rows and its RMS, or the RMS comes from the
+// previous layer's partial sums of squares; the x rotation normalises on the fly,
+// and the output tasks can also write r + out and that row's new partial sums.
 //
 // The rotations R = blockdiag(H_b diag(s)) / sqrt(b) are not separate steps: a
 // decoding CTA rotates the chunks of x (or h) its column groups lie in, straight
