@@ -141,7 +141,9 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_rank{gpu_index}.csv")
+        # the raw samples (the JSON line carries their summary); VQ3_BENCH_OUT picks the folder
+        out_dir = os.environ.get("VQ3_BENCH_OUT", os.path.join(ROOT, "bench_out"))
+        self.path = os.path.join(out_dir, f"clocks_bench_rank{gpu_index}.csv")
 
     def __enter__(self):
         try:
