@@ -112,3 +112,38 @@ def test_prenorm_chain_matches_stack(vq3, rows):
         vq3.mlp_prenorm_step(r[i % 2], layer, out, r[(i + 1) % 2], ss=ss_in, ss_next=ss[1 + i % 2])
     ref = O.stack(x, blocks, 1e-6)
     assert_parity(r[len(layers) % 2].cpu().numpy(), ref, f"4-sublayer chain rows={rows}")
+
+
+@pytest.mark.parametrize("fmt", ["2x16", "lut4"])
+@pytest.mark.parametrize("rows", [8, 20])
+def test_prenorm_step_formats(vq3, fmt, rows):
+    bb = S.mlp_block(S.rng(40, 1), 1024, 2048, 1024, fmt)
+    layer = vq3.MLP.from_block(bb, DEV)
+    r = S.activations(S.rng(41, 0), rows, 1024)
+    out = torch.empty((rows, 1024), dtype=torch.float16, device=DEV)
+    r_next = torch.empty_like(out)
+    ss_next = torch.empty((rows, 64), dtype=torch.float32, device=DEV)
+    vq3.mlp_prenorm_step(f16(r), layer, out, r_next, ss=torch.from_numpy(partial_squares(r)).to(DEV),
+                         ss_next=ss_next)
+    got = out.cpu().numpy()
+    assert_parity(got, O.mlp_f64(O.rmsnorm(r, 1e-6), bb), f"prenorm step {fmt} rows={rows}")
+    rn = r_next.cpu().numpy()
+    assert np.array_equal(rn.view(np.uint16), O.residual_add(r, got).view(np.uint16))
+    assert np.array_equal(ss_next.cpu().numpy(), partial_squares(rn))
+
+
+@pytest.mark.parametrize("rows", [8, 20])
+def test_prenorm_step_repeats_bit_identical(vq3, blk, rows):
+    _, layer = blk
+    r = f16(S.activations(S.rng(42, 0), rows, 5120))
+    ss = torch.from_numpy(partial_squares(r.cpu().numpy())).to(DEV)
+    outs = []
+    for _ in range(2):
+        out = torch.empty((rows, 5120), dtype=torch.float16, device=DEV)
+        r_next = torch.empty_like(out)
+        ss_next = torch.empty((rows, 320), dtype=torch.float32, device=DEV)
+        vq3.mlp_prenorm_step(r, layer, out, r_next, ss=ss, ss_next=ss_next)
+        outs.append((out.cpu().numpy().view(np.uint16), r_next.cpu().numpy().view(np.uint16),
+                     ss_next.cpu().numpy().view(np.uint32)))
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b)
