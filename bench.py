@@ -32,9 +32,9 @@ BLOCK_BYTES = 3 * S.stream_bytes(HIDDEN, INTER) + 2 * (2 * INTER + HIDDEN) + 3 *
 FLOP_PER_ROW = 2 * (2 * HIDDEN * INTER + INTER * HIDDEN)  # 534,773,760
 METRIC = "VQ3 Hadamard-MLP rows/s; weight GB/s vs HBM peak @T=8; TFLOP/s @prefill"
 REF_BUDGET_S = 100.0
-# DRAM bytes (read + write) of one persistent_kernel launch at T=8, from the ncu capture
-# summarised in profiles/persistent_kernel_mlp_5120x17408_T8.md; None when the kernel has
-# changed since that capture.
+# DRAM bytes (read + write) of one persistent_kernel launch at T=8, from one ncu capture of
+# the kernel (dram__bytes_read.sum + dram__bytes_write.sum); None when the kernel has changed
+# since that capture.
 TRAFFIC_PER_LAUNCH = 103_789_824
 
 

@@ -71,12 +71,26 @@ extern "C" int vq3_mlp_forward_noalloc(const uint16_t* x, int rows, const vq3_ml
   if (e != cudaSuccess)
     return set_error(VQ3_ECUDA, "mlp_noalloc: cudaGetSymbolAddress: %s (%s)", cudaGetErrorName(e),
                      cudaGetErrorString(e));
-  // The array keeps the previous call's contents; the counter words must start at zero.
+  // The array keeps the previous call's contents. The status word (offset 0) and the
+  // counter words after it must start at zero: one clear covers both, so a wait that
+  // gave up in an earlier call does not make this call skip its waits.
   size_t off = 0, bytes = 0;
   mlp_counter_range(layer, &off, &bytes);
-  e = cudaMemsetAsync(static_cast<char*>(scratch) + off, 0, bytes, static_cast<cudaStream_t>(stream));
+  e = cudaMemsetAsync(scratch, 0, off + bytes, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess)
-    return set_error(VQ3_ECUDA, "mlp_noalloc: clearing counters: %s (%s)", cudaGetErrorName(e),
+    return set_error(VQ3_ECUDA, "mlp_noalloc: clearing the status and counter words: %s (%s)", cudaGetErrorName(e),
                      cudaGetErrorString(e));
   return mlp_forward_capped(x, rows, layer, out, scratch, kNoAllocScratchBytes, stream, cap);
+}
+
+extern "C" int vq3_noalloc_status(int* status_host, void* stream) {
+  if (!status_host) return set_error(VQ3_EINVAL, "noalloc_status: null pointer");
+  void* scratch = nullptr;
+  cudaError_t e = scratch_address(&scratch);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(status_host, scratch, sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess)
+    return set_error(VQ3_ECUDA, "noalloc_status: %s (%s)", cudaGetErrorName(e), cudaGetErrorString(e));
+  return set_error(VQ3_OK, "");
 }

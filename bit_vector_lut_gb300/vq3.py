@@ -72,6 +72,8 @@ def _load() -> ctypes.CDLL:
                                              c_void_p, c_void_p, c_size_t, c_void_p]),
         "vq3_mlp_prenorm_step": (c_int, [c_void_p, c_void_p, c_int, POINTER(vq3_mlp_layer), c_float, c_void_p,
                                          c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+        "vq3_mlp_forward_noalloc": (c_int, [c_void_p, c_int, POINTER(vq3_mlp_layer), c_void_p, c_void_p]),
+        "vq3_noalloc_status": (c_int, [POINTER(c_int), c_void_p]),
         "vq3_last_error": (ctypes.c_char_p, []),
         "vq3_version": (ctypes.c_char_p, []),
     }
@@ -253,6 +255,23 @@ def mlp_forward(x: torch.Tensor, layer: MLP, out=None, ws=None, stream=None) -> 
     _check(lib.vq3_mlp_forward(x.data_ptr(), rows, ctypes.byref(layer.struct), out.data_ptr(), ws.data_ptr(),
                                ws.numel(), _stream(stream)))
     return out
+
+
+def mlp_forward_noalloc(x: torch.Tensor, layer: MLP, out=None, stream=None) -> torch.Tensor:
+    """The MLP block with its scratch in the library's fixed device array (no workspace)."""
+    rows = x.shape[0]
+    if out is None:
+        out = torch.empty((rows, layer.down.d_out), dtype=torch.float16, device=x.device)
+    _check(lib.vq3_mlp_forward_noalloc(x.data_ptr(), rows, ctypes.byref(layer.struct), out.data_ptr(),
+                                       _stream(stream)))
+    return out
+
+
+def noalloc_status(stream=None) -> int:
+    """Status word of the fixed array: 0, or 3 when a wait in the last no-alloc call gave up."""
+    v = c_int(0)
+    _check(lib.vq3_noalloc_status(ctypes.byref(v), _stream(stream)))
+    return int(v.value)
 
 
 def mlp_kernel_launches(rows: int, layer: MLP) -> int:

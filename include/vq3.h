@@ -129,11 +129,20 @@ typedef struct vq3_mlp_layer {
 } vq3_mlp_layer;
 
 /* Size in bytes of one matrix's GPU-layout indices (equal to the canonical
- * stream's size: 6 bits per output pair and input column). 0 if unsupported. */
+ * stream's size: 6 bits per output pair and input column, i.e. 3 bits per weight).
+ * Cited: model card "anemll/anemll-forge-qwen3.8-27B", "Release 0.2" bullet
+ * "Three bits per MLP weight" (one six-bit index per pair of output channels).
+ * 0 if unsupported (d_in or d_out not a positive multiple of 64). */
 VQ3_API size_t vq3_packed_bytes(int d_in, int d_out);
 
 /*
  * Host-side, offline. Reorders a canonical index stream into the GPU layout.
+ * Cited: model card "anemll/anemll-forge-qwen3.8-27B", "Release 0.2" bullet
+ * "Three bits per MLP weight" (six-bit indices, one per output pair and input
+ * column) and "Files and runtime compatibility" (the shipped three-bit vector
+ * LUTs). The pages fix neither the index order nor the bit order; the canonical
+ * stream below is the plainest reading (row-major [d_out/2][d_in] indices,
+ * least significant bit first, "packed little-endian" as the workloads state).
  * canonical: host, ceil(6*(d_out/2)*d_in/8) bytes. Index k = p*d_in + i
  *   (output pair p, input column i) occupies stream bits [6k, 6k+6), stream bit
  *   j being bit (j mod 8) of byte j/8 (least significant bit first).
@@ -144,7 +153,8 @@ VQ3_API size_t vq3_packed_bytes(int d_in, int d_out);
 VQ3_API int vq3_pack_layout(const uint8_t* canonical, int d_in, int d_out, void* dst_host);
 
 /* Host-side inverse of vq3_pack_layout (pad bits of the canonical stream are
- * written as zero). Same errors. */
+ * written as zero), so the private GPU layout round-trips to the interchange
+ * stream bit for bit. Same citation and errors as vq3_pack_layout. */
 VQ3_API int vq3_unpack_layout(const void* packed_host, int d_in, int d_out, uint8_t* canonical);
 
 /* The same three calls for any index format (VQ3_FORMAT_*): the GPU layout is
@@ -178,11 +188,12 @@ VQ3_API int fwht_rotate(const uint16_t* x, int rows, int n, int block, const uin
  * count. Calls that share a workspace must not overlap on the GPU (same
  * stream, or ordered by events).
  * Device status: the first 32-bit word of the workspace stays 0. It becomes 3
- * if a wait inside a kernel gave up after its bounded number of polls (about
- * a second); the kernel still ends, the outputs of that call are invalid, and
- * later calls on the workspace skip their waits until vq3_workspace_init
- * clears the word.
+ * if a wait inside a kernel gave up after its time bound (about a second); the
+ * kernel still ends, the outputs of that call are invalid, and later calls on
+ * the workspace skip their waits until vq3_workspace_init clears the word.
  * vq3_workspace_status copies it to the host after the stream's prior work.
+ * These four calls have no counterpart on the pages: they are this library's
+ * interface for caller-owned scratch.
  */
 VQ3_API size_t vq3_linear_workspace_bytes(int rows, const vq3_linear* L);
 VQ3_API size_t vq3_mlp_workspace_bytes(int rows, const vq3_mlp_layer* layer);
@@ -191,6 +202,11 @@ VQ3_API int vq3_workspace_status(const void* workspace, int* status_host, void* 
 
 /*
  * One rotated VQ3 linear layer: out = fp16( W (R x) ), FP32 accumulation.
+ * Cited: model card "anemll/anemll-forge-qwen3.8-27B", "Release 0.2" bullets
+ * "Three bits per MLP weight" (W = diag(scales) C[idx]) and "Token-mixer
+ * rotations" (the input multiplied online by 1,024-wide Hadamard blocks with
+ * seeded signs, the weights stored in the rotated basis); table row "Token
+ * mixers" for the optional rank-64 factors.
  * x: device FP16 [rows][d_in]; out: device FP16 [rows][d_out] (must not alias x).
  * Errors: VQ3_EINVAL, VQ3_EALIGN, VQ3_EUNSUPPORTED, VQ3_ENOSPACE, VQ3_ECUDA.
  */
@@ -237,6 +253,7 @@ VQ3_API int vq3_delta_rule_forward(const uint16_t* q, const uint16_t* k, const u
                                    uint16_t* out, void* stream);
 
 /*
+ * Cited as vq3_residual_rmsnorm and vq3_mlp_forward (the two fused).
  * One layer of the pre-norm residual stack: r' = fp16(r_in + delta) (r_in alone when
  * delta is NULL), n = fp16(r' / sqrt(mean(r'^2) + eps)) per row, out = the MLP block
  * of n (as vq3_mlp_forward); r' is written to r_out. Up to 16 rows the residual
@@ -251,6 +268,8 @@ VQ3_API int vq3_mlp_forward_residual(const uint16_t* r_in, const uint16_t* delta
                                      void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Cited as vq3_residual_rmsnorm and vq3_mlp_forward (the two fused; the partial sums of
+ * squares are this library's way to hand the next RMS over, not the pages').
  * One pre-norm MLP sublayer of the residual stack, chained through sums of squares so
  * that no kernel reads whole rows for the RMS:
  *   n      = fp16(r / sqrt(mean(r^2) + eps))   per row (unit-weight RMSNorm)
@@ -271,12 +290,14 @@ VQ3_API int vq3_mlp_prenorm_step(const uint16_t* r, const float* ss, int rows, c
                                  uint16_t* out, uint16_t* r_next, float* ss_next, void* workspace, size_t ws_bytes,
                                  void* stream);
 
-/* Number of kernels one vq3_mlp_forward call launches at `rows` rows: one per
+/* Interface query (no counterpart on the pages).
+ * Number of kernels one vq3_mlp_forward call launches at `rows` rows: one per
  * pass of 8 or 16 rows below 17 rows, 4 from 17 rows on (-1 on a bad
  * descriptor). */
 VQ3_API int vq3_mlp_kernel_launches(int rows, const vq3_mlp_layer* layer);
 
 /*
+ * Cited as vq3_mlp_forward (an interface convenience for host buffers).
  * Same as vq3_mlp_forward with HOST buffers: copies x (pinned or pageable host
  * memory) to the workspace, runs the block, copies the result back into
  * out_host and waits for the stream. Workspace: vq3_mlp_host_workspace_bytes.
@@ -305,23 +326,47 @@ VQ3_API int vq3_mlp_forward_host(const uint16_t* x_host, int rows, const vq3_mlp
  *   - Every call on a device shares the one array and it keeps the previous
  *     call's contents (the call clears the parts that must start at zero), so
  *     calls that overlap on the GPU race: order them on one stream or with events.
+ *   - The array starts with a device status word, like a workspace. Each call
+ *     clears it (with the counter words) before its kernels run; it becomes 3 if
+ *     a bounded wait inside that call gave up (about a second), and that call's
+ *     output is then invalid. vq3_noalloc_status reads it.
  * Arguments, output and errors otherwise as vq3_mlp_forward.
  */
 #define VQ3_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 VQ3_API int vq3_mlp_forward_noalloc(const uint16_t* x, int rows, const vq3_mlp_layer* layer, uint16_t* out,
                                     void* stream);
 
+/* Status word of the no-alloc array on the current device after the stream's prior
+ * work (0, or 3 when a wait in the last vq3_mlp_forward_noalloc call gave up); copies
+ * it to *status_host and waits for the stream. Allocates nothing. Errors: VQ3_EINVAL
+ * (null pointer), VQ3_ECUDA. */
+VQ3_API int vq3_noalloc_status(int* status_host, void* stream);
+
 /*
  * Pre-norm residual step between stacked layers:
  *   resid  <- fp16(resid + delta)                       (skipped if delta == NULL)
  *   normed <- fp16(resid / sqrt(mean(resid^2) + eps))    (unit weight, FP32 math)
+ * Cited: model card "anemll/anemll-forge-qwen3.8-27B", "Release 0.2" table row
+ * "MLP gate / up / down" (the VQ3 MLP in all 64 layers of the dense model) and
+ * "ANEMLL ANE LLM conversion pipeline", opening summary "Model rewrite for ANE"
+ * (FP16-only graphs with a precise RMSNorm built from ANE ops). The pages give
+ * neither the norm's placement nor its epsilon: pre-norm, unit weight and eps
+ * inside the square root is the plainest reading, with eps = 1e-6 as the
+ * stacked-layer workload states.
  * resid, delta, normed: device FP16 [rows][n]; normed may not alias resid.
+ * Errors: VQ3_EINVAL (rows < 0, n <= 0, eps < 0 or NaN, null resid or normed),
+ * VQ3_EALIGN (a pointer not 16-byte aligned), VQ3_ECUDA.
  */
 VQ3_API int vq3_residual_rmsnorm(uint16_t* resid, const uint16_t* delta, int rows, int n, float eps,
                          uint16_t* normed, void* stream);
 
 /*
- * Debug/test: writes the dense weight of L from its GPU layout.
+ * Debug/test: writes the dense weight of L from its GPU layout. Cited: model card
+ * "anemll/anemll-forge-qwen3.8-27B", "Release 0.2" bullet "Three bits per MLP
+ * weight" (centroid component c of index idx[p][i] is the weight of output
+ * channel 2p+c at input i, times that channel's scale) and "ANEMLL ANE LLM
+ * conversion pipeline", "Facts" (the two-component vectors run along output
+ * channels).
  * apply_scale = 0: w_out[o][i] = C[idx[o/2][i]][o%2] (exact copy of the FP16 centroid);
  * apply_scale = 1: w_out[o][i] = fp16(fp32(scale[o]) * fp32(C[...])) (the FP32
  * product is exact, so this is the correctly rounded weight).

@@ -45,6 +45,31 @@ def test_noalloc_matches_workspace_entry_point_twice():
         assert rc == 0, vq3.lib.vq3_last_error().decode()
         torch.cuda.synchronize(dev)
         assert_parity(out.cpu().numpy(), ref, f"no-alloc call {call}")
+        # every wait of the call ended in time: the array's status word reads 0
+        assert vq3.noalloc_status(stream) == 0
+
+
+def test_noalloc_allocates_no_device_memory():
+    # the point of the entry point: after a first call (which looks up the array's
+    # address), a call changes neither the driver's free memory nor torch's pool
+    vq3, noalloc = _lib()
+    dev = torch.device("cuda:0")
+    wl = S.mlp_27b(seed=1, rows=64)
+    layer = vq3.MLP.from_block(wl.layers[0], dev)
+    x = torch.from_numpy(wl.x).to(dev)
+    out = torch.empty_like(x)
+    stream = torch.cuda.current_stream(dev)
+    rc = noalloc(x.data_ptr(), x.shape[0], ctypes.byref(layer.struct), out.data_ptr(), stream.cuda_stream)
+    assert rc == 0, vq3.lib.vq3_last_error().decode()
+    torch.cuda.synchronize(dev)
+    free0, _ = torch.cuda.mem_get_info(dev)
+    reserved0 = torch.cuda.memory_reserved(dev)
+    rc = noalloc(x.data_ptr(), x.shape[0], ctypes.byref(layer.struct), out.data_ptr(), stream.cuda_stream)
+    assert rc == 0, vq3.lib.vq3_last_error().decode()
+    torch.cuda.synchronize(dev)
+    free1, _ = torch.cuda.mem_get_info(dev)
+    assert free1 == free0
+    assert torch.cuda.memory_reserved(dev) == reserved0
 
 
 def test_noalloc_runs_rows_beyond_one_pass():
