@@ -62,6 +62,7 @@ from __future__ import annotations
 
 import functools
 import math
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -230,20 +231,29 @@ def lowrank_f64(xr, m) -> np.ndarray | None:
     return z @ _as_f16_f64(U).T
 
 
-def linear_f64(x, m, round_rotated: bool = False, row_chunk: int = 2048) -> np.ndarray:
+def linear_f64(x, m, row_chunk: int = 2048, workers: int = 1) -> np.ndarray:
     """y = W (R x) in float64 for one VQ3 matrix `m` (fields as in synth.inputs.Matrix),
     plus U (V R x) when the matrix carries low-rank factors.
 
     x is taken at its own precision (FP16 inputs convert exactly); nothing is rounded.
+    The output channels are computed in ranges of `row_chunk`; with workers > 1 the
+    ranges run on that many threads (each output is computed the same way either way).
     """
     xr = rotate(np.asarray(x, dtype=np.float64), m.block, m.signs)
-    if round_rotated:
-        xr = xr.astype(np.float16).astype(np.float64)
     y = np.empty((xr.shape[0], m.d_out), dtype=np.float64)
-    for r0 in range(0, m.d_out, row_chunk):
+
+    def out_range(r0):
         r1 = min(m.d_out, r0 + row_chunk)
         W = dense_weight(m.stream, m.codebook, m.scales, m.d_in, m.d_out, rows=(r0, r1), fmt=fmt_of(m))
         y[:, r0:r1] = xr @ W.T
+
+    starts = range(0, m.d_out, row_chunk)
+    if workers > 1:
+        with ThreadPoolExecutor(workers) as ex:
+            list(ex.map(out_range, starts))
+    else:
+        for r0 in starts:
+            out_range(r0)
     lr = lowrank_f64(xr, m)
     if lr is not None:
         y += lr
@@ -255,22 +265,16 @@ def linear(x, m) -> np.ndarray:
     return linear_f64(x, m).astype(np.float16)
 
 
-def mlp_f64(x, blk, round_intermediates: bool = False) -> np.ndarray:
-    """SwiGLU block: y = W_d R_d (silu(W_g R x) * (W_u R x)), float64 throughout.
-
-    With round_intermediates the rotated inputs and h are rounded to FP16 where a
-    kernel stores them; this is a diagnostic to tell rounding from bugs.
-    """
-    g = linear_f64(x, blk.gate, round_rotated=round_intermediates)
-    u = linear_f64(x, blk.up, round_rotated=round_intermediates)
+def mlp_f64(x, blk, workers: int = 1) -> np.ndarray:
+    """SwiGLU block: y = W_d R_d (silu(W_g R x) * (W_u R x)), float64 throughout."""
+    g = linear_f64(x, blk.gate, workers=workers)
+    u = linear_f64(x, blk.up, workers=workers)
     h = silu(g) * u
-    if round_intermediates:
-        h = h.astype(np.float16).astype(np.float64)
-    return linear_f64(h, blk.down, round_rotated=round_intermediates)
+    return linear_f64(h, blk.down, workers=workers)
 
 
-def mlp(x, blk) -> np.ndarray:
-    return mlp_f64(x, blk).astype(np.float16)
+def mlp(x, blk, workers: int = 1) -> np.ndarray:
+    return mlp_f64(x, blk, workers).astype(np.float16)
 
 
 def rmsnorm(r, eps: float = 1e-6) -> np.ndarray:
@@ -283,14 +287,16 @@ def residual_add(r, delta) -> np.ndarray:
     return (_as_f16_f64(r) + _as_f16_f64(delta)).astype(np.float16)
 
 
-def stack(x, blocks, eps: float = 1e-6, trace: list | None = None) -> np.ndarray:
-    """Pre-norm residual stack: r <- fp16(r + fp16(MLP_l(fp16(RMSNorm(r))))) for each layer."""
+def stack(x, blocks, eps: float = 1e-6, trace: list | None = None, workers: int = 1) -> np.ndarray:
+    """Pre-norm residual stack: r <- fp16(r + fp16(MLP_l(fp16(RMSNorm(r))))) for each layer.
+
+    `blocks` may be any iterable (a generator keeps one layer in host memory at a time)."""
     r = np.asarray(x, dtype=np.float16)
     if trace is not None:
         trace.append(r.copy())
     for blk in blocks:
         n = rmsnorm(r, eps)
-        r = residual_add(r, mlp(n, blk))
+        r = residual_add(r, mlp(n, blk, workers))
         if trace is not None:
             trace.append(r.copy())
     return r

@@ -6,6 +6,8 @@ C ABI and kernels as the three-bit format (model card
 / down" and "Token mixers"). Layout and lookups are compared bit for bit; float
 outputs with the tolerance of tests/parity.py."""
 
+import os
+
 import numpy as np
 import pytest
 
@@ -78,12 +80,14 @@ def test_codebook_permutation_invariance_bit_exact(vq3, fmt):
 @pytest.fixture(scope="module", params=FMTS)
 def block(vq3, request):
     fmt = request.param
-    wl = S.mlp_format(fmt, rows=64)
+    # 2048 rows: the benchmark times these formats there (the first rows of a taller X
+    # equal a shorter X, so one oracle run serves every row count below)
+    wl = S.mlp_format(fmt, rows=2048)
     blk = wl.layers[0]
-    return fmt, wl, blk, vq3.MLP.from_block(blk, DEV), O.mlp_f64(wl.x, blk)
+    return fmt, wl, blk, vq3.MLP.from_block(blk, DEV), O.mlp_f64(wl.x, blk, workers=min(16, os.cpu_count() or 1))
 
 
-@pytest.mark.parametrize("rows", [1, 8, 16, 17, 64])
+@pytest.mark.parametrize("rows", [1, 8, 16, 17, 64, 2048])
 def test_mlp_5120x17408(vq3, block, rows):
     fmt, wl, blk, layer, ref = block
     got = vq3.mlp_forward(f16(wl.x[:rows]), layer).cpu().numpy()

@@ -292,6 +292,20 @@ def test_stack_matches_layerwise_definition():
     assert np.array_equal(rr, r)
 
 
+def test_threaded_ranges_and_generator_blocks_match():
+    # output channels in several ranges on several threads: the same values as one serial
+    # pass, and as the brute force; a stack fed a generator equals one fed a list
+    m = small_matrix(40, 8, 16, 4, True)
+    x = S.activations(S.rng(41, 0), 3, 8)
+    serial = O.linear_f64(x, m)
+    threaded = O.linear_f64(x, m, row_chunk=4, workers=3)
+    assert np.array_equal(serial, threaded)
+    assert np.allclose(threaded, np.array(bf.linear(x.tolist(), m)), rtol=1e-12, atol=1e-15)
+    wl = S.mlp_stack(seed=6, rows=2, layers=3, hidden=64, inter=128, block=64)
+    ref = O.stack(wl.x, wl.layers)
+    assert np.array_equal(O.stack(wl.x, (b for b in wl.layers), workers=2), ref)
+
+
 def test_rmsnorm_unit_rms():
     x = S.activations(S.rng(3, 0), 4, 512) * np.float16(3)
     n = O.rmsnorm(x).astype(np.float64)
