@@ -25,8 +25,8 @@
 //
 // There are no grid-wide barriers. Every consumer waits only for what it reads,
 // through counters in the workspace: segment groups count the CTAs that wrote
-// their pieces, h chunks count finished SwiGLU tasks. Waits poll a bounded number
-// of times (on timeout the status word gets 3 and the kernel still ends). The
+// their pieces, h chunks count finished SwiGLU tasks. Waits are bounded in time
+// (on timeout the status word gets 3 and the kernel still ends). The
 // cooperative launch makes all CTAs co-resident and no wait depends on work
 // ordered after it in any CTA, so every wait ends. The last CTA to finish
 // resets the counters to zero for the next launch.
@@ -63,7 +63,7 @@ struct Tab {
   static constexpr uint32_t kStride = (uint32_t)Fmt<F>::kEntries * 128u;  // 8 KB or 2 KB
   static constexpr uint32_t kAlign = 2u * kStride;
 };
-constexpr long long kSpinLimit = 1ll << 21;  // polls of one wait: well over a second
+constexpr unsigned long long kWaitNs = 1000000000ull;  // a wait gives up after one second
 
 // ------------------------------------------------------------------ primitives
 
@@ -141,17 +141,30 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
 
 // ------------------------------------------------------------------ counters
 
-// Thread 0 polls until *p >= target (bounded; after any timeout in the launch,
-// status 3, it returns at once).
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Thread 0 polls until *p >= target. The counter is polled first, so a wait whose data is
+// ready costs one acquire load. Otherwise the wait is bounded in time: after kWaitNs it
+// sets the status word to 3 and returns; and once any wait of the launch has given up
+// (status 3, checked every 64 polls) every wait returns at once.
 __device__ __forceinline__ void poll_geq(const unsigned* p, unsigned target, int* status) {
+  if (ld_acquire(p) >= target) return;
   if (*(volatile int*)status == 3) return;
-  long long it = 0;
-  while (ld_acquire(p) < target) {
-    if (++it > kSpinLimit) {
-      atomicExch(status, 3);
-      return;
-    }
+  const unsigned long long t0 = globaltimer_ns();
+  for (unsigned it = 1;; ++it) {
     __nanosleep(32);
+    if (ld_acquire(p) >= target) return;
+    if ((it & 63u) == 0u) {
+      if (*(volatile int*)status == 3) return;
+      if (globaltimer_ns() - t0 > kWaitNs) {
+        atomicExch(status, 3);
+        return;
+      }
+    }
   }
 }
 
