@@ -344,33 +344,39 @@ cudaError_t run_prefill_mlp(const uint16_t* x, int rows, const vq3_mlp_layer& l,
   uint16_t* xr = reinterpret_cast<uint16_t*>(ws + w.xr);
   float* h = reinterpret_cast<float*>(ws + w.h);
   uint16_t* hr = reinterpret_cast<uint16_t*>(ws + w.hr);
-  cudaError_t e = launch_fwht(x, rows, H, l.gate.block, l.gate.signs, xr, st);
+  // x' and h' in the operand order of the GEMM kernel that serves this many rows
+  const bool wide = prefill_wide(rows);
+  auto gemm = wide ? launch_prefill_wide_gemm : launch_prefill_gemm;
+  cudaError_t e = launch_fwht(x, rows, H, l.gate.block, l.gate.signs, xr, st, wide ? 0 : 1);
   if (e != cudaSuccess) return e;
   PrefillArgs gu = prefill_args(xr, rows, l.gate, &l.up, ws, w);
   gu.out32 = h;
-  if ((e = launch_prefill_gemm(gu, st)) != cudaSuccess) return e;
-  if ((e = launch_fwht_f32(h, rows, I, l.down.block, l.down.signs, hr, st)) != cudaSuccess) return e;
+  if ((e = gemm(gu, st)) != cudaSuccess) return e;
+  if ((e = launch_fwht_f32(h, rows, I, l.down.block, l.down.signs, hr, st, wide ? 0 : 1)) != cudaSuccess) return e;
   PrefillArgs dn = prefill_args(hr, rows, l.down, nullptr, ws, w);
   dn.out16 = out;
-  return launch_prefill_gemm(dn, st);
+  return gemm(dn, st);
 }
 
 cudaError_t run_prefill_linear(const uint16_t* x, int rows, const vq3_linear& L, char* ws, uint16_t* out,
                                cudaStream_t st) {
   const PrefillWs w = prefill_ws(rows, L.d_in, 0, linear_ctl_bytes(L.d_in, L.d_out), L.lr_rank, L.d_out);
   uint16_t* xr = reinterpret_cast<uint16_t*>(ws + w.xr);
-  cudaError_t e = launch_fwht(x, rows, L.d_in, L.block, L.signs, xr, st);
+  // x' in the operand order of the GEMM kernel that serves this many rows
+  const bool wide = prefill_wide(rows);
+  cudaError_t e = launch_fwht(x, rows, L.d_in, L.block, L.signs, xr, st, wide ? 0 : 1);
   if (e != cudaSuccess) return e;
   PrefillArgs a = prefill_args(xr, rows, L, nullptr, ws, w);
   if (L.lr_rank) {
     float* ylr = reinterpret_cast<float*>(ws + w.ylr);
     float* zpart = reinterpret_cast<float*>(ws + w.zpart);
-    if ((e = launch_lowrank(xr, rows, L.d_in, L.lr_v, L.lr_u, L.lr_rank, L.d_out, zpart, ylr, st)) != cudaSuccess)
+    if ((e = launch_lowrank(xr, rows, L.d_in, L.lr_v, L.lr_u, L.lr_rank, L.d_out, zpart, ylr, st, wide ? 0 : 1)) !=
+        cudaSuccess)
       return e;
     a.lr_y = ylr;
   }
   a.out16 = out;
-  return launch_prefill_gemm(a, st);
+  return wide ? launch_prefill_wide_gemm(a, st) : launch_prefill_gemm(a, st);
 }
 
 // Runs fn(i) for i in [0, n) on up to hardware_concurrency host threads (the

@@ -34,7 +34,7 @@ constexpr int kChunk = 512;  // inputs per CTA of the projection
 
 __global__ void __launch_bounds__(256) lowrank_project_kernel(const uint16_t* __restrict__ xr, int rows, int d_in,
                                                               const uint16_t* __restrict__ V, int rank,
-                                                              float* __restrict__ part) {
+                                                              float* __restrict__ part, int xr_mma_order) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kc = blockIdx.x;
   const int j0 = blockIdx.y * 8;
@@ -51,7 +51,18 @@ __global__ void __launch_bounds__(256) lowrank_project_kernel(const uint16_t* __
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
         float vv[8];
-        unpack8(__ldg(reinterpret_cast<const uint4*>(V + (size_t)(j0 + jj) * d_in + i0)), vv);
+        if (xr_mma_order) {
+          // x' holds the inputs of its 16-column group in the GEMM's operand order: take
+          // the V entries of the inputs that positions i0 .. i0+7 hold
+          const uint16_t* vrow = V + (size_t)(j0 + jj) * d_in + (i0 & ~15);
+          float v16[16];
+          unpack8(__ldg(reinterpret_cast<const uint4*>(vrow)), *reinterpret_cast<float(*)[8]>(v16));
+          unpack8(__ldg(reinterpret_cast<const uint4*>(vrow + 8)), *reinterpret_cast<float(*)[8]>(v16 + 8));
+#pragma unroll
+          for (int k = 0; k < 8; ++k) vv[k] = v16[mma_order_input((i0 & 15) + k)];
+        } else {
+          unpack8(__ldg(reinterpret_cast<const uint4*>(V + (size_t)(j0 + jj) * d_in + i0)), vv);
+        }
 #pragma unroll
         for (int k = 0; k < 8; ++k) acc[jj] = fmaf(vv[k], xv[k], acc[jj]);
       }
@@ -112,11 +123,11 @@ __global__ void __launch_bounds__(256) lowrank_expand_kernel(const float* __rest
 int lowrank_chunks(int d_in) { return (d_in + kChunk - 1) / kChunk; }
 
 cudaError_t launch_lowrank(const uint16_t* xr, int rows, int d_in, const uint16_t* V, const uint16_t* U, int rank,
-                           int d_out, float* part, float* ylr, cudaStream_t st) {
+                           int d_out, float* part, float* ylr, cudaStream_t st, int xr_mma_order) {
   if (rows <= 0 || rank <= 0) return cudaSuccess;
   const int n_kc = lowrank_chunks(d_in);
   const dim3 g1((unsigned)n_kc, (unsigned)(rank / 8), (unsigned)((rows + 7) / 8));
-  lowrank_project_kernel<<<g1, 256, 0, st>>>(xr, rows, d_in, V, rank, part);
+  lowrank_project_kernel<<<g1, 256, 0, st>>>(xr, rows, d_in, V, rank, part, xr_mma_order);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const dim3 g2((unsigned)((d_out + 255) / 256), (unsigned)((rows + 15) / 16));

@@ -28,10 +28,12 @@ __device__ __forceinline__ float load_elem(const uint16_t* p) { return __half2fl
 __device__ __forceinline__ float load_elem(const float* p) { return *p; }
 
 // out[row][col] row-major FP16 (may alias an FP16 x: every element is read before
-// any is written). T: FP16 (uint16_t) or FP32 input.
+// any is written). T: FP16 (uint16_t) or FP32 input. With mma_order the columns of
+// each 16-column group are stored in the tensor-core GEMM's operand order (see
+// mma_order_col).
 template <int B, typename T>
 __global__ void __launch_bounds__(kRotThreads) fwht_kernel(const T* x, int n, const uint32_t* __restrict__ signs,
-                                                            uint16_t* out, float scale) {
+                                                            uint16_t* out, float scale, int mma_order) {
   constexpr int V = (B + kRotThreads - 1) / kRotThreads;  // values per thread
   constexpr int ACTIVE = B < kRotThreads ? B : kRotThreads;
   __shared__ float sm[V * kRotThreads];
@@ -91,17 +93,21 @@ __global__ void __launch_bounds__(kRotThreads) fwht_kernel(const T* x, int n, co
     }
   }
 
+  const size_t row_base = (size_t)row * n;
 #pragma unroll
   for (int s = 0; s < V; ++s) {
     const int j = s * kRotThreads + tid;
-    if (tid < ACTIVE) out[base + j] = __half_as_ushort(__float2half_rn(v[s] * scale));
+    const int col = blk * B + j;
+    if (tid < ACTIVE)
+      out[row_base + (mma_order ? mma_order_col(col) : col)] = __half_as_ushort(__float2half_rn(v[s] * scale));
   }
 }
 
 template <int B, typename T>
-cudaError_t launch_b(const T* x, int rows, int n, const uint32_t* signs, uint16_t* out, cudaStream_t st) {
+cudaError_t launch_b(const T* x, int rows, int n, const uint32_t* signs, uint16_t* out, int mma_order,
+                     cudaStream_t st) {
   const long long grid = (long long)rows * (n / B);
-  fwht_kernel<B, T><<<(unsigned)grid, kRotThreads, 0, st>>>(x, n, signs, out, 1.0f / sqrtf((float)B));
+  fwht_kernel<B, T><<<(unsigned)grid, kRotThreads, 0, st>>>(x, n, signs, out, 1.0f / sqrtf((float)B), mma_order);
   return cudaGetLastError();
 }
 
@@ -173,32 +179,33 @@ __global__ void __launch_bounds__(256) residual_add_ss_kernel(const uint16_t* __
 
 namespace {
 template <typename T>
-cudaError_t launch_any(const T* x, int rows, int n, int block, const uint32_t* signs, uint16_t* out,
+cudaError_t launch_any(const T* x, int rows, int n, int block, const uint32_t* signs, uint16_t* out, int mma_order,
                        cudaStream_t st) {
+  if (mma_order && n % 16) return cudaErrorInvalidValue;
   switch (block) {
-    case 2: return launch_b<2, T>(x, rows, n, signs, out, st);
-    case 4: return launch_b<4, T>(x, rows, n, signs, out, st);
-    case 8: return launch_b<8, T>(x, rows, n, signs, out, st);
-    case 16: return launch_b<16, T>(x, rows, n, signs, out, st);
-    case 32: return launch_b<32, T>(x, rows, n, signs, out, st);
-    case 64: return launch_b<64, T>(x, rows, n, signs, out, st);
-    case 128: return launch_b<128, T>(x, rows, n, signs, out, st);
-    case 256: return launch_b<256, T>(x, rows, n, signs, out, st);
-    case 512: return launch_b<512, T>(x, rows, n, signs, out, st);
-    case 1024: return launch_b<1024, T>(x, rows, n, signs, out, st);
+    case 2: return launch_b<2, T>(x, rows, n, signs, out, mma_order, st);
+    case 4: return launch_b<4, T>(x, rows, n, signs, out, mma_order, st);
+    case 8: return launch_b<8, T>(x, rows, n, signs, out, mma_order, st);
+    case 16: return launch_b<16, T>(x, rows, n, signs, out, mma_order, st);
+    case 32: return launch_b<32, T>(x, rows, n, signs, out, mma_order, st);
+    case 64: return launch_b<64, T>(x, rows, n, signs, out, mma_order, st);
+    case 128: return launch_b<128, T>(x, rows, n, signs, out, mma_order, st);
+    case 256: return launch_b<256, T>(x, rows, n, signs, out, mma_order, st);
+    case 512: return launch_b<512, T>(x, rows, n, signs, out, mma_order, st);
+    case 1024: return launch_b<1024, T>(x, rows, n, signs, out, mma_order, st);
     default: return cudaErrorInvalidValue;
   }
 }
 }  // namespace
 
 cudaError_t launch_fwht(const uint16_t* x, int rows, int n, int block, const uint32_t* signs,
-                        uint16_t* out, cudaStream_t st) {
-  return launch_any<uint16_t>(x, rows, n, block, signs, out, st);
+                        uint16_t* out, cudaStream_t st, int mma_order) {
+  return launch_any<uint16_t>(x, rows, n, block, signs, out, mma_order, st);
 }
 
 cudaError_t launch_fwht_f32(const float* x, int rows, int n, int block, const uint32_t* signs, uint16_t* out,
-                            cudaStream_t st) {
-  return launch_any<float>(x, rows, n, block, signs, out, st);
+                            cudaStream_t st, int mma_order) {
+  return launch_any<float>(x, rows, n, block, signs, out, mma_order, st);
 }
 
 cudaError_t launch_residual_rmsnorm(uint16_t* resid, const uint16_t* delta, int rows, int n, float eps,

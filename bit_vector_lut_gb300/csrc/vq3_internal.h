@@ -150,11 +150,29 @@ bool persist_cells_fit(int d_in, int d_out, int n_mats, int grid);
 int persist_chunk(int d, int block);  // rotation chunk: whole blocks, up to 1024 columns
 cudaError_t launch_persistent(const PersistArgs& a, int nt, cudaStream_t st);
 
+// Column order of the tensor-core GEMM's activation operand. The GEMM keeps its decoded
+// weight tiles in tensor memory, written by tcgen05.st 16x256b: there the K pairs of each
+// 16-input group sit in the column order (0, 4, 1, 5, 2, 6, 3, 7), so the activations (the
+// other operand) carry the same order: input pair c of a 16-column group is stored at pair
+// position 2c (c < 4) or 2(c - 4) + 1. The contraction over K is unchanged.
+__host__ __device__ inline int mma_order_col(int col) {
+  const int c = (col & 15) >> 1;
+  const int pos = c < 4 ? 2 * c : 2 * (c - 4) + 1;
+  return (col & ~15) | (pos << 1) | (col & 1);
+}
+// Input column held at stored column `col` of a row in that order (the inverse map).
+__host__ __device__ inline int mma_order_input(int col) {
+  const int pos = (col & 15) >> 1;
+  const int c = (pos >> 1) + 4 * (pos & 1);
+  return (col & ~15) | (c << 1) | (col & 1);
+}
+
+// mma_order: store the rotated rows in the GEMM's operand order (mma_order_col); n % 16 == 0.
 cudaError_t launch_fwht(const uint16_t* x, int rows, int n, int block, const uint32_t* signs,
-                        uint16_t* out, cudaStream_t st);
+                        uint16_t* out, cudaStream_t st, int mma_order = 0);
 // Same rotation of FP32 rows, written as FP16.
 cudaError_t launch_fwht_f32(const float* x, int rows, int n, int block, const uint32_t* signs, uint16_t* out,
-                            cudaStream_t st);
+                            cudaStream_t st, int mma_order = 0);
 
 // One VQ3 matrix (or the gate/up pair) against rotated FP16 activations on
 // tcgen05 tensor cores: out16 = fp16(s0 * W0 x') for one matrix, or, with
@@ -178,11 +196,21 @@ struct PrefillArgs {
   unsigned* flags;         // one word per CTA, zero between calls: its slot is filled
   long long work;          // (tile, K step) pairs; set by launch_prefill_gemm
 };
-int prefill_tile_rows(int rows);  // rows per output tile: 64, 128 or 256
+// Two tensor-core GEMM kernels serve the many-row path. Up to kPrefillNarrowRows rows:
+// launch_prefill_gemm, output tiles of 64 or 128 rows, 4 or 2 tiles per K step sharing one
+// activation tile, the decoded weights in tensor memory, activations in the operand order of
+// mma_order_col. Above: launch_prefill_wide_gemm, tiles of 256 rows, the decoded weights in
+// shared memory, activations in their natural order.
+constexpr int kPrefillNarrowRows = 128;
+inline bool prefill_wide(int rows) { return rows > kPrefillNarrowRows; }
+long long prefill_wide_work(int rows, int d_in, int d_out, int swiglu);
+int prefill_wide_grid(int rows, int d_in, int d_out, int swiglu);
+cudaError_t launch_prefill_wide_gemm(const PrefillArgs& a, cudaStream_t st);
+int prefill_tile_rows(int rows);  // rows per output tile of launch_prefill_gemm: 64 or 128
 long long prefill_work(int rows, int d_in, int d_out, int swiglu);
 int prefill_max_grid();           // most CTAs of one launch (one per SM)
 int prefill_grid(int rows, int d_in, int d_out, int swiglu);
-size_t prefill_part_bytes(int rows);  // size of PrefillArgs::part
+size_t prefill_part_bytes(int rows);  // size of PrefillArgs::part (serves both kernels)
 cudaError_t launch_prefill_gemm(const PrefillArgs& a, cudaStream_t st);
 // r_next = fp16(r + d), ss[row][g] = sum of r_next^2 over columns 16g .. 16g+15 (or none: ss null).
 cudaError_t launch_residual_add_ss(const uint16_t* r, const uint16_t* d, uint16_t* r_next, float* ss, int rows,
@@ -201,8 +229,9 @@ cudaError_t launch_delta_rule(const uint16_t* q, const uint16_t* k, const uint16
 // correction (V [rank][d_in], U [d_out][rank] FP16); the projection's sums over
 // lowrank_chunks(d_in) input chunks go through part [chunks][rows][rank].
 int lowrank_chunks(int d_in);
+// xr_mma_order: the rows of xr are stored in the GEMM's operand order (mma_order_col).
 cudaError_t launch_lowrank(const uint16_t* xr, int rows, int d_in, const uint16_t* V, const uint16_t* U, int rank,
-                           int d_out, float* part, float* ylr, cudaStream_t st);
+                           int d_out, float* part, float* ylr, cudaStream_t st, int xr_mma_order = 0);
 
 // vq3_mlp_forward with passes of at most `pass_cap` rows (8, 16 or 32), and its
 // workspace size; vq3_mlp_forward itself uses 32.
