@@ -67,19 +67,39 @@ def whole_job_rate(units_per_rank: float, world: int, seconds: float) -> float:
     return world * units_per_rank / seconds
 
 
+def blas_threads():
+    """Threads of the BLAS that numpy calls: threadpoolctl when it is installed, else the
+    OpenBLAS thread-count entry point of the library loaded into this process, else None."""
+    np.ones((4, 4)) @ np.ones((4, 4))  # make sure the BLAS is loaded
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"), default=0)
+        if n:
+            return n
+    except Exception:
+        pass
+    try:
+        import ctypes
+        paths = sorted({ln.split()[-1] for ln in open("/proc/self/maps") if "openblas" in ln.lower() and ".so" in ln})
+        for path in paths:
+            lib = ctypes.CDLL(path)
+            for name in ("openblas_get_num_threads", "openblas_get_num_threads64_", "scipy_openblas_get_num_threads64_",
+                         "scipy_openblas_get_num_threads"):
+                f = getattr(lib, name, None)
+                if f is not None:
+                    f.restype = ctypes.c_int
+                    return int(f())
+    except Exception:
+        pass
+    return None
+
+
 def cpu_cores() -> dict:
     try:
         aff = len(os.sched_getaffinity(0))
     except AttributeError:
         aff = os.cpu_count()
-    blas = None
-    try:
-        from threadpoolctl import threadpool_info
-        info = threadpool_info()
-        blas = max((i.get("num_threads", 0) for i in info if i.get("user_api") == "blas"), default=None)
-    except Exception:
-        pass
-    return {"cpu_count": os.cpu_count(), "affinity": aff, "blas_threads": blas}
+    return {"cpu_count": os.cpu_count(), "affinity": aff, "blas_threads": blas_threads()}
 
 
 # ------------------------------------------------------------------ oracle (CPU baseline / reference arm)
@@ -92,14 +112,16 @@ class OracleSample:
     the down rows are computed once at set-up, untimed. A step counts as
     T * (its share of the block's three weight products' multiply-adds) rows."""
 
-    def __init__(self, rows: int, f: float):
+    def __init__(self, rows: int, f: float, outliers: bool = False):
         from oracle import vq3_oracle as O
         self.O = O
-        self.wl = S.mlp_27b(seed=1, rows=rows)
+        self.wl = S.mlp_prefill_outliers(seed=2, rows=rows) if outliers else S.mlp_27b(seed=1, rows=rows)
         blk = self.wl.layers[0]
         self.xr = O.rotate(self.wl.x.astype(np.float64), blk.gate.block, blk.gate.signs)
-        g = O.linear_f64(self.wl.x, blk.gate)
-        u = O.linear_f64(self.wl.x, blk.up)
+        # set-up only (untimed): h of every intermediate channel, output ranges on host threads
+        workers = os.cpu_count() or 1
+        g = O.linear_f64(self.wl.x, blk.gate, workers=workers)
+        u = O.linear_f64(self.wl.x, blk.up, workers=workers)
         self.hr = O.rotate(O.silu(g) * u, blk.down.block, blk.down.signs)
         self.set_fraction(f)
 
@@ -117,6 +139,48 @@ class OracleSample:
         Wd = O.dense_weight(blk.down.stream, blk.down.codebook, blk.down.scales, INTER, HIDDEN, rows=(0, self.n_dn))
         _ = self.hr @ Wd.T
         return self.wl.x.shape[0] * self.share
+
+
+def oracle_config_rates(budget_s: float = 3.0) -> dict:
+    """Rows/s of the oracle as it stands on the three single-block workloads: the 256 -> 256
+    linear (seed 0, 8 rows: whole calls), the block at 8 rows (seed 1) and the 64-row chunk with
+    outlier channels (seed 2) (a sampled fraction of each matrix's channels per step, sized to
+    about budget_s / 2 per step, two steps, scaled to whole rows). Run once with the host's
+    cores and once in a child process pinned to one BLAS and OpenMP thread."""
+    from oracle import vq3_oracle as O
+    res = {}
+    wl = S.linear_256(seed=0, rows=8)
+    n, t0 = 0, time.perf_counter()
+    while n < 3 or time.perf_counter() - t0 < budget_s:
+        O.linear_f64(wl.x, wl.layers[0])
+        n += 1
+    res["linear_256x256_T8"] = round(8 * n / (time.perf_counter() - t0), 2)
+    for name, rows, outl in (("mlp_5120x17408_T8", 8, False), ("mlp_5120x17408_T64_outliers", 64, True)):
+        smp = OracleSample(rows, 1.0 / 256, outliers=outl)
+        t0 = time.perf_counter()
+        smp.step()
+        t_small = time.perf_counter() - t0
+        smp.set_fraction(min(0.25, max(1.0 / 2048, (budget_s / 2) / max(t_small, 1e-6) / 256)))
+        units, t0 = 0.0, time.perf_counter()
+        for _ in range(2):
+            units += smp.step()
+        res[name] = round(units / (time.perf_counter() - t0), 4)
+    return res
+
+
+def oracle_config_baseline() -> dict:
+    """oracle_config_rates on all host cores, and in a child process with one BLAS/OpenMP thread."""
+    all_cores = oracle_config_rates()
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    one = None
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-config-rates"], env=env,
+                           capture_output=True, text=True, timeout=600)
+        one = json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:  # reported, not fatal
+        one = {"error": str(e)[:200]}
+    return {"all_cores": all_cores, "all_cores_blas_threads": blas_threads(), "one_thread": one,
+            "unit": "rows/s"}
 
 
 def time_oracle(rows: int, f: float, steps: int, warmup: int):
@@ -311,7 +375,9 @@ def _run_ours_on(args, torch, vq3, dev, stream, rows, sets, x_host, x, out, ws, 
 
     extra, stack, fmts, mixers = {}, {}, {}, {}
     if not args.quick and rank == 0:
-        extra = prefill_sweep(vq3, dev, stream, pk)
+        extra = prefill_sweep(vq3, dev, stream, pk, l2)
+        extra["config_outliers_T64"] = prefill_outliers_line(vq3, dev, stream, pk, l2)
+        extra["config_linear_256_T8"] = linear256_line(vq3, dev, stream)
         stack = stack64(vq3, dev, stream, pk)
         fmts = format_lines(vq3, dev, stream, pk, l2)
         mixers = token_mixer_lines(vq3, dev, stream, pk, l2)
@@ -347,6 +413,8 @@ def _run_ours_on(args, torch, vq3, dev, stream, rows, sets, x_host, x, out, ws, 
                                               f"and up channels and {smp.n_dn} down channels "
                                               f"({smp.share:.4f} of the block's multiply-adds; rotations untimed), "
                                               f"{dt:.1f} s, scaled to whole rows"}
+            if not args.quick:
+                line["cpu_baseline"]["per_config"] = oracle_config_baseline()
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -492,32 +560,102 @@ def delta_rule_lines(vq3, dev, stream) -> dict:
     return res
 
 
-def prefill_sweep(vq3, dev, stream, pk) -> dict:
-    """TFLOP/s of one block at prefill row counts (weights L2-resident across repeats at these sizes is
-    irrelevant: they are tensor-bound)."""
+def graph_block_us(vq3, torch, dev, stream, x, sets, rows, min_blocks) -> tuple[float, int]:
+    """Microseconds per block: a CUDA graph of one cycle through the weight sets (one block per
+    set, each set's weights streamed from HBM) replayed until at least `min_blocks` blocks ran,
+    timed with CUDA events on the launching stream; and the workspace status."""
+    out = torch.empty((rows, HIDDEN), dtype=torch.float16, device=dev)
+    ws = vq3.workspace(vq3.mlp_workspace_bytes(rows, sets[0]), dev, stream)
+    for lay in sets:  # warm-up: module load, tensor maps, first touches
+        vq3.mlp_forward(x, lay, out=out, ws=ws, stream=stream)
+    gph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gph, stream=stream):
+        for lay in sets:
+            vq3.mlp_forward(x, lay, out=out, ws=ws, stream=stream)
+    gph.replay()
+    torch.cuda.synchronize(dev)
+    reps = max(1, math.ceil(min_blocks / len(sets)))
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        gph.replay()
+    b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b) * 1e3 / (reps * len(sets)), vq3.workspace_status(ws, stream)
+
+
+def weight_sets(vq3, dev, seed: int, l2: int) -> list:
+    """Independent weight sets of one block (seeds seed + 1000 k) that together exceed 4x L2."""
+    n = max(2, math.ceil(4 * l2 / BLOCK_BYTES))
+    return [vq3.MLP.from_block(S.mlp_block(S.rng(seed + 1000 * k, 1), HIDDEN, INTER, 1024), dev) for k in range(n)]
+
+
+def prefill_sweep(vq3, dev, stream, pk, l2) -> dict:
+    """The row sweep of one block (seed 4): T in {1, 8, 64, 512, 2048, 4096}. Each T runs through
+    a CUDA graph cycling independent weight sets (> 4x L2, so weights stream from HBM at every T),
+    at least 24 blocks per T (12 at 2048 and 4096 rows). TFLOP/s against the measured bf16 peak,
+    weight GB/s against the measured HBM copy peak."""
     import torch
     res = {}
-    wl = S.mlp_27b(seed=4, rows=1)
-    layer = vq3.MLP.from_block(wl.layers[0], dev)
-    for rows in (64, 512, 2048, 4096):
+    sets = weight_sets(vq3, dev, 4, l2)
+    for rows in S.SWEEP_ROWS:
         x = torch.from_numpy(S.activations(S.rng(4, 0), rows, HIDDEN)).to(dev)
-        out = torch.empty_like(x)
-        ws = vq3.workspace(vq3.mlp_workspace_bytes(rows, layer), dev, stream)
-        for _ in range(2):
-            vq3.mlp_forward(x, layer, out=out, ws=ws, stream=stream)
-        reps = 3 if rows >= 2048 else 10
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(reps):
-            vq3.mlp_forward(x, layer, out=out, ws=ws, stream=stream)
-        b.record(stream)
-        b.synchronize()
-        ms = a.elapsed_time(b) / reps
-        tf = FLOP_PER_ROW * rows / (ms / 1e3) / 1e12
-        res[f"T{rows}"] = {"ms": round(ms, 4), "tflops": round(tf, 2), "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4),
-                           "rows_per_s": round(rows / (ms / 1e3), 1)}
+        us, st = graph_block_us(vq3, torch, dev, stream, x, sets, rows, 12 if rows >= 2048 else 24)
+        tf = FLOP_PER_ROW * rows / (us / 1e6) / 1e12
+        gbs = BLOCK_BYTES / (us / 1e6) / 1e9
+        res[f"T{rows}"] = {"us": round(us, 2), "tflops": round(tf, 2), "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4),
+                           "weight_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4),
+                           "rows_per_s": round(rows / (us / 1e6), 1),
+                           "launches_per_block": vq3.mlp_kernel_launches(rows, sets[0]), "status": st}
+    res["weight_sets"] = len(sets)
     return res
+
+
+def prefill_outliers_line(vq3, dev, stream, pk, l2) -> dict:
+    """The 64-row prefill chunk with outlier channels: seed 2, X ~ N(0,1) FP16 with 51 of the 5120
+    channels (1%) scaled x50, weights cycling through independent sets (> 4x L2) in a CUDA graph."""
+    import torch
+    sets = weight_sets(vq3, dev, 2, l2)
+    wl = S.mlp_prefill_outliers(seed=2, rows=64)
+    x = torch.from_numpy(wl.x).to(dev)
+    us, st = graph_block_us(vq3, torch, dev, stream, x, sets, 64, 48)
+    tf = FLOP_PER_ROW * 64 / (us / 1e6) / 1e12
+    gbs = BLOCK_BYTES / (us / 1e6) / 1e9
+    return {"workload": "mlp_5120x17408_T64_outliers", "us": round(us, 2), "rows_per_s": round(64 / (us / 1e6), 1),
+            "tflops": round(tf, 2), "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4),
+            "weight_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4),
+            "roof_us": {"tensor": round(FLOP_PER_ROW * 64 / (pk["bf16_tflops"] * 1e12) * 1e6, 2),
+                        "hbm": round(BLOCK_BYTES / (pk["hbm_gbs"] * 1e9) * 1e6, 2)},
+            "weight_sets": len(sets), "status": st}
+
+
+def linear256_line(vq3, dev, stream) -> dict:
+    """The single 256 -> 256 VQ3 linear (seed 0, 8 rows, one 256-point rotation block): a
+    launch-latency-bound case, so microseconds per call (mean of 200 calls in a CUDA graph)."""
+    import torch
+    wl = S.linear_256(seed=0, rows=8)
+    lin = vq3.Linear.from_matrix(wl.layers[0], dev)
+    x = torch.from_numpy(wl.x).to(dev)
+    out = torch.empty((8, 256), dtype=torch.float16, device=dev)
+    ws = vq3.workspace(vq3.linear_workspace_bytes(8, lin), dev, stream)
+    vq3.linear_forward(x, lin, out=out, ws=ws, stream=stream)
+    gph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gph, stream=stream):
+        for _ in range(200):
+            vq3.linear_forward(x, lin, out=out, ws=ws, stream=stream)
+    gph.replay()
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(3):
+        gph.replay()
+    b.record(stream)
+    b.synchronize()
+    us = a.elapsed_time(b) * 1e3 / 600
+    return {"workload": "linear_256x256_T8", "us": round(us, 3), "rows_per_s": round(8 / (us / 1e6), 1),
+            "launches_per_call": 1, "status": vq3.workspace_status(ws, stream)}
 
 
 def stack64(vq3, dev, stream, pk) -> dict:
@@ -603,7 +741,11 @@ def main():
     ap.add_argument("--oracle-steps", type=int, default=32)
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture, if current")
+    ap.add_argument("--oracle-config-rates", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_config_rates:  # the one-thread leg of the CPU baseline (a child process)
+        print(json.dumps(dict(oracle_config_rates(), blas_threads=blas_threads())), flush=True)
+        return
     if args.warmup < 3:
         args.warmup = 3
     line = run_reference(args) if args.impl == "reference" else run_ours(args)
