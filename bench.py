@@ -35,7 +35,7 @@ REF_BUDGET_S = 100.0
 # DRAM bytes (read + write) of one persistent_kernel launch at T=8, from one ncu capture of
 # the kernel (dram__bytes_read.sum + dram__bytes_write.sum); None when the kernel has changed
 # since that capture.
-TRAFFIC_PER_LAUNCH = 103_789_824
+TRAFFIC_PER_LAUNCH = 104_197_376
 
 
 def peaks() -> dict:
@@ -703,6 +703,25 @@ def stack64(vq3, dev, stream, pk) -> dict:
             "status": vq3.workspace_status(ws, stream)}
 
 
+def run_profile_case(args) -> None:
+    """A small case for profiler captures: one weight set (~100 MB on the device) and
+    --steps blocks at --rows rows through vq3_mlp_forward, untimed."""
+    import torch
+    from bit_vector_lut_gb300 import vq3
+    dev = torch.device("cuda:0")
+    wl = S.mlp_27b(seed=1, rows=args.rows)
+    layer = vq3.MLP.from_block(wl.layers[0], dev)
+    x = torch.from_numpy(wl.x).to(dev)
+    out = torch.empty_like(x)
+    ws = vq3.workspace(vq3.mlp_workspace_bytes(args.rows, layer), dev)
+    for _ in range(args.steps):
+        vq3.mlp_forward(x, layer, out=out, ws=ws)
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"profile_case": f"mlp_5120x17408_T{args.rows}", "blocks": args.steps,
+                      "launches_per_block": vq3.mlp_kernel_launches(args.rows, layer),
+                      "status": vq3.workspace_status(ws)}), flush=True)
+
+
 def run_reference(args) -> dict | None:
     rank, world, _ = dist_env()
     if rank != 0:
@@ -742,7 +761,12 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture, if current")
     ap.add_argument("--oracle-config-rates", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--profile-case", action="store_true",
+                    help="run --steps untimed blocks at --rows on one weight set (a small case for ncu) and exit")
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args)
+        return
     if args.oracle_config_rates:  # the one-thread leg of the CPU baseline (a child process)
         print(json.dumps(dict(oracle_config_rates(), blas_threads=blas_threads())), flush=True)
         return
