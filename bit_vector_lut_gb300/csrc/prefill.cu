@@ -172,12 +172,21 @@ __host__ __device__ constexpr uint32_t idesc_f16(int m, int n) {
   return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-// D (tensor memory) (+)= A (tensor memory) x B (shared memory descriptor), issued by one
-// elected lane of a converged warp (the operands are warp-uniform).
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+// The four K = 16 MMAs of one K step (64 inputs) of one tile, from one elected lane:
+// A columns a_tmem + 0, 8, 16, 24 (tensor memory), B descriptors bdesc + 0, 2, 4, 6 (32
+// bytes further along the swizzled rows each); the first accumulates only if acc != 0.
+__device__ __forceinline__ void mma_ts_kstep(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t acc) {
   asm volatile(
-      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
-      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "{\n .reg .pred p, q, e;\n .reg .b32 a1, a2, a3;\n .reg .b64 b1, b2, b3;\n"
+      " setp.ne.b32 p, %4, 0;\n setp.eq.b32 q, %4, %4;\n"
+      " add.u32 a1, %1, 8;\n add.u32 a2, %1, 16;\n add.u32 a3, %1, 24;\n"
+      " add.u64 b1, %2, 2;\n add.u64 b2, %2, 4;\n add.u64 b3, %2, 6;\n"
+      " elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, q;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, q;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, q;\n}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(acc)
       : "memory");
 }
@@ -593,18 +602,15 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
           // a wait gave up: no further MMAs (the consumers return at once); one decision per warp
           if (__shfl_sync(0xffffffffu, *abort, 0)) continue;
           tc_fence_after();
-          const uint32_t bt = b_tile(ls);
+          // one descriptor per step: K = 16 moves 8 columns along the A tile and 32 bytes (2
+          // descriptor units) along the swizzled B rows
+          const uint64_t bd = smem_desc_sw128(b_tile(ls));
+          const uint32_t at0 = tmem + (uint32_t)(kTileCols + as * G * kACols);
+          const uint32_t first = kk > g.k0 ? 1u : 0u;
 #pragma unroll
           for (int t = 0; t < G; ++t) {
             if (!tile_live(tg, t)) continue;
-            const uint32_t acc = tmem + (uint32_t)(t * N);
-            const uint32_t at = tmem + (uint32_t)(kTileCols + (as * G + t) * kACols);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              // K = 16: 8 columns of the A tile, 32 bytes along the swizzled B rows
-              mma_ts(acc, at + (uint32_t)(8 * j), smem_desc_sw128(bt + (uint32_t)(j * 32)), idesc,
-                     (kk > g.k0 || j > 0) ? 1u : 0u);
-            }
+            mma_ts_kstep(tmem + (uint32_t)(t * N), at0 + (uint32_t)(t * kACols), bd, idesc, first);
           }
           mma_commit_elect(load_empty(ls));  // both complete when this step's MMAs have read their operands
           mma_commit_elect(a_empty(as));
