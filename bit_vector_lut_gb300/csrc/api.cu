@@ -74,19 +74,20 @@ int passes(int rows, int pass_cap) {
 }
 
 // Pieces of one decode step of the persistent kernel.
-size_t persist_pieces_bytes(int rows, int d_in, int d_out, int n_mats) {
+size_t persist_pieces_bytes(int rows, int d_in, int d_out, int n_mats, int rank = 0) {
   const int nt = dec_tiles_per_pass(rows);
   const size_t piece = (size_t)512 * nt * sizeof(float);
   const size_t n_seg = (size_t)(d_out / kSuChannels) * n_mats;
   const int grid = persist_decode_grid(d_in, d_out, n_mats, persist_grid(nt));
-  return n_seg * persist_max_pieces(d_in, d_out, n_mats, grid) * piece;
+  const int lw = rank ? persist_lowrank_weight(d_in, d_out, grid) : 0;
+  return n_seg * persist_max_pieces(d_in, d_out, n_mats, grid, lw) * piece;
 }
 
 int seg_groups(int d_out, int n_mats) { return ((d_out / kSuChannels) * n_mats + kDecWarps - 1) / kDecWarps; }
 
 // Counter words of the persistent kernel (word 0: finished CTAs).
 struct CtlLayout {
-  int off_g, off_hd, off_o, n;
+  int off_g, off_hd, off_o, off_z, n;
 };
 
 CtlLayout ctl_mlp(int H, int I) {
@@ -101,7 +102,8 @@ CtlLayout ctl_mlp(int H, int I) {
 CtlLayout ctl_linear(int d_in, int d_out) {
   CtlLayout c{};
   c.off_o = c.off_g = c.off_hd = 1;
-  c.n = c.off_o + seg_groups(d_out, 1);
+  c.off_z = c.off_o + seg_groups(d_out, 1);  // partials of the low-rank projection written
+  c.n = c.off_z + 1;
   return c;
 }
 
@@ -117,10 +119,10 @@ size_t ctl_bytes(int n_words) {
 size_t mlp_ctl_bytes(int H, int I) { return ctl_bytes(ctl_mlp(H, I).n); }
 size_t linear_ctl_bytes(int d_in, int d_out) { return ctl_bytes(ctl_linear(d_in, d_out).n); }
 
-// [status word][counter words][pieces]([x' FP16 [rows][d_in]][U V x' FP32 [rows][d_out]]
-// [projection sums FP32 [chunks][rows][rank]] with low-rank factors)
+// [status word][counter words][pieces]([partials of z = V x', one [8 * NT][64] FP32 per
+// CTA of the first segment group] with low-rank factors)
 struct LinearWs {
-  size_t status, counters, pieces, xr, ylr, zpart, total;
+  size_t status, counters, pieces, lrz, total;
 };
 
 LinearWs linear_ws(int rows, int d_in, int d_out, int rank) {
@@ -129,14 +131,13 @@ LinearWs linear_ws(int rows, int d_in, int d_out, int rank) {
   w.counters = kCtlOffset;
   size_t off = kCtlOffset + linear_ctl_bytes(d_in, d_out);
   w.pieces = off;
-  off = round_up(off + persist_pieces_bytes(rows, d_in, d_out, 1), 256);
-  w.xr = w.ylr = w.zpart = off;
+  off = round_up(off + persist_pieces_bytes(rows, d_in, d_out, 1, rank), 256);
+  w.lrz = off;
   if (rank) {
-    off = round_up(off + (size_t)rows * d_in * 2, 256);
-    w.ylr = off;
-    off = round_up(off + (size_t)rows * d_out * sizeof(float), 256);
-    w.zpart = off;
-    off = round_up(off + (size_t)lowrank_chunks(d_in) * rows * rank * sizeof(float), 256);
+    const int nt = dec_tiles_per_pass(rows);
+    const int grid = persist_decode_grid(d_in, d_out, 1, persist_grid(nt));
+    const int lw = persist_lowrank_weight(d_in, d_out, grid);
+    off = round_up(off + (size_t)persist_max_pieces(d_in, d_out, 1, grid, lw) * 512 * nt * sizeof(float), 256);
   }
   w.total = off;
   return w;
@@ -196,7 +197,7 @@ struct PersistBufs {
   float *hbuf, *pieces1, *pieces3;
   unsigned* ctl;
   int* status;
-  float* lr_y;  // U V x' of the low-rank correction (linear layer with factors)
+  float* lr_z;  // partials of z = V x' (linear layer with low-rank factors)
   // pre-norm residual step fused ahead of the MLP block (see PersistArgs::norm)
   int norm;
   const uint16_t* res_delta;
@@ -250,7 +251,13 @@ cudaError_t run_persistent(const uint16_t* x, int rows, int nt, const vq3_mlp_la
   } else {
     a.mlp = 0;
     a.format = L->format;
-    a.lr_y = b.lr_y;
+    if (L->lr_rank) {
+      if (nt > 2) return cudaErrorInvalidValue;  // the projection's running sums cover up to 16 rows
+      a.lr_v = L->lr_v;
+      a.lr_u = L->lr_u;
+      a.lr_rank = L->lr_rank;
+      a.lr_z = b.lr_z;
+    }
     a.d_model = L->d_in;
     a.d_model_out = L->d_out;
     a.block_in = L->block;
@@ -258,7 +265,8 @@ cudaError_t run_persistent(const uint16_t* x, int rows, int nt, const vq3_mlp_la
     a.x_chunk = persist_chunk(L->d_in, a.block_in);
     a.gate = a.up = a.down = dec_mat(*L);
     a.grid1 = persist_decode_grid(L->d_in, L->d_out, 1, a.grid);
-    a.max_pieces1 = persist_max_pieces(L->d_in, L->d_out, 1, a.grid1);
+    a.lr_lw = L->lr_rank ? persist_lowrank_weight(L->d_in, L->d_out, a.grid1) : 0;
+    a.max_pieces1 = persist_max_pieces(L->d_in, L->d_out, 1, a.grid1, a.lr_lw);
     c = ctl_linear(L->d_in, L->d_out);
   }
   if (layer ? !(persist_cells_fit(a.d_model, a.d_inter, 2, a.grid1) && persist_cells_fit(a.d_inter, a.d_model, 1, a.grid3))
@@ -270,6 +278,7 @@ cudaError_t run_persistent(const uint16_t* x, int rows, int nt, const vq3_mlp_la
   a.off_g = c.off_g;
   a.off_hd = c.off_hd;
   a.off_o = c.off_o;
+  a.off_z = c.off_z;
   for (int row0 = 0; row0 < rows; row0 += 8 * nt) {
     a.row0 = row0;
     a.rows = rows - row0 < 8 * nt ? rows - row0 : 8 * nt;
@@ -627,16 +636,7 @@ int vq3_linear_forward(const uint16_t* x, int rows, const vq3_linear* L, uint16_
   b.pieces1 = reinterpret_cast<float*>(ws + w.pieces);
   b.ctl = reinterpret_cast<unsigned*>(ws + w.counters);
   b.status = reinterpret_cast<int*>(ws + w.status);
-  if (L->lr_rank) {
-    // U V x' for all rows ahead of the decode kernel, whose output step adds it
-    uint16_t* xr = reinterpret_cast<uint16_t*>(ws + w.xr);
-    b.lr_y = reinterpret_cast<float*>(ws + w.ylr);
-    cudaError_t e = launch_fwht(x, rows, L->d_in, L->block, L->signs, xr, st);
-    if (e == cudaSuccess)
-      e = launch_lowrank(xr, rows, L->d_in, L->lr_v, L->lr_u, L->lr_rank, L->d_out,
-                         reinterpret_cast<float*>(ws + w.zpart), b.lr_y, st);
-    if (e != cudaSuccess) return cuda_fail(e, "linear: launch");
-  }
+  b.lr_z = reinterpret_cast<float*>(ws + w.lrz);  // the low-rank correction is formed inside the kernel
   cudaError_t e = run_persistent(x, rows, dec_tiles_per_pass(rows), nullptr, L, b, out, st);
   if (e != cudaSuccess) return cuda_fail(e, "linear: launch");
   return ok();
@@ -830,6 +830,13 @@ int vq3_mlp_kernel_launches(int rows, const vq3_mlp_layer* layer) {
   if (rows == 0) return 0;
   if (rows >= kPrefillRows) return 4;  // rotate x, gate/up GEMM, rotate h, down GEMM
   return passes(rows, 32);             // one persistent kernel per pass of 8, 16 or 32 rows
+}
+
+int vq3_linear_kernel_launches(int rows, const vq3_linear* L) {
+  if (check_linear(L, "linear") || rows < 0) return -1;
+  if (rows == 0) return 0;
+  if (rows >= kPrefillRows) return L->lr_rank ? 4 : 2;  // rotate x, (project, expand,) GEMM
+  return 1;  // the decode kernel alone, the low-rank correction formed inside it
 }
 
 size_t vq3_mlp_host_workspace_bytes(int rows, const vq3_mlp_layer* layer) {

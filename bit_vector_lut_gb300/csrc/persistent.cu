@@ -119,6 +119,24 @@ __device__ __forceinline__ uint4 lds128(uint32_t saddr) {
   return v;
 }
 
+__device__ __forceinline__ void lds64(uint32_t saddr, uint32_t& a, uint32_t& b) {
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(a), "=r"(b) : "r"(saddr) : "memory");
+}
+__device__ __forceinline__ float lds_f32(uint32_t saddr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(saddr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts_f32(uint32_t saddr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(saddr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t saddr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(saddr) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
 // 32-bit unsigned arithmetic throughout (the launcher checks cells * grid < 2^32):
@@ -130,6 +148,26 @@ __device__ __forceinline__ int range_begin(int cells, int grid, int b) {
 // CTA owning cell x (largest b with range_begin(b) <= x).
 __device__ __forceinline__ int cta_of(int x, int cells, int grid) {
   return (int)((((unsigned)x + 1u) * (unsigned)grid - 1u) / (unsigned)cells);
+}
+
+// The same partition with the cells of the first segment group weighted 1 + lw / 8 (lw > 0: a
+// linear layer with low-rank factors, whose first-group CTAs also form z): in eighths of a cell,
+// cell x ends at cost(x) = 8 x + lw min(x, n0), CTA b starts at the first cell whose cost reaches
+// b T / grid (T = cost(cells)), and cta_of inverts that. lw = 0 is the partition above.
+__device__ __forceinline__ unsigned wcost(int x, int n0, int lw) {
+  return 8u * (unsigned)x + (unsigned)lw * (unsigned)(x < n0 ? x : n0);
+}
+__device__ __forceinline__ int range_begin_w(int cells, int grid, int b, int n0, int lw) {
+  if (!lw) return range_begin(cells, grid, b);
+  const unsigned T = wcost(cells, n0, lw);
+  const unsigned target = (unsigned)b * T / (unsigned)grid;
+  const unsigned w0 = (unsigned)(8 + lw), c0 = w0 * (unsigned)n0;
+  if (target <= c0) return (int)((target + w0 - 1u) / w0);
+  return n0 + (int)((target - c0 + 7u) / 8u);
+}
+__device__ __forceinline__ int cta_of_w(int x, int cells, int grid, int n0, int lw) {
+  if (!lw) return cta_of(x, cells, grid);
+  return (int)(((wcost(x, n0, lw) + 1u) * (unsigned)grid - 1u) / wcost(cells, n0, lw));
 }
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -203,6 +241,14 @@ struct DecodeJob {
   const unsigned* ready;    // per chunk: complete when >= ready_target (null: ready at launch)
   unsigned ready_target;
   unsigned* group_done;     // per segment group: +1 per CTA whose pieces of the group are written
+  // low-rank projection z = V x' (linear job with factors, else lr_v null): formed by the CTAs
+  // of the first segment group from their stage slots, one partial per CTA in lr_z
+  const uint16_t* lr_v;
+  int lr_rank;
+  float* lr_z;
+  unsigned* lr_done;        // +1 per CTA whose partial of z is written
+  int lw;                   // extra weight of a first-group cell in the CTA ranges, eighths (0: none)
+  uint32_t zacc;            // shared address: per warp [NT][4][32 lanes] FP32 running sums
 
   __device__ int n_kg() const { return d_in / kSuInputs; }
   __device__ int n_seg() const { return (d_out / kSuChannels) * n_mats; }
@@ -211,7 +257,7 @@ struct DecodeJob {
   // CTAs that write pieces of segment group g (slots 0 .. count-1)
   __device__ int contributors(int g) const {
     const int x0 = g * n_kg();
-    return cta_of(x0 + n_kg() - 1, cells(), grid) - cta_of(x0, cells(), grid) + 1;
+    return cta_of_w(x0 + n_kg() - 1, cells(), grid, n_kg(), lw) - cta_of_w(x0, cells(), grid, n_kg(), lw) + 1;
   }
   __device__ const float* seg_pieces(int sg, int piece_floats) const {
     return pieces + (size_t)sg * max_pieces * piece_floats;
@@ -466,6 +512,116 @@ __device__ __forceinline__ void stage_round(const DecodeJob& a, const T* src, in
   }
 }
 
+// ------------------------------------------------------------------ low-rank projection
+//
+// z = V x' for a linear layer with factors (W = diag(s) C[idx] + U V on the rotated input:
+// model card "anemll/anemll-forge-qwen3.8-27B", table row "Token mixers", rank-64 factors).
+// The CTAs that decode the first segment group hold, between them, every column group's
+// rotated activations in their stage slots once each, so they form z from those slots: per
+// slot, warp w takes factor rows 16 (w >> 2) .. + 15 over k-step w & 3, one m16n8k16 per
+// 8-row tile, into running sums of its own in shared memory (after the round's cells are
+// decoded: the decode loop itself is the same as without factors). Where the CTA's part of
+// the first group ends, the sums of the four k-step warps of each row tile are added in
+// k-step order and written as the CTA's partial of z, and a counter of its own is raised.
+
+// The factor columns of a batch of up to kLrBatch first-group slots sit in the rotation scratch
+// (idle while cells are decoded): row q of V at q * kLrRow bytes, the batch's column groups one
+// after another. The row stride is 4 words past a multiple of 32, so a fragment load (rows g,
+// columns 2t) touches 32 distinct banks.
+constexpr int kLrBatch = 7;
+constexpr uint32_t kLrRow = kLrBatch * 128 + 16;
+
+// Copies V's columns of column groups kg0 .. kg0 + n - 1 (n <= kLrBatch) into the scratch as
+// 16-byte copies spread over the CTA's threads (consecutive threads take consecutive chunks of a
+// row), committed by every thread as one copy group.
+__device__ __forceinline__ void lr_copy(const DecodeJob& a, const SmemView& sv, int kg0, int n) {
+  const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(sv.scratch));
+  const int per_row = n * (kSuInputs / 8);  // 16-byte chunks of a row
+  for (int i = threadIdx.x; i < a.lr_rank * per_row; i += kThreads) {
+    const int q = i / per_row, k = i - q * per_row;
+    cp_async16(base + (uint32_t)q * kLrRow + (uint32_t)k * 16u,
+               a.lr_v + (size_t)q * a.d_in + (size_t)kg0 * kSuInputs + (size_t)k * 8);
+  }
+  cp_async_commit();
+}
+
+// Warp's share over the batch's slots: slot p of the round (column group kg0 + p) is column
+// block p - b0 of the copied factor rows. Within a k-step the stage holds the inputs in natural
+// order (b0: columns 2t, 2t+1; b1: 2t+8, 2t+9), as the copied rows do; rows past the rank are zero.
+template <int NT>
+__device__ __forceinline__ void lowrank_slots(const DecodeJob& a, const SmemView& sv, int b0, int n) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int s = warp & 3, t = lane & 3;
+  const int qlo = 16 * (warp >> 2) + (lane >> 2), qhi = qlo + 8;
+  const bool lo = qlo < a.lr_rank, hi = qhi < a.lr_rank;
+  const uint32_t vs = static_cast<uint32_t>(__cvta_generic_to_shared(sv.scratch)) + (uint32_t)(16 * s + 2 * t) * 2u;
+  const uint32_t vlo = vs + (uint32_t)qlo * kLrRow, vhi = vs + (uint32_t)qhi * kLrRow;
+  const uint32_t zw = a.zacc + (uint32_t)(warp * NT * 128 + lane) * 4u;
+  float z[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) z[nt][j] = lds_f32(zw + (uint32_t)((nt * 4 + j) * 128));
+#pragma unroll
+  for (int i = 0; i < kLrBatch; ++i) {
+    if (i >= n) break;
+    const uint32_t c = (uint32_t)i * 128u;
+    uint32_t av[4];
+    av[0] = lo ? lds32(vlo + c) : 0u;        // row g:   columns 2t, 2t+1
+    av[1] = hi ? lds32(vhi + c) : 0u;        // row g+8
+    av[2] = lo ? lds32(vlo + c + 16u) : 0u;  // row g:   columns 2t+8, 2t+9
+    av[3] = hi ? lds32(vhi + c + 16u) : 0u;  // row g+8
+    const int p = b0 + i;
+    const uint32_t xb = sv.stage + (uint32_t)(p * NT * 1024) +
+                        (uint32_t)((s >> 1) * 32 + (lane ^ (p & 7))) * 16u + 8u * (uint32_t)(s & 1);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      uint32_t x0, x1;
+      lds64(xb + (uint32_t)(nt * 1024), x0, x1);
+      mma16816(z[nt], av, x0, x1);
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) sts_f32(zw + (uint32_t)((nt * 4 + j) * 128), z[nt][j]);
+}
+
+// z's share of a round's first-group slots [0, n0) (column groups kg0 ..), one batch of factor
+// columns at a time. Called after the round's first cell: the first batch's copy group was
+// committed before the round's cells, so all but the one cell copy group committed since it
+// have to be complete; a later batch waits for every group (the cells' copies in flight too).
+template <int NT>
+__device__ __forceinline__ void lr_round(const DecodeJob& a, const SmemView& sv, int kg0, int n0) {
+  for (int b0 = 0; b0 < n0; b0 += kLrBatch) {
+    const int nb = min(kLrBatch, n0 - b0);
+    if (b0) {
+      __syncthreads();  // the previous batch's reads of the scratch are done
+      lr_copy(a, sv, kg0 + b0, nb);
+      cp_async_wait<0>();
+    } else {
+      cp_async_wait<1>();
+    }
+    __syncthreads();  // every thread's copies are visible to the CTA
+    lowrank_slots<NT>(a, sv, b0, nb);
+  }
+}
+
+// The CTA's partial of z, [8 * NT token rows][64 factor rows], into slot blockIdx.x (the
+// first group's contributors are CTAs 0, 1, ...).
+template <int NT>
+__device__ __forceinline__ void lowrank_piece(const DecodeJob& a) {
+  __syncthreads();  // every warp's running sums are in shared memory
+  for (int it = threadIdx.x; it < 512 * NT; it += kThreads) {
+    const int L = it & 31, j = (it >> 5) & 3, mnt = it >> 7, nt = mnt % NT, m = mnt / NT;
+    float z = 0.f;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) z += lds_f32(a.zacc + (uint32_t)((((m * 4 + s) * NT + nt) * 4 + j) * 32 + L) * 4u);
+    const int q = 16 * m + (L >> 2) + 8 * (j >> 1), row = 8 * nt + 2 * (L & 3) + (j & 1);
+    __stcg(a.lr_z + ((size_t)blockIdx.x * 8 * NT + row) * 64 + q, z);
+  }
+}
+
 // ------------------------------------------------------------------ decode
 
 // A fragment of k-step S, 16-channel tile M, from the lane's string.
@@ -622,8 +778,8 @@ __device__ __forceinline__ void cell_range(const DecodeJob& a, int& c0, int& c1)
 // The job's cell range of this CTA.
 __device__ __forceinline__ void set_range(DecodeJob& a) {
   const int cells = a.cells();
-  a.c0 = range_begin(cells, a.grid, blockIdx.x);
-  a.c1 = range_begin(cells, a.grid, blockIdx.x + 1);
+  a.c0 = range_begin_w(cells, a.grid, blockIdx.x, a.n_kg(), a.lw);
+  a.c1 = range_begin_w(cells, a.grid, blockIdx.x + 1, a.n_kg(), a.lw);
 }
 
 // Points the cursor at column group kg of group g.
@@ -674,7 +830,8 @@ __device__ __forceinline__ Cursor decode_begin(const DecodeJob& a, const SmemVie
 
 // Decodes the CTA's range of cells; `cur` has issued the copies of its first
 // 1 .. kSlots cells, the rest of the prologue follows the first stage.
-template <int F, int NT, typename T>
+// LR: a linear layer with low-rank factors (its CTAs of the first segment group also form z).
+template <int F, int NT, typename T, bool LR>
 __device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cursor& cur, const SmemView& sv,
                                            const TableLoad<F>* tables, int* status) {
   constexpr int PIECE = 512 * NT;
@@ -700,6 +857,12 @@ __device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cur
   int sg = 0;
   const int total = (int)(c1 - c0);
   int first = 1;  // the next cell starts the range's part of a group
+  if constexpr (LR && NT <= 2) {
+    if (c0 < n_kg) {  // this warp's running sums of z start at zero
+#pragma unroll
+      for (int k = 0; k < NT * 4; ++k) sts_f32(a.zacc + (uint32_t)((warp * NT * 4 + k) * 32 + lane) * 4u, 0.f);
+    }
+  }
   for (int r0 = 0; r0 < total; r0 += KS) {
     const int kg_s = kg;  // column group of the round's first cell
     const int len = total - r0 < KS ? total - r0 : KS;
@@ -716,7 +879,12 @@ __device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cur
     stage_round<NT, T>(a, src, kg_s, len, sv);
     if (tables && r0 == 0) tables->store(sv.tab);  // ordered before the decode by the barrier below
     for (; issued < kSlots; ++issued) issue_cell<F>(a, cur, ring_lane);  // rest of the prologue
+    // the round's cells of the first segment group (cell index = column group there)
+    const int n0 = (LR && NT <= 2 && c0 + r0 < n_kg) ? min(len, n_kg - (c0 + r0)) : 0;
     __syncthreads();
+    if constexpr (LR) {
+      if (n0) lr_copy(a, sv, c0 + r0, min(n0, kLrBatch));  // lands while the first cell is decoded
+    }
     for (int p = 0; p < len; ++p) {
       if (first) {  // the range's part of group g starts
         sg = g * kWarps + warp;
@@ -733,12 +901,25 @@ __device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cur
       if (live)
         compute_cell<F, NT>(ring + use_slot, sv.stage + (uint32_t)(p * NT * 1024), lane, p & 7, lane_base, acc);
       issue_cell<F>(a, cur, ring_lane);  // refill the slot just read, kSlots cells ahead
+      if constexpr (LR && NT <= 2) {
+        if (n0 && p == 0) {
+          // z's share of the round's first-group cells (the stage holds them all; the factor
+          // copies issued before the loop have landed while the first cell was decoded): early,
+          // so that z is complete well before the segment groups are; where the CTA's part of
+          // the first group ends in this round, its partial of z
+          lr_round<NT>(a, sv, c0 + r0, n0);
+          if ((c1 < n_kg ? c1 : n_kg) <= c0 + r0 + len) {
+            lowrank_piece<NT>(a);
+            signal(a.lr_done, nullptr);
+          }
+        }
+      }
       use_slot = use_slot == (kSlots - 1) * kSlot ? 0u : use_slot + kSlot;
       first = (++kg == n_kg);
       if (first || r0 + p + 1 == total) {
         // this warp's segment over the range's part of group g: one piece
         if (live) {
-          const int piece = blockIdx.x - cta_of(g * n_kg, a.cells(), a.grid);
+          const int piece = blockIdx.x - cta_of_w(g * n_kg, a.cells(), a.grid, n_kg, a.lw);
           float* pc = a.pieces + ((size_t)sg * a.max_pieces + piece) * PIECE;
 #pragma unroll
           for (int m = 0; m < 4; ++m)
@@ -839,6 +1020,37 @@ __device__ __forceinline__ void swiglu_tasks(const PersistArgs& a, const DecodeJ
   }
 }
 
+// U z for one output task with factors, on the tensor cores: the task's items form four
+// (16-channel tile m, 8-row tile nt) accumulator tiles; warp w takes tile w >> 2 over
+// factors 16 (w & 3) .. + 15, with U's rows (channel pairs 2 (8m + g), + 1, as the pieces
+// pair them) as A and z as B, split as z = hi + lo in FP16 (two MMAs, ~22 bits of z).
+// Each warp writes its partial tile to yp [4 tiles][4 k-steps][4][32] (FP32).
+template <int NT>
+__device__ __forceinline__ void lowrank_out_mma(int part, int rank, uint32_t ur, const float* zs, float* yp) {
+  constexpr int kZs = 68;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int tl = warp >> 2, s = warp & 3;
+  const int mnt = part * 4 + tl, m = mnt / NT, nt = mnt % NT;
+  const int q0 = 16 * s + 2 * t;  // factor of b0 / a0 (q0 + 8: b1 / a2)
+  const uint32_t r0 = ur + (uint32_t)(16 * m + 2 * g) * 144u + (uint32_t)q0 * 2u;  // channel 2 (8m + g)
+  uint32_t a[4];
+  a[0] = q0 < rank ? lds32(r0) : 0u;
+  a[1] = q0 < rank ? lds32(r0 + 144u) : 0u;  // channel 2 (8m + g) + 1
+  a[2] = q0 + 8 < rank ? lds32(r0 + 16u) : 0u;
+  a[3] = q0 + 8 < rank ? lds32(r0 + 144u + 16u) : 0u;
+  const float* zr = zs + (nt * 8 + g) * kZs + q0;  // token row nt * 8 + g is column g
+  const float2 z0 = *reinterpret_cast<const float2*>(zr);
+  const float2 z1 = *reinterpret_cast<const float2*>(zr + 8);
+  const __half2 h0 = __float22half2_rn(z0), h1 = __float22half2_rn(z1);
+  const float2 e0 = __half22float2(h0), e1 = __half22float2(h1);
+  const __half2 l0 = __floats2half2_rn(z0.x - e0.x, z0.y - e0.y), l1 = __floats2half2_rn(z1.x - e1.x, z1.y - e1.y);
+  float c[4] = {0.f, 0.f, 0.f, 0.f};
+  mma16816(c, a, *reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+  mma16816(c, a, *reinterpret_cast<const uint32_t*>(&l0), *reinterpret_cast<const uint32_t*>(&l1));
+#pragma unroll
+  for (int j = 0; j < 4; ++j) yp[((tl * 4 + s) * 4 + j) * 32 + lane] = c[j];
+}
+
 // One task per (64 output channels, 8-row tile): out = fp16(scale * sum of pieces).
 template <int NT>
 __device__ __forceinline__ void output_tasks(const PersistArgs& a, const DecodeJob& j, const SmemView& sv, int* status) {
@@ -849,13 +1061,12 @@ __device__ __forceinline__ void output_tasks(const PersistArgs& a, const DecodeJ
     const int sg = t / NT, part = t % NT;
     const int g = sg / kWarps;
     const int count = j.contributors(g);
-    // the scale and the low-rank term are inputs: their loads go out before the wait
+    // the scale is an input: its load goes out before the wait
     const int it = part * 512 + threadIdx.x;
     int r, c;
     item_pos<NT>(it, r, c);
     const int ch = sg * kSuChannels + c;
     const float sc = __half2float(__ushort_as_half(__ldg(j.scales0 + ch)));
-    const float lr = (a.lr_y && r < a.rows) ? __ldg(a.lr_y + (size_t)(a.row0 + r) * j.d_out + ch) : 0.f;
     const float rin = (a.res_next && r < a.rows) ? load1(a.x + (size_t)(a.row0 + r) * j.d_out + ch) : 0.f;
     if (threadIdx.x == 0) {
       poll_geq(j.group_done + g, (unsigned)count, status);
@@ -872,7 +1083,6 @@ __device__ __forceinline__ void output_tasks(const PersistArgs& a, const DecodeJ
     }
     if (r < a.rows) {
       float v = sc * y;
-      if (a.lr_y) v += lr;  // low-rank correction
       const __half o16 = __float2half_rn(v);
       a.out[(size_t)(a.row0 + r) * j.d_out + ch] = __half_as_ushort(o16);
       if (a.res_next) {
@@ -899,18 +1109,156 @@ __device__ __forceinline__ void output_tasks(const PersistArgs& a, const DecodeJ
   }
 }
 
+// The output tasks of a linear layer with low-rank factors: out = fp16(scale * sum of pieces
+// + U z), z summed from the first group's partials in CTA order, then U z on the tensor cores
+// with its k-step partials added in order, all before the single rounding. A CTA takes its
+// tasks t and t + grid together, so that their loads overlap; the tasks are dealt from the
+// last CTA down, so that the CTAs of the first group (which also formed z) take one.
+template <int NT>
+__device__ __forceinline__ void output_tasks_lr(const PersistArgs& a, const DecodeJob& j, const SmemView& sv, int* status) {
+  constexpr int PIECE = 512 * NT;
+  constexpr int P = 32;           // piece loads in flight
+  constexpr int kZs = 68;         // row stride of z in shared memory: 16-byte rows, banks apart
+  const int n_seg = j.d_out / kSuChannels;
+  const int n_tasks = n_seg * NT;
+  const int G = gridDim.x;
+  const int count0 = j.contributors(0);
+  // scratch (free in this step): z [8 * NT][kZs] at 16 KB; U's rows of the tasks taken together
+  // at 24 KB (task k's 64 channels from k * 64 rows on, 144-byte rows: the channels a warp reads
+  // fall on distinct banks); the U z partials of task k at 44 KB + k * 8 KB
+  float* zs = sv.scratch + 4096;
+  constexpr uint32_t kUs = 144;
+  const uint32_t us = static_cast<uint32_t>(__cvta_generic_to_shared(sv.scratch)) + 24u * 1024u;
+  float* yp = sv.scratch + 11 * 1024;
+  bool have_z = false;  // zs holds z (formed once per CTA, before its first tasks' pieces)
+  for (int t0 = G - 1 - (int)blockIdx.x; t0 < n_tasks; t0 += 2 * G) {
+    const int nk = t0 + G < n_tasks ? 2 : 1;  // tasks taken together (uniform over the CTA)
+    {
+      // U's rows, copied while the pieces are awaited (16 bytes per thread and copy; the
+      // previous tasks' reads of them ended before the barrier that followed them)
+      const int per_row = a.lr_rank / 8;  // 16-byte chunks of a row
+      for (int i = threadIdx.x; i < nk * kSuChannels * per_row; i += kThreads) {
+        const int row = i / per_row, k = i - row * per_row;  // row: task row >> 6, channel row & 63
+        const uint16_t* src = a.lr_u + ((size_t)((t0 + (row >> 6) * G) / NT) * kSuChannels + (row & 63)) * a.lr_rank;
+        cp_async16(us + (uint32_t)row * kUs + (uint32_t)k * 16u, src + k * 8);
+      }
+      cp_async_commit();
+    }
+    int sg[2], part[2], cnt[2], r[2], c[2], ch[2];
+    float sc[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int t = (k < nk) ? t0 + k * G : t0;  // a missing second task repeats the first (not stored)
+      sg[k] = t / NT;
+      part[k] = t % NT;
+      cnt[k] = j.contributors(sg[k] / kWarps);
+      item_pos<NT>(part[k] * 512 + threadIdx.x, r[k], c[k]);
+      ch[k] = sg[k] * kSuChannels + c[k];
+      // the scale is an input: its load goes out before the wait
+      sc[k] = __half2float(__ushort_as_half(__ldg(j.scales0 + ch[k])));
+    }
+    const bool do_z = !have_z;  // the CTA's first tasks also form z
+    if (threadIdx.x == 0) {
+      poll_geq(j.group_done + sg[0] / kWarps, (unsigned)cnt[0], status);
+      if (nk == 2) poll_geq(j.group_done + sg[1] / kWarps, (unsigned)cnt[1], status);
+      if (do_z) poll_geq(j.lr_done, (unsigned)count0, status);  // z's partials
+    }
+    __syncthreads();  // as for the SwiGLU tasks
+    // z[row][q] = the sum of the partials of CTAs 0, 1, ..., count0 - 1 in that order: the
+    // loads of its first ZP partials go out together with the pieces' loads below
+    constexpr int ZP = NT == 1 ? 16 : 8;
+    float zb[NT][ZP];
+    if (do_z) {
+#pragma unroll
+      for (int i = 0; i < NT; ++i)
+#pragma unroll
+        for (int k = 0; k < ZP; ++k)
+          zb[i][k] = k < count0 ? __ldcg(j.lr_z + threadIdx.x + i * kThreads + (size_t)k * PIECE) : 0.f;
+    }
+    // both tasks' sums of pieces, each in piece (= CTA) order: the first task's pieces then the
+    // second's, loaded P at a time
+    float y[2] = {0.f, 0.f};
+    {
+      const float* b0 = j.seg_pieces(sg[0], PIECE) + part[0] * 512 + threadIdx.x;
+      const float* b1 = j.seg_pieces(sg[1], PIECE) + part[1] * 512 + threadIdx.x - (size_t)cnt[0] * PIECE;
+      const int tot = cnt[0] + (nk == 2 ? cnt[1] : 0);
+      for (int q0 = 0; q0 < tot; q0 += P) {
+        float v[P];
+#pragma unroll
+        for (int q = 0; q < P; ++q) {
+          const int i = q0 + q;
+          v[q] = i < cnt[0] ? __ldcg(b0 + (size_t)i * PIECE) : (i < tot ? __ldcg(b1 + (size_t)i * PIECE) : 0.f);
+        }
+#pragma unroll
+        for (int q = 0; q < P; ++q) {
+          if (q0 + q < cnt[0])
+            y[0] += v[q];
+          else
+            y[1] += v[q];
+        }
+      }
+    }
+    if (do_z) {
+#pragma unroll
+      for (int i = 0; i < NT; ++i) {
+        const int e = threadIdx.x + i * kThreads;  // [row][q] of the pass, 64 factors per row
+        float z = 0.f;
+#pragma unroll
+        for (int k = 0; k < ZP; ++k) z += zb[i][k];
+        for (int k0 = ZP; k0 < count0; k0 += ZP) {  // more than ZP contributors
+          float v[ZP];
+#pragma unroll
+          for (int k = 0; k < ZP; ++k) v[k] = k0 + k < count0 ? __ldcg(j.lr_z + e + (size_t)(k0 + k) * PIECE) : 0.f;
+#pragma unroll
+          for (int k = 0; k < ZP; ++k) z += v[k];
+        }
+        zs[(e >> 6) * kZs + (e & 63)] = z;
+      }
+      have_z = true;
+    }
+    {
+      cp_async_wait<0>();
+      __syncthreads();  // z and every thread's copies of U's rows are visible
+      lowrank_out_mma<NT>(part[0], a.lr_rank, us, zs, yp);
+      if (nk == 2) lowrank_out_mma<NT>(part[1], a.lr_rank, us + 64u * kUs, zs, yp + 2048);
+      __syncthreads();  // the U z partials are in shared memory
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      if (k >= nk) break;
+      if (r[k] < a.rows) {
+        float v = sc[k] * y[k];
+        {
+          // low-rank correction: the item's four k-step partials in order (its tile is
+          // warp >> 2 of the task, its accumulator register warp & 3)
+          const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+          const float* q = yp + k * 2048 + ((warp >> 2) * 16 + (warp & 3)) * 32 + lane;
+          v += ((q[0] + q[128]) + q[256]) + q[384];
+        }
+        const __half o16 = __float2half_rn(v);
+        a.out[(size_t)(a.row0 + r[k]) * j.d_out + ch[k]] = __half_as_ushort(o16);
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ the kernel
 
-template <int NT, int F>
+template <int NT, int F, bool LR = false>
 struct Smem {
   static constexpr uint32_t kRing = kWarps * Ring<F>::kWarpBytes;
   static constexpr uint32_t kStage = StageCfg<NT>::kBytes;
   static constexpr uint32_t kScratch = kWarps * 4096;  // rotation scratch, 4 KB per warp
+  // running sums of the low-rank projection (linear layers with factors, up to 16 rows):
+  // [warp][NT][4][32]
+  static constexpr uint32_t kZacc = (LR && NT <= 2) ? (uint32_t)(kWarps * NT * 128 * 4) : 0u;
   static constexpr uint32_t kTabs = 3 * Tab<F>::kStride;  // gate, up, down (or one matrix)
-  static constexpr uint32_t kTotal = kRing + kStage + kScratch + Tab<F>::kAlign + kTabs;
+  static constexpr uint32_t kTotal = kRing + kStage + kScratch + kZacc + Tab<F>::kAlign + kTabs;
 };
 
-template <int NT, int F>
+// LR: the instantiation for a linear layer with low-rank factors (up to 16 rows); the others
+// carry none of its code.
+template <int NT, int F, bool LR>
 __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) {
   extern __shared__ __align__(16) unsigned char dsm[];
   __shared__ int s_flag;
@@ -920,10 +1268,10 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
   SmemView sv;
   const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(dsm));
   sv.ring = base;
-  using SM = Smem<NT, F>;
+  using SM = Smem<NT, F, LR>;
   sv.stage = base + SM::kRing;
   sv.scratch = reinterpret_cast<float*>(dsm + SM::kRing + SM::kStage);
-  sv.tab = (base + SM::kRing + SM::kStage + SM::kScratch + Tab<F>::kAlign - 1) & ~(Tab<F>::kAlign - 1);
+  sv.tab = (base + SM::kRing + SM::kStage + SM::kScratch + SM::kZacc + Tab<F>::kAlign - 1) & ~(Tab<F>::kAlign - 1);
   sv.flag = &s_flag;
   int* status = a.status;
   unsigned* ctl = a.ctl;
@@ -950,7 +1298,21 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
   j1.ready = nullptr;
   j1.ready_target = 0;
   j1.group_done = ctl + (a.mlp ? a.off_g : a.off_o);
+  j1.lr_v = LR ? a.lr_v : nullptr;
+  j1.lr_rank = a.lr_rank;
+  j1.lr_z = a.lr_z;
+  j1.lr_done = ctl + a.off_z;
+  j1.lw = LR ? a.lr_lw : 0;
+  j1.zacc = base + SM::kRing + SM::kStage + SM::kScratch;
   set_range(j1);
+  if (LR && (int)threadIdx.x < NT) {
+    // U's rows of this CTA's output tasks (64 channels each), towards L2 (copied from there later)
+    const int n_seg = a.d_model_out / kSuChannels;
+    for (int t = blockIdx.x; t < n_seg * NT; t += gridDim.x)
+      if (t % NT == (int)threadIdx.x)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.lr_u + (size_t)(t / NT) * kSuChannels * a.lr_rank),
+                     "r"((uint32_t)(kSuChannels * a.lr_rank * 2)) : "memory");
+  }
   if (a.mlp && threadIdx.x == 0) {
     // the down step's cell range, worked out now, away from the hand-off before that step
     const int n_seg3 = a.d_model / kSuChannels;
@@ -1040,7 +1402,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
     }
     __syncthreads();
   }
-  decode_run<F, NT, uint16_t>(j1, a.x + (size_t)a.row0 * a.d_model, cur, sv, &tables, status);
+  decode_run<F, NT, uint16_t, LR>(j1, a.x + (size_t)a.row0 * a.d_model, cur, sv, &tables, status);
 
   if (a.mlp) {
     DecodeJob j3;
@@ -1062,13 +1424,21 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
     j3.ready = ctl + a.off_hd;
     j3.ready_target = (unsigned)(a.h_chunk / kSuChannels);
     j3.group_done = ctl + a.off_o;
+    j3.lr_v = nullptr;
+    j3.lr_rank = 0;
+    j3.lr_z = nullptr;
+    j3.lr_done = nullptr;
+    j3.lw = 0;
+    j3.zacc = 0u;
     j3.c0 = s_range3[0];  // written by thread 0 before the first barrier of the gate/up step
     j3.c1 = s_range3[1];
     swiglu_tasks<NT>(a, j1, ctl + a.off_hd, status);
     // one cell's index copies ahead of the h rotation, the rest after it (as for x)
     Cursor cur3 = decode_begin<F>(j3, sv, 1);
-    decode_run<F, NT, float>(j3, a.hbuf, cur3, sv, nullptr, status);
+    decode_run<F, NT, float, false>(j3, a.hbuf, cur3, sv, nullptr, status);
     output_tasks<NT>(a, j3, sv, status);
+  } else if constexpr (LR && NT <= 2) {
+    output_tasks_lr<NT>(a, j1, sv, status);
   } else {
     output_tasks<NT>(a, j1, sv, status);
   }
@@ -1089,19 +1459,21 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
 // Every format's kernel needs more than half an SM's shared memory: one CTA per SM,
 // so the grid (and the workspace sized from it) is the same for all formats.
 static_assert(2 * Smem<1, VQ3_FORMAT_2X16>::kTotal > 228 * 1024, "one CTA per SM");
-static_assert(Smem<4, VQ3_FORMAT_LUT4>::kTotal <= 227 * 1024 && Smem<4, VQ3_FORMAT_2X64>::kTotal <= 227 * 1024,
+static_assert(Smem<4, VQ3_FORMAT_LUT4>::kTotal <= 227 * 1024 && Smem<4, VQ3_FORMAT_2X64>::kTotal <= 227 * 1024 &&
+                  Smem<2, VQ3_FORMAT_LUT4, true>::kTotal <= 227 * 1024 &&
+                  Smem<2, VQ3_FORMAT_2X64, true>::kTotal <= 227 * 1024,
               "shared memory per CTA");
 
-template <int NT, int F>
+template <int NT, int F, bool LR>
 cudaError_t launch_nt(const PersistArgs& a, cudaStream_t st) {
-  const int smem = (int)Smem<NT, F>::kTotal;
+  const int smem = (int)Smem<NT, F, LR>::kTotal;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(persistent_kernel<NT, F>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(persistent_kernel<NT, F, LR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
@@ -1115,7 +1487,7 @@ cudaError_t launch_nt(const PersistArgs& a, cudaStream_t st) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, persistent_kernel<NT, F>, a);
+  e = cudaLaunchKernelEx(&cfg, persistent_kernel<NT, F, LR>, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1124,9 +1496,9 @@ template <int NT>
 int occupancy() {
   using K = Smem<NT, VQ3_FORMAT_2X64>;
   int n = 0;
-  if (cudaFuncSetAttribute(persistent_kernel<NT, VQ3_FORMAT_2X64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(persistent_kernel<NT, VQ3_FORMAT_2X64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)K::kTotal) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, persistent_kernel<NT, VQ3_FORMAT_2X64>, kThreads, K::kTotal) !=
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, persistent_kernel<NT, VQ3_FORMAT_2X64, false>, kThreads, K::kTotal) !=
           cudaSuccess) {
     cudaGetLastError();
     return 1;
@@ -1166,18 +1538,31 @@ bool persist_cells_fit(int d_in, int d_out, int n_mats, int grid) {
   return cells * grid < (1ll << 32);  // the kernel's cell arithmetic is 32-bit unsigned
 }
 
-int persist_max_pieces(int d_in, int d_out, int n_mats, int grid) {
+int persist_max_pieces(int d_in, int d_out, int n_mats, int grid, int lw) {
   const long long n_kg = d_in / kSuInputs;
   const long long n_seg = (long long)(d_out / kSuChannels) * n_mats;
   const long long n_grp = (n_seg + kDecWarps - 1) / kDecWarps;
   const long long cells = n_grp * n_kg;
+  // the kernel's partition (cta_of_w), in 64-bit here
+  auto cost = [&](long long x) { return 8 * x + lw * (x < n_kg ? x : n_kg); };
+  auto cta = [&](long long x) { return lw ? ((cost(x) + 1) * grid - 1) / cost(cells) : ((x + 1) * grid - 1) / cells; };
   int best = 1;
   for (long long s = 0; s < n_grp; ++s) {
-    const long long x0 = s * n_kg, x1 = x0 + n_kg - 1;
-    const long long b0 = ((x0 + 1) * grid - 1) / cells, b1 = ((x1 + 1) * grid - 1) / cells;
+    const long long b0 = cta(s * n_kg), b1 = cta(s * n_kg + n_kg - 1);
     if (b1 - b0 + 1 > best) best = (int)(b1 - b0 + 1);
   }
   return best;
+}
+
+int persist_lowrank_weight(int d_in, int d_out, int grid) {
+  // first-group cells weighted 1 + 2/8 when there are at least 4 cells per CTA (so that every
+  // CTA keeps a cell) and the kernel's 32-bit partition arithmetic holds
+  const long long n_kg = d_in / kSuInputs;
+  const long long cells = ((d_out / kSuChannels) + kDecWarps - 1) / kDecWarps * n_kg;
+  constexpr int lw = 2;
+  if (cells < 4ll * grid) return 0;
+  if ((8 * cells + lw * n_kg + 1) * grid >= (1ll << 32)) return 0;
+  return lw;
 }
 
 int persist_chunk(int d, int block) {
@@ -1191,9 +1576,10 @@ namespace {
 template <int F>
 cudaError_t launch_fmt(const PersistArgs& a, int nt, cudaStream_t st) {
   switch (nt) {
-    case 1: return launch_nt<1, F>(a, st);
-    case 2: return launch_nt<2, F>(a, st);
-    case 4: return launch_nt<4, F>(a, st);
+    // a linear layer with low-rank factors has its own instantiation (up to 16 rows)
+    case 1: return a.lr_v ? launch_nt<1, F, true>(a, st) : launch_nt<1, F, false>(a, st);
+    case 2: return a.lr_v ? launch_nt<2, F, true>(a, st) : launch_nt<2, F, false>(a, st);
+    case 4: return a.lr_v ? cudaErrorInvalidValue : launch_nt<4, F, false>(a, st);
     default: return cudaErrorInvalidValue;
   }
 }

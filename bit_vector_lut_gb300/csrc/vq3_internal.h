@@ -104,8 +104,15 @@ struct PersistArgs {
   int row0, rows;           // rows of this pass: [row0, row0 + rows), rows <= 8 * NT
   int mlp;                  // 1: MLP block (gate, up, down); 0: one linear layer (gate)
   int format;               // VQ3_FORMAT_* of every matrix
-  const float* lr_y;        // low-rank correction U V x' [rows][d_out] FP32 for all rows of the
-                            // call (linear layer only), or null
+  // low-rank correction U (V x') of a linear layer (null lr_v: none; MLP: none). The CTAs
+  // that decode the first segment group also form z = V x' from their rotated activations
+  // and write one partial [8 * NT][64] FP32 each to lr_z; the output step sums them in CTA
+  // order and adds U z before rounding.
+  const uint16_t* lr_v;     // [lr_rank][d_model], FP16
+  const uint16_t* lr_u;     // [d_model_out][lr_rank], FP16
+  int lr_rank;              // a multiple of 8, <= 64
+  float* lr_z;              // max_pieces1 x [8 * NT][64] FP32
+  int lr_lw;                // the first group's cell weight in the CTA ranges (persist_lowrank_weight)
   // pre-norm residual step fused ahead of the block (MLP only): the block's input rows are
   // fp16(r' / sqrt(mean(r'^2) + eps)) with r' = fp16(x + res_delta) (x alone when res_delta is
   // null), and r' is written to res_out (which aliases neither x nor res_delta)
@@ -138,13 +145,17 @@ struct PersistArgs {
   int n_ctl;
   int off_g, off_hd, off_o; // word offsets: gate/up segment groups, h chunks (SwiGLU tasks
                             // done), output segment groups; word 0 counts finished CTAs
+  int off_z;                // linear layer: CTAs whose partial of z (low-rank) is written
   int* status;              // workspace status word (3: a wait timed out)
   uint16_t* out;            // row-major [*][d_model] (linear: [*][d_out])
 };
 
 int persist_grid(int nt);  // CTAs of the persistent kernel: resident CTAs per SM x SMs
 int persist_decode_grid(int d_in, int d_out, int n_mats, int grid);  // decoding CTAs (<= cells)
-int persist_max_pieces(int d_in, int d_out, int n_mats, int grid);
+int persist_max_pieces(int d_in, int d_out, int n_mats, int grid, int lw = 0);
+// Extra weight (eighths of a cell) of the first segment group's cells in the decode kernel's CTA
+// ranges for a linear layer with low-rank factors (those CTAs also form z), or 0.
+int persist_lowrank_weight(int d_in, int d_out, int grid);
 // Whether the decode kernel's 32-bit cell arithmetic holds (cells x grid < 2^32).
 bool persist_cells_fit(int d_in, int d_out, int n_mats, int grid);
 int persist_chunk(int d, int block);  // rotation chunk: whole blocks, up to 1024 columns

@@ -61,6 +61,7 @@ def _load() -> ctypes.CDLL:
         "vq3_linear_forward": (c_int, [c_void_p, c_int, POINTER(vq3_linear), c_void_p, c_void_p, c_size_t, c_void_p]),
         "vq3_mlp_forward": (c_int, [c_void_p, c_int, POINTER(vq3_mlp_layer), c_void_p, c_void_p, c_size_t, c_void_p]),
         "vq3_mlp_kernel_launches": (c_int, [c_int, POINTER(vq3_mlp_layer)]),
+        "vq3_linear_kernel_launches": (c_int, [c_int, POINTER(vq3_linear)]),
         "vq3_mlp_host_workspace_bytes": (c_size_t, [c_int, POINTER(vq3_mlp_layer)]),
         "vq3_mlp_forward_host": (c_int, [c_void_p, c_int, POINTER(vq3_mlp_layer), c_void_p, c_void_p, c_size_t,
                                          c_void_p]),
@@ -276,6 +277,10 @@ def noalloc_status(stream=None) -> int:
 
 def mlp_kernel_launches(rows: int, layer: MLP) -> int:
     return int(lib.vq3_mlp_kernel_launches(rows, ctypes.byref(layer.struct)))
+
+
+def linear_kernel_launches(rows: int, lin: Linear) -> int:
+    return int(lib.vq3_linear_kernel_launches(rows, ctypes.byref(lin.struct)))
 
 
 def mlp_forward_host(x: np.ndarray, layer: MLP, ws: torch.Tensor, out: np.ndarray | None = None,

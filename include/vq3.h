@@ -297,6 +297,15 @@ VQ3_API int vq3_mlp_prenorm_step(const uint16_t* r, const float* ss, int rows, c
 VQ3_API int vq3_mlp_kernel_launches(int rows, const vq3_mlp_layer* layer);
 
 /*
+ * Number of kernels one vq3_linear_forward call launches at `rows` rows: 1
+ * below 17 rows (the decode kernel, which also forms the low-rank correction
+ * of a layer with factors); from 17 rows on 2 (rotation, GEMM), 4 with
+ * low-rank factors (plus their projection and expansion). -1 on a bad
+ * descriptor or negative rows.
+ */
+VQ3_API int vq3_linear_kernel_launches(int rows, const vq3_linear* L);
+
+/*
  * Cited as vq3_mlp_forward (an interface convenience for host buffers).
  * Same as vq3_mlp_forward with HOST buffers: copies x (pinned or pageable host
  * memory) to the workspace, runs the block, copies the result back into
