@@ -11,9 +11,10 @@
 //     U      = (I + N)^-1 (V - Gamma K S0)
 //     O      = Gamma Q S0 + M U,  M[t][j] = (gamma_t / gamma_j) beta_j (q_t . k_j)  for j <= t
 //     S8     = gamma_8 S0 + K^T diag(beta_j gamma_8 / gamma_j) U
-// Every column of S, V, U and O is independent of the others, so one CTA takes one
-// head and 16 of its d_v columns, keeps that slice of the state in shared memory
-// and walks the blocks in order. FP32 arithmetic, FP16 inputs and outputs.
+// Every column of S, V, U and O is independent of the others, so a CTA takes one
+// head and 16 of its d_v columns and walks the blocks in order. Two kernels: the
+// tensor-core one below (d_k a multiple of 16 up to 128) and, for other d_k, one in
+// FP32 on CUDA cores that keeps the state slice in shared memory.
 #include <cuda_fp16.h>
 
 #include "vq3_internal.h"
@@ -161,13 +162,296 @@ __global__ void __launch_bounds__(kDThreads) delta_rule_kernel(const uint16_t* _
   for (int e = tid; e < d_k * kCols; e += kDThreads) Sg[(size_t)(e / kCols) * d_v + c0 + e % kCols] = Ss[e];
 }
 
+
+// ---------------------------------------------------------------- tensor-core path (d_k = 16 KS <= 128)
+//
+// One warp per (head, 16 columns of d_v). The state slice is held transposed, S^T [16 columns]
+// [d_k], as the accumulators of m16n8k16 tiles (n-tile n: d_k 8n .. 8n+7): that is also the
+// A-operand layout of the next product S^T [K; Q]^T, so the state never leaves the registers
+// between blocks. The FP32 operands that enter the tensor cores (the state, the weighted U)
+// are split into two FP16 parts, hi = fp16(x) and lo = fp16(x - hi), and multiplied as two
+// MMAs into FP32 accumulators (about 22 bits of each operand; K and Q are FP16 inputs).
+// Per chunk of up to 64 tokens: K, Q, V staged in shared memory; for every 8-token block the
+// state-independent parts first (K K^T and Q K^T as one 16 x 8 tile, then N, the closed-form
+// P = (I - N)(I + N^2)(I + N^4), M and the weights), then the blocks in order:
+//     [X_K | X_Q] = S^T [K; Q]^T,  R^T = V^T - X_K Gamma,  U^T = R^T P^T,
+//     O^T = X_Q Gamma + U^T M^T,   S^T = gamma_8 S^T + (U diag(w))^T K,  w_j = beta_j gamma_8 / gamma_j.
+
+constexpr int kTcChunk = 64;  // tokens staged at a time (8 blocks)
+
+__device__ __forceinline__ void mma_tc(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// (x, y) -> FP16 pair hi and the pair of what hi leaves, lo.
+__device__ __forceinline__ void split2(float x, float y, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(x, y);
+  const float2 e = __half22float2(h);
+  const __half2 l = __floats2half2_rn(x - e.x, y - e.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+template <int KS>
+__global__ void __launch_bounds__(32) delta_rule_tc_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+                                                           const uint16_t* __restrict__ v,
+                                                           const float* __restrict__ beta,
+                                                           const float* __restrict__ alpha, int tokens, int heads,
+                                                           int d_v, float* __restrict__ state,
+                                                           uint16_t* __restrict__ out) {
+  constexpr int DK = 16 * KS;
+  constexpr int NTD = DK / 8;       // state n-tiles
+  constexpr int RS = DK + 8;        // staged row stride in halves: 4 words past a multiple of 32
+  __shared__ __align__(16) uint16_t Ks[kTcChunk * RS];
+  __shared__ __align__(16) uint16_t Qs[kTcChunk * RS];
+  __shared__ float Vs[kTcChunk][16];
+  __shared__ float Pm[kTcChunk / 8][8][8], Mm[kTcChunk / 8][8][8];
+  __shared__ float Gm[kTcChunk / 8][8], Wm[kTcChunk / 8][8];
+  __shared__ float Al[kTcChunk], Be[kTcChunk];  // alpha, beta of the chunk's tokens (1, 0 past the last)
+  __shared__ float Nn[8][8], N2[8][8], N4[8][8], Am[8][8], KK[8][8], QK[8][8];
+  const int lane = threadIdx.x, g = lane >> 2, t = lane & 3;
+  const int h = blockIdx.x, c0 = blockIdx.y * 16;
+  float* Sg = state + (size_t)h * DK * d_v + c0;
+
+  // the state slice into the accumulator layout: acc[n] = S^T[g, g+8][8n + 2t, +1]
+  float acc[NTD][4];
+#pragma unroll
+  for (int n = 0; n < NTD; ++n) {
+    const int d = 8 * n + 2 * t;
+    acc[n][0] = Sg[(size_t)d * d_v + g];
+    acc[n][1] = Sg[(size_t)(d + 1) * d_v + g];
+    acc[n][2] = Sg[(size_t)d * d_v + g + 8];
+    acc[n][3] = Sg[(size_t)(d + 1) * d_v + g + 8];
+  }
+
+  for (int base = 0; base < tokens; base += kTcChunk) {
+    const int nt = tokens - base < kTcChunk ? tokens - base : kTcChunk;
+    const int nb = (nt + 7) / 8;
+    // ---- stage K, Q (16-byte copies), V; tokens past the last are zero (beta 0, alpha 1 below)
+    const uint32_t ks = static_cast<uint32_t>(__cvta_generic_to_shared(Ks));
+    const uint32_t qs = static_cast<uint32_t>(__cvta_generic_to_shared(Qs));
+    for (int i = lane; i < nb * 8 * (DK / 8); i += 32) {
+      const int tk = i / (DK / 8), c = i % (DK / 8);
+      const uint32_t off = (uint32_t)(tk * RS + c * 8) * 2u;
+      if (tk < nt) {
+        const size_t src = ((size_t)(base + tk) * heads + h) * DK + c * 8;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(ks + off), "l"(k + src) : "memory");
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(qs + off), "l"(q + src) : "memory");
+      } else {
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(ks + off), "r"(0u) : "memory");
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(qs + off), "r"(0u) : "memory");
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    for (int i = lane; i < nb * 8; i += 32) {
+      Al[i] = i < nt ? alpha[(size_t)(base + i) * heads + h] : 1.f;
+      Be[i] = i < nt ? beta[(size_t)(base + i) * heads + h] : 0.f;
+    }
+    for (int i = lane; i < nb * 8 * 16; i += 32) {
+      const int tk = i >> 4, c = i & 15;
+      Vs[tk][c] = tk < nt ? __half2float(__ushort_as_half(v[((size_t)(base + tk) * heads + h) * d_v + c0 + c])) : 0.f;
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncwarp();
+
+    // ---- the state-independent parts of every block
+    for (int b = 0; b < nb; ++b) {
+      const int tb = 8 * b;
+      float gk[4] = {0.f, 0.f, 0.f, 0.f};  // rows g: k_g . k_{2t}, k_g . k_{2t+1}; rows g+8: q_g . k_..
+#pragma unroll
+      for (int s = 0; s < KS; ++s) {
+        const uint16_t* kr = Ks + (tb + g) * RS + 16 * s + 2 * t;
+        const uint16_t* qr = Qs + (tb + g) * RS + 16 * s + 2 * t;
+        const uint32_t k0 = *reinterpret_cast<const uint32_t*>(kr), k1 = *reinterpret_cast<const uint32_t*>(kr + 8);
+        const uint32_t q0 = *reinterpret_cast<const uint32_t*>(qr), q1 = *reinterpret_cast<const uint32_t*>(qr + 8);
+        const uint32_t a[4] = {k0, q0, k1, q1};
+        mma_tc(gk, a, k0, k1);
+      }
+      KK[g][2 * t] = gk[0];
+      KK[g][2 * t + 1] = gk[1];
+      QK[g][2 * t] = gk[2];
+      QK[g][2 * t + 1] = gk[3];
+      if (lane == 0) {
+        float gam = 1.f;
+        for (int j = 0; j < 8; ++j) {  // gamma_j = alpha_1 ... alpha_j; beta, then the weights below
+          gam *= Al[tb + j];
+          Gm[b][j] = gam;
+          Wm[b][j] = Be[tb + j];
+        }
+      }
+      __syncwarp();
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {  // N (strictly lower) and M (lower with the diagonal)
+        const int e = lane + 32 * e2, ti = e >> 3, j = e & 7;
+        const float f = Gm[b][ti] / Gm[b][j] * Wm[b][j];
+        Nn[ti][j] = j < ti ? f * KK[ti][j] : 0.f;
+        Mm[b][ti][j] = j <= ti ? f * QK[ti][j] : 0.f;
+      }
+      __syncwarp();
+      auto mul8 = [&](float (*x)[8], float (*y)[8], float (*z)[8], float dx, float dy) {
+        // z = (dx I + x)(dy I + y), two entries per lane
+        float r2[2];
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const int e = lane + 32 * e2, ti = e >> 3, j = e & 7;
+          float s = 0.f;
+#pragma unroll
+          for (int m = 0; m < 8; ++m) s = fmaf((ti == m ? dx : 0.f) + x[ti][m], (m == j ? dy : 0.f) + y[m][j], s);
+          r2[e2] = s;
+        }
+        __syncwarp();
+        z[lane >> 3][lane & 7] = r2[0];
+        z[(lane + 32) >> 3][lane & 7] = r2[1];
+        __syncwarp();
+      };
+      mul8(Nn, Nn, N2, 0.f, 0.f);   // N^2
+      mul8(N2, N2, N4, 0.f, 0.f);   // N^4
+      // (I - N)(I + N^2): negate N in place first
+      Nn[lane >> 3][lane & 7] = -Nn[lane >> 3][lane & 7];
+      Nn[(lane + 32) >> 3][lane & 7] = -Nn[(lane + 32) >> 3][lane & 7];
+      __syncwarp();
+      mul8(Nn, N2, Am, 1.f, 1.f);
+      mul8(Am, N4, Pm[b], 0.f, 1.f);  // P = A (I + N^4)
+      if (lane < 8) Wm[b][lane] = Wm[b][lane] * Gm[b][7] / Gm[b][lane];  // w_j = beta_j gamma_8 / gamma_j
+      __syncwarp();
+    }
+
+    // ---- the blocks in order
+    for (int b = 0; b < nb; ++b) {
+      const int tb = 8 * b;
+      float xk[4] = {0.f, 0.f, 0.f, 0.f}, xq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int s = 0; s < KS; ++s) {
+        uint32_t ah[4], al[4];
+        split2(acc[2 * s][0], acc[2 * s][1], ah[0], al[0]);
+        split2(acc[2 * s][2], acc[2 * s][3], ah[1], al[1]);
+        split2(acc[2 * s + 1][0], acc[2 * s + 1][1], ah[2], al[2]);
+        split2(acc[2 * s + 1][2], acc[2 * s + 1][3], ah[3], al[3]);
+        const uint16_t* kr = Ks + (tb + g) * RS + 16 * s + 2 * t;
+        const uint16_t* qr = Qs + (tb + g) * RS + 16 * s + 2 * t;
+        const uint32_t k0 = *reinterpret_cast<const uint32_t*>(kr), k1 = *reinterpret_cast<const uint32_t*>(kr + 8);
+        const uint32_t q0 = *reinterpret_cast<const uint32_t*>(qr), q1 = *reinterpret_cast<const uint32_t*>(qr + 8);
+        mma_tc(xk, ah, k0, k1);
+        mma_tc(xq, ah, q0, q1);
+        mma_tc(xk, al, k0, k1);
+        mma_tc(xq, al, q0, q1);
+      }
+      // xk = (K S)^T at [g][2t], [g][2t+1], [g+8][2t], [g+8][2t+1]; likewise xq = (Q S)^T
+      const float* gm = Gm[b];
+      const int j0 = 2 * t, j1 = 2 * t + 1;
+      const float r0 = Vs[tb + j0][g] - gm[j0] * xk[0], r1 = Vs[tb + j1][g] - gm[j1] * xk[1];
+      const float r2 = Vs[tb + j0][g + 8] - gm[j0] * xk[2], r3 = Vs[tb + j1][g + 8] - gm[j1] * xk[3];
+      // U^T[c][i] = sum_j P[i][j] R^T[c][j]: this lane's two j, then the four lanes of row g
+      float ulo[8], uhi[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        ulo[i] = fmaf(Pm[b][i][j1], r1, Pm[b][i][j0] * r0);
+        uhi[i] = fmaf(Pm[b][i][j1], r3, Pm[b][i][j0] * r2);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        ulo[i] += __shfl_xor_sync(0xffffffffu, ulo[i], 1);
+        uhi[i] += __shfl_xor_sync(0xffffffffu, uhi[i], 1);
+        ulo[i] += __shfl_xor_sync(0xffffffffu, ulo[i], 2);
+        uhi[i] += __shfl_xor_sync(0xffffffffu, uhi[i], 2);
+      }
+      // this lane's entries (selected, not indexed: the arrays stay in registers)
+      float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        u0 = i == j0 ? ulo[i] : u0;
+        u1 = i == j1 ? ulo[i] : u1;
+        u2 = i == j0 ? uhi[i] : u2;
+        u3 = i == j1 ? uhi[i] : u3;
+      }
+      // O^T[c][i] = gamma_i X_Q[c][i] + sum_{j <= i} M[i][j] U^T[c][j] (the full sum over j: M is zero above)
+      float olo[8], ohi[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        olo[i] = fmaf(Mm[b][i][j1], u1, Mm[b][i][j0] * u0);
+        ohi[i] = fmaf(Mm[b][i][j1], u3, Mm[b][i][j0] * u2);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        olo[i] += __shfl_xor_sync(0xffffffffu, olo[i], 1);
+        ohi[i] += __shfl_xor_sync(0xffffffffu, ohi[i], 1);
+        olo[i] += __shfl_xor_sync(0xffffffffu, olo[i], 2);
+        ohi[i] += __shfl_xor_sync(0xffffffffu, ohi[i], 2);
+      }
+      {
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          s0 = i == j0 ? olo[i] : s0;
+          s1 = i == j1 ? olo[i] : s1;
+          s2 = i == j0 ? ohi[i] : s2;
+          s3 = i == j1 ? ohi[i] : s3;
+        }
+        const float o0 = fmaf(gm[j0], xq[0], s0), o1 = fmaf(gm[j1], xq[1], s1);
+        const float o2 = fmaf(gm[j0], xq[2], s2), o3 = fmaf(gm[j1], xq[3], s3);
+        const int tk0 = base + tb + j0, tk1 = base + tb + j1;
+        if (tk0 < tokens) {
+          uint16_t* o = out + ((size_t)tk0 * heads + h) * d_v + c0;
+          o[g] = __half_as_ushort(__float2half_rn(o0));
+          o[g + 8] = __half_as_ushort(__float2half_rn(o2));
+        }
+        if (tk1 < tokens) {
+          uint16_t* o = out + ((size_t)tk1 * heads + h) * d_v + c0;
+          o[g] = __half_as_ushort(__float2half_rn(o1));
+          o[g + 8] = __half_as_ushort(__float2half_rn(o3));
+        }
+      }
+      // S^T <- gamma_8 S^T + W^T K with W^T[c][j] = U^T[c][j] w_j (tokens 8..15 of the k-step are zero)
+      uint32_t wh[4], wl[4];
+      split2(u0 * Wm[b][j0], u1 * Wm[b][j1], wh[0], wl[0]);
+      split2(u2 * Wm[b][j0], u3 * Wm[b][j1], wh[1], wl[1]);
+      wh[2] = wh[3] = wl[2] = wl[3] = 0u;
+      const float g8 = gm[7];
+#pragma unroll
+      for (int n = 0; n < NTD; ++n) {
+        const uint16_t kv0 = Ks[(tb + j0) * RS + 8 * n + g], kv1 = Ks[(tb + j1) * RS + 8 * n + g];
+        const uint32_t bk = (uint32_t)kv0 | ((uint32_t)kv1 << 16);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[n][r] *= g8;
+        mma_tc(acc[n], wh, bk, 0u);
+        mma_tc(acc[n], wl, bk, 0u);
+      }
+    }
+    __syncwarp();  // the staged chunk is read no more
+  }
+#pragma unroll
+  for (int n = 0; n < NTD; ++n) {
+    const int d = 8 * n + 2 * t;
+    Sg[(size_t)d * d_v + g] = acc[n][0];
+    Sg[(size_t)(d + 1) * d_v + g] = acc[n][1];
+    Sg[(size_t)d * d_v + g + 8] = acc[n][2];
+    Sg[(size_t)(d + 1) * d_v + g + 8] = acc[n][3];
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_delta_rule(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* beta,
                               const float* alpha, int tokens, int heads, int d_k, int d_v, float* state,
                               uint16_t* out, cudaStream_t st) {
-  const size_t smem = (size_t)(d_k * kCols + 2 * kB * d_k) * sizeof(float);
   const dim3 grid((unsigned)heads, (unsigned)(d_v / kCols));
+  const bool al = (reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k)) % 16 == 0;
+  if (d_k % 16 == 0 && d_k <= 128 && al) {  // the tensor-core path (16-byte staging of q and k)
+    switch (d_k / 16) {
+      case 1: delta_rule_tc_kernel<1><<<grid, 32, 0, st>>>(q, k, v, beta, alpha, tokens, heads, d_v, state, out); break;
+      case 2: delta_rule_tc_kernel<2><<<grid, 32, 0, st>>>(q, k, v, beta, alpha, tokens, heads, d_v, state, out); break;
+      case 3: delta_rule_tc_kernel<3><<<grid, 32, 0, st>>>(q, k, v, beta, alpha, tokens, heads, d_v, state, out); break;
+      case 4: delta_rule_tc_kernel<4><<<grid, 32, 0, st>>>(q, k, v, beta, alpha, tokens, heads, d_v, state, out); break;
+      case 5: delta_rule_tc_kernel<5><<<grid, 32, 0, st>>>(q, k, v, beta, alpha, tokens, heads, d_v, state, out); break;
+      case 6: delta_rule_tc_kernel<6><<<grid, 32, 0, st>>>(q, k, v, beta, alpha, tokens, heads, d_v, state, out); break;
+      case 7: delta_rule_tc_kernel<7><<<grid, 32, 0, st>>>(q, k, v, beta, alpha, tokens, heads, d_v, state, out); break;
+      default: delta_rule_tc_kernel<8><<<grid, 32, 0, st>>>(q, k, v, beta, alpha, tokens, heads, d_v, state, out); break;
+    }
+    return cudaGetLastError();
+  }
+  const size_t smem = (size_t)(d_k * kCols + 2 * kB * d_k) * sizeof(float);
   delta_rule_kernel<<<grid, kDThreads, smem, st>>>(q, k, v, beta, alpha, tokens, heads, d_k, d_v, state, out);
   return cudaGetLastError();
 }

@@ -43,9 +43,11 @@ def run_oracle(w):
     return outs, states
 
 
-@pytest.mark.parametrize("tokens", [1, 8, 13, 64])
-@pytest.mark.parametrize("d_k,d_v", [(128, 128), (64, 32)])
+@pytest.mark.parametrize("tokens", [1, 8, 13, 64, 136])
+@pytest.mark.parametrize("d_k,d_v", [(128, 128), (64, 32), (32, 16), (24, 16)])
 def test_delta_rule_matches_recurrence(vq3, tokens, d_k, d_v):
+    # d_k a multiple of 16 up to 128: the tensor-core kernel (64 tokens staged at a time, so 136
+    # tokens take three chunks); d_k = 24: the CUDA-core kernel
     w = S.delta_rule_inputs(seed=9, tokens=tokens, heads=16, d_k=d_k, d_v=d_v)
     out, state = run_gpu(vq3, w)
     ref_out, ref_state = run_oracle(w)
