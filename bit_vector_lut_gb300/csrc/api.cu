@@ -295,7 +295,8 @@ constexpr int kPrefillRows = 17;  // from this many rows on, the tcgen05 path (t
 
 // [status word][counter words: part flags][x' FP16 [rows][d_in]]
 // [h FP32 [rows][d_inter]][h' FP16 [rows][d_inter]][parts of split tiles]
-// ([U V x' FP32 [rows][d_out]][projection sums FP32 [chunks][rows][rank]] with low-rank factors)
+// ([U V x' FP32 [rows][d_out]][projection parts FP32 [splits][rows][rank], then z [rows][rank]]
+// with low-rank factors)
 struct PrefillWs {
   size_t status, flags, xr, h, hr, part, ylr, zpart, total;
 };
@@ -317,7 +318,7 @@ PrefillWs prefill_ws(int rows, int d_in, int d_inter, size_t ctl, int rank = 0, 
   if (rank) {
     off = round_up(off + (size_t)rows * d_out * sizeof(float), 256);
     w.zpart = off;
-    off = round_up(off + (size_t)lowrank_chunks(d_in) * rows * rank * sizeof(float), 256);
+    off = round_up(off + lowrank_part_floats(d_in, rows, rank) * sizeof(float), 256);
   }
   w.total = off;
   return w;
@@ -835,7 +836,7 @@ int vq3_mlp_kernel_launches(int rows, const vq3_mlp_layer* layer) {
 int vq3_linear_kernel_launches(int rows, const vq3_linear* L) {
   if (check_linear(L, "linear") || rows < 0) return -1;
   if (rows == 0) return 0;
-  if (rows >= kPrefillRows) return L->lr_rank ? 4 : 2;  // rotate x, (project, expand,) GEMM
+  if (rows >= kPrefillRows) return L->lr_rank ? 5 : 2;  // rotate x, (project, reduce, expand,) GEMM
   return 1;  // the decode kernel alone, the low-rank correction formed inside it
 }
 

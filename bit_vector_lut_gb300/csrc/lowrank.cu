@@ -1,18 +1,20 @@
-// The low-rank correction of a VQ3 linear layer, y_lr = U (V x') for the rotated
-// input rows x', in FP32; the output step of the decode kernel and the epilogue
-// of the tensor-core GEMM add it before the single FP16 rounding of y.
+// The low-rank correction of a VQ3 linear layer at prefill sizes (17 rows and more),
+// y_lr = U (V x') for the rotated input rows x', in FP32; the epilogue of the tensor-core
+// GEMM adds it before the single FP16 rounding of y. (Below 17 rows the decode kernel forms
+// the same correction itself.)
 //
 // Source: model card "anemll/anemll-forge-qwen3.8-27B", release-comparison table
 // row "Token mixers" (rank-64 factors) and "ANEMLL ANE LLM conversion pipeline",
 // "Facts" (rank-64 residual correction): the weight is diag(s) C[idx] + U V on
 // the rotated input.
 //
-// Projection: one CTA computes 8 rows x 8 factor rows j over one chunk of 512
-// inputs: warp w takes row r = 8 * blockIdx.z + w, each lane 8 consecutive
-// inputs of each 256-input step (one 16-byte load of x' and of each of the 8 V
-// rows), and the 8 sums are reduced across the warp in a fixed order. The
-// chunks' sums are added in chunk order by the expansion kernel, so the result
-// does not depend on timing.
+// Three launches, all on m16n8k16 tensor cores or plain adds:
+//   projection  part[sp] = x' V^T over input split sp (64-row tiles x the 64 factor rows,
+//               x' and V staged by 16-byte cp.async, two stages);
+//   reduction   z = sum of part[sp] in split order (FP32);
+//   expansion   y_lr = z U^T (64-row x 128-output tiles; z enters the MMA as two FP16
+//               parts hi = fp16(z), lo = fp16(z - hi), U as FP16).
+// The split count grows as the row tiles shrink, so that a few rows still fill the GPU.
 #include <cuda_fp16.h>
 
 #include "vq3_internal.h"
@@ -20,118 +22,200 @@
 namespace vq3 {
 namespace {
 
-__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
-  const __half2* h = reinterpret_cast<const __half2*>(&v);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float2 p = __half22float2(h[k]);
-    f[2 * k] = p.x;
-    f[2 * k + 1] = p.y;
-  }
+constexpr int kLT = 64;        // rows per tile
+constexpr int kLK = 64;        // inputs per stage
+constexpr int kLS = kLK + 8;   // staged row stride in halves: 4 words past a multiple of 32
+
+__device__ __forceinline__ void mma_lr(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+__device__ __forceinline__ void cp16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src) : "memory");
+}
+__device__ __forceinline__ void zero16(void* dst) { *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u); }
+__device__ __forceinline__ uint32_t ld32(const uint16_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
 
-constexpr int kChunk = 512;  // inputs per CTA of the projection
+// Input pair held by position pair p of a 16-input group when x' is in the GEMM's operand
+// order (positions 2p, 2p+1 hold inputs 2c, 2c+1 with c = p/2 + 4 (p % 2)).
+__device__ __forceinline__ int held_pair(int p) { return (p >> 1) + 4 * (p & 1); }
 
-__global__ void __launch_bounds__(256) lowrank_project_kernel(const uint16_t* __restrict__ xr, int rows, int d_in,
+// part[sp][r][q] = sum over the inputs of split sp of x'[r][i] V[q][i]. CTA (row tile, split):
+// warp w takes rows 16w .. 16w+15 of the tile and all 64 factor rows (8 n-tiles).
+template <bool kMmaOrder>
+__global__ void __launch_bounds__(128) lowrank_project_kernel(const uint16_t* __restrict__ xr, int rows, int d_in,
                                                               const uint16_t* __restrict__ V, int rank,
-                                                              float* __restrict__ part, int xr_mma_order) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kc = blockIdx.x;
-  const int j0 = blockIdx.y * 8;
-  const int r = blockIdx.z * 8 + warp;
-  if (r >= rows) return;  // whole warp: no block-wide synchronisation below
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  const uint16_t* xrow = xr + (size_t)r * d_in;
+                                                              float* __restrict__ part, int n_split) {
+  __shared__ __align__(16) uint16_t xs[2][kLT * kLS];
+  __shared__ __align__(16) uint16_t vs[2][64 * kLS];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int r0 = blockIdx.x * kLT, sp = blockIdx.y;
+  const int n_kg = d_in / kLK;
+  const int kg0 = (int)((long long)sp * n_kg / n_split), kg1 = (int)((long long)(sp + 1) * n_kg / n_split);
+  auto stage = [&](int buf, int kg) {
+    for (int i = tid; i < 64 * 8; i += 128) {
+      const int row = i >> 3, c = i & 7;
+      uint16_t* dx = xs[buf] + row * kLS + c * 8;
+      if (r0 + row < rows) cp16(dx, xr + (size_t)(r0 + row) * d_in + (size_t)kg * kLK + c * 8);
+      else zero16(dx);
+      uint16_t* dv = vs[buf] + row * kLS + c * 8;
+      if (row < rank) cp16(dv, V + (size_t)row * d_in + (size_t)kg * kLK + c * 8);
+      else zero16(dv);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  float acc[8][4];
 #pragma unroll
-  for (int step = 0; step < kChunk / 256; ++step) {
-    const int i0 = kc * kChunk + step * 256 + 8 * lane;
-    if (i0 < d_in) {  // d_in is a multiple of 64: an 8-input group is wholly in or out
-      float xv[8];
-      unpack8(*reinterpret_cast<const uint4*>(xrow + i0), xv);
+  for (int n = 0; n < 8; ++n)
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        float vv[8];
-        if (xr_mma_order) {
-          // x' holds the inputs of its 16-column group in the GEMM's operand order: take
-          // the V entries of the inputs that positions i0 .. i0+7 hold
-          const uint16_t* vrow = V + (size_t)(j0 + jj) * d_in + (i0 & ~15);
-          float v16[16];
-          unpack8(__ldg(reinterpret_cast<const uint4*>(vrow)), *reinterpret_cast<float(*)[8]>(v16));
-          unpack8(__ldg(reinterpret_cast<const uint4*>(vrow + 8)), *reinterpret_cast<float(*)[8]>(v16 + 8));
+    for (int j = 0; j < 4; ++j) acc[n][j] = 0.f;
+  // the V word offsets of b0 / b1 within a 16-input group (the inputs x' holds at positions 2t.. / 2t+8..)
+  const int vo0 = kMmaOrder ? 2 * held_pair(t) : 2 * t, vo1 = kMmaOrder ? 2 * held_pair(t + 4) : 2 * t + 8;
+  if (kg0 < kg1) stage(0, kg0);
+  for (int kg = kg0; kg < kg1; ++kg) {
+    const int buf = (kg - kg0) & 1;
+    if (kg + 1 < kg1) {
+      stage(buf ^ 1, kg + 1);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
+    __syncthreads();  // the stage's copies (and zero fills) of every thread are visible
+    const uint16_t* xa = xs[buf] + (16 * warp + g) * kLS + 2 * t;
+    const uint16_t* vb = vs[buf] + g * kLS;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) vv[k] = v16[mma_order_input((i0 & 15) + k)];
-        } else {
-          unpack8(__ldg(reinterpret_cast<const uint4*>(V + (size_t)(j0 + jj) * d_in + i0)), vv);
-        }
+    for (int s = 0; s < kLK / 16; ++s) {
+      const uint32_t a[4] = {ld32(xa + 16 * s), ld32(xa + 8 * kLS + 16 * s), ld32(xa + 16 * s + 8),
+                             ld32(xa + 8 * kLS + 16 * s + 8)};
 #pragma unroll
-        for (int k = 0; k < 8; ++k) acc[jj] = fmaf(vv[k], xv[k], acc[jj]);
+      for (int n = 0; n < 8; ++n) {
+        const uint16_t* vr = vb + 8 * n * kLS + 16 * s;
+        mma_lr(acc[n], a, ld32(vr + vo0), ld32(vr + vo1));
       }
     }
+    __syncthreads();  // every warp is done with this stage before it is refilled
   }
 #pragma unroll
-  for (int jj = 0; jj < 8; ++jj)
+  for (int n = 0; n < 8; ++n) {
+    const int q = 8 * n + 2 * t;
+    if (q >= rank) continue;  // rank is a multiple of 8: q and q + 1 are both in or both out
 #pragma unroll
-    for (int h = 16; h > 0; h >>= 1) acc[jj] += __shfl_xor_sync(0xffffffffu, acc[jj], h);
-  if (lane == 0) {
-    float* o = part + ((size_t)kc * rows + r) * rank + j0;  // chunk kc's sums
-#pragma unroll
-    for (int jj = 0; jj < 8; ++jj) o[jj] = acc[jj];
+    for (int h = 0; h < 2; ++h) {
+      const int r = r0 + 16 * warp + g + 8 * h;
+      if (r < rows)
+        *reinterpret_cast<float2*>(part + ((size_t)sp * rows + r) * rank + q) = make_float2(acc[n][2 * h], acc[n][2 * h + 1]);
+    }
   }
 }
 
-// y_lr[r][o] = sum_q U[o][q] z[r][q], z[r][q] = sum over chunks kc = 0, 1, ... of
-// part[kc][r][q] in that order. One CTA: 256 output channels x 16 rows; z of its
-// rows is summed into shared memory once, each thread keeps its U row in registers.
-__global__ void __launch_bounds__(256) lowrank_expand_kernel(const float* __restrict__ part, int n_chunks, int rows,
-                                                             int rank, const uint16_t* __restrict__ U, int d_out,
-                                                             float* __restrict__ ylr) {
-  __shared__ float zs[16][64];
-  const int r0 = blockIdx.y * 16;
-  for (int e = threadIdx.x; e < 16 * 64; e += blockDim.x) {
-    const int rr = e / 64, q = e % 64;
-    float s = 0.f;  // entries past the rank stay zero
-    if (q < rank && r0 + rr < rows)
-      for (int kc = 0; kc < n_chunks; ++kc) s += __ldg(part + ((size_t)kc * rows + r0 + rr) * rank + q);
-    zs[rr][q] = s;
+// z[r][q] = part[0][r][q] + part[1][r][q] + ... in split order.
+__global__ void __launch_bounds__(256) lowrank_reduce_kernel(const float* __restrict__ part, int n_split, int n,
+                                                             float* __restrict__ z) {
+  const int e = blockIdx.x * 256 + threadIdx.x;
+  if (e >= n) return;
+  float s = 0.f;
+  for (int k0 = 0; k0 < n_split; k0 += 8) {
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = k0 + k < n_split ? __ldg(part + (size_t)(k0 + k) * n + e) : 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) s += v[k];
   }
+  z[e] = s;
+}
+
+// y_lr[r][o] = sum_q z[r][q] U[o][q]. CTA: 64 rows x 128 outputs; warp w: rows 16w .. 16w+15,
+// 16 n-tiles of 8 outputs. z (FP32) enters as FP16 hi and lo parts, two MMAs per tile and k-step.
+__global__ void __launch_bounds__(128) lowrank_expand_kernel(const float* __restrict__ z, int rows, int rank,
+                                                             const uint16_t* __restrict__ U, int d_out,
+                                                             float* __restrict__ ylr) {
+  __shared__ uint32_t zh[kLT][36], zl[kLT][36];        // FP16 pairs of z [row][q pair], stride 36 words
+  __shared__ __align__(16) uint16_t us[128 * kLS];    // U rows of the tile's outputs, q 0 .. 63
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int o0 = blockIdx.x * 128, r0 = blockIdx.y * kLT;
+  for (int i = tid; i < 128 * 8; i += 128) {  // U: 16-byte chunks of each row (q past the rank zero)
+    const int row = i >> 3, c = i & 7;
+    uint16_t* du = us + row * kLS + c * 8;
+    if (o0 + row < d_out && c * 8 < rank) cp16(du, U + (size_t)(o0 + row) * rank + c * 8);
+    else zero16(du);
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  for (int i = tid; i < kLT * 32; i += 128) {  // z pairs, split into FP16 hi / lo
+    const int row = i >> 5, qp = i & 31;
+    float2 v = make_float2(0.f, 0.f);
+    if (r0 + row < rows && 2 * qp < rank) v = *reinterpret_cast<const float2*>(z + (size_t)(r0 + row) * rank + 2 * qp);
+    const __half2 h = __floats2half2_rn(v.x, v.y);
+    const float2 e = __half22float2(h);
+    const __half2 l = __floats2half2_rn(v.x - e.x, v.y - e.y);
+    zh[row][qp] = *reinterpret_cast<const uint32_t*>(&h);
+    zl[row][qp] = *reinterpret_cast<const uint32_t*>(&l);
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
   __syncthreads();
-  const int o = blockIdx.x * 256 + threadIdx.x;
-  if (o >= d_out) return;
-  float u[64];
+  float acc[16][4];
 #pragma unroll
-  for (int q8 = 0; q8 < 8; ++q8) {
-    if (q8 * 8 < rank) {
-      float f[8];
-      unpack8(__ldg(reinterpret_cast<const uint4*>(U + (size_t)o * rank + q8 * 8)), f);
+  for (int n = 0; n < 16; ++n)
 #pragma unroll
-      for (int k = 0; k < 8; ++k) u[q8 * 8 + k] = f[k];
-    } else {
+    for (int j = 0; j < 4; ++j) acc[n][j] = 0.f;
+  const int ra = 16 * warp + g;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) u[q8 * 8 + k] = 0.f;
+  for (int s = 0; s < 4; ++s) {
+    const uint32_t ah[4] = {zh[ra][8 * s + t], zh[ra + 8][8 * s + t], zh[ra][8 * s + 4 + t], zh[ra + 8][8 * s + 4 + t]};
+    const uint32_t al[4] = {zl[ra][8 * s + t], zl[ra + 8][8 * s + t], zl[ra][8 * s + 4 + t], zl[ra + 8][8 * s + 4 + t]};
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+      const uint16_t* ub = us + (8 * n + g) * kLS + 16 * s + 2 * t;
+      const uint32_t b0 = ld32(ub), b1 = ld32(ub + 8);
+      mma_lr(acc[n], ah, b0, b1);
+      mma_lr(acc[n], al, b0, b1);
     }
   }
-  for (int rr = 0; rr < 16 && r0 + rr < rows; ++rr) {
-    float y = 0.f;
 #pragma unroll
-    for (int q = 0; q < 64; ++q) y = fmaf(u[q], zs[rr][q], y);  // entries past the rank are zero
-    ylr[(size_t)(r0 + rr) * d_out + o] = y;
+  for (int n = 0; n < 16; ++n) {
+    const int o = o0 + 8 * n + 2 * t;
+    if (o >= d_out) continue;  // d_out is a multiple of 64: a tile's n-tiles past it are whole
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = r0 + ra + 8 * h;
+      if (r < rows) *reinterpret_cast<float2*>(ylr + (size_t)r * d_out + o) = make_float2(acc[n][2 * h], acc[n][2 * h + 1]);
+    }
   }
 }
 
 }  // namespace
 
-int lowrank_chunks(int d_in) { return (d_in + kChunk - 1) / kChunk; }
+int lowrank_chunks(int d_in, int rows) {
+  // splits of the input: about two CTAs per SM over the row tiles, at most one per 64 inputs
+  const int tiles = (rows + kLT - 1) / kLT;
+  int n = (2 * device_sm_count() + tiles - 1) / tiles;
+  const int n_kg = d_in / kLK;
+  if (n > n_kg) n = n_kg;
+  return n < 1 ? 1 : n;
+}
+
+size_t lowrank_part_floats(int d_in, int rows, int rank) {
+  return ((size_t)lowrank_chunks(d_in, rows) + 1) * rows * rank;  // the splits' parts, then z
+}
 
 cudaError_t launch_lowrank(const uint16_t* xr, int rows, int d_in, const uint16_t* V, const uint16_t* U, int rank,
                            int d_out, float* part, float* ylr, cudaStream_t st, int xr_mma_order) {
   if (rows <= 0 || rank <= 0) return cudaSuccess;
-  const int n_kc = lowrank_chunks(d_in);
-  const dim3 g1((unsigned)n_kc, (unsigned)(rank / 8), (unsigned)((rows + 7) / 8));
-  lowrank_project_kernel<<<g1, 256, 0, st>>>(xr, rows, d_in, V, rank, part, xr_mma_order);
+  const int n_split = lowrank_chunks(d_in, rows);
+  const dim3 g1((unsigned)((rows + kLT - 1) / kLT), (unsigned)n_split);
+  if (xr_mma_order)
+    lowrank_project_kernel<true><<<g1, 128, 0, st>>>(xr, rows, d_in, V, rank, part, n_split);
+  else
+    lowrank_project_kernel<false><<<g1, 128, 0, st>>>(xr, rows, d_in, V, rank, part, n_split);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const dim3 g2((unsigned)((d_out + 255) / 256), (unsigned)((rows + 15) / 16));
-  lowrank_expand_kernel<<<g2, 256, 0, st>>>(part, n_kc, rows, rank, U, d_out, ylr);
+  float* z = part + (size_t)n_split * rows * rank;
+  const int n = rows * rank;
+  lowrank_reduce_kernel<<<(n + 255) / 256, 256, 0, st>>>(part, n_split, n, z);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const dim3 g3((unsigned)((d_out + 127) / 128), (unsigned)((rows + kLT - 1) / kLT));
+  lowrank_expand_kernel<<<g3, 128, 0, st>>>(z, rows, rank, U, d_out, ylr);
   return cudaGetLastError();
 }
 

@@ -238,8 +238,10 @@ cudaError_t launch_delta_rule(const uint16_t* q, const uint16_t* k, const uint16
                               uint16_t* out, cudaStream_t st);
 // ylr[r][o] = sum_j U[o][j] z[r][j], z[r][j] = sum_i V[j][i] xr[r][i] (FP32) for the low-rank
 // correction (V [rank][d_in], U [d_out][rank] FP16); the projection's sums over
-// lowrank_chunks(d_in) input chunks go through part [chunks][rows][rank].
-int lowrank_chunks(int d_in);
+// lowrank_chunks(d_in, rows) input splits go through part [splits][rows][rank], then z
+// [rows][rank] after them: lowrank_part_floats(d_in, rows, rank) floats in all.
+int lowrank_chunks(int d_in, int rows);
+size_t lowrank_part_floats(int d_in, int rows, int rank);
 // xr_mma_order: the rows of xr are stored in the GEMM's operand order (mma_order_col).
 cudaError_t launch_lowrank(const uint16_t* xr, int rows, int d_in, const uint16_t* V, const uint16_t* U, int rank,
                            int d_out, float* part, float* ylr, cudaStream_t st, int xr_mma_order = 0);

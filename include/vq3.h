@@ -302,9 +302,9 @@ VQ3_API int vq3_mlp_kernel_launches(int rows, const vq3_mlp_layer* layer);
 /*
  * Number of kernels one vq3_linear_forward call launches at `rows` rows: 1
  * below 17 rows (the decode kernel, which also forms the low-rank correction
- * of a layer with factors); from 17 rows on 2 (rotation, GEMM), 4 with
- * low-rank factors (plus their projection and expansion). -1 on a bad
- * descriptor or negative rows.
+ * of a layer with factors); from 17 rows on 2 (rotation, GEMM), 5 with
+ * low-rank factors (plus their projection, its reduction and the expansion).
+ * -1 on a bad descriptor or negative rows.
  */
 VQ3_API int vq3_linear_kernel_launches(int rows, const vq3_linear* L);
 

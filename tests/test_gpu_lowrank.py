@@ -108,4 +108,22 @@ def test_linear_kernel_launches(vq3):
     S.add_lowrank(S.rng(75, 3), m, 16, 0.02)
     lr = vq3.Linear.from_matrix(m, DEV)
     assert [vq3.linear_kernel_launches(r, plain) for r in (0, 1, 16, 17, 300)] == [0, 1, 1, 2, 2]
-    assert [vq3.linear_kernel_launches(r, lr) for r in (0, 1, 16, 17, 300)] == [0, 1, 1, 4, 4]
+    assert [vq3.linear_kernel_launches(r, lr) for r in (0, 1, 16, 17, 300)] == [0, 1, 1, 5, 5]
+
+
+@pytest.mark.parametrize("rows", [64, 2048])
+def test_prefill_lowrank_token_mixer_5120x12288(vq3, rows):
+    # from 17 rows the correction runs as projection (split over the input), reduction and
+    # expansion on the tensor cores, added in the GEMM epilogue; 64 rows: the narrow GEMM (x' in
+    # its operand order), 2048: the wide one
+    m = S.matrix(S.rng(76, 1), 5120, 12288, 1024, "2x16")
+    S.add_lowrank(S.rng(76, 3), m, 64, 0.02)
+    lin = vq3.Linear.from_matrix(m, DEV)
+    x = S.activations(S.rng(76, 0), rows, 5120)
+    got = vq3.linear_forward(f16(x), lin).cpu().numpy()
+    if rows <= 64:
+        assert_parity(got, O.linear_f64(x, m, workers=8), f"5120->12288 rank 64 rows={rows}")
+    else:
+        # sampled rows against the oracle (every 64th row and the last)
+        idx = np.r_[0:rows:64, rows - 1]
+        assert_parity(got[idx], O.linear_f64(x[idx], m, workers=8), f"5120->12288 rank 64 rows={rows} (sampled)")
