@@ -116,12 +116,12 @@ __global__ void __launch_bounds__(256) lowrank_reduce_kernel(const float* __rest
   const int e = blockIdx.x * 256 + threadIdx.x;
   if (e >= n) return;
   float s = 0.f;
-  for (int k0 = 0; k0 < n_split; k0 += 8) {
-    float v[8];
+  for (int k0 = 0; k0 < n_split; k0 += 16) {  // sixteen splits' loads in flight, added in order
+    float v[16];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) v[k] = k0 + k < n_split ? __ldg(part + (size_t)(k0 + k) * n + e) : 0.f;
+    for (int k = 0; k < 16; ++k) v[k] = k0 + k < n_split ? __ldg(part + (size_t)(k0 + k) * n + e) : 0.f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) s += v[k];
+    for (int k = 0; k < 16; ++k) s += v[k];
   }
   z[e] = s;
 }
@@ -142,15 +142,25 @@ __global__ void __launch_bounds__(128) lowrank_expand_kernel(const float* __rest
     else zero16(du);
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
-  for (int i = tid; i < kLT * 32; i += 128) {  // z pairs, split into FP16 hi / lo
-    const int row = i >> 5, qp = i & 31;
-    float2 v = make_float2(0.f, 0.f);
-    if (r0 + row < rows && 2 * qp < rank) v = *reinterpret_cast<const float2*>(z + (size_t)(r0 + row) * rank + 2 * qp);
-    const __half2 h = __floats2half2_rn(v.x, v.y);
-    const float2 e = __half22float2(h);
-    const __half2 l = __floats2half2_rn(v.x - e.x, v.y - e.y);
-    zh[row][qp] = *reinterpret_cast<const uint32_t*>(&h);
-    zl[row][qp] = *reinterpret_cast<const uint32_t*>(&l);
+  {
+    // z pairs, split into FP16 hi / lo: the thread's 16 pairs are loaded first, then converted
+    constexpr int kPer = kLT * 32 / 128;
+    float2 v[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = tid + 128 * k, row = i >> 5, qp = i & 31;
+      v[k] = (r0 + row < rows && 2 * qp < rank) ? *reinterpret_cast<const float2*>(z + (size_t)(r0 + row) * rank + 2 * qp)
+                                                : make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = tid + 128 * k, row = i >> 5, qp = i & 31;
+      const __half2 h = __floats2half2_rn(v[k].x, v[k].y);
+      const float2 e = __half22float2(h);
+      const __half2 l = __floats2half2_rn(v[k].x - e.x, v[k].y - e.y);
+      zh[row][qp] = *reinterpret_cast<const uint32_t*>(&h);
+      zl[row][qp] = *reinterpret_cast<const uint32_t*>(&l);
+    }
   }
   asm volatile("cp.async.wait_group 0;" ::: "memory");
   __syncthreads();
@@ -188,10 +198,12 @@ __global__ void __launch_bounds__(128) lowrank_expand_kernel(const float* __rest
 
 int lowrank_chunks(int d_in, int rows) {
   // splits of the input: about two CTAs per SM over the row tiles, at most one per 64 inputs
+  // and at most 32 (the reduction adds them 16 at a time)
   const int tiles = (rows + kLT - 1) / kLT;
   int n = (2 * device_sm_count() + tiles - 1) / tiles;
   const int n_kg = d_in / kLK;
   if (n > n_kg) n = n_kg;
+  if (n > 32) n = 32;
   return n < 1 ? 1 : n;
 }
 
