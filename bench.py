@@ -35,7 +35,7 @@ REF_BUDGET_S = 100.0
 # DRAM bytes (read + write) of one persistent_kernel launch at T=8, from one ncu capture of
 # the kernel (dram__bytes_read.sum + dram__bytes_write.sum); None when the kernel has changed
 # since that capture.
-TRAFFIC_PER_LAUNCH = 104_197_376
+TRAFFIC_PER_LAUNCH = 104_139_008
 
 
 def peaks() -> dict:
@@ -704,11 +704,37 @@ def stack64(vq3, dev, stream, pk) -> dict:
 
 
 def run_profile_case(args) -> None:
-    """A small case for profiler captures: one weight set (~100 MB on the device) and
-    --steps blocks at --rows rows through vq3_mlp_forward, untimed."""
+    """A small case for profiler captures, untimed: --steps calls at --rows rows on one weight
+    set of the MLP block (~100 MB on the device), or with --case of the 5120 -> 12288
+    projection with rank-64 factors (two-bit format), or of the delta-rule block (16 heads,
+    128 x 128, --rows tokens)."""
     import torch
     from bit_vector_lut_gb300 import vq3
     dev = torch.device("cuda:0")
+    if args.case == "lowrank":
+        m = S.matrix(S.rng(80, 1), 5120, 12288, 1024, "2x16")
+        S.add_lowrank(S.rng(80, 3), m, 64, 0.02)
+        lin = vq3.Linear.from_matrix(m, dev)
+        x = torch.from_numpy(S.activations(S.rng(80, 0), args.rows, 5120)).to(dev)
+        out = torch.empty((args.rows, 12288), dtype=torch.float16, device=dev)
+        ws = vq3.workspace(vq3.linear_workspace_bytes(args.rows, lin), dev)
+        for _ in range(args.steps):
+            vq3.linear_forward(x, lin, out=out, ws=ws)
+        torch.cuda.synchronize(dev)
+        print(json.dumps({"profile_case": f"linear_5120x12288_2x16_rank64_T{args.rows}", "calls": args.steps,
+                          "launches_per_call": vq3.linear_kernel_launches(args.rows, lin),
+                          "status": vq3.workspace_status(ws)}), flush=True)
+        return
+    if args.case == "delta":
+        w = S.delta_rule_inputs(seed=12, tokens=args.rows, heads=16, d_k=128, d_v=128)
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+        q, k, v, be, al, state = t(w.q), t(w.k), t(w.v), t(w.beta), t(w.alpha), t(w.state)
+        out = torch.empty((args.rows, 16, 128), dtype=torch.float16, device=dev)
+        for _ in range(args.steps):
+            vq3.delta_rule_forward(q, k, v, be, al, state, out=out)
+        torch.cuda.synchronize(dev)
+        print(json.dumps({"profile_case": f"delta_rule_16x128x128_T{args.rows}", "calls": args.steps}), flush=True)
+        return
     wl = S.mlp_27b(seed=1, rows=args.rows)
     layer = vq3.MLP.from_block(wl.layers[0], dev)
     x = torch.from_numpy(wl.x).to(dev)
@@ -763,6 +789,9 @@ def main():
     ap.add_argument("--oracle-config-rates", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--profile-case", action="store_true",
                     help="run --steps untimed blocks at --rows on one weight set (a small case for ncu) and exit")
+    ap.add_argument("--case", choices=["mlp", "lowrank", "delta"], default="mlp",
+                    help="with --profile-case: the MLP block, the 5120 -> 12288 projection with rank-64 factors, "
+                         "or the delta-rule block")
     args = ap.parse_args()
     if args.profile_case:
         run_profile_case(args)
