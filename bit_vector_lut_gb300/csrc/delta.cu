@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(32) delta_rule_tc_kernel(const uint16_t* __res
   constexpr int RS = DK + 8;        // staged row stride in halves: 4 words past a multiple of 32
   __shared__ __align__(16) uint16_t Ks[kTcChunk * RS];
   __shared__ __align__(16) uint16_t Qs[kTcChunk * RS];
-  __shared__ float Vs[kTcChunk][16];
+  __shared__ __align__(16) uint16_t Vh[kTcChunk][16];  // V of the chunk's tokens, this CTA's 16 columns
   __shared__ float Pm[kTcChunk / 8][8][8], Mm[kTcChunk / 8][8][8];
   __shared__ float Gm[kTcChunk / 8][8], Wm[kTcChunk / 8][8];
   __shared__ float Al[kTcChunk], Be[kTcChunk];  // alpha, beta of the chunk's tokens (1, 0 past the last)
@@ -249,10 +249,16 @@ __global__ void __launch_bounds__(32) delta_rule_tc_kernel(const uint16_t* __res
       Al[i] = i < nt ? alpha[(size_t)(base + i) * heads + h] : 1.f;
       Be[i] = i < nt ? beta[(size_t)(base + i) * heads + h] : 0.f;
     }
-    for (int i = lane; i < nb * 8 * 16; i += 32) {
-      const int tk = i >> 4, c = i & 15;
-      Vs[tk][c] = tk < nt ? __half2float(__ushort_as_half(v[((size_t)(base + tk) * heads + h) * d_v + c0 + c])) : 0.f;
+    for (int i = lane; i < nb * 8 * 2; i += 32) {  // two 16-byte halves of each token's 16 columns
+      const int tk = i >> 1, c = (i & 1) * 8;
+      const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(&Vh[tk][c]));
+      if (tk < nt)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
+                     "l"(v + ((size_t)(base + tk) * heads + h) * d_v + c0 + c) : "memory");
+      else
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0u) : "memory");
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncwarp();
 
@@ -341,8 +347,8 @@ __global__ void __launch_bounds__(32) delta_rule_tc_kernel(const uint16_t* __res
       // xk = (K S)^T at [g][2t], [g][2t+1], [g+8][2t], [g+8][2t+1]; likewise xq = (Q S)^T
       const float* gm = Gm[b];
       const int j0 = 2 * t, j1 = 2 * t + 1;
-      const float r0 = Vs[tb + j0][g] - gm[j0] * xk[0], r1 = Vs[tb + j1][g] - gm[j1] * xk[1];
-      const float r2 = Vs[tb + j0][g + 8] - gm[j0] * xk[2], r3 = Vs[tb + j1][g + 8] - gm[j1] * xk[3];
+      const float r0 = h2f(Vh[tb + j0][g]) - gm[j0] * xk[0], r1 = h2f(Vh[tb + j1][g]) - gm[j1] * xk[1];
+      const float r2 = h2f(Vh[tb + j0][g + 8]) - gm[j0] * xk[2], r3 = h2f(Vh[tb + j1][g + 8]) - gm[j1] * xk[3];
       // U^T[c][i] = sum_j P[i][j] R^T[c][j]: this lane's two j, then the four lanes of row g
       float ulo[8], uhi[8];
 #pragma unroll
@@ -437,7 +443,7 @@ cudaError_t launch_delta_rule(const uint16_t* q, const uint16_t* k, const uint16
                               const float* alpha, int tokens, int heads, int d_k, int d_v, float* state,
                               uint16_t* out, cudaStream_t st) {
   const dim3 grid((unsigned)heads, (unsigned)(d_v / kCols));
-  const bool al = (reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k)) % 16 == 0;
+  const bool al = (reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) % 16 == 0;
   if (d_k % 16 == 0 && d_k <= 128 && al) {  // the tensor-core path (16-byte staging of q and k)
     switch (d_k / 16) {
       case 1: delta_rule_tc_kernel<1><<<grid, 32, 0, st>>>(q, k, v, beta, alpha, tokens, heads, d_v, state, out); break;

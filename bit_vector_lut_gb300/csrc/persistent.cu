@@ -1293,8 +1293,8 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
   j1.scale = a.scale_in;
   j1.chunk = a.x_chunk;
   j1.signs = a.signs_in;
-  j1.inv = a.norm ? s_inv : nullptr;
-  j1.res_delta = (a.norm && a.res_delta) ? a.res_delta + (size_t)a.row0 * a.d_model : nullptr;
+  j1.inv = (!LR && a.norm) ? s_inv : nullptr;
+  j1.res_delta = (!LR && a.norm && a.res_delta) ? a.res_delta + (size_t)a.row0 * a.d_model : nullptr;
   j1.ready = nullptr;
   j1.ready_target = 0;
   j1.group_done = ctl + (a.mlp ? a.off_g : a.off_o);
@@ -1313,7 +1313,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.lr_u + (size_t)(t / NT) * kSuChannels * a.lr_rank),
                      "r"((uint32_t)(kSuChannels * a.lr_rank * 2)) : "memory");
   }
-  if (a.mlp && threadIdx.x == 0) {
+  if (!LR && a.mlp && threadIdx.x == 0) {  // (the low-rank instantiation serves linear layers only)
     // the down step's cell range, worked out now, away from the hand-off before that step
     const int n_seg3 = a.d_model / kSuChannels;
     const int cells3 = (n_seg3 + kWarps - 1) / kWarps * (a.d_inter / kSuInputs);
@@ -1326,7 +1326,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
   // one cell's index copies, then the rotation of x (its loads not queued behind
   // the bulk of the prologue), then the rest of the prologue
   Cursor cur = decode_begin<F>(j1, sv, 1);
-  if (a.norm && a.ss_in) {
+  if (!LR && a.norm && a.ss_in) {
     // the rows' sums of squares from the previous layer's partials (16 columns each): one
     // warp per row, lanes over the partials in a fixed order, then the warp's xor tree
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, n_part = a.d_model / 16;
@@ -1339,7 +1339,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
       if (lane == 0) s_inv[rr] = 1.0f / sqrtf(ss / (float)a.d_model + a.eps);
     }
     __syncthreads();
-  } else if (a.norm) {
+  } else if (!LR && a.norm) {
     // pre-norm residual step for the pass's rows: r' = fp16(x + delta) over the whole row
     // (every CTA, for its own 1/rms), the 64-column slices s with s % grid == CTA written to
     // res_out. Each row is split into `parts` column ranges, one warp each (parts = warps per
@@ -1404,7 +1404,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
   }
   decode_run<F, NT, uint16_t, LR>(j1, a.x + (size_t)a.row0 * a.d_model, cur, sv, &tables, status);
 
-  if (a.mlp) {
+  if (!LR && a.mlp) {
     DecodeJob j3;
     j3.d_in = a.d_inter;
     j3.d_out = a.d_model;

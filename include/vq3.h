@@ -244,7 +244,7 @@ VQ3_API int vq3_mlp_forward(const uint16_t* x, int rows, const vq3_mlp_layer* la
  * beta, alpha: device FP32 [tokens][heads];  state: device FP32 [heads][d_k][d_v],
  *   read as the state before the first token and overwritten with the state after
  *   the last (FP32 accumulation, out rounded to FP16 once). With d_k a multiple of 16
- *   up to 128 and q, k 16-byte aligned the products run on the tensor cores, the FP32
+ *   up to 128 and q, k, v 16-byte aligned the products run on the tensor cores, the FP32
  *   state and weighted values entering them as two FP16 parts (hi and the remainder,
  *   about 22 bits); otherwise FP32 on CUDA cores.
  * d_k a multiple of 8 in [8, 256]; d_v a multiple of 16. Deterministic.
