@@ -165,19 +165,23 @@ __global__ void __launch_bounds__(kDThreads) delta_rule_kernel(const uint16_t* _
 
 // ---------------------------------------------------------------- tensor-core path (d_k = 16 KS <= 128)
 //
-// One warp per (head, 16 columns of d_v). The state slice is held transposed, S^T [16 columns]
-// [d_k], as the accumulators of m16n8k16 tiles (n-tile n: d_k 8n .. 8n+7): that is also the
-// A-operand layout of the next product S^T [K; Q]^T, so the state never leaves the registers
-// between blocks. The FP32 operands that enter the tensor cores (the state, the weighted U)
-// are split into two FP16 parts, hi = fp16(x) and lo = fp16(x - hi), and multiplied as two
-// MMAs into FP32 accumulators (about 22 bits of each operand; K and Q are FP16 inputs).
-// Per chunk of up to 64 tokens: K, Q, V staged in shared memory; for every 8-token block the
-// state-independent parts first (K K^T and Q K^T as one 16 x 8 tile, then N, the closed-form
-// P = (I - N)(I + N^2)(I + N^4), M and the weights), then the blocks in order:
-//     [X_K | X_Q] = S^T [K; Q]^T,  R^T = V^T - X_K Gamma,  U^T = R^T P^T,
-//     O^T = X_Q Gamma + U^T M^T,   S^T = gamma_8 S^T + (U diag(w))^T K,  w_j = beta_j gamma_8 / gamma_j.
+// One CTA of KS warps per (head, 16 columns of d_v). The state slice is held transposed,
+// S^T [16 columns][d_k], as the accumulators of m16n8k16 tiles (n-tile n: d_k 8n .. 8n+7),
+// warp w holding n-tiles 2w and 2w+1 (d_k 16w .. 16w+15): that is also the A-operand layout of
+// k-step w of the next product S^T [K; Q]^T, so the state never leaves the registers between
+// blocks. The FP32 operands that enter the tensor cores (the state, the weighted U) are split
+// into two FP16 parts, hi = fp16(x) and lo = fp16(x - hi), and multiplied as two MMAs into FP32
+// accumulators (about 22 bits of each operand; K and Q are FP16 inputs).
+// Per chunk of up to 64 tokens: K, Q, V, alpha, beta staged in shared memory; the state-
+// independent parts of the 8-token blocks first, warp w taking blocks w, w + KS, ... (K K^T and
+// Q K^T as one 16 x 8 tile, then N, the closed-form P = (I - N)(I + N^2)(I + N^4), M and the
+// weights); then the blocks in order:
+//     [X_K | X_Q] = S^T [K; Q]^T   (each warp its k-step; the partials added in warp order)
+//     R^T = V^T - X_K Gamma,  U^T = R^T P^T,  O^T = X_Q Gamma + U^T M^T   (every warp, redundantly)
+//     S^T = gamma_8 S^T + (U diag(w))^T K,  w_j = beta_j gamma_8 / gamma_j   (each warp its tiles)
 
 constexpr int kTcChunk = 64;  // tokens staged at a time (8 blocks)
+constexpr int kTcBlocks = kTcChunk / 8;
 
 __device__ __forceinline__ void mma_tc(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
@@ -194,32 +198,70 @@ __device__ __forceinline__ void split2(float x, float y, uint32_t& hi, uint32_t&
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
+// Dynamic shared memory of the kernel (bytes from the base; every part 16-byte aligned).
 template <int KS>
-__global__ void __launch_bounds__(32) delta_rule_tc_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
-                                                           const uint16_t* __restrict__ v,
-                                                           const float* __restrict__ beta,
-                                                           const float* __restrict__ alpha, int tokens, int heads,
-                                                           int d_v, float* __restrict__ state,
-                                                           uint16_t* __restrict__ out) {
-  constexpr int DK = 16 * KS;
-  constexpr int NTD = DK / 8;       // state n-tiles
-  constexpr int RS = DK + 8;        // staged row stride in halves: 4 words past a multiple of 32
-  __shared__ __align__(16) uint16_t Ks[kTcChunk * RS];
-  __shared__ __align__(16) uint16_t Qs[kTcChunk * RS];
-  __shared__ __align__(16) uint16_t Vh[kTcChunk][16];  // V of the chunk's tokens, this CTA's 16 columns
-  __shared__ float Pm[kTcChunk / 8][8][8], Mm[kTcChunk / 8][8][8];
-  __shared__ float Gm[kTcChunk / 8][8], Wm[kTcChunk / 8][8];
-  __shared__ float Al[kTcChunk], Be[kTcChunk];  // alpha, beta of the chunk's tokens (1, 0 past the last)
-  __shared__ float Nn[8][8], N2[8][8], N4[8][8], Am[8][8], KK[8][8], QK[8][8];
-  const int lane = threadIdx.x, g = lane >> 2, t = lane & 3;
+struct TcSmem {
+  static constexpr int DK = 16 * KS;
+  static constexpr int RS = DK + 8;  // staged row stride in halves: 4 words past a multiple of 32
+  static constexpr uint32_t kK = 0;
+  static constexpr uint32_t kQ = kK + kTcChunk * RS * 2;
+  static constexpr uint32_t kV = kQ + kTcChunk * RS * 2;       // FP16 [64][16]
+  static constexpr uint32_t kAl = kV + kTcChunk * 16 * 2;      // alpha [64], beta [64]
+  static constexpr uint32_t kP = kAl + 2 * kTcChunk * 4;       // P, M [blocks][8][8]
+  static constexpr uint32_t kG = kP + 2 * kTcBlocks * 64 * 4;  // gamma, w [blocks][8]
+  // phase-1 scratch [KS][6][8][8] and, later in the chunk, the X partials [2][KS][8][32]
+  static constexpr uint32_t kU = kG + 2 * kTcBlocks * 8 * 4;
+  static constexpr uint32_t kUBytes = (uint32_t)KS * 2048u;
+  static constexpr uint32_t kTotal = kU + kUBytes;
+};
+
+// z = (dx I + x)(dy I + y) for 8 x 8 matrices in a warp's shared scratch, two entries per lane.
+__device__ __forceinline__ void mul8(float (*x)[8], float (*y)[8], float (*z)[8], float dx, float dy, int lane) {
+  float r2[2];
+#pragma unroll
+  for (int e2 = 0; e2 < 2; ++e2) {
+    const int e = lane + 32 * e2, ti = e >> 3, j = e & 7;
+    float s = 0.f;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) s = fmaf((ti == m ? dx : 0.f) + x[ti][m], (m == j ? dy : 0.f) + y[m][j], s);
+    r2[e2] = s;
+  }
+  __syncwarp();
+  z[lane >> 3][lane & 7] = r2[0];
+  z[(lane + 32) >> 3][lane & 7] = r2[1];
+  __syncwarp();
+}
+
+template <int KS>
+__global__ void __launch_bounds__(32 * KS, 1) delta_rule_tc_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+                                                                const uint16_t* __restrict__ v,
+                                                                const float* __restrict__ beta,
+                                                                const float* __restrict__ alpha, int tokens, int heads,
+                                                                int d_v, float* __restrict__ state,
+                                                                uint16_t* __restrict__ out) {
+  using L = TcSmem<KS>;
+  constexpr int DK = L::DK, RS = L::RS, NT = 32 * KS;
+  extern __shared__ __align__(16) unsigned char dsm[];
+  uint16_t* Ks = reinterpret_cast<uint16_t*>(dsm + L::kK);
+  uint16_t* Qs = reinterpret_cast<uint16_t*>(dsm + L::kQ);
+  uint16_t (*Vh)[16] = reinterpret_cast<uint16_t (*)[16]>(dsm + L::kV);
+  float* Al = reinterpret_cast<float*>(dsm + L::kAl);
+  float* Be = Al + kTcChunk;
+  float (*Pm)[8][8] = reinterpret_cast<float (*)[8][8]>(dsm + L::kP);
+  float (*Mm)[8][8] = Pm + kTcBlocks;
+  float (*Gm)[8] = reinterpret_cast<float (*)[8]>(dsm + L::kG);
+  float (*Wm)[8] = Gm + kTcBlocks;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  float (*Sc)[8][8] = reinterpret_cast<float (*)[8][8]>(dsm + L::kU + (uint32_t)warp * 1536u);  // 6 of them
+  float* Xp = reinterpret_cast<float*>(dsm + L::kU);  // [2][KS][8][32]
   const int h = blockIdx.x, c0 = blockIdx.y * 16;
   float* Sg = state + (size_t)h * DK * d_v + c0;
 
-  // the state slice into the accumulator layout: acc[n] = S^T[g, g+8][8n + 2t, +1]
-  float acc[NTD][4];
+  // this warp's tiles of the state slice: acc[n] = S^T[g, g+8][16 warp + 8n + 2t, +1]
+  float acc[2][4];
 #pragma unroll
-  for (int n = 0; n < NTD; ++n) {
-    const int d = 8 * n + 2 * t;
+  for (int n = 0; n < 2; ++n) {
+    const int d = 16 * warp + 8 * n + 2 * t;
     acc[n][0] = Sg[(size_t)d * d_v + g];
     acc[n][1] = Sg[(size_t)(d + 1) * d_v + g];
     acc[n][2] = Sg[(size_t)d * d_v + g + 8];
@@ -229,10 +271,10 @@ __global__ void __launch_bounds__(32) delta_rule_tc_kernel(const uint16_t* __res
   for (int base = 0; base < tokens; base += kTcChunk) {
     const int nt = tokens - base < kTcChunk ? tokens - base : kTcChunk;
     const int nb = (nt + 7) / 8;
-    // ---- stage K, Q (16-byte copies), V; tokens past the last are zero (beta 0, alpha 1 below)
+    // ---- stage K, Q, V (16-byte copies), alpha, beta; tokens past the last are zero (beta 0, alpha 1)
     const uint32_t ks = static_cast<uint32_t>(__cvta_generic_to_shared(Ks));
     const uint32_t qs = static_cast<uint32_t>(__cvta_generic_to_shared(Qs));
-    for (int i = lane; i < nb * 8 * (DK / 8); i += 32) {
+    for (int i = tid; i < nb * 8 * (DK / 8); i += NT) {
       const int tk = i / (DK / 8), c = i % (DK / 8);
       const uint32_t off = (uint32_t)(tk * RS + c * 8) * 2u;
       if (tk < nt) {
@@ -244,12 +286,7 @@ __global__ void __launch_bounds__(32) delta_rule_tc_kernel(const uint16_t* __res
         asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(qs + off), "r"(0u) : "memory");
       }
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    for (int i = lane; i < nb * 8; i += 32) {
-      Al[i] = i < nt ? alpha[(size_t)(base + i) * heads + h] : 1.f;
-      Be[i] = i < nt ? beta[(size_t)(base + i) * heads + h] : 0.f;
-    }
-    for (int i = lane; i < nb * 8 * 2; i += 32) {  // two 16-byte halves of each token's 16 columns
+    for (int i = tid; i < nb * 8 * 2; i += NT) {  // two 16-byte halves of each token's 16 columns
       const int tk = i >> 1, c = (i & 1) * 8;
       const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(&Vh[tk][c]));
       if (tk < nt)
@@ -259,12 +296,17 @@ __global__ void __launch_bounds__(32) delta_rule_tc_kernel(const uint16_t* __res
         asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0u) : "memory");
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
+    for (int i = tid; i < nb * 8; i += NT) {
+      Al[i] = i < nt ? alpha[(size_t)(base + i) * heads + h] : 1.f;
+      Be[i] = i < nt ? beta[(size_t)(base + i) * heads + h] : 0.f;
+    }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
-    __syncwarp();
+    __syncthreads();  // every thread's copies and stores are visible
 
-    // ---- the state-independent parts of every block
-    for (int b = 0; b < nb; ++b) {
+    // ---- the state-independent parts of every block: warp w takes blocks w, w + KS, ...
+    for (int b = warp; b < nb; b += KS) {
       const int tb = 8 * b;
+      float (*Nn)[8] = Sc[0], (*N2)[8] = Sc[1], (*N4)[8] = Sc[2], (*Am)[8] = Sc[3], (*KK)[8] = Sc[4], (*QK)[8] = Sc[5];
       float gk[4] = {0.f, 0.f, 0.f, 0.f};  // rows g: k_g . k_{2t}, k_g . k_{2t+1}; rows g+8: q_g . k_..
 #pragma unroll
       for (int s = 0; s < KS; ++s) {
@@ -296,55 +338,57 @@ __global__ void __launch_bounds__(32) delta_rule_tc_kernel(const uint16_t* __res
         Mm[b][ti][j] = j <= ti ? f * QK[ti][j] : 0.f;
       }
       __syncwarp();
-      auto mul8 = [&](float (*x)[8], float (*y)[8], float (*z)[8], float dx, float dy) {
-        // z = (dx I + x)(dy I + y), two entries per lane
-        float r2[2];
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const int e = lane + 32 * e2, ti = e >> 3, j = e & 7;
-          float s = 0.f;
-#pragma unroll
-          for (int m = 0; m < 8; ++m) s = fmaf((ti == m ? dx : 0.f) + x[ti][m], (m == j ? dy : 0.f) + y[m][j], s);
-          r2[e2] = s;
-        }
-        __syncwarp();
-        z[lane >> 3][lane & 7] = r2[0];
-        z[(lane + 32) >> 3][lane & 7] = r2[1];
-        __syncwarp();
-      };
-      mul8(Nn, Nn, N2, 0.f, 0.f);   // N^2
-      mul8(N2, N2, N4, 0.f, 0.f);   // N^4
-      // (I - N)(I + N^2): negate N in place first
-      Nn[lane >> 3][lane & 7] = -Nn[lane >> 3][lane & 7];
+      mul8(Nn, Nn, N2, 0.f, 0.f, lane);  // N^2
+      mul8(N2, N2, N4, 0.f, 0.f, lane);  // N^4
+      Nn[lane >> 3][lane & 7] = -Nn[lane >> 3][lane & 7];  // then (I - N)(I + N^2)
       Nn[(lane + 32) >> 3][lane & 7] = -Nn[(lane + 32) >> 3][lane & 7];
       __syncwarp();
-      mul8(Nn, N2, Am, 1.f, 1.f);
-      mul8(Am, N4, Pm[b], 0.f, 1.f);  // P = A (I + N^4)
+      mul8(Nn, N2, Am, 1.f, 1.f, lane);
+      mul8(Am, N4, Pm[b], 0.f, 1.f, lane);  // P = A (I + N^4)
       if (lane < 8) Wm[b][lane] = Wm[b][lane] * Gm[b][7] / Gm[b][lane];  // w_j = beta_j gamma_8 / gamma_j
       __syncwarp();
     }
+    __syncthreads();  // every block's P, M, gamma and w are visible; the scratch is free for X
 
     // ---- the blocks in order
     for (int b = 0; b < nb; ++b) {
       const int tb = 8 * b;
-      float xk[4] = {0.f, 0.f, 0.f, 0.f}, xq[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int s = 0; s < KS; ++s) {
+      // this warp's k-step of [X_K | X_Q] = S^T [K; Q]^T (d_k 16 warp .. + 15)
+      {
         uint32_t ah[4], al[4];
-        split2(acc[2 * s][0], acc[2 * s][1], ah[0], al[0]);
-        split2(acc[2 * s][2], acc[2 * s][3], ah[1], al[1]);
-        split2(acc[2 * s + 1][0], acc[2 * s + 1][1], ah[2], al[2]);
-        split2(acc[2 * s + 1][2], acc[2 * s + 1][3], ah[3], al[3]);
-        const uint16_t* kr = Ks + (tb + g) * RS + 16 * s + 2 * t;
-        const uint16_t* qr = Qs + (tb + g) * RS + 16 * s + 2 * t;
+        split2(acc[0][0], acc[0][1], ah[0], al[0]);
+        split2(acc[0][2], acc[0][3], ah[1], al[1]);
+        split2(acc[1][0], acc[1][1], ah[2], al[2]);
+        split2(acc[1][2], acc[1][3], ah[3], al[3]);
+        const uint16_t* kr = Ks + (tb + g) * RS + 16 * warp + 2 * t;
+        const uint16_t* qr = Qs + (tb + g) * RS + 16 * warp + 2 * t;
         const uint32_t k0 = *reinterpret_cast<const uint32_t*>(kr), k1 = *reinterpret_cast<const uint32_t*>(kr + 8);
         const uint32_t q0 = *reinterpret_cast<const uint32_t*>(qr), q1 = *reinterpret_cast<const uint32_t*>(qr + 8);
+        float xk[4] = {0.f, 0.f, 0.f, 0.f}, xq[4] = {0.f, 0.f, 0.f, 0.f};
         mma_tc(xk, ah, k0, k1);
         mma_tc(xq, ah, q0, q1);
         mma_tc(xk, al, k0, k1);
         mma_tc(xq, al, q0, q1);
+        float* xp = Xp + (((b & 1) * KS + warp) * 8) * 32 + lane;  // double-buffered by block parity
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          xp[j * 32] = xk[j];
+          xp[(j + 4) * 32] = xq[j];
+        }
       }
-      // xk = (K S)^T at [g][2t], [g][2t+1], [g+8][2t], [g+8][2t+1]; likewise xq = (Q S)^T
+      __syncthreads();  // every warp's partial is in shared memory
+      // the partials added in warp (= k-step) order: (K S)^T and (Q S)^T at [g][2t], [g][2t+1],
+      // [g+8][2t], [g+8][2t+1] (every warp forms the same sums)
+      float xk[4] = {0.f, 0.f, 0.f, 0.f}, xq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int w2 = 0; w2 < KS; ++w2) {
+        const float* xp = Xp + (((b & 1) * KS + w2) * 8) * 32 + lane;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          xk[j] += xp[j * 32];
+          xq[j] += xp[(j + 4) * 32];
+        }
+      }
       const float* gm = Gm[b];
       const int j0 = 2 * t, j1 = 2 * t + 1;
       const float r0 = h2f(Vh[tb + j0][g]) - gm[j0] * xk[0], r1 = h2f(Vh[tb + j1][g]) - gm[j1] * xk[1];
@@ -372,21 +416,21 @@ __global__ void __launch_bounds__(32) delta_rule_tc_kernel(const uint16_t* __res
         u2 = i == j0 ? uhi[i] : u2;
         u3 = i == j1 ? uhi[i] : u3;
       }
-      // O^T[c][i] = gamma_i X_Q[c][i] + sum_{j <= i} M[i][j] U^T[c][j] (the full sum over j: M is zero above)
-      float olo[8], ohi[8];
+      if (warp == 0) {
+        // O^T[c][i] = gamma_i X_Q[c][i] + sum_{j <= i} M[i][j] U^T[c][j] (the full sum over j: M is zero above)
+        float olo[8], ohi[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        olo[i] = fmaf(Mm[b][i][j1], u1, Mm[b][i][j0] * u0);
-        ohi[i] = fmaf(Mm[b][i][j1], u3, Mm[b][i][j0] * u2);
-      }
+        for (int i = 0; i < 8; ++i) {
+          olo[i] = fmaf(Mm[b][i][j1], u1, Mm[b][i][j0] * u0);
+          ohi[i] = fmaf(Mm[b][i][j1], u3, Mm[b][i][j0] * u2);
+        }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        olo[i] += __shfl_xor_sync(0xffffffffu, olo[i], 1);
-        ohi[i] += __shfl_xor_sync(0xffffffffu, ohi[i], 1);
-        olo[i] += __shfl_xor_sync(0xffffffffu, olo[i], 2);
-        ohi[i] += __shfl_xor_sync(0xffffffffu, ohi[i], 2);
-      }
-      {
+        for (int i = 0; i < 8; ++i) {
+          olo[i] += __shfl_xor_sync(0xffffffffu, olo[i], 1);
+          ohi[i] += __shfl_xor_sync(0xffffffffu, ohi[i], 1);
+          olo[i] += __shfl_xor_sync(0xffffffffu, olo[i], 2);
+          ohi[i] += __shfl_xor_sync(0xffffffffu, ohi[i], 2);
+        }
         float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -409,15 +453,17 @@ __global__ void __launch_bounds__(32) delta_rule_tc_kernel(const uint16_t* __res
           o[g + 8] = __half_as_ushort(__float2half_rn(o3));
         }
       }
-      // S^T <- gamma_8 S^T + W^T K with W^T[c][j] = U^T[c][j] w_j (tokens 8..15 of the k-step are zero)
+      // this warp's state tiles: S^T <- gamma_8 S^T + W^T K with W^T[c][j] = U^T[c][j] w_j (tokens
+      // 8 .. 15 of the k-step are zero)
       uint32_t wh[4], wl[4];
       split2(u0 * Wm[b][j0], u1 * Wm[b][j1], wh[0], wl[0]);
       split2(u2 * Wm[b][j0], u3 * Wm[b][j1], wh[1], wl[1]);
       wh[2] = wh[3] = wl[2] = wl[3] = 0u;
       const float g8 = gm[7];
 #pragma unroll
-      for (int n = 0; n < NTD; ++n) {
-        const uint16_t kv0 = Ks[(tb + j0) * RS + 8 * n + g], kv1 = Ks[(tb + j1) * RS + 8 * n + g];
+      for (int n = 0; n < 2; ++n) {
+        const int d = 16 * warp + 8 * n + g;
+        const uint16_t kv0 = Ks[(tb + j0) * RS + d], kv1 = Ks[(tb + j1) * RS + d];
         const uint32_t bk = (uint32_t)kv0 | ((uint32_t)kv1 << 16);
 #pragma unroll
         for (int r = 0; r < 4; ++r) acc[n][r] *= g8;
@@ -425,16 +471,35 @@ __global__ void __launch_bounds__(32) delta_rule_tc_kernel(const uint16_t* __res
         mma_tc(acc[n], wl, bk, 0u);
       }
     }
-    __syncwarp();  // the staged chunk is read no more
+    __syncthreads();  // the staged chunk and the partials are read no more
   }
 #pragma unroll
-  for (int n = 0; n < NTD; ++n) {
-    const int d = 8 * n + 2 * t;
+  for (int n = 0; n < 2; ++n) {
+    const int d = 16 * warp + 8 * n + 2 * t;
     Sg[(size_t)d * d_v + g] = acc[n][0];
     Sg[(size_t)(d + 1) * d_v + g] = acc[n][1];
     Sg[(size_t)d * d_v + g + 8] = acc[n][2];
     Sg[(size_t)(d + 1) * d_v + g + 8] = acc[n][3];
   }
+}
+
+template <int KS>
+cudaError_t launch_delta_tc(dim3 grid, const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* beta,
+                            const float* alpha, int tokens, int heads, int d_v, float* state, uint16_t* out,
+                            cudaStream_t st) {
+  constexpr int smem = (int)TcSmem<KS>::kTotal;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(delta_rule_tc_kernel<KS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  delta_rule_tc_kernel<KS><<<grid, 32 * KS, smem, st>>>(q, k, v, beta, alpha, tokens, heads, d_v, state, out);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -444,18 +509,17 @@ cudaError_t launch_delta_rule(const uint16_t* q, const uint16_t* k, const uint16
                               uint16_t* out, cudaStream_t st) {
   const dim3 grid((unsigned)heads, (unsigned)(d_v / kCols));
   const bool al = (reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) % 16 == 0;
-  if (d_k % 16 == 0 && d_k <= 128 && al) {  // the tensor-core path (16-byte staging of q and k)
+  if (d_k % 16 == 0 && d_k <= 128 && al) {  // the tensor-core path (16-byte staging of q, k and v)
     switch (d_k / 16) {
-      case 1: delta_rule_tc_kernel<1><<<grid, 32, 0, st>>>(q, k, v, beta, alpha, tokens, heads, d_v, state, out); break;
-      case 2: delta_rule_tc_kernel<2><<<grid, 32, 0, st>>>(q, k, v, beta, alpha, tokens, heads, d_v, state, out); break;
-      case 3: delta_rule_tc_kernel<3><<<grid, 32, 0, st>>>(q, k, v, beta, alpha, tokens, heads, d_v, state, out); break;
-      case 4: delta_rule_tc_kernel<4><<<grid, 32, 0, st>>>(q, k, v, beta, alpha, tokens, heads, d_v, state, out); break;
-      case 5: delta_rule_tc_kernel<5><<<grid, 32, 0, st>>>(q, k, v, beta, alpha, tokens, heads, d_v, state, out); break;
-      case 6: delta_rule_tc_kernel<6><<<grid, 32, 0, st>>>(q, k, v, beta, alpha, tokens, heads, d_v, state, out); break;
-      case 7: delta_rule_tc_kernel<7><<<grid, 32, 0, st>>>(q, k, v, beta, alpha, tokens, heads, d_v, state, out); break;
-      default: delta_rule_tc_kernel<8><<<grid, 32, 0, st>>>(q, k, v, beta, alpha, tokens, heads, d_v, state, out); break;
+      case 1: return launch_delta_tc<1>(grid, q, k, v, beta, alpha, tokens, heads, d_v, state, out, st);
+      case 2: return launch_delta_tc<2>(grid, q, k, v, beta, alpha, tokens, heads, d_v, state, out, st);
+      case 3: return launch_delta_tc<3>(grid, q, k, v, beta, alpha, tokens, heads, d_v, state, out, st);
+      case 4: return launch_delta_tc<4>(grid, q, k, v, beta, alpha, tokens, heads, d_v, state, out, st);
+      case 5: return launch_delta_tc<5>(grid, q, k, v, beta, alpha, tokens, heads, d_v, state, out, st);
+      case 6: return launch_delta_tc<6>(grid, q, k, v, beta, alpha, tokens, heads, d_v, state, out, st);
+      case 7: return launch_delta_tc<7>(grid, q, k, v, beta, alpha, tokens, heads, d_v, state, out, st);
+      default: return launch_delta_tc<8>(grid, q, k, v, beta, alpha, tokens, heads, d_v, state, out, st);
     }
-    return cudaGetLastError();
   }
   const size_t smem = (size_t)(d_k * kCols + 2 * kB * d_k) * sizeof(float);
   delta_rule_kernel<<<grid, kDThreads, smem, st>>>(q, k, v, beta, alpha, tokens, heads, d_k, d_v, state, out);
