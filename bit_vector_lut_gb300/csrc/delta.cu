@@ -209,7 +209,7 @@ struct TcSmem {
   static constexpr uint32_t kAl = kV + kTcChunk * 16 * 2;      // alpha [64], beta [64]
   static constexpr uint32_t kP = kAl + 2 * kTcChunk * 4;       // P, M [blocks][8][8]
   static constexpr uint32_t kG = kP + 2 * kTcBlocks * 64 * 4;  // gamma, w [blocks][8]
-  // phase-1 scratch [KS][6][8][8] and, later in the chunk, the X partials [2][KS][8][32]
+  // phase-1 scratch [KS][6][8][8] and, later in the chunk, the X partials [2][KS][2][32][4]
   static constexpr uint32_t kU = kG + 2 * kTcBlocks * 8 * 4;
   static constexpr uint32_t kUBytes = (uint32_t)KS * 2048u;
   static constexpr uint32_t kTotal = kU + kUBytes;
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(32 * KS, 1) delta_rule_tc_kernel(const uint16_
   float (*Wm)[8] = Gm + kTcBlocks;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   float (*Sc)[8][8] = reinterpret_cast<float (*)[8][8]>(dsm + L::kU + (uint32_t)warp * 1536u);  // 6 of them
-  float* Xp = reinterpret_cast<float*>(dsm + L::kU);  // [2][KS][8][32]
+  float* Xp = reinterpret_cast<float*>(dsm + L::kU);  // [2][KS][2][32][4]
   const int h = blockIdx.x, c0 = blockIdx.y * 16;
   float* Sg = state + (size_t)h * DK * d_v + c0;
 
@@ -369,12 +369,10 @@ __global__ void __launch_bounds__(32 * KS, 1) delta_rule_tc_kernel(const uint16_
         mma_tc(xq, ah, q0, q1);
         mma_tc(xk, al, k0, k1);
         mma_tc(xq, al, q0, q1);
-        float* xp = Xp + (((b & 1) * KS + warp) * 8) * 32 + lane;  // double-buffered by block parity
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          xp[j * 32] = xk[j];
-          xp[(j + 4) * 32] = xq[j];
-        }
+        // [parity][warp][K | Q][lane][4]: 16-byte stores, lanes 16 bytes apart (double-buffered by parity)
+        float4* xp = reinterpret_cast<float4*>(Xp) + ((b & 1) * KS + warp) * 64 + lane;
+        xp[0] = make_float4(xk[0], xk[1], xk[2], xk[3]);
+        xp[32] = make_float4(xq[0], xq[1], xq[2], xq[3]);
       }
       __syncthreads();  // every warp's partial is in shared memory
       // the partials added in warp (= k-step) order: (K S)^T and (Q S)^T at [g][2t], [g][2t+1],
@@ -382,12 +380,16 @@ __global__ void __launch_bounds__(32 * KS, 1) delta_rule_tc_kernel(const uint16_
       float xk[4] = {0.f, 0.f, 0.f, 0.f}, xq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int w2 = 0; w2 < KS; ++w2) {
-        const float* xp = Xp + (((b & 1) * KS + w2) * 8) * 32 + lane;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          xk[j] += xp[j * 32];
-          xq[j] += xp[(j + 4) * 32];
-        }
+        const float4* xp = reinterpret_cast<const float4*>(Xp) + ((b & 1) * KS + w2) * 64 + lane;
+        const float4 pk = xp[0], pq = xp[32];
+        xk[0] += pk.x;
+        xk[1] += pk.y;
+        xk[2] += pk.z;
+        xk[3] += pk.w;
+        xq[0] += pq.x;
+        xq[1] += pq.y;
+        xq[2] += pq.z;
+        xq[3] += pq.w;
       }
       const float* gm = Gm[b];
       const int j0 = 2 * t, j1 = 2 * t + 1;
@@ -397,8 +399,9 @@ __global__ void __launch_bounds__(32 * KS, 1) delta_rule_tc_kernel(const uint16_
       float ulo[8], uhi[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        ulo[i] = fmaf(Pm[b][i][j1], r1, Pm[b][i][j0] * r0);
-        uhi[i] = fmaf(Pm[b][i][j1], r3, Pm[b][i][j0] * r2);
+        const float2 pp = *reinterpret_cast<const float2*>(&Pm[b][i][j0]);  // P[i][2t], P[i][2t+1]
+        ulo[i] = fmaf(pp.y, r1, pp.x * r0);
+        uhi[i] = fmaf(pp.y, r3, pp.x * r2);
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -421,8 +424,9 @@ __global__ void __launch_bounds__(32 * KS, 1) delta_rule_tc_kernel(const uint16_
         float olo[8], ohi[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          olo[i] = fmaf(Mm[b][i][j1], u1, Mm[b][i][j0] * u0);
-          ohi[i] = fmaf(Mm[b][i][j1], u3, Mm[b][i][j0] * u2);
+          const float2 mm = *reinterpret_cast<const float2*>(&Mm[b][i][j0]);  // M[i][2t], M[i][2t+1]
+          olo[i] = fmaf(mm.y, u1, mm.x * u0);
+          ohi[i] = fmaf(mm.y, u3, mm.x * u2);
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
