@@ -482,6 +482,18 @@ void mlp_counter_range(const vq3_mlp_layer* layer, size_t* offset, size_t* bytes
   *bytes = mlp_ctl_bytes(layer->gate.d_in, layer->gate.d_out);
 }
 
+// For the other host-side files of the library: the same thread-local error message.
+int report_error(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+int report_ok() { return ok(); }
+
 }  // namespace vq3
 
 using namespace vq3;

@@ -94,6 +94,10 @@ constexpr int kDecWarps = 16;  // warps per decoding CTA = segments per group
 constexpr int kDecMaxGrid = 2048;
 
 int device_sm_count();
+// The C ABI's thread-local error message, for host code outside api.cu: report_error sets it
+// (printf format) and returns code; report_ok clears it and returns VQ3_OK.
+int report_error(int code, const char* fmt, ...);
+int report_ok();
 int dec_tiles_per_pass(int rows);  // 8-row tiles per pass: 1, 2 or 4 (8, 16 or 32 rows)
 // One pass (up to 32 rows) of the MLP block, or of a single linear layer, as
 // one persistent cooperative kernel. Its steps (decode gate/up, SwiGLU, decode

@@ -42,6 +42,13 @@ class vq3_mlp_layer(ctypes.Structure):
     _fields_ = [("gate", vq3_linear), ("up", vq3_linear), ("down", vq3_linear)]
 
 
+class vq3_blob_view(ctypes.Structure):
+    _fields_ = [("d_in", c_int), ("d_out", c_int), ("block", c_int), ("format", c_int), ("lr_rank", c_int),
+                ("has_signs", c_int), ("canonical", c_void_p), ("packed", c_void_p), ("scales", c_void_p),
+                ("codebook", c_void_p), ("codebook_bytes", c_size_t), ("signs", c_void_p), ("lr_u", c_void_p),
+                ("lr_v", c_void_p)]
+
+
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
@@ -53,6 +60,10 @@ def _load() -> ctypes.CDLL:
         "vq3_packed_bytes_fmt": (c_size_t, [c_int, c_int, c_int]),
         "vq3_pack_layout_fmt": (c_int, [c_int, POINTER(c_uint8), c_int, c_int, c_void_p]),
         "vq3_unpack_layout_fmt": (c_int, [c_int, c_void_p, c_int, c_int, POINTER(c_uint8)]),
+        "vq3_blob_bytes": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+        "vq3_blob_write": (c_int, [c_int, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
+                                   c_void_p, c_void_p, c_void_p, c_size_t]),
+        "vq3_blob_read": (c_int, [c_void_p, c_size_t, POINTER(vq3_blob_view)]),
         "fwht_rotate": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]),
         "vq3_linear_workspace_bytes": (c_size_t, [c_int, POINTER(vq3_linear)]),
         "vq3_mlp_workspace_bytes": (c_size_t, [c_int, POINTER(vq3_mlp_layer)]),
@@ -136,6 +147,67 @@ def unpack_layout(packed: np.ndarray, d_in: int, d_out: int, fmt: str = "2x64") 
 
 # ---------------------------------------------------------------- weights on the device
 
+_FORMAT_NAMES = {v[0]: k for k, v in FORMATS.items()}
+
+
+def blob_bytes(d_in: int, d_out: int, fmt: str = "2x64", lr_rank: int = 0, has_signs: bool = False) -> int:
+    """Size of the packed-weight blob of one matrix (0 if the descriptor is unsupported)."""
+    return int(lib.vq3_blob_bytes(d_in, d_out, FORMATS[fmt][0], lr_rank, int(bool(has_signs))))
+
+
+def _np_ptr(a):
+    return None if a is None else a.ctypes.data_as(c_void_p)
+
+
+def save_blob(m) -> bytes:
+    """The packed-weight blob of one matrix (any object with d_in, d_out, block, stream, codebook,
+    scales, signs and optionally fmt, lr_u, lr_v), built by vq3_blob_write."""
+    fmt = getattr(m, "fmt", "2x64") or "2x64"
+    stream = np.ascontiguousarray(m.stream, dtype=np.uint8)
+    scales = np.ascontiguousarray(m.scales, dtype=np.float16)
+    codebook = np.ascontiguousarray(m.codebook, dtype=np.float16).reshape(-1)
+    signs = None if m.signs is None else np.ascontiguousarray(m.signs, dtype=np.uint32)
+    lr_u, lr_v = getattr(m, "lr_u", None), getattr(m, "lr_v", None)
+    rank = 0
+    if lr_u is not None:
+        lr_u = np.ascontiguousarray(lr_u, dtype=np.float16)
+        lr_v = np.ascontiguousarray(lr_v, dtype=np.float16)
+        rank = int(lr_u.shape[1])
+    n = blob_bytes(m.d_in, m.d_out, fmt, rank, signs is not None)
+    if n == 0:
+        raise Vq3Error(-3, f"blob: unsupported matrix {m.d_in} x {m.d_out} ({fmt}, rank {rank})")
+    out = np.empty(n, dtype=np.uint8)
+    _check(lib.vq3_blob_write(m.d_in, m.d_out, m.block, FORMATS[fmt][0], _np_ptr(stream), _np_ptr(scales),
+                              _np_ptr(codebook), _np_ptr(signs), rank, _np_ptr(lr_u), _np_ptr(lr_v),
+                              _np_ptr(out), n))
+    return out.tobytes()
+
+
+def load_blob(data: bytes) -> dict:
+    """Checks a packed-weight blob (vq3_blob_read) and returns copies of its parts as numpy arrays."""
+    buf = np.frombuffer(data, dtype=np.uint8)
+    view = vq3_blob_view()
+    _check(lib.vq3_blob_read(_np_ptr(buf), buf.size, ctypes.byref(view)))
+    base = buf.ctypes.data
+
+    def part(ptr, count, dtype):
+        off = ptr - base
+        return buf[off:off + count * np.dtype(dtype).itemsize].view(dtype).copy()
+
+    fmt = _FORMAT_NAMES[view.format]
+    nbytes = packed_bytes(view.d_in, view.d_out, fmt)
+    out = {"d_in": view.d_in, "d_out": view.d_out, "block": view.block, "fmt": fmt,
+           "stream": part(view.canonical, nbytes, np.uint8), "packed": part(view.packed, nbytes, np.uint8),
+           "scales": part(view.scales, view.d_out, np.float16),
+           "codebook": part(view.codebook, view.codebook_bytes // 2, np.float16),
+           "signs": part(view.signs, view.d_in // 32, np.uint32) if view.has_signs else None,
+           "lr_u": None, "lr_v": None}
+    if view.lr_rank:
+        out["lr_u"] = part(view.lr_u, view.d_out * view.lr_rank, np.float16).reshape(view.d_out, view.lr_rank)
+        out["lr_v"] = part(view.lr_v, view.lr_rank * view.d_in, np.float16).reshape(view.lr_rank, view.d_in)
+    return out
+
+
 class Linear:
     """One VQ3 matrix resident on the GPU (packed indices, codebook, scales, signs)."""
 
@@ -163,6 +235,20 @@ class Linear:
             lu = torch.from_numpy(np.ascontiguousarray(lr_u, dtype=np.float16)).to(device)
             lv = torch.from_numpy(np.ascontiguousarray(lr_v, dtype=np.float16)).to(device)
         return cls(d_in, d_out, block, packed, cb, sc, sg, fmt, lu, lv)
+
+    @classmethod
+    def from_blob(cls, data: bytes, device="cuda"):
+        """From a packed-weight blob (save_blob): its GPU-layout section is copied as it is."""
+        b = load_blob(data)
+        packed = torch.from_numpy(b["packed"]).to(device)
+        cb = torch.from_numpy(b["codebook"]).to(device)
+        sc = torch.from_numpy(b["scales"]).to(device)
+        sg = None if b["signs"] is None else torch.from_numpy(b["signs"].view(np.int32)).to(device)
+        lu = lv = None
+        if b["lr_u"] is not None:
+            lu = torch.from_numpy(b["lr_u"]).to(device)
+            lv = torch.from_numpy(b["lr_v"]).to(device)
+        return cls(b["d_in"], b["d_out"], b["block"], packed, cb, sc, sg, b["fmt"], lu, lv)
 
     @classmethod
     def from_matrix(cls, m, device="cuda"):

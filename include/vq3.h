@@ -166,6 +166,48 @@ VQ3_API int vq3_pack_layout_fmt(int format, const uint8_t* canonical, int d_in, 
 VQ3_API int vq3_unpack_layout_fmt(int format, const void* packed_host, int d_in, int d_out, uint8_t* canonical);
 
 /*
+ * Packed-weight blob: one matrix as a single host byte buffer (a file's contents),
+ * so that a converted layer is stored once and loaded without repacking. This
+ * library's own format: the pages ship their converted layers in their runtime's
+ * files and do not give that layout. Host-side, offline; allocates nothing.
+ * Layout (little-endian, every section at a 256-byte aligned offset):
+ *   header, 256 bytes: magic "VQ3BLOB1"; version (1); d_in, d_out, block, format,
+ *     lr_rank, flags (bit 0: sign bits present); offset and size of each section
+ *     below; FNV-1a 64-bit hash of every byte after the header;
+ *   canonical index stream (vq3_pack_layout_fmt's input, vq3_packed_bytes_fmt bytes);
+ *   GPU-layout indices (vq3_pack_layout_fmt of that stream, the same size);
+ *   scales FP16 [d_out]; codebook (FP16x2 [64] or [16] words, FP16 [16] for lut4);
+ *   sign bits [d_in / 32] when present; U FP16 [d_out][lr_rank] and
+ *   V FP16 [lr_rank][d_in] when lr_rank > 0.
+ * vq3_blob_bytes: the blob's size, 0 for an unsupported descriptor.
+ * vq3_blob_write: host inputs -> out (out_bytes >= vq3_blob_bytes). signs may be
+ *   NULL; lr_u, lr_v are read only when lr_rank > 0. It builds the GPU layout itself.
+ * vq3_blob_read: checks the magic, version, descriptor, section table, hash and
+ *   that the GPU-layout section is the layout of the canonical one, then fills
+ *   *view with the descriptor and host pointers into blob (valid while it is).
+ * Errors: VQ3_EINVAL (null pointer, bad sizes, a blob that fails a check: the
+ *   message says which), VQ3_EUNSUPPORTED (format, d_in / d_out, block, lr_rank),
+ *   VQ3_ENOSPACE (out_bytes too small).
+ */
+typedef struct vq3_blob_view {
+  int d_in, d_out, block, format, lr_rank, has_signs;
+  const uint8_t* canonical;   /* vq3_packed_bytes_fmt(format, d_in, d_out) bytes */
+  const void* packed;         /* the same size, GPU layout */
+  const uint16_t* scales;     /* [d_out] */
+  const void* codebook;       /* codebook_bytes */
+  size_t codebook_bytes;
+  const uint32_t* signs;      /* [d_in / 32] or NULL */
+  const uint16_t* lr_u;       /* [d_out][lr_rank] or NULL */
+  const uint16_t* lr_v;       /* [lr_rank][d_in] or NULL */
+} vq3_blob_view;
+
+VQ3_API size_t vq3_blob_bytes(int d_in, int d_out, int format, int lr_rank, int has_signs);
+VQ3_API int vq3_blob_write(int d_in, int d_out, int block, int format, const uint8_t* canonical,
+                           const uint16_t* scales, const void* codebook, const uint32_t* signs, int lr_rank,
+                           const uint16_t* lr_u, const uint16_t* lr_v, void* out, size_t out_bytes);
+VQ3_API int vq3_blob_read(const void* blob, size_t bytes, vq3_blob_view* view);
+
+/*
  * Blocked, normalised fast Walsh-Hadamard transform of each row:
  *   out[r, j*b:(j+1)*b] = H_b diag(s_j) x[r, j*b:(j+1)*b] / sqrt(b).
  * Cited: model card "anemll/anemll-forge-qwen3.8-27B", "Release 0.2" bullet
