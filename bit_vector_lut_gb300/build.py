@@ -3,6 +3,11 @@
 Each translation unit compiles in parallel to bit_vector_lut_gb300/_build/,
 then one nvcc -shared link writes bit_vector_lut_gb300/libvq3.so.
 Objects are rebuilt when their source or any header is newer.
+
+build(bounds_check=True) writes a second library, libvq3_bc.so (objects in _build_bc/),
+compiled with -DVQ3_BOUNDS_CHECK: every computed global index of the kernels is checked
+against its buffer's extent, out-of-range accesses are skipped and counted, and
+vq3_bounds_check reads the counts. vq3.py loads it when VQ3_LIB names its path.
 """
 
 from __future__ import annotations
@@ -18,6 +23,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libvq3.so")
+BUILD_BC = os.path.join(PKG, "_build_bc")
+LIB_BC = os.path.join(PKG, "libvq3_bc.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -52,8 +59,8 @@ def _stale(obj: str, src: str, hdr_mtime: float) -> bool:
     return m < os.path.getmtime(src) or m < hdr_mtime
 
 
-def _compile(src: str, obj: str, verbose: bool) -> None:
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+def _compile(src: str, obj: str, verbose: bool, extra: list[str]) -> None:
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -63,24 +70,26 @@ def _compile(src: str, obj: str, verbose: bool) -> None:
         sys.stderr.write(r.stdout + r.stderr)
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, bounds_check: bool = False) -> str:
+    build_dir, lib = (BUILD_BC, LIB_BC) if bounds_check else (BUILD, LIB)
+    extra = ["-DVQ3_BOUNDS_CHECK"] if bounds_check else []
+    os.makedirs(build_dir, exist_ok=True)
     hdr_mtime = max([os.path.getmtime(h) for h in headers()] + [os.path.getmtime(__file__)])
     srcs = sources()
-    objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    objs = [os.path.join(build_dir, os.path.basename(s)[:-3] + ".o") for s in srcs]
     todo = [(s, o) for s, o in zip(srcs, objs) if force or _stale(o, s, hdr_mtime)]
     if todo:
         with ThreadPoolExecutor(max_workers=min(8, len(todo))) as ex:
-            list(ex.map(lambda so: _compile(so[0], so[1], verbose), todo))
-    if todo or force or not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
-        tmp = LIB + ".tmp"
+            list(ex.map(lambda so: _compile(so[0], so[1], verbose, extra), todo))
+    if todo or force or not os.path.exists(lib) or any(os.path.getmtime(o) > os.path.getmtime(lib) for o in objs):
+        tmp = lib + ".tmp"
         cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv))
+    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv, bounds_check="--bounds-check" in sys.argv))

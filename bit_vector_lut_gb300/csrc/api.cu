@@ -502,7 +502,33 @@ extern "C" {
 
 const char* vq3_last_error(void) { return g_err.c_str(); }
 
-const char* vq3_version(void) { return "vq3-gb300 0.2 (sm_103a; layout su64x64-m16n8k16)"; }
+const char* vq3_version(void) {
+#ifdef VQ3_BOUNDS_CHECK
+  return "vq3-gb300 0.2 (sm_103a; layout su64x64-m16n8k16; bounds-check build)";
+#else
+  return "vq3-gb300 0.2 (sm_103a; layout su64x64-m16n8k16)";
+#endif
+}
+
+int vq3_bounds_check(unsigned* out, int n_out, int reset) {
+#ifdef VQ3_BOUNDS_CHECK
+  if (!out || n_out < 2 * VQ3_BOUNDS_FILES)
+    return report_error(VQ3_EINVAL, "bounds_check: out needs %d entries", 2 * VQ3_BOUNDS_FILES);
+  cudaError_t (*const rd[VQ3_BOUNDS_FILES])(unsigned*, bool) = {bounds_read_persistent, bounds_read_lowrank,
+                                                                 bounds_read_delta,      bounds_read_rotate,
+                                                                 bounds_read_prefill,    bounds_read_prefill_wide};
+  for (int f = 0; f < VQ3_BOUNDS_FILES; ++f) {
+    const cudaError_t e = rd[f](out + 2 * f, reset != 0);
+    if (e != cudaSuccess) return report_error(VQ3_ECUDA, "bounds_check: %s", cudaGetErrorString(e));
+  }
+  return report_ok();
+#else
+  (void)out;
+  (void)n_out;
+  (void)reset;
+  return report_error(VQ3_EUNSUPPORTED, "bounds_check: this library was built without -DVQ3_BOUNDS_CHECK");
+#endif
+}
 
 size_t vq3_packed_bytes_fmt(int format, int d_in, int d_out) {
   if (!format_supported(format) || !layout_supported(d_in, d_out)) return 0;

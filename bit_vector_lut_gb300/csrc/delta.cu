@@ -20,6 +20,7 @@
 #include "vq3_internal.h"
 
 namespace vq3 {
+VQ3_BOUNDS_RECORD(delta)
 namespace {
 
 constexpr int kB = 8;       // tokens per block
@@ -45,20 +46,24 @@ __global__ void __launch_bounds__(kDThreads) delta_rule_kernel(const uint16_t* _
   const int tid = threadIdx.x;
   const int h = blockIdx.x, c0 = blockIdx.y * kCols;
   float* Sg = state + (size_t)h * d_k * d_v;
-  for (int e = tid; e < d_k * kCols; e += kDThreads) Ss[e] = Sg[(size_t)(e / kCols) * d_v + c0 + e % kCols];
+  const size_t n_state = (size_t)heads * d_k * d_v, n_qk = (size_t)tokens * heads * d_k, n_v = (size_t)tokens * heads * d_v;
+  (void)n_state; (void)n_qk; (void)n_v;
+  for (int e = tid; e < d_k * kCols; e += kDThreads)
+    Ss[e] = VQ3_IN((size_t)h * d_k * d_v + (size_t)(e / kCols) * d_v + c0 + e % kCols, n_state, 1)
+                ? Sg[(size_t)(e / kCols) * d_v + c0 + e % kCols] : 0.f;
   const int t_ = tid / kCols, c_ = tid % kCols;  // (token, column) of this thread in the 8 x 16 phases
 
   for (int b0 = 0; b0 < tokens; b0 += kB) {
     // ---- block inputs; tokens past the last act as k = q = v = 0, beta = 0, alpha = 1
     for (int e = tid; e < kB * d_k; e += kDThreads) {
       const int t = e / d_k, i = e % d_k;
-      const bool ok = b0 + t < tokens;
       const size_t o = ((size_t)(b0 + t) * heads + h) * d_k + i;
+      const bool ok = b0 + t < tokens && VQ3_IN(o, n_qk, 2);
       Ks[e] = ok ? h2f(k[o]) : 0.f;
       Qs[e] = ok ? h2f(q[o]) : 0.f;
     }
     {
-      const bool ok = b0 + t_ < tokens;
+      const bool ok = b0 + t_ < tokens && VQ3_IN(((size_t)(b0 + t_) * heads + h) * d_v + c0 + c_, n_v, 3);
       Vs[t_][c_] = ok ? h2f(v[((size_t)(b0 + t_) * heads + h) * d_v + c0 + c_]) : 0.f;
     }
     if (tid < kB) {
@@ -141,7 +146,7 @@ __global__ void __launch_bounds__(kDThreads) delta_rule_kernel(const uint16_t* _
     {
       float s = ga[t_] * QS[t_][c_];
       for (int j = 0; j <= t_; ++j) s = fmaf(ga[t_] / ga[j] * be[j] * QK[t_][j], U[j][c_], s);
-      if (b0 + t_ < tokens)
+      if (b0 + t_ < tokens && VQ3_IN(((size_t)(b0 + t_) * heads + h) * d_v + c0 + c_, n_v, 4))
         out[((size_t)(b0 + t_) * heads + h) * d_v + c0 + c_] = __half_as_ushort(__float2half_rn(s));
     }
     // ---- S = gamma_8 S0 + K^T diag(beta_j gamma_8 / gamma_j) U
@@ -159,7 +164,9 @@ __global__ void __launch_bounds__(kDThreads) delta_rule_kernel(const uint16_t* _
     }
     __syncthreads();
   }
-  for (int e = tid; e < d_k * kCols; e += kDThreads) Sg[(size_t)(e / kCols) * d_v + c0 + e % kCols] = Ss[e];
+  for (int e = tid; e < d_k * kCols; e += kDThreads)
+    if (VQ3_IN((size_t)h * d_k * d_v + (size_t)(e / kCols) * d_v + c0 + e % kCols, n_state, 5))
+      Sg[(size_t)(e / kCols) * d_v + c0 + e % kCols] = Ss[e];
 }
 
 
@@ -256,12 +263,18 @@ __global__ void __launch_bounds__(32 * KS, 1) delta_rule_tc_kernel(const uint16_
   float* Xp = reinterpret_cast<float*>(dsm + L::kU);  // [2][KS][2][32][4]
   const int h = blockIdx.x, c0 = blockIdx.y * 16;
   float* Sg = state + (size_t)h * DK * d_v + c0;
+  const size_t n_state = (size_t)heads * DK * d_v, n_qk = (size_t)tokens * heads * DK, n_v = (size_t)tokens * heads * d_v;
+  (void)n_state; (void)n_qk; (void)n_v;
 
   // this warp's tiles of the state slice: acc[n] = S^T[g, g+8][16 warp + 8n + 2t, +1]
   float acc[2][4];
 #pragma unroll
   for (int n = 0; n < 2; ++n) {
     const int d = 16 * warp + 8 * n + 2 * t;
+    if (!VQ3_IN((size_t)h * DK * d_v + c0 + (size_t)(d + 1) * d_v + g + 8, n_state, 11)) {
+      acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+      continue;
+    }
     acc[n][0] = Sg[(size_t)d * d_v + g];
     acc[n][1] = Sg[(size_t)(d + 1) * d_v + g];
     acc[n][2] = Sg[(size_t)d * d_v + g + 8];
@@ -277,7 +290,7 @@ __global__ void __launch_bounds__(32 * KS, 1) delta_rule_tc_kernel(const uint16_
     for (int i = tid; i < nb * 8 * (DK / 8); i += NT) {
       const int tk = i / (DK / 8), c = i % (DK / 8);
       const uint32_t off = (uint32_t)(tk * RS + c * 8) * 2u;
-      if (tk < nt) {
+      if (tk < nt && VQ3_IN(((size_t)(base + tk) * heads + h) * DK + c * 8 + 7, n_qk, 12)) {
         const size_t src = ((size_t)(base + tk) * heads + h) * DK + c * 8;
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(ks + off), "l"(k + src) : "memory");
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(qs + off), "l"(q + src) : "memory");
@@ -289,7 +302,7 @@ __global__ void __launch_bounds__(32 * KS, 1) delta_rule_tc_kernel(const uint16_
     for (int i = tid; i < nb * 8 * 2; i += NT) {  // two 16-byte halves of each token's 16 columns
       const int tk = i >> 1, c = (i & 1) * 8;
       const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(&Vh[tk][c]));
-      if (tk < nt)
+      if (tk < nt && VQ3_IN(((size_t)(base + tk) * heads + h) * d_v + c0 + c + 7, n_v, 13))
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
                      "l"(v + ((size_t)(base + tk) * heads + h) * d_v + c0 + c) : "memory");
       else
@@ -446,12 +459,12 @@ __global__ void __launch_bounds__(32 * KS, 1) delta_rule_tc_kernel(const uint16_
         const float o0 = fmaf(gm[j0], xq[0], s0), o1 = fmaf(gm[j1], xq[1], s1);
         const float o2 = fmaf(gm[j0], xq[2], s2), o3 = fmaf(gm[j1], xq[3], s3);
         const int tk0 = base + tb + j0, tk1 = base + tb + j1;
-        if (tk0 < tokens) {
+        if (tk0 < tokens && VQ3_IN(((size_t)tk0 * heads + h) * d_v + c0 + g + 8, n_v, 14)) {
           uint16_t* o = out + ((size_t)tk0 * heads + h) * d_v + c0;
           o[g] = __half_as_ushort(__float2half_rn(o0));
           o[g + 8] = __half_as_ushort(__float2half_rn(o2));
         }
-        if (tk1 < tokens) {
+        if (tk1 < tokens && VQ3_IN(((size_t)tk1 * heads + h) * d_v + c0 + g + 8, n_v, 14)) {
           uint16_t* o = out + ((size_t)tk1 * heads + h) * d_v + c0;
           o[g] = __half_as_ushort(__float2half_rn(o1));
           o[g + 8] = __half_as_ushort(__float2half_rn(o3));
@@ -480,6 +493,7 @@ __global__ void __launch_bounds__(32 * KS, 1) delta_rule_tc_kernel(const uint16_
 #pragma unroll
   for (int n = 0; n < 2; ++n) {
     const int d = 16 * warp + 8 * n + 2 * t;
+    if (!VQ3_IN((size_t)h * DK * d_v + c0 + (size_t)(d + 1) * d_v + g + 8, n_state, 15)) continue;
     Sg[(size_t)d * d_v + g] = acc[n][0];
     Sg[(size_t)(d + 1) * d_v + g] = acc[n][1];
     Sg[(size_t)d * d_v + g + 8] = acc[n][2];

@@ -20,6 +20,7 @@
 #include "vq3_internal.h"
 
 namespace vq3 {
+VQ3_BOUNDS_RECORD(lowrank)
 namespace {
 
 constexpr int kLT = 64;        // rows per tile
@@ -58,10 +59,12 @@ __global__ void __launch_bounds__(128) lowrank_project_kernel(const uint16_t* __
     for (int i = tid; i < 64 * 8; i += 128) {
       const int row = i >> 3, c = i & 7;
       uint16_t* dx = xs[buf] + row * kLS + c * 8;
-      if (r0 + row < rows) cp16(dx, xr + (size_t)(r0 + row) * d_in + (size_t)kg * kLK + c * 8);
+      if (r0 + row < rows && VQ3_IN((size_t)(r0 + row) * d_in + (size_t)kg * kLK + c * 8 + 7, (size_t)rows * d_in, 1))
+        cp16(dx, xr + (size_t)(r0 + row) * d_in + (size_t)kg * kLK + c * 8);
       else zero16(dx);
       uint16_t* dv = vs[buf] + row * kLS + c * 8;
-      if (row < rank) cp16(dv, V + (size_t)row * d_in + (size_t)kg * kLK + c * 8);
+      if (row < rank && VQ3_IN((size_t)row * d_in + (size_t)kg * kLK + c * 8 + 7, (size_t)rank * d_in, 2))
+        cp16(dv, V + (size_t)row * d_in + (size_t)kg * kLK + c * 8);
       else zero16(dv);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
@@ -104,7 +107,7 @@ __global__ void __launch_bounds__(128) lowrank_project_kernel(const uint16_t* __
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int r = r0 + 16 * warp + g + 8 * h;
-      if (r < rows)
+      if (r < rows && VQ3_IN(((size_t)sp * rows + r) * rank + q + 1, (size_t)n_split * rows * rank, 3))
         *reinterpret_cast<float2*>(part + ((size_t)sp * rows + r) * rank + q) = make_float2(acc[n][2 * h], acc[n][2 * h + 1]);
     }
   }
@@ -119,7 +122,9 @@ __global__ void __launch_bounds__(256) lowrank_reduce_kernel(const float* __rest
   for (int k0 = 0; k0 < n_split; k0 += 16) {  // sixteen splits' loads in flight, added in order
     float v[16];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) v[k] = k0 + k < n_split ? __ldg(part + (size_t)(k0 + k) * n + e) : 0.f;
+    for (int k = 0; k < 16; ++k)
+      v[k] = k0 + k < n_split && VQ3_IN((size_t)(k0 + k) * n + e, (size_t)n_split * n, 4) ? __ldg(part + (size_t)(k0 + k) * n + e)
+                                                                                          : 0.f;
 #pragma unroll
     for (int k = 0; k < 16; ++k) s += v[k];
   }
@@ -138,7 +143,8 @@ __global__ void __launch_bounds__(128) lowrank_expand_kernel(const float* __rest
   for (int i = tid; i < 128 * 8; i += 128) {  // U: 16-byte chunks of each row (q past the rank zero)
     const int row = i >> 3, c = i & 7;
     uint16_t* du = us + row * kLS + c * 8;
-    if (o0 + row < d_out && c * 8 < rank) cp16(du, U + (size_t)(o0 + row) * rank + c * 8);
+    if (o0 + row < d_out && c * 8 < rank && VQ3_IN((size_t)(o0 + row) * rank + c * 8 + 7, (size_t)d_out * rank, 5))
+      cp16(du, U + (size_t)(o0 + row) * rank + c * 8);
     else zero16(du);
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
@@ -149,7 +155,8 @@ __global__ void __launch_bounds__(128) lowrank_expand_kernel(const float* __rest
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       const int i = tid + 128 * k, row = i >> 5, qp = i & 31;
-      v[k] = (r0 + row < rows && 2 * qp < rank) ? *reinterpret_cast<const float2*>(z + (size_t)(r0 + row) * rank + 2 * qp)
+      v[k] = (r0 + row < rows && 2 * qp < rank && VQ3_IN((size_t)(r0 + row) * rank + 2 * qp + 1, (size_t)rows * rank, 6))
+                 ? *reinterpret_cast<const float2*>(z + (size_t)(r0 + row) * rank + 2 * qp)
                                                 : make_float2(0.f, 0.f);
     }
 #pragma unroll
@@ -189,7 +196,8 @@ __global__ void __launch_bounds__(128) lowrank_expand_kernel(const float* __rest
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int r = r0 + ra + 8 * h;
-      if (r < rows) *reinterpret_cast<float2*>(ylr + (size_t)r * d_out + o) = make_float2(acc[n][2 * h], acc[n][2 * h + 1]);
+      if (r < rows && VQ3_IN((size_t)r * d_out + o + 1, (size_t)rows * d_out, 7))
+        *reinterpret_cast<float2*>(ylr + (size_t)r * d_out + o) = make_float2(acc[n][2 * h], acc[n][2 * h + 1]);
     }
   }
 }

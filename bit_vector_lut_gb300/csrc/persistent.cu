@@ -51,6 +51,7 @@
 #include "vq3_internal.h"
 
 namespace vq3 {
+VQ3_BOUNDS_RECORD(persistent)
 namespace {
 
 constexpr int kWarps = kDecWarps;  // 16
@@ -386,10 +387,10 @@ __device__ __forceinline__ float round16(float v) { return __half2float(__float2
 template <typename T>
 __device__ __forceinline__ float act(const DecodeJob& a, const T* src, int row, int col) {
   const size_t o = (size_t)row * a.src_ld + col;
-  float v = load1(src + o);
+  float v = VQ3_IN(o, (size_t)a.rows * a.src_ld, 2) ? load1(src + o) : 0.f;
   if constexpr (sizeof(T) == 2) {
     if (a.inv) {
-      if (a.res_delta) v = round16(v + load1(a.res_delta + o));
+      if (a.res_delta) v = round16(v + (VQ3_IN(o, (size_t)a.rows * a.src_ld, 3) ? load1(a.res_delta + o) : 0.f));
       v = round16(v * a.inv[row]);
     }
   }
@@ -438,7 +439,9 @@ __device__ __forceinline__ void stage_round(const DecodeJob& a, const T* src, in
         const T* s = src + (size_t)row * a.src_ld + c * 1024;
         float v[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = load1(s + 32 * j + lane);
+        for (int j = 0; j < 32; ++j)
+          v[j] = VQ3_IN((size_t)row * a.src_ld + c * 1024 + 32 * j + lane, (size_t)a.rows * a.src_ld, 5)
+                     ? load1(s + 32 * j + lane) : 0.f;
         if constexpr (sizeof(T) == 2) {
           if (a.inv) {
             // pre-norm residual step: fp16(fp16(x + delta) * inv[row]), its loads after x's
@@ -447,7 +450,9 @@ __device__ __forceinline__ void stage_round(const DecodeJob& a, const T* src, in
               const uint16_t* sd = a.res_delta + (size_t)row * a.src_ld + c * 1024;
               float dl[32];
 #pragma unroll
-              for (int j = 0; j < 32; ++j) dl[j] = load1(sd + 32 * j + lane);
+              for (int j = 0; j < 32; ++j)
+                dl[j] = VQ3_IN((size_t)row * a.src_ld + c * 1024 + 32 * j + lane, (size_t)a.rows * a.src_ld, 6)
+                            ? load1(sd + 32 * j + lane) : 0.f;
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = round16(v[j] + dl[j]);
             }
@@ -457,7 +462,8 @@ __device__ __forceinline__ void stage_round(const DecodeJob& a, const T* src, in
         }
         if (a.signs) {
           // bit j of t: the sign of column c * 1024 + 32 j + lane (one word per lane, transposed)
-          const uint32_t t = warp_bit_transpose(__ldg(a.signs + c * 32 + lane), lane);
+          const uint32_t t =
+              warp_bit_transpose(VQ3_IN(c * 32 + lane, a.d_in / 32, 7) ? __ldg(a.signs + c * 32 + lane) : 0u, lane);
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __int_as_float(__float_as_int(v[j]) ^ ((t << (31 - j)) & 0x80000000u));
         }
@@ -492,7 +498,7 @@ __device__ __forceinline__ void stage_round(const DecodeJob& a, const T* src, in
       for (int e = threadIdx.x; e < nr * a.chunk; e += kThreads) {
         const int rr = e / a.chunk, col = c * a.chunk + e % a.chunk;
         float v = act(a, src, nt * 8 + rr, col);
-        if (a.signs && sign_bit(a.signs, col)) v = -v;
+        if (a.signs && VQ3_IN(col >> 5, a.d_in / 32, 4) && sign_bit(a.signs, col)) v = -v;
         buf[e] = v;
       }
       __syncthreads();
@@ -539,8 +545,9 @@ __device__ __forceinline__ void lr_copy(const DecodeJob& a, const SmemView& sv, 
   const int per_row = n * (kSuInputs / 8);  // 16-byte chunks of a row
   for (int i = threadIdx.x; i < a.lr_rank * per_row; i += kThreads) {
     const int q = i / per_row, k = i - q * per_row;
-    cp_async16(base + (uint32_t)q * kLrRow + (uint32_t)k * 16u,
-               a.lr_v + (size_t)q * a.d_in + (size_t)kg0 * kSuInputs + (size_t)k * 8);
+    if (VQ3_IN((size_t)q * a.d_in + (size_t)kg0 * kSuInputs + (size_t)k * 8, (size_t)a.lr_rank * a.d_in, 20))
+      cp_async16(base + (uint32_t)q * kLrRow + (uint32_t)k * 16u,
+                 a.lr_v + (size_t)q * a.d_in + (size_t)kg0 * kSuInputs + (size_t)k * 8);
   }
   cp_async_commit();
 }
@@ -618,7 +625,8 @@ __device__ __forceinline__ void lowrank_piece(const DecodeJob& a) {
 #pragma unroll
     for (int s = 0; s < 4; ++s) z += lds_f32(a.zacc + (uint32_t)((((m * 4 + s) * NT + nt) * 4 + j) * 32 + L) * 4u);
     const int q = 16 * m + (L >> 2) + 8 * (j >> 1), row = 8 * nt + 2 * (L & 3) + (j & 1);
-    __stcg(a.lr_z + ((size_t)blockIdx.x * 8 * NT + row) * 64 + q, z);
+    if (VQ3_IN(((size_t)blockIdx.x * 8 * NT + row) * 64 + q, (size_t)a.max_pieces * 512 * NT, 21))
+      __stcg(a.lr_z + ((size_t)blockIdx.x * 8 * NT + row) * 64 + q, z);
   }
 }
 
@@ -760,6 +768,10 @@ struct Cursor {
   int g;             // group of the next cell
   uint32_t slot;     // ring slot of the next copy: byte offset
   bool live;         // the warp's segment exists in group g
+#ifdef VQ3_BOUNDS_CHECK
+  const uint4* base;  // the matrix's packed indices and their extent in 16-byte units
+  size_t extent;
+#endif
 };
 
 constexpr int kSlots = 3;
@@ -795,6 +807,10 @@ __device__ __forceinline__ void cursor_group(const DecodeJob& a, Cursor& cur, in
   const int mat = two ? (sg & 1) : 0;
   const int mg = two ? (sg >> 1) : sg;
   cur.src = (mat ? a.packed1 : a.packed0) + ((size_t)mg * n_kg + kg) * FmtSizes<F>::kSuUint4 + lane;
+#ifdef VQ3_BOUNDS_CHECK
+  cur.base = mat ? a.packed1 : a.packed0;
+  cur.extent = (size_t)(a.d_out / kSuChannels) * n_kg * FmtSizes<F>::kSuUint4;
+#endif
 }
 
 // Issues the index copies of the warp's segment in the cursor's next cell (an
@@ -804,7 +820,8 @@ __device__ __forceinline__ void issue_cell(const DecodeJob& a, Cursor& cur, uint
   if (cur.left > 0 && cur.live) {
     const uint32_t s = ring_lane + cur.slot;
 #pragma unroll
-    for (int q = 0; q < FmtSizes<F>::kChunks; ++q) cp_async16(s + (uint32_t)(q * 512), cur.src + 32 * q);
+    for (int q = 0; q < FmtSizes<F>::kChunks; ++q)
+      if (VQ3_IN(cur.src + 32 * q - cur.base, cur.extent, 1)) cp_async16(s + (uint32_t)(q * 512), cur.src + 32 * q);
   }
   cp_async_commit();
   constexpr uint32_t kSlot = (uint32_t)Ring<F>::kSlotBytes;
@@ -926,7 +943,9 @@ __device__ __forceinline__ void decode_run(const DecodeJob& a, const T* src, Cur
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-              for (int j = 0; j < 4; ++j) __stcg(pc + ((m * NT + nt) * 4 + j) * 32 + lane, acc[m][nt][j]);
+              for (int j = 0; j < 4; ++j)
+                if (VQ3_IN(pc - a.pieces + ((m * NT + nt) * 4 + j) * 32 + lane, (size_t)n_seg * a.max_pieces * PIECE, 8))
+                  __stcg(pc + ((m * NT + nt) * 4 + j) * 32 + lane, acc[m][nt][j]);
         }
         signal(a.group_done + g, nullptr);
       }
@@ -969,13 +988,14 @@ __device__ __forceinline__ void swiglu_tasks(const PersistArgs& a, const DecodeJ
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int ch = (k && two ? m1 : m0) * kSuChannels + c;
-        sc[q][k][0] = __half2float(__ushort_as_half(__ldg(a.gate.scales + ch)));
-        sc[q][k][1] = __half2float(__ushort_as_half(__ldg(a.up.scales + ch)));
+        const bool sok = VQ3_IN(ch, a.d_inter, 10);
+        sc[q][k][0] = sok ? __half2float(__ushort_as_half(__ldg(a.gate.scales + ch))) : 0.f;
+        sc[q][k][1] = sok ? __half2float(__ushort_as_half(__ldg(a.up.scales + ch))) : 0.f;
       }
     }
     if (threadIdx.x == 0) {
-      poll_geq(gu.group_done + g0, (unsigned)n0, status);
-      if (two) poll_geq(gu.group_done + g1, (unsigned)n1, status);
+      if (VQ3_IN(gu.group_done + g0 - a.ctl, a.n_ctl, 26)) poll_geq(gu.group_done + g0, (unsigned)n0, status);
+      if (two && VQ3_IN(gu.group_done + g1 - a.ctl, a.n_ctl, 26)) poll_geq(gu.group_done + g1, (unsigned)n1, status);
     }
     __syncthreads();  // thread 0's acquire loads, then the barrier: the pieces are visible to the CTA
     const float* pg0 = gu.seg_pieces(2 * m0, PIECE);
@@ -992,10 +1012,11 @@ __device__ __forceinline__ void swiglu_tasks(const PersistArgs& a, const DecodeJ
 #pragma unroll
         for (int j = 0; j < P; ++j) {
           const size_t o = it + (size_t)(q0 + j) * PIECE;
-          v[0][j] = (q0 + j < n0) ? __ldcg(pg0 + o) : 0.f;
-          v[1][j] = (q0 + j < n0) ? __ldcg(pu0 + o) : 0.f;
-          v[2][j] = (q0 + j < n1) ? __ldcg(pg1 + o) : 0.f;
-          v[3][j] = (q0 + j < n1) ? __ldcg(pu1 + o) : 0.f;
+          const size_t ext = (size_t)gu.n_seg() * gu.max_pieces * PIECE;
+          v[0][j] = (q0 + j < n0 && VQ3_IN(pg0 - gu.pieces + o, ext, 9)) ? __ldcg(pg0 + o) : 0.f;
+          v[1][j] = (q0 + j < n0 && VQ3_IN(pu0 - gu.pieces + o, ext, 9)) ? __ldcg(pu0 + o) : 0.f;
+          v[2][j] = (q0 + j < n1 && VQ3_IN(pg1 - gu.pieces + o, ext, 9)) ? __ldcg(pg1 + o) : 0.f;
+          v[3][j] = (q0 + j < n1 && VQ3_IN(pu1 - gu.pieces + o, ext, 9)) ? __ldcg(pu1 + o) : 0.f;
         }
 #pragma unroll
         for (int j = 0; j < P; ++j) {
@@ -1012,11 +1033,15 @@ __device__ __forceinline__ void swiglu_tasks(const PersistArgs& a, const DecodeJ
         for (int k = 0; k < 2; ++k) {
           if (k == 1 && !two) break;
           const int ch = (k ? m1 : m0) * kSuChannels + c;
-          __stcg(a.hbuf + (size_t)r * a.d_inter + ch, silu_f(sc[q][k][0] * s[2 * k]) * (sc[q][k][1] * s[2 * k + 1]));
+          if (VQ3_IN((size_t)r * a.d_inter + ch, (size_t)8 * NT * a.d_inter, 11))
+            __stcg(a.hbuf + (size_t)r * a.d_inter + ch, silu_f(sc[q][k][0] * s[2 * k]) * (sc[q][k][1] * s[2 * k + 1]));
         }
       }
     }
-    signal(h_done + m0 / per_chunk, two ? h_done + m1 / per_chunk : nullptr);
+    const bool hok = VQ3_IN(h_done + m0 / per_chunk - a.ctl, a.n_ctl, 27) &&
+                     (!two || VQ3_IN(h_done + m1 / per_chunk - a.ctl, a.n_ctl, 27));
+    if (hok) signal(h_done + m0 / per_chunk, two ? h_done + m1 / per_chunk : nullptr);
+    else __syncthreads();  // (a bounds-check build's skip keeps the barrier count of signal)
   }
 }
 
@@ -1066,10 +1091,12 @@ __device__ __forceinline__ void output_tasks(const PersistArgs& a, const DecodeJ
     int r, c;
     item_pos<NT>(it, r, c);
     const int ch = sg * kSuChannels + c;
-    const float sc = __half2float(__ushort_as_half(__ldg(j.scales0 + ch)));
-    const float rin = (a.res_next && r < a.rows) ? load1(a.x + (size_t)(a.row0 + r) * j.d_out + ch) : 0.f;
+    const size_t oext = (size_t)(a.row0 + a.rows) * j.d_out;  // x, out, res_next of the call up to this pass
+    const float sc = VQ3_IN(ch, j.d_out, 12) ? __half2float(__ushort_as_half(__ldg(j.scales0 + ch))) : 0.f;
+    const float rin = (a.res_next && r < a.rows && VQ3_IN((size_t)(a.row0 + r) * j.d_out + ch, oext, 13))
+                          ? load1(a.x + (size_t)(a.row0 + r) * j.d_out + ch) : 0.f;
     if (threadIdx.x == 0) {
-      poll_geq(j.group_done + g, (unsigned)count, status);
+      if (VQ3_IN(j.group_done + g - a.ctl, a.n_ctl, 26)) poll_geq(j.group_done + g, (unsigned)count, status);
     }
     __syncthreads();  // as for the SwiGLU tasks
     const float* base = j.seg_pieces(sg, PIECE) + it;
@@ -1077,18 +1104,22 @@ __device__ __forceinline__ void output_tasks(const PersistArgs& a, const DecodeJ
     for (int q0 = 0; q0 < count; q0 += P) {
       float v[P];
 #pragma unroll
-      for (int q = 0; q < P; ++q) v[q] = (q0 + q < count) ? __ldcg(base + (size_t)(q0 + q) * PIECE) : 0.f;
+      for (int q = 0; q < P; ++q)
+        v[q] = (q0 + q < count &&
+                VQ3_IN(base - j.pieces + (size_t)(q0 + q) * PIECE, (size_t)n_seg * j.max_pieces * PIECE, 14))
+                   ? __ldcg(base + (size_t)(q0 + q) * PIECE) : 0.f;
 #pragma unroll
       for (int q = 0; q < P; ++q) y += v[q];
     }
     if (r < a.rows) {
       float v = sc * y;
       const __half o16 = __float2half_rn(v);
-      a.out[(size_t)(a.row0 + r) * j.d_out + ch] = __half_as_ushort(o16);
+      if (VQ3_IN((size_t)(a.row0 + r) * j.d_out + ch, oext, 15)) a.out[(size_t)(a.row0 + r) * j.d_out + ch] = __half_as_ushort(o16);
       if (a.res_next) {
         // the next residual, r + out, and its squares for the partial sums below
         const float rn = round16(rin + __half2float(o16));
-        a.res_next[(size_t)(a.row0 + r) * j.d_out + ch] = __half_as_ushort(__float2half_rn(rn));
+        if (VQ3_IN((size_t)(a.row0 + r) * j.d_out + ch, oext, 16))
+          a.res_next[(size_t)(a.row0 + r) * j.d_out + ch] = __half_as_ushort(__float2half_rn(rn));
         sv.scratch[r * 64 + c] = __fmul_rn(rn, rn);
       }
     }
@@ -1102,7 +1133,8 @@ __device__ __forceinline__ void output_tasks(const PersistArgs& a, const DecodeJ
         float ssum = 0.f;
 #pragma unroll
         for (int k = 0; k < 16; ++k) ssum += sv.scratch[rr * 64 + 16 * gq + k];
-        a.ss_next[(size_t)(a.row0 + rr) * (j.d_out / 16) + sg * 4 + gq] = ssum;
+        if (VQ3_IN((size_t)(a.row0 + rr) * (j.d_out / 16) + sg * 4 + gq, (size_t)(a.row0 + a.rows) * (j.d_out / 16), 17))
+          a.ss_next[(size_t)(a.row0 + rr) * (j.d_out / 16) + sg * 4 + gq] = ssum;
       }
       __syncthreads();  // the scratch is reused by the next task
     }
@@ -1140,7 +1172,8 @@ __device__ __forceinline__ void output_tasks_lr(const PersistArgs& a, const Deco
       for (int i = threadIdx.x; i < nk * kSuChannels * per_row; i += kThreads) {
         const int row = i / per_row, k = i - row * per_row;  // row: task row >> 6, channel row & 63
         const uint16_t* src = a.lr_u + ((size_t)((t0 + (row >> 6) * G) / NT) * kSuChannels + (row & 63)) * a.lr_rank;
-        cp_async16(us + (uint32_t)row * kUs + (uint32_t)k * 16u, src + k * 8);
+        if (VQ3_IN(src + k * 8 - a.lr_u, (size_t)j.d_out * a.lr_rank, 18))
+          cp_async16(us + (uint32_t)row * kUs + (uint32_t)k * 16u, src + k * 8);
       }
       cp_async_commit();
     }
@@ -1155,12 +1188,14 @@ __device__ __forceinline__ void output_tasks_lr(const PersistArgs& a, const Deco
       item_pos<NT>(part[k] * 512 + threadIdx.x, r[k], c[k]);
       ch[k] = sg[k] * kSuChannels + c[k];
       // the scale is an input: its load goes out before the wait
-      sc[k] = __half2float(__ushort_as_half(__ldg(j.scales0 + ch[k])));
+      sc[k] = VQ3_IN(ch[k], j.d_out, 12) ? __half2float(__ushort_as_half(__ldg(j.scales0 + ch[k]))) : 0.f;
     }
     const bool do_z = !have_z;  // the CTA's first tasks also form z
     if (threadIdx.x == 0) {
-      poll_geq(j.group_done + sg[0] / kWarps, (unsigned)cnt[0], status);
-      if (nk == 2) poll_geq(j.group_done + sg[1] / kWarps, (unsigned)cnt[1], status);
+      if (VQ3_IN(j.group_done + sg[0] / kWarps - a.ctl, a.n_ctl, 26))
+        poll_geq(j.group_done + sg[0] / kWarps, (unsigned)cnt[0], status);
+      if (nk == 2 && VQ3_IN(j.group_done + sg[1] / kWarps - a.ctl, a.n_ctl, 26))
+        poll_geq(j.group_done + sg[1] / kWarps, (unsigned)cnt[1], status);
       if (do_z) poll_geq(j.lr_done, (unsigned)count0, status);  // z's partials
     }
     __syncthreads();  // as for the SwiGLU tasks
@@ -1173,7 +1208,8 @@ __device__ __forceinline__ void output_tasks_lr(const PersistArgs& a, const Deco
       for (int i = 0; i < NT; ++i)
 #pragma unroll
         for (int k = 0; k < ZP; ++k)
-          zb[i][k] = k < count0 ? __ldcg(j.lr_z + threadIdx.x + i * kThreads + (size_t)k * PIECE) : 0.f;
+          zb[i][k] = (k < count0 && VQ3_IN(threadIdx.x + i * kThreads + (size_t)k * PIECE, (size_t)j.max_pieces * PIECE, 19))
+                         ? __ldcg(j.lr_z + threadIdx.x + i * kThreads + (size_t)k * PIECE) : 0.f;
     }
     // both tasks' sums of pieces, each in piece (= CTA) order: the first task's pieces then the
     // second's, loaded P at a time
@@ -1187,7 +1223,9 @@ __device__ __forceinline__ void output_tasks_lr(const PersistArgs& a, const Deco
 #pragma unroll
         for (int q = 0; q < P; ++q) {
           const int i = q0 + q;
-          v[q] = i < cnt[0] ? __ldcg(b0 + (size_t)i * PIECE) : (i < tot ? __ldcg(b1 + (size_t)i * PIECE) : 0.f);
+          const size_t pext = (size_t)n_seg * j.max_pieces * PIECE;
+          v[q] = i < cnt[0] ? (VQ3_IN(b0 - j.pieces + (size_t)i * PIECE, pext, 14) ? __ldcg(b0 + (size_t)i * PIECE) : 0.f)
+                            : ((i < tot && VQ3_IN(b1 - j.pieces + (size_t)i * PIECE, pext, 14)) ? __ldcg(b1 + (size_t)i * PIECE) : 0.f);
         }
 #pragma unroll
         for (int q = 0; q < P; ++q) {
@@ -1208,7 +1246,9 @@ __device__ __forceinline__ void output_tasks_lr(const PersistArgs& a, const Deco
         for (int k0 = ZP; k0 < count0; k0 += ZP) {  // more than ZP contributors
           float v[ZP];
 #pragma unroll
-          for (int k = 0; k < ZP; ++k) v[k] = k0 + k < count0 ? __ldcg(j.lr_z + e + (size_t)(k0 + k) * PIECE) : 0.f;
+          for (int k = 0; k < ZP; ++k)
+            v[k] = (k0 + k < count0 && VQ3_IN(e + (size_t)(k0 + k) * PIECE, (size_t)j.max_pieces * PIECE, 19))
+                       ? __ldcg(j.lr_z + e + (size_t)(k0 + k) * PIECE) : 0.f;
 #pragma unroll
           for (int k = 0; k < ZP; ++k) z += v[k];
         }
@@ -1236,7 +1276,8 @@ __device__ __forceinline__ void output_tasks_lr(const PersistArgs& a, const Deco
           v += ((q[0] + q[128]) + q[256]) + q[384];
         }
         const __half o16 = __float2half_rn(v);
-        a.out[(size_t)(a.row0 + r[k]) * j.d_out + ch[k]] = __half_as_ushort(o16);
+        if (VQ3_IN((size_t)(a.row0 + r[k]) * j.d_out + ch[k], (size_t)(a.row0 + a.rows) * j.d_out, 15))
+          a.out[(size_t)(a.row0 + r[k]) * j.d_out + ch[k]] = __half_as_ushort(o16);
       }
     }
   }
@@ -1333,7 +1374,8 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
     for (int rr = warp; rr < a.rows; rr += kWarps) {
       const float* p = a.ss_in + (size_t)(a.row0 + rr) * n_part;
       float ss = 0.f;
-      for (int q = lane; q < n_part; q += 32) ss += __ldcg(p + q);
+      for (int q = lane; q < n_part; q += 32)
+        if (VQ3_IN((size_t)(a.row0 + rr) * n_part + q, (size_t)(a.row0 + a.rows) * n_part, 22)) ss += __ldcg(p + q);
 #pragma unroll
       for (int h = 16; h > 0; h >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, h);
       if (lane == 0) s_inv[rr] = 1.0f / sqrtf(ss / (float)a.d_model + a.eps);
@@ -1359,7 +1401,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int g = gb + u * 32 + lane;
-          if (g < g1) {
+          if (g < g1 && VQ3_IN(ro / 8 + g, (size_t)(a.row0 + a.rows) * d / 8, 23)) {
             xv[u] = __ldg(reinterpret_cast<const uint4*>(a.x + ro) + g);
             if (a.res_delta) dv[u] = __ldg(reinterpret_cast<const uint4*>(a.res_delta + ro) + g);
           }
@@ -1386,7 +1428,8 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(PersistArgs a) 
             ss = fmaf(f.x, f.x, ss);
             ss = fmaf(f.y, f.y, ss);
           }
-          if (a.res_out && (g >> 3) % (int)gridDim.x == (int)blockIdx.x)
+          if (a.res_out && (g >> 3) % (int)gridDim.x == (int)blockIdx.x &&
+              VQ3_IN(ro / 8 + g, (size_t)(a.row0 + a.rows) * d / 8, 25))
             *(reinterpret_cast<uint4*>(a.res_out + ro) + g) = rv;
         }
       }

@@ -45,6 +45,7 @@
 #include "vq3_internal.h"
 
 namespace vq3 {
+VQ3_BOUNDS_RECORD(prefill)
 namespace {
 
 constexpr int kTmaWarp = 0;                     // lane 0 issues the tile copies
@@ -656,7 +657,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
             tmem_ld16(taddr + (uint32_t)c0, r);
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-            for (int j = 0; j < 16; ++j) __stcg(part + (size_t)(c0 + j) * kTileM + row, __uint_as_float(r[j]));
+            for (int j = 0; j < 16; ++j)
+              if (VQ3_IN((size_t)(part - a.part) + (size_t)(c0 + j) * kTileM + row,
+                         (size_t)gridDim.x * 2 * G * kTileM * N, 1))
+                __stcg(part + (size_t)(c0 + j) * kTileM + row, __uint_as_float(r[j]));
           }
         } else if (!a.swiglu) {
           const int ch = mt * kTileM + chan;
@@ -671,7 +675,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
             for (int j = 0; j < 16; ++j) {
               float v = __uint_as_float(r[j]) * sc;
               const int rr = row0 + c0 + j;
-              if (live && c0 + j < cols) {
+              if (live && c0 + j < cols && VQ3_IN((size_t)rr * a.d_out + ch, (size_t)a.rows * a.d_out, 2)) {
                 if (a.lr_y) v += __ldg(a.lr_y + (size_t)rr * a.d_out + ch);  // low-rank correction
                 a.out16[(size_t)rr * a.d_out + ch] = __half_as_ushort(__float2half_rn(v));
               }
@@ -697,7 +701,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 const float hv = silu_f(sc * __uint_as_float(r[j])) * xch[j * 64 + row];
-                if (c0 + j < cols) __stcg(a.out32 + (size_t)(row0 + c0 + j) * a.d_out + jch, hv);
+                if (c0 + j < cols && VQ3_IN((size_t)(row0 + c0 + j) * a.d_out + jch, (size_t)a.rows * a.d_out, 3))
+                  __stcg(a.out32 + (size_t)(row0 + c0 + j) * a.d_out + jch, hv);
               }
             }
             asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -799,6 +804,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
       const float4* p1 = reinterpret_cast<const float4*>(a.part + (size_t)(ca + 1) * cta_floats +
                                                          (size_t)t * tile_floats + (size_t)c16 * 16 * kTileM);
       auto sum_parts = [&](int off4) {
+        if (!VQ3_IN((size_t)(p0 - reinterpret_cast<const float4*>(a.part)) + off4, (size_t)gridDim.x * stride4, 4) ||
+            (np > 1 && !VQ3_IN((size_t)(p1 - reinterpret_cast<const float4*>(a.part)) + (size_t)(np - 2) * stride4 + off4,
+                                (size_t)gridDim.x * stride4, 5)))
+          return make_float4(0.f, 0.f, 0.f, 0.f);
         float4 v = __ldcg(p0 + off4);
         int p = 0;
         for (; p + 8 <= np - 1; p += 8) {
@@ -820,7 +829,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int ch = mt * kTileM + tile_channel(4 * f + k);
-          if (ch >= a.d_out) continue;
+          if (ch >= a.d_out || !VQ3_IN((size_t)rr * a.d_out + ch, (size_t)a.rows * a.d_out, 6)) continue;
           float o = vv[k] * __half2float(__ushort_as_half(a.scale0[ch]));
           if (a.lr_y) o += __ldg(a.lr_y + (size_t)rr * a.d_out + ch);
           a.out16[(size_t)rr * a.d_out + ch] = __half_as_ushort(__float2half_rn(o));
@@ -836,7 +845,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
           const int jch = mt * 64 + tile_channel(4 * f + k);
           const float sg = __half2float(__ushort_as_half(a.scale0[jch]));
           const float su2 = __half2float(__ushort_as_half(a.scale1[jch]));
-          __stcg(a.out32 + (size_t)rr * a.d_out + jch, silu_f(sg * g4[k]) * (su2 * u4[k]));
+          if (VQ3_IN((size_t)rr * a.d_out + jch, (size_t)a.rows * a.d_out, 7))
+            __stcg(a.out32 + (size_t)rr * a.d_out + jch, silu_f(sg * g4[k]) * (su2 * u4[k]));
         }
       }
     }

@@ -43,6 +43,7 @@
 #include "vq3_internal.h"
 
 namespace vq3 {
+VQ3_BOUNDS_RECORD(prefill_wide)
 namespace {
 
 constexpr int kTmaWarp = 0;                     // lane 0 issues the tile copies
@@ -579,7 +580,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
           tmem_ld16(taddr + (uint32_t)c0, r);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-          for (int j = 0; j < 16; ++j) __stcg(part + (size_t)(c0 + j) * kTileM + row, __uint_as_float(r[j]));
+          for (int j = 0; j < 16; ++j)
+            if (VQ3_IN((size_t)blockIdx.x * kTileM * N + (size_t)(c0 + j) * kTileM + row, (size_t)gridDim.x * kTileM * N, 1))
+              __stcg(part + (size_t)(c0 + j) * kTileM + row, __uint_as_float(r[j]));
         }
         tc_fence_before();
         mbar_arrive(acc_empty(b));
@@ -596,6 +599,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
             ++n_parts;
           if (e == 0 && waits) {
             for (int p = 1; p <= n_parts && !*abort; ++p) {
+              if (!VQ3_IN(blockIdx.x + p, gridDim.x, 2)) break;
               const unsigned long long t0 = globaltimer_ns();
               for (unsigned spin = 1; ld_acquire_u32(a.flags + blockIdx.x + p) == 0u && !*abort; ++spin) {
                 __nanosleep(64);
@@ -622,6 +626,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
             for (int p = 0; p < n_parts; ++p) {
+              if (!VQ3_IN((size_t)(blockIdx.x + 1 + p) * kTileM * N + (size_t)(c0 + 15) * kTileM + row,
+                          (size_t)gridDim.x * kTileM * N, 3))
+                break;
 #pragma unroll
               for (int j = 0; j < 16; ++j) v[j] += __ldcg(parts + (size_t)p * kTileM * N + (size_t)(c0 + j) * kTileM + row);
             }
@@ -631,12 +638,13 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
               // low-rank correction, one value per output (lanes: consecutive channels)
 #pragma unroll
               for (int j = 0; j < 16; ++j)
-                if (c0 + j < cols) v[j] += __ldg(a.lr_y + (size_t)(row0 + c0 + j) * a.d_out + ch);
+                if (c0 + j < cols && VQ3_IN((size_t)(row0 + c0 + j) * a.d_out + ch, (size_t)a.rows * a.d_out, 4))
+                  v[j] += __ldg(a.lr_y + (size_t)(row0 + c0 + j) * a.d_out + ch);
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int rr = row0 + c0 + j;
-              if (live && c0 + j < cols)
+              if (live && c0 + j < cols && VQ3_IN((size_t)rr * a.d_out + ch, (size_t)a.rows * a.d_out, 5))
                 a.out16[(size_t)rr * a.d_out + ch] = __half_as_ushort(__float2half_rn(v[j]));
             }
           }
@@ -654,6 +662,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
             for (int p = 0; p < n_parts; ++p) {
+              if (!VQ3_IN((size_t)(blockIdx.x + 1 + p) * kTileM * N + (size_t)(c0 + 15) * kTileM + row,
+                          (size_t)gridDim.x * kTileM * N, 3))
+                break;
 #pragma unroll
               for (int j = 0; j < 16; ++j) v[j] += __ldcg(parts + (size_t)p * kTileM * N + (size_t)(c0 + j) * kTileM + row);
             }
@@ -667,7 +678,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
               for (int j = 0; j < 16; ++j) {
                 const int rr = row0 + c0 + j;
                 const float hv = silu_f(sc * v[j]) * xch[j * 64 + row];
-                if (c0 + j < cols) __stcg(a.out32 + (size_t)rr * a.d_out + jch, hv);
+                if (c0 + j < cols && VQ3_IN((size_t)rr * a.d_out + jch, (size_t)a.rows * a.d_out, 6))
+                  __stcg(a.out32 + (size_t)rr * a.d_out + jch, hv);
               }
             }
             asm volatile("bar.sync 1, 128;" ::: "memory");

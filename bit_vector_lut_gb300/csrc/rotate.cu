@@ -16,6 +16,7 @@
 #include "vq3_internal.h"
 
 namespace vq3 {
+VQ3_BOUNDS_RECORD(rotate)
 namespace {
 
 constexpr int kRotThreads = 128;
@@ -48,11 +49,11 @@ __global__ void __launch_bounds__(kRotThreads) fwht_kernel(const T* x, int n, co
   for (int s = 0; s < V; ++s) {
     const int j = s * kRotThreads + tid;
     float f = 0.f;
-    if (tid < ACTIVE) {
+    if (tid < ACTIVE && VQ3_IN(base + j, (size_t)gridDim.x * B, 1)) {  // grid = rows x blocks per row
       f = load_elem(x + base + j);
       if (signs) {
         const int col = blk * B + j;
-        if ((__ldg(signs + (col >> 5)) >> (col & 31)) & 1u) f = -f;
+        if (VQ3_IN(col >> 5, n / 32, 2) && ((__ldg(signs + (col >> 5)) >> (col & 31)) & 1u)) f = -f;
       }
     }
     v[s] = f;
@@ -98,7 +99,7 @@ __global__ void __launch_bounds__(kRotThreads) fwht_kernel(const T* x, int n, co
   for (int s = 0; s < V; ++s) {
     const int j = s * kRotThreads + tid;
     const int col = blk * B + j;
-    if (tid < ACTIVE)
+    if (tid < ACTIVE && VQ3_IN(row_base + (mma_order ? mma_order_col(col) : col), (size_t)gridDim.x * B, 3))
       out[row_base + (mma_order ? mma_order_col(col) : col)] = __half_as_ushort(__float2half_rn(v[s] * scale));
   }
 }
@@ -155,6 +156,7 @@ __global__ void __launch_bounds__(256) residual_add_ss_kernel(const uint16_t* __
     float s = 0.f;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
+      if (!VQ3_IN(base + 16 * g + 8 * h + 7, (size_t)gridDim.x * n, 4)) continue;  // grid = rows
       const uint4 rv = *reinterpret_cast<const uint4*>(r + base + 16 * g + 8 * h);
       const uint4 dv = *reinterpret_cast<const uint4*>(d + base + 16 * g + 8 * h);
       const __half2* rh = reinterpret_cast<const __half2*>(&rv);

@@ -94,6 +94,43 @@ constexpr int kDecWarps = 16;  // warps per decoding CTA = segments per group
 constexpr int kDecMaxGrid = 2048;
 
 int device_sm_count();
+
+// ---------------------------------------------------------------------------
+// Bounds-check build (-DVQ3_BOUNDS_CHECK): an instrumented global access checks its element
+// index against the extent of the buffer it addresses, VQ3_IN(index, extent, site); a
+// violation skips the access and is counted in a per-file device record with the first
+// site (file id << 8 | site). Each instrumented file defines its record with
+// VQ3_BOUNDS_RECORD(name) inside namespace vq3; vq3_bounds_check collects them. In other
+// builds VQ3_IN is `true` and nothing is recorded.
+#ifdef VQ3_BOUNDS_CHECK
+__device__ inline bool vq3_in_bounds(size_t i, size_t n, unsigned site, unsigned* rec) {
+  if (i < n) return true;
+  if (atomicAdd(&rec[0], 1u) == 0u) atomicExch(&rec[1], site);
+  return false;
+}
+#define VQ3_BOUNDS_RECORD(name)                                                            \
+  namespace {                                                                              \
+  __device__ unsigned g_bounds[2];                                                         \
+  }                                                                                        \
+  cudaError_t bounds_read_##name(unsigned* host, bool reset) {                             \
+    cudaError_t e = cudaMemcpyFromSymbol(host, g_bounds, sizeof(g_bounds));                \
+    if (e == cudaSuccess && reset) {                                                       \
+      const unsigned z[2] = {0u, 0u};                                                      \
+      e = cudaMemcpyToSymbol(g_bounds, z, sizeof(z));                                      \
+    }                                                                                      \
+    return e;                                                                              \
+  }
+#define VQ3_IN(idx, n, site) vq3_in_bounds((size_t)(idx), (size_t)(n), (unsigned)(site), g_bounds)
+cudaError_t bounds_read_persistent(unsigned* host, bool reset);
+cudaError_t bounds_read_lowrank(unsigned* host, bool reset);
+cudaError_t bounds_read_delta(unsigned* host, bool reset);
+cudaError_t bounds_read_rotate(unsigned* host, bool reset);
+cudaError_t bounds_read_prefill(unsigned* host, bool reset);
+cudaError_t bounds_read_prefill_wide(unsigned* host, bool reset);
+#else
+#define VQ3_BOUNDS_RECORD(name)
+#define VQ3_IN(idx, n, site) true
+#endif
 // The C ABI's thread-local error message, for host code outside api.cu: report_error sets it
 // (printf format) and returns code; report_ok clears it and returns VQ3_OK.
 int report_error(int code, const char* fmt, ...);

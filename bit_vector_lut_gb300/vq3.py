@@ -16,7 +16,8 @@ import numpy as np
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libvq3.so")
+# VQ3_LIB may name another build of the same library (the bounds-check build, libvq3_bc.so)
+LIB_PATH = os.environ.get("VQ3_LIB") or os.path.join(_PKG, "libvq3.so")
 
 VQ3_OK = 0
 ERRORS = {-1: "VQ3_EINVAL", -2: "VQ3_EALIGN", -3: "VQ3_EUNSUPPORTED", -4: "VQ3_ECUDA", -5: "VQ3_ENOSPACE"}
@@ -88,6 +89,7 @@ def _load() -> ctypes.CDLL:
         "vq3_noalloc_status": (c_int, [POINTER(c_int), c_void_p]),
         "vq3_last_error": (ctypes.c_char_p, []),
         "vq3_version": (ctypes.c_char_p, []),
+        "vq3_bounds_check": (c_int, [POINTER(ctypes.c_uint), c_int, c_int]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -118,6 +120,17 @@ def _stream(stream) -> int | None:
 
 def version() -> str:
     return lib.vq3_version().decode()
+
+
+BOUNDS_FILES = ("decode", "lowrank", "delta", "rotate", "prefill", "prefill_wide")
+
+
+def bounds_check(reset: bool = True) -> dict[str, tuple[int, int]]:
+    """Bounds-check build only: {kernel file: (accesses skipped, site of the first)}.
+    Raises Vq3Error (VQ3_EUNSUPPORTED) in the normal build."""
+    buf = (ctypes.c_uint * (2 * len(BOUNDS_FILES)))()
+    _check(lib.vq3_bounds_check(buf, len(buf), 1 if reset else 0))
+    return {name: (int(buf[2 * f]), int(buf[2 * f + 1])) for f, name in enumerate(BOUNDS_FILES)}
 
 
 # ---------------------------------------------------------------- layout (host)

@@ -434,6 +434,22 @@ VQ3_API const char* vq3_last_error(void);
 /* Library build/version string. */
 VQ3_API const char* vq3_version(void);
 
+/*
+ * Bounds-check build (the library compiled with -DVQ3_BOUNDS_CHECK; in any other
+ * build this returns VQ3_EUNSUPPORTED and writes nothing). In that build every
+ * global load and store of the kernels that is addressed by computed indices checks
+ * the index against the extent of the buffer it addresses (the extents the entry
+ * points' arguments fix); an access out of range is skipped and counted. This reads
+ * the counts: out[2 f] = accesses skipped in kernel file f, out[2 f + 1] = the site
+ * number of the first one (0 if none), for f = 0 decode, 1 low-rank factors,
+ * 2 delta rule, 3 rotation and residual, 4 prefill up to 128 rows, 5 prefill above.
+ * reset != 0 clears the counts after reading. n_out: entries of out, at least
+ * VQ3_BOUNDS_FILES * 2 (else VQ3_EINVAL). Synchronous on the device (waits for all
+ * work); call it between, not during, launches.
+ */
+#define VQ3_BOUNDS_FILES 6
+VQ3_API int vq3_bounds_check(unsigned* out, int n_out, int reset);
+
 #ifdef __cplusplus
 }
 #endif

@@ -5,6 +5,7 @@ rejects bad arguments with the documented status before touching the GPU."""
 import ctypes
 import os
 import re
+import subprocess
 
 import numpy as np
 import pytest
@@ -229,3 +230,22 @@ def test_delta_rule_argument_checks():
     assert f(p, p, p, p, p, 8, 0, 128, 64, p, p, None) == -1   # no heads
     assert f(p, p, p, p, p, 8, 4, 128, 64, None, p, None) == -1
     assert f(None, None, None, None, None, 0, 4, 128, 64, p, None, None) == 0  # zero tokens: nothing to do
+
+
+def test_bounds_check_unsupported_in_normal_build():
+    # the normal build records nothing: the call says so without touching the GPU
+    if "bounds-check" in vq3.version():
+        pytest.skip("VQ3_LIB selects the bounds-check build")
+    with pytest.raises(vq3.Vq3Error, match="VQ3_BOUNDS_CHECK"):
+        vq3.bounds_check()
+
+
+@pytest.mark.parametrize("src", ["rotate.cu", "lowrank.cu", "delta.cu"])
+def test_bounds_check_variant_compiles(tmp_path, src):
+    # the instrumented form of the smaller kernel files compiles (the whole library is built in
+    # that form, and run, by the GPU test)
+    from bit_vector_lut_gb300 import build as B
+    r = subprocess.run(
+        [B.nvcc(), *B.ARCH, *B.NVCC_FLAGS, "-DVQ3_BOUNDS_CHECK", "-c", os.path.join(B.CSRC, src), "-o",
+         str(tmp_path / "x.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-3000:]
