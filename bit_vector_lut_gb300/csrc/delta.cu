@@ -47,7 +47,6 @@ __global__ void __launch_bounds__(kDThreads) delta_rule_kernel(const uint16_t* _
   const int h = blockIdx.x, c0 = blockIdx.y * kCols;
   float* Sg = state + (size_t)h * d_k * d_v;
   const size_t n_state = (size_t)heads * d_k * d_v, n_qk = (size_t)tokens * heads * d_k, n_v = (size_t)tokens * heads * d_v;
-  (void)n_state; (void)n_qk; (void)n_v;
   for (int e = tid; e < d_k * kCols; e += kDThreads)
     Ss[e] = VQ3_IN((size_t)h * d_k * d_v + (size_t)(e / kCols) * d_v + c0 + e % kCols, n_state, 1)
                 ? Sg[(size_t)(e / kCols) * d_v + c0 + e % kCols] : 0.f;
@@ -264,7 +263,6 @@ __global__ void __launch_bounds__(32 * KS, 1) delta_rule_tc_kernel(const uint16_
   const int h = blockIdx.x, c0 = blockIdx.y * 16;
   float* Sg = state + (size_t)h * DK * d_v + c0;
   const size_t n_state = (size_t)heads * DK * d_v, n_qk = (size_t)tokens * heads * DK, n_v = (size_t)tokens * heads * d_v;
-  (void)n_state; (void)n_qk; (void)n_v;
 
   // this warp's tiles of the state slice: acc[n] = S^T[g, g+8][16 warp + 8n + 2t, +1]
   float acc[2][4];

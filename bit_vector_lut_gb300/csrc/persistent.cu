@@ -821,7 +821,10 @@ __device__ __forceinline__ void issue_cell(const DecodeJob& a, Cursor& cur, uint
     const uint32_t s = ring_lane + cur.slot;
 #pragma unroll
     for (int q = 0; q < FmtSizes<F>::kChunks; ++q)
-      if (VQ3_IN(cur.src + 32 * q - cur.base, cur.extent, 1)) cp_async16(s + (uint32_t)(q * 512), cur.src + 32 * q);
+#ifdef VQ3_BOUNDS_CHECK
+      if (VQ3_IN(cur.src + 32 * q - cur.base, cur.extent, 1))
+#endif
+        cp_async16(s + (uint32_t)(q * 512), cur.src + 32 * q);
   }
   cp_async_commit();
   constexpr uint32_t kSlot = (uint32_t)Ring<F>::kSlotBytes;

@@ -129,7 +129,7 @@ cudaError_t bounds_read_prefill(unsigned* host, bool reset);
 cudaError_t bounds_read_prefill_wide(unsigned* host, bool reset);
 #else
 #define VQ3_BOUNDS_RECORD(name)
-#define VQ3_IN(idx, n, site) true
+#define VQ3_IN(idx, n, site) ((void)(n), true)  // the extent is used only by the check
 #endif
 // The C ABI's thread-local error message, for host code outside api.cu: report_error sets it
 // (printf format) and returns code; report_ok clears it and returns VQ3_OK.
