@@ -436,7 +436,8 @@ VQ3_API const char* vq3_version(void);
 
 /*
  * Bounds-check build (the library compiled with -DVQ3_BOUNDS_CHECK; in any other
- * build this returns VQ3_EUNSUPPORTED and writes nothing). In that build every
+ * build this returns VQ3_EUNSUPPORTED and writes nothing). A debugging aid of this
+ * library, no counterpart on the pages. In that build every
  * global load and store of the kernels that is addressed by computed indices checks
  * the index against the extent of the buffer it addresses (the extents the entry
  * points' arguments fix); an access out of range is skipped and counted. This reads
