@@ -249,3 +249,44 @@ def test_bounds_check_variant_compiles(tmp_path, src):
         [B.nvcc(), *B.ARCH, *B.NVCC_FLAGS, "-DVQ3_BOUNDS_CHECK", "-c", os.path.join(B.CSRC, src), "-o",
          str(tmp_path / "x.o")], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr[-3000:]
+
+
+def declarations():
+    """{name: (return type, [argument types])} of every VQ3_API function in include/vq3.h."""
+    txt = open(os.path.join(ROOT, "include", "vq3.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    out = {}
+    for m in re.finditer(r"VQ3_API\s+([\w\s\*]+?)\b(\w+)\s*\(([^)]*)\)\s*;", txt):
+        ret, name, args = m.group(1).strip(), m.group(2), " ".join(m.group(3).split())
+        types = []
+        if args and args != "void":
+            for a in args.split(","):
+                a = a.strip()
+                types.append(a[: len(a) - len(re.search(r"\w+$", a).group(0))].strip() if "*" in a or " " in a else a)
+        out[name] = (ret, types)
+    return out
+
+
+def _kind(ctype_name: str) -> str:
+    t = ctype_name.replace("const ", "").strip()
+    if "*" in t:
+        return "ptr"
+    return {"int": "int", "size_t": "size", "float": "float", "unsigned": "uint"}[t]
+
+
+def _ctypes_kind(t) -> str:
+    if t in (ctypes.c_void_p, ctypes.c_char_p) or (isinstance(t, type) and issubclass(t, ctypes._Pointer)):
+        return "ptr"
+    return {ctypes.c_int: "int", ctypes.c_size_t: "size", ctypes.c_float: "float", ctypes.c_uint: "uint"}[t]
+
+
+def test_binding_signatures_match_the_header():
+    # every declared call has a binding whose argument and return kinds match the header's
+    # (a size_t passed as a 32-bit int, or a dropped argument, would corrupt the call)
+    decl = declarations()
+    assert len(decl) >= 30
+    for name, (ret, args) in decl.items():
+        f = getattr(vq3.lib, name)
+        assert f.argtypes is not None, f"{name}: no ctypes signature"
+        assert [_kind(a) for a in args] == [_ctypes_kind(t) for t in f.argtypes], name
+        assert _kind(ret) == _ctypes_kind(f.restype), name
