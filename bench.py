@@ -377,6 +377,7 @@ def _run_ours_on(args, torch, vq3, dev, stream, rows, sets, x_host, x, out, ws, 
     if not args.quick and rank == 0:
         extra = prefill_sweep(vq3, dev, stream, pk, l2)
         extra["config_outliers_T64"] = prefill_outliers_line(vq3, dev, stream, pk, l2)
+        fp16_matmul_reference(extra, dev, stream)
         extra["config_linear_256_T8"] = linear256_line(vq3, dev, stream)
         stack = stack64(vq3, dev, stream, pk)
         fmts = format_lines(vq3, dev, stream, pk, l2)
@@ -610,6 +611,39 @@ def prefill_sweep(vq3, dev, stream, pk, l2) -> dict:
                            "launches_per_block": vq3.mlp_kernel_launches(rows, sets[0]), "status": st}
     res["weight_sets"] = len(sets)
     return res
+
+
+def fp16_matmul_reference(sweep: dict, dev, stream) -> None:
+    """A second denominator for the sweep's TFLOP/s: cuBLAS's dense FP16 GEMM (torch.matmul,
+    8192 x 8192 x 8192, FP32 accumulate) timed in the same run on the same stream, 3 warm-up
+    and 10 timed calls. Each sweep point and the outlier chunk get their fraction of it."""
+    import torch
+    n = 8192
+    try:
+        g = torch.Generator(device=dev).manual_seed(5)
+        a = torch.randn((n, n), device=dev, dtype=torch.float16, generator=g)
+        b = torch.randn((n, n), device=dev, dtype=torch.float16, generator=g)
+        stream.wait_stream(torch.cuda.current_stream(dev))
+    except RuntimeError as e:  # a reference figure only: the line keeps the reason
+        sweep["fp16_matmul_tflops"] = {"error": str(e)[:200]}
+        return
+    with torch.cuda.stream(stream):
+        c = torch.matmul(a, b)
+        for _ in range(2):
+            torch.matmul(a, b, out=c)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(10):
+            torch.matmul(a, b, out=c)
+        e1.record(stream)
+    e1.synchronize()
+    tflops = 2.0 * n ** 3 * 10 / (e0.elapsed_time(e1) / 1e3) / 1e12
+    sweep["fp16_matmul_tflops"] = round(tflops, 1)
+    for k, v in sweep.items():
+        if isinstance(v, dict) and "tflops" in v:
+            v["frac_of_fp16_matmul"] = round(v["tflops"] / tflops, 4)
+    del a, b, c
 
 
 def prefill_outliers_line(vq3, dev, stream, pk, l2) -> dict:
