@@ -154,7 +154,11 @@ VQ3_API int vq3_pack_layout(const uint8_t* canonical, int d_in, int d_out, void*
 
 /* Host-side inverse of vq3_pack_layout (pad bits of the canonical stream are
  * written as zero), so the private GPU layout round-trips to the interchange
- * stream bit for bit. Same citation and errors as vq3_pack_layout. */
+ * stream bit for bit. Cited: model card "anemll/anemll-forge-qwen3.8-27B",
+ * "Release 0.2" bullet "Three bits per MLP weight" (one six-bit index per pair of
+ * output channels and input column); the stream's order (pair-major, input
+ * fastest, indices LSB-first) is this library's reading, as for vq3_pack_layout,
+ * since the pages give no order. Errors as vq3_pack_layout. */
 VQ3_API int vq3_unpack_layout(const void* packed_host, int d_in, int d_out, uint8_t* canonical);
 
 /* The same three calls for any index format (VQ3_FORMAT_*): the GPU layout is
